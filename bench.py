@@ -1,2 +1,429 @@
-def decode_bytes_per_head_step(dk, dv):
-    return 2 * dk * dv * 4 + dk * 2 * 3 + dk * 4 + 2
+"""Benchmark of the KDA forward on one GB300 (or N independent replicas).
+
+One step = one pass of the whole prefill hot path over the one-layer K3
+workload (B=1, T=8192, H=96, dk=dv=128, bf16 q/k/v/beta, fp32 state and h0):
+  kda_gate (z -> g)  then  kda_chunk_fwd (q, k, v, g, beta, h0 -> o, hT).
+Inputs are resident in HBM when the timed region starts and are larger than
+L2 (z, q, k, v are 201 MB each), so no L2 flush is needed between steps.
+
+The JSON line also carries
+  * roofline -- the dominant kernel's algorithmic bytes per launch over its mean
+    CUDA-event duration (timed on its launching stream), against the measured
+    HBM copy bandwidth; plus the whole step against the method's byte floor;
+  * decode -- the decode step (512 sequences x 96 heads, fp32 state in place),
+    achieved HBM GB/s against the same peak;
+  * e2e -- the same prefill metric through the public API with host buffers
+    (pinned host -> device copies of the step's inputs, device -> host copy of
+    o and hT inside the timed region);
+  * cpu_baseline -- the fp64 oracle on the host cores over a bounded sample.
+
+``--impl reference`` times the oracle alone (the reference arm of this build).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+D = 128
+METRIC = "KDA prefill tokens/s (H=96,d=128) and % roofline; decode-step HBM GB/s"
+
+
+# ------------------------------------------------------------------ byte counts
+def prefill_bytes_per_token_head(io_bytes: int = 2, dk: int = D, dv: int = D) -> int:
+    """Algorithmic HBM bytes of kda_chunk_fwd per token and head: q, k, v and o in
+    the input dtype, g in fp32, beta in the input dtype."""
+    return (2 * dk + dv) * io_bytes + dk * 4 + io_bytes + dv * io_bytes
+
+
+def gate_bytes_per_token_head(z_bytes: int = 2, dk: int = D) -> int:
+    """Algorithmic bytes of kda_gate: z read in its dtype, g written in fp32."""
+    return dk * z_bytes + dk * 4
+
+
+def state_bytes(dk: int = D, dv: int = D) -> int:
+    return dk * dv * 4
+
+
+def decode_bytes_per_head_step(dk: int = D, dv: int = D) -> int:
+    """Decode: fp32 state read + written, q, k, v, o (bf16), g (fp32), beta (bf16)."""
+    return 2 * state_bytes(dk, dv) + dk * 2 * 3 + dk * 4 + 2
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# ----------------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons every 200 ms."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int = 0):
+        self.gpu = gpu_index
+        self.samples = []
+        self._stop = threading.Event()
+        self._thr = None
+        self.marks = []
+
+    def start(self):
+        self._thr = threading.Thread(target=self._run, daemon=True)
+        self._thr.start()
+
+    def mark(self, on: bool):
+        self.marks.append((time.time(), on))
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                out = subprocess.run(["nvidia-smi", "-i", str(self.gpu),
+                                      f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits"],
+                                     capture_output=True, text=True, timeout=5).stdout.strip()
+                if out:
+                    self.samples.append((time.time(), [x.strip() for x in out.split(",")]))
+            except Exception:
+                pass
+            self._stop.wait(0.2)
+
+    def stop(self):
+        self._stop.set()
+        if self._thr:
+            self._thr.join(timeout=10)
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        # samples taken while a timed region was open
+        spans, t_on = [], None
+        for t, on in self.marks:
+            if on:
+                t_on = t
+            elif t_on is not None:
+                spans.append((t_on, t))
+                t_on = None
+        inside = [s for t, s in self.samples if any(a <= t <= b for a, b in spans)] or \
+            [s for _, s in self.samples]
+        sm = [float(s[1]) for s in inside if _isnum(s[1])]
+        mx = [float(s[2]) for s in inside if _isnum(s[2])]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for s in inside:
+            for i, n in enumerate(names):
+                if len(s) > 5 + i and s[5 + i].lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(inside)}
+
+
+def _isnum(x):
+    try:
+        float(x)
+        return True
+    except ValueError:
+        return False
+
+
+# ------------------------------------------------------------- measured traffic
+def kernel_traffic(name: str):
+    """Per-launch DRAM bytes of `name` from the committed ncu summary, if the
+    summary's source hash still matches the kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(rf"^\|\s*{re.escape(name)}\s*\|\s*([0-9.eE+]+)\s*\|\s*([0-9a-f]+)\s*\|", text,
+                  re.M)
+    if not m:
+        return None
+    src = os.path.join(ROOT, "chunked_gated_delta_fwd_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(src)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(src, f), "rb").read())
+    if h.hexdigest()[:12] != m.group(2):
+        return None
+    return float(m.group(1))
+
+
+# ------------------------------------------------------------------------ arms
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def run_reference(args):
+    """The oracle, timed on the host cores over a bounded sample of the workload."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import numpy as np
+    import torch
+
+    import oracle
+    import workloads
+
+    w = workloads.prefill()
+    heads = args.ref_heads
+    T = w.seq_lens[0]
+    gen = torch.Generator().manual_seed(w.seed)
+    # same distributions as the GPU workload, drawn for the sampled heads only
+    q = torch.nn.functional.normalize(torch.randn(T, heads, D, generator=gen), dim=-1).bfloat16()
+    k = torch.nn.functional.normalize(torch.randn(T, heads, D, generator=gen), dim=-1).bfloat16()
+    v = torch.randn(T, heads, D, generator=gen).bfloat16()
+    z = torch.randn(T, heads, D, generator=gen).bfloat16()
+    beta = torch.sigmoid(torch.randn(T, heads, generator=gen)).bfloat16()
+    A = torch.rand(heads, generator=gen) * 2 - 1
+    h0 = torch.randn(1, heads, D, D, generator=gen) * 0.02
+    cores = os.cpu_count() or 1
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        g = oracle.gate(z, A)
+        oracle.recurrence(q, k, v, g, beta, h0, n_threads=cores)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    per_step = statistics.median(times)
+    tokens_per_s = T * heads / per_step / w.H  # H=96 tokens/s equivalent
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": per_step * 1e3 * w.H / heads, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "sample": f"{heads} of {w.H} heads x {T} tokens",
+                   "global_batch": 1, "seq_len": T, "parallelism": "none (host cores)"},
+        "cpu_baseline": {"value": tokens_per_s, "unit": "tokens/s", "cores": min(cores, heads),
+                         "kind": "oracle",
+                         "sample": f"gate + fp64 recurrence over {heads} heads x {T} tokens, "
+                                   f"scaled to H={w.H}"},
+        "e2e": {"value": tokens_per_s, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def cpu_baseline(heads=16, T=8192, seed=1002):
+    """fp64 oracle over a bounded sample (heads x T tokens), scaled to H=96."""
+    import torch
+
+    import oracle
+
+    gen = torch.Generator().manual_seed(seed)
+    q = torch.nn.functional.normalize(torch.randn(T, heads, D, generator=gen), dim=-1).bfloat16()
+    k = torch.nn.functional.normalize(torch.randn(T, heads, D, generator=gen), dim=-1).bfloat16()
+    v = torch.randn(T, heads, D, generator=gen).bfloat16()
+    z = torch.randn(T, heads, D, generator=gen).bfloat16()
+    beta = torch.sigmoid(torch.randn(T, heads, generator=gen)).bfloat16()
+    A = torch.rand(heads, generator=gen) * 2 - 1
+    cores = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    g = oracle.gate(z, A)
+    oracle.recurrence(q, k, v, g, beta, None, n_threads=cores)
+    dt = time.perf_counter() - t0
+    return {"value": T * heads / dt / 96, "unit": "tokens/s", "cores": min(cores, heads),
+            "kind": "oracle",
+            "sample": f"gate + fp64 recurrence, {heads} heads x {T} tokens "
+                      f"({dt:.1f} s), scaled to H=96"}
+
+
+def run_gpu(args):
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    import chunked_gated_delta_fwd_gb300 as kda
+    import workloads
+
+    hbm_peak, bf16_peak, peak_src = load_peaks()
+    w = workloads.prefill()
+    inp = workloads.make_inputs(w, dev)
+    NT, H = w.n_tokens, w.H
+    ws = torch.empty(kda.chunk_fwd_workspace_size(NT, 1, H, torch.bfloat16), dtype=torch.uint8,
+                     device=dev)
+    g = torch.empty(NT, H, D, dtype=torch.float32, device=dev)
+    o = torch.empty(NT, H, D, dtype=torch.bfloat16, device=dev)
+    hT = torch.empty(1, H, D, D, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kda.gate(inp["z"], inp["A"], out=g)
+        kda.chunk_fwd(inp["q"], inp["k"], inp["v"], g, inp["beta"], inp["h0"], inp["cu_seqlens"],
+                      workspace=ws, out=o, final_state_out=hT)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    def timed(fn, steps, warmup):
+        for _ in range(warmup):
+            fn()
+        barrier()
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        clocks.mark(True)
+        start.record(stream)
+        for _ in range(steps):
+            fn()
+        stop.record(stream)
+        barrier()
+        clocks.mark(False)
+        ms = start.elapsed_time(stop) / steps
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    clocks = ClockSampler(dev.index or 0)
+    clocks.start()
+    ms_step = timed(step, args.steps, args.warmup)
+    tokens_per_s = NT * world / (ms_step * 1e-3)
+
+    # per-kernel event timing pass (same steps, profiling on)
+    kda.profile_enable(True)
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize(dev)
+    per_kernel = kda.profile_collect()
+    kda.profile_enable(False)
+    launches = sum(n for n, _ in per_kernel.values())
+    dom_name, (dom_n, dom_ms) = max(per_kernel.items(), key=lambda kv: kv[1][1])
+    dom_avg_ms = dom_ms / dom_n
+    tok_heads = NT * H
+    kernel_bytes = {
+        "kda_gate": tok_heads * gate_bytes_per_token_head(2),
+        "kda_simt_prep": tok_heads * (prefill_bytes_per_token_head(2) - D * 2),
+        "kda_simt_chain": tok_heads * D * 2 + 2 * H * state_bytes(),
+    }
+    alg_bytes = kernel_bytes.get(dom_name)
+    achieved = alg_bytes / (dom_avg_ms * 1e-3) / 1e9 if alg_bytes else None
+    step_bytes = tok_heads * (prefill_bytes_per_token_head(2) + gate_bytes_per_token_head(2)) \
+        + 2 * H * state_bytes()
+    step_floor_ms = step_bytes / (hbm_peak * 1e9) * 1e3
+
+    # decode step (512 x 96, fp32 state, in place)
+    dw = workloads.decode()
+    S = workloads.make_decode_state(dw, dev)
+    dinp = workloads.make_decode_step(dw, 0, dev)
+    dg = kda.gate(dinp["z"], dinp["A"])
+    do = torch.empty(dw.N, dw.H, D, dtype=torch.bfloat16, device=dev)
+
+    def dstep():
+        kda.recurrent_step(dinp["q"], dinp["k"], dinp["v"], dg, dinp["beta"], S, out=do)
+
+    ms_dec = timed(dstep, max(args.steps, 20), args.warmup)
+    dec_bytes = dw.N * dw.H * decode_bytes_per_head_step()
+    dec_gbs = dec_bytes / (ms_dec * 1e-3) / 1e9
+    del S
+
+    # end to end through the public API with host buffers
+    pin = {k: v.cpu().pin_memory() for k, v in inp.items() if isinstance(v, torch.Tensor)
+           and k in ("z", "q", "k", "v", "beta", "A", "h0", "cu_seqlens")}
+    o_host = torch.empty(NT, H, D, dtype=torch.bfloat16).pin_memory()
+    hT_host = torch.empty(1, H, D, D, dtype=torch.float32).pin_memory()
+    dbuf = {k: torch.empty_like(v, device=dev) for k, v in pin.items()}
+    h2d = sum(v.numel() * v.element_size() for v in pin.values())
+    d2h = o_host.numel() * 2 + hT_host.numel() * 4
+
+    def e2e_step():
+        for k_, v_ in pin.items():
+            dbuf[k_].copy_(v_, non_blocking=True)
+        kda.gate(dbuf["z"], dbuf["A"], out=g)
+        kda.chunk_fwd(dbuf["q"], dbuf["k"], dbuf["v"], g, dbuf["beta"], dbuf["h0"],
+                      dbuf["cu_seqlens"], workspace=ws, out=o, final_state_out=hT)
+        o_host.copy_(o, non_blocking=True)
+        hT_host.copy_(hT, non_blocking=True)
+
+    ms_e2e = timed(e2e_step, max(3, args.steps // 4), max(3, args.warmup))
+    clocks.stop()
+    e2e_tps = NT * world / (ms_e2e * 1e-3)
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = cpu_baseline()
+    line = {
+        "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "global_batch": world, "seq_len": NT, "heads": H,
+                   "dk": D, "dv": D, "chunk": 64, "step": "kda_gate + kda_chunk_fwd",
+                   "l2": "inputs larger than L2 (201 MB per q/k/v/z tensor), no flush",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": achieved,
+                     "peak": hbm_peak, "unit": "GB/s",
+                     "frac": (achieved / hbm_peak) if achieved else None,
+                     "traffic": kernel_traffic(dom_name),
+                     "alg_bytes_per_launch": alg_bytes, "mean_launch_ms": dom_avg_ms,
+                     "peak_source": f"{peak_src} hbm_gbs",
+                     "step_floor_ms": step_floor_ms, "step_frac": step_floor_ms / ms_step},
+        "kernels": {k: {"launches": n, "mean_ms": t / n} for k, (n, t) in per_kernel.items()},
+        "decode": {"workload": dw.name, "ms_per_step": ms_dec, "achieved_gbs": dec_gbs,
+                   "peak_gbs": hbm_peak, "frac": dec_gbs / hbm_peak,
+                   "bytes_per_step": dec_bytes},
+        "e2e": {"value": e2e_tps, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
+        "gpu_launches": launches,
+        "cpu_baseline": cpu,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--ref-heads", type=int, default=16)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,238 @@
+"""GB300 Kimi Delta Attention (KDA) forward -- Python binding of libkda.
+
+A thin ctypes layer over the C ABI in ``include/kda.h``: it checks tensor
+dtypes, devices and contiguity, passes ``data_ptr()`` values and the current
+CUDA stream, and raises :class:`KdaError` on a non-OK status.  Every step of
+the computation runs in the library's CUDA kernels; there is no CPU or
+PyTorch fallback, and importing this package fails if ``libkda.so`` has not
+been built (``python -m chunked_gated_delta_fwd_gb300._build``).
+
+Entry points (same names as the C calls, without the ``kda_`` prefix):
+
+* :func:`gate` -- ``g = g_min * Sigmoid(exp(A_h) z)`` (optionally the in-chunk
+  running sum),
+* :func:`chunk_fwd` -- prefill over whole (packed, variable-length) sequences,
+* :func:`recurrent_step` -- one decode token per sequence, state in place.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import _build
+
+__all__ = ["KdaError", "gate", "chunk_fwd", "chunk_fwd_workspace_size", "recurrent_step",
+           "library_path", "lib", "get_device_error", "profile_enable", "profile_collect", "G_MIN", "F32", "BF16", "FP32_CORES"]
+
+G_MIN = -5.0
+F32, BF16 = 0, 1
+FP32_CORES = 1  # flag of chunk_fwd: evaluate bf16 inputs on fp32 CUDA cores
+
+_STATUS = {
+    0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED_SHAPE",
+    3: "KDA_ERR_UNSUPPORTED_DTYPE", 4: "KDA_ERR_MISALIGNED", 5: "KDA_ERR_WORKSPACE_TOO_SMALL",
+    6: "KDA_ERR_CUDA", 7: "KDA_ERR_DEVICE_TIMEOUT", 8: "KDA_ERR_NO_DEVICE",
+}
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+def library_path() -> str:
+    return os.environ.get("KDA_LIBRARY", _build.LIB)
+
+
+def _load() -> ctypes.CDLL:
+    path = library_path()
+    if not os.path.exists(path):
+        raise ImportError(f"libkda.so not found at {path}; build it with "
+                          f"`python -m chunked_gated_delta_fwd_gb300._build`")
+    L = ctypes.CDLL(path)
+    vp, i32, i64, f32, sz, u32 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                                  ctypes.c_size_t, ctypes.c_uint)
+    L.kda_gate.argtypes = [vp, i32, vp, f32, vp, i64, i32, i32, vp, vp, i32, vp]
+    L.kda_chunk_fwd_workspace_size.argtypes = [i64, i32, i32, i32]
+    L.kda_chunk_fwd_workspace_size.restype = sz
+    L.kda_chunk_fwd.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i64, i32, i32, i32, vp,
+                                vp, vp, sz, vp]
+    L.kda_chunk_fwd_ex.argtypes = L.kda_chunk_fwd.argtypes + [u32]
+    L.kda_recurrent_step.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, vp]
+    L.kda_last_error_string.restype = ctypes.c_char_p
+    L.kda_get_device_error.argtypes = [vp]
+    L.kda_version.restype = ctypes.c_char_p
+    L.kda_profile_enable.argtypes = [i32]
+    L.kda_profile_get.argtypes = [i32, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(i32),
+                                  ctypes.POINTER(ctypes.c_double)]
+    for fn in (L.kda_gate, L.kda_chunk_fwd, L.kda_chunk_fwd_ex, L.kda_recurrent_step,
+               L.kda_get_device_error):
+        fn.restype = ctypes.c_int
+    return L
+
+
+lib = _load()
+
+
+def _check(status: int):
+    if status != 0:
+        raise KdaError(status, lib.kda_last_error_string().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"unsupported dtype {t.dtype} (bfloat16 or float32)")
+
+
+def _need(t: torch.Tensor, name: str, dtype=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def gate(z: torch.Tensor, A: torch.Tensor, g_min: float = G_MIN, *, out=None,
+         with_cumsum: bool = False, cu_seqlens: Optional[torch.Tensor] = None):
+    """g = g_min * Sigmoid(exp(A[h]) * z) for z of shape [..., H, 128] (bf16/fp32).
+
+    Returns g (fp32, z's shape), or (g, gcum) with ``with_cumsum`` where gcum is the
+    running sum of g inside each 64-token chunk of each sequence.
+    """
+    _need(z, "z")
+    _need(A, "A", torch.float32, z.device)
+    H, dk = z.shape[-2], z.shape[-1]
+    NT = z.numel() // (H * dk) if z.numel() else 0
+    g = out if out is not None else torch.empty(z.shape, dtype=torch.float32, device=z.device)
+    _need(g, "out", torch.float32, z.device)
+    gcum = torch.empty_like(g) if with_cumsum else None
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32, z.device)
+    n_seqs = cu_seqlens.numel() - 1 if cu_seqlens is not None else 1
+    with torch.cuda.device(z.device):
+        _check(lib.kda_gate(_ptr(z), _dtype_code(z), _ptr(A), float(g_min), _ptr(g), NT, H, dk,
+                            _ptr(gcum), _ptr(cu_seqlens), n_seqs, _stream(z.device)))
+    return (g, gcum) if with_cumsum else g
+
+
+def chunk_fwd_workspace_size(n_tokens: int, n_seqs: int, H: int, dtype=torch.bfloat16,
+                             flags: int = 0) -> int:
+    code = F32 if (flags & FP32_CORES) else (BF16 if dtype == torch.bfloat16 else F32)
+    return int(lib.kda_chunk_fwd_workspace_size(int(n_tokens), int(n_seqs), int(H), code))
+
+
+def chunk_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, *, output_final_state=True,
+              workspace=None, flags: int = 0, out=None, final_state_out=None):
+    """KDA prefill over whole sequences.
+
+    q, k: [B, T, H, 128] or packed [T, H, 128] (with ``cu_seqlens``), bf16 or fp32;
+    v like q; g: same shape, fp32 log-decays in [-5, 0]; beta: [..., H] (dtype of q);
+    h0: [N, H, 128, 128] fp32 (the state stored transposed, [dv][dk]) or None;
+    cu_seqlens: int32 [N+1] on the device, or None for B sequences of length T.
+    Returns ``(o, hT)`` with o like v and hT [N, H, 128, 128] fp32 (None if not asked).
+    """
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta)):
+        _need(t, name, q.dtype, dev)
+    _need(g, "g", torch.float32, dev)
+    dt = _dtype_code(q)
+    H, dk, dv = q.shape[-2], q.shape[-1], v.shape[-1]
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+        N = cu_seqlens.numel() - 1
+        B, T = 1, q.numel() // (H * dk)
+        if q.dim() == 4 and q.shape[0] != 1:
+            raise ValueError("with cu_seqlens, q must be packed as [1, NT, H, D] or [NT, H, D]")
+    else:
+        if q.dim() != 4:
+            raise ValueError("q must be [B, T, H, D] without cu_seqlens")
+        B, T = q.shape[0], q.shape[1]
+        N = B
+    NT = B * T if cu_seqlens is None else T
+    if h0 is not None:
+        _need(h0, "h0", torch.float32, dev)
+        if tuple(h0.shape) != (N, H, dv, dk):
+            raise ValueError(f"h0 must be [{N}, {H}, {dv}, {dk}], got {tuple(h0.shape)}")
+    o = out if out is not None else torch.empty(v.shape, dtype=v.dtype, device=dev)
+    _need(o, "out", v.dtype, dev)
+    hT = None
+    if output_final_state:
+        hT = final_state_out if final_state_out is not None else torch.empty(
+            (N, H, dv, dk), dtype=torch.float32, device=dev)
+        _need(hT, "final_state_out", torch.float32, dev)
+    need = chunk_fwd_workspace_size(NT, N, H, q.dtype, flags)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", torch.uint8, dev)
+    with torch.cuda.device(dev):
+        _check(lib.kda_chunk_fwd_ex(_ptr(q), _ptr(k), _ptr(v), dt, _ptr(g), _ptr(beta), _ptr(h0),
+                                    _ptr(cu_seqlens), N, B, T, H, dk, dv, _ptr(o), _ptr(hT),
+                                    _ptr(workspace), workspace.numel(), _stream(dev),
+                                    int(flags)))
+    return o, hT
+
+
+def recurrent_step(q, k, v, g, beta, S, *, out=None):
+    """One decode token: q, k, v [N, H, 128] (bf16/fp32), g [N, H, 128] fp32,
+    beta [N, H], S [N, H, 128, 128] fp32 updated in place.  Returns o [N, H, 128]."""
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta)):
+        _need(t, name, q.dtype, dev)
+    _need(g, "g", torch.float32, dev)
+    _need(S, "S", torch.float32, dev)
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    o = out if out is not None else torch.empty(v.shape, dtype=v.dtype, device=dev)
+    _need(o, "out", v.dtype, dev)
+    with torch.cuda.device(dev):
+        _check(lib.kda_recurrent_step(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(g),
+                                      _ptr(beta), _ptr(S), _ptr(o), N, H, dk, dv, _stream(dev)))
+    return o
+
+
+def profile_enable(on: bool = True):
+    """Start (clearing earlier records) or stop per-kernel CUDA-event timing."""
+    lib.kda_profile_enable(1 if on else 0)
+
+
+def profile_collect() -> dict:
+    """Waits for the recorded events; returns {kernel: (launches, total_ms)}."""
+    n = lib.kda_profile_collect()
+    if n < 0:
+        raise KdaError(6, "profile collection failed")
+    out = {}
+    for i in range(n):
+        name = ctypes.c_char_p()
+        launches = ctypes.c_int()
+        total = ctypes.c_double()
+        lib.kda_profile_get(i, ctypes.byref(name), ctypes.byref(launches), ctypes.byref(total))
+        out[name.value.decode()] = (launches.value, total.value)
+    return out
+
+
+def get_device_error(device=None):
+    """Raise KdaError if a kernel recorded a device-side error (syncs the stream)."""
+    device = device or torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(device):
+        _check(lib.kda_get_device_error(_stream(device)))

@@ -1,0 +1,406 @@
+// kda_api.cu -- the C ABI of libkda (declared in include/kda.h): argument
+// validation, workspace sizing, the device-side chunk plan and kernel dispatch.
+//
+// All checks happen on the host before anything is enqueued, so a call that
+// returns an error has launched nothing.  Nothing here synchronizes except
+// kda_get_device_error().
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/kda.h"
+#include "kda_internal.cuh"
+
+namespace kda {
+
+// Device error flag: bounded waits and the plan's sequence checks write a code
+// here; kda_get_device_error() reads and clears it.
+__device__ int g_device_error;
+
+int* device_error_flag() {
+  static int* ptrs[64] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int*>(p);
+  }
+  return ptrs[dev];
+}
+
+// ---------------------------------------------------------------- profiling
+namespace {
+struct ProfRecord {
+  const char* name;
+  cudaEvent_t start, stop;
+};
+struct ProfState {
+  std::mutex mu;
+  bool on = false;
+  ProfRecord* recs = nullptr;
+  int n = 0, cap = 0;
+  // aggregated results after kda_profile_collect()
+  const char* names[64];
+  int launches[64];
+  double total_ms[64];
+  int n_names = 0;
+};
+ProfState& prof() {
+  static ProfState p;
+  return p;
+}
+}  // namespace
+
+ProfScope::ProfScope(const char* name, cudaStream_t s) : slot(-1), stream(s) {
+  ProfState& P = prof();
+  std::lock_guard<std::mutex> lock(P.mu);
+  if (!P.on) return;
+  if (P.n == P.cap) {
+    const int ncap = P.cap ? 2 * P.cap : 1024;
+    ProfRecord* r = static_cast<ProfRecord*>(realloc(P.recs, sizeof(ProfRecord) * ncap));
+    if (!r) return;
+    P.recs = r;
+    P.cap = ncap;
+  }
+  ProfRecord& rec = P.recs[P.n];
+  if (cudaEventCreate(&rec.start) != cudaSuccess) return;
+  if (cudaEventCreate(&rec.stop) != cudaSuccess) {
+    cudaEventDestroy(rec.start);
+    return;
+  }
+  rec.name = name;
+  cudaEventRecord(rec.start, s);
+  slot = P.n++;
+}
+
+ProfScope::~ProfScope() {
+  if (slot < 0) return;
+  ProfState& P = prof();
+  std::lock_guard<std::mutex> lock(P.mu);
+  cudaEventRecord(P.recs[slot].stop, stream);
+}
+
+size_t plan_bytes(int n_seqs) {
+  const size_t b = 2 * sizeof(int32_t) * (size_t)(n_seqs + 1);
+  return (b + 255) & ~size_t(255);
+}
+
+// One CTA: writes cu[N+1] (copied from cu_seqlens, or n*T_per_seq) and the
+// exclusive prefix sum of ceil(len/64) into chunk_off[N+1].  Invalid sequence
+// offsets (decreasing, outside [0, NT], cu[0] != 0 or cu[N] != NT) are clamped so
+// that no later kernel can index outside the inputs, and flag an error.
+__global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ cu_in, int n_seqs,
+                                                    int64_t T_per_seq, int64_t n_tokens,
+                                                    int32_t* __restrict__ cu_out,
+                                                    int32_t* __restrict__ chunk_off,
+                                                    int* err_flag) {
+  __shared__ int32_t warp_sums[32];
+  __shared__ int32_t carry;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    carry = 0;
+  }
+  __syncthreads();
+  bool bad = false;
+  for (int base = 0; base <= n_seqs; base += blockDim.x) {
+    const int n = base + tid;
+    int32_t cu_n = 0, nchunks = 0;
+    if (n <= n_seqs) {
+      int64_t x = cu_in ? (int64_t)cu_in[n] : (int64_t)n * T_per_seq;
+      if (n == 0 && x != 0) bad = true;
+      if (n == n_seqs && x != n_tokens) bad = true;
+      if (x < 0) { x = 0; bad = true; }
+      if (x > n_tokens) { x = n_tokens; bad = true; }
+      cu_n = (int32_t)x;
+      cu_out[n] = cu_n;
+    }
+    __syncthreads();
+    if (n < n_seqs) {
+      int64_t nx = cu_in ? (int64_t)cu_in[n + 1] : (int64_t)(n + 1) * T_per_seq;
+      if (nx > n_tokens) nx = n_tokens;
+      if (nx < cu_n) { nx = cu_n; bad = true; }
+      nchunks = (int32_t)((nx - cu_n + kChunk - 1) / kChunk);
+    }
+    // block-wide exclusive scan of nchunks
+    int32_t v = nchunks;
+    const int lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
+    }
+    if (lane == 31) warp_sums[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+      int32_t w = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      warp_sums[lane] = w;
+    }
+    __syncthreads();
+    const int32_t incl = v + (warp > 0 ? warp_sums[warp - 1] : 0);
+    if (n <= n_seqs) chunk_off[n] = carry + incl - nchunks;
+    __syncthreads();
+    if (tid == blockDim.x - 1) carry += incl;
+    __syncthreads();
+  }
+  if (bad && err_flag) atomicExch(err_flag, kDevErrBadSeqlens);
+}
+
+cudaError_t launch_plan(const int32_t* cu_seqlens_or_null, int n_seqs, int64_t T_per_seq,
+                        int64_t n_tokens, void* ws, int* err_flag, cudaStream_t s) {
+  int32_t* cu = static_cast<int32_t*>(ws);
+  int32_t* off = cu + (n_seqs + 1);
+  ProfScope prof_scope("kda_plan", s);
+  plan_kernel<<<1, 1024, 0, s>>>(cu_seqlens_or_null, n_seqs, T_per_seq, n_tokens, cu, off,
+                                 err_flag);
+  return cudaGetLastError();
+}
+
+}  // namespace kda
+
+// ============================================================================ C ABI
+namespace {
+
+thread_local char t_err[512] = "no error";
+
+kda_status_t fail(kda_status_t st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_err, sizeof(t_err), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+kda_status_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(KDA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+kda_status_t check_device() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3)
+    return fail(KDA_ERR_NO_DEVICE, "device %d is sm_%d%d; libkda is built for sm_103a only", dev,
+                major, minor);
+  return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kda_version(void) { return "0.1.0"; }
+
+int kda_profile_enable(int on) {
+  kda::ProfState& P = kda::prof();
+  std::lock_guard<std::mutex> lock(P.mu);
+  for (int i = 0; i < P.n; ++i) {
+    cudaEventDestroy(P.recs[i].start);
+    cudaEventDestroy(P.recs[i].stop);
+  }
+  P.n = 0;
+  P.n_names = 0;
+  P.on = on != 0;
+  return 0;
+}
+
+int kda_profile_collect(void) {
+  kda::ProfState& P = kda::prof();
+  std::lock_guard<std::mutex> lock(P.mu);
+  P.n_names = 0;
+  for (int i = 0; i < P.n; ++i) {
+    if (cudaEventSynchronize(P.recs[i].stop) != cudaSuccess) return -1;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, P.recs[i].start, P.recs[i].stop) != cudaSuccess) return -1;
+    int j = 0;
+    while (j < P.n_names && strcmp(P.names[j], P.recs[i].name) != 0) ++j;
+    if (j == P.n_names) {
+      if (P.n_names == 64) continue;
+      P.names[j] = P.recs[i].name;
+      P.launches[j] = 0;
+      P.total_ms[j] = 0.0;
+      ++P.n_names;
+    }
+    P.launches[j] += 1;
+    P.total_ms[j] += ms;
+  }
+  return P.n_names;
+}
+
+int kda_profile_get(int i, const char** name, int* launches, double* total_ms) {
+  kda::ProfState& P = kda::prof();
+  std::lock_guard<std::mutex> lock(P.mu);
+  if (i < 0 || i >= P.n_names || !name || !launches || !total_ms) return -1;
+  *name = P.names[i];
+  *launches = P.launches[i];
+  *total_ms = P.total_ms[i];
+  return 0;
+}
+
+const char* kda_last_error_string(void) { return t_err; }
+
+kda_status_t kda_get_device_error(kda_stream_t stream) {
+  int* flag = kda::device_error_flag();
+  if (!flag) return fail(KDA_ERR_CUDA, "device error flag unavailable");
+  int host = 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(&host, flag, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "reading device error flag");
+  if (host == 0) return KDA_OK;
+  const int zero = 0;
+  e = cudaMemcpyAsync(flag, &zero, sizeof(int), cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing device error flag");
+  if (host == kda::kDevErrTimeout)
+    return fail(KDA_ERR_DEVICE_TIMEOUT, "a bounded device-side wait gave up");
+  if (host == kda::kDevErrBadSeqlens)
+    return fail(KDA_ERR_INVALID_ARG,
+                "cu_seqlens was not nondecreasing from 0 to n_tokens (clamped on the device)");
+  return fail(KDA_ERR_CUDA, "device error code %d", host);
+}
+
+kda_status_t kda_gate(const void* z, int z_dtype, const float* A, float g_min, float* g,
+                      int64_t n_tokens, int H, int dk, float* gcum, const int32_t* cu_seqlens,
+                      int n_seqs, kda_stream_t stream) {
+  if (z_dtype != KDA_F32 && z_dtype != KDA_BF16)
+    return fail(KDA_ERR_UNSUPPORTED_DTYPE, "kda_gate: z_dtype %d", z_dtype);
+  if (dk != kda::kD) return fail(KDA_ERR_UNSUPPORTED_SHAPE, "kda_gate: dk=%d (need 128)", dk);
+  if (H < 1) return fail(KDA_ERR_UNSUPPORTED_SHAPE, "kda_gate: H=%d", H);
+  if (n_tokens < 0 || n_tokens > INT32_MAX)
+    return fail(KDA_ERR_INVALID_ARG, "kda_gate: n_tokens=%lld", (long long)n_tokens);
+  if (!(g_min < 0.f)) return fail(KDA_ERR_INVALID_ARG, "kda_gate: g_min must be < 0");
+  if (n_tokens == 0) return KDA_OK;
+  if (!z || !A || !g) return fail(KDA_ERR_INVALID_ARG, "kda_gate: null z, A or g");
+  if (!aligned16(z) || !aligned16(g) || (gcum && !aligned16(gcum)))
+    return fail(KDA_ERR_MISALIGNED, "kda_gate: z, g, gcum must be 16-byte aligned");
+  if (gcum && cu_seqlens && n_seqs < 1)
+    return fail(KDA_ERR_INVALID_ARG, "kda_gate: n_seqs=%d with cu_seqlens", n_seqs);
+  kda_status_t st = check_device();
+  if (st != KDA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (gcum)
+    e = kda::launch_gate_cumsum(z, z_dtype == KDA_BF16, A, g_min, g, gcum, n_tokens, H,
+                                cu_seqlens, cu_seqlens ? n_seqs : 1, s);
+  else
+    e = kda::launch_gate(z, z_dtype == KDA_BF16, A, g_min, g, n_tokens, H, s);
+  if (e != cudaSuccess) return cuda_fail(e, "kda_gate launch");
+  return KDA_OK;
+}
+
+size_t kda_chunk_fwd_workspace_size(int64_t n_tokens, int n_seqs, int H, int dtype) {
+  if (n_tokens < 0 || n_seqs < 1 || H < 1) return 0;
+  if (dtype == KDA_BF16)
+    return kda::plan_bytes(n_seqs) + kda::tc_workspace_bytes(n_tokens, n_seqs, H);
+  if (dtype == KDA_F32)
+    return kda::plan_bytes(n_seqs) + kda::simt_workspace_bytes(n_tokens, n_seqs, H);
+  return 0;
+}
+
+kda_status_t kda_chunk_fwd_ex(const void* q, const void* k, const void* v, int dtype,
+                                const float* g, const void* beta, const float* h0,
+                                const int32_t* cu_seqlens, int n_seqs, int B, int64_t T, int H,
+                                int dk, int dv, void* o, float* hT, void* workspace,
+                                size_t ws_bytes, kda_stream_t stream, unsigned flags) {
+  if (dtype != KDA_F32 && dtype != KDA_BF16)
+    return fail(KDA_ERR_UNSUPPORTED_DTYPE, "kda_chunk_fwd: dtype %d", dtype);
+  if (dk != kda::kD || dv != kda::kD)
+    return fail(KDA_ERR_UNSUPPORTED_SHAPE, "kda_chunk_fwd: dk=%d dv=%d (need 128)", dk, dv);
+  if (H < 1) return fail(KDA_ERR_UNSUPPORTED_SHAPE, "kda_chunk_fwd: H=%d", H);
+  int N;
+  int64_t NT, T_per_seq = 0;
+  if (cu_seqlens) {
+    if (B != 1) return fail(KDA_ERR_INVALID_ARG, "kda_chunk_fwd: B must be 1 with cu_seqlens");
+    if (n_seqs < 1) return fail(KDA_ERR_INVALID_ARG, "kda_chunk_fwd: n_seqs=%d", n_seqs);
+    N = n_seqs;
+    NT = T;
+  } else {
+    if (B < 1) return fail(KDA_ERR_INVALID_ARG, "kda_chunk_fwd: B=%d", B);
+    N = B;
+    NT = (int64_t)B * T;
+    T_per_seq = T;
+  }
+  if (T < 0 || NT > INT32_MAX - 2 * kda::kChunk)
+    return fail(KDA_ERR_INVALID_ARG, "kda_chunk_fwd: token count out of range");
+  if ((NT > 0 && (!q || !k || !v || !g || !beta || !o)) || (N > 0 && !workspace))
+    return fail(KDA_ERR_INVALID_ARG, "kda_chunk_fwd: null required pointer");
+  const void* ptrs[] = {q, k, v, g, beta, h0, o, hT};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p))
+      return fail(KDA_ERR_MISALIGNED, "kda_chunk_fwd: pointers must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(KDA_ERR_MISALIGNED, "kda_chunk_fwd: workspace must be 256-byte aligned");
+  const size_t need = kda_chunk_fwd_workspace_size(
+      NT, N, H, (flags & KDA_CHUNK_FP32_CORES) ? (int)KDA_F32 : dtype);
+  if (ws_bytes < need)
+    return fail(KDA_ERR_WORKSPACE_TOO_SMALL, "kda_chunk_fwd: workspace %zu < %zu bytes",
+                ws_bytes, need);
+  if (flags & ~(unsigned)KDA_CHUNK_FP32_CORES)
+    return fail(KDA_ERR_INVALID_ARG, "kda_chunk_fwd_ex: unknown flags 0x%x", flags);
+  kda_status_t st = check_device();
+  if (st != KDA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int* err = kda::device_error_flag();
+  cudaError_t e = kda::launch_plan(cu_seqlens, N, T_per_seq, NT, workspace, err, s);
+  if (e != cudaSuccess) return cuda_fail(e, "kda_chunk_fwd plan launch");
+  if (dtype == KDA_BF16 && !(flags & KDA_CHUNK_FP32_CORES))
+    e = kda::launch_chunk_tc(q, k, v, g, beta, h0, o, hT, NT, N, H, workspace, err, s);
+  else
+    e = kda::launch_chunk_simt(q, k, v, dtype == KDA_BF16, g, beta, h0, o, hT, NT, N, H,
+                               workspace, s);
+  if (e != cudaSuccess) return cuda_fail(e, "kda_chunk_fwd launch");
+  return KDA_OK;
+}
+
+kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v, int dtype,
+                           const float* g, const void* beta, const float* h0,
+                           const int32_t* cu_seqlens, int n_seqs, int B, int64_t T, int H,
+                           int dk, int dv, void* o, float* hT, void* workspace, size_t ws_bytes,
+                           kda_stream_t stream) {
+  return kda_chunk_fwd_ex(q, k, v, dtype, g, beta, h0, cu_seqlens, n_seqs, B, T, H, dk, dv, o, hT,
+                          workspace, ws_bytes, stream, 0u);
+}
+
+kda_status_t kda_recurrent_step(const void* q, const void* k, const void* v, int dtype,
+                                const float* g, const void* beta, float* S, void* o, int N, int H,
+                                int dk, int dv, kda_stream_t stream) {
+  if (dtype != KDA_F32 && dtype != KDA_BF16)
+    return fail(KDA_ERR_UNSUPPORTED_DTYPE, "kda_recurrent_step: dtype %d", dtype);
+  if (dk != kda::kD || dv != kda::kD)
+    return fail(KDA_ERR_UNSUPPORTED_SHAPE, "kda_recurrent_step: dk=%d dv=%d (need 128)", dk, dv);
+  if (H < 1 || N < 0) return fail(KDA_ERR_UNSUPPORTED_SHAPE, "kda_recurrent_step: N=%d H=%d", N, H);
+  if ((int64_t)N * H > INT32_MAX)
+    return fail(KDA_ERR_INVALID_ARG, "kda_recurrent_step: N*H too large");
+  if (N == 0) return KDA_OK;
+  if (!q || !k || !v || !g || !beta || !S || !o)
+    return fail(KDA_ERR_INVALID_ARG, "kda_recurrent_step: null pointer");
+  const void* ptrs[] = {q, k, v, g, S, o};
+  for (const void* p : ptrs)
+    if (!aligned16(p))
+      return fail(KDA_ERR_MISALIGNED, "kda_recurrent_step: pointers must be 16-byte aligned");
+  kda_status_t st = check_device();
+  if (st != KDA_OK) return st;
+  cudaError_t e = kda::launch_decode(q, k, v, dtype == KDA_BF16, g, beta, S, o, N, H,
+                                     reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kda_recurrent_step launch");
+  return KDA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,111 @@
+// kda_decode.cu -- K5: one decode token of KDA for N x H independent states,
+// updated in place, in the delta form
+//     S <- D S + beta k (v^T - k^T D S),   D = Diag(exp(g)),   o = S^T q
+// ("Kimi K3: architecture, training and inference systems" (weigao.cc),
+//  section 3.1 for the form, sections 11.2 / 13.2 for the in-place decode step).
+//
+// The state is stored transposed, S^T [dv][dk] fp32, so row j (one value column
+// of S) is 128 contiguous floats = 512 bytes.  Per row j:
+//     s_bar = alpha (.) s_j,   p = k . s_bar,   r = q . s_bar
+//     s_j  <- s_bar + beta (v_j - p) k
+//     o_j   = q . s_j = r + beta (v_j - p) (q . k)
+// One CTA per (sequence, head), four warps, each warp streams 32 rows; lane l
+// holds channels 4l..4l+3, so a row is one coalesced 128-bit load and one
+// 128-bit store per lane.  p and r are reduced together with butterfly
+// shuffles.  The kernel is HBM-bound: 2 x 64 KiB of state per head and step.
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int kDecodeThreads = 128;
+constexpr int kRowsPerIter = 8;  // rows in flight per warp
+
+template <typename T>
+__global__ void __launch_bounds__(kDecodeThreads) decode_kernel(
+    const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+    const float* __restrict__ g, const T* __restrict__ beta, float* __restrict__ S,
+    T* __restrict__ o) {
+  const int unit = blockIdx.x;  // n * H + h
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int64_t vec = (int64_t)unit * kD;
+
+  float qv[4], kv[4], alpha[4];
+  load4(q + vec + 4 * lane, qv);
+  load4(k + vec + 4 * lane, kv);
+  {
+    const float4 gg = *reinterpret_cast<const float4*>(g + vec + 4 * lane);
+    alpha[0] = expf(gg.x);
+    alpha[1] = expf(gg.y);
+    alpha[2] = expf(gg.z);
+    alpha[3] = expf(gg.w);
+  }
+  const float b = to_f32(beta[unit]);
+  float qk = qv[0] * kv[0] + qv[1] * kv[1] + qv[2] * kv[2] + qv[3] * kv[3];
+#pragma unroll
+  for (int o_ = 16; o_ > 0; o_ >>= 1) qk += __shfl_xor_sync(0xffffffffu, qk, o_);
+  const int row0 = warp * 32;
+  const float v_mine = to_f32(v[vec + row0 + lane]);
+  float o_mine = 0.f;
+
+  float4* Srow = reinterpret_cast<float4*>(S + (int64_t)unit * kD * kD) + row0 * (kD / 4) + lane;
+
+#pragma unroll 1
+  for (int r0 = 0; r0 < 32; r0 += kRowsPerIter) {
+    float4 s[kRowsPerIter];
+#pragma unroll
+    for (int i = 0; i < kRowsPerIter; ++i) s[i] = __ldcs(Srow + (r0 + i) * (kD / 4));
+    float p[kRowsPerIter], r[kRowsPerIter];
+#pragma unroll
+    for (int i = 0; i < kRowsPerIter; ++i) {
+      s[i].x *= alpha[0];
+      s[i].y *= alpha[1];
+      s[i].z *= alpha[2];
+      s[i].w *= alpha[3];
+      p[i] = kv[0] * s[i].x + kv[1] * s[i].y + kv[2] * s[i].z + kv[3] * s[i].w;
+      r[i] = qv[0] * s[i].x + qv[1] * s[i].y + qv[2] * s[i].z + qv[3] * s[i].w;
+    }
+#pragma unroll
+    for (int o_ = 16; o_ > 0; o_ >>= 1) {
+#pragma unroll
+      for (int i = 0; i < kRowsPerIter; ++i) {
+        p[i] += __shfl_xor_sync(0xffffffffu, p[i], o_);
+        r[i] += __shfl_xor_sync(0xffffffffu, r[i], o_);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kRowsPerIter; ++i) {
+      const float vj = __shfl_sync(0xffffffffu, v_mine, r0 + i);
+      const float u = b * (vj - p[i]);
+      s[i].x = fmaf(u, kv[0], s[i].x);
+      s[i].y = fmaf(u, kv[1], s[i].y);
+      s[i].z = fmaf(u, kv[2], s[i].z);
+      s[i].w = fmaf(u, kv[3], s[i].w);
+      __stcs(Srow + (r0 + i) * (kD / 4), s[i]);
+      if (lane == r0 + i) o_mine = fmaf(u, qk, r[i]);
+    }
+  }
+  o[vec + row0 + lane] = from_f32<T>(o_mine);
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const void* q, const void* k, const void* v, int bf16, const float* g,
+                          const void* beta, float* S, void* o, int N, int H, cudaStream_t s) {
+  const unsigned grid = (unsigned)((int64_t)N * H);
+  ProfScope prof_scope("kda_decode", s);
+  if (bf16) {
+    using T = __nv_bfloat16;
+    decode_kernel<T><<<grid, kDecodeThreads, 0, s>>>(
+        static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), g,
+        static_cast<const T*>(beta), S, static_cast<T*>(o));
+  } else {
+    decode_kernel<float><<<grid, kDecodeThreads, 0, s>>>(
+        static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v),
+        g, static_cast<const float*>(beta), S, static_cast<float*>(o));
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -1,0 +1,137 @@
+// kda_gate.cu -- K1: the bounded log-decay of KDA,
+//     g = g_min * Sigmoid(exp(A_h) * z)        ("Kimi K3 technical report review"
+//                                               (devpress/CSDN), section 3.2, Eq. 5)
+// and, optionally, its running sum inside each 64-token chunk of each sequence
+// (the log of the in-chunk cumulative decay Gamma of the chunkwise form,
+// "Kimi K3 notes" (s1mplewind blog), section "Chunkwise form").
+//
+// Memory-bound elementwise work: 8 elements per thread per step with 16-byte
+// (bf16) or 32-byte (fp32) loads and 32-byte stores, grid-stride over a grid
+// sized to the SM count.
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+__device__ __forceinline__ float bounded_decay(float z, float scale, float g_min) {
+  // g_min * Sigmoid(x) = g_min / (1 + exp(-x)); exp(-x) -> inf gives 0, -> 0 gives g_min.
+  return g_min / (1.0f + expf(-scale * z));
+}
+
+template <typename Tz>
+__global__ void __launch_bounds__(256) gate_kernel(const Tz* __restrict__ z,
+                                                   const float* __restrict__ A, float g_min,
+                                                   float* __restrict__ g, int64_t n_groups,
+                                                   int H) {
+  // group = 8 consecutive channels of one (token, head); kD / 8 = 16 groups per (t, h)
+  for (int64_t grp = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; grp < n_groups;
+       grp += (int64_t)gridDim.x * blockDim.x) {
+    const int h = (int)((grp / (kD / 8)) % H);
+    const float scale = expf(__ldg(A + h));
+    float x[8];
+    load8(z + grp * 8, x);
+    float4 lo, hi;
+    lo.x = bounded_decay(x[0], scale, g_min);
+    lo.y = bounded_decay(x[1], scale, g_min);
+    lo.z = bounded_decay(x[2], scale, g_min);
+    lo.w = bounded_decay(x[3], scale, g_min);
+    hi.x = bounded_decay(x[4], scale, g_min);
+    hi.y = bounded_decay(x[5], scale, g_min);
+    hi.z = bounded_decay(x[6], scale, g_min);
+    hi.w = bounded_decay(x[7], scale, g_min);
+    float4* out = reinterpret_cast<float4*>(g + grp * 8);
+    out[0] = lo;
+    out[1] = hi;
+  }
+}
+
+// One CTA per (64-token window, head); thread c walks the window's tokens for
+// channel c, resetting the running sum at every chunk start (cu[n] + 64 m).  A
+// window that begins inside a chunk first re-accumulates that chunk's earlier
+// tokens.  Stores are coalesced across the 128 channel threads.
+template <typename Tz>
+__global__ void __launch_bounds__(128) gate_cumsum_kernel(const Tz* __restrict__ z,
+                                                          const float* __restrict__ A,
+                                                          float g_min, float* __restrict__ g,
+                                                          float* __restrict__ gcum,
+                                                          int64_t n_tokens, int H,
+                                                          const int32_t* __restrict__ cu,
+                                                          int n_seqs) {
+  const int c = threadIdx.x;
+  const int h = blockIdx.y;
+  const int64_t t0 = (int64_t)blockIdx.x * kChunk;
+  const int64_t t1 = min(t0 + kChunk, n_tokens);
+  const float scale = expf(__ldg(A + h));
+  auto seq_start = [&](int n) -> int64_t {
+    if (!cu) return 0;
+    int64_t x = cu[n];
+    return x < 0 ? 0 : (x > n_tokens ? n_tokens : x);
+  };
+  auto seq_end = [&](int n) -> int64_t { return cu ? seq_start(n + 1) : n_tokens; };
+  // sequence containing t0: the last n with start(n) <= t0
+  int n = 0;
+  if (cu) {
+    int lo = 0, hi = n_seqs - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (seq_start(mid) <= t0) lo = mid; else hi = mid - 1;
+    }
+    n = lo;
+  }
+  int64_t cs = seq_start(n);
+  cs += ((t0 - cs) / kChunk) * kChunk;  // start of the chunk holding t0
+  float acc = 0.f;
+  for (int64_t t = cs; t < t0; ++t)
+    acc += bounded_decay(to_f32(z[(t * H + h) * kD + c]), scale, g_min);
+  for (int64_t t = t0; t < t1; ++t) {
+    while (n + 1 < n_seqs && seq_end(n) <= t) {
+      ++n;
+      if (seq_start(n) == t) acc = 0.f;  // a new sequence starts a new chunk
+    }
+    if (((t - seq_start(n)) % kChunk) == 0) acc = 0.f;
+    const int64_t i = (t * H + h) * kD + c;
+    const float gv = bounded_decay(to_f32(z[i]), scale, g_min);
+    acc += gv;
+    g[i] = gv;
+    gcum[i] = acc;
+  }
+}
+
+int grid_for(int64_t work, int threads) {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t need = (work + threads - 1) / threads;
+  const int64_t cap = (int64_t)sms * 8;
+  return (int)(need < cap ? (need < 1 ? 1 : need) : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_gate(const void* z, int z_bf16, const float* A, float g_min, float* g,
+                        int64_t n_tokens, int H, cudaStream_t s) {
+  const int64_t n_groups = n_tokens * H * (kD / 8);
+  const int grid = grid_for(n_groups, 256);
+  ProfScope prof_scope("kda_gate", s);
+  if (z_bf16)
+    gate_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(z), A, g_min, g, n_groups, H);
+  else
+    gate_kernel<<<grid, 256, 0, s>>>(static_cast<const float*>(z), A, g_min, g, n_groups, H);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gate_cumsum(const void* z, int z_bf16, const float* A, float g_min, float* g,
+                               float* gcum, int64_t n_tokens, int H, const int32_t* cu,
+                               int n_seqs, cudaStream_t s) {
+  const dim3 grid((unsigned)((n_tokens + kChunk - 1) / kChunk), (unsigned)H);
+  ProfScope prof_scope("kda_gate_cumsum", s);
+  if (z_bf16)
+    gate_cumsum_kernel<<<grid, kD, 0, s>>>(static_cast<const __nv_bfloat16*>(z), A, g_min, g, gcum,
+                                           n_tokens, H, cu, n_seqs);
+  else
+    gate_cumsum_kernel<<<grid, kD, 0, s>>>(static_cast<const float*>(z), A, g_min, g, gcum,
+                                           n_tokens, H, cu, n_seqs);
+  return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -1,0 +1,183 @@
+/*
+ * kda.h -- C ABI of the GB300 Kimi Delta Attention (KDA) forward library.
+ *
+ * KDA, per head, with state S in R^{dk x dv}:
+ *     S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = S_t^T q_t
+ *     alpha_t = exp(g_t),  g_t = g_min * Sigmoid(exp(A_h) * z_t),  g_min = -5
+ * ("Kimi K3 technical report review" (devpress/CSDN), section 3.1 Eq. 1 and
+ *  section 3.2 Eq. 5; "Kimi K3: architecture, training and inference systems"
+ *  (weigao.cc), section 3.1).
+ *
+ * Conventions shared by every call
+ *  - Pointers are DEVICE pointers unless a name says otherwise; the caller owns
+ *    every buffer and the stream.  The library allocates no device memory, keeps
+ *    no pointer after a call returns, and enqueues all work on `stream`
+ *    (asynchronous: results are ready when the stream reaches them).
+ *  - Token-major layouts.  A batch of N sequences is packed along the token
+ *    axis: q, k: [NT][H][dk], v, o: [NT][H][dv], g: [NT][H][dk], beta: [NT][H].
+ *    Sequence n owns tokens cu_seqlens[n] .. cu_seqlens[n+1]-1.
+ *  - The state is stored TRANSPOSED, fp32: S^T as [N][H][dv][dk] (dk contiguous),
+ *    the [B, H, V, K] layout of the FlashKDA state ("Kimi K3: architecture,
+ *    training and inference systems", section 13.1).  hT of kda_chunk_fwd and S of
+ *    kda_recurrent_step use the same layout, so a prefill's hT is a decode's S.
+ *  - dk = dv = 128 is required (the published K3 head size); anything else
+ *    returns KDA_ERR_UNSUPPORTED_SHAPE.
+ *  - Every pointer must be 16-byte aligned and every tensor contiguous;
+ *    otherwise KDA_ERR_MISALIGNED.  Arguments are checked before any launch: a
+ *    call that returns an error has enqueued nothing.
+ *  - Errors: a non-zero kda_status_t; kda_last_error_string() (per thread)
+ *    describes the last error.  Device-side waits are bounded: a kernel whose
+ *    wait runs out of iterations records KDA_ERR_DEVICE_TIMEOUT in a device flag
+ *    and exits; kda_get_device_error() reads and clears it.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* kda_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  KDA_OK = 0,
+  KDA_ERR_INVALID_ARG = 1,       /* null pointer where one is required, bad count or bound */
+  KDA_ERR_UNSUPPORTED_SHAPE = 2, /* dk or dv other than 128, H < 1 */
+  KDA_ERR_UNSUPPORTED_DTYPE = 3, /* dtype code not in kda_dtype_t */
+  KDA_ERR_MISALIGNED = 4,        /* pointer not 16-byte aligned */
+  KDA_ERR_WORKSPACE_TOO_SMALL = 5,
+  KDA_ERR_CUDA = 6,            /* a CUDA runtime call or launch failed */
+  KDA_ERR_DEVICE_TIMEOUT = 7,  /* a bounded device-side wait gave up */
+  KDA_ERR_NO_DEVICE = 8        /* no usable sm_103 device for this call */
+} kda_status_t;
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype_t;
+
+/*
+ * kda_gate -- bounded log-decay, elementwise:
+ *     g[t][h][c] = g_min * Sigmoid(exp(A[h]) * z[t][h][c])
+ * ("Kimi K3 technical report review", section 3.2, Eq. 5; g lies in [g_min, 0]).
+ *
+ *   z        [n_tokens][H][dk], dtype z_dtype (KDA_F32 or KDA_BF16)
+ *   A        [H] fp32, one log-scale per head
+ *   g_min    lower bound of the decay (the K3 report fixes -5); must be < 0
+ *   g        [n_tokens][H][dk] fp32, written
+ *   gcum     optional (NULL to skip) [n_tokens][H][dk] fp32: the inclusive running
+ *            sum of g inside each 64-token chunk of each sequence, restarting at
+ *            every chunk start (token cu[n] + 64 m) -- the log of the in-chunk
+ *            cumulative decay Gamma of the chunkwise form ("Kimi K3 notes"
+ *            (s1mplewind blog), section "Chunkwise form").
+ *   cu_seqlens optional device int32 [n_seqs+1] giving the sequence starts for
+ *            gcum; NULL means one sequence of n_tokens tokens.  Ignored if gcum is NULL.
+ * n_tokens == 0 is a no-op.
+ */
+kda_status_t kda_gate(const void* z, int z_dtype, const float* A, float g_min, float* g,
+                      int64_t n_tokens, int H, int dk, float* gcum, const int32_t* cu_seqlens,
+                      int n_seqs, kda_stream_t stream);
+
+/*
+ * kda_chunk_fwd_workspace_size -- bytes of device workspace kda_chunk_fwd needs
+ * for n_tokens tokens in n_seqs sequences and H heads with inputs of `dtype`.
+ * Returns 0 for invalid arguments.
+ */
+size_t kda_chunk_fwd_workspace_size(int64_t n_tokens, int n_seqs, int H, int dtype);
+
+/*
+ * kda_chunk_fwd -- prefill: the KDA forward over whole sequences, evaluated in
+ * 64-token chunks with the WY/UT chunkwise form ("Kimi K3 notes", section
+ * "Chunkwise form"; "Hybrid KDA-MLA: Kimi K3 attention explained", section
+ * "KDA kernel"), variable-length sequences included.
+ *
+ *   q, k     [NT][H][dk], dtype; q and k are expected L2-normalised per token and head
+ *   v        [NT][H][dv], dtype
+ *   dtype    KDA_BF16 (tensor-core path, fp32 accumulation and fp32 state) or
+ *            KDA_F32 (fp32 CUDA-core path)
+ *   g        [NT][H][dk] fp32 log-decays.  PRECONDITION: g_min_bound <= g <= 0 with
+ *            g_min_bound = -5 (the output range of kda_gate with g_min = -5); the
+ *            16-token tile range argument of the K3 report relies on it.  Values
+ *            outside are not checked and give unspecified (possibly non-finite) output.
+ *   beta     [NT][H], dtype, write strengths (expected in [0, 1])
+ *   h0       optional [N][H][dv][dk] fp32 initial states (NULL = zero state)
+ *   cu_seqlens optional device int32 [N+1], nondecreasing, cu[0] = 0, cu[N] = NT;
+ *            NULL means B sequences of T tokens each (N = B, NT = B*T).
+ *   n_seqs   N when cu_seqlens is given (ignored otherwise)
+ *   B, T     batch and length when cu_seqlens is NULL; with cu_seqlens, B must be 1
+ *            and T = NT
+ *   o        [NT][H][dv], dtype, written (must not alias an input)
+ *   hT       optional [N][H][dv][dk] fp32 final states (NULL to skip).  hT may alias
+ *            h0: each (sequence, head) state is read before it is written.
+ *   workspace, ws_bytes  device scratch of at least
+ *            kda_chunk_fwd_workspace_size(NT, N, H, dtype) bytes, 256-byte aligned;
+ *            its contents on entry do not matter and are garbage on return.
+ * A sequence of length 0 gets hT = h0 (or zeros).  NT == 0 writes only hT.
+ */
+kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v, int dtype,
+                           const float* g, const void* beta, const float* h0,
+                           const int32_t* cu_seqlens, int n_seqs, int B, int64_t T, int H,
+                           int dk, int dv, void* o, float* hT, void* workspace, size_t ws_bytes,
+                           kda_stream_t stream);
+
+/* Flags of kda_chunk_fwd_ex. */
+enum { KDA_CHUNK_FP32_CORES = 1u /* evaluate on fp32 CUDA cores even for bf16 inputs */ };
+
+/*
+ * kda_chunk_fwd_ex -- kda_chunk_fwd with option flags (0 = kda_chunk_fwd).
+ * KDA_CHUNK_FP32_CORES selects the fp32 CUDA-core evaluation of the same chunkwise
+ * form for bf16 inputs (the path KDA_F32 inputs always take); its workspace
+ * requirement is kda_chunk_fwd_workspace_size(NT, N, H, KDA_F32).  Unknown flag
+ * bits return KDA_ERR_INVALID_ARG.
+ */
+kda_status_t kda_chunk_fwd_ex(const void* q, const void* k, const void* v, int dtype,
+                              const float* g, const void* beta, const float* h0,
+                              const int32_t* cu_seqlens, int n_seqs, int B, int64_t T, int H,
+                              int dk, int dv, void* o, float* hT, void* workspace,
+                              size_t ws_bytes, kda_stream_t stream, unsigned flags);
+
+/*
+ * kda_recurrent_step -- decode: one token per sequence, state updated in place
+ * (the recurrent form used for cached single-token decode, "Kimi K3:
+ * architecture, training and inference systems", sections 11.2 and 13.2), taken
+ * in the delta form of section 3.1:
+ *     S <- D S + beta k (v^T - k^T D S),  D = Diag(exp(g)),   o = S^T q.
+ *
+ *   q, k     [N][H][dk], dtype;  v [N][H][dv], dtype;  beta [N][H], dtype
+ *   g        [N][H][dk] fp32, any values <= 0
+ *   S        [N][H][dv][dk] fp32, read and overwritten in place
+ *   o        [N][H][dv], dtype, written
+ */
+kda_status_t kda_recurrent_step(const void* q, const void* k, const void* v, int dtype,
+                                const float* g, const void* beta, float* S, void* o, int N, int H,
+                                int dk, int dv, kda_stream_t stream);
+
+/* Message for the last non-OK status returned on this thread (never NULL). */
+const char* kda_last_error_string(void);
+
+/* Reads and clears the device error flag set by bounded waits in the kernels.
+ * Synchronizes `stream`.  Returns KDA_OK or KDA_ERR_DEVICE_TIMEOUT. */
+kda_status_t kda_get_device_error(kda_stream_t stream);
+
+/*
+ * Per-kernel timing with CUDA events (a tracing aid; off by default).
+ * kda_profile_enable(1) clears earlier records and makes every kernel launch of
+ * the library record a start and a stop event on the stream it is launched on;
+ * kda_profile_enable(0) stops recording (and also clears).  kda_profile_collect()
+ * waits for the recorded events and aggregates them per kernel name, returning
+ * the number of distinct kernels (or -1 on a CUDA error); kda_profile_get(i, ...)
+ * returns kernel i's name (static storage), launch count and total milliseconds.
+ * Host-side state is global to the process and guarded by a mutex.
+ */
+int kda_profile_enable(int on);
+int kda_profile_collect(void);
+int kda_profile_get(int i, const char** name, int* launches, double* total_ms);
+
+/* Library version, "major.minor.patch". */
+const char* kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KDA_H_ */

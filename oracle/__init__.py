@@ -217,3 +217,23 @@ def chunked(q, k, v, g, beta, h0=None, cu_seqlens=None, C: int = 64):
                 S = gC[:, None] * S + (np.exp(G[-1][None, :] - G) * K).T @ Vt
             hT[n, h] = S.T
     return o, hT
+
+
+def chunk_cumsum(g, cu_seqlens=None, C: int = 64) -> np.ndarray:
+    """Running sum of g inside each C-token chunk of each sequence (chunks start
+    at cu[n] + C m): the log of the in-chunk cumulative decay Gamma of the
+    chunkwise form ("Kimi K3 notes", section "Chunkwise form")."""
+    g = _f64(g)
+    NT = g.shape[0]
+    if cu_seqlens is None:
+        cu = [0, NT]
+    else:
+        if hasattr(cu_seqlens, "detach"):
+            cu_seqlens = cu_seqlens.detach().cpu().numpy()
+        cu = [int(x) for x in cu_seqlens]
+    out = np.zeros_like(g)
+    for n in range(len(cu) - 1):
+        for s in range(cu[n], cu[n + 1], C):
+            e = min(s + C, cu[n + 1])
+            out[s:e] = np.cumsum(g[s:e], axis=0)
+    return out

@@ -1,0 +1,48 @@
+"""Shared helpers of the GPU parity tests: tolerances and error metrics.
+
+Tolerances (stated for the KDA forward with these input types):
+* bf16 q/k/v/beta with fp32 state: relative L2 error <= 1e-2 and max abs
+  error <= 3e-2, on o and on the final states;
+* fp32 inputs: relative L2 error <= 1e-5.
+rel_L2 = |x - ref|_2 / |ref|_2 over the whole tensor, max_abs = max |x - ref|.
+"""
+
+import numpy as np
+import torch
+
+BF16_REL_L2 = 1e-2
+BF16_MAX_ABS = 3e-2
+F32_REL_L2 = 1e-5
+
+
+def to64(x):
+    if isinstance(x, torch.Tensor):
+        return x.detach().to("cpu").double().numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def errors(got, ref):
+    got, ref = to64(got), to64(ref)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), "non-finite values in the GPU result"
+    diff = got - ref
+    nref = np.linalg.norm(ref.ravel())
+    rel = np.linalg.norm(diff.ravel()) / (nref if nref > 0 else 1.0)
+    mabs = float(np.max(np.abs(diff))) if diff.size else 0.0
+    return float(rel), mabs
+
+
+def assert_close(got, ref, dtype, what=""):
+    rel, mabs = errors(got, ref)
+    if dtype == torch.float32:
+        assert rel <= F32_REL_L2, f"{what}: rel_L2 {rel:.3e} > {F32_REL_L2}"
+    else:
+        assert rel <= BF16_REL_L2, f"{what}: rel_L2 {rel:.3e} > {BF16_REL_L2}"
+        assert mabs <= BF16_MAX_ABS, f"{what}: max_abs {mabs:.3e} > {BF16_MAX_ABS}"
+    return rel, mabs
+
+
+def cuda_ok():
+    if not torch.cuda.is_available():
+        return False
+    return torch.cuda.get_device_capability(0) == (10, 3)

@@ -307,6 +307,22 @@ def pin_decode_step_is_one_token(lib):
         assert np.allclose(o[n], on[0], atol=1e-13) and np.allclose(S1[n], hn[0], atol=1e-13)
 
 
+def pin_chunk_cumsum(lib):
+    """The in-chunk running sum: C = 1 returns g, one chunk covering a sequence
+    is a plain cumulative sum, and the chunks of a sequence add up to its total."""
+    r = _rng(25)
+    g = r.uniform(-5, 0, (70, 2, 3))
+    cu = [0, 70]
+    assert np.array_equal(oracle.chunk_cumsum(g, cu, C=1), g)
+    assert np.allclose(oracle.chunk_cumsum(g, cu, C=128), np.cumsum(g, axis=0), atol=1e-13)
+    c64 = oracle.chunk_cumsum(g, cu, C=64)
+    assert np.allclose(c64[63] + c64[69], g.sum(axis=0), atol=1e-12)
+    assert np.allclose(c64[64], g[64], atol=0)  # a new chunk starts at token 64
+    cu2 = [0, 10, 70]
+    c2 = oracle.chunk_cumsum(g, cu2, C=64)
+    assert np.allclose(c2[10], g[10], atol=0)  # a new sequence starts a new chunk
+
+
 ALL_PINS = [
     pin_gate_midpoint,
     pin_gate_A0_is_scaled_logistic,
@@ -328,4 +344,5 @@ ALL_PINS = [
     pin_non_expansive,
     pin_segment_composition,
     pin_decode_step_is_one_token,
+    pin_chunk_cumsum,
 ]

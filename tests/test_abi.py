@@ -1,0 +1,125 @@
+"""The C ABI without a GPU: the library loads, exports every declared symbol,
+and rejects bad arguments on the host before touching the device."""
+
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from chunked_gated_delta_fwd_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    path = _build.build()
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    lib.kda_chunk_fwd_workspace_size.argtypes = [i64, i32, i32, i32]
+    lib.kda_chunk_fwd_workspace_size.restype = sz
+    lib.kda_chunk_fwd_ex.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i64, i32, i32, i32,
+                                     vp, vp, vp, sz, vp, ctypes.c_uint]
+    lib.kda_chunk_fwd.argtypes = lib.kda_chunk_fwd_ex.argtypes[:-1]
+    lib.kda_gate.argtypes = [vp, i32, vp, ctypes.c_float, vp, i64, i32, i32, vp, vp, i32, vp]
+    lib.kda_recurrent_step.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, vp]
+    lib.kda_last_error_string.restype = ctypes.c_char_p
+    lib.kda_version.restype = ctypes.c_char_p
+    return lib
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_three_calls():
+    names = declared_functions()
+    for n in ("kda_gate", "kda_chunk_fwd", "kda_recurrent_step"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), f"{name} declared in kda.h but not exported"
+
+
+def test_version(L):
+    assert re.match(rb"^\d+\.\d+\.\d+$", L.kda_version())
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: every case below fails on the host
+
+
+def _chunk(L, dtype=1, dk=128, dv=128, H=2, B=1, T=64, ws=FAKE, ws_bytes=1 << 40, q=FAKE,
+           cu=None, n_seqs=0, flags=0):
+    return L.kda_chunk_fwd_ex(q, FAKE, FAKE, dtype, FAKE, FAKE, None, cu, n_seqs, B, T, H, dk, dv,
+                              FAKE, FAKE, ws, ws_bytes, None, flags)
+
+
+def test_chunk_rejects_bad_arguments(L):
+    assert _chunk(L, dk=64) == 2
+    assert _chunk(L, dv=256) == 2
+    assert _chunk(L, H=0) == 2
+    assert _chunk(L, dtype=7) == 3
+    assert _chunk(L, q=FAKE + 8) == 4
+    assert _chunk(L, ws=FAKE + 16) == 4
+    assert _chunk(L, ws_bytes=16) == 5
+    assert _chunk(L, flags=2) == 1
+    assert _chunk(L, B=2, cu=FAKE, n_seqs=2) == 1  # B must be 1 with cu_seqlens
+    assert _chunk(L, cu=FAKE, n_seqs=0) == 1
+    assert _chunk(L, q=None) == 1
+    assert b"workspace" in L.kda_last_error_string() or L.kda_last_error_string()
+
+
+def test_workspace_size(L):
+    a = L.kda_chunk_fwd_workspace_size(8192, 1, 96, 1)
+    b = L.kda_chunk_fwd_workspace_size(8192, 1, 96, 0)
+    assert a > 0 and b > 0
+    assert L.kda_chunk_fwd_workspace_size(-1, 1, 96, 1) == 0
+    assert L.kda_chunk_fwd_workspace_size(10, 0, 96, 1) == 0
+    assert L.kda_chunk_fwd_workspace_size(10, 1, 96, 5) == 0
+    # grows with tokens and heads
+    assert L.kda_chunk_fwd_workspace_size(16384, 1, 96, 1) > a
+    assert L.kda_chunk_fwd_workspace_size(8192, 1, 97, 1) > a
+
+
+def test_gate_rejects_bad_arguments(L):
+    assert L.kda_gate(FAKE, 0, FAKE, -5.0, FAKE, 10, 2, 64, None, None, 1, None) == 2
+    assert L.kda_gate(FAKE, 3, FAKE, -5.0, FAKE, 10, 2, 128, None, None, 1, None) == 3
+    assert L.kda_gate(FAKE, 0, FAKE, 1.0, FAKE, 10, 2, 128, None, None, 1, None) == 1
+    assert L.kda_gate(FAKE + 4, 0, FAKE, -5.0, FAKE, 10, 2, 128, None, None, 1, None) == 4
+    assert L.kda_gate(None, 0, FAKE, -5.0, FAKE, 10, 2, 128, None, None, 1, None) == 1
+    assert L.kda_gate(FAKE, 0, FAKE, -5.0, FAKE, 0, 2, 128, None, None, 1, None) == 0  # no-op
+
+
+def test_recurrent_step_rejects_bad_arguments(L):
+    args = [FAKE, FAKE, FAKE, 1, FAKE, FAKE, FAKE, FAKE, 4, 2, 128, 128, None]
+    bad = list(args); bad[10] = 64
+    assert L.kda_recurrent_step(*bad) == 2
+    bad = list(args); bad[3] = 9
+    assert L.kda_recurrent_step(*bad) == 3
+    bad = list(args); bad[6] = FAKE + 4
+    assert L.kda_recurrent_step(*bad) == 4
+    bad = list(args); bad[0] = None
+    assert L.kda_recurrent_step(*bad) == 1
+    bad = list(args); bad[8] = 0
+    assert L.kda_recurrent_step(*bad) == 0  # N = 0 is a no-op
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")
+def test_valid_call_without_gpu_fails_cleanly(L):
+    st = _chunk(L)
+    assert st in (6, 8), st
+
+
+def test_python_binding_imports_and_refuses_cpu_tensors():
+    import chunked_gated_delta_fwd_gb300 as kda
+
+    z = torch.zeros(4, 2, 128)
+    with pytest.raises(ValueError):
+        kda.gate(z, torch.zeros(2))

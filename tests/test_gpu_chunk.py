@@ -1,0 +1,198 @@
+"""GPU parity of the chunked prefill (kda_chunk_fwd) against the fp64 oracle.
+
+Small cases cover ragged tails (T = 1 .. 200 around the 16-token tile and the
+64-token chunk), variable-length packing with empty sequences, initial states,
+near-bound decays and both evaluation paths for bf16 inputs (tensor cores and
+fp32 CUDA cores).  Full-size workloads are checked on sampled heads or
+sequences, or on the prefix the oracle can afford.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests.gpu_helpers import assert_close, errors, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kda():
+    import chunked_gated_delta_fwd_gb300 as m
+
+    return m
+
+
+def _inputs(lens, H, dtype, seed, h0=True, g_lo=-5.0, g_hi=0.0, device="cuda"):
+    w = workloads.custom(lens, H=H, dtype=dtype, seed=seed, h0_std=0.5 if h0 else None)
+    inp = workloads.make_inputs(w, "cpu")
+    NT = w.n_tokens
+    g = workloads.uniform_decay((NT, H, 128), "cpu", seed=seed + 1, lo=g_lo, hi=g_hi)
+    dev = {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    dev["g"] = g.to(device)
+    return inp, g, dev
+
+
+def _run(kda, dev, flags=0, varlen=True):
+    return kda.chunk_fwd(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["h0"],
+                         dev["cu_seqlens"] if varlen else None, flags=flags)
+
+
+PATHS = [(torch.float32, 0), (torch.bfloat16, 0), (torch.bfloat16, 1)]
+PATH_IDS = ["f32", "bf16-tc", "bf16-f32cores"]
+
+
+@pytest.mark.parametrize("T", [1, 15, 16, 17, 63, 64, 65, 127, 200])
+@pytest.mark.parametrize("dtype,flags", PATHS, ids=PATH_IDS)
+def test_single_sequence_ragged(kda, T, dtype, flags):
+    inp, g, dev = _inputs([T], H=2, dtype=dtype, seed=100 + T)
+    o, hT = _run(kda, dev, flags)
+    o_ref, h_ref = oracle.recurrence(inp["q"], inp["k"], inp["v"], g, inp["beta"], inp["h0"],
+                                     inp["cu_seqlens"])
+    assert_close(o, o_ref, dtype, f"o T={T}")
+    assert_close(hT, h_ref, dtype, f"hT T={T}")
+
+
+@pytest.mark.parametrize("dtype,flags", PATHS, ids=PATH_IDS)
+def test_varlen_with_empty_sequences(kda, dtype, flags):
+    lens = [5, 0, 70, 64, 129, 1, 0, 300]
+    inp, g, dev = _inputs(lens, H=3, dtype=dtype, seed=7)
+    o, hT = _run(kda, dev, flags)
+    o_ref, h_ref = oracle.recurrence(inp["q"], inp["k"], inp["v"], g, inp["beta"], inp["h0"],
+                                     inp["cu_seqlens"])
+    assert_close(o, o_ref, dtype, "o varlen")
+    assert_close(hT, h_ref, dtype, "hT varlen")
+
+
+@pytest.mark.parametrize("dtype,flags", PATHS, ids=PATH_IDS)
+def test_batched_without_cu_seqlens(kda, dtype, flags):
+    B, T, H = 3, 130, 2
+    inp, g, dev = _inputs([T] * B, H=H, dtype=dtype, seed=9)
+    shp = lambda t: t.view(B, T, *t.shape[1:])
+    o, hT = kda.chunk_fwd(shp(dev["q"]), shp(dev["k"]), shp(dev["v"]), shp(dev["g"]),
+                          shp(dev["beta"]), dev["h0"], None, flags=flags)
+    o_ref, h_ref = oracle.recurrence(inp["q"], inp["k"], inp["v"], g, inp["beta"], inp["h0"],
+                                     inp["cu_seqlens"])
+    assert_close(o.view(B * T, H, 128), o_ref, dtype, "o batched")
+    assert_close(hT, h_ref, dtype, "hT batched")
+
+
+@pytest.mark.parametrize("dtype,flags", PATHS, ids=PATH_IDS)
+def test_near_bound_decay_and_zero_state(kda, dtype, flags):
+    """All decays in [-5, -4.5]: every 16-token tile sits near the e^80 edge."""
+    inp, g, dev = _inputs([256, 77], H=2, dtype=dtype, seed=11, h0=False, g_lo=-5.0, g_hi=-4.5)
+    o, hT = _run(kda, dev, flags)
+    o_ref, h_ref = oracle.recurrence(inp["q"], inp["k"], inp["v"], g, inp["beta"], None,
+                                     inp["cu_seqlens"])
+    assert_close(o, o_ref, dtype, "o near-bound")
+    assert_close(hT, h_ref, dtype, "hT near-bound")
+
+
+@pytest.mark.parametrize("dtype,flags", PATHS, ids=PATH_IDS)
+def test_no_decay_slow_forgetting(kda, dtype, flags):
+    """g in [-0.01, 0]: almost no forgetting, the state accumulates over 4 chunks."""
+    inp, g, dev = _inputs([256], H=2, dtype=dtype, seed=12, g_lo=-0.01, g_hi=0.0)
+    o, hT = _run(kda, dev, flags)
+    o_ref, h_ref = oracle.recurrence(inp["q"], inp["k"], inp["v"], g, inp["beta"], inp["h0"],
+                                     inp["cu_seqlens"])
+    assert_close(o, o_ref, dtype, "o slow decay")
+    assert_close(hT, h_ref, dtype, "hT slow decay")
+
+
+def test_final_state_may_alias_initial_state(kda):
+    inp, g, dev = _inputs([100, 40], H=2, dtype=torch.bfloat16, seed=13)
+    h = dev["h0"].clone()
+    kda.chunk_fwd(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], h, dev["cu_seqlens"],
+                  final_state_out=h)
+    _, h_ref = oracle.recurrence(inp["q"], inp["k"], inp["v"], g, inp["beta"], inp["h0"],
+                                 inp["cu_seqlens"])
+    assert_close(h, h_ref, torch.bfloat16, "aliased hT")
+
+
+def test_all_sequences_empty_returns_initial_state(kda):
+    H = 2
+    h0 = torch.randn(3, H, 128, 128, device="cuda")
+    z = torch.zeros(0, H, 128, device="cuda", dtype=torch.bfloat16)
+    cu = torch.zeros(4, dtype=torch.int32, device="cuda")
+    _, hT = kda.chunk_fwd(z, z, z, torch.zeros(0, H, 128, device="cuda"),
+                          torch.zeros(0, H, device="cuda", dtype=torch.bfloat16), h0, cu)
+    assert torch.equal(hT, h0)
+
+
+def test_bad_cu_seqlens_is_reported_not_faulted(kda):
+    inp, g, dev = _inputs([64, 64], H=1, dtype=torch.bfloat16, seed=14)
+    bad = torch.tensor([0, 100, 50], dtype=torch.int32, device="cuda")  # decreasing
+    kda.chunk_fwd(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], None, bad)
+    with pytest.raises(kda.KdaError) as ei:
+        kda.get_device_error()
+    assert ei.value.status == 1
+    kda.get_device_error()  # cleared
+
+
+def test_tiny_fp32_workload_end_to_end(kda):
+    """B=1, H=2, T=256, fp32 inputs, A=0, zero state: gate + chunked prefill on the
+    GPU against the oracle's gate + recurrence, relative L2 <= 1e-5."""
+    w = workloads.tiny()
+    inp = workloads.make_inputs(w, "cpu")
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    g = kda.gate(dev["z"], dev["A"])
+    o, hT = kda.chunk_fwd(dev["q"], dev["k"], dev["v"], g, dev["beta"], None, dev["cu_seqlens"])
+    g_ref = oracle.gate(inp["z"], inp["A"])
+    o_ref, h_ref = oracle.recurrence(inp["q"], inp["k"], inp["v"], g_ref, inp["beta"], None,
+                                     inp["cu_seqlens"])
+    assert_close(o, o_ref, torch.float32, "o tiny")
+    assert_close(hT, h_ref, torch.float32, "hT tiny")
+
+
+def _full_size(kda, w, sample_pairs, seed):
+    """Runs gate + chunk on a full-size workload (inputs generated on the GPU) and
+    checks sampled (sequence, head) pairs against the oracle."""
+    dev = workloads.make_inputs(w, "cuda")
+    g = kda.gate(dev["z"], dev["A"])
+    o, hT = kda.chunk_fwd(dev["q"], dev["k"], dev["v"], g, dev["beta"], dev["h0"],
+                          dev["cu_seqlens"])
+    torch.cuda.synchronize()
+    cu = dev["cu_seqlens"].cpu().numpy().astype(np.int64)
+    r = np.random.default_rng(seed)
+    pairs = sorted({(int(r.integers(w.n_seqs)), int(r.integers(w.H))) for _ in range(sample_pairs)})
+    for n, h in pairs:
+        a, b = int(cu[n]), int(cu[n + 1])
+        sl = lambda t: t[a:b, h:h + 1]
+        g_ref = oracle.gate(sl(dev["z"]), dev["A"][h:h + 1])
+        h0 = None if dev["h0"] is None else dev["h0"][n:n + 1, h:h + 1]
+        o_ref, h_ref = oracle.recurrence(sl(dev["q"]), sl(dev["k"]), sl(dev["v"]), g_ref,
+                                         sl(dev["beta"]), h0)
+        assert_close(sl(o), o_ref, w.dtype, f"o seq {n} head {h}")
+        assert_close(hT[n:n + 1, h:h + 1], h_ref, w.dtype, f"hT seq {n} head {h}")
+
+
+def test_prefill_full_size_sampled(kda):
+    """B=1, T=8192, H=96, bf16, random h0: 12 sampled heads against the oracle."""
+    _full_size(kda, workloads.prefill(), 12, seed=2)
+
+
+def test_varlen_full_size_sampled(kda):
+    """32 packed sequences (~270K tokens), H=96: 6 sampled (sequence, head) pairs."""
+    _full_size(kda, workloads.varlen(), 6, seed=3)
+
+
+def test_long_context_prefix(kda):
+    """T=1,048,576, H=16 workload: the 4096-token prefix against the oracle, and the
+    first 4096 outputs of a 16384-token run equal the prefix run (causality)."""
+    w = workloads.long_context(T=16384)
+    dev = workloads.make_inputs(w, "cuda")
+    g = kda.gate(dev["z"], dev["A"])
+    P = 4096
+    cuP = torch.tensor([0, P], dtype=torch.int32, device="cuda")
+    oP, hP = kda.chunk_fwd(dev["q"][:P], dev["k"][:P], dev["v"][:P], g[:P], dev["beta"][:P], None,
+                           cuP)
+    g_ref = oracle.gate(dev["z"][:P], dev["A"])
+    o_ref, h_ref = oracle.recurrence(dev["q"][:P], dev["k"][:P], dev["v"][:P], g_ref,
+                                     dev["beta"][:P], None)
+    assert_close(oP, o_ref, torch.bfloat16, "o prefix")
+    assert_close(hP, h_ref, torch.bfloat16, "hT prefix")
+    o_full, _ = kda.chunk_fwd(dev["q"], dev["k"], dev["v"], g, dev["beta"], None,
+                              dev["cu_seqlens"])
+    assert torch.equal(o_full[:P], oP)

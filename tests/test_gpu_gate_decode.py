@@ -1,0 +1,93 @@
+"""GPU parity of the gate (K1) and the decode step (K5) against the fp64 oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests.gpu_helpers import assert_close, errors, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kda():
+    import chunked_gated_delta_fwd_gb300 as m
+
+    return m
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_gate_matches_oracle(kda, dtype):
+    w = workloads.custom([300], H=3, dtype=dtype, z_std=3.0, A_range=1.0, seed=41)
+    inp = workloads.make_inputs(w, "cpu")
+    g = kda.gate(inp["z"].cuda(), inp["A"].cuda())
+    ref = oracle.gate(inp["z"], inp["A"])
+    _, mabs = errors(g, ref)
+    assert mabs <= 2e-6, mabs
+    assert float(g.max()) <= 0.0 and float(g.min()) >= -5.0
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_gate_chunk_cumsum_matches_oracle(kda, dtype):
+    lens = [100, 0, 200, 1, 64, 65]
+    w = workloads.custom(lens, H=2, dtype=dtype, seed=42)
+    inp = workloads.make_inputs(w, "cpu")
+    cu = inp["cu_seqlens"]
+    g, gc = kda.gate(inp["z"].cuda(), inp["A"].cuda(), with_cumsum=True, cu_seqlens=cu.cuda())
+    g_ref = oracle.gate(inp["z"], inp["A"])
+    assert errors(g, g_ref)[1] <= 2e-6
+    assert errors(gc, oracle.chunk_cumsum(g_ref, cu))[1] <= 1e-4
+    # without cu_seqlens: one sequence
+    g1, gc1 = kda.gate(inp["z"].cuda(), inp["A"].cuda(), with_cumsum=True)
+    assert errors(gc1, oracle.chunk_cumsum(g_ref, None))[1] <= 1e-4
+
+
+def _decode_case(kda, N, H, dtype, steps, seed, sample=None):
+    """Runs `steps` decode steps on the GPU from a seeded state; the oracle follows
+    the sampled (n, h) states.  Gate on both sides (GPU gate vs oracle gate)."""
+    w = workloads.DecodeWorkload("t", N=N, H=H, dtype=dtype, steps=steps, seed=seed)
+    S = workloads.make_decode_state(w, "cuda")
+    if sample is None:
+        sel = [(n, h) for n in range(N) for h in range(H)]
+    else:
+        r = np.random.default_rng(seed)
+        sel = sorted({(int(r.integers(N)), int(r.integers(H))) for _ in range(sample)})
+    ns = torch.tensor([s[0] for s in sel])
+    hs = torch.tensor([s[1] for s in sel])
+    S_ref = to64(S[ns, hs])[:, None]  # [m, 1, dv, dk]
+    worst = (0.0, 0.0)
+    for step in range(steps):
+        inp = workloads.make_decode_step(w, step, "cuda")
+        g = kda.gate(inp["z"], inp["A"])
+        o = kda.recurrent_step(inp["q"], inp["k"], inp["v"], g, inp["beta"], S)
+        pick = lambda t: t[ns, hs].unsqueeze(1)
+        z_sel = to64(pick(inp["z"]))  # [m, 1, dk]
+        A_sel = to64(inp["A"][hs])  # per sample
+        g_ref = np.stack([oracle.gate(z_sel[i:i + 1], A_sel[i:i + 1]) for i in range(len(sel))])[:, 0]
+        o_ref, S_ref = oracle.decode_step(pick(inp["q"]), pick(inp["k"]), pick(inp["v"]), g_ref,
+                                          pick(inp["beta"]), S_ref)
+        rel, mabs = assert_close(o[ns, hs].unsqueeze(1), o_ref, dtype, f"o step {step}")
+        worst = (max(worst[0], rel), max(worst[1], mabs))
+    assert_close(S[ns, hs].unsqueeze(1), S_ref, dtype, "final state")
+    return worst
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_decode_small(kda, dtype):
+    _decode_case(kda, N=5, H=3, dtype=dtype, steps=4, seed=51)
+
+
+def test_decode_full_size_sampled(kda):
+    """512 sequences x 96 heads, fp32 state (3.2 GB), 100 in-place steps; the
+    oracle follows 48 sampled (sequence, head) states through all steps."""
+    _decode_case(kda, N=512, H=96, dtype=torch.bfloat16, steps=100, seed=1005, sample=48)
+
+
+def test_decode_zero_sequences_is_noop(kda):
+    S = torch.zeros(0, 2, 128, 128, device="cuda")
+    q = torch.zeros(0, 2, 128, device="cuda", dtype=torch.bfloat16)
+    o = kda.recurrent_step(q, q, q, torch.zeros(0, 2, 128, device="cuda"),
+                           torch.zeros(0, 2, device="cuda", dtype=torch.bfloat16), S)
+    assert o.shape == (0, 2, 128)
