@@ -227,7 +227,7 @@ def run_reference(args):
     return 0
 
 
-def cpu_baseline(heads=16, T=8192, seed=1002):
+def cpu_baseline(heads=96, T=8192, seed=1002):
     """fp64 oracle over a bounded sample (heads x T tokens), scaled to H=96."""
     import torch
 

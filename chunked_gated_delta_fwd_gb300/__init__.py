@@ -5,7 +5,7 @@ dtypes, devices and contiguity, passes ``data_ptr()`` values and the current
 CUDA stream, and raises :class:`KdaError` on a non-OK status.  Every step of
 the computation runs in the library's CUDA kernels; there is no CPU or
 PyTorch fallback, and importing this package fails if ``libkda.so`` has not
-been built (``python -m chunked_gated_delta_fwd_gb300._build``).
+been built (``python chunked_gated_delta_fwd_gb300/_build.py``).
 
 Entry points (same names as the C calls, without the ``kda_`` prefix):
 
@@ -53,7 +53,7 @@ def _load() -> ctypes.CDLL:
     path = library_path()
     if not os.path.exists(path):
         raise ImportError(f"libkda.so not found at {path}; build it with "
-                          f"`python -m chunked_gated_delta_fwd_gb300._build`")
+                          f"`python chunked_gated_delta_fwd_gb300/_build.py`")
     L = ctypes.CDLL(path)
     vp, i32, i64, f32, sz, u32 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
                                   ctypes.c_size_t, ctypes.c_uint)

@@ -8,7 +8,7 @@ import re
 import pytest
 import torch
 
-from chunked_gated_delta_fwd_gb300 import _build
+import __graft_entry__
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "kda.h")
@@ -16,7 +16,7 @@ HEADER = os.path.join(ROOT, "include", "kda.h")
 
 @pytest.fixture(scope="module")
 def L():
-    path = _build.build()
+    path = __graft_entry__._build_module().build()
     lib = ctypes.CDLL(path)
     vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
     lib.kda_chunk_fwd_workspace_size.argtypes = [i64, i32, i32, i32]
