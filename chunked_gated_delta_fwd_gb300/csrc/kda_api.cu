@@ -203,6 +203,12 @@ kda_status_t check_device() {
 
 }  // namespace
 
+namespace kda {
+// Lets other translation units of the library set the message that
+// kda_last_error_string() returns on this thread.
+void set_error_message(const char* msg) { fail(KDA_OK, "%s", msg); }
+}  // namespace kda
+
 extern "C" {
 
 const char* kda_version(void) { return "0.1.0"; }

@@ -138,6 +138,34 @@ kda_status_t kda_chunk_fwd_ex(const void* q, const void* k, const void* v, int d
                               size_t ws_bytes, kda_stream_t stream, unsigned flags);
 
 /*
+ * kda_chunk_fwd_noalloc -- kda_chunk_fwd without a caller-supplied workspace.
+ * The KDA pages have no counterpart for this entry point: it exists for callers
+ * that must not allocate device memory where they run the prefill (a serving
+ * engine that reserved all device memory up front, a plugin host that offers no
+ * allocator, a latency-critical loop that cannot pay an allocation's implicit
+ * synchronization).  Arguments, layouts and results are those of kda_chunk_fwd.
+ *
+ * The scratch comes from one fixed array of KDA_NOALLOC_SCRATCH_BYTES in device
+ * memory, declared by the library; every GPU that loads the library holds it
+ * until the process exits.  The call allocates nothing.  A problem whose
+ * workspace (kda_chunk_fwd_workspace_size) exceeds the capacity is rejected with
+ * KDA_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.  The first call on a
+ * device resolves the array's device address (cudaGetSymbolAddress, with that
+ * device current); make that first call before any stream capture.  All calls
+ * share the array and it keeps the last call's contents (nothing in it needs to
+ * start at zero); calls whose work overlaps on the GPU, e.g. on two streams
+ * without ordering between them, race on it.
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES ((size_t)128 << 20) /* 128 MiB */
+kda_status_t kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v, int dtype,
+                                   const float* g, const void* beta, const float* h0,
+                                   const int32_t* cu_seqlens, int n_seqs, int B, int64_t T,
+                                   int H, int dk, int dv, void* o, float* hT,
+                                   kda_stream_t stream);
+/* Capacity in bytes of the array behind kda_chunk_fwd_noalloc. */
+size_t kda_chunk_fwd_noalloc_capacity(void);
+
+/*
  * kda_recurrent_step -- decode: one token per sequence, state updated in place
  * (the recurrent form used for cached single-token decode, "Kimi K3:
  * architecture, training and inference systems", sections 11.2 and 13.2), taken
