@@ -38,6 +38,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 D = 128
+TC_UNIT_BYTES = 73728  # bf16 tiles the tensor-core prep kernel writes per (chunk, head)
 METRIC = "KDA prefill tokens/s (H=96,d=128) and % roofline; decode-step HBM GB/s"
 
 
@@ -322,10 +323,15 @@ def run_gpu(args):
     dom_name, (dom_n, dom_ms) = max(per_kernel.items(), key=lambda kv: kv[1][1])
     dom_avg_ms = dom_ms / dom_n
     tok_heads = NT * H
+    units = (NT // 64) * H  # (chunk, head) units of this single-sequence workload
     kernel_bytes = {
         "kda_gate": tok_heads * gate_bytes_per_token_head(2),
-        "kda_simt_prep": tok_heads * (prefill_bytes_per_token_head(2) - D * 2),
-        "kda_simt_chain": tok_heads * D * 2 + 2 * H * state_bytes(),
+        # inputs q, k, v, g, beta in; MMA-ready tiles (72 KiB) + gamma (512 B) out per unit
+        "kda_tc_prep": tok_heads * (prefill_bytes_per_token_head(2) - D * 2)
+        + units * (TC_UNIT_BYTES + D * 4),
+        # tiles + gamma in, o out, h0 in and hT out per (sequence, head)
+        "kda_tc_chain": units * (TC_UNIT_BYTES + D * 4) + tok_heads * D * 2
+        + 2 * H * state_bytes(),
     }
     alg_bytes = kernel_bytes.get(dom_name)
     achieved = alg_bytes / (dom_avg_ms * 1e-3) / 1e9 if alg_bytes else None

@@ -19,18 +19,21 @@
 // is k_r * exp(G_r - R_a) <= 1 (resp. q_r * exp(G_r - R_a)); their product over
 // the channels is sum_c k_rc k_ic exp(G_rc - G_ic).
 //
-// Kernel 1, tc_prep: one persistent CTA per SM walks (chunk, head) units and
-// writes, per unit, MMA-ready bf16 tiles to the workspace:
-//   WQ [128 rows][128]: rows 0..63 = W, rows 64..127 = Gamma*Q   (B of MMA1)
-//   UT [128 rows][64] : U^T (dv rows, token columns)             (read by threads)
-//   AK [192 rows][64] : rows 0..63 = A_qk, rows 64..191 = Kt^T   (B of MMA2)
-// and gamma_C (fp32 [128]) separately.
+// Kernel 1, tc_prep: one persistent CTA per SM walks (chunk, head) units.  A copy
+// warp prefetches the next unit's k, q, v, g rows into shared memory with 1-D
+// bulk copies while eight compute warps (thread = channel x row half) build the
+// operands, run the MMAs, invert I + A_kk blockwise in fp32 and write, per unit,
+// MMA-ready bf16 tiles to the workspace:
+//   WQ: MN-major, 128 token rows x 128 channels (W rows 0..63, Gamma*Q rows 64..127)
+//   UT: K-major, U^T (128 value rows x 64 tokens)
+//   AQ: MN-major, A_qk (64 x 64);  KT: K-major, Kt^T (128 channel rows x 64 tokens)
+// plus gamma_C (fp32 [128]).
 // Kernel 2, tc_chain: one CTA per (sequence, head) walks its chunks in order.
-// TMEM holds S^T (lanes = dv, columns = dk) and two buffers for
+// TMEM holds S^T (lanes = dv, columns = dk) and two D1 buffers:
 //   MMA1: D1 = S^T [W; Gamma*Q]^T        -> (W S)^T | (Gamma*Q S)^T
 //   MMA2: D1[:,64:] += Vt^T A_qk^T ;  S^T += Vt^T Kt  (after S^T *= gamma_C)
-// where Vt^T = U^T - (W S)^T is formed by the epilogue warps.  Tiles stream in
-// with 1-D bulk async copies through a two-stage ring.
+// where Vt^T = U^T - (W S)^T is formed by eight epilogue warps.  Tiles stream
+// in with bulk async copies through a two-stage ring.
 #include "kda_internal.cuh"
 #include "kda_sm100.cuh"
 
@@ -43,29 +46,63 @@ constexpr int C = kChunk;  // 64
 constexpr int D = kD;      // 128
 
 // ---- workspace unit (bytes)
-constexpr uint32_t kWQ = 0;                   // 128 rows x 128 cols bf16, SW128 K-major
-constexpr uint32_t kUT = 32768;               // 128 rows x 64 cols
-constexpr uint32_t kAK = 49152;               // 192 rows x 64 cols
+constexpr uint32_t kWQ = 0;        // MN-major X=128 (tokens), K=128: 32 KB
+constexpr uint32_t kUT = 32768;    // K-major 128 rows x 64: 16 KB
+constexpr uint32_t kAQ = 49152;    // MN-major X=64 (rows r), K=64 (columns i): 8 KB
+constexpr uint32_t kKT = 57344;    // K-major 128 rows x 64: 16 KB
 constexpr uint32_t kUnitBytes = 73728;
 constexpr uint32_t kGamBytes = D * 4;
 
 // ============================================================== prep kernel
-constexpr int kPrepThreads = 128;
+constexpr int kPrepCompute = 256;                // (channel, row half)
+constexpr int kPrepThreads = kPrepCompute + 32;  // + the copy warp
+constexpr uint32_t kInRowBytes = 3 * 256 + 512;  // k, q, v (bf16) and g (fp32) per token
 // shared memory (offsets from a 1024-aligned base)
-constexpr uint32_t kP_Bop = 0;         // [Kb t0; Qb t0; Kb t1; Qb t1; ...] 128 rows x 128 (32 KB)
-constexpr uint32_t kP_T = 0;           //   reused: T (64 x 64 bf16, 8 KB) after the products
-constexpr uint32_t kP_L = 8192;        //   reused: L (64 x 65 fp32) after the products
-constexpr uint32_t kP_KC01 = 32768;    // [KC(0); KC(1)] 128 rows x 128 (32 KB)
-constexpr uint32_t kP_KC23 = 65536;    // [KC(2); KC(3)]
-constexpr uint32_t kP_BKg = 98304;     // (beta Gamma K)^T 128 rows x 64 (16 KB)
-constexpr uint32_t kP_BV = 114688;     // (beta V)^T 128 rows x 64
-constexpr uint32_t kP_beta = 131072;   // 64 fp32
-constexpr uint32_t kP_bars = 131328;   // 2 mbarriers + TMEM base
-constexpr uint32_t kP_Smem = kP_bars + 64 + 1024;  // + alignment slack
+constexpr uint32_t kI_K = 0, kI_Q = 16384, kI_V = 32768, kI_G = 49152;  // staged rows
+constexpr uint32_t kP_Bop = 81920;           // MN-major X=128 (Kb/Qb rows), K=128
+constexpr uint32_t kP_L = kP_Bop;            //   reused after the products: fp32 [64][65]
+constexpr uint32_t kP_P = kP_Bop + 16640;    //   fp32 scratch, 3 x 16 x 16
+constexpr uint32_t kP_T = kP_Bop + 20480;    //   bf16 T, MN-major X=64, K=64
+constexpr uint32_t kP_KC01 = 114688;         // MN-major X=128 ([KC(0) | KC(1)] rows), K=128
+constexpr uint32_t kP_KC23 = 147456;         // [KC(2) | KC(3)]
+constexpr uint32_t kP_BKg = 180224;          // K-major (beta Gamma K)^T 128 x 64
+constexpr uint32_t kP_BV = 196608;           // K-major (beta V)^T 128 x 64
+constexpr uint32_t kP_beta = 212992;         // 64 fp32
+constexpr uint32_t kP_R = kP_beta + 256;     // R_0..R_3, [4][128] fp32
+constexpr uint32_t kP_GC = kP_R + 2048;      // G at the chunk end, [128] fp32
+constexpr uint32_t kP_bars = kP_GC + 512;    // in_full, in_empty, p, w + TMEM base
+constexpr uint32_t kP_Smem = kP_bars + 64 + 1024;
 constexpr int kLdL = 65;
 
-__device__ __forceinline__ void st_bf16(uint8_t* base, uint32_t off, float x) {
-  *reinterpret_cast<__nv_bfloat16*>(base + off) = __float2bfloat16_rn(x);
+__device__ __forceinline__ uint4 pack8(const float* x) {
+  return make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
+                    pack_bf16(x[6], x[7]));
+}
+
+struct UnitInfo {
+  int chunk, h;
+  int64_t t0;
+  int len;
+};
+
+__device__ __forceinline__ UnitInfo unit_info(const Plan& plan, int H, int64_t u) {
+  UnitInfo ui;
+  ui.chunk = (int)(u / H);
+  ui.h = (int)(u % H);
+  int lo = 0, hi = plan.n_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(plan.chunk_off + mid) <= ui.chunk) lo = mid; else hi = mid - 1;
+  }
+  ui.t0 = (int64_t)__ldg(plan.cu + lo) + (int64_t)(ui.chunk - __ldg(plan.chunk_off + lo)) * C;
+  ui.len = (int)min((int64_t)C, (int64_t)__ldg(plan.cu + lo + 1) - ui.t0);
+  return ui;
+}
+
+// T (lower unit-triangular) is kept transposed in the upper part of Lbuf:
+// T[r][c] for r > c at Lbuf[c][r]; L (strictly lower) at Lbuf[r][c].
+__device__ __forceinline__ float t_at(const float* Lb, int r, int c) {
+  return r == c ? 1.f : (r < c ? 0.f : Lb[c * kLdL + r]);
 }
 
 __global__ void __launch_bounds__(kPrepThreads, 1)
@@ -77,16 +114,22 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
   uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_addr(sm);
   float* beta_s = reinterpret_cast<float*>(sm + kP_beta);
-  float* Ls = reinterpret_cast<float*>(sm + kP_L);
+  float* Rs = reinterpret_cast<float*>(sm + kP_R);
+  float* GCs = reinterpret_cast<float*>(sm + kP_GC);
+  float* Lb = reinterpret_cast<float*>(sm + kP_L);
+  float* Ps = reinterpret_cast<float*>(sm + kP_P);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kP_bars);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kP_bars + 16);
-  const uint32_t bar_p = smem_addr(&bars[0]), bar_w = smem_addr(&bars[1]);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kP_bars + 32);
+  const uint32_t bar_full = smem_addr(&bars[0]), bar_empty = smem_addr(&bars[1]);
+  const uint32_t bar_p = smem_addr(&bars[2]), bar_w = smem_addr(&bars[3]);
   const int t = threadIdx.x, warp = t >> 5;
 
   // the KC tiles keep zero rows beyond their tile for the whole kernel
   for (uint32_t o = t * 16; o < 65536; o += kPrepThreads * 16)
     *reinterpret_cast<uint4*>(sm + kP_KC01 + o) = make_uint4(0, 0, 0, 0);
   if (t == 0) {
+    mbar_init(bar_full, 1);
+    mbar_init(bar_empty, kPrepCompute);
     mbar_init(bar_p, 1);
     mbar_init(bar_w, 1);
     mbar_fence_init();
@@ -96,201 +139,262 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
   const int total = __ldg(plan.chunk_off + plan.n_seqs);
-  uint32_t iter = 0;
 
-  for (int64_t u = blockIdx.x; u < units_ub; u += gridDim.x) {
-    const int chunk = (int)(u / H), h = (int)(u % H);
-    if (chunk >= total) break;  // units are chunk-major: the rest are past the end
-    int n = 0;
-    {
-      int lo = 0, hi = plan.n_seqs - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (__ldg(plan.chunk_off + mid) <= chunk) lo = mid; else hi = mid - 1;
-      }
-      n = lo;
-    }
-    const int64_t t0 = (int64_t)__ldg(plan.cu + n) + (int64_t)(chunk - __ldg(plan.chunk_off + n)) * C;
-    const int len = (int)min((int64_t)C, (int64_t)__ldg(plan.cu + n + 1) - t0);
-    uint8_t* unit = tiles + (size_t)u * kUnitBytes;
-    const int c = t;  // channel owned by this thread in the elementwise passes
-
-    // ---- pass 1: running log-decay of channel c, tile references
-    float G[C];
-    {
-      float acc = 0.f;
-#pragma unroll
-      for (int r = 0; r < C; ++r) {
-        const float gv = (r < len) ? __ldg(g + ((t0 + r) * H + h) * D + c) : 0.f;
-        acc += gv;
-        G[r] = acc;
-      }
-    }
-    if (t < C) beta_s[t] = (t < len) ? __bfloat162float(beta[(t0 + t) * H + h]) : 0.f;
-    const float R[4] = {0.f, G[15], G[31], G[47]};
-    const float GC = G[63];
-    __syncthreads();
-
-    // ---- pass 2: operands
-#pragma unroll
-    for (int a = 0; a < 4; ++a) {
-      float E[4];  // exp(R_a' - R_a) for a' >= a
-#pragma unroll
-      for (int ap = 0; ap < 4; ++ap) E[ap] = (ap > a) ? __expf(R[ap] - R[a]) : 1.f;
-      const float eRa = __expf(R[a]);           // exp(R_a) <= 1
-      const float eCa = __expf(GC - R[a]);      // exp(G_C - R_a) <= 1
-      float kr[16], qr[16], vr[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int r = a * 16 + j;
-        const int64_t off = ((t0 + r) * H + h) * D + c;
-        const bool in = r < len;
-        kr[j] = in ? __bfloat162float(k[off]) : 0.f;
-        qr[j] = in ? __bfloat162float(q[off]) : 0.f;
-        vr[j] = in ? __bfloat162float(v[off]) : 0.f;
-      }
-      uint32_t pk_kg[8], pk_v[8], pk_kt[8];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int r = a * 16 + j;
-        const float d = G[r] - R[a];  // (-80, 0]
-        const float f = __expf(d), fi = __expf(-d);
-        const float kb = kr[j] * f, qb = qr[j] * f, kn = kr[j] * fi;
-        st_bf16(sm, kP_Bop + sw128_offset(128, 32 * a + j, c), kb);
-        st_bf16(sm, kP_Bop + sw128_offset(128, 32 * a + 16 + j, c), qb);
-#pragma unroll
-        for (int ap = a; ap < 4; ++ap)
-          st_bf16(sm, (ap < 2 ? kP_KC01 : kP_KC23) + sw128_offset(128, 64 * (ap & 1) + r, c),
-                  kn * E[ap]);
-        const float kg = kb * eRa * beta_s[r];
-        const float vb = vr[j] * beta_s[r];
-        const float kt = kn * eCa;
-        if (j & 1) {
-          pk_kg[j >> 1] = pack_bf16(__uint_as_float(pk_kg[j >> 1]), kg);
-          pk_v[j >> 1] = pack_bf16(__uint_as_float(pk_v[j >> 1]), vb);
-          pk_kt[j >> 1] = pack_bf16(__uint_as_float(pk_kt[j >> 1]), kt);
-        } else {
-          pk_kg[j >> 1] = __float_as_uint(kg);
-          pk_v[j >> 1] = __float_as_uint(vb);
-          pk_kt[j >> 1] = __float_as_uint(kt);
+  if (warp == kPrepCompute / 32) {
+    // ------------------------------------------------------------ copy warp
+    if ((t & 31) == 0) {
+      uint32_t it = 0;
+      for (int64_t u = blockIdx.x; u < units_ub; u += gridDim.x, ++it) {
+        const UnitInfo ui = unit_info(plan, H, u);
+        if (ui.chunk >= total) break;
+        if (it > 0 && !mbar_wait(bar_empty, (it - 1) & 1, err)) break;
+        mbar_arrive_expect_tx(bar_full, (uint32_t)ui.len * kInRowBytes);
+        for (int r = 0; r < ui.len; ++r) {
+          const int64_t row = (ui.t0 + r) * H + ui.h;
+          bulk_g2s(sbase + kI_K + r * 256, k + row * D, 256, bar_full);
+          bulk_g2s(sbase + kI_Q + r * 256, q + row * D, 256, bar_full);
+          bulk_g2s(sbase + kI_V + r * 256, v + row * D, 256, bar_full);
+          bulk_g2s(sbase + kI_G + r * 512, g + row * D, 512, bar_full);
         }
-        // Gamma*Q -> WQ rows 64.., column c
-        *reinterpret_cast<__nv_bfloat16*>(unit + kWQ + sw128_offset(128, 64 + r, c)) =
-            __float2bfloat16_rn(qb * eRa);
       }
-#pragma unroll
-      for (int hc = 0; hc < 2; ++hc) {
-        const int ch = 2 * a + hc;  // token chunk of 8
-        const uint4 wk = make_uint4(pk_kg[4 * hc], pk_kg[4 * hc + 1], pk_kg[4 * hc + 2], pk_kg[4 * hc + 3]);
-        const uint4 wv = make_uint4(pk_v[4 * hc], pk_v[4 * hc + 1], pk_v[4 * hc + 2], pk_v[4 * hc + 3]);
-        const uint4 wt = make_uint4(pk_kt[4 * hc], pk_kt[4 * hc + 1], pk_kt[4 * hc + 2], pk_kt[4 * hc + 3]);
-        *reinterpret_cast<uint4*>(sm + kP_BKg + sw128_chunk(128, c, ch)) = wk;
-        *reinterpret_cast<uint4*>(sm + kP_BV + sw128_chunk(128, c, ch)) = wv;
-        *reinterpret_cast<uint4*>(unit + kAK + sw128_chunk(192, 64 + c, ch)) = wt;
-      }
+      // copies still in flight must land before the CTA may exit
+      if (it > 0) mbar_wait(bar_full, (it - 1) & 1, nullptr);
     }
-    gam_out[(size_t)u * D + c] = __expf(GC);
+  } else {
+    // --------------------------------------------------------- compute warps
+    const int c = t & 127, hf = t >> 7;  // channel, row half (rows 32*hf .. 32*hf+31)
+    const int lane = t & 127;            // TMEM lane of this thread in the epilogues
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    const __nv_bfloat16* sK = reinterpret_cast<const __nv_bfloat16*>(sm + kI_K);
+    const __nv_bfloat16* sQ = reinterpret_cast<const __nv_bfloat16*>(sm + kI_Q);
+    const __nv_bfloat16* sV = reinterpret_cast<const __nv_bfloat16*>(sm + kI_V);
+    const float* sG = reinterpret_cast<const float*>(sm + kI_G);
+    uint32_t it = 0;
+    for (int64_t u = blockIdx.x; u < units_ub; u += gridDim.x, ++it) {
+      const UnitInfo ui = unit_info(plan, H, u);
+      if (ui.chunk >= total) break;
+      const int len = ui.len;
+      uint8_t* unit = tiles + (size_t)u * kUnitBytes;
+      if (t < C) beta_s[t] = (t < len) ? __bfloat162float(beta[(ui.t0 + t) * H + ui.h]) : 0.f;
+      bool ok = mbar_wait(bar_full, it & 1, err);
+      if (!named_sync_and(1, kPrepCompute, ok)) break;
 
-    // ---- block products: D[:, 0:64] = [KC0; KC1] x Bop[0:64]^T, D[:, 64:128] = [KC2; KC3] x Bop[64:128]^T
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (t == 0) {
-      tc_fence_after();
-      const uint32_t id = idesc_bf16(128, 64);
-      mma_tile(tmem + 0, sbase + kP_KC01, 128, sbase + kP_Bop, 128, D, id, false);
-      mma_tile(tmem + 64, sbase + kP_KC23, 128, sbase + kP_Bop + 64 * 128, 128, D, id, false);
-      mma_commit(bar_p);
-    }
-    bool ok = mbar_wait(bar_p, iter & 1, err);
-    if (!__syncthreads_and(ok)) break;
-    tc_fence_after();
-    {
-      const int half = t >> 6, i = t & 63;
-      float pv[2][32];
-      tmem_ld32(lane_addr + 32 * half, pv[0]);
-      tmem_ld32(lane_addr + 64 + 32 * half, pv[1]);
-      tmem_wait_ld();
+      // ---- pass 1: running log-decay of channel c over this thread's 32 rows
+      float G[32];
+      {
+        float acc = 0.f;
 #pragma unroll
-      for (int s = 0; s < 2; ++s) {
-        const int a = half + 2 * s;
+        for (int j = 0; j < 32; ++j) {
+          const int r = 32 * hf + j;
+          acc += (r < len) ? sG[r * D + c] : 0.f;
+          G[j] = acc;
+        }
+      }
+      if (hf == 0) {
+        Rs[c] = 0.f;
+        Rs[D + c] = G[15];
+        Rs[2 * D + c] = G[31];
+      }
+      named_sync(1, kPrepCompute);
+      if (hf == 1) {
+        const float off = Rs[2 * D + c];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) G[j] += off;
+        Rs[3 * D + c] = G[15];
+        GCs[c] = G[31];
+      }
+      named_sync(1, kPrepCompute);
+      const float R[4] = {Rs[c], Rs[D + c], Rs[2 * D + c], Rs[3 * D + c]};
+      const float GC = GCs[c];
+
+      // ---- pass 2: operands for this thread's two tiles
+#pragma unroll
+      for (int lt = 0; lt < 2; ++lt) {
+        const int a = 2 * hf + lt;
+        const float Ra = hf ? R[2 + lt] : R[lt];  // static indices: R stays in registers
+        float E[4];
+#pragma unroll
+        for (int ap = 0; ap < 4; ++ap) E[ap] = (ap > a) ? __expf(R[ap] - Ra) : 1.f;
+        const float eRa = __expf(Ra);       // exp(R_a) <= 1
+        const float eCa = __expf(GC - Ra);  // exp(G_C - R_a) <= 1
+#pragma unroll
+        for (int hq = 0; hq < 2; ++hq) {  // 8 rows = one 16-byte chunk per operand
+          float kb[8], qb[8], kn[8], kg[8], vb[8], kt[8], qg[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int j = 8 * hq + e, r = 16 * a + j;
+            const bool in = r < len;
+            const float kk = in ? __bfloat162float(sK[r * D + c]) : 0.f;
+            const float qq = in ? __bfloat162float(sQ[r * D + c]) : 0.f;
+            const float vv = in ? __bfloat162float(sV[r * D + c]) : 0.f;
+            const float d = G[16 * lt + j] - Ra;  // (-80, 0]
+            const float f = __expf(d), fi = __expf(-d);
+            kb[e] = kk * f;
+            qb[e] = qq * f;
+            kn[e] = kk * fi;
+            kg[e] = kb[e] * eRa * beta_s[r];
+            vb[e] = vv * beta_s[r];
+            kt[e] = kn[e] * eCa;
+            qg[e] = qb[e] * eRa;
+          }
+          *reinterpret_cast<uint4*>(sm + kP_Bop + mn_chunk(128, 4 * a + hq, c)) = pack8(kb);
+          *reinterpret_cast<uint4*>(sm + kP_Bop + mn_chunk(128, 4 * a + 2 + hq, c)) = pack8(qb);
+#pragma unroll
+          for (int ap = 0; ap < 4; ++ap) {
+            if (ap < a) continue;
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = kn[e] * E[ap];
+            const uint32_t kc = (ap < 2) ? kP_KC01 : kP_KC23;
+            *reinterpret_cast<uint4*>(sm + kc + mn_chunk(128, 8 * (ap & 1) + 2 * a + hq, c)) =
+                pack8(x);
+          }
+          *reinterpret_cast<uint4*>(sm + kP_BKg + sw128_chunk(128, c, 2 * a + hq)) = pack8(kg);
+          *reinterpret_cast<uint4*>(sm + kP_BV + sw128_chunk(128, c, 2 * a + hq)) = pack8(vb);
+          *reinterpret_cast<uint4*>(unit + kKT + sw128_chunk(128, c, 2 * a + hq)) = pack8(kt);
+          *reinterpret_cast<uint4*>(unit + kWQ + mn_chunk(128, 8 + 2 * a + hq, c)) = pack8(qg);
+        }
+      }
+      if (hf == 0) gam_out[(size_t)u * D + c] = __expf(GC);
+      mbar_arrive(bar_empty);  // the staged rows are consumed: the copy warp may refill
+
+      // ---- block products: D[:, 0:64] = [KC0|KC1] x Bop[0:64]^T, D[:, 64:128] = [KC2|KC3] x Bop[64:128]^T
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_sync(1, kPrepCompute);
+      if (t == 0) {
+        tc_fence_after();
+        const uint32_t id = idesc_bf16_mn(128, 64, 1, 1);
+        for (int s = 0; s < D / 16; ++s)
+          mma_bf16(tmem + 0, mnmajor_desc(sbase + kP_KC01, 2048, s),
+                   mnmajor_desc(sbase + kP_Bop, 2048, s), id, s > 0);
+        for (int s = 0; s < D / 16; ++s)
+          mma_bf16(tmem + 64, mnmajor_desc(sbase + kP_KC23, 2048, s),
+                   mnmajor_desc(sbase + kP_Bop + 1024, 2048, s), id, s > 0);
+        mma_commit(bar_p);
+      }
+      ok = mbar_wait(bar_p, it & 1, err);
+      if (!named_sync_and(1, kPrepCompute, ok)) break;
+      tc_fence_after();
+      {
+        // lane = key index i (+64 for the odd tile of the pair); hf picks the pair
+        const int i = lane & 63, a = 2 * hf + (lane >> 6);
+        float pv[32];
+        tmem_ld32(lane_addr + 64 * hf + 32 * (lane >> 6), pv);
+        tmem_wait_ld();
+        float aq[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int r = 16 * a + j;
-          Ls[r * kLdL + i] = (i < r) ? beta_s[r] * pv[s][j] : 0.f;
-          *reinterpret_cast<__nv_bfloat16*>(unit + kAK + sw128_offset(192, r, i)) =
-              __float2bfloat16_rn((i <= r) ? pv[s][16 + j] : 0.f);
+          Lb[r * kLdL + i] = (i < r) ? beta_s[r] * pv[j] : 0.f;
+          aq[j] = (i <= r) ? pv[16 + j] : 0.f;
+        }
+        *reinterpret_cast<uint4*>(unit + kAQ + mn_chunk(64, 2 * a, i)) = pack8(aq);
+        *reinterpret_cast<uint4*>(unit + kAQ + mn_chunk(64, 2 * a + 1, i)) = pack8(aq + 8);
+      }
+      named_sync(1, kPrepCompute);
+
+      // ---- T = (I + L)^{-1}, blockwise over 16 x 16 blocks, fp32
+      if (t < C) {  // diagonal blocks: forward substitution, one column per thread
+        const int ba = t >> 4, cc = t & 15, o = 16 * ba;
+        float x[16];
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+          float acc = 0.f;
+#pragma unroll
+          for (int i2 = 0; i2 < m; ++i2) acc = fmaf(Lb[(o + m) * kLdL + o + i2], x[i2], acc);
+          x[m] = (m < cc) ? 0.f : (m == cc ? 1.f : -acc);
+        }
+#pragma unroll
+        for (int m = 0; m < 16; ++m)
+          if (m > cc) Lb[(o + cc) * kLdL + o + m] = x[m];
+      }
+      named_sync(1, kPrepCompute);
+      // T_{a+d, a} = -T_{a+d, a+d} * (sum_{b=a}^{a+d-1} L_{a+d, b} T_{b, a}), d = 1, 2, 3
+#pragma unroll 1
+      for (int d = 1; d < 4; ++d) {
+        const int nblk = 4 - d;
+        for (int e = t; e < nblk * 256; e += kPrepCompute) {
+          const int a = e >> 8, m = (e >> 4) & 15, n = e & 15;
+          const int rr = 16 * (a + d) + m, cc = 16 * a + n;
+          float acc = 0.f;
+          for (int kk = cc; kk < 16 * (a + d); ++kk) acc = fmaf(Lb[rr * kLdL + kk], t_at(Lb, kk, cc), acc);
+          Ps[e] = acc;
+        }
+        named_sync(1, kPrepCompute);
+        for (int e = t; e < nblk * 256; e += kPrepCompute) {
+          const int a = e >> 8, m = (e >> 4) & 15, n = e & 15;
+          const int o = 16 * (a + d);
+          float acc = 0.f;
+          for (int kk = 0; kk <= m; ++kk) acc = fmaf(t_at(Lb, o + m, o + kk), Ps[(a << 8) | (kk << 4) | n], acc);
+          Lb[(16 * a + n) * kLdL + o + m] = -acc;
+        }
+        named_sync(1, kPrepCompute);
+      }
+      {  // T -> bf16 B operand (MN-major, X = row r, K = column j)
+        const int j = t >> 2, qq = t & 3;
+        float x[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) x[e] = t_at(Lb, 16 * qq + e, j);
+        *reinterpret_cast<uint4*>(sm + kP_T + mn_chunk(64, 2 * qq, j)) = pack8(x);
+        *reinterpret_cast<uint4*>(sm + kP_T + mn_chunk(64, 2 * qq + 1, j)) = pack8(x + 8);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_sync(1, kPrepCompute);
+      if (t == 0) {
+        tc_fence_after();
+        const uint32_t id = idesc_bf16_mn(128, 64, 0, 1);
+        for (int s = 0; s < C / 16; ++s)  // W^T = (beta Gamma K)^T T^T
+          mma_bf16(tmem + 128, kmajor_desc(sbase + kP_BKg, 128, s),
+                   mnmajor_desc(sbase + kP_T, 1024, s), id, s > 0);
+        for (int s = 0; s < C / 16; ++s)  // U^T = (beta V)^T T^T
+          mma_bf16(tmem + 192, kmajor_desc(sbase + kP_BV, 128, s),
+                   mnmajor_desc(sbase + kP_T, 1024, s), id, s > 0);
+        mma_commit(bar_w);
+      }
+      ok = mbar_wait(bar_w, it & 1, err);
+      if (!named_sync_and(1, kPrepCompute, ok)) break;
+      tc_fence_after();
+      {
+        float w0[32], w1[32];
+        tmem_ld32(lane_addr + 128 + 64 * hf, w0);
+        tmem_ld32(lane_addr + 160 + 64 * hf, w1);
+        tmem_wait_ld();
+        if (hf == 0) {  // W[r][dk]: W block of WQ, K-row dk = lane
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch)
+            *reinterpret_cast<uint4*>(unit + kWQ + mn_chunk(128, ch, lane)) =
+                pack8(ch < 4 ? &w0[8 * ch] : &w1[8 * (ch - 4)]);
+        } else {  // U^T row dv = lane
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch)
+            *reinterpret_cast<uint4*>(unit + kUT + sw128_chunk(128, lane, ch)) =
+                pack8(ch < 4 ? &w0[8 * ch] : &w1[8 * (ch - 4)]);
         }
       }
+      tc_fence_before();
+      named_sync(1, kPrepCompute);
     }
-    __syncthreads();
-
-    // ---- T = (I + L)^{-1}: forward substitution, one column per thread (warps 0-1)
-    if (t < C) {
-      const int jc = t;
-      float x[C];
-#pragma unroll
-      for (int r = 0; r < C; ++r) {
-        float acc = 0.f;
-#pragma unroll
-        for (int i = 0; i < r; ++i) acc = fmaf(Ls[r * kLdL + i], x[i], acc);
-        x[r] = (r < jc) ? 0.f : (r == jc ? 1.f : -acc);
-      }
-#pragma unroll
-      for (int r = 0; r < C; ++r) st_bf16(sm, kP_T + sw128_offset(64, r, jc), x[r]);
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (t == 0) {
-      tc_fence_after();
-      const uint32_t id = idesc_bf16(128, 64);
-      mma_tile(tmem + 128, sbase + kP_BKg, 128, sbase + kP_T, 64, C, id, false);  // W^T
-      mma_tile(tmem + 192, sbase + kP_BV, 128, sbase + kP_T, 64, C, id, false);   // U^T
-      mma_commit(bar_w);
-    }
-    ok = mbar_wait(bar_w, iter & 1, err);
-    if (!__syncthreads_and(ok)) break;
-    tc_fence_after();
-    {
-      float w0[32], w1[32];
-      tmem_ld32(lane_addr + 128, w0);
-      tmem_ld32(lane_addr + 160, w1);
-      tmem_wait_ld();
-#pragma unroll
-      for (int r = 0; r < 32; ++r) {
-        *reinterpret_cast<__nv_bfloat16*>(unit + kWQ + sw128_offset(128, r, c)) = __float2bfloat16_rn(w0[r]);
-        *reinterpret_cast<__nv_bfloat16*>(unit + kWQ + sw128_offset(128, 32 + r, c)) = __float2bfloat16_rn(w1[r]);
-      }
-      tmem_ld32(lane_addr + 192, w0);
-      tmem_ld32(lane_addr + 224, w1);
-      tmem_wait_ld();
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        const float* src = ch < 4 ? &w0[8 * ch] : &w1[8 * (ch - 4)];
-        const uint4 wv = make_uint4(pack_bf16(src[0], src[1]), pack_bf16(src[2], src[3]),
-                                    pack_bf16(src[4], src[5]), pack_bf16(src[6], src[7]));
-        *reinterpret_cast<uint4*>(unit + kUT + sw128_chunk(128, c, ch)) = wv;
-      }
-    }
-    tc_fence_before();
-    __syncthreads();
-    ++iter;
   }
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 256);
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
 }
 
 // ============================================================= chain kernel
 constexpr int kStages = 2;
-constexpr uint32_t kStageBytes = 75776;                 // unit (72 KB) + gamma (512 B), 1024-aligned
-constexpr uint32_t kC_Sbf = kStages * kStageBytes;      // S^T bf16, 128 x 128 (32 KB)
-constexpr uint32_t kC_Vt = kC_Sbf + 32768;              // Vt^T bf16, 128 x 64 (16 KB)
-constexpr uint32_t kC_bars = kC_Vt + 16384;
+constexpr uint32_t kStageBytes = 75776;             // unit (72 KB) + gamma (512 B), 1024-aligned
+constexpr uint32_t kC_Sbf = kStages * kStageBytes;  // S^T bf16, K-major 128 x 128 (32 KB)
+constexpr uint32_t kC_Vt = kC_Sbf + 32768;          // Vt^T bf16, K-major 128 x 64 (16 KB)
+constexpr uint32_t kC_O = kC_Vt + 16384;            // O staging, [64][128] bf16 row-major
+constexpr uint32_t kC_bars = kC_O + 16384;
 constexpr uint32_t kC_Smem = kC_bars + 128 + 1024;
-constexpr int kChainThreads = 160;  // warps 0-3: epilogue (TMEM lanes), warp 4: copies + MMA
+constexpr int kEpi = 256;                 // epilogue: (TMEM lane, column half)
+constexpr int kChainThreads = kEpi + 32;  // + copy/MMA warp
 
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int* err,
                                               volatile int* abort_flag) {
@@ -318,10 +422,11 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   const uint32_t sbase = smem_addr(sm);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kC_bars);
   // bars: 0,1 = full[stage], 2 = S ready (bf16 copy written, S scaled), 3 = MMA1 done,
-  //       4 = Vt ready, 5 = MMA2 done
+  //       4 = Vt ready, 5 = MMA2 done, 6 = O staging written, 7 = O staging read
   const uint32_t bar_full0 = smem_addr(&bars[0]);
   const uint32_t bar_s = smem_addr(&bars[2]), bar_m1 = smem_addr(&bars[3]);
   const uint32_t bar_vt = smem_addr(&bars[4]), bar_m2 = smem_addr(&bars[5]);
+  const uint32_t bar_ow = smem_addr(&bars[6]), bar_or = smem_addr(&bars[7]);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kC_bars + 64);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kC_bars + 72);
   const int t = threadIdx.x, warp = t >> 5;
@@ -329,10 +434,12 @@ __global__ void __launch_bounds__(kChainThreads, 1)
 
   if (t == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(bar_full0 + 8 * s, 1);
-    mbar_init(bar_s, 128);
+    mbar_init(bar_s, kEpi);
     mbar_init(bar_m1, 1);
-    mbar_init(bar_vt, 128);
+    mbar_init(bar_vt, kEpi);
     mbar_init(bar_m2, 1);
+    mbar_init(bar_ow, kEpi);
+    mbar_init(bar_or, kEpi);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -347,7 +454,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   const int64_t tend = max(tstart, (int64_t)__ldg(plan.cu + n + 1));
   const int64_t state = ((int64_t)n * H + h) * D * D;
 
-  if (warp == 4) {
+  if (warp == kEpi / 32) {
     // ------------------------------------------------ copies + MMA issue (one thread)
     if ((t & 31) == 0) {
       auto issue = [&](int jj) {
@@ -360,7 +467,9 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       };
       int issued = 0, consumed = 0;
       for (; issued < min(kStages, nch); ++issued) issue(issued);
-      const uint32_t id1 = idesc_bf16(128, 128), id2a = idesc_bf16(128, 64);
+      const uint32_t id1 = idesc_bf16_mn(128, 128, 0, 1);   // S^T x WQ (MN-major B)
+      const uint32_t id2a = idesc_bf16_mn(128, 64, 0, 1);   // Vt^T x A_qk (MN-major B)
+      const uint32_t id2b = idesc_bf16_mn(128, 128, 0, 0);  // Vt^T x Kt^T (K-major B)
       int j = 0;
       bool mma_pending = false;
       for (; j < nch; ++j) {
@@ -371,12 +480,18 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         consumed = j + 1;
         tc_fence_after();
         const uint32_t d1 = tmem + 128 + 128 * (j & 1);
-        mma_tile(d1, sbase + kC_Sbf, 128, st + kWQ, 128, D, id1, false);
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_bf16(d1, kmajor_desc(sbase + kC_Sbf, 128, ks), mnmajor_desc(st + kWQ, 2048, ks), id1,
+                   ks > 0);
         mma_commit(bar_m1);
         if (!wait_or_abort(bar_vt, j & 1, err, abort_flag)) { mma_pending = true; break; }
         tc_fence_after();
-        mma_tile(d1 + 64, sbase + kC_Vt, 128, st + kAK, 192, C, id2a, true);
-        mma_tile(tmem + 0, sbase + kC_Vt, 128, st + kAK + 64 * 128, 192, C, id1, true);
+        for (int ks = 0; ks < C / 16; ++ks)
+          mma_bf16(d1 + 64, kmajor_desc(sbase + kC_Vt, 128, ks), mnmajor_desc(st + kAQ, 1024, ks),
+                   id2a, 1u);
+        for (int ks = 0; ks < C / 16; ++ks)
+          mma_bf16(tmem + 0, kmajor_desc(sbase + kC_Vt, 128, ks), kmajor_desc(st + kKT, 128, ks),
+                   id2b, 1u);
         mma_commit(bar_m2);
         if (j + kStages < nch) {
           if (!wait_or_abort(bar_m2, j & 1, err, abort_flag)) { mma_pending = true; break; }
@@ -391,36 +506,49 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       }
     }
   } else {
-    // ------------------------------------------------ epilogue warps: TMEM lane = dv = t
-    const uint32_t lane = tmem + ((uint32_t)(warp * 32) << 16);
+    // ------------------------- epilogue warps: TMEM lane = dv, ch = column half
+    const int lane = t & 127, ch = t >> 7;
+    const uint32_t lrow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     {
       float sv[32];
 #pragma unroll
-      for (int qq = 0; qq < 4; ++qq) {
+      for (int qq = 0; qq < 2; ++qq) {
+        const int col = 64 * ch + 32 * qq;
         if (h0) {
 #pragma unroll
           for (int i = 0; i < 32; i += 4) {
-            const float4 x = *reinterpret_cast<const float4*>(h0 + state + (int64_t)t * D + 32 * qq + i);
+            const float4 x = *reinterpret_cast<const float4*>(h0 + state + (int64_t)lane * D + col + i);
             sv[i] = x.x; sv[i + 1] = x.y; sv[i + 2] = x.z; sv[i + 3] = x.w;
           }
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) sv[i] = 0.f;
         }
-        tmem_st32(lane + 32 * qq, sv);
+        tmem_st32(lrow + col, sv);
       }
       tmem_wait_st();
     }
-    auto store_o = [&](int jj) {
-      float ov[2][32];
-      const uint32_t d1 = lane + 128 + 128 * (jj & 1) + 64;
-      tmem_ld32(d1, ov[0]);
-      tmem_ld32(d1 + 32, ov[1]);
+    __nv_bfloat16* Ost = reinterpret_cast<__nv_bfloat16*>(sm + kC_O);
+    auto store_o = [&](int jj) -> bool {
+      // staging handoff on mbarriers (bounded waits): written -> read -> reusable
+      if (jj > 0 && !wait_or_abort(bar_or, (jj - 1) & 1, err, abort_flag)) return false;
+      float ov[32];
+      tmem_ld32(lrow + 128 + 128 * (jj & 1) + 64 + 32 * ch, ov);
       tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 32; ++e) Ost[(32 * ch + e) * D + lane] = __float2bfloat16_rn(ov[e]);
+      mbar_arrive(bar_ow);
+      if (!wait_or_abort(bar_ow, jj & 1, err, abort_flag)) return false;
       const int64_t tc = tstart + (int64_t)jj * C;
 #pragma unroll
-      for (int r = 0; r < C; ++r)
-        if (tc + r < tend) o[((tc + r) * H + h) * D + t] = __float2bfloat16_rn(ov[r >> 5][r & 31]);
+      for (int qq = 0; qq < 4; ++qq) {
+        const int id = t + kEpi * qq, r = id >> 4, cc = id & 15;
+        if (tc + r < tend)
+          *reinterpret_cast<uint4*>(o + ((tc + r) * H + h) * D + 8 * cc) =
+              *reinterpret_cast<const uint4*>(Ost + r * D + 8 * cc);
+      }
+      mbar_arrive(bar_or);
+      return true;
     };
     bool alive = true;
     for (int j = 0; j < nch && alive; ++j) {
@@ -432,48 +560,46 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       if (!wait_or_abort(bar_full0 + 8 * s, (j / kStages) & 1, err, abort_flag)) { alive = false; break; }
       tc_fence_after();
 #pragma unroll
-      for (int qq = 0; qq < 4; ++qq) {
+      for (int qq = 0; qq < 2; ++qq) {
+        const int col = 64 * ch + 32 * qq;
         float sv[32];
-        tmem_ld32(lane + 32 * qq, sv);
+        tmem_ld32(lrow + col, sv);
         tmem_wait_ld();
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          const uint4 w = make_uint4(pack_bf16(sv[8 * ch], sv[8 * ch + 1]),
-                                     pack_bf16(sv[8 * ch + 2], sv[8 * ch + 3]),
-                                     pack_bf16(sv[8 * ch + 4], sv[8 * ch + 5]),
-                                     pack_bf16(sv[8 * ch + 6], sv[8 * ch + 7]));
-          *reinterpret_cast<uint4*>(sm + kC_Sbf + sw128_chunk(128, t, 4 * qq + ch)) = w;
-        }
+        for (int e = 0; e < 4; ++e)
+          *reinterpret_cast<uint4*>(sm + kC_Sbf + sw128_chunk(128, lane, col / 8 + e)) =
+              pack8(&sv[8 * e]);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) sv[i] *= gam_s[32 * qq + i];
-        tmem_st32(lane + 32 * qq, sv);
+        for (int i = 0; i < 32; i += 4) {
+          const float4 gm = *reinterpret_cast<const float4*>(gam_s + col + i);
+          sv[i] *= gm.x; sv[i + 1] *= gm.y; sv[i + 2] *= gm.z; sv[i + 3] *= gm.w;
+        }
+        tmem_st32(lrow + col, sv);
       }
       tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar_s);
       // E2 of the previous chunk (its D1 buffer is not touched by MMA1 of this chunk)
-      if (j > 0) store_o(j - 1);
-      // E1: Vt^T = U^T - (W S)^T
+      if (j > 0 && !store_o(j - 1)) { alive = false; break; }
+      // E1: Vt^T = U^T - (W S)^T on this thread's 32 tokens
       if (!wait_or_abort(bar_m1, j & 1, err, abort_flag)) { alive = false; break; }
       tc_fence_after();
       {
-        float wsv[2][32];
-        const uint32_t d1 = lane + 128 + 128 * (j & 1);
-        tmem_ld32(d1, wsv[0]);
-        tmem_ld32(d1 + 32, wsv[1]);
+        float wsv[32];
+        tmem_ld32(lrow + 128 + 128 * (j & 1) + 32 * ch, wsv);
         tmem_wait_ld();
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const uint4 uu = *reinterpret_cast<const uint4*>(st + kUT + sw128_chunk(128, t, ch));
-          const float* wsrc = &wsv[ch >> 2][8 * (ch & 3)];
+        for (int e = 0; e < 4; ++e) {
+          const uint4 uu = *reinterpret_cast<const uint4*>(st + kUT + sw128_chunk(128, lane, 4 * ch + e));
           const uint32_t uw[4] = {uu.x, uu.y, uu.z, uu.w};
-          uint32_t out[4];
+          float x[8];
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            out[e] = pack_bf16(bf16_lo(uw[e]) - wsrc[2 * e], bf16_hi(uw[e]) - wsrc[2 * e + 1]);
-          *reinterpret_cast<uint4*>(sm + kC_Vt + sw128_chunk(128, t, ch)) =
-              make_uint4(out[0], out[1], out[2], out[3]);
+          for (int p = 0; p < 4; ++p) {
+            x[2 * p] = bf16_lo(uw[p]) - wsv[8 * e + 2 * p];
+            x[2 * p + 1] = bf16_hi(uw[p]) - wsv[8 * e + 2 * p + 1];
+          }
+          *reinterpret_cast<uint4*>(sm + kC_Vt + sw128_chunk(128, lane, 4 * ch + e)) = pack8(x);
         }
       }
       fence_proxy_async_smem();
@@ -487,13 +613,14 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     if (hT && !*abort_flag) {
       tc_fence_after();
 #pragma unroll
-      for (int qq = 0; qq < 4; ++qq) {
+      for (int qq = 0; qq < 2; ++qq) {
+        const int col = 64 * ch + 32 * qq;
         float sv[32];
-        tmem_ld32(lane + 32 * qq, sv);
+        tmem_ld32(lrow + col, sv);
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 32; i += 4)
-          *reinterpret_cast<float4*>(hT + state + (int64_t)t * D + 32 * qq + i) =
+          *reinterpret_cast<float4*>(hT + state + (int64_t)lane * D + col + i) =
               make_float4(sv[i], sv[i + 1], sv[i + 2], sv[i + 3]);
       }
     }
@@ -538,7 +665,8 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
   if (units > 0) {
     e = cudaFuncSetAttribute(tc_prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kP_Smem);
     if (e != cudaSuccess) return e;
-    const int grid = (int)(units < sm_count() ? units : sm_count());
+    const int sms = sm_count();
+    const int grid = (int)(units < sms ? units : sms);
     ProfScope prof_scope("kda_tc_prep", s);
     tc_prep<<<grid, kPrepThreads, kP_Smem, s>>>(
         static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), g,

@@ -86,6 +86,24 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// ------------------------------------------------------- named barriers
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// Barrier `id` over `nthreads` threads that also ANDs `p` across them.
+__device__ __forceinline__ bool named_sync_and(uint32_t id, uint32_t nthreads, bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred a, b;\n\t"
+      "setp.ne.u32 a, %1, 0;\n\t"
+      "bar.red.and.pred b, %2, %3, a;\n\t"
+      "selp.u32 %0, 1, 0, b;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)p), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
 // ----------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -215,6 +233,48 @@ __host__ __device__ __forceinline__ uint32_t sw128_offset(int rows, int row, int
 __host__ __device__ __forceinline__ uint32_t sw128_chunk(int rows, int row, int ch) {
   const int kb = ch >> 3, w = ch & 7;
   return (uint32_t)(kb * rows * 128 + row * 128 + ((w ^ (row & 7)) << 4));
+}
+
+// ---- MN-major SW128 tiles ------------------------------------------------
+// A tile whose M (or N) extent X is a multiple of 64 and whose K extent is a
+// multiple of 8: 1024-byte atoms of 8 K-rows x 64 X-elements (128 bytes per
+// K-row, 16-byte chunks permuted by chunk ^ (k % 8)); atoms along X are 1024
+// bytes apart (LBO), groups of 8 K-rows are (X/64)*1024 bytes apart (SBO).  A
+// thread that owns one K index writes its run of X contiguously.
+__host__ __device__ __forceinline__ uint32_t mn_sbo(int X) { return (uint32_t)(X >> 6) * 1024u; }
+__host__ __device__ __forceinline__ uint32_t mn_offset(int X, int x, int k) {
+  return (uint32_t)((x >> 6) * 1024) + (uint32_t)(k >> 3) * mn_sbo(X) + (uint32_t)((k & 7) * 128) +
+         (uint32_t)(((((x & 63) >> 3) ^ (k & 7)) << 4) | ((x & 7) << 1));
+}
+// 16-byte chunk holding X elements 8*xc .. 8*xc+7 of K-row k.
+__host__ __device__ __forceinline__ uint32_t mn_chunk(int X, int xc, int k) {
+  return (uint32_t)((xc >> 3) * 1024) + (uint32_t)(k >> 3) * mn_sbo(X) + (uint32_t)((k & 7) * 128) +
+         (uint32_t)(((xc & 7) ^ (k & 7)) << 4);
+}
+
+__device__ __forceinline__ uint64_t make_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+// Descriptor of K step s (16 elements of K) of a K-major tile with `rows` rows per
+// 64-column block, starting at `base`.
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int rows, int s) {
+  return make_desc(base + (uint32_t)(s >> 2) * (uint32_t)rows * 128u + (uint32_t)(s & 3) * 32u, 16u,
+                   1024u);
+}
+// Descriptor of K step s of an MN-major tile with SBO `sbo`, starting at `base`.
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, uint32_t sbo, int s) {
+  return make_desc(base + (uint32_t)s * 2u * sbo, 1024u, sbo);
+}
+// Instruction descriptor with operand majorness (0 = K-major, 1 = MN-major).
+__host__ __device__ constexpr uint32_t idesc_bf16_mn(int M, int N, int a_mn, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
