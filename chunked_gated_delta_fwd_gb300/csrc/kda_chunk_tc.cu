@@ -54,25 +54,27 @@ constexpr uint32_t kUnitBytes = 73728;
 constexpr uint32_t kGamBytes = D * 4;
 
 // ============================================================== prep kernel
-constexpr int kPrepCompute = 256;                // (channel, row half)
+constexpr int kPrepCompute = 256;                // 8 compute warps
 constexpr int kPrepThreads = kPrepCompute + 32;  // + the copy warp
 constexpr uint32_t kInRowBytes = 3 * 256 + 512;  // k, q, v (bf16) and g (fp32) per token
 // shared memory (offsets from a 1024-aligned base)
 constexpr uint32_t kI_K = 0, kI_Q = 16384, kI_V = 32768, kI_G = 49152;  // staged rows
-constexpr uint32_t kP_Bop = 81920;           // MN-major X=128 (Kb/Qb rows), K=128
-constexpr uint32_t kP_L = kP_Bop;            //   reused after the products: fp32 [64][65]
-constexpr uint32_t kP_P = kP_Bop + 16640;    //   fp32 scratch, 3 x 16 x 16
-constexpr uint32_t kP_T = kP_Bop + 20480;    //   bf16 T, MN-major X=64, K=64
-constexpr uint32_t kP_KC01 = 114688;         // MN-major X=128 ([KC(0) | KC(1)] rows), K=128
-constexpr uint32_t kP_KC23 = 147456;         // [KC(2) | KC(3)]
-constexpr uint32_t kP_BKg = 180224;          // K-major (beta Gamma K)^T 128 x 64
-constexpr uint32_t kP_BV = 196608;           // K-major (beta V)^T 128 x 64
-constexpr uint32_t kP_beta = 212992;         // 64 fp32
-constexpr uint32_t kP_R = kP_beta + 256;     // R_0..R_3, [4][128] fp32
-constexpr uint32_t kP_GC = kP_R + 2048;      // G at the chunk end, [128] fp32
-constexpr uint32_t kP_bars = kP_GC + 512;    // in_full, in_empty, p, w + TMEM base
+constexpr uint32_t kP_Bop = 81920;         // MN-major X=128 (Kb/Qb rows), K=128
+constexpr uint32_t kP_T = kP_Bop;          //   reused after the products: bf16 T, MN-major 64x64
+constexpr uint32_t kP_KC01 = 114688;       // MN-major X=128 ([KC(0) | KC(1)] rows), K=128
+constexpr uint32_t kP_KC23 = 147456;       // [KC(2) | KC(3)]
+// reused after the products (re-zeroed before the next unit's operands):
+constexpr uint32_t kP_Lb = kP_KC01;          // L, fp32 [64][65] (strictly lower part)
+constexpr uint32_t kP_Tb = kP_Lb + 16640;    // T, fp32 [64][68] row-major
+constexpr uint32_t kP_Ps = kP_Tb + 17408;    // block-product scratch, fp32 [3][16][16]
+constexpr uint32_t kScratchBytes = 16640 + 17408 + 3072;
+constexpr uint32_t kP_BKg = 180224;        // K-major (beta Gamma K)^T 128 x 64
+constexpr uint32_t kP_BV = 196608;         // K-major (beta V)^T 128 x 64
+constexpr uint32_t kP_beta = 212992;       // 64 fp32
+constexpr uint32_t kP_Tot = kP_beta + 256; // per-tile sums of g, [4][128] fp32
+constexpr uint32_t kP_bars = kP_Tot + 2048;  // in_full, in_empty, p, w + TMEM base
 constexpr uint32_t kP_Smem = kP_bars + 64 + 1024;
-constexpr int kLdL = 65;
+constexpr int kLdL = 65, kLdT = 68;
 
 __device__ __forceinline__ uint4 pack8(const float* x) {
   return make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
@@ -99,10 +101,48 @@ __device__ __forceinline__ UnitInfo unit_info(const Plan& plan, int H, int64_t u
   return ui;
 }
 
-// T (lower unit-triangular) is kept transposed in the upper part of Lbuf:
-// T[r][c] for r > c at Lbuf[c][r]; L (strictly lower) at Lbuf[r][c].
-__device__ __forceinline__ float t_at(const float* Lb, int r, int c) {
-  return r == c ? 1.f : (r < c ? 0.f : Lb[c * kLdL + r]);
+// One block stage of T = (I + L)^{-1}: for every block (a + d, a),
+//   P = sum_{b=a}^{a+d-1} L_{a+d, b} T_{b, a},   T_{a+d, a} = -T_{a+d, a+d} P.
+// 64 threads per block, each owning one row m and four columns.
+template <int d>
+__device__ __forceinline__ void inverse_stage(int t, const float* Lb, float* Tb, float* Ps) {
+  const bool act = t < (4 - d) * 64;
+  const int a = t >> 6, tt = t & 63, m = tt >> 2, nq = tt & 3;
+  const int R = a + d;
+  if (act) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int bb = 0; bb < d; ++bb) {
+      const int b = a + bb;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const float l = Lb[(16 * R + m) * kLdL + 16 * b + k];
+        const float4 tv = *reinterpret_cast<const float4*>(Tb + (16 * b + k) * kLdT + 16 * a + 4 * nq);
+        acc[0] = fmaf(l, tv.x, acc[0]);
+        acc[1] = fmaf(l, tv.y, acc[1]);
+        acc[2] = fmaf(l, tv.z, acc[2]);
+        acc[3] = fmaf(l, tv.w, acc[3]);
+      }
+    }
+    *reinterpret_cast<float4*>(Ps + a * 256 + m * 16 + 4 * nq) =
+        make_float4(acc[0], acc[1], acc[2], acc[3]);
+  }
+  named_sync(1, kPrepCompute);
+  if (act) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {  // T_RR is unit lower triangular with stored zeros
+      const float w = Tb[(16 * R + m) * kLdT + 16 * R + kk];
+      const float4 pv = *reinterpret_cast<const float4*>(Ps + a * 256 + kk * 16 + 4 * nq);
+      acc[0] = fmaf(w, pv.x, acc[0]);
+      acc[1] = fmaf(w, pv.y, acc[1]);
+      acc[2] = fmaf(w, pv.z, acc[2]);
+      acc[3] = fmaf(w, pv.w, acc[3]);
+    }
+    *reinterpret_cast<float4*>(Tb + (16 * R + m) * kLdT + 16 * a + 4 * nq) =
+        make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
+  }
+  named_sync(1, kPrepCompute);
 }
 
 __global__ void __launch_bounds__(kPrepThreads, 1)
@@ -114,17 +154,17 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
   uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_addr(sm);
   float* beta_s = reinterpret_cast<float*>(sm + kP_beta);
-  float* Rs = reinterpret_cast<float*>(sm + kP_R);
-  float* GCs = reinterpret_cast<float*>(sm + kP_GC);
-  float* Lb = reinterpret_cast<float*>(sm + kP_L);
-  float* Ps = reinterpret_cast<float*>(sm + kP_P);
+  float* Tot = reinterpret_cast<float*>(sm + kP_Tot);
+  float* Lb = reinterpret_cast<float*>(sm + kP_Lb);
+  float* Tb = reinterpret_cast<float*>(sm + kP_Tb);
+  float* Ps = reinterpret_cast<float*>(sm + kP_Ps);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kP_bars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kP_bars + 32);
   const uint32_t bar_full = smem_addr(&bars[0]), bar_empty = smem_addr(&bars[1]);
   const uint32_t bar_p = smem_addr(&bars[2]), bar_w = smem_addr(&bars[3]);
   const int t = threadIdx.x, warp = t >> 5;
 
-  // the KC tiles keep zero rows beyond their tile for the whole kernel
+  // the KC tiles keep zero rows beyond their tile (re-zeroed after scratch use)
   for (uint32_t o = t * 16; o < 65536; o += kPrepThreads * 16)
     *reinterpret_cast<uint4*>(sm + kP_KC01 + o) = make_uint4(0, 0, 0, 0);
   if (t == 0) {
@@ -163,8 +203,10 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     }
   } else {
     // --------------------------------------------------------- compute warps
-    const int c = t & 127, hf = t >> 7;  // channel, row half (rows 32*hf .. 32*hf+31)
-    const int lane = t & 127;            // TMEM lane of this thread in the epilogues
+    // operand passes: thread -> channels (cp, cp+1), 16-token tile ta
+    const int cp = 2 * (t & 63), ta = t >> 6;
+    // epilogues: thread -> TMEM lane (t & 127), column half hf
+    const int lane = t & 127, hf = t >> 7;
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     const __nv_bfloat16* sK = reinterpret_cast<const __nv_bfloat16*>(sm + kI_K);
     const __nv_bfloat16* sQ = reinterpret_cast<const __nv_bfloat16*>(sm + kI_Q);
@@ -180,83 +222,88 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       bool ok = mbar_wait(bar_full, it & 1, err);
       if (!named_sync_and(1, kPrepCompute, ok)) break;
 
-      // ---- pass 1: running log-decay of channel c over this thread's 32 rows
-      float G[32];
+      // ---- pass 1: running log-decay inside this thread's tile, for both channels
+      float Gl[2][16];
       {
-        float acc = 0.f;
+        float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int r = 32 * hf + j;
-          acc += (r < len) ? sG[r * D + c] : 0.f;
-          G[j] = acc;
+        for (int j = 0; j < 16; ++j) {
+          const int r = 16 * ta + j;
+          const float2 gg = (r < len) ? *reinterpret_cast<const float2*>(sG + r * D + cp)
+                                      : make_float2(0.f, 0.f);
+          s0 += gg.x;
+          s1 += gg.y;
+          Gl[0][j] = s0;
+          Gl[1][j] = s1;
         }
-      }
-      if (hf == 0) {
-        Rs[c] = 0.f;
-        Rs[D + c] = G[15];
-        Rs[2 * D + c] = G[31];
+        *reinterpret_cast<float2*>(Tot + ta * D + cp) = make_float2(s0, s1);
       }
       named_sync(1, kPrepCompute);
-      if (hf == 1) {
-        const float off = Rs[2 * D + c];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) G[j] += off;
-        Rs[3 * D + c] = G[15];
-        GCs[c] = G[31];
-      }
-      named_sync(1, kPrepCompute);
-      const float R[4] = {Rs[c], Rs[D + c], Rs[2 * D + c], Rs[3 * D + c]};
-      const float GC = GCs[c];
 
-      // ---- pass 2: operands for this thread's two tiles
+      // ---- pass 2: operands for this thread's tile, one channel at a time
 #pragma unroll
-      for (int lt = 0; lt < 2; ++lt) {
-        const int a = 2 * hf + lt;
-        const float Ra = hf ? R[2 + lt] : R[lt];  // static indices: R stays in registers
-        float E[4];
+      for (int hq = 0; hq < 2; ++hq) {  // 8 rows = one 16-byte chunk per operand
+        float kr[2][8], qr[2][8], vr[2][8];
 #pragma unroll
-        for (int ap = 0; ap < 4; ++ap) E[ap] = (ap > a) ? __expf(R[ap] - Ra) : 1.f;
-        const float eRa = __expf(Ra);       // exp(R_a) <= 1
-        const float eCa = __expf(GC - Ra);  // exp(G_C - R_a) <= 1
+        for (int e = 0; e < 8; ++e) {
+          const int r = 16 * ta + 8 * hq + e;
+          uint32_t kw = 0, qw = 0, vw = 0;
+          if (r < len) {
+            kw = *reinterpret_cast<const uint32_t*>(sK + r * D + cp);
+            qw = *reinterpret_cast<const uint32_t*>(sQ + r * D + cp);
+            vw = *reinterpret_cast<const uint32_t*>(sV + r * D + cp);
+          }
+          kr[0][e] = bf16_lo(kw); kr[1][e] = bf16_hi(kw);
+          qr[0][e] = bf16_lo(qw); qr[1][e] = bf16_hi(qw);
+          vr[0][e] = bf16_lo(vw); vr[1][e] = bf16_hi(vw);
+        }
 #pragma unroll
-        for (int hq = 0; hq < 2; ++hq) {  // 8 rows = one 16-byte chunk per operand
+        for (int ch2 = 0; ch2 < 2; ++ch2) {
+          const int c = cp + ch2;
+          // tile references R_b = sum of the tile sums before tile b; G_C = all four
+          float R[4], GC = 0.f;
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            R[b] = GC;
+            GC += Tot[b * D + c];
+          }
+          const float Ra = ta == 0 ? R[0] : (ta == 1 ? R[1] : (ta == 2 ? R[2] : R[3]));
+          const float eRa = __expf(Ra);       // exp(R_a) <= 1
+          const float eCa = __expf(GC - Ra);  // exp(G_C - R_a) <= 1
           float kb[8], qb[8], kn[8], kg[8], vb[8], kt[8], qg[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const int j = 8 * hq + e, r = 16 * a + j;
-            const bool in = r < len;
-            const float kk = in ? __bfloat162float(sK[r * D + c]) : 0.f;
-            const float qq = in ? __bfloat162float(sQ[r * D + c]) : 0.f;
-            const float vv = in ? __bfloat162float(sV[r * D + c]) : 0.f;
-            const float d = G[16 * lt + j] - Ra;  // (-80, 0]
-            const float f = __expf(d), fi = __expf(-d);
-            kb[e] = kk * f;
-            qb[e] = qq * f;
-            kn[e] = kk * fi;
+            const int r = 16 * ta + 8 * hq + e;
+            const float dd = Gl[ch2][8 * hq + e];  // G_r - R_a, in (-80, 0]
+            const float f = __expf(dd), fi = __expf(-dd);
+            kb[e] = kr[ch2][e] * f;
+            qb[e] = qr[ch2][e] * f;
+            kn[e] = kr[ch2][e] * fi;
             kg[e] = kb[e] * eRa * beta_s[r];
-            vb[e] = vv * beta_s[r];
+            vb[e] = vr[ch2][e] * beta_s[r];
             kt[e] = kn[e] * eCa;
             qg[e] = qb[e] * eRa;
           }
-          *reinterpret_cast<uint4*>(sm + kP_Bop + mn_chunk(128, 4 * a + hq, c)) = pack8(kb);
-          *reinterpret_cast<uint4*>(sm + kP_Bop + mn_chunk(128, 4 * a + 2 + hq, c)) = pack8(qb);
+          *reinterpret_cast<uint4*>(sm + kP_Bop + mn_chunk(128, 4 * ta + hq, c)) = pack8(kb);
+          *reinterpret_cast<uint4*>(sm + kP_Bop + mn_chunk(128, 4 * ta + 2 + hq, c)) = pack8(qb);
 #pragma unroll
           for (int ap = 0; ap < 4; ++ap) {
-            if (ap < a) continue;
+            if (ap < ta) continue;
+            const float E = (ap > ta) ? __expf(R[ap] - Ra) : 1.f;  // exp(R_ap - R_a) <= 1
             float x[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = kn[e] * E[ap];
+            for (int e = 0; e < 8; ++e) x[e] = kn[e] * E;
             const uint32_t kc = (ap < 2) ? kP_KC01 : kP_KC23;
-            *reinterpret_cast<uint4*>(sm + kc + mn_chunk(128, 8 * (ap & 1) + 2 * a + hq, c)) =
+            *reinterpret_cast<uint4*>(sm + kc + mn_chunk(128, 8 * (ap & 1) + 2 * ta + hq, c)) =
                 pack8(x);
           }
-          *reinterpret_cast<uint4*>(sm + kP_BKg + sw128_chunk(128, c, 2 * a + hq)) = pack8(kg);
-          *reinterpret_cast<uint4*>(sm + kP_BV + sw128_chunk(128, c, 2 * a + hq)) = pack8(vb);
-          *reinterpret_cast<uint4*>(unit + kKT + sw128_chunk(128, c, 2 * a + hq)) = pack8(kt);
-          *reinterpret_cast<uint4*>(unit + kWQ + mn_chunk(128, 8 + 2 * a + hq, c)) = pack8(qg);
+          *reinterpret_cast<uint4*>(sm + kP_BKg + sw128_chunk(128, c, 2 * ta + hq)) = pack8(kg);
+          *reinterpret_cast<uint4*>(sm + kP_BV + sw128_chunk(128, c, 2 * ta + hq)) = pack8(vb);
+          *reinterpret_cast<uint4*>(unit + kKT + sw128_chunk(128, c, 2 * ta + hq)) = pack8(kt);
+          *reinterpret_cast<uint4*>(unit + kWQ + mn_chunk(128, 8 + 2 * ta + hq, c)) = pack8(qg);
+          if (ta == 0 && hq == 0) gam_out[(size_t)u * D + c] = __expf(GC);
         }
       }
-      if (hf == 0) gam_out[(size_t)u * D + c] = __expf(GC);
       mbar_arrive(bar_empty);  // the staged rows are consumed: the copy warp may refill
 
       // ---- block products: D[:, 0:64] = [KC0|KC1] x Bop[0:64]^T, D[:, 64:128] = [KC2|KC3] x Bop[64:128]^T
@@ -295,8 +342,9 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       }
       named_sync(1, kPrepCompute);
 
-      // ---- T = (I + L)^{-1}, blockwise over 16 x 16 blocks, fp32
-      if (t < C) {  // diagonal blocks: forward substitution, one column per thread
+      // ---- T = (I + L)^{-1} in fp32: diagonal 16x16 blocks by forward substitution
+      //      (one column per thread), then the three block-substitution stages
+      if (t < C) {
         const int ba = t >> 4, cc = t & 15, o = 16 * ba;
         float x[16];
 #pragma unroll
@@ -307,36 +355,20 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
           x[m] = (m < cc) ? 0.f : (m == cc ? 1.f : -acc);
         }
 #pragma unroll
-        for (int m = 0; m < 16; ++m)
-          if (m > cc) Lb[(o + cc) * kLdL + o + m] = x[m];
+        for (int m = 0; m < 16; ++m) Tb[(o + m) * kLdT + o + cc] = x[m];
       }
       named_sync(1, kPrepCompute);
-      // T_{a+d, a} = -T_{a+d, a+d} * (sum_{b=a}^{a+d-1} L_{a+d, b} T_{b, a}), d = 1, 2, 3
-#pragma unroll 1
-      for (int d = 1; d < 4; ++d) {
-        const int nblk = 4 - d;
-        for (int e = t; e < nblk * 256; e += kPrepCompute) {
-          const int a = e >> 8, m = (e >> 4) & 15, n = e & 15;
-          const int rr = 16 * (a + d) + m, cc = 16 * a + n;
-          float acc = 0.f;
-          for (int kk = cc; kk < 16 * (a + d); ++kk) acc = fmaf(Lb[rr * kLdL + kk], t_at(Lb, kk, cc), acc);
-          Ps[e] = acc;
-        }
-        named_sync(1, kPrepCompute);
-        for (int e = t; e < nblk * 256; e += kPrepCompute) {
-          const int a = e >> 8, m = (e >> 4) & 15, n = e & 15;
-          const int o = 16 * (a + d);
-          float acc = 0.f;
-          for (int kk = 0; kk <= m; ++kk) acc = fmaf(t_at(Lb, o + m, o + kk), Ps[(a << 8) | (kk << 4) | n], acc);
-          Lb[(16 * a + n) * kLdL + o + m] = -acc;
-        }
-        named_sync(1, kPrepCompute);
-      }
-      {  // T -> bf16 B operand (MN-major, X = row r, K = column j)
+      inverse_stage<1>(t, Lb, Tb, Ps);
+      inverse_stage<2>(t, Lb, Tb, Ps);
+      inverse_stage<3>(t, Lb, Tb, Ps);
+      {  // T -> bf16 B operand (MN-major, X = row r, K = column j); zero above the diagonal
         const int j = t >> 2, qq = t & 3;
         float x[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) x[e] = t_at(Lb, 16 * qq + e, j);
+        for (int e = 0; e < 16; ++e) {
+          const int r = 16 * qq + e;
+          x[e] = (r >= j) ? Tb[r * kLdT + j] : 0.f;
+        }
         *reinterpret_cast<uint4*>(sm + kP_T + mn_chunk(64, 2 * qq, j)) = pack8(x);
         *reinterpret_cast<uint4*>(sm + kP_T + mn_chunk(64, 2 * qq + 1, j)) = pack8(x + 8);
       }
@@ -354,6 +386,9 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                    mnmajor_desc(sbase + kP_T, 1024, s), id, s > 0);
         mma_commit(bar_w);
       }
+      // the KC scratch (L, T, products) goes back to zero for the next unit's KC rows
+      for (uint32_t o = t * 16; o < kScratchBytes; o += kPrepCompute * 16)
+        *reinterpret_cast<uint4*>(sm + kP_Lb + o) = make_uint4(0, 0, 0, 0);
       ok = mbar_wait(bar_w, it & 1, err);
       if (!named_sync_and(1, kPrepCompute, ok)) break;
       tc_fence_after();
@@ -555,33 +590,34 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       const int s = j % kStages;
       uint8_t* st = sm + s * kStageBytes;
       const float* gam_s = reinterpret_cast<const float*>(st + kUnitBytes);
-      // E0: S^T row -> bf16 operand copy, then S^T *= gamma_C (column-wise)
+      // E0: S^T row -> bf16 operand copy (MMA1 may start), then S^T *= gamma_C
       if (j > 0 && !wait_or_abort(bar_m2, (j - 1) & 1, err, abort_flag)) { alive = false; break; }
       if (!wait_or_abort(bar_full0 + 8 * s, (j / kStages) & 1, err, abort_flag)) { alive = false; break; }
       tc_fence_after();
-#pragma unroll
-      for (int qq = 0; qq < 2; ++qq) {
-        const int col = 64 * ch + 32 * qq;
-        float sv[32];
-        tmem_ld32(lrow + col, sv);
+      {
+        float sv[2][32];
+        tmem_ld32(lrow + 64 * ch, sv[0]);
+        tmem_ld32(lrow + 64 * ch + 32, sv[1]);
         tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          *reinterpret_cast<uint4*>(sm + kC_Sbf + sw128_chunk(128, lane, col / 8 + e)) =
-              pack8(&sv[8 * e]);
+        for (int e = 0; e < 8; ++e)
+          *reinterpret_cast<uint4*>(sm + kC_Sbf + sw128_chunk(128, lane, 8 * ch + e)) =
+              pack8(&sv[e >> 2][8 * (e & 3)]);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar_s);
+        // the scaled state is ordered before MMA2 by the Vt-ready barrier below
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          const float4 gm = *reinterpret_cast<const float4*>(gam_s + col + i);
-          sv[i] *= gm.x; sv[i + 1] *= gm.y; sv[i + 2] *= gm.z; sv[i + 3] *= gm.w;
+        for (int qq = 0; qq < 2; ++qq) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const float4 gm = *reinterpret_cast<const float4*>(gam_s + 64 * ch + 32 * qq + i);
+            sv[qq][i] *= gm.x; sv[qq][i + 1] *= gm.y; sv[qq][i + 2] *= gm.z; sv[qq][i + 3] *= gm.w;
+          }
+          tmem_st32(lrow + 64 * ch + 32 * qq, sv[qq]);
         }
-        tmem_st32(lrow + col, sv);
+        tmem_wait_st();
       }
-      tmem_wait_st();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar_s);
-      // E2 of the previous chunk (its D1 buffer is not touched by MMA1 of this chunk)
-      if (j > 0 && !store_o(j - 1)) { alive = false; break; }
       // E1: Vt^T = U^T - (W S)^T on this thread's 32 tokens
       if (!wait_or_abort(bar_m1, j & 1, err, abort_flag)) { alive = false; break; }
       tc_fence_after();
@@ -605,6 +641,9 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar_vt);
+      // E2 of the previous chunk, overlapping MMA2 (MMA1 of this chunk used the
+      // other D1 buffer; MMA1 of the next chunk waits for this thread's next E0)
+      if (j > 0 && !store_o(j - 1)) { alive = false; break; }
     }
     if (alive && nch > 0 && wait_or_abort(bar_m2, (nch - 1) & 1, err, abort_flag)) {
       tc_fence_after();
