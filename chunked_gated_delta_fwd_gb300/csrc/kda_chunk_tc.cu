@@ -37,6 +37,10 @@
 #include "kda_internal.cuh"
 #include "kda_sm100.cuh"
 
+#include <cuda.h>
+
+#include <mutex>
+
 namespace kda {
 namespace {
 
@@ -56,7 +60,7 @@ constexpr uint32_t kGamBytes = D * 4;
 // ============================================================== prep kernel
 constexpr int kPrepCompute = 256;                // 8 compute warps
 constexpr int kPrepThreads = kPrepCompute + 32;  // + the copy warp
-constexpr uint32_t kInRowBytes = 3 * 256 + 512;  // k, q, v (bf16) and g (fp32) per token
+constexpr uint32_t kInUnitBytes = C * (3 * 256 + 512);  // k, q, v (bf16) and g (fp32) boxes
 // shared memory (offsets from a 1024-aligned base)
 constexpr uint32_t kI_K = 0, kI_Q = 16384, kI_V = 32768, kI_G = 49152;  // staged rows
 constexpr uint32_t kP_Bop = 81920;         // MN-major X=128 (Kb/Qb rows), K=128
@@ -146,8 +150,8 @@ __device__ __forceinline__ void inverse_stage(int t, const float* Lb, float* Tb,
 }
 
 __global__ void __launch_bounds__(kPrepThreads, 1)
-    tc_prep(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-            const __nv_bfloat16* __restrict__ v, const float* __restrict__ g,
+    tc_prep(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
+            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
             const __nv_bfloat16* __restrict__ beta, Plan plan, int H, int64_t units_ub,
             uint8_t* __restrict__ tiles, float* __restrict__ gam_out, int* err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -183,20 +187,21 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
 
   if (warp == kPrepCompute / 32) {
     // ------------------------------------------------------------ copy warp
+    // One tensor copy per input per unit: 64 tokens x 1 head x 128 channels.
+    // Tokens past the end of the packed batch arrive as zeros; tokens of the
+    // next sequence are masked by the compute warps.
     if ((t & 31) == 0) {
       uint32_t it = 0;
       for (int64_t u = blockIdx.x; u < units_ub; u += gridDim.x, ++it) {
         const UnitInfo ui = unit_info(plan, H, u);
         if (ui.chunk >= total) break;
         if (it > 0 && !mbar_wait(bar_empty, (it - 1) & 1, err)) break;
-        mbar_arrive_expect_tx(bar_full, (uint32_t)ui.len * kInRowBytes);
-        for (int r = 0; r < ui.len; ++r) {
-          const int64_t row = (ui.t0 + r) * H + ui.h;
-          bulk_g2s(sbase + kI_K + r * 256, k + row * D, 256, bar_full);
-          bulk_g2s(sbase + kI_Q + r * 256, q + row * D, 256, bar_full);
-          bulk_g2s(sbase + kI_V + r * 256, v + row * D, 256, bar_full);
-          bulk_g2s(sbase + kI_G + r * 512, g + row * D, 512, bar_full);
-        }
+        mbar_arrive_expect_tx(bar_full, kInUnitBytes);
+        const int t0 = (int)ui.t0;
+        tma_load_3d(sbase + kI_K, &tm_k, 0, ui.h, t0, bar_full);
+        tma_load_3d(sbase + kI_Q, &tm_q, 0, ui.h, t0, bar_full);
+        tma_load_3d(sbase + kI_V, &tm_v, 0, ui.h, t0, bar_full);
+        tma_load_3d(sbase + kI_G, &tm_g, 0, ui.h, t0, bar_full);
       }
       // copies still in flight must land before the CTA may exit
       if (it > 0) mbar_wait(bar_full, (it - 1) & 1, nullptr);
@@ -672,6 +677,41 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   }
 }
 
+// cuTensorMapEncodeTiled, resolved once through the runtime's driver entry points
+// (the library does not link libcuda directly).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &qr) == cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Tensor map over a token-major [NT][H][128] tensor: boxes of 64 tokens of one head.
+cudaError_t encode_rows(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int esz,
+                        int H, int64_t n_tokens) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)n_tokens};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * esz, (cuuint64_t)H * D * esz};
+  const cuuint32_t box[3] = {(cuuint32_t)D, 1u, (cuuint32_t)C};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUresult r = fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 int sm_count() {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
@@ -701,15 +741,21 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
   float* gam = reinterpret_cast<float*>(tiles + (size_t)units * kUnitBytes);
   cudaError_t e;
   using T = __nv_bfloat16;
-  if (units > 0) {
+  if (units > 0 && n_tokens > 0) {  // with no tokens there are no chunks to prepare
     e = cudaFuncSetAttribute(tc_prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kP_Smem);
     if (e != cudaSuccess) return e;
     const int sms = sm_count();
     const int grid = (int)(units < sms ? units : sms);
+    CUtensorMap tm[4];
+    e = encode_rows(&tm[0], k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n_tokens);
+    if (e == cudaSuccess) e = encode_rows(&tm[1], q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n_tokens);
+    if (e == cudaSuccess) e = encode_rows(&tm[2], v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n_tokens);
+    if (e == cudaSuccess) e = encode_rows(&tm[3], g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, n_tokens);
+    if (e != cudaSuccess) return e;
     ProfScope prof_scope("kda_tc_prep", s);
-    tc_prep<<<grid, kPrepThreads, kP_Smem, s>>>(
-        static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), g,
-        static_cast<const T*>(beta), plan, H, units, tiles, gam, err);
+    tc_prep<<<grid, kPrepThreads, kP_Smem, s>>>(tm[0], tm[1], tm[2], tm[3],
+                                                 static_cast<const T*>(beta), plan, H, units,
+                                                 tiles, gam, err);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
