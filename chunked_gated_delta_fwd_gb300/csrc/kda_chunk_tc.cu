@@ -426,15 +426,18 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
 }
 
 // ============================================================= chain kernel
-constexpr int kStages = 2;
+constexpr int kStages = 3;
 constexpr uint32_t kStageBytes = 75776;             // unit (72 KB) + gamma (512 B), 1024-aligned
-constexpr uint32_t kC_Sbf = kStages * kStageBytes;  // S^T bf16, K-major 128 x 128 (32 KB)
-constexpr uint32_t kC_Vt = kC_Sbf + 32768;          // Vt^T bf16, K-major 128 x 64 (16 KB)
-constexpr uint32_t kC_O = kC_Vt + 16384;            // O staging, [64][128] bf16 row-major
-constexpr uint32_t kC_bars = kC_O + 16384;
+constexpr uint32_t kC_bars = kStages * kStageBytes;
+// TMEM columns: S^T fp32 [0,128); two D1 buffers [128,256), [256,384); the bf16 A
+// operands of MMA1 (S^T, packed pairs, [384,448)) and MMA2 (Vt^T, two buffers of 32
+// columns at [448,512)).
+constexpr uint32_t kT_SB = 384, kT_VT = 448;
 constexpr uint32_t kC_Smem = kC_bars + 128 + 1024;
-constexpr int kEpi = 256;                 // epilogue: (TMEM lane, column half)
-constexpr int kChainThreads = kEpi + 32;  // + copy/MMA warp
+constexpr int kEpi = 256;    // epilogue warps 0-7: (TMEM lane, column half)
+constexpr int kStore = 128;  // store warps 8-11: TMEM lane = value row, all 64 tokens
+constexpr int kMmaWarp = (kEpi + kStore) / 32;  // warp 12: copies + MMA issue
+constexpr int kChainThreads = kEpi + kStore + 32;
 
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int* err,
                                               volatile int* abort_flag) {
@@ -461,14 +464,16 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_addr(sm);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kC_bars);
-  // bars: 0,1 = full[stage], 2 = S ready (bf16 copy written, S scaled), 3 = MMA1 done,
-  //       4 = Vt ready, 5 = MMA2 done, 6 = O staging written, 7 = O staging read
+  // bars: 0..2 = full[stage], 3 = S copy ready, 4 = MMA1 done, 5 = Vt ready (S scaled),
+  //       6 = S update done, 7,8 = O of D1 buffer b final, 9,10 = D1 buffer b read out,
+  //       11 = drain (abort path)
   const uint32_t bar_full0 = smem_addr(&bars[0]);
-  const uint32_t bar_s = smem_addr(&bars[2]), bar_m1 = smem_addr(&bars[3]);
-  const uint32_t bar_vt = smem_addr(&bars[4]), bar_m2 = smem_addr(&bars[5]);
-  const uint32_t bar_ow = smem_addr(&bars[6]), bar_or = smem_addr(&bars[7]);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kC_bars + 64);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kC_bars + 72);
+  const uint32_t bar_s = smem_addr(&bars[3]), bar_m1 = smem_addr(&bars[4]);
+  const uint32_t bar_vt = smem_addr(&bars[5]), bar_m2 = smem_addr(&bars[6]);
+  const uint32_t bar_o0 = smem_addr(&bars[7]), bar_f0 = smem_addr(&bars[9]);
+  const uint32_t bar_dr = smem_addr(&bars[11]);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kC_bars + 96);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kC_bars + 104);
   const int t = threadIdx.x, warp = t >> 5;
   const int n = blockIdx.x, h = blockIdx.y;
 
@@ -478,8 +483,11 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     mbar_init(bar_m1, 1);
     mbar_init(bar_vt, kEpi);
     mbar_init(bar_m2, 1);
-    mbar_init(bar_ow, kEpi);
-    mbar_init(bar_or, kEpi);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_o0 + 8 * b, 1);
+      mbar_init(bar_f0 + 8 * b, kStore);
+    }
+    mbar_init(bar_dr, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -494,7 +502,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   const int64_t tend = max(tstart, (int64_t)__ldg(plan.cu + n + 1));
   const int64_t state = ((int64_t)n * H + h) * D * D;
 
-  if (warp == kEpi / 32) {
+  if (warp == kMmaWarp) {
     // ------------------------------------------------ copies + MMA issue (one thread)
     if ((t & 31) == 0) {
       auto issue = [&](int jj) {
@@ -511,41 +519,66 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       const uint32_t id2a = idesc_bf16_mn(128, 64, 0, 1);   // Vt^T x A_qk (MN-major B)
       const uint32_t id2b = idesc_bf16_mn(128, 128, 0, 0);  // Vt^T x Kt^T (K-major B)
       int j = 0;
-      bool mma_pending = false;
+      bool any_mma = false;
+      // O^T += Vt^T A_qk^T of chunk jj, issued one chunk late (after the next chunk's
+      // MMA1), where it measured faster than right after the state update.
+      auto o_mma = [&](int jj) {
+        const uint32_t stj = sbase + (jj % kStages) * kStageBytes;
+        const uint32_t d1j = tmem + 128 + 128 * (jj & 1);
+        for (int ks = 0; ks < C / 16; ++ks)
+          mma_bf16_ta(d1j + 64, tmem + kT_VT + 32 * (jj & 1) + 8 * ks,
+                      mnmajor_desc(stj + kAQ, 1024, ks), id2a, 1u);
+        mma_commit(bar_o0 + 8 * (jj & 1));  // every MMA of chunk jj is complete
+      };
+      // the stage of chunk jj is refilled once every MMA of chunk jj has read it (done
+      // one chunk later, when that is certainly the case)
+      auto refill = [&](int jj) -> bool {
+        if (jj + kStages >= nch) return true;
+        if (!wait_or_abort(bar_o0 + 8 * (jj & 1), (jj >> 1) & 1, err, abort_flag)) return false;
+        issue(issued++);
+        return true;
+      };
       for (; j < nch; ++j) {
         const int s = j % kStages;
         const uint32_t st = sbase + s * kStageBytes;
         if (!wait_or_abort(bar_s, j & 1, err, abort_flag)) break;
         if (!wait_or_abort(bar_full0 + 8 * s, (j / kStages) & 1, err, abort_flag)) break;
         consumed = j + 1;
+        // D1 buffer j&1 must have been read out by the store warps (chunk j-2)
+        if (j >= 2 && !wait_or_abort(bar_f0 + 8 * (j & 1), ((j - 2) >> 1) & 1, err, abort_flag))
+          break;
         tc_fence_after();
         const uint32_t d1 = tmem + 128 + 128 * (j & 1);
+        // (W S)^T | (Gamma Q S)^T in one N = 128 product, A = bf16 S^T from TMEM
         for (int ks = 0; ks < D / 16; ++ks)
-          mma_bf16(d1, kmajor_desc(sbase + kC_Sbf, 128, ks), mnmajor_desc(st + kWQ, 2048, ks), id1,
-                   ks > 0);
+          mma_bf16_ta(d1, tmem + kT_SB + 8 * ks, mnmajor_desc(st + kWQ, 2048, ks), id1, ks > 0);
         mma_commit(bar_m1);
-        if (!wait_or_abort(bar_vt, j & 1, err, abort_flag)) { mma_pending = true; break; }
+        any_mma = true;
+        if (j > 0) o_mma(j - 1);
+        if (!wait_or_abort(bar_vt, j & 1, err, abort_flag)) break;
         tc_fence_after();
+        // S^T += Vt^T Kt (the scaled state is ordered by the Vt barrier)
         for (int ks = 0; ks < C / 16; ++ks)
-          mma_bf16(d1 + 64, kmajor_desc(sbase + kC_Vt, 128, ks), mnmajor_desc(st + kAQ, 1024, ks),
-                   id2a, 1u);
-        for (int ks = 0; ks < C / 16; ++ks)
-          mma_bf16(tmem + 0, kmajor_desc(sbase + kC_Vt, 128, ks), kmajor_desc(st + kKT, 128, ks),
-                   id2b, 1u);
+          mma_bf16_ta(tmem + 0, tmem + kT_VT + 32 * (j & 1) + 8 * ks,
+                      kmajor_desc(st + kKT, 128, ks), id2b, 1u);
         mma_commit(bar_m2);
-        if (j + kStages < nch) {
-          if (!wait_or_abort(bar_m2, j & 1, err, abort_flag)) { mma_pending = true; break; }
-          issue(issued++);
-        }
+        if (j > 0 && !refill(j - 1)) break;
+      }
+      if (!*abort_flag && nch > 0) {
+        o_mma(nch - 1);
+        refill(nch - 1);
       }
       if (*abort_flag) {
         // drain: copies and MMAs already issued must land before the CTA exits
         for (int jj = consumed; jj < issued; ++jj)
           mbar_wait(bar_full0 + 8 * (jj % kStages), (jj / kStages) & 1, nullptr);
-        if (mma_pending) mbar_wait(bar_m2, j & 1, nullptr);
+        if (any_mma) {
+          mma_commit(bar_dr);
+          mbar_wait(bar_dr, 0, nullptr);
+        }
       }
     }
-  } else {
+  } else if (warp < kEpi / 32) {
     // ------------------------- epilogue warps: TMEM lane = dv, ch = column half
     const int lane = t & 127, ch = t >> 7;
     const uint32_t lrow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
@@ -568,28 +601,6 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       }
       tmem_wait_st();
     }
-    __nv_bfloat16* Ost = reinterpret_cast<__nv_bfloat16*>(sm + kC_O);
-    auto store_o = [&](int jj) -> bool {
-      // staging handoff on mbarriers (bounded waits): written -> read -> reusable
-      if (jj > 0 && !wait_or_abort(bar_or, (jj - 1) & 1, err, abort_flag)) return false;
-      float ov[32];
-      tmem_ld32(lrow + 128 + 128 * (jj & 1) + 64 + 32 * ch, ov);
-      tmem_wait_ld();
-#pragma unroll
-      for (int e = 0; e < 32; ++e) Ost[(32 * ch + e) * D + lane] = __float2bfloat16_rn(ov[e]);
-      mbar_arrive(bar_ow);
-      if (!wait_or_abort(bar_ow, jj & 1, err, abort_flag)) return false;
-      const int64_t tc = tstart + (int64_t)jj * C;
-#pragma unroll
-      for (int qq = 0; qq < 4; ++qq) {
-        const int id = t + kEpi * qq, r = id >> 4, cc = id & 15;
-        if (tc + r < tend)
-          *reinterpret_cast<uint4*>(o + ((tc + r) * H + h) * D + 8 * cc) =
-              *reinterpret_cast<const uint4*>(Ost + r * D + 8 * cc);
-      }
-      mbar_arrive(bar_or);
-      return true;
-    };
     bool alive = true;
     for (int j = 0; j < nch && alive; ++j) {
       const int s = j % kStages;
@@ -604,11 +615,13 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         tmem_ld32(lrow + 64 * ch, sv[0]);
         tmem_ld32(lrow + 64 * ch + 32, sv[1]);
         tmem_wait_ld();
+        {
+          uint32_t pk[32];  // bf16 pairs of this thread's 64 columns of S^T
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          *reinterpret_cast<uint4*>(sm + kC_Sbf + sw128_chunk(128, lane, 8 * ch + e)) =
-              pack8(&sv[e >> 2][8 * (e & 3)]);
-        fence_proxy_async_smem();
+          for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(sv[e >> 4][2 * (e & 15)], sv[e >> 4][2 * (e & 15) + 1]);
+          tmem_st32u(lrow + kT_SB + 32 * ch, pk);
+        }
+        tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar_s);
         // the scaled state is ordered before MMA2 by the Vt-ready barrier below
@@ -630,30 +643,24 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         float wsv[32];
         tmem_ld32(lrow + 128 + 128 * (j & 1) + 32 * ch, wsv);
         tmem_wait_ld();
+        uint32_t pk[16];  // bf16 pairs of this thread's 32 tokens of Vt^T
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const uint4 uu = *reinterpret_cast<const uint4*>(st + kUT + sw128_chunk(128, lane, 4 * ch + e));
           const uint32_t uw[4] = {uu.x, uu.y, uu.z, uu.w};
-          float x[8];
 #pragma unroll
-          for (int p = 0; p < 4; ++p) {
-            x[2 * p] = bf16_lo(uw[p]) - wsv[8 * e + 2 * p];
-            x[2 * p + 1] = bf16_hi(uw[p]) - wsv[8 * e + 2 * p + 1];
-          }
-          *reinterpret_cast<uint4*>(sm + kC_Vt + sw128_chunk(128, lane, 4 * ch + e)) = pack8(x);
+          for (int p = 0; p < 4; ++p)
+            pk[4 * e + p] = pack_bf16(bf16_lo(uw[p]) - wsv[8 * e + 2 * p],
+                                      bf16_hi(uw[p]) - wsv[8 * e + 2 * p + 1]);
         }
+        tmem_st16(lrow + kT_VT + 32 * (j & 1) + 16 * ch, pk);
+        tmem_wait_st();
       }
-      fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar_vt);
-      // E2 of the previous chunk, overlapping MMA2 (MMA1 of this chunk used the
-      // other D1 buffer; MMA1 of the next chunk waits for this thread's next E0)
-      if (j > 0 && !store_o(j - 1)) { alive = false; break; }
     }
-    if (alive && nch > 0 && wait_or_abort(bar_m2, (nch - 1) & 1, err, abort_flag)) {
+    if (alive && nch > 0 && wait_or_abort(bar_m2, (nch - 1) & 1, err, abort_flag))
       tc_fence_after();
-      store_o(nch - 1);
-    }
     if (hT && !*abort_flag) {
       tc_fence_after();
 #pragma unroll
@@ -667,6 +674,30 @@ __global__ void __launch_bounds__(kChainThreads, 1)
           *reinterpret_cast<float4*>(hT + state + (int64_t)lane * D + col + i) =
               make_float4(sv[i], sv[i + 1], sv[i + 2], sv[i + 3]);
       }
+    }
+  } else {
+    // ------------------------- store warps: o rows of each chunk, off the serial path
+    // Thread = value row dv; it reads the 64 outputs of its row from the chunk's D1
+    // buffer and writes them (2-byte stores, 64 contiguous bytes per warp), then
+    // frees the buffer for MMA1 two chunks later.
+    const int dv = t - kEpi;
+    const uint32_t lrow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    for (int j = 0; j < nch; ++j) {
+      const int b = j & 1;
+      if (!wait_or_abort(bar_o0 + 8 * b, (j >> 1) & 1, err, abort_flag)) break;
+      tc_fence_after();
+      float ov[2][32];
+      const uint32_t d1 = lrow + 128 + 128 * b + 64;
+      tmem_ld32(d1, ov[0]);
+      tmem_ld32(d1 + 32, ov[1]);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar_f0 + 8 * b);
+      const int64_t tc = tstart + (int64_t)j * C;
+      __nv_bfloat16* orow = o + (tc * H + h) * D + dv;
+#pragma unroll
+      for (int r = 0; r < C; ++r)
+        if (tc + r < tend) orow[(int64_t)r * H * D] = __float2bfloat16_rn(ov[r >> 5][r & 31]);
     }
   }
   tc_fence_before();
