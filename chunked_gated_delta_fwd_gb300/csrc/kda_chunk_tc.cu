@@ -50,7 +50,8 @@ constexpr int C = kChunk;  // 64
 constexpr int D = kD;      // 128
 
 // ---- workspace unit (bytes)
-constexpr uint32_t kWQ = 0;        // MN-major X=128 (tokens), K=128: 32 KB
+constexpr uint32_t kW = 0;         // MN-major X=64 (tokens), K=128: 16 KB
+constexpr uint32_t kQ = 16384;     // same layout; [W | Q] read as one X=128 operand
 constexpr uint32_t kUT = 32768;    // K-major 128 rows x 64: 16 KB
 constexpr uint32_t kAQ = 49152;    // MN-major X=64 (rows r), K=64 (columns i): 8 KB
 constexpr uint32_t kKT = 57344;    // K-major 128 rows x 64: 16 KB
@@ -58,13 +59,14 @@ constexpr uint32_t kUnitBytes = 73728;
 constexpr uint32_t kGamBytes = D * 4;
 
 // ============================================================== prep kernel
-constexpr int kPrepCompute = 256;                // 8 compute warps
-constexpr int kPrepThreads = kPrepCompute + 32;  // + the copy warp
+constexpr int kPrepCompute = 512;                // 16 warps; thread 0 also issues the copies
+constexpr int kPrepThreads = kPrepCompute;
 constexpr uint32_t kInUnitBytes = C * (3 * 256 + 512);  // k, q, v (bf16) and g (fp32) boxes
 // shared memory (offsets from a 1024-aligned base)
 constexpr uint32_t kI_K = 0, kI_Q = 16384, kI_V = 32768, kI_G = 49152;  // staged rows
 constexpr uint32_t kP_Bop = 81920;         // MN-major X=128 (Kb/Qb rows), K=128
 constexpr uint32_t kP_T = kP_Bop;          //   reused after the products: bf16 T, MN-major 64x64
+constexpr uint32_t kP_AQs = kP_Bop + 8192;  //   and the A_qk tile on its way out
 constexpr uint32_t kP_KC01 = 114688;       // MN-major X=128 ([KC(0) | KC(1)] rows), K=128
 constexpr uint32_t kP_KC23 = 147456;       // [KC(2) | KC(3)]
 // reused after the products (re-zeroed before the next unit's operands):
@@ -75,9 +77,9 @@ constexpr uint32_t kScratchBytes = 16640 + 17408 + 3072;
 constexpr uint32_t kP_BKg = 180224;        // K-major (beta Gamma K)^T 128 x 64
 constexpr uint32_t kP_BV = 196608;         // K-major (beta V)^T 128 x 64
 constexpr uint32_t kP_beta = 212992;       // 64 fp32
-constexpr uint32_t kP_Tot = kP_beta + 256; // per-tile sums of g, [4][128] fp32
-constexpr uint32_t kP_bars = kP_Tot + 2048;  // in_full, in_empty, p, w + TMEM base
-constexpr uint32_t kP_Smem = kP_bars + 64 + 1024;
+constexpr uint32_t kP_Tot = kP_beta + 256; // per-half-tile sums of g, [8][128] fp32
+constexpr uint32_t kP_bars = kP_Tot + 4096;  // in_full, (unused), p, w + TMEM base
+constexpr uint32_t kP_Smem = kP_bars + 128 + 1024;
 constexpr int kLdL = 65, kLdT = 68;
 
 __device__ __forceinline__ uint4 pack8(const float* x) {
@@ -164,7 +166,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
   float* Ps = reinterpret_cast<float*>(sm + kP_Ps);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kP_bars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kP_bars + 32);
-  const uint32_t bar_full = smem_addr(&bars[0]), bar_empty = smem_addr(&bars[1]);
+  const uint32_t bar_full = smem_addr(&bars[0]);
   const uint32_t bar_p = smem_addr(&bars[2]), bar_w = smem_addr(&bars[3]);
   const int t = threadIdx.x, warp = t >> 5;
 
@@ -173,7 +175,6 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     *reinterpret_cast<uint4*>(sm + kP_KC01 + o) = make_uint4(0, 0, 0, 0);
   if (t == 0) {
     mbar_init(bar_full, 1);
-    mbar_init(bar_empty, kPrepCompute);
     mbar_init(bar_p, 1);
     mbar_init(bar_w, 1);
     mbar_fence_init();
@@ -185,131 +186,185 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const int total = __ldg(plan.chunk_off + plan.n_seqs);
 
-  if (warp == kPrepCompute / 32) {
-    // ------------------------------------------------------------ copy warp
-    // One tensor copy per input per unit: 64 tokens x 1 head x 128 channels.
-    // Tokens past the end of the packed batch arrive as zeros; tokens of the
-    // next sequence are masked by the compute warps.
-    if ((t & 31) == 0) {
-      uint32_t it = 0;
-      for (int64_t u = blockIdx.x; u < units_ub; u += gridDim.x, ++it) {
-        const UnitInfo ui = unit_info(plan, H, u);
-        if (ui.chunk >= total) break;
-        if (it > 0 && !mbar_wait(bar_empty, (it - 1) & 1, err)) break;
-        mbar_arrive_expect_tx(bar_full, kInUnitBytes);
+  // Inputs: one tensor copy per input per unit (64 tokens x 1 head x 128
+  // channels) into the single staging buffer. Thread kIssuer issues unit n+1's
+  // copies as soon as every thread has read unit n's rows into registers.
+  // Unit positions run two units ahead in a two-slot ring (slot n & 1): while
+  // warps 0-1 invert unit n's diagonal blocks, warps 2-3 fetch beta of unit
+  // n+1 and the position of unit n+2, and thread kPrefetcher warms L2 with
+  // unit n+2's rows, so no global-load latency sits on the critical path.
+  // Tokens past the end of the packed batch arrive as zeros; tokens of the
+  // next sequence are masked below.
+  constexpr int kIssuer = 64, kLocator = 96, kPrefetcher = 128, kStorer = 192;
+  UnitInfo* slots = reinterpret_cast<UnitInfo*>(sm + kP_bars + 64);
+  uint32_t issued = 0;  // copies issued (thread kIssuer)
+  float beta_nx = 0.f;  // beta of token t - 64 of the next unit (threads 64..127)
+  auto locate = [&](int64_t u) {
+    UnitInfo ui;
+    if (u < units_ub) ui = unit_info(plan, H, u); else ui.chunk = total;
+    return ui;
+  };
+  auto issue_copies = [&](const UnitInfo& ui) {
+    if (ui.chunk >= total) return;
+    mbar_arrive_expect_tx(bar_full, kInUnitBytes);
+    const int t0 = (int)ui.t0;
+    tma_load_3d(sbase + kI_K, &tm_k, 0, ui.h, t0, bar_full);
+    tma_load_3d(sbase + kI_Q, &tm_q, 0, ui.h, t0, bar_full);
+    tma_load_3d(sbase + kI_V, &tm_v, 0, ui.h, t0, bar_full);
+    tma_load_3d(sbase + kI_G, &tm_g, 0, ui.h, t0, bar_full);
+    ++issued;
+  };
+  // warps 2-3 (+ kPrefetcher): beta of unit `un` (slot sn), position of unit `uf` into slot sf
+  auto fetch_ahead = [&](const UnitInfo& un, int64_t uf, int sf) {
+    if (t >= 64 && t < 128) {
+      beta_nx = (un.chunk < total && t - 64 < un.len)
+                    ? __bfloat162float(beta[(un.t0 + t - 64) * H + un.h]) : 0.f;
+      if (t == kLocator) slots[sf] = locate(uf);
+    } else if (t == kPrefetcher) {
+      const UnitInfo ui = locate(uf);
+      if (ui.chunk < total) {
         const int t0 = (int)ui.t0;
-        tma_load_3d(sbase + kI_K, &tm_k, 0, ui.h, t0, bar_full);
-        tma_load_3d(sbase + kI_Q, &tm_q, 0, ui.h, t0, bar_full);
-        tma_load_3d(sbase + kI_V, &tm_v, 0, ui.h, t0, bar_full);
-        tma_load_3d(sbase + kI_G, &tm_g, 0, ui.h, t0, bar_full);
+        tma_prefetch_l2_3d(&tm_k, 0, ui.h, t0);
+        tma_prefetch_l2_3d(&tm_q, 0, ui.h, t0);
+        tma_prefetch_l2_3d(&tm_v, 0, ui.h, t0);
+        tma_prefetch_l2_3d(&tm_g, 0, ui.h, t0);
       }
-      // copies still in flight must land before the CTA may exit
-      if (it > 0) mbar_wait(bar_full, (it - 1) & 1, nullptr);
     }
-  } else {
+  };
+  if (t == kLocator) {
+    const UnitInfo u0 = locate(blockIdx.x);
+    slots[0] = u0;
+    slots[1] = locate(blockIdx.x + gridDim.x);
+  }
+  named_sync(1, kPrepCompute);
+  if (t == kIssuer) issue_copies(slots[0]);
+  fetch_ahead(slots[0], blockIdx.x + gridDim.x, 1);  // slot 1 is rewritten with the same position
+  named_sync(1, kPrepCompute);
+  uint32_t it = 0;
+  {
     // --------------------------------------------------------- compute warps
-    // operand passes: thread -> channels (cp, cp+1), 16-token tile ta
-    const int cp = 2 * (t & 63), ta = t >> 6;
-    // epilogues: thread -> TMEM lane (t & 127), column half hf
-    const int lane = t & 127, hf = t >> 7;
+    // operand passes: thread -> channel pair (cp, cp+1), 8-token half hq of tile ta.
+    // The two channels are visited in a per-thread order (sw) so that each warp's
+    // 16-byte stores cover all eight 16-byte positions of the swizzle pattern.
+    const int pr = t & 63, rg = t >> 6, ta = rg >> 1, hq = rg & 1;
+    const int cp = 2 * pr, sw = (pr >> 2) & 1;
+    // read-outs: thread -> TMEM lane (t & 127), column quarter q4
+    const int lane = t & 127, q4 = t >> 7;
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     const __nv_bfloat16* sK = reinterpret_cast<const __nv_bfloat16*>(sm + kI_K);
     const __nv_bfloat16* sQ = reinterpret_cast<const __nv_bfloat16*>(sm + kI_Q);
     const __nv_bfloat16* sV = reinterpret_cast<const __nv_bfloat16*>(sm + kI_V);
     const float* sG = reinterpret_cast<const float*>(sm + kI_G);
-    uint32_t it = 0;
     for (int64_t u = blockIdx.x; u < units_ub; u += gridDim.x, ++it) {
-      const UnitInfo ui = unit_info(plan, H, u);
+      const UnitInfo ui = slots[it & 1];
       if (ui.chunk >= total) break;
       const int len = ui.len;
       uint8_t* unit = tiles + (size_t)u * kUnitBytes;
-      if (t < C) beta_s[t] = (t < len) ? __bfloat162float(beta[(ui.t0 + t) * H + ui.h]) : 0.f;
+      if (t >= 64 && t < 128) beta_s[t - 64] = beta_nx;
+      if (t == kStorer) bulk_wait_read_all();  // the staging space is rewritten below
       bool ok = mbar_wait(bar_full, it & 1, err);
       if (!named_sync_and(1, kPrepCompute, ok)) break;
 
-      // ---- pass 1: running log-decay inside this thread's tile, for both channels
-      float Gl[2][16];
+      // ---- pass 1: running log-decay over this thread's 8 rows, both channels
+      const int r0 = 16 * ta + 8 * hq;
+      float Gl[2][8];
       {
         float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int r = 16 * ta + j;
+        for (int e = 0; e < 8; ++e) {
+          const int r = r0 + e;
           const float2 gg = (r < len) ? *reinterpret_cast<const float2*>(sG + r * D + cp)
                                       : make_float2(0.f, 0.f);
           s0 += gg.x;
           s1 += gg.y;
-          Gl[0][j] = s0;
-          Gl[1][j] = s1;
+          Gl[0][e] = s0;
+          Gl[1][e] = s1;
         }
-        *reinterpret_cast<float2*>(Tot + ta * D + cp) = make_float2(s0, s1);
+        *reinterpret_cast<float2*>(Tot + rg * D + cp) = make_float2(s0, s1);
       }
       named_sync(1, kPrepCompute);
 
-      // ---- pass 2: operands for this thread's tile, one channel at a time
+      // ---- pass 2: operands of this thread's 8 rows, one channel at a time
+      uint32_t kw[8], qw[8], vw[8];
+      float bt[8];
 #pragma unroll
-      for (int hq = 0; hq < 2; ++hq) {  // 8 rows = one 16-byte chunk per operand
-        float kr[2][8], qr[2][8], vr[2][8];
+      for (int e = 0; e < 8; ++e) {
+        const int r = r0 + e;
+        const bool in = r < len;
+        kw[e] = in ? *reinterpret_cast<const uint32_t*>(sK + r * D + cp) : 0u;
+        qw[e] = in ? *reinterpret_cast<const uint32_t*>(sQ + r * D + cp) : 0u;
+        vw[e] = in ? *reinterpret_cast<const uint32_t*>(sV + r * D + cp) : 0u;
+        bt[e] = beta_s[r];
+      }
+      named_sync(1, kPrepCompute);  // the staged rows are all read: refill them
+      if (t == kIssuer) issue_copies(slots[(it + 1) & 1]);
+      if (sw) {  // visit channel cp + 1 first: swap the pair so o2 picks the half
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const int r = 16 * ta + 8 * hq + e;
-          uint32_t kw = 0, qw = 0, vw = 0;
-          if (r < len) {
-            kw = *reinterpret_cast<const uint32_t*>(sK + r * D + cp);
-            qw = *reinterpret_cast<const uint32_t*>(sQ + r * D + cp);
-            vw = *reinterpret_cast<const uint32_t*>(sV + r * D + cp);
-          }
-          kr[0][e] = bf16_lo(kw); kr[1][e] = bf16_hi(kw);
-          qr[0][e] = bf16_lo(qw); qr[1][e] = bf16_hi(qw);
-          vr[0][e] = bf16_lo(vw); vr[1][e] = bf16_hi(vw);
-        }
-#pragma unroll
-        for (int ch2 = 0; ch2 < 2; ++ch2) {
-          const int c = cp + ch2;
-          // tile references R_b = sum of the tile sums before tile b; G_C = all four
-          float R[4], GC = 0.f;
-#pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            R[b] = GC;
-            GC += Tot[b * D + c];
-          }
-          const float Ra = ta == 0 ? R[0] : (ta == 1 ? R[1] : (ta == 2 ? R[2] : R[3]));
-          const float eRa = __expf(Ra);       // exp(R_a) <= 1
-          const float eCa = __expf(GC - Ra);  // exp(G_C - R_a) <= 1
-          float kb[8], qb[8], kn[8], kg[8], vb[8], kt[8], qg[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int r = 16 * ta + 8 * hq + e;
-            const float dd = Gl[ch2][8 * hq + e];  // G_r - R_a, in (-80, 0]
-            const float f = __expf(dd), fi = __expf(-dd);
-            kb[e] = kr[ch2][e] * f;
-            qb[e] = qr[ch2][e] * f;
-            kn[e] = kr[ch2][e] * fi;
-            kg[e] = kb[e] * eRa * beta_s[r];
-            vb[e] = vr[ch2][e] * beta_s[r];
-            kt[e] = kn[e] * eCa;
-            qg[e] = qb[e] * eRa;
-          }
-          *reinterpret_cast<uint4*>(sm + kP_Bop + mn_chunk(128, 4 * ta + hq, c)) = pack8(kb);
-          *reinterpret_cast<uint4*>(sm + kP_Bop + mn_chunk(128, 4 * ta + 2 + hq, c)) = pack8(qb);
-#pragma unroll
-          for (int ap = 0; ap < 4; ++ap) {
-            if (ap < ta) continue;
-            const float E = (ap > ta) ? __expf(R[ap] - Ra) : 1.f;  // exp(R_ap - R_a) <= 1
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = kn[e] * E;
-            const uint32_t kc = (ap < 2) ? kP_KC01 : kP_KC23;
-            *reinterpret_cast<uint4*>(sm + kc + mn_chunk(128, 8 * (ap & 1) + 2 * ta + hq, c)) =
-                pack8(x);
-          }
-          *reinterpret_cast<uint4*>(sm + kP_BKg + sw128_chunk(128, c, 2 * ta + hq)) = pack8(kg);
-          *reinterpret_cast<uint4*>(sm + kP_BV + sw128_chunk(128, c, 2 * ta + hq)) = pack8(vb);
-          *reinterpret_cast<uint4*>(unit + kKT + sw128_chunk(128, c, 2 * ta + hq)) = pack8(kt);
-          *reinterpret_cast<uint4*>(unit + kWQ + mn_chunk(128, 8 + 2 * ta + hq, c)) = pack8(qg);
-          if (ta == 0 && hq == 0) gam_out[(size_t)u * D + c] = __expf(GC);
+          kw[e] = __byte_perm(kw[e], 0u, 0x1032);
+          qw[e] = __byte_perm(qw[e], 0u, 0x1032);
+          vw[e] = __byte_perm(vw[e], 0u, 0x1032);
+          const float tmp = Gl[0][e];
+          Gl[0][e] = Gl[1][e];
+          Gl[1][e] = tmp;
         }
       }
-      mbar_arrive(bar_empty);  // the staged rows are consumed: the copy warp may refill
+#pragma unroll
+      for (int o2 = 0; o2 < 2; ++o2) {
+        const int s2 = o2 ^ sw, c = cp + s2;
+        // R_b = sum of the half-tile sums before tile b; G_C = all of them
+        float R[4], GC = 0.f, inner = 0.f;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          R[b] = GC;
+          const float h0s = Tot[(2 * b) * D + c], h1s = Tot[(2 * b + 1) * D + c];
+          if (b == ta && hq == 1) inner = h0s;  // the first half of this thread's tile
+          GC += h0s + h1s;
+        }
+        const float Ra = ta == 0 ? R[0] : (ta == 1 ? R[1] : (ta == 2 ? R[2] : R[3]));
+        const float eRa = __expf(Ra);       // exp(R_a) <= 1
+        const float eCa = __expf(GC - Ra);  // exp(G_C - R_a) <= 1
+        float f[8], fi[8], kv[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float dd = Gl[o2][e] + inner;  // G_r - R_a, in (-80, 0]
+          f[e] = __expf(dd);
+          fi[e] = __expf(-dd);
+          kv[e] = o2 ? bf16_hi(kw[e]) : bf16_lo(kw[e]);
+        }
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = kv[e] * f[e];  // k exp(G_r - R_a)
+        *reinterpret_cast<uint4*>(sm + kP_Bop + mn_chunk(128, 4 * ta + hq, c)) = pack8(x);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] *= eRa * bt[e];  // beta Gamma k
+        *reinterpret_cast<uint4*>(sm + kP_BKg + sw128_chunk(128, c, 2 * ta + hq)) = pack8(x);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = (o2 ? bf16_hi(qw[e]) : bf16_lo(qw[e])) * f[e];
+        *reinterpret_cast<uint4*>(sm + kP_Bop + mn_chunk(128, 4 * ta + 2 + hq, c)) = pack8(x);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] *= eRa;  // Gamma q
+        *reinterpret_cast<uint4*>(unit + kQ + mn_chunk(64, 2 * ta + hq, c)) = pack8(x);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = (o2 ? bf16_hi(vw[e]) : bf16_lo(vw[e])) * bt[e];
+        *reinterpret_cast<uint4*>(sm + kP_BV + sw128_chunk(128, c, 2 * ta + hq)) = pack8(x);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) kv[e] *= fi[e];  // k exp(R_a - G_r)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = kv[e] * eCa;  // (gamma_C / Gamma) k
+        *reinterpret_cast<uint4*>(unit + kKT + sw128_chunk(128, c, 2 * ta + hq)) = pack8(x);
+#pragma unroll
+        for (int ap = 0; ap < 4; ++ap) {
+          if (ap < ta) continue;
+          const float E = (ap > ta) ? __expf(R[ap] - Ra) : 1.f;  // exp(R_ap - R_a) <= 1
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] = kv[e] * E;
+          const uint32_t kc = (ap < 2) ? kP_KC01 : kP_KC23;
+          *reinterpret_cast<uint4*>(sm + kc + mn_chunk(128, 8 * (ap & 1) + 2 * ta + hq, c)) =
+              pack8(x);
+        }
+        if (rg == 0) gam_out[(size_t)u * D + c] = __expf(GC);
+      }
 
       // ---- block products: D[:, 0:64] = [KC0|KC1] x Bop[0:64]^T, D[:, 64:128] = [KC2|KC3] x Bop[64:128]^T
       fence_proxy_async_smem();
@@ -330,22 +385,30 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       if (!named_sync_and(1, kPrepCompute, ok)) break;
       tc_fence_after();
       {
-        // lane = key index i (+64 for the odd tile of the pair); hf picks the pair
-        const int i = lane & 63, a = 2 * hf + (lane >> 6);
-        float pv[32];
-        tmem_ld32(lane_addr + 64 * hf + 32 * (lane >> 6), pv);
+        // lane = key index i (+64 for the odd tile of a pair); q4 = (pair, K rows | Q rows)
+        const int i = lane & 63, a = 2 * (q4 >> 1) + (lane >> 6), part = q4 & 1;
+        float pv[16];
+        tmem_ld16(lane_addr + 64 * (q4 >> 1) + 32 * (lane >> 6) + 16 * part, pv);
         tmem_wait_ld();
-        float aq[16];
+        if (part == 0) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int r = 16 * a + j;
-          Lb[r * kLdL + i] = (i < r) ? beta_s[r] * pv[j] : 0.f;
-          aq[j] = (i <= r) ? pv[16 + j] : 0.f;
+          for (int j = 0; j < 16; ++j) {
+            const int r = 16 * a + j;
+            Lb[r * kLdL + i] = (i < r) ? beta_s[r] * pv[j] : 0.f;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) pv[j] = (i <= 16 * a + j) ? pv[j] : 0.f;
+          *reinterpret_cast<uint4*>(sm + kP_AQs + mn_chunk(64, 2 * a, i)) = pack8(pv);
+          *reinterpret_cast<uint4*>(sm + kP_AQs + mn_chunk(64, 2 * a + 1, i)) = pack8(pv + 8);
+          fence_proxy_async_smem();
         }
-        *reinterpret_cast<uint4*>(unit + kAQ + mn_chunk(64, 2 * a, i)) = pack8(aq);
-        *reinterpret_cast<uint4*>(unit + kAQ + mn_chunk(64, 2 * a + 1, i)) = pack8(aq + 8);
       }
       named_sync(1, kPrepCompute);
+      if (t == kStorer) {  // the staged tiles leave as whole-tile bulk copies
+        bulk_s2g(unit + kAQ, sbase + kP_AQs, 8192);
+        bulk_commit();
+      }
 
       // ---- T = (I + L)^{-1} in fp32: diagonal 16x16 blocks by forward substitution
       //      (one column per thread), then the three block-substitution stages
@@ -361,21 +424,22 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         }
 #pragma unroll
         for (int m = 0; m < 16; ++m) Tb[(o + m) * kLdT + o + cc] = x[m];
+      } else {
+        fetch_ahead(slots[(it + 1) & 1], u + 2 * (int64_t)gridDim.x, it & 1);
       }
       named_sync(1, kPrepCompute);
       inverse_stage<1>(t, Lb, Tb, Ps);
       inverse_stage<2>(t, Lb, Tb, Ps);
       inverse_stage<3>(t, Lb, Tb, Ps);
       {  // T -> bf16 B operand (MN-major, X = row r, K = column j); zero above the diagonal
-        const int j = t >> 2, qq = t & 3;
-        float x[16];
+        const int j = t >> 3, o8 = t & 7;
+        float x[8];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int r = 16 * qq + e;
+        for (int e = 0; e < 8; ++e) {
+          const int r = 8 * o8 + e;
           x[e] = (r >= j) ? Tb[r * kLdT + j] : 0.f;
         }
-        *reinterpret_cast<uint4*>(sm + kP_T + mn_chunk(64, 2 * qq, j)) = pack8(x);
-        *reinterpret_cast<uint4*>(sm + kP_T + mn_chunk(64, 2 * qq + 1, j)) = pack8(x + 8);
+        *reinterpret_cast<uint4*>(sm + kP_T + mn_chunk(64, o8, j)) = pack8(x);
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -398,26 +462,34 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       if (!named_sync_and(1, kPrepCompute, ok)) break;
       tc_fence_after();
       {
-        float w0[32], w1[32];
-        tmem_ld32(lane_addr + 128 + 64 * hf, w0);
-        tmem_ld32(lane_addr + 160 + 64 * hf, w1);
+        float w[32];
+        tmem_ld32(lane_addr + 128 + 32 * q4, w);
         tmem_wait_ld();
-        if (hf == 0) {  // W[r][dk]: W block of WQ, K-row dk = lane
+        if (q4 < 2) {  // W tokens 32*q4 .. +31 of K-row dk = lane, staged in the BKg space
 #pragma unroll
-          for (int ch = 0; ch < 8; ++ch)
-            *reinterpret_cast<uint4*>(unit + kWQ + mn_chunk(128, ch, lane)) =
-                pack8(ch < 4 ? &w0[8 * ch] : &w1[8 * (ch - 4)]);
-        } else {  // U^T row dv = lane
+          for (int ch = 0; ch < 4; ++ch)
+            *reinterpret_cast<uint4*>(sm + kP_BKg + mn_chunk(64, 4 * q4 + ch, lane)) =
+                pack8(&w[8 * ch]);
+        } else {  // U^T row dv = lane, tokens 32*(q4-2) .. +31, staged in the BV space
 #pragma unroll
-          for (int ch = 0; ch < 8; ++ch)
-            *reinterpret_cast<uint4*>(unit + kUT + sw128_chunk(128, lane, ch)) =
-                pack8(ch < 4 ? &w0[8 * ch] : &w1[8 * (ch - 4)]);
+          for (int ch = 0; ch < 4; ++ch)
+            *reinterpret_cast<uint4*>(sm + kP_BV + sw128_chunk(128, lane, 4 * (q4 - 2) + ch)) =
+                pack8(&w[8 * ch]);
         }
       }
+      fence_proxy_async_smem();
       tc_fence_before();
       named_sync(1, kPrepCompute);
+      if (t == kStorer) {
+        bulk_s2g(unit + kW, sbase + kP_BKg, 16384);
+        bulk_s2g(unit + kUT, sbase + kP_BV, 16384);
+        bulk_commit();
+      }
     }
   }
+  if (t == kStorer) bulk_wait_all();
+  // a copy still in flight (after an abort) must land before the CTA may exit
+  if (t == kIssuer && issued > it) mbar_wait(bar_full, (issued - 1) & 1, nullptr);
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
@@ -551,7 +623,8 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         const uint32_t d1 = tmem + 128 + 128 * (j & 1);
         // (W S)^T | (Gamma Q S)^T in one N = 128 product, A = bf16 S^T from TMEM
         for (int ks = 0; ks < D / 16; ++ks)
-          mma_bf16_ta(d1, tmem + kT_SB + 8 * ks, mnmajor_desc(st + kWQ, 2048, ks), id1, ks > 0);
+          mma_bf16_ta(d1, tmem + kT_SB + 8 * ks, mnmajor_desc_lbo(st + kW, kQ - kW, 1024, ks), id1,
+                      ks > 0);
         mma_commit(bar_m1);
         any_mma = true;
         if (j > 0) o_mma(j - 1);
