@@ -54,6 +54,12 @@ def gate_bytes_per_token_head(z_bytes: int = 2, dk: int = D) -> int:
     return dk * z_bytes + dk * 4
 
 
+def fused_prefill_bytes_per_token_head(io_bytes: int = 2, dk: int = D, dv: int = D) -> int:
+    """Algorithmic bytes of the fused-gate prefill (kda_chunk_fwd_gated) per token
+    and head: q, k, v, z, beta and o in the input dtype (g is never stored)."""
+    return (3 * dk + dv) * io_bytes + io_bytes + dv * io_bytes
+
+
 def state_bytes(dk: int = D, dv: int = D) -> int:
     return dk * dv * 4
 
@@ -278,10 +284,18 @@ def run_gpu(args):
     hT = torch.empty(1, H, D, D, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step():
+    def step_separate():
         kda.gate(inp["z"], inp["A"], out=g)
         kda.chunk_fwd(inp["q"], inp["k"], inp["v"], g, inp["beta"], inp["h0"], inp["cu_seqlens"],
                       workspace=ws, out=o, final_state_out=hT)
+
+    def step_fused():
+        kda.chunk_fwd_gated(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["beta"],
+                            inp["h0"], inp["cu_seqlens"], workspace=ws, out=o,
+                            final_state_out=hT)
+
+    fused = args.path == "fused"
+    step, alt_step = (step_fused, step_separate) if fused else (step_separate, step_fused)
 
     def barrier():
         if world > 1:
@@ -311,6 +325,7 @@ def run_gpu(args):
     clocks.start()
     ms_step = timed(step, args.steps, args.warmup)
     tokens_per_s = NT * world / (ms_step * 1e-3)
+    ms_alt = timed(alt_step, args.steps, args.warmup)
 
     # per-kernel event timing pass (same steps, profiling on)
     kda.profile_enable(True)
@@ -329,14 +344,20 @@ def run_gpu(args):
         # inputs q, k, v, g, beta in; MMA-ready tiles (72 KiB) + gamma (512 B) out per unit
         "kda_tc_prep": tok_heads * (prefill_bytes_per_token_head(2) - D * 2)
         + units * (TC_UNIT_BYTES + D * 4),
+        # inputs q, k, v, z, beta in; the same tiles out
+        "kda_tc_prep_gated": tok_heads * (fused_prefill_bytes_per_token_head(2) - D * 2)
+        + units * (TC_UNIT_BYTES + D * 4),
         # tiles + gamma in, o out, h0 in and hT out per (sequence, head)
         "kda_tc_chain": units * (TC_UNIT_BYTES + D * 4) + tok_heads * D * 2
         + 2 * H * state_bytes(),
     }
     alg_bytes = kernel_bytes.get(dom_name)
     achieved = alg_bytes / (dom_avg_ms * 1e-3) / 1e9 if alg_bytes else None
-    step_bytes = tok_heads * (prefill_bytes_per_token_head(2) + gate_bytes_per_token_head(2)) \
-        + 2 * H * state_bytes()
+    if fused:
+        step_bytes = tok_heads * fused_prefill_bytes_per_token_head(2) + 2 * H * state_bytes()
+    else:
+        step_bytes = tok_heads * (prefill_bytes_per_token_head(2)
+                                  + gate_bytes_per_token_head(2)) + 2 * H * state_bytes()
     step_floor_ms = step_bytes / (hbm_peak * 1e9) * 1e3
 
     # decode step (512 x 96, fp32 state, in place)
@@ -366,9 +387,14 @@ def run_gpu(args):
     def e2e_step():
         for k_, v_ in pin.items():
             dbuf[k_].copy_(v_, non_blocking=True)
-        kda.gate(dbuf["z"], dbuf["A"], out=g)
-        kda.chunk_fwd(dbuf["q"], dbuf["k"], dbuf["v"], g, dbuf["beta"], dbuf["h0"],
-                      dbuf["cu_seqlens"], workspace=ws, out=o, final_state_out=hT)
+        if fused:
+            kda.chunk_fwd_gated(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["z"], dbuf["A"],
+                                dbuf["beta"], dbuf["h0"], dbuf["cu_seqlens"], workspace=ws, out=o,
+                                final_state_out=hT)
+        else:
+            kda.gate(dbuf["z"], dbuf["A"], out=g)
+            kda.chunk_fwd(dbuf["q"], dbuf["k"], dbuf["v"], g, dbuf["beta"], dbuf["h0"],
+                          dbuf["cu_seqlens"], workspace=ws, out=o, final_state_out=hT)
         o_host.copy_(o, non_blocking=True)
         hT_host.copy_(hT, non_blocking=True)
 
@@ -389,7 +415,9 @@ def run_gpu(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": w.name, "global_batch": world, "seq_len": NT, "heads": H,
-                   "dk": D, "dv": D, "chunk": 64, "step": "kda_gate + kda_chunk_fwd",
+                   "dk": D, "dv": D, "chunk": 64,
+                   "step": "kda_chunk_fwd_gated (gate fused)" if fused
+                   else "kda_gate + kda_chunk_fwd",
                    "l2": "inputs larger than L2 (201 MB per q/k/v/z tensor), no flush",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": achieved,
@@ -400,6 +428,9 @@ def run_gpu(args):
                      "peak_source": f"{peak_src} hbm_gbs",
                      "step_floor_ms": step_floor_ms, "step_frac": step_floor_ms / ms_step},
         "kernels": {k: {"launches": n, "mean_ms": t / n} for k, (n, t) in per_kernel.items()},
+        "alt_step": {"step": "kda_gate + kda_chunk_fwd" if fused
+                     else "kda_chunk_fwd_gated (gate fused)", "ms_per_step": ms_alt,
+                     "value": NT * world / (ms_alt * 1e-3)},
         "decode": {"workload": dw.name, "ms_per_step": ms_dec, "achieved_gbs": dec_gbs,
                    "peak_gbs": hbm_peak, "frac": dec_gbs / hbm_peak,
                    "bytes_per_step": dec_bytes},
@@ -423,6 +454,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--ref-heads", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", choices=["fused", "separate"], default="fused",
+                    help="prefill step: gate fused into the chunk kernels, or kda_gate then "
+                         "kda_chunk_fwd (the other one is timed too, as alt_step)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

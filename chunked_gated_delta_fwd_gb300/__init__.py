@@ -25,7 +25,7 @@ import torch
 
 from . import _build
 
-__all__ = ["KdaError", "gate", "chunk_fwd", "chunk_fwd_workspace_size", "recurrent_step",
+__all__ = ["KdaError", "gate", "chunk_fwd", "chunk_fwd_gated", "chunk_fwd_workspace_size", "recurrent_step",
            "library_path", "lib", "get_device_error", "profile_enable", "profile_collect", "G_MIN", "F32", "BF16", "FP32_CORES"]
 
 G_MIN = -5.0
@@ -63,6 +63,8 @@ def _load() -> ctypes.CDLL:
     L.kda_chunk_fwd.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i64, i32, i32, i32, vp,
                                 vp, vp, sz, vp]
     L.kda_chunk_fwd_ex.argtypes = L.kda_chunk_fwd.argtypes + [u32]
+    L.kda_chunk_fwd_gated.argtypes = [vp, vp, vp, i32, vp, vp, f32, vp, vp, vp, i32, i32, i64,
+                                      i32, i32, i32, vp, vp, vp, sz, vp]
     L.kda_recurrent_step.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, vp]
     L.kda_last_error_string.restype = ctypes.c_char_p
     L.kda_get_device_error.argtypes = [vp]
@@ -70,8 +72,8 @@ def _load() -> ctypes.CDLL:
     L.kda_profile_enable.argtypes = [i32]
     L.kda_profile_get.argtypes = [i32, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(i32),
                                   ctypes.POINTER(ctypes.c_double)]
-    for fn in (L.kda_gate, L.kda_chunk_fwd, L.kda_chunk_fwd_ex, L.kda_recurrent_step,
-               L.kda_get_device_error):
+    for fn in (L.kda_gate, L.kda_chunk_fwd, L.kda_chunk_fwd_ex, L.kda_chunk_fwd_gated,
+               L.kda_recurrent_step, L.kda_get_device_error):
         fn.restype = ctypes.c_int
     return L
 
@@ -152,10 +154,42 @@ def chunk_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, *, output_final_state=
     cu_seqlens: int32 [N+1] on the device, or None for B sequences of length T.
     Returns ``(o, hT)`` with o like v and hT [N, H, 128, 128] fp32 (None if not asked).
     """
+    _need(g, "g", torch.float32, q.device)
+    c = _chunk_setup(q, k, v, beta, h0, cu_seqlens, output_final_state, workspace, flags, out,
+                     final_state_out)
+    with torch.cuda.device(q.device):
+        _check(lib.kda_chunk_fwd_ex(_ptr(q), _ptr(k), _ptr(v), c["dt"], _ptr(g), _ptr(beta),
+                                    _ptr(h0), _ptr(cu_seqlens), c["N"], c["B"], c["T"], c["H"],
+                                    c["dk"], c["dv"], _ptr(c["o"]), _ptr(c["hT"]),
+                                    _ptr(c["ws"]), c["ws"].numel(), _stream(q.device),
+                                    int(flags)))
+    return c["o"], c["hT"]
+
+
+def chunk_fwd_gated(q, k, v, z, A, beta, h0=None, cu_seqlens=None, *, g_min: float = -5.0,
+                    output_final_state=True, workspace=None, out=None, final_state_out=None):
+    """KDA prefill with the bounded gate g = g_min * Sigmoid(exp(A_h) z) evaluated
+    inside the chunk kernels (g is never materialised).  bf16 only; z like k,
+    A fp32 [H].  Everything else as ``chunk_fwd``."""
+    _need(z, "z", q.dtype, q.device)
+    _need(A, "A", torch.float32, q.device)
+    c = _chunk_setup(q, k, v, beta, h0, cu_seqlens, output_final_state, workspace, 0, out,
+                     final_state_out)
+    with torch.cuda.device(q.device):
+        _check(lib.kda_chunk_fwd_gated(_ptr(q), _ptr(k), _ptr(v), c["dt"], _ptr(z), _ptr(A),
+                                       float(g_min), _ptr(beta), _ptr(h0), _ptr(cu_seqlens),
+                                       c["N"], c["B"], c["T"], c["H"], c["dk"], c["dv"],
+                                       _ptr(c["o"]), _ptr(c["hT"]), _ptr(c["ws"]),
+                                       c["ws"].numel(), _stream(q.device)))
+    return c["o"], c["hT"]
+
+
+def _chunk_setup(q, k, v, beta, h0, cu_seqlens, output_final_state, workspace, flags, out,
+                 final_state_out):
+    """Checks the chunk inputs and allocates the outputs and the workspace."""
     dev = q.device
     for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta)):
         _need(t, name, q.dtype, dev)
-    _need(g, "g", torch.float32, dev)
     dt = _dtype_code(q)
     H, dk, dv = q.shape[-2], q.shape[-1], v.shape[-1]
     if cu_seqlens is not None:
@@ -185,12 +219,7 @@ def chunk_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, *, output_final_state=
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     _need(workspace, "workspace", torch.uint8, dev)
-    with torch.cuda.device(dev):
-        _check(lib.kda_chunk_fwd_ex(_ptr(q), _ptr(k), _ptr(v), dt, _ptr(g), _ptr(beta), _ptr(h0),
-                                    _ptr(cu_seqlens), N, B, T, H, dk, dv, _ptr(o), _ptr(hT),
-                                    _ptr(workspace), workspace.numel(), _stream(dev),
-                                    int(flags)))
-    return o, hT
+    return dict(dt=dt, N=N, B=B, T=T, H=H, dk=dk, dv=dv, o=o, hT=hT, ws=workspace)
 
 
 def recurrent_step(q, k, v, g, beta, S, *, out=None):

@@ -320,59 +320,97 @@ size_t kda_chunk_fwd_workspace_size(int64_t n_tokens, int n_seqs, int H, int dty
   return 0;
 }
 
-kda_status_t kda_chunk_fwd_ex(const void* q, const void* k, const void* v, int dtype,
-                                const float* g, const void* beta, const float* h0,
-                                const int32_t* cu_seqlens, int n_seqs, int B, int64_t T, int H,
-                                int dk, int dv, void* o, float* hT, void* workspace,
-                                size_t ws_bytes, kda_stream_t stream, unsigned flags) {
+}  // extern "C"
+
+namespace {
+
+// Shared body of the chunk entry points.  Exactly one of g and z is non-null; with
+// z the gate is evaluated inside the tensor-core prepare kernel (bf16 only).
+kda_status_t chunk_fwd_impl(const char* fn, const void* q, const void* k, const void* v,
+                            int dtype, const float* g, const void* z, const float* A,
+                            float g_min, const void* beta, const float* h0,
+                            const int32_t* cu_seqlens, int n_seqs, int B, int64_t T, int H,
+                            int dk, int dv, void* o, float* hT, void* workspace,
+                            size_t ws_bytes, kda_stream_t stream, unsigned flags) {
   if (dtype != KDA_F32 && dtype != KDA_BF16)
-    return fail(KDA_ERR_UNSUPPORTED_DTYPE, "kda_chunk_fwd: dtype %d", dtype);
+    return fail(KDA_ERR_UNSUPPORTED_DTYPE, "%s: dtype %d", fn, dtype);
   if (dk != kda::kD || dv != kda::kD)
-    return fail(KDA_ERR_UNSUPPORTED_SHAPE, "kda_chunk_fwd: dk=%d dv=%d (need 128)", dk, dv);
-  if (H < 1) return fail(KDA_ERR_UNSUPPORTED_SHAPE, "kda_chunk_fwd: H=%d", H);
+    return fail(KDA_ERR_UNSUPPORTED_SHAPE, "%s: dk=%d dv=%d (need 128)", fn, dk, dv);
+  if (H < 1) return fail(KDA_ERR_UNSUPPORTED_SHAPE, "%s: H=%d", fn, H);
   int N;
   int64_t NT, T_per_seq = 0;
   if (cu_seqlens) {
-    if (B != 1) return fail(KDA_ERR_INVALID_ARG, "kda_chunk_fwd: B must be 1 with cu_seqlens");
-    if (n_seqs < 1) return fail(KDA_ERR_INVALID_ARG, "kda_chunk_fwd: n_seqs=%d", n_seqs);
+    if (B != 1) return fail(KDA_ERR_INVALID_ARG, "%s: B must be 1 with cu_seqlens", fn);
+    if (n_seqs < 1) return fail(KDA_ERR_INVALID_ARG, "%s: n_seqs=%d", fn, n_seqs);
     N = n_seqs;
     NT = T;
   } else {
-    if (B < 1) return fail(KDA_ERR_INVALID_ARG, "kda_chunk_fwd: B=%d", B);
+    if (B < 1) return fail(KDA_ERR_INVALID_ARG, "%s: B=%d", fn, B);
     N = B;
     NT = (int64_t)B * T;
     T_per_seq = T;
   }
   if (T < 0 || NT > INT32_MAX - 2 * kda::kChunk)
-    return fail(KDA_ERR_INVALID_ARG, "kda_chunk_fwd: token count out of range");
-  if ((NT > 0 && (!q || !k || !v || !g || !beta || !o)) || (N > 0 && !workspace))
-    return fail(KDA_ERR_INVALID_ARG, "kda_chunk_fwd: null required pointer");
-  const void* ptrs[] = {q, k, v, g, beta, h0, o, hT};
+    return fail(KDA_ERR_INVALID_ARG, "%s: token count out of range", fn);
+  if ((NT > 0 && (!q || !k || !v || !(g || (z && A)) || !beta || !o)) || (N > 0 && !workspace))
+    return fail(KDA_ERR_INVALID_ARG, "%s: null required pointer", fn);
+  const void* ptrs[] = {q, k, v, g, z, beta, h0, o, hT};
   for (const void* p : ptrs)
     if (p && !aligned16(p))
-      return fail(KDA_ERR_MISALIGNED, "kda_chunk_fwd: pointers must be 16-byte aligned");
+      return fail(KDA_ERR_MISALIGNED, "%s: pointers must be 16-byte aligned", fn);
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-    return fail(KDA_ERR_MISALIGNED, "kda_chunk_fwd: workspace must be 256-byte aligned");
+    return fail(KDA_ERR_MISALIGNED, "%s: workspace must be 256-byte aligned", fn);
   const size_t need = kda_chunk_fwd_workspace_size(
       NT, N, H, (flags & KDA_CHUNK_FP32_CORES) ? (int)KDA_F32 : dtype);
   if (ws_bytes < need)
-    return fail(KDA_ERR_WORKSPACE_TOO_SMALL, "kda_chunk_fwd: workspace %zu < %zu bytes",
+    return fail(KDA_ERR_WORKSPACE_TOO_SMALL, "%s: workspace %zu < %zu bytes", fn,
                 ws_bytes, need);
   if (flags & ~(unsigned)KDA_CHUNK_FP32_CORES)
-    return fail(KDA_ERR_INVALID_ARG, "kda_chunk_fwd_ex: unknown flags 0x%x", flags);
+    return fail(KDA_ERR_INVALID_ARG, "%s: unknown flags 0x%x", fn, flags);
   kda_status_t st = check_device();
   if (st != KDA_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int* err = kda::device_error_flag();
   cudaError_t e = kda::launch_plan(cu_seqlens, N, T_per_seq, NT, workspace, err, s);
-  if (e != cudaSuccess) return cuda_fail(e, "kda_chunk_fwd plan launch");
+  if (e != cudaSuccess) return cuda_fail(e, "chunk plan launch");
   if (dtype == KDA_BF16 && !(flags & KDA_CHUNK_FP32_CORES))
-    e = kda::launch_chunk_tc(q, k, v, g, beta, h0, o, hT, NT, N, H, workspace, err, s);
+    e = kda::launch_chunk_tc(q, k, v, g, z, A, g_min, beta, h0, o, hT, NT, N, H, workspace, err,
+                             s);
   else
     e = kda::launch_chunk_simt(q, k, v, dtype == KDA_BF16, g, beta, h0, o, hT, NT, N, H,
                                workspace, s);
-  if (e != cudaSuccess) return cuda_fail(e, "kda_chunk_fwd launch");
+  if (e != cudaSuccess) return cuda_fail(e, "chunk launch");
   return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status_t kda_chunk_fwd_ex(const void* q, const void* k, const void* v, int dtype,
+                              const float* g, const void* beta, const float* h0,
+                              const int32_t* cu_seqlens, int n_seqs, int B, int64_t T, int H,
+                              int dk, int dv, void* o, float* hT, void* workspace,
+                              size_t ws_bytes, kda_stream_t stream, unsigned flags) {
+  return chunk_fwd_impl("kda_chunk_fwd", q, k, v, dtype, g, nullptr, nullptr, 0.f, beta, h0,
+                        cu_seqlens, n_seqs, B, T, H, dk, dv, o, hT, workspace, ws_bytes, stream,
+                        flags);
+}
+
+kda_status_t kda_chunk_fwd_gated(const void* q, const void* k, const void* v, int dtype,
+                                 const void* z, const float* A, float g_min, const void* beta,
+                                 const float* h0, const int32_t* cu_seqlens, int n_seqs, int B,
+                                 int64_t T, int H, int dk, int dv, void* o, float* hT,
+                                 void* workspace, size_t ws_bytes, kda_stream_t stream) {
+  if (dtype != KDA_BF16)
+    return fail(KDA_ERR_UNSUPPORTED_DTYPE,
+                "kda_chunk_fwd_gated: dtype %d (bf16 only; for fp32 call kda_gate first)", dtype);
+  if (!(g_min >= -5.f && g_min < 0.f))
+    return fail(KDA_ERR_INVALID_ARG, "kda_chunk_fwd_gated: g_min=%g outside [-5, 0)",
+                (double)g_min);
+  return chunk_fwd_impl("kda_chunk_fwd_gated", q, k, v, dtype, nullptr, z, A, g_min, beta, h0,
+                        cu_seqlens, n_seqs, B, T, H, dk, dv, o, hT, workspace, ws_bytes, stream,
+                        0u);
 }
 
 kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v, int dtype,

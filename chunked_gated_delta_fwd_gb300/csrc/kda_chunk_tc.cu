@@ -53,7 +53,7 @@ constexpr int D = kD;      // 128
 constexpr uint32_t kW = 0;         // MN-major X=64 (tokens), K=128: 16 KB
 constexpr uint32_t kQ = 16384;     // same layout; [W | Q] read as one X=128 operand
 constexpr uint32_t kUT = 32768;    // K-major 128 rows x 64: 16 KB
-constexpr uint32_t kAQ = 49152;    // MN-major X=64 (rows r), K=64 (columns i): 8 KB
+constexpr uint32_t kAQ = 49152;    // K-major A_qk, 64 rows r x 64 columns i: 8 KB
 constexpr uint32_t kKT = 57344;    // K-major 128 rows x 64: 16 KB
 constexpr uint32_t kUnitBytes = 73728;
 constexpr uint32_t kGamBytes = D * 4;
@@ -61,22 +61,27 @@ constexpr uint32_t kGamBytes = D * 4;
 // ============================================================== prep kernel
 constexpr int kPrepCompute = 512;                // 16 warps; thread 0 also issues the copies
 constexpr int kPrepThreads = kPrepCompute;
-constexpr uint32_t kInUnitBytes = C * (3 * 256 + 512);  // k, q, v (bf16) and g (fp32) boxes
+// staged boxes per unit: k, q, v (bf16) and g (fp32), or z (bf16) when the gate is fused
+template <bool kZ>
+__host__ __device__ constexpr uint32_t in_unit_bytes() { return C * (3 * 256 + (kZ ? 256 : 512)); }
 // shared memory (offsets from a 1024-aligned base)
 constexpr uint32_t kI_K = 0, kI_Q = 16384, kI_V = 32768, kI_G = 49152;  // staged rows
 constexpr uint32_t kP_Bop = 81920;         // MN-major X=128 (Kb/Qb rows), K=128
 constexpr uint32_t kP_T = kP_Bop;          //   reused after the products: bf16 T, MN-major 64x64
 constexpr uint32_t kP_AQs = kP_Bop + 8192;  //   and the A_qk tile on its way out
-constexpr uint32_t kP_KC01 = 114688;       // MN-major X=128 ([KC(0) | KC(1)] rows), K=128
-constexpr uint32_t kP_KC23 = 147456;       // [KC(2) | KC(3)]
-// reused after the products (re-zeroed before the next unit's operands):
-constexpr uint32_t kP_Lb = kP_KC01;          // L, fp32 [64][65] (strictly lower part)
+// MN-major X=192, K=128: [KC(0) | KC(1) | KC(2) | KC(3)] at X = 0, 16, 48, 96
+// (16, 32, 48, 64 rows), X = 160..191 unused
+constexpr uint32_t kP_KC = 114688;
+constexpr int kKCX = 192;
+// reused after the products (the next unit rewrites every KC row it reads):
+constexpr uint32_t kP_Lb = kP_KC;            // L, fp32 [64][65] (lower blocks)
 constexpr uint32_t kP_Tb = kP_Lb + 16640;    // T, fp32 [64][68] row-major
 constexpr uint32_t kP_Ps = kP_Tb + 17408;    // block-product scratch, fp32 [3][16][16]
 constexpr uint32_t kScratchBytes = 16640 + 17408 + 3072;
-constexpr uint32_t kP_BKg = 180224;        // K-major (beta Gamma K)^T 128 x 64
-constexpr uint32_t kP_BV = 196608;         // K-major (beta V)^T 128 x 64
-constexpr uint32_t kP_beta = 212992;       // 64 fp32
+static_assert(kScratchBytes <= 49152, "the inverse scratch lives in the KC operand space");
+constexpr uint32_t kP_BKg = 163840;        // K-major (beta Gamma K)^T 128 x 64
+constexpr uint32_t kP_BV = 180224;         // K-major (beta V)^T 128 x 64
+constexpr uint32_t kP_beta = 196608;       // 64 fp32
 constexpr uint32_t kP_Tot = kP_beta + 256; // per-half-tile sums of g, [8][128] fp32
 constexpr uint32_t kP_bars = kP_Tot + 4096;  // in_full, (unused), p, w + TMEM base
 constexpr uint32_t kP_Smem = kP_bars + 128 + 1024;
@@ -91,6 +96,7 @@ struct UnitInfo {
   int chunk, h;
   int64_t t0;
   int len;
+  float ea;  // exp(A_h), when the gate is fused
 };
 
 __device__ __forceinline__ UnitInfo unit_info(const Plan& plan, int H, int64_t u) {
@@ -151,11 +157,15 @@ __device__ __forceinline__ void inverse_stage(int t, const float* Lb, float* Tb,
   named_sync(1, kPrepCompute);
 }
 
+// kZ: tm_g maps z (bf16) instead of g, and g = g_min * Sigmoid(exp(A_h) z) is formed
+// while the decays are summed ("Kimi K3 technical report review", section 3.2).
+template <bool kZ>
 __global__ void __launch_bounds__(kPrepThreads, 1)
     tc_prep(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
-            const __nv_bfloat16* __restrict__ beta, Plan plan, int H, int64_t units_ub,
-            uint8_t* __restrict__ tiles, float* __restrict__ gam_out, int* err) {
+            const __nv_bfloat16* __restrict__ beta, const float* __restrict__ A, float g_min,
+            Plan plan, int H, int64_t units_ub, uint8_t* __restrict__ tiles,
+            float* __restrict__ gam_out, int* err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_addr(sm);
@@ -170,16 +180,16 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
   const uint32_t bar_p = smem_addr(&bars[2]), bar_w = smem_addr(&bars[3]);
   const int t = threadIdx.x, warp = t >> 5;
 
-  // the KC tiles keep zero rows beyond their tile (re-zeroed after scratch use)
-  for (uint32_t o = t * 16; o < 65536; o += kPrepThreads * 16)
-    *reinterpret_cast<uint4*>(sm + kP_KC01 + o) = make_uint4(0, 0, 0, 0);
+  // the unused X = 160..191 part of the KC operand starts out as zeros
+  for (uint32_t o = t * 16; o < 49152; o += kPrepThreads * 16)
+    *reinterpret_cast<uint4*>(sm + kP_KC + o) = make_uint4(0, 0, 0, 0);
   if (t == 0) {
     mbar_init(bar_full, 1);
     mbar_init(bar_p, 1);
     mbar_init(bar_w, 1);
     mbar_fence_init();
   }
-  if (warp == 0) tmem_alloc(smem_addr(tmem_slot), 256);
+  if (warp == 0) tmem_alloc(smem_addr(tmem_slot), 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -202,11 +212,12 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
   auto locate = [&](int64_t u) {
     UnitInfo ui;
     if (u < units_ub) ui = unit_info(plan, H, u); else ui.chunk = total;
+    ui.ea = (kZ && ui.chunk < total) ? expf(__ldg(A + ui.h)) : 0.f;
     return ui;
   };
   auto issue_copies = [&](const UnitInfo& ui) {
     if (ui.chunk >= total) return;
-    mbar_arrive_expect_tx(bar_full, kInUnitBytes);
+    mbar_arrive_expect_tx(bar_full, in_unit_bytes<kZ>());
     const int t0 = (int)ui.t0;
     tma_load_3d(sbase + kI_K, &tm_k, 0, ui.h, t0, bar_full);
     tma_load_3d(sbase + kI_Q, &tm_q, 0, ui.h, t0, bar_full);
@@ -273,8 +284,17 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int r = r0 + e;
-          const float2 gg = (r < len) ? *reinterpret_cast<const float2*>(sG + r * D + cp)
-                                      : make_float2(0.f, 0.f);
+          float2 gg = make_float2(0.f, 0.f);
+          if (r < len) {
+            if constexpr (kZ) {  // g = g_min / (1 + exp(-exp(A_h) z))
+              const uint32_t zw = *reinterpret_cast<const uint32_t*>(
+                  reinterpret_cast<const __nv_bfloat16*>(sG) + r * D + cp);
+              gg.x = __fdividef(g_min, 1.f + __expf(-ui.ea * bf16_lo(zw)));
+              gg.y = __fdividef(g_min, 1.f + __expf(-ui.ea * bf16_hi(zw)));
+            } else {
+              gg = *reinterpret_cast<const float2*>(sG + r * D + cp);
+            }
+          }
           s0 += gg.x;
           s1 += gg.y;
           Gl[0][e] = s0;
@@ -359,48 +379,54 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
           const float E = (ap > ta) ? __expf(R[ap] - Ra) : 1.f;  // exp(R_ap - R_a) <= 1
 #pragma unroll
           for (int e = 0; e < 8; ++e) x[e] = kv[e] * E;
-          const uint32_t kc = (ap < 2) ? kP_KC01 : kP_KC23;
-          *reinterpret_cast<uint4*>(sm + kc + mn_chunk(128, 8 * (ap & 1) + 2 * ta + hq, c)) =
+          *reinterpret_cast<uint4*>(sm + kP_KC + mn_chunk(kKCX, ap * (ap + 1) + 2 * ta + hq, c)) =
               pack8(x);
         }
         if (rg == 0) gam_out[(size_t)u * D + c] = __expf(GC);
       }
 
-      // ---- block products: D[:, 0:64] = [KC0|KC1] x Bop[0:64]^T, D[:, 64:128] = [KC2|KC3] x Bop[64:128]^T
+      // ---- block products in one N=192 MMA chain: D[m][n] = Bop row m . KC row n
+      //      over the channels; lane m = 32 ta + 16 part + j is K row (part 0) or
+      //      Q row (part 1) j of tile ta, and KC(ta) sits at columns 8 ta (ta + 1)
       fence_proxy_async_smem();
       tc_fence_before();
       named_sync(1, kPrepCompute);
       if (t == 0) {
         tc_fence_after();
-        const uint32_t id = idesc_bf16_mn(128, 64, 1, 1);
+        const uint32_t id = idesc_bf16_mn(128, kKCX, 1, 1);
         for (int s = 0; s < D / 16; ++s)
-          mma_bf16(tmem + 0, mnmajor_desc(sbase + kP_KC01, 2048, s),
-                   mnmajor_desc(sbase + kP_Bop, 2048, s), id, s > 0);
-        for (int s = 0; s < D / 16; ++s)
-          mma_bf16(tmem + 64, mnmajor_desc(sbase + kP_KC23, 2048, s),
-                   mnmajor_desc(sbase + kP_Bop + 1024, 2048, s), id, s > 0);
+          mma_bf16(tmem + 0, mnmajor_desc(sbase + kP_Bop, 2048, s),
+                   mnmajor_desc(sbase + kP_KC, mn_sbo(kKCX), s), id, s > 0);
         mma_commit(bar_p);
       }
       ok = mbar_wait(bar_p, it & 1, err);
       if (!named_sync_and(1, kPrepCompute, ok)) break;
       tc_fence_after();
       {
-        // lane = key index i (+64 for the odd tile of a pair); q4 = (pair, K rows | Q rows)
-        const int i = lane & 63, a = 2 * (q4 >> 1) + (lane >> 6), part = q4 & 1;
+        // warp -> tile tw = warp & 3 (its TMEM lane quarter) and key piece pc = warp >> 2
+        // (keys i = 16 pc .. +15); lane -> row r = 16 tw + (lane & 15), K or Q row
+        const int tw = warp & 3, pc = warp >> 2, r = 16 * tw + (t & 15);
+        const bool qrow = (t & 16) != 0;
         float pv[16];
-        tmem_ld16(lane_addr + 64 * (q4 >> 1) + 32 * (lane >> 6) + 16 * part, pv);
-        tmem_wait_ld();
-        if (part == 0) {
+        if (pc <= tw) {  // keys of tiles up to tw only (warp-uniform)
+          tmem_ld16(lane_addr + 8 * tw * (tw + 1) + 16 * pc, pv);
+          tmem_wait_ld();
+        } else {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int r = 16 * a + j;
-            Lb[r * kLdL + i] = (i < r) ? beta_s[r] * pv[j] : 0.f;
+          for (int jj = 0; jj < 16; ++jj) pv[jj] = 0.f;
+        }
+        if (!qrow) {
+          if (pc <= tw) {
+            const float br = beta_s[r];
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj)
+              Lb[r * kLdL + 16 * pc + jj] = (16 * pc + jj < r) ? br * pv[jj] : 0.f;
           }
         } else {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) pv[j] = (i <= 16 * a + j) ? pv[j] : 0.f;
-          *reinterpret_cast<uint4*>(sm + kP_AQs + mn_chunk(64, 2 * a, i)) = pack8(pv);
-          *reinterpret_cast<uint4*>(sm + kP_AQs + mn_chunk(64, 2 * a + 1, i)) = pack8(pv + 8);
+          for (int jj = 0; jj < 16; ++jj) pv[jj] = (16 * pc + jj <= r) ? pv[jj] : 0.f;
+          *reinterpret_cast<uint4*>(sm + kP_AQs + sw128_chunk(64, r, 2 * pc)) = pack8(pv);
+          *reinterpret_cast<uint4*>(sm + kP_AQs + sw128_chunk(64, r, 2 * pc + 1)) = pack8(pv + 8);
           fence_proxy_async_smem();
         }
       }
@@ -448,22 +474,19 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         tc_fence_after();
         const uint32_t id = idesc_bf16_mn(128, 64, 0, 1);
         for (int s = 0; s < C / 16; ++s)  // W^T = (beta Gamma K)^T T^T
-          mma_bf16(tmem + 128, kmajor_desc(sbase + kP_BKg, 128, s),
+          mma_bf16(tmem + 256, kmajor_desc(sbase + kP_BKg, 128, s),
                    mnmajor_desc(sbase + kP_T, 1024, s), id, s > 0);
         for (int s = 0; s < C / 16; ++s)  // U^T = (beta V)^T T^T
-          mma_bf16(tmem + 192, kmajor_desc(sbase + kP_BV, 128, s),
+          mma_bf16(tmem + 320, kmajor_desc(sbase + kP_BV, 128, s),
                    mnmajor_desc(sbase + kP_T, 1024, s), id, s > 0);
         mma_commit(bar_w);
       }
-      // the KC scratch (L, T, products) goes back to zero for the next unit's KC rows
-      for (uint32_t o = t * 16; o < kScratchBytes; o += kPrepCompute * 16)
-        *reinterpret_cast<uint4*>(sm + kP_Lb + o) = make_uint4(0, 0, 0, 0);
       ok = mbar_wait(bar_w, it & 1, err);
       if (!named_sync_and(1, kPrepCompute, ok)) break;
       tc_fence_after();
       {
         float w[32];
-        tmem_ld32(lane_addr + 128 + 32 * q4, w);
+        tmem_ld32(lane_addr + 256 + 32 * q4, w);
         tmem_wait_ld();
         if (q4 < 2) {  // W tokens 32*q4 .. +31 of K-row dk = lane, staged in the BKg space
 #pragma unroll
@@ -493,7 +516,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, 512);
   }
 }
 
@@ -588,7 +611,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       int issued = 0, consumed = 0;
       for (; issued < min(kStages, nch); ++issued) issue(issued);
       const uint32_t id1 = idesc_bf16_mn(128, 128, 0, 1);   // S^T x WQ (MN-major B)
-      const uint32_t id2a = idesc_bf16_mn(128, 64, 0, 1);   // Vt^T x A_qk (MN-major B)
+      const uint32_t id2a = idesc_bf16_mn(128, 64, 0, 0);   // Vt^T x A_qk^T (K-major B)
       const uint32_t id2b = idesc_bf16_mn(128, 128, 0, 0);  // Vt^T x Kt^T (K-major B)
       int j = 0;
       bool any_mma = false;
@@ -599,7 +622,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         const uint32_t d1j = tmem + 128 + 128 * (jj & 1);
         for (int ks = 0; ks < C / 16; ++ks)
           mma_bf16_ta(d1j + 64, tmem + kT_VT + 32 * (jj & 1) + 8 * ks,
-                      mnmajor_desc(stj + kAQ, 1024, ks), id2a, 1u);
+                      kmajor_desc(stj + kAQ, 64, ks), id2a, 1u);
         mma_commit(bar_o0 + 8 * (jj & 1));  // every MMA of chunk jj is complete
       };
       // the stage of chunk jj is refilled once every MMA of chunk jj has read it (done
@@ -831,9 +854,9 @@ size_t tc_workspace_bytes(int64_t n_tokens, int n_seqs, int H) {
 }
 
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const float* g,
-                            const void* beta, const float* h0, void* o, float* hT,
-                            int64_t n_tokens, int n_seqs, int H, void* ws, int* err,
-                            cudaStream_t s) {
+                            const void* z, const float* A, float g_min, const void* beta,
+                            const float* h0, void* o, float* hT, int64_t n_tokens, int n_seqs,
+                            int H, void* ws, int* err, cudaStream_t s) {
   Plan plan;
   plan.cu = static_cast<const int32_t*>(ws);
   plan.chunk_off = plan.cu + (n_seqs + 1);
@@ -845,8 +868,10 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
   float* gam = reinterpret_cast<float*>(tiles + (size_t)units * kUnitBytes);
   cudaError_t e;
   using T = __nv_bfloat16;
+  const bool fused = z != nullptr;
   if (units > 0 && n_tokens > 0) {  // with no tokens there are no chunks to prepare
-    e = cudaFuncSetAttribute(tc_prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kP_Smem);
+    auto kern = fused ? tc_prep<true> : tc_prep<false>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kP_Smem);
     if (e != cudaSuccess) return e;
     const int sms = sm_count();
     const int grid = (int)(units < sms ? units : sms);
@@ -854,12 +879,14 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
     e = encode_rows(&tm[0], k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n_tokens);
     if (e == cudaSuccess) e = encode_rows(&tm[1], q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n_tokens);
     if (e == cudaSuccess) e = encode_rows(&tm[2], v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n_tokens);
-    if (e == cudaSuccess) e = encode_rows(&tm[3], g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, n_tokens);
+    if (e == cudaSuccess)
+      e = fused ? encode_rows(&tm[3], z, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n_tokens)
+                : encode_rows(&tm[3], g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, n_tokens);
     if (e != cudaSuccess) return e;
-    ProfScope prof_scope("kda_tc_prep", s);
-    tc_prep<<<grid, kPrepThreads, kP_Smem, s>>>(tm[0], tm[1], tm[2], tm[3],
-                                                 static_cast<const T*>(beta), plan, H, units,
-                                                 tiles, gam, err);
+    ProfScope prof_scope(fused ? "kda_tc_prep_gated" : "kda_tc_prep", s);
+    kern<<<grid, kPrepThreads, kP_Smem, s>>>(tm[0], tm[1], tm[2], tm[3],
+                                             static_cast<const T*>(beta), A, g_min, plan, H,
+                                             units, tiles, gam, err);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

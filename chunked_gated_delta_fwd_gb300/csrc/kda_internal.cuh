@@ -104,9 +104,11 @@ cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v, int b
 
 // bf16 tensor-core (tcgen05) chunk path.
 size_t tc_workspace_bytes(int64_t n_tokens, int n_seqs, int H);
+// With z non-null the gate is fused: g is formed from z (bf16), A and g_min and g
+// is ignored.
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const float* g,
-                            const void* beta, const float* h0, void* o, float* hT,
-                            int64_t n_tokens, int n_seqs, int H, void* ws, int* err_flag,
-                            cudaStream_t s);
+                            const void* z, const float* A, float g_min, const void* beta,
+                            const float* h0, void* o, float* hT, int64_t n_tokens, int n_seqs,
+                            int H, void* ws, int* err_flag, cudaStream_t s);
 
 }  // namespace kda

@@ -138,6 +138,30 @@ kda_status_t kda_chunk_fwd_ex(const void* q, const void* k, const void* v, int d
                               size_t ws_bytes, kda_stream_t stream, unsigned flags);
 
 /*
+ * kda_chunk_fwd_gated -- kda_chunk_fwd with the bounded gate evaluated inside the
+ * chunk kernels instead of read as g.  The gate is that of kda_gate ("Kimi K3
+ * technical report review", section 3.2: g = g_min * Sigmoid(exp(A_h) z)); it is
+ * formed from z while each chunk's decays are summed and is never written to
+ * memory, as the FlashKDA prepare kernel forms its gate prefix sums in place
+ * ("Kimi K3 notes", section "FlashKDA", kernel K1).  Only the bf16 tensor-core
+ * path has this form.
+ *   z      [NT, H, dk] of `dtype`, device, same layout and alignment as k.
+ *   A      fp32 [H], device (per-head log scale of the gate).
+ *   g_min  lower bound of the gate, in [-5, 0): the 16-token tile range argument
+ *          needs g >= -5.
+ * Every other argument, the workspace size (kda_chunk_fwd_workspace_size with
+ * KDA_BF16) and the results are those of kda_chunk_fwd with g = kda_gate(z, A).
+ * Errors: dtype other than KDA_BF16 -> KDA_ERR_UNSUPPORTED_DTYPE (for fp32 inputs
+ * call kda_gate, then kda_chunk_fwd); g_min outside [-5, 0) -> KDA_ERR_INVALID_ARG;
+ * otherwise as kda_chunk_fwd.
+ */
+kda_status_t kda_chunk_fwd_gated(const void* q, const void* k, const void* v, int dtype,
+                                 const void* z, const float* A, float g_min, const void* beta,
+                                 const float* h0, const int32_t* cu_seqlens, int n_seqs, int B,
+                                 int64_t T, int H, int dk, int dv, void* o, float* hT,
+                                 void* workspace, size_t ws_bytes, kda_stream_t stream);
+
+/*
  * kda_chunk_fwd_noalloc -- kda_chunk_fwd without a caller-supplied workspace.
  * The KDA pages have no counterpart for this entry point: it exists for callers
  * that must not allocate device memory where they run the prefill (a serving

@@ -24,6 +24,8 @@ def L():
     lib.kda_chunk_fwd_ex.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i64, i32, i32, i32,
                                      vp, vp, vp, sz, vp, ctypes.c_uint]
     lib.kda_chunk_fwd.argtypes = lib.kda_chunk_fwd_ex.argtypes[:-1]
+    lib.kda_chunk_fwd_gated.argtypes = [vp, vp, vp, i32, vp, vp, ctypes.c_float, vp, vp, vp, i32,
+                                        i32, i64, i32, i32, i32, vp, vp, vp, sz, vp]
     lib.kda_gate.argtypes = [vp, i32, vp, ctypes.c_float, vp, i64, i32, i32, vp, vp, i32, vp]
     lib.kda_recurrent_step.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, vp]
     lib.kda_last_error_string.restype = ctypes.c_char_p
@@ -74,6 +76,23 @@ def test_chunk_rejects_bad_arguments(L):
     assert _chunk(L, cu=FAKE, n_seqs=0) == 1
     assert _chunk(L, q=None) == 1
     assert b"workspace" in L.kda_last_error_string() or L.kda_last_error_string()
+
+
+def _gated(L, dtype=1, g_min=-5.0, z=FAKE, A=FAKE, dk=128, ws_bytes=1 << 40):
+    return L.kda_chunk_fwd_gated(FAKE, FAKE, FAKE, dtype, z, A, g_min, FAKE, None, None, 0, 1, 64,
+                                 2, dk, 128, FAKE, FAKE, FAKE, ws_bytes, None)
+
+
+def test_chunk_gated_rejects_bad_arguments(L):
+    assert _gated(L, dtype=0) == 3       # fp32: call kda_gate, then kda_chunk_fwd
+    assert _gated(L, g_min=-6.0) == 1    # below the tile range bound
+    assert _gated(L, g_min=0.0) == 1
+    assert _gated(L, z=None) == 1
+    assert _gated(L, A=None) == 1
+    assert _gated(L, z=FAKE + 8) == 4
+    assert _gated(L, dk=64) == 2
+    assert _gated(L, ws_bytes=16) == 5
+    assert b"kda_chunk_fwd_gated" in L.kda_last_error_string()
 
 
 def test_workspace_size(L):

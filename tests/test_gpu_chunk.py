@@ -146,13 +146,17 @@ def test_tiny_fp32_workload_end_to_end(kda):
     assert_close(hT, h_ref, torch.float32, "hT tiny")
 
 
-def _full_size(kda, w, sample_pairs, seed):
-    """Runs gate + chunk on a full-size workload (inputs generated on the GPU) and
-    checks sampled (sequence, head) pairs against the oracle."""
+def _full_size(kda, w, sample_pairs, seed, gated=False):
+    """Runs gate + chunk (or the fused-gate chunk) on a full-size workload (inputs
+    generated on the GPU) and checks sampled (sequence, head) pairs against the oracle."""
     dev = workloads.make_inputs(w, "cuda")
-    g = kda.gate(dev["z"], dev["A"])
-    o, hT = kda.chunk_fwd(dev["q"], dev["k"], dev["v"], g, dev["beta"], dev["h0"],
-                          dev["cu_seqlens"])
+    if gated:
+        o, hT = kda.chunk_fwd_gated(dev["q"], dev["k"], dev["v"], dev["z"], dev["A"],
+                                    dev["beta"], dev["h0"], dev["cu_seqlens"])
+    else:
+        g = kda.gate(dev["z"], dev["A"])
+        o, hT = kda.chunk_fwd(dev["q"], dev["k"], dev["v"], g, dev["beta"], dev["h0"],
+                              dev["cu_seqlens"])
     torch.cuda.synchronize()
     cu = dev["cu_seqlens"].cpu().numpy().astype(np.int64)
     r = np.random.default_rng(seed)
@@ -176,6 +180,43 @@ def test_prefill_full_size_sampled(kda):
 def test_varlen_full_size_sampled(kda):
     """32 packed sequences (~270K tokens), H=96: 6 sampled (sequence, head) pairs."""
     _full_size(kda, workloads.varlen(), 6, seed=3)
+
+
+def test_prefill_full_size_sampled_gated(kda):
+    """The same workload through kda_chunk_fwd_gated (gate formed inside the kernels)."""
+    _full_size(kda, workloads.prefill(), 12, seed=4, gated=True)
+
+
+def test_varlen_full_size_sampled_gated(kda):
+    _full_size(kda, workloads.varlen(), 6, seed=5, gated=True)
+
+
+@pytest.mark.parametrize("z_scale,A_val", [(1.0, None), (6.0, 1.0), (6.0, -3.0)],
+                         ids=["random-A", "near-bound", "slow"])
+def test_gated_ragged_varlen(kda, z_scale, A_val):
+    """Fused gate on ragged packed sequences (empty ones included): decays spread
+    over (-5, 0), pushed to the -5 bound (z, A large) and to almost no decay."""
+    lens = [5, 0, 70, 64, 129, 1, 0, 300, 17]
+    w = workloads.custom(lens, H=3, dtype=torch.bfloat16, seed=21, h0_std=0.5)
+    inp = workloads.make_inputs(w, "cpu")
+    z = (inp["z"].float() * z_scale).to(torch.bfloat16)
+    A = inp["A"] if A_val is None else torch.full_like(inp["A"], A_val)
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    o, hT = kda.chunk_fwd_gated(dev["q"], dev["k"], dev["v"], z.cuda(), A.cuda(), dev["beta"],
+                                dev["h0"], dev["cu_seqlens"])
+    g_ref = oracle.gate(z, A)
+    o_ref, h_ref = oracle.recurrence(inp["q"], inp["k"], inp["v"], g_ref, inp["beta"], inp["h0"],
+                                     inp["cu_seqlens"])
+    assert_close(o, o_ref, torch.bfloat16, "o gated")
+    assert_close(hT, h_ref, torch.bfloat16, "hT gated")
+
+
+def test_gated_rejects_fp32(kda):
+    w = workloads.custom([64], H=2, dtype=torch.float32, seed=1)
+    dev = workloads.make_inputs(w, "cuda")
+    with pytest.raises(kda.KdaError):
+        kda.chunk_fwd_gated(dev["q"], dev["k"], dev["v"], dev["z"], dev["A"], dev["beta"], None,
+                            dev["cu_seqlens"])
 
 
 def test_long_context_prefix(kda):
