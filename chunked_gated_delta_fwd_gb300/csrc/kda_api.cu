@@ -87,20 +87,36 @@ ProfScope::~ProfScope() {
   cudaEventRecord(P.recs[slot].stop, stream);
 }
 
-size_t plan_bytes(int n_seqs) {
+static size_t plan_head_bytes(int n_seqs) {
   const size_t b = 2 * sizeof(int32_t) * (size_t)(n_seqs + 1);
   return (b + 255) & ~size_t(255);
 }
 
-// One CTA: writes cu[N+1] (copied from cu_seqlens, or n*T_per_seq) and the
-// exclusive prefix sum of ceil(len/64) into chunk_off[N+1].  Invalid sequence
+size_t plan_bytes(int64_t n_tokens, int n_seqs) {
+  const size_t tab = sizeof(int2) * (size_t)chunks_upper_bound(n_tokens, n_seqs);
+  return plan_head_bytes(n_seqs) + ((tab + 255) & ~size_t(255));
+}
+
+Plan plan_in(void* ws, int64_t n_tokens, int n_seqs) {
+  (void)n_tokens;
+  Plan plan;
+  plan.cu = static_cast<const int32_t*>(ws);
+  plan.chunk_off = plan.cu + (n_seqs + 1);
+  plan.tab = reinterpret_cast<const int2*>(static_cast<const char*>(ws) + plan_head_bytes(n_seqs));
+  plan.n_seqs = n_seqs;
+  return plan;
+}
+
+// One CTA: writes cu[N+1] (copied from cu_seqlens, or n*T_per_seq), the
+// exclusive prefix sum of ceil(len/64) into chunk_off[N+1], and for every chunk
+// its first token and token count into tab.  Invalid sequence
 // offsets (decreasing, outside [0, NT], cu[0] != 0 or cu[N] != NT) are clamped so
 // that no later kernel can index outside the inputs, and flag an error.
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ cu_in, int n_seqs,
                                                     int64_t T_per_seq, int64_t n_tokens,
                                                     int32_t* __restrict__ cu_out,
                                                     int32_t* __restrict__ chunk_off,
-                                                    int* err_flag) {
+                                                    int2* __restrict__ tab, int* err_flag) {
   __shared__ int32_t warp_sums[32];
   __shared__ int32_t carry;
   const int tid = threadIdx.x;
@@ -154,16 +170,29 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
     if (tid == blockDim.x - 1) carry += incl;
     __syncthreads();
   }
+  __syncthreads();
+  const int total = chunk_off[n_seqs];
+  for (int j = tid; j < total; j += blockDim.x) {
+    int lo = 0, hi = n_seqs - 1;  // the last sequence whose chunks start at or before j
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (chunk_off[mid] <= j) lo = mid; else hi = mid - 1;
+    }
+    const int64_t t0 = (int64_t)cu_out[lo] + (int64_t)(j - chunk_off[lo]) * kChunk;
+    const int64_t end = cu_out[lo + 1];
+    tab[j] = make_int2((int)t0, (int)(end - t0 < kChunk ? end - t0 : kChunk));
+  }
   if (bad && err_flag) atomicExch(err_flag, kDevErrBadSeqlens);
 }
 
 cudaError_t launch_plan(const int32_t* cu_seqlens_or_null, int n_seqs, int64_t T_per_seq,
                         int64_t n_tokens, void* ws, int* err_flag, cudaStream_t s) {
-  int32_t* cu = static_cast<int32_t*>(ws);
-  int32_t* off = cu + (n_seqs + 1);
+  const Plan plan = plan_in(ws, n_tokens, n_seqs);
   ProfScope prof_scope("kda_plan", s);
-  plan_kernel<<<1, 1024, 0, s>>>(cu_seqlens_or_null, n_seqs, T_per_seq, n_tokens, cu, off,
-                                 err_flag);
+  plan_kernel<<<1, 1024, 0, s>>>(cu_seqlens_or_null, n_seqs, T_per_seq, n_tokens,
+                                 const_cast<int32_t*>(plan.cu),
+                                 const_cast<int32_t*>(plan.chunk_off),
+                                 const_cast<int2*>(plan.tab), err_flag);
   return cudaGetLastError();
 }
 
@@ -314,9 +343,9 @@ kda_status_t kda_gate(const void* z, int z_dtype, const float* A, float g_min, f
 size_t kda_chunk_fwd_workspace_size(int64_t n_tokens, int n_seqs, int H, int dtype) {
   if (n_tokens < 0 || n_seqs < 1 || H < 1) return 0;
   if (dtype == KDA_BF16)
-    return kda::plan_bytes(n_seqs) + kda::tc_workspace_bytes(n_tokens, n_seqs, H);
+    return kda::plan_bytes(n_tokens, n_seqs) + kda::tc_workspace_bytes(n_tokens, n_seqs, H);
   if (dtype == KDA_F32)
-    return kda::plan_bytes(n_seqs) + kda::simt_workspace_bytes(n_tokens, n_seqs, H);
+    return kda::plan_bytes(n_tokens, n_seqs) + kda::simt_workspace_bytes(n_tokens, n_seqs, H);
   return 0;
 }
 

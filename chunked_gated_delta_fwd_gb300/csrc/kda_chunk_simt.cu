@@ -308,11 +308,8 @@ cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v, int b
                               const float* g, const void* beta, const float* h0, void* o,
                               float* hT, int64_t n_tokens, int n_seqs, int H, void* ws,
                               cudaStream_t s) {
-  Plan plan;
-  plan.cu = static_cast<const int32_t*>(ws);
-  plan.chunk_off = plan.cu + (n_seqs + 1);
-  plan.n_seqs = n_seqs;
-  float* body = reinterpret_cast<float*>(static_cast<char*>(ws) + plan_bytes(n_seqs));
+  const Plan plan = plan_in(ws, n_tokens, n_seqs);
+  float* body = reinterpret_cast<float*>(static_cast<char*>(ws) + plan_bytes(n_tokens, n_seqs));
   const int64_t chunks = chunks_upper_bound(n_tokens, n_seqs);
   const size_t prep_smem = sizeof(PrepSmem), chain_smem = sizeof(ChainSmem);
   cudaError_t e;

@@ -84,8 +84,14 @@ constexpr uint32_t kP_BV = 180224;         // K-major (beta V)^T 128 x 64
 constexpr uint32_t kP_beta = 196608;       // 64 fp32
 constexpr uint32_t kP_Tot = kP_beta + 256; // per-half-tile sums of g, [8][128] fp32
 constexpr uint32_t kP_bars = kP_Tot + 4096;  // in_full, (unused), p, w + TMEM base
-constexpr uint32_t kP_Smem = kP_bars + 128 + 1024;
+// With the gate fused (z staged in bf16) the upper half of the g staging space and
+// one more 16 KB block hold the unit's Gamma*Q and Kt^T tiles on their way out.
+constexpr uint32_t kP_Qs = kI_G + 16384;
+constexpr uint32_t kP_KTs = (kP_bars + 128 + 1023) & ~1023u;
+constexpr uint32_t kP_Smem = kP_KTs + 16384 + 1024;
+static_assert(kP_Smem <= 232448, "prep shared memory");
 constexpr int kLdL = 65, kLdT = 68;
+constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ uint4 pack8(const float* x) {
   return make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
@@ -96,63 +102,67 @@ struct UnitInfo {
   int chunk, h;
   int64_t t0;
   int len;
-  float ea;  // exp(A_h), when the gate is fused
+  float ea;  // exp(A_h) log2(e), when the gate is fused
 };
 
+// Position of unit u = (chunk, head) from the plan's chunk table.  Chunks at or
+// beyond the plan's total read unused table entries and are never processed.
 __device__ __forceinline__ UnitInfo unit_info(const Plan& plan, int H, int64_t u) {
   UnitInfo ui;
   ui.chunk = (int)(u / H);
   ui.h = (int)(u % H);
-  int lo = 0, hi = plan.n_seqs - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(plan.chunk_off + mid) <= ui.chunk) lo = mid; else hi = mid - 1;
-  }
-  ui.t0 = (int64_t)__ldg(plan.cu + lo) + (int64_t)(ui.chunk - __ldg(plan.chunk_off + lo)) * C;
-  ui.len = (int)min((int64_t)C, (int64_t)__ldg(plan.cu + lo + 1) - ui.t0);
+  const int2 e = __ldg(plan.tab + ui.chunk);
+  ui.t0 = e.x;
+  ui.len = e.y;
+  ui.ea = 0.f;
   return ui;
 }
 
 // One block stage of T = (I + L)^{-1}: for every block (a + d, a),
 //   P = sum_{b=a}^{a+d-1} L_{a+d, b} T_{b, a},   T_{a+d, a} = -T_{a+d, a+d} P.
-// 64 threads per block, each owning one row m and four columns.
+// 128 threads per block, each owning one row m and two columns (even and odd
+// k summed separately to halve the dependent chains).
 template <int d>
 __device__ __forceinline__ void inverse_stage(int t, const float* Lb, float* Tb, float* Ps) {
-  const bool act = t < (4 - d) * 64;
-  const int a = t >> 6, tt = t & 63, m = tt >> 2, nq = tt & 3;
+  const bool act = t < (4 - d) * 128;
+  const int a = t >> 7, tt = t & 127, m = tt >> 3, nq = tt & 7;
   const int R = a + d;
   if (act) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float2 e = make_float2(0.f, 0.f), o = make_float2(0.f, 0.f);
 #pragma unroll
     for (int bb = 0; bb < d; ++bb) {
       const int b = a + bb;
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const float l = Lb[(16 * R + m) * kLdL + 16 * b + k];
-        const float4 tv = *reinterpret_cast<const float4*>(Tb + (16 * b + k) * kLdT + 16 * a + 4 * nq);
-        acc[0] = fmaf(l, tv.x, acc[0]);
-        acc[1] = fmaf(l, tv.y, acc[1]);
-        acc[2] = fmaf(l, tv.z, acc[2]);
-        acc[3] = fmaf(l, tv.w, acc[3]);
+      for (int k = 0; k < 16; k += 2) {
+        const float l0 = Lb[(16 * R + m) * kLdL + 16 * b + k];
+        const float l1 = Lb[(16 * R + m) * kLdL + 16 * b + k + 1];
+        const float2 t0 = *reinterpret_cast<const float2*>(Tb + (16 * b + k) * kLdT + 16 * a + 2 * nq);
+        const float2 t1 =
+            *reinterpret_cast<const float2*>(Tb + (16 * b + k + 1) * kLdT + 16 * a + 2 * nq);
+        e.x = fmaf(l0, t0.x, e.x);
+        e.y = fmaf(l0, t0.y, e.y);
+        o.x = fmaf(l1, t1.x, o.x);
+        o.y = fmaf(l1, t1.y, o.y);
       }
     }
-    *reinterpret_cast<float4*>(Ps + a * 256 + m * 16 + 4 * nq) =
-        make_float4(acc[0], acc[1], acc[2], acc[3]);
+    *reinterpret_cast<float2*>(Ps + a * 256 + m * 16 + 2 * nq) = make_float2(e.x + o.x, e.y + o.y);
   }
   named_sync(1, kPrepCompute);
   if (act) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float2 e = make_float2(0.f, 0.f), o = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int kk = 0; kk < 16; ++kk) {  // T_RR is unit lower triangular with stored zeros
-      const float w = Tb[(16 * R + m) * kLdT + 16 * R + kk];
-      const float4 pv = *reinterpret_cast<const float4*>(Ps + a * 256 + kk * 16 + 4 * nq);
-      acc[0] = fmaf(w, pv.x, acc[0]);
-      acc[1] = fmaf(w, pv.y, acc[1]);
-      acc[2] = fmaf(w, pv.z, acc[2]);
-      acc[3] = fmaf(w, pv.w, acc[3]);
+    for (int kk = 0; kk < 16; kk += 2) {  // T_RR is unit lower triangular with stored zeros
+      const float w0 = Tb[(16 * R + m) * kLdT + 16 * R + kk];
+      const float w1 = Tb[(16 * R + m) * kLdT + 16 * R + kk + 1];
+      const float2 p0 = *reinterpret_cast<const float2*>(Ps + a * 256 + kk * 16 + 2 * nq);
+      const float2 p1 = *reinterpret_cast<const float2*>(Ps + a * 256 + (kk + 1) * 16 + 2 * nq);
+      e.x = fmaf(w0, p0.x, e.x);
+      e.y = fmaf(w0, p0.y, e.y);
+      o.x = fmaf(w1, p1.x, o.x);
+      o.y = fmaf(w1, p1.y, o.y);
     }
-    *reinterpret_cast<float4*>(Tb + (16 * R + m) * kLdT + 16 * a + 4 * nq) =
-        make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
+    *reinterpret_cast<float2*>(Tb + (16 * R + m) * kLdT + 16 * a + 2 * nq) =
+        make_float2(-(e.x + o.x), -(e.y + o.y));
   }
   named_sync(1, kPrepCompute);
 }
@@ -195,16 +205,19 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int total = __ldg(plan.chunk_off + plan.n_seqs);
+  const float gmin2 = g_min * kLog2e;  // the fused gate's bound in base-2 units
 
   // Inputs: one tensor copy per input per unit (64 tokens x 1 head x 128
   // channels) into the single staging buffer. Thread kIssuer issues unit n+1's
   // copies as soon as every thread has read unit n's rows into registers.
-  // Unit positions run two units ahead in a two-slot ring (slot n & 1): while
-  // warps 0-1 invert unit n's diagonal blocks, warps 2-3 fetch beta of unit
-  // n+1 and the position of unit n+2, and thread kPrefetcher warms L2 with
-  // unit n+2's rows, so no global-load latency sits on the critical path.
-  // Tokens past the end of the packed batch arrive as zeros; tokens of the
-  // next sequence are masked below.
+  // Unit positions run two units ahead in a two-slot ring (slot n & 1), read from
+  // the plan's chunk table: while unit n's products run on the tensor cores,
+  // warps 2-3 load beta of unit n+1 and threads kLocator / kPrefetcher load the
+  // table entry of unit n+2; the entry is written to its slot, and unit n+2's
+  // rows are prefetched into L2, only after the inverse, once the loads have
+  // long arrived.  No global-load latency sits on the critical path.  Tokens past
+  // the end of the packed batch arrive as zeros; tokens of the next sequence are
+  // masked below.
   constexpr int kIssuer = 64, kLocator = 96, kPrefetcher = 128, kStorer = 192;
   UnitInfo* slots = reinterpret_cast<UnitInfo*>(sm + kP_bars + 64);
   uint32_t issued = 0;  // copies issued (thread kIssuer)
@@ -212,7 +225,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
   auto locate = [&](int64_t u) {
     UnitInfo ui;
     if (u < units_ub) ui = unit_info(plan, H, u); else ui.chunk = total;
-    ui.ea = (kZ && ui.chunk < total) ? expf(__ldg(A + ui.h)) : 0.f;
+    ui.ea = (kZ && ui.chunk < total) ? expf(__ldg(A + ui.h)) * kLog2e : 0.f;
     return ui;
   };
   auto issue_copies = [&](const UnitInfo& ui) {
@@ -225,31 +238,76 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     tma_load_3d(sbase + kI_G, &tm_g, 0, ui.h, t0, bar_full);
     ++issued;
   };
-  // warps 2-3 (+ kPrefetcher): beta of unit `un` (slot sn), position of unit `uf` into slot sf
-  auto fetch_ahead = [&](const UnitInfo& un, int64_t uf, int sf) {
-    if (t >= 64 && t < 128) {
+  // pending table entry of the unit two ahead (threads kLocator and kPrefetcher)
+  bool pend_ok = false;
+  int pend_chunk = 0, pend_h = 0;
+  int2 pend_e = make_int2(0, 0);
+  float pend_a = 0.f;
+  // (chunk, head) of the unit two ahead, stepped by the grid size without dividing
+  const int64_t chunks_ub = units_ub / H;
+  const int grid_q = (int)(gridDim.x / H), grid_r = (int)(gridDim.x % H);
+  int64_t uf_chunk;
+  int uf_h;
+  {
+    const int64_t u2 = blockIdx.x + 2 * (int64_t)gridDim.x;
+    uf_chunk = u2 / H;
+    uf_h = (int)(u2 % H);
+  }
+  // loads only: beta of unit `un`, the table entry (and A_h) of the unit two ahead;
+  // then steps that unit by the grid
+  auto fetch_start = [&](const UnitInfo& un) {
+    if (t >= 64 && t < 128)
       beta_nx = (un.chunk < total && t - 64 < un.len)
                     ? __bfloat162float(beta[(un.t0 + t - 64) * H + un.h]) : 0.f;
-      if (t == kLocator) slots[sf] = locate(uf);
-    } else if (t == kPrefetcher) {
-      const UnitInfo ui = locate(uf);
-      if (ui.chunk < total) {
-        const int t0 = (int)ui.t0;
-        tma_prefetch_l2_3d(&tm_k, 0, ui.h, t0);
-        tma_prefetch_l2_3d(&tm_q, 0, ui.h, t0);
-        tma_prefetch_l2_3d(&tm_v, 0, ui.h, t0);
-        tma_prefetch_l2_3d(&tm_g, 0, ui.h, t0);
+    if (t == kLocator || t == kPrefetcher) {
+      pend_ok = uf_chunk < chunks_ub;
+      if (pend_ok) {
+        pend_chunk = (int)uf_chunk;
+        pend_h = uf_h;
+        pend_e = __ldg(plan.tab + pend_chunk);
+        if (kZ) pend_a = __ldg(A + pend_h);
+      }
+      uf_chunk += grid_q;
+      uf_h += grid_r;
+      if (uf_h >= H) {
+        uf_h -= H;
+        ++uf_chunk;
       }
     }
   };
+  // uses of the loads: slot sf <- unit `uf`, its rows into L2
+  auto fetch_finish = [&](int sf) {
+    const bool live = pend_ok && pend_chunk < total;
+    if (t == kLocator) {
+      UnitInfo ui;
+      ui.chunk = live ? pend_chunk : total;
+      ui.h = pend_h;
+      ui.t0 = pend_e.x;
+      ui.len = pend_e.y;
+      ui.ea = (kZ && live) ? expf(pend_a) * kLog2e : 0.f;
+      slots[sf] = ui;
+    } else if (t == kPrefetcher && live) {
+      tma_prefetch_l2_3d(&tm_k, 0, pend_h, pend_e.x);
+      tma_prefetch_l2_3d(&tm_q, 0, pend_h, pend_e.x);
+      tma_prefetch_l2_3d(&tm_v, 0, pend_h, pend_e.x);
+      tma_prefetch_l2_3d(&tm_g, 0, pend_h, pend_e.x);
+    }
+  };
   if (t == kLocator) {
-    const UnitInfo u0 = locate(blockIdx.x);
-    slots[0] = u0;
+    slots[0] = locate(blockIdx.x);
     slots[1] = locate(blockIdx.x + gridDim.x);
   }
   named_sync(1, kPrepCompute);
   if (t == kIssuer) issue_copies(slots[0]);
-  fetch_ahead(slots[0], blockIdx.x + gridDim.x, 1);  // slot 1 is rewritten with the same position
+  if (t >= 64 && t < 128)  // beta of unit 0
+    beta_nx = (slots[0].chunk < total && t - 64 < slots[0].len)
+                  ? __bfloat162float(beta[(slots[0].t0 + t - 64) * H + slots[0].h]) : 0.f;
+  if (t == kPrefetcher && slots[1].chunk < total) {  // unit 1's rows into L2
+    tma_prefetch_l2_3d(&tm_k, 0, slots[1].h, (int)slots[1].t0);
+    tma_prefetch_l2_3d(&tm_q, 0, slots[1].h, (int)slots[1].t0);
+    tma_prefetch_l2_3d(&tm_v, 0, slots[1].h, (int)slots[1].t0);
+    tma_prefetch_l2_3d(&tm_g, 0, slots[1].h, (int)slots[1].t0);
+  }
   named_sync(1, kPrepCompute);
   uint32_t it = 0;
   {
@@ -272,11 +330,11 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       const int len = ui.len;
       uint8_t* unit = tiles + (size_t)u * kUnitBytes;
       if (t >= 64 && t < 128) beta_s[t - 64] = beta_nx;
-      if (t == kStorer) bulk_wait_read_all();  // the staging space is rewritten below
       bool ok = mbar_wait(bar_full, it & 1, err);
       if (!named_sync_and(1, kPrepCompute, ok)) break;
 
-      // ---- pass 1: running log-decay over this thread's 8 rows, both channels
+      // ---- pass 1: running log-decay over this thread's 8 rows, both channels, in
+      //      base-2 units (G log2 e) so that every decay below is one ex2
       const int r0 = 16 * ta + 8 * hq;
       float Gl[2][8];
       {
@@ -289,10 +347,12 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             if constexpr (kZ) {  // g = g_min / (1 + exp(-exp(A_h) z))
               const uint32_t zw = *reinterpret_cast<const uint32_t*>(
                   reinterpret_cast<const __nv_bfloat16*>(sG) + r * D + cp);
-              gg.x = __fdividef(g_min, 1.f + __expf(-ui.ea * bf16_lo(zw)));
-              gg.y = __fdividef(g_min, 1.f + __expf(-ui.ea * bf16_hi(zw)));
+              gg.x = __fdividef(gmin2, 1.f + exp2_approx(-ui.ea * bf16_lo(zw)));
+              gg.y = __fdividef(gmin2, 1.f + exp2_approx(-ui.ea * bf16_hi(zw)));
             } else {
               gg = *reinterpret_cast<const float2*>(sG + r * D + cp);
+              gg.x *= kLog2e;
+              gg.y *= kLog2e;
             }
           }
           s0 += gg.x;
@@ -302,6 +362,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         }
         *reinterpret_cast<float2*>(Tot + rg * D + cp) = make_float2(s0, s1);
       }
+      if (t == kStorer) bulk_wait_read_all();  // pass 2 rewrites the staging space
       named_sync(1, kPrepCompute);
 
       // ---- pass 2: operands of this thread's 8 rows, one channel at a time
@@ -330,6 +391,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         }
       }
 #pragma unroll
+      float gam_c[2];  // gamma_C of this thread's two channels
+#pragma unroll
       for (int o2 = 0; o2 < 2; ++o2) {
         const int s2 = o2 ^ sw, c = cp + s2;
         // R_b = sum of the half-tile sums before tile b; G_C = all of them
@@ -342,14 +405,14 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
           GC += h0s + h1s;
         }
         const float Ra = ta == 0 ? R[0] : (ta == 1 ? R[1] : (ta == 2 ? R[2] : R[3]));
-        const float eRa = __expf(Ra);       // exp(R_a) <= 1
-        const float eCa = __expf(GC - Ra);  // exp(G_C - R_a) <= 1
+        const float eRa = exp2_approx(Ra);       // exp(R_a) <= 1
+        const float eCa = exp2_approx(GC - Ra);  // exp(G_C - R_a) <= 1
         float f[8], fi[8], kv[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float dd = Gl[o2][e] + inner;  // G_r - R_a, in (-80, 0]
-          f[e] = __expf(dd);
-          fi[e] = __expf(-dd);
+          f[e] = exp2_approx(dd);
+          fi[e] = exp2_approx(-dd);
           kv[e] = o2 ? bf16_hi(kw[e]) : bf16_lo(kw[e]);
         }
         float x[8];
@@ -364,7 +427,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         *reinterpret_cast<uint4*>(sm + kP_Bop + mn_chunk(128, 4 * ta + 2 + hq, c)) = pack8(x);
 #pragma unroll
         for (int e = 0; e < 8; ++e) x[e] *= eRa;  // Gamma q
-        *reinterpret_cast<uint4*>(unit + kQ + mn_chunk(64, 2 * ta + hq, c)) = pack8(x);
+        *reinterpret_cast<uint4*>((kZ ? sm + kP_Qs : unit + kQ) + mn_chunk(64, 2 * ta + hq, c)) =
+            pack8(x);
 #pragma unroll
         for (int e = 0; e < 8; ++e) x[e] = (o2 ? bf16_hi(vw[e]) : bf16_lo(vw[e])) * bt[e];
         *reinterpret_cast<uint4*>(sm + kP_BV + sw128_chunk(128, c, 2 * ta + hq)) = pack8(x);
@@ -372,17 +436,18 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         for (int e = 0; e < 8; ++e) kv[e] *= fi[e];  // k exp(R_a - G_r)
 #pragma unroll
         for (int e = 0; e < 8; ++e) x[e] = kv[e] * eCa;  // (gamma_C / Gamma) k
-        *reinterpret_cast<uint4*>(unit + kKT + sw128_chunk(128, c, 2 * ta + hq)) = pack8(x);
+        *reinterpret_cast<uint4*>((kZ ? sm + kP_KTs : unit + kKT) +
+                                  sw128_chunk(128, c, 2 * ta + hq)) = pack8(x);
 #pragma unroll
         for (int ap = 0; ap < 4; ++ap) {
           if (ap < ta) continue;
-          const float E = (ap > ta) ? __expf(R[ap] - Ra) : 1.f;  // exp(R_ap - R_a) <= 1
+          const float E = (ap > ta) ? exp2_approx(R[ap] - Ra) : 1.f;  // exp(R_ap - R_a) <= 1
 #pragma unroll
           for (int e = 0; e < 8; ++e) x[e] = kv[e] * E;
           *reinterpret_cast<uint4*>(sm + kP_KC + mn_chunk(kKCX, ap * (ap + 1) + 2 * ta + hq, c)) =
               pack8(x);
         }
-        if (rg == 0) gam_out[(size_t)u * D + c] = __expf(GC);
+        gam_c[o2] = exp2_approx(GC);
       }
 
       // ---- block products in one N=192 MMA chain: D[m][n] = Bop row m . KC row n
@@ -398,6 +463,17 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
           mma_bf16(tmem + 0, mnmajor_desc(sbase + kP_Bop, 2048, s),
                    mnmajor_desc(sbase + kP_KC, mn_sbo(kKCX), s), id, s > 0);
         mma_commit(bar_p);
+      }
+      // loads for the units ahead while the products run
+      fetch_start(slots[(it + 1) & 1]);
+      if (rg == 0) {  // global stores only after the proxy fence above (it waits for them)
+        gam_out[(size_t)u * D + cp + sw] = gam_c[0];
+        gam_out[(size_t)u * D + cp + (sw ^ 1)] = gam_c[1];
+      }
+      if (kZ && t == kStorer) {
+        bulk_s2g(unit + kQ, sbase + kP_Qs, 16384);
+        bulk_s2g(unit + kKT, sbase + kP_KTs, 16384);
+        bulk_commit();
       }
       ok = mbar_wait(bar_p, it & 1, err);
       if (!named_sync_and(1, kPrepCompute, ok)) break;
@@ -427,31 +503,47 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
           for (int jj = 0; jj < 16; ++jj) pv[jj] = (16 * pc + jj <= r) ? pv[jj] : 0.f;
           *reinterpret_cast<uint4*>(sm + kP_AQs + sw128_chunk(64, r, 2 * pc)) = pack8(pv);
           *reinterpret_cast<uint4*>(sm + kP_AQs + sw128_chunk(64, r, 2 * pc + 1)) = pack8(pv + 8);
-          fence_proxy_async_smem();
         }
       }
       named_sync(1, kPrepCompute);
-      if (t == kStorer) {  // the staged tiles leave as whole-tile bulk copies
-        bulk_s2g(unit + kAQ, sbase + kP_AQs, 8192);
-        bulk_commit();
-      }
 
-      // ---- T = (I + L)^{-1} in fp32: diagonal 16x16 blocks by forward substitution
-      //      (one column per thread), then the three block-substitution stages
-      if (t < C) {
-        const int ba = t >> 4, cc = t & 15, o = 16 * ba;
-        float x[16];
+      // ---- T = (I + L)^{-1} in fp32.  Each diagonal 16x16 block from its 8x8 halves,
+      //      [A 0; C B]^{-1} = [A^{-1} 0; -B^{-1} C A^{-1}  B^{-1}], then the three
+      //      block-substitution stages for the blocks below the diagonal
+      if (t < C) {  // A^{-1}, B^{-1}: 8x8 forward substitution, one column per thread
+        const int ob = 8 * (t >> 3), cc = t & 7;
+        float x[8];
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
+        for (int m = 0; m < 8; ++m) {
           float acc = 0.f;
 #pragma unroll
-          for (int i2 = 0; i2 < m; ++i2) acc = fmaf(Lb[(o + m) * kLdL + o + i2], x[i2], acc);
+          for (int i2 = 0; i2 < m; ++i2) acc = fmaf(Lb[(ob + m) * kLdL + ob + i2], x[i2], acc);
           x[m] = (m < cc) ? 0.f : (m == cc ? 1.f : -acc);
         }
 #pragma unroll
-        for (int m = 0; m < 16; ++m) Tb[(o + m) * kLdT + o + cc] = x[m];
-      } else {
-        fetch_ahead(slots[(it + 1) & 1], u + 2 * (int64_t)gridDim.x, it & 1);
+        for (int m = 0; m < 8; ++m) Tb[(ob + m) * kLdT + ob + cc] = x[m];
+        if (((t >> 3) & 1) == 0) {  // the zero upper-right 8x8 of the 16x16 block
+#pragma unroll
+          for (int m = 0; m < 8; ++m) Tb[(ob + m) * kLdT + ob + 8 + cc] = 0.f;
+        }
+      }
+      named_sync(1, kPrepCompute);
+      if (t < 256) {  // P = C A^{-1} per block
+        const int ba = t >> 6, i = (t >> 3) & 7, j = t & 7, o = 16 * ba;
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)  // A^{-1} has stored zeros above the diagonal
+          acc = fmaf(Lb[(o + 8 + i) * kLdL + o + k], Tb[(o + k) * kLdT + o + j], acc);
+        Ps[ba * 64 + i * 8 + j] = acc;
+      }
+      named_sync(1, kPrepCompute);
+      if (t < 256) {  // lower-left 8x8 = -B^{-1} P
+        const int ba = t >> 6, i = (t >> 3) & 7, j = t & 7, o = 16 * ba;
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)  // B^{-1} has stored zeros above the diagonal
+          acc = fmaf(Tb[(o + 8 + i) * kLdT + o + 8 + k], Ps[ba * 64 + k * 8 + j], acc);
+        Tb[(o + 8 + i) * kLdT + o + j] = -acc;
       }
       named_sync(1, kPrepCompute);
       inverse_stage<1>(t, Lb, Tb, Ps);
@@ -467,6 +559,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         }
         *reinterpret_cast<uint4*>(sm + kP_T + mn_chunk(64, o8, j)) = pack8(x);
       }
+      fetch_finish(it & 1);
       fence_proxy_async_smem();
       tc_fence_before();
       named_sync(1, kPrepCompute);
@@ -503,7 +596,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       named_sync(1, kPrepCompute);
-      if (t == kStorer) {
+      if (t == kStorer) {  // staged tiles leave as whole-tile bulk copies
+        bulk_s2g(unit + kAQ, sbase + kP_AQs, 8192);
         bulk_s2g(unit + kW, sbase + kP_BKg, 16384);
         bulk_s2g(unit + kUT, sbase + kP_BV, 16384);
         bulk_commit();
@@ -857,12 +951,9 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
                             const void* z, const float* A, float g_min, const void* beta,
                             const float* h0, void* o, float* hT, int64_t n_tokens, int n_seqs,
                             int H, void* ws, int* err, cudaStream_t s) {
-  Plan plan;
-  plan.cu = static_cast<const int32_t*>(ws);
-  plan.chunk_off = plan.cu + (n_seqs + 1);
-  plan.n_seqs = n_seqs;
+  const Plan plan = plan_in(ws, n_tokens, n_seqs);
   const int64_t units = chunks_upper_bound(n_tokens, n_seqs) * H;
-  uintptr_t body = reinterpret_cast<uintptr_t>(ws) + plan_bytes(n_seqs);
+  uintptr_t body = reinterpret_cast<uintptr_t>(ws) + plan_bytes(n_tokens, n_seqs);
   body = (body + 1023) & ~uintptr_t(1023);
   uint8_t* tiles = reinterpret_cast<uint8_t*>(body);
   float* gam = reinterpret_cast<float*>(tiles + (size_t)units * kUnitBytes);

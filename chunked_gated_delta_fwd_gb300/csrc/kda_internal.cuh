@@ -76,9 +76,12 @@ __device__ __forceinline__ void load4(const __nv_bfloat16* p, float* out) {
 struct Plan {
   const int32_t* cu;
   const int32_t* chunk_off;
+  const int2* tab;  // per chunk: (first token, token count)
   int n_seqs;
 };
-size_t plan_bytes(int n_seqs);
+size_t plan_bytes(int64_t n_tokens, int n_seqs);
+// The plan arrays as laid out at the start of the workspace.
+Plan plan_in(void* ws, int64_t n_tokens, int n_seqs);
 cudaError_t launch_plan(const int32_t* cu_seqlens_or_null, int n_seqs, int64_t T_per_seq,
                         int64_t n_tokens, void* ws, int* err_flag, cudaStream_t s);
 // Upper bound of the number of 64-token chunks of n_seqs sequences totalling n_tokens.
