@@ -446,6 +446,38 @@ def run_gpu(args):
     return 0
 
 
+def run_profile_case(args):
+    """A small case for ncu captures (a few GB on the device at most, inputs above
+    L2): one decode step on N=128 x H=96 (0.8 GB state), then --reps prefill steps
+    (fused gate, and gate + chunk) on B=1, T=8192, H=32 bf16.  Prints one line."""
+    import torch
+
+    import chunked_gated_delta_fwd_gb300 as kda
+    import workloads
+
+    dev = torch.device("cuda", 0)
+    dw = workloads.DecodeWorkload("profile decode", N=128, H=96)
+    S = workloads.make_decode_state(dw, dev)
+    di = workloads.make_decode_step(dw, 0, dev)
+    dg = kda.gate(di["z"], di["A"])
+    kda.recurrent_step(di["q"], di["k"], di["v"], dg, di["beta"], S)
+    torch.cuda.synchronize(dev)
+    del S
+    w = workloads.custom([8192], H=32, dtype=torch.bfloat16, seed=3, h0_std=0.02)
+    inp = workloads.make_inputs(w, dev)
+    for _ in range(args.reps):
+        o, hT = kda.chunk_fwd_gated(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"],
+                                    inp["beta"], inp["h0"], inp["cu_seqlens"])
+        g = kda.gate(inp["z"], inp["A"])
+        o2, _ = kda.chunk_fwd(inp["q"], inp["k"], inp["v"], g, inp["beta"], inp["h0"],
+                              inp["cu_seqlens"])
+    torch.cuda.synchronize(dev)
+    print(json.dumps({"profile_case": "decode N=128 H=96; prefill B=1 T=8192 H=32",
+                      "reps": args.reps, "o_mean_abs": float(o.float().abs().mean()),
+                      "paths_max_diff": float((o.float() - o2.float()).abs().max())}))
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -457,7 +489,12 @@ def main(argv=None):
     ap.add_argument("--path", choices=["fused", "separate"], default="fused",
                     help="prefill step: gate fused into the chunk kernels, or kda_gate then "
                          "kda_chunk_fwd (the other one is timed too, as alt_step)")
+    ap.add_argument("--profile-case", action="store_true",
+                    help="run the small profiling case (for ncu captures) instead of the bench")
+    ap.add_argument("--reps", type=int, default=2, help="prefill steps of --profile-case")
     args = ap.parse_args(argv)
+    if args.profile_case:
+        return run_profile_case(args)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
