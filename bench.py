@@ -182,6 +182,19 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The maximum of x over all ranks of the default process group (x itself on
+    one rank): the job's time is that of its slowest rank."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_reference(args):
     """The oracle, timed on the host cores over a bounded sample of the workload."""
     rank, world, _ = dist_env()
@@ -314,12 +327,7 @@ def run_gpu(args):
         stop.record(stream)
         barrier()
         clocks.mark(False)
-        ms = start.elapsed_time(stop) / steps
-        if world > 1:
-            t = torch.tensor([ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms
+        return max_over_ranks(start.elapsed_time(stop) / steps, world, dev)
 
     clocks = ClockSampler(dev.index or 0)
     clocks.start()
