@@ -459,9 +459,12 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       if (t == 0) {
         tc_fence_after();
         const uint32_t id = idesc_bf16_mn(128, kKCX, 1, 1);
+        const uint64_t da = mnmajor_desc(sbase + kP_Bop, 2048, 0);
+        const uint64_t db = mnmajor_desc(sbase + kP_KC, mn_sbo(kKCX), 0);
+#pragma unroll
         for (int s = 0; s < D / 16; ++s)
-          mma_bf16(tmem + 0, mnmajor_desc(sbase + kP_Bop, 2048, s),
-                   mnmajor_desc(sbase + kP_KC, mn_sbo(kKCX), s), id, s > 0);
+          mma_bf16(tmem + 0, desc_advance(da, s * 2 * 2048), desc_advance(db, s * 2 * mn_sbo(kKCX)),
+                   id, s > 0);
         mma_commit(bar_p);
       }
       // loads for the units ahead while the products run
@@ -566,12 +569,15 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       if (t == 0) {
         tc_fence_after();
         const uint32_t id = idesc_bf16_mn(128, 64, 0, 1);
+        const uint64_t dk = kmajor_desc(sbase + kP_BKg, 128, 0);
+        const uint64_t dv = kmajor_desc(sbase + kP_BV, 128, 0);
+        const uint64_t dt = mnmajor_desc(sbase + kP_T, 1024, 0);
+#pragma unroll
         for (int s = 0; s < C / 16; ++s)  // W^T = (beta Gamma K)^T T^T
-          mma_bf16(tmem + 256, kmajor_desc(sbase + kP_BKg, 128, s),
-                   mnmajor_desc(sbase + kP_T, 1024, s), id, s > 0);
+          mma_bf16(tmem + 256, desc_advance(dk, s * 32), desc_advance(dt, s * 2048), id, s > 0);
+#pragma unroll
         for (int s = 0; s < C / 16; ++s)  // U^T = (beta V)^T T^T
-          mma_bf16(tmem + 320, kmajor_desc(sbase + kP_BV, 128, s),
-                   mnmajor_desc(sbase + kP_T, 1024, s), id, s > 0);
+          mma_bf16(tmem + 320, desc_advance(dv, s * 32), desc_advance(dt, s * 2048), id, s > 0);
         mma_commit(bar_w);
       }
       ok = mbar_wait(bar_w, it & 1, err);
@@ -625,7 +631,7 @@ constexpr uint32_t kT_SB = 384, kT_VT = 448;
 constexpr uint32_t kC_Smem = kC_bars + 128 + 1024;
 constexpr int kEpi = 256;    // epilogue warps 0-7: (TMEM lane, column half)
 constexpr int kStore = 128;  // store warps 8-11: TMEM lane = value row, all 64 tokens
-constexpr int kMmaWarp = (kEpi + kStore) / 32;  // warp 12: copies + MMA issue
+constexpr int kCopyWarp = (kEpi + kStore) / 32;  // warp 12: tile copies
 constexpr int kChainThreads = kEpi + kStore + 32;
 
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int* err,
@@ -653,24 +659,24 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_addr(sm);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kC_bars);
-  // bars: 0..2 = full[stage], 3 = S copy ready, 4 = MMA1 done, 5 = Vt ready (S scaled),
-  //       6 = S update done, 7,8 = O of D1 buffer b final, 9,10 = D1 buffer b read out,
-  //       11 = drain (abort path)
-  const uint32_t bar_full0 = smem_addr(&bars[0]);
-  const uint32_t bar_s = smem_addr(&bars[3]), bar_m1 = smem_addr(&bars[4]);
-  const uint32_t bar_vt = smem_addr(&bars[5]), bar_m2 = smem_addr(&bars[6]);
-  const uint32_t bar_o0 = smem_addr(&bars[7]), bar_f0 = smem_addr(&bars[9]);
-  const uint32_t bar_dr = smem_addr(&bars[11]);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kC_bars + 96);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kC_bars + 104);
+  // bars: 0..2 = full[stage], 3..5 = empty[stage] (every MMA of its chunk done),
+  //       6 = MMA1 done, 7 = S update done, 8,9 = O of D1 buffer b final,
+  //       10,11 = D1 buffer b read out, 12 = drain (abort path)
+  const uint32_t bar_full0 = smem_addr(&bars[0]), bar_empty0 = smem_addr(&bars[3]);
+  const uint32_t bar_m1 = smem_addr(&bars[6]), bar_m2 = smem_addr(&bars[7]);
+  const uint32_t bar_o0 = smem_addr(&bars[8]), bar_f0 = smem_addr(&bars[10]);
+  const uint32_t bar_dr = smem_addr(&bars[12]);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kC_bars + 112);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kC_bars + 120);
   const int t = threadIdx.x, warp = t >> 5;
   const int n = blockIdx.x, h = blockIdx.y;
 
   if (t == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(bar_full0 + 8 * s, 1);
-    mbar_init(bar_s, kEpi);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar_full0 + 8 * s, 1);
+      mbar_init(bar_empty0 + 8 * s, 1);
+    }
     mbar_init(bar_m1, 1);
-    mbar_init(bar_vt, kEpi);
     mbar_init(bar_m2, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_o0 + 8 * b, 1);
@@ -691,8 +697,12 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   const int64_t tend = max(tstart, (int64_t)__ldg(plan.cu + n + 1));
   const int64_t state = ((int64_t)n * H + h) * D * D;
 
-  if (warp == kMmaWarp) {
-    // ------------------------------------------------ copies + MMA issue (one thread)
+  if (warp == kCopyWarp) {
+    // ------------------------------------------------------ tile copies (one thread)
+    // A stage is refilled once every MMA of the chunk it held has completed (its
+    // empty barrier, committed after the chunk's last MMA): the refill for chunk
+    // jj + kStages is what lets that stage's barriers advance again, so no wait
+    // here can fall two phases behind.
     if ((t & 31) == 0) {
       auto issue = [&](int jj) {
         const int s = jj % kStages;
@@ -702,70 +712,17 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         bulk_g2s(sbase + s * kStageBytes, tiles + (size_t)u * kUnitBytes, kUnitBytes, bar);
         bulk_g2s(sbase + s * kStageBytes + kUnitBytes, gam + (size_t)u * D, kGamBytes, bar);
       };
-      int issued = 0, consumed = 0;
+      int issued = 0;
       for (; issued < min(kStages, nch); ++issued) issue(issued);
-      const uint32_t id1 = idesc_bf16_mn(128, 128, 0, 1);   // S^T x WQ (MN-major B)
-      const uint32_t id2a = idesc_bf16_mn(128, 64, 0, 0);   // Vt^T x A_qk^T (K-major B)
-      const uint32_t id2b = idesc_bf16_mn(128, 128, 0, 0);  // Vt^T x Kt^T (K-major B)
-      int j = 0;
-      bool any_mma = false;
-      // O^T += Vt^T A_qk^T of chunk jj, issued one chunk late (after the next chunk's
-      // MMA1), where it measured faster than right after the state update.
-      auto o_mma = [&](int jj) {
-        const uint32_t stj = sbase + (jj % kStages) * kStageBytes;
-        const uint32_t d1j = tmem + 128 + 128 * (jj & 1);
-        for (int ks = 0; ks < C / 16; ++ks)
-          mma_bf16_ta(d1j + 64, tmem + kT_VT + 32 * (jj & 1) + 8 * ks,
-                      kmajor_desc(stj + kAQ, 64, ks), id2a, 1u);
-        mma_commit(bar_o0 + 8 * (jj & 1));  // every MMA of chunk jj is complete
-      };
-      // the stage of chunk jj is refilled once every MMA of chunk jj has read it (done
-      // one chunk later, when that is certainly the case)
-      auto refill = [&](int jj) -> bool {
-        if (jj + kStages >= nch) return true;
-        if (!wait_or_abort(bar_o0 + 8 * (jj & 1), (jj >> 1) & 1, err, abort_flag)) return false;
-        issue(issued++);
-        return true;
-      };
-      for (; j < nch; ++j) {
-        const int s = j % kStages;
-        const uint32_t st = sbase + s * kStageBytes;
-        if (!wait_or_abort(bar_s, j & 1, err, abort_flag)) break;
-        if (!wait_or_abort(bar_full0 + 8 * s, (j / kStages) & 1, err, abort_flag)) break;
-        consumed = j + 1;
-        // D1 buffer j&1 must have been read out by the store warps (chunk j-2)
-        if (j >= 2 && !wait_or_abort(bar_f0 + 8 * (j & 1), ((j - 2) >> 1) & 1, err, abort_flag))
+      for (int jj = 0; issued < nch; ++jj) {
+        if (!wait_or_abort(bar_empty0 + 8 * (jj % kStages), (jj / kStages) & 1, err, abort_flag))
           break;
-        tc_fence_after();
-        const uint32_t d1 = tmem + 128 + 128 * (j & 1);
-        // (W S)^T | (Gamma Q S)^T in one N = 128 product, A = bf16 S^T from TMEM
-        for (int ks = 0; ks < D / 16; ++ks)
-          mma_bf16_ta(d1, tmem + kT_SB + 8 * ks, mnmajor_desc_lbo(st + kW, kQ - kW, 1024, ks), id1,
-                      ks > 0);
-        mma_commit(bar_m1);
-        any_mma = true;
-        if (j > 0) o_mma(j - 1);
-        if (!wait_or_abort(bar_vt, j & 1, err, abort_flag)) break;
-        tc_fence_after();
-        // S^T += Vt^T Kt (the scaled state is ordered by the Vt barrier)
-        for (int ks = 0; ks < C / 16; ++ks)
-          mma_bf16_ta(tmem + 0, tmem + kT_VT + 32 * (j & 1) + 8 * ks,
-                      kmajor_desc(st + kKT, 128, ks), id2b, 1u);
-        mma_commit(bar_m2);
-        if (j > 0 && !refill(j - 1)) break;
-      }
-      if (!*abort_flag && nch > 0) {
-        o_mma(nch - 1);
-        refill(nch - 1);
+        issue(issued++);
       }
       if (*abort_flag) {
-        // drain: copies and MMAs already issued must land before the CTA exits
-        for (int jj = consumed; jj < issued; ++jj)
+        // copies already issued must land before the CTA exits
+        for (int jj = max(0, issued - kStages); jj < issued; ++jj)
           mbar_wait(bar_full0 + 8 * (jj % kStages), (jj / kStages) & 1, nullptr);
-        if (any_mma) {
-          mma_commit(bar_dr);
-          mbar_wait(bar_dr, 0, nullptr);
-        }
       }
     }
   } else if (warp < kEpi / 32) {
@@ -791,45 +748,69 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       }
       tmem_wait_st();
     }
+    // Thread 0 issues the MMAs as soon as the epilogue warps meet at a named
+    // barrier (measured faster than handing off to a separate MMA warp, through
+    // an mbarrier or a named barrier).  Barriers that end a wait reduce the
+    // threads' results with bar.red.and, so an expired wait stops every epilogue
+    // thread at the same point.
+    const uint32_t id1 = idesc_bf16_mn(128, 128, 0, 1);   // S^T x [W; Gamma Q]^T (MN-major B)
+    const uint32_t id2a = idesc_bf16_mn(128, 64, 0, 0);   // Vt^T x A_qk^T (K-major B)
+    const uint32_t id2b = idesc_bf16_mn(128, 128, 0, 0);  // Vt^T x Kt^T (K-major B)
+    bool any_mma = false;
     bool alive = true;
     for (int j = 0; j < nch && alive; ++j) {
       const int s = j % kStages;
       uint8_t* st = sm + s * kStageBytes;
+      const uint32_t sts = sbase + s * kStageBytes;
       const float* gam_s = reinterpret_cast<const float*>(st + kUnitBytes);
       // E0: S^T row -> bf16 operand copy (MMA1 may start), then S^T *= gamma_C
-      if (j > 0 && !wait_or_abort(bar_m2, (j - 1) & 1, err, abort_flag)) { alive = false; break; }
-      if (!wait_or_abort(bar_full0 + 8 * s, (j / kStages) & 1, err, abort_flag)) { alive = false; break; }
+      bool ok = j == 0 || wait_or_abort(bar_m2, (j - 1) & 1, err, abort_flag);
+      ok = ok && wait_or_abort(bar_full0 + 8 * s, (j / kStages) & 1, err, abort_flag);
+      if (!named_sync_and(1, kEpi, ok)) { alive = false; break; }
       tc_fence_after();
+      float sv[2][32];
+      tmem_ld32(lrow + 64 * ch, sv[0]);
+      tmem_ld32(lrow + 64 * ch + 32, sv[1]);
+      tmem_wait_ld();
       {
-        float sv[2][32];
-        tmem_ld32(lrow + 64 * ch, sv[0]);
-        tmem_ld32(lrow + 64 * ch + 32, sv[1]);
-        tmem_wait_ld();
-        {
-          uint32_t pk[32];  // bf16 pairs of this thread's 64 columns of S^T
+        uint32_t pk[32];  // bf16 pairs of this thread's 64 columns of S^T
 #pragma unroll
-          for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(sv[e >> 4][2 * (e & 15)], sv[e >> 4][2 * (e & 15) + 1]);
-          tmem_st32u(lrow + kT_SB + 32 * ch, pk);
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar_s);
-        // the scaled state is ordered before MMA2 by the Vt-ready barrier below
-#pragma unroll
-        for (int qq = 0; qq < 2; ++qq) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            const float4 gm = *reinterpret_cast<const float4*>(gam_s + 64 * ch + 32 * qq + i);
-            sv[qq][i] *= gm.x; sv[qq][i + 1] *= gm.y; sv[qq][i + 2] *= gm.z; sv[qq][i + 3] *= gm.w;
-          }
-          tmem_st32(lrow + 64 * ch + 32 * qq, sv[qq]);
-        }
-        tmem_wait_st();
+        for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(sv[e >> 4][2 * (e & 15)], sv[e >> 4][2 * (e & 15) + 1]);
+        tmem_st32u(lrow + kT_SB + 32 * ch, pk);
       }
+      tmem_wait_st();
+      tc_fence_before();
+      named_sync(1, kEpi);
+      if (t == 0) {
+        tc_fence_after();
+        // D1 buffer j&1 must have been read out by the store warps (chunk j-2)
+        if (j < 2 || wait_or_abort(bar_f0 + 8 * (j & 1), ((j - 2) >> 1) & 1, err, abort_flag)) {
+          const uint32_t d1 = tmem + 128 + 128 * (j & 1);
+          // (W S)^T | (Gamma Q S)^T in one N = 128 product, A = bf16 S^T from TMEM; the
+          // descriptor of K step ks is the step-0 descriptor with its start advanced
+          const uint64_t bw = mnmajor_desc_lbo(sts + kW, kQ - kW, 1024, 0);
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks)
+            mma_bf16_ta(d1, tmem + kT_SB + 8 * ks, desc_advance(bw, ks * 2048), id1, ks > 0);
+          mma_commit(bar_m1);
+          any_mma = true;
+        }
+      }
+      // the scaled state is ordered before MMA2 by the barrier after E1
+#pragma unroll
+      for (int qq = 0; qq < 2; ++qq) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          const float4 gm = *reinterpret_cast<const float4*>(gam_s + 64 * ch + 32 * qq + i);
+          sv[qq][i] *= gm.x; sv[qq][i + 1] *= gm.y; sv[qq][i + 2] *= gm.z; sv[qq][i + 3] *= gm.w;
+        }
+        tmem_st32(lrow + 64 * ch + 32 * qq, sv[qq]);
+      }
+      tmem_wait_st();
       // E1: Vt^T = U^T - (W S)^T on this thread's 32 tokens
-      if (!wait_or_abort(bar_m1, j & 1, err, abort_flag)) { alive = false; break; }
-      tc_fence_after();
-      {
+      ok = wait_or_abort(bar_m1, j & 1, err, abort_flag);
+      if (ok) {
+        tc_fence_after();
         float wsv[32];
         tmem_ld32(lrow + 128 + 128 * (j & 1) + 32 * ch, wsv);
         tmem_wait_ld();
@@ -847,7 +828,27 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         tmem_wait_st();
       }
       tc_fence_before();
-      mbar_arrive(bar_vt);
+      if (!named_sync_and(1, kEpi, ok)) { alive = false; break; }
+      if (t == 0) {
+        tc_fence_after();
+        // S^T += Vt^T Kt, then O^T += Vt^T A_qk^T onto (Gamma Q S)^T
+        const uint32_t vt = tmem + kT_VT + 32 * (j & 1);
+        const uint64_t bk = kmajor_desc(sts + kKT, 128, 0), ba = kmajor_desc(sts + kAQ, 64, 0);
+#pragma unroll
+        for (int ks = 0; ks < C / 16; ++ks)
+          mma_bf16_ta(tmem + 0, vt + 8 * ks, desc_advance(bk, ks * 32), id2b, 1u);
+        mma_commit(bar_m2);
+        const uint32_t d1 = tmem + 128 + 128 * (j & 1);
+#pragma unroll
+        for (int ks = 0; ks < C / 16; ++ks)
+          mma_bf16_ta(d1 + 64, vt + 8 * ks, desc_advance(ba, ks * 32), id2a, 1u);
+        mma_commit(bar_o0 + 8 * (j & 1));  // o of chunk j final
+        mma_commit(bar_empty0 + 8 * s);    // every MMA of chunk j done: stage s may refill
+      }
+    }
+    if (t == 0 && *abort_flag && any_mma) {  // drain: MMAs in flight land before exit
+      mma_commit(bar_dr);
+      mbar_wait(bar_dr, 0, nullptr);
     }
     if (alive && nch > 0 && wait_or_abort(bar_m2, (nch - 1) & 1, err, abort_flag))
       tc_fence_after();

@@ -130,6 +130,11 @@ __device__ __forceinline__ void bulk_wait_all() {
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+// Arrives at barrier `id` (over `nthreads` threads) without waiting: the producer
+// half of a producer/consumer hand-off whose consumers call named_sync.
+__device__ __forceinline__ void named_arrive(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 // Barrier `id` over `nthreads` threads that also ANDs `p` across them.
 __device__ __forceinline__ bool named_sync_and(uint32_t id, uint32_t nthreads, bool p) {
   uint32_t r;
@@ -351,6 +356,11 @@ __device__ __forceinline__ uint64_t make_desc(uint32_t saddr, uint32_t lbo, uint
 __device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int rows, int s) {
   return make_desc(base + (uint32_t)(s >> 2) * (uint32_t)rows * 128u + (uint32_t)(s & 3) * 32u, 16u,
                    1024u);
+}
+// The descriptor `d` with its start address advanced by `bytes` (a multiple of 16
+// that keeps the address inside shared memory, so the 14-bit field cannot carry).
+__device__ __forceinline__ uint64_t desc_advance(uint64_t d, uint32_t bytes) {
+  return d + (uint64_t)(bytes >> 4);
 }
 // Descriptor of K step s of an MN-major tile with SBO `sbo`, starting at `base`.
 __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, uint32_t sbo, int s) {
