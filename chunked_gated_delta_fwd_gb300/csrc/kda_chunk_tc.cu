@@ -118,55 +118,6 @@ __device__ __forceinline__ UnitInfo unit_info(const Plan& plan, int H, int64_t u
   return ui;
 }
 
-// One block stage of T = (I + L)^{-1}: for every block (a + d, a),
-//   P = sum_{b=a}^{a+d-1} L_{a+d, b} T_{b, a},   T_{a+d, a} = -T_{a+d, a+d} P.
-// 128 threads per block, each owning one row m and two columns (even and odd
-// k summed separately to halve the dependent chains).
-template <int d>
-__device__ __forceinline__ void inverse_stage(int t, const float* Lb, float* Tb, float* Ps) {
-  const bool act = t < (4 - d) * 128;
-  const int a = t >> 7, tt = t & 127, m = tt >> 3, nq = tt & 7;
-  const int R = a + d;
-  if (act) {
-    float2 e = make_float2(0.f, 0.f), o = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int bb = 0; bb < d; ++bb) {
-      const int b = a + bb;
-#pragma unroll
-      for (int k = 0; k < 16; k += 2) {
-        const float l0 = Lb[(16 * R + m) * kLdL + 16 * b + k];
-        const float l1 = Lb[(16 * R + m) * kLdL + 16 * b + k + 1];
-        const float2 t0 = *reinterpret_cast<const float2*>(Tb + (16 * b + k) * kLdT + 16 * a + 2 * nq);
-        const float2 t1 =
-            *reinterpret_cast<const float2*>(Tb + (16 * b + k + 1) * kLdT + 16 * a + 2 * nq);
-        e.x = fmaf(l0, t0.x, e.x);
-        e.y = fmaf(l0, t0.y, e.y);
-        o.x = fmaf(l1, t1.x, o.x);
-        o.y = fmaf(l1, t1.y, o.y);
-      }
-    }
-    *reinterpret_cast<float2*>(Ps + a * 256 + m * 16 + 2 * nq) = make_float2(e.x + o.x, e.y + o.y);
-  }
-  named_sync(1, kPrepCompute);
-  if (act) {
-    float2 e = make_float2(0.f, 0.f), o = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int kk = 0; kk < 16; kk += 2) {  // T_RR is unit lower triangular with stored zeros
-      const float w0 = Tb[(16 * R + m) * kLdT + 16 * R + kk];
-      const float w1 = Tb[(16 * R + m) * kLdT + 16 * R + kk + 1];
-      const float2 p0 = *reinterpret_cast<const float2*>(Ps + a * 256 + kk * 16 + 2 * nq);
-      const float2 p1 = *reinterpret_cast<const float2*>(Ps + a * 256 + (kk + 1) * 16 + 2 * nq);
-      e.x = fmaf(w0, p0.x, e.x);
-      e.y = fmaf(w0, p0.y, e.y);
-      o.x = fmaf(w1, p1.x, o.x);
-      o.y = fmaf(w1, p1.y, o.y);
-    }
-    *reinterpret_cast<float2*>(Tb + (16 * R + m) * kLdT + 16 * a + 2 * nq) =
-        make_float2(-(e.x + o.x), -(e.y + o.y));
-  }
-  named_sync(1, kPrepCompute);
-}
-
 // kZ: tm_g maps z (bf16) instead of g, and g = g_min * Sigmoid(exp(A_h) z) is formed
 // while the decays are summed ("Kimi K3 technical report review", section 3.2).
 template <bool kZ>
@@ -390,7 +341,6 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
           Gl[1][e] = tmp;
         }
       }
-#pragma unroll
       float gam_c[2];  // gamma_C of this thread's two channels
 #pragma unroll
       for (int o2 = 0; o2 < 2; ++o2) {
@@ -549,9 +499,102 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         Tb[(o + 8 + i) * kLdT + o + j] = -acc;
       }
       named_sync(1, kPrepCompute);
-      inverse_stage<1>(t, Lb, Tb, Ps);
-      inverse_stage<2>(t, Lb, Tb, Ps);
-      inverse_stage<3>(t, Lb, Tb, Ps);
+      // Blocks below the diagonal by doubling: first the 16x16 blocks (1,0), (3,2)
+      // of the two 32x32 diagonal blocks, then their 32x32 lower-left block,
+      //   [A 0; C B]^{-1} lower-left = -B^{-1} (C A^{-1})   (at both levels).
+      // Register-blocked: a thread computes 2 rows x 4 columns, so each shared-memory
+      // load feeds four (L) or two (T) FMAs.
+      if (t < 64) {  // level 1: P = L_{a+1,a} D_a (a = 0, 2)
+        const int blk = t >> 5, a = 2 * blk, R = a + 1, rp = (t >> 2) & 7, cq = t & 3;
+        float acc[2][4] = {};
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {  // D_a has stored zeros above its diagonal
+          const float4 tv = *reinterpret_cast<const float4*>(Tb + (16 * a + k) * kLdT + 16 * a + 4 * cq);
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const float l = Lb[(16 * R + 2 * rp + r) * kLdL + 16 * a + k];
+            acc[r][0] = fmaf(l, tv.x, acc[r][0]);
+            acc[r][1] = fmaf(l, tv.y, acc[r][1]);
+            acc[r][2] = fmaf(l, tv.z, acc[r][2]);
+            acc[r][3] = fmaf(l, tv.w, acc[r][3]);
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+          *reinterpret_cast<float4*>(Ps + blk * 256 + (2 * rp + r) * 16 + 4 * cq) =
+              make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+      }
+      named_sync(1, kPrepCompute);
+      if (t < 64) {  // level 1: T_{a+1,a} = -D_{a+1} P
+        const int blk = t >> 5, a = 2 * blk, R = a + 1, rp = (t >> 2) & 7, cq = t & 3;
+        float acc[2][4] = {};
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {  // D_{a+1} has stored zeros above its diagonal
+          const float4 pv = *reinterpret_cast<const float4*>(Ps + blk * 256 + k * 16 + 4 * cq);
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const float w = Tb[(16 * R + 2 * rp + r) * kLdT + 16 * R + k];
+            acc[r][0] = fmaf(w, pv.x, acc[r][0]);
+            acc[r][1] = fmaf(w, pv.y, acc[r][1]);
+            acc[r][2] = fmaf(w, pv.z, acc[r][2]);
+            acc[r][3] = fmaf(w, pv.w, acc[r][3]);
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+          *reinterpret_cast<float4*>(Tb + (16 * R + 2 * rp + r) * kLdT + 16 * a + 4 * cq) =
+              make_float4(-acc[r][0], -acc[r][1], -acc[r][2], -acc[r][3]);
+      }
+      named_sync(1, kPrepCompute);
+      // level 2: M = L[32:64, 0:32] T[0:32, 0:32] into the unused upper-right block of Tb
+      // (rows 0..31, columns 32..63); T[0:16, 16:32] is not stored (zero).
+      float* Mb = Tb + 32;
+      if (t < 128) {
+        const int rp = t >> 3, cq = t & 7, k0 = cq >= 4 ? 16 : 0;
+        float acc[2][4] = {};
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          if (k >= k0) {
+            const float4 tv = *reinterpret_cast<const float4*>(Tb + k * kLdT + 4 * cq);
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const float l = Lb[(32 + 2 * rp + r) * kLdL + k];
+              acc[r][0] = fmaf(l, tv.x, acc[r][0]);
+              acc[r][1] = fmaf(l, tv.y, acc[r][1]);
+              acc[r][2] = fmaf(l, tv.z, acc[r][2]);
+              acc[r][3] = fmaf(l, tv.w, acc[r][3]);
+            }
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+          *reinterpret_cast<float4*>(Mb + (2 * rp + r) * kLdT + 4 * cq) =
+              make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+      }
+      named_sync(1, kPrepCompute);
+      if (t < 128) {  // level 2: T[32:64, 0:32] = -T[32:64, 32:64] M; T[32:48, 48:64] is zero
+        const int rp = t >> 3, cq = t & 7, kn = rp < 8 ? 16 : 32;
+        float acc[2][4] = {};
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          if (k < kn) {
+            const float4 mv = *reinterpret_cast<const float4*>(Mb + k * kLdT + 4 * cq);
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const float w = Tb[(32 + 2 * rp + r) * kLdT + 32 + k];
+              acc[r][0] = fmaf(w, mv.x, acc[r][0]);
+              acc[r][1] = fmaf(w, mv.y, acc[r][1]);
+              acc[r][2] = fmaf(w, mv.z, acc[r][2]);
+              acc[r][3] = fmaf(w, mv.w, acc[r][3]);
+            }
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+          *reinterpret_cast<float4*>(Tb + (32 + 2 * rp + r) * kLdT + 4 * cq) =
+              make_float4(-acc[r][0], -acc[r][1], -acc[r][2], -acc[r][3]);
+      }
+      named_sync(1, kPrepCompute);
       {  // T -> bf16 B operand (MN-major, X = row r, K = column j); zero above the diagonal
         const int j = t >> 3, o8 = t & 7;
         float x[8];
