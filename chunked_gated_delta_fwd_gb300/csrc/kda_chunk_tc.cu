@@ -671,7 +671,7 @@ constexpr uint32_t kC_bars = kStages * kStageBytes;
 // operands of MMA1 (S^T, packed pairs, [384,448)) and MMA2 (Vt^T, two buffers of 32
 // columns at [448,512)).
 constexpr uint32_t kT_SB = 384, kT_VT = 448;
-constexpr uint32_t kC_Smem = kC_bars + 128 + 1024;
+constexpr uint32_t kC_Smem = kC_bars + 256 + 1024;
 constexpr int kEpi = 256;    // epilogue warps 0-7: (TMEM lane, column half)
 constexpr int kStore = 128;  // store warps 8-11: TMEM lane = value row, all 64 tokens
 constexpr int kCopyWarp = (kEpi + kStore) / 32;  // warp 12: tile copies
@@ -704,20 +704,21 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kC_bars);
   // bars: 0..2 = full[stage], 3..5 = empty[stage] (every MMA of its chunk done),
   //       6 = MMA1 done, 7 = S update done, 8,9 = O of D1 buffer b final,
-  //       10,11 = D1 buffer b read out, 12 = drain (abort path)
+  //       10,11 = D1 buffer b read out, 12..14 = drain of MMA-issuing thread i (abort path),
+  //       15 = the (Gamma Q S)^T half of MMA1 done (it reads the bf16 S^T copy)
   const uint32_t bar_full0 = smem_addr(&bars[0]), bar_empty0 = smem_addr(&bars[3]);
   const uint32_t bar_m1 = smem_addr(&bars[6]), bar_m2 = smem_addr(&bars[7]);
   const uint32_t bar_o0 = smem_addr(&bars[8]), bar_f0 = smem_addr(&bars[10]);
-  const uint32_t bar_dr = smem_addr(&bars[12]);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kC_bars + 112);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kC_bars + 120);
+  const uint32_t bar_dr = smem_addr(&bars[12]), bar_q = smem_addr(&bars[15]);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kC_bars + 192);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kC_bars + 200);
   const int t = threadIdx.x, warp = t >> 5;
   const int n = blockIdx.x, h = blockIdx.y;
 
   if (t == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar_full0 + 8 * s, 1);
-      mbar_init(bar_empty0 + 8 * s, 1);
+      mbar_init(bar_empty0 + 8 * s, 3);  // one commit from each MMA-issuing thread
     }
     mbar_init(bar_m1, 1);
     mbar_init(bar_m2, 1);
@@ -725,7 +726,8 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       mbar_init(bar_o0 + 8 * b, 1);
       mbar_init(bar_f0 + 8 * b, kStore);
     }
-    mbar_init(bar_dr, 1);
+    for (int i = 0; i < 3; ++i) mbar_init(bar_dr + 8 * i, 1);
+    mbar_init(bar_q, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -796,7 +798,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     // an mbarrier or a named barrier).  Barriers that end a wait reduce the
     // threads' results with bar.red.and, so an expired wait stops every epilogue
     // thread at the same point.
-    const uint32_t id1 = idesc_bf16_mn(128, 128, 0, 1);   // S^T x [W; Gamma Q]^T (MN-major B)
+    const uint32_t id1 = idesc_bf16_mn(128, 64, 0, 1);    // S^T x W^T or S^T x (Gamma Q)^T
     const uint32_t id2a = idesc_bf16_mn(128, 64, 0, 0);   // Vt^T x A_qk^T (K-major B)
     const uint32_t id2b = idesc_bf16_mn(128, 128, 0, 0);  // Vt^T x Kt^T (K-major B)
     bool any_mma = false;
@@ -807,7 +809,9 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       const uint32_t sts = sbase + s * kStageBytes;
       const float* gam_s = reinterpret_cast<const float*>(st + kUnitBytes);
       // E0: S^T row -> bf16 operand copy (MMA1 may start), then S^T *= gamma_C
-      bool ok = j == 0 || wait_or_abort(bar_m2, (j - 1) & 1, err, abort_flag);
+      // S^T updated, and the bf16 copy of the previous chunk read by both MMA1 halves
+      bool ok = j == 0 || (wait_or_abort(bar_m2, (j - 1) & 1, err, abort_flag) &&
+                           wait_or_abort(bar_q, (j - 1) & 1, err, abort_flag));
       ok = ok && wait_or_abort(bar_full0 + 8 * s, (j / kStages) & 1, err, abort_flag);
       if (!named_sync_and(1, kEpi, ok)) { alive = false; break; }
       tc_fence_after();
@@ -824,18 +828,30 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       named_sync(1, kEpi);
+      // MMA1 in two N = 64 halves issued by two threads (an issuing thread stalls
+      // while the tensor pipe drains, so no single warp carries all of it): thread 0
+      // the (W S)^T half that the Vt pass waits for, thread 32 the (Gamma Q S)^T
+      // half, which only the output needs.  A = bf16 S^T from TMEM; the descriptor
+      // of K step ks is the step-0 descriptor with its start advanced.
+      const uint32_t d1 = tmem + 128 + 128 * (j & 1);
       if (t == 0) {
         tc_fence_after();
-        // D1 buffer j&1 must have been read out by the store warps (chunk j-2)
+        const uint64_t bw = mnmajor_desc(sts + kW, 1024, 0);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_bf16_ta(d1, tmem + kT_SB + 8 * ks, desc_advance(bw, ks * 2048), id1, ks > 0);
+        mma_commit(bar_m1);
+        mma_commit(bar_empty0 + 8 * s);
+        any_mma = true;
+      } else if (t == 32) {
+        tc_fence_after();
+        // the output half of D1 buffer j&1 must have been read out (chunk j-2)
         if (j < 2 || wait_or_abort(bar_f0 + 8 * (j & 1), ((j - 2) >> 1) & 1, err, abort_flag)) {
-          const uint32_t d1 = tmem + 128 + 128 * (j & 1);
-          // (W S)^T | (Gamma Q S)^T in one N = 128 product, A = bf16 S^T from TMEM; the
-          // descriptor of K step ks is the step-0 descriptor with its start advanced
-          const uint64_t bw = mnmajor_desc_lbo(sts + kW, kQ - kW, 1024, 0);
+          const uint64_t bq = mnmajor_desc(sts + kQ, 1024, 0);
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks)
-            mma_bf16_ta(d1, tmem + kT_SB + 8 * ks, desc_advance(bw, ks * 2048), id1, ks > 0);
-          mma_commit(bar_m1);
+            mma_bf16_ta(d1 + 64, tmem + kT_SB + 8 * ks, desc_advance(bq, ks * 2048), id1, ks > 0);
+          mma_commit(bar_q);
           any_mma = true;
         }
       }
@@ -872,26 +888,29 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       }
       tc_fence_before();
       if (!named_sync_and(1, kEpi, ok)) { alive = false; break; }
-      if (t == 0) {
+      const uint32_t vt = tmem + kT_VT + 32 * (j & 1);
+      if (t == 64) {  // S^T += Vt^T Kt
         tc_fence_after();
-        // S^T += Vt^T Kt, then O^T += Vt^T A_qk^T onto (Gamma Q S)^T
-        const uint32_t vt = tmem + kT_VT + 32 * (j & 1);
-        const uint64_t bk = kmajor_desc(sts + kKT, 128, 0), ba = kmajor_desc(sts + kAQ, 64, 0);
+        const uint64_t bk = kmajor_desc(sts + kKT, 128, 0);
 #pragma unroll
         for (int ks = 0; ks < C / 16; ++ks)
           mma_bf16_ta(tmem + 0, vt + 8 * ks, desc_advance(bk, ks * 32), id2b, 1u);
         mma_commit(bar_m2);
-        const uint32_t d1 = tmem + 128 + 128 * (j & 1);
+        mma_commit(bar_empty0 + 8 * s);
+        any_mma = true;
+      } else if (t == 32) {  // O^T += Vt^T A_qk^T onto (Gamma Q S)^T, after this thread's half
+        tc_fence_after();
+        const uint64_t ba = kmajor_desc(sts + kAQ, 64, 0);
 #pragma unroll
         for (int ks = 0; ks < C / 16; ++ks)
           mma_bf16_ta(d1 + 64, vt + 8 * ks, desc_advance(ba, ks * 32), id2a, 1u);
         mma_commit(bar_o0 + 8 * (j & 1));  // o of chunk j final
-        mma_commit(bar_empty0 + 8 * s);    // every MMA of chunk j done: stage s may refill
+        mma_commit(bar_empty0 + 8 * s);
       }
     }
-    if (t == 0 && *abort_flag && any_mma) {  // drain: MMAs in flight land before exit
-      mma_commit(bar_dr);
-      mbar_wait(bar_dr, 0, nullptr);
+    if ((t == 0 || t == 32 || t == 64) && *abort_flag && any_mma) {  // drain MMAs in flight
+      mma_commit(bar_dr + 8 * (t >> 5));
+      mbar_wait(bar_dr + 8 * (t >> 5), 0, nullptr);
     }
     if (alive && nch > 0 && wait_or_abort(bar_m2, (nch - 1) & 1, err, abort_flag))
       tc_fence_after();
