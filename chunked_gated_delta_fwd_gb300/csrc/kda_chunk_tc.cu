@@ -19,21 +19,26 @@
 // is k_r * exp(G_r - R_a) <= 1 (resp. q_r * exp(G_r - R_a)); their product over
 // the channels is sum_c k_rc k_ic exp(G_rc - G_ic).
 //
-// Kernel 1, tc_prep: one persistent CTA per SM walks (chunk, head) units.  A copy
-// warp prefetches the next unit's k, q, v, g rows into shared memory with 1-D
-// bulk copies while eight compute warps (thread = channel x row half) build the
-// operands, run the MMAs, invert I + A_kk blockwise in fp32 and write, per unit,
-// MMA-ready bf16 tiles to the workspace:
-//   WQ: MN-major, 128 token rows x 128 channels (W rows 0..63, Gamma*Q rows 64..127)
+// Kernel 1, tc_prep: one persistent 512-thread CTA per SM walks (chunk, head)
+// units.  A unit's k, q, v and g (or z, with the gate formed in-kernel) arrive
+// through 3-D tensor TMA copies issued as soon as the previous unit's rows are in
+// registers; every thread builds the operands of 8 tokens x 2 channels, one
+// thread issues the MMAs (the four tile products in one N=192 chain, then W^T and
+// U^T), the (I + A_kk)^{-1} inverse runs in fp32 on the CUDA cores, and the unit
+// leaves as MMA-ready bf16 tiles written with whole-tile bulk copies:
+//   W, Gamma*Q: MN-major, 64 token columns x 128 channels each (one operand with
+//               a 16 KB atom stride)
 //   UT: K-major, U^T (128 value rows x 64 tokens)
-//   AQ: MN-major, A_qk (64 x 64);  KT: K-major, Kt^T (128 channel rows x 64 tokens)
+//   AQ: K-major, A_qk (64 x 64);  KT: K-major, Kt^T (128 channel rows x 64 tokens)
 // plus gamma_C (fp32 [128]).
 // Kernel 2, tc_chain: one CTA per (sequence, head) walks its chunks in order.
-// TMEM holds S^T (lanes = dv, columns = dk) and two D1 buffers:
-//   MMA1: D1 = S^T [W; Gamma*Q]^T        -> (W S)^T | (Gamma*Q S)^T
-//   MMA2: D1[:,64:] += Vt^T A_qk^T ;  S^T += Vt^T Kt  (after S^T *= gamma_C)
-// where Vt^T = U^T - (W S)^T is formed by eight epilogue warps.  Tiles stream
-// in with bulk async copies through a two-stage ring.
+// TMEM holds S^T (lanes = dv, columns = dk, fp32 for the whole sequence), its bf16
+// copy (the A operand of MMA1), two D1 buffers and two Vt^T buffers:
+//   MMA1: D1 = S^T [W; Gamma*Q]^T      -> (W S)^T | (Gamma*Q S)^T
+//   MMA2: S^T += Vt^T Kt (after S^T *= gamma_C);  D1[:, 64:] += Vt^T A_qk^T
+// where Vt^T = U^T - (W S)^T is formed by eight epilogue warps, three of whose
+// threads issue the MMAs after named barriers; four store warps write o, and a
+// copy warp streams the tiles through a three-stage ring of bulk copies.
 #include "kda_internal.cuh"
 #include "kda_sm100.cuh"
 
