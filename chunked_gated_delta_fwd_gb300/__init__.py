@@ -26,11 +26,13 @@ import torch
 from . import _build
 
 __all__ = ["KdaError", "gate", "chunk_fwd", "chunk_fwd_gated", "chunk_fwd_workspace_size", "recurrent_step",
-           "library_path", "lib", "get_device_error", "profile_enable", "profile_collect", "G_MIN", "F32", "BF16", "FP32_CORES"]
+           "library_path", "lib", "get_device_error", "profile_enable", "profile_collect", "G_MIN", "F32", "BF16", "FP32_CORES", "SEQUENTIAL",
+           "segment_chunks"]
 
 G_MIN = -5.0
 F32, BF16 = 0, 1
 FP32_CORES = 1  # flag of chunk_fwd: evaluate bf16 inputs on fp32 CUDA cores
+SEQUENTIAL = 2  # flag of chunk_fwd: never split a sequence's chain into segments
 
 _STATUS = {
     0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED_SHAPE",
@@ -60,6 +62,8 @@ def _load() -> ctypes.CDLL:
     L.kda_gate.argtypes = [vp, i32, vp, f32, vp, i64, i32, i32, vp, vp, i32, vp]
     L.kda_chunk_fwd_workspace_size.argtypes = [i64, i32, i32, i32]
     L.kda_chunk_fwd_workspace_size.restype = sz
+    L.kda_chunk_fwd_workspace_size_ex.argtypes = [i64, i32, i32, i32, u32]
+    L.kda_chunk_fwd_workspace_size_ex.restype = sz
     L.kda_chunk_fwd.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i64, i32, i32, i32, vp,
                                 vp, vp, sz, vp]
     L.kda_chunk_fwd_ex.argtypes = L.kda_chunk_fwd.argtypes + [u32]
@@ -140,8 +144,14 @@ def gate(z: torch.Tensor, A: torch.Tensor, g_min: float = G_MIN, *, out=None,
 
 def chunk_fwd_workspace_size(n_tokens: int, n_seqs: int, H: int, dtype=torch.bfloat16,
                              flags: int = 0) -> int:
-    code = F32 if (flags & FP32_CORES) else (BF16 if dtype == torch.bfloat16 else F32)
-    return int(lib.kda_chunk_fwd_workspace_size(int(n_tokens), int(n_seqs), int(H), code))
+    code = BF16 if dtype == torch.bfloat16 else F32
+    return int(lib.kda_chunk_fwd_workspace_size_ex(int(n_tokens), int(n_seqs), int(H), code,
+                                                   int(flags)))
+
+
+def segment_chunks(n: int) -> int:
+    """Flag bits forcing chain segments of n chunks (KDA_CHUNK_SEGMENT_CHUNKS)."""
+    return (int(n) & 0xFFFF) << 16
 
 
 def chunk_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, *, output_final_state=True,

@@ -340,13 +340,21 @@ kda_status_t kda_gate(const void* z, int z_dtype, const float* A, float g_min, f
   return KDA_OK;
 }
 
-size_t kda_chunk_fwd_workspace_size(int64_t n_tokens, int n_seqs, int H, int dtype) {
+size_t kda_chunk_fwd_workspace_size_ex(int64_t n_tokens, int n_seqs, int H, int dtype,
+                                       unsigned flags) {
   if (n_tokens < 0 || n_seqs < 1 || H < 1) return 0;
-  if (dtype == KDA_BF16)
-    return kda::plan_bytes(n_tokens, n_seqs) + kda::tc_workspace_bytes(n_tokens, n_seqs, H);
-  if (dtype == KDA_F32)
+  if (dtype == KDA_BF16 && !(flags & KDA_CHUNK_FP32_CORES)) {
+    const int segc = kda::chain_segment_chunks(n_tokens, n_seqs, H, (int)(flags >> 16),
+                                               (flags & KDA_CHUNK_SEQUENTIAL) != 0);
+    return kda::plan_bytes(n_tokens, n_seqs) + kda::tc_workspace_bytes(n_tokens, n_seqs, H, segc);
+  }
+  if (dtype == KDA_F32 || dtype == KDA_BF16)
     return kda::plan_bytes(n_tokens, n_seqs) + kda::simt_workspace_bytes(n_tokens, n_seqs, H);
   return 0;
+}
+
+size_t kda_chunk_fwd_workspace_size(int64_t n_tokens, int n_seqs, int H, int dtype) {
+  return kda_chunk_fwd_workspace_size_ex(n_tokens, n_seqs, H, dtype, 0u);
 }
 
 }  // extern "C"
@@ -389,12 +397,11 @@ kda_status_t chunk_fwd_impl(const char* fn, const void* q, const void* k, const 
       return fail(KDA_ERR_MISALIGNED, "%s: pointers must be 16-byte aligned", fn);
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return fail(KDA_ERR_MISALIGNED, "%s: workspace must be 256-byte aligned", fn);
-  const size_t need = kda_chunk_fwd_workspace_size(
-      NT, N, H, (flags & KDA_CHUNK_FP32_CORES) ? (int)KDA_F32 : dtype);
+  const size_t need = kda_chunk_fwd_workspace_size_ex(NT, N, H, dtype, flags);
   if (ws_bytes < need)
     return fail(KDA_ERR_WORKSPACE_TOO_SMALL, "%s: workspace %zu < %zu bytes", fn,
                 ws_bytes, need);
-  if (flags & ~(unsigned)KDA_CHUNK_FP32_CORES)
+  if (flags & ~(unsigned)(KDA_CHUNK_FP32_CORES | KDA_CHUNK_SEQUENTIAL | 0xffff0000u))
     return fail(KDA_ERR_INVALID_ARG, "%s: unknown flags 0x%x", fn, flags);
   kda_status_t st = check_device();
   if (st != KDA_OK) return st;
@@ -403,8 +410,10 @@ kda_status_t chunk_fwd_impl(const char* fn, const void* q, const void* k, const 
   cudaError_t e = kda::launch_plan(cu_seqlens, N, T_per_seq, NT, workspace, err, s);
   if (e != cudaSuccess) return cuda_fail(e, "chunk plan launch");
   if (dtype == KDA_BF16 && !(flags & KDA_CHUNK_FP32_CORES))
-    e = kda::launch_chunk_tc(q, k, v, g, z, A, g_min, beta, h0, o, hT, NT, N, H, workspace, err,
-                             s);
+    e = kda::launch_chunk_tc(q, k, v, g, z, A, g_min, beta, h0, o, hT, NT, N, H,
+                             kda::chain_segment_chunks(NT, N, H, (int)(flags >> 16),
+                                                       (flags & KDA_CHUNK_SEQUENTIAL) != 0),
+                             workspace, err, s);
   else
     e = kda::launch_chunk_simt(q, k, v, dtype == KDA_BF16, g, beta, h0, o, hT, NT, N, H,
                                workspace, s);

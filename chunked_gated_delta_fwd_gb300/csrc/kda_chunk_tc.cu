@@ -699,10 +699,72 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int
   }
 }
 
+// Sequence-segment parallel chain (the KCP algebra applied inside one GPU: "Kimi
+// K3 technical report review", section 8.1 Eq. 17).  A long sequence is cut into P
+// segments; with A_c = Diag(gamma_C) - Kt^T W the linear part of one chunk step,
+// a segment maps its incoming state to S_end = S~ + M S_in, where S~ is the
+// segment run from a zero state and M the product of its A_c.
+//   mode 1 (grid z = 0): segment 0 runs from h0 with outputs (its end state is
+//          exact); segments k >= 1 run from zero without outputs (S~);
+//   mode 1 (grid z = 1): segments 1 .. P-2 run from the identity with U = 0 (M^T);
+//   scan:  S_in(1) = S_end(0), S_in(k+1) = S~(k) + M(k) S_in(k)  (seg_scan_kernel);
+//   mode 2: segments k >= 1 run from S_in(k) with outputs; the last writes hT.
+// mode 0 is the plain chain, one CTA per (sequence, head).  States are S^T.
+struct SegArgs {
+  int mode;
+  const int4* tab;  // per segment: (sequence, first chunk, chunks, k | P << 16); x < 0: unused
+  float* s_end;     // [segments][H][128][128]
+  float* m_t;
+  float* s_in;
+};
+
 __global__ void __launch_bounds__(kChainThreads, 1)
     tc_chain(const uint8_t* __restrict__ tiles, const float* __restrict__ gam,
              const float* __restrict__ h0, Plan plan, int H, __nv_bfloat16* __restrict__ o,
-             float* __restrict__ hT, int* err) {
+             float* __restrict__ hT, SegArgs sg, int* err) {
+  // ---- this CTA's job: chunk range, initial and final state, outputs or not
+  const int h = blockIdx.y;
+  int n, c0, nch;
+  int64_t tstart;
+  const float* init = nullptr;  // initial S^T (null: zero, unless `ident`)
+  bool ident = false, use_u = true, write_o = true;
+  float* fin = nullptr;         // final S^T goes here (null: nowhere)
+  if (sg.mode == 0) {
+    n = blockIdx.x;
+    c0 = __ldg(plan.chunk_off + n);
+    nch = __ldg(plan.chunk_off + n + 1) - c0;
+    tstart = __ldg(plan.cu + n);
+    const int64_t sn = ((int64_t)n * H + h) * D * D;
+    init = h0 ? h0 + sn : nullptr;
+    fin = hT ? hT + sn : nullptr;
+  } else {
+    const int4 e = sg.tab[blockIdx.x];
+    if (e.x < 0) return;  // beyond the last segment (uniform over the CTA)
+    n = e.x;
+    c0 = e.y;
+    nch = e.z;
+    const int k = e.w & 0xffff, P = e.w >> 16;
+    tstart = nch > 0 ? (int64_t)__ldg(plan.tab + c0).x : (int64_t)__ldg(plan.cu + n);
+    const int64_t sn = ((int64_t)n * H + h) * D * D;
+    const int64_t ss = ((int64_t)blockIdx.x * H + h) * D * D;
+    if (sg.mode == 1 && blockIdx.z == 0) {
+      init = (k == 0 && h0) ? h0 + sn : nullptr;
+      write_o = k == 0;
+      fin = P == 1 ? (hT ? hT + sn : nullptr) : sg.s_end + ss;
+    } else if (sg.mode == 1) {
+      if (k == 0 || k == P - 1) return;
+      ident = true;
+      use_u = false;
+      write_o = false;
+      fin = sg.m_t + ss;
+    } else {
+      if (k == 0) return;
+      init = sg.s_in + ss;
+      fin = (k == P - 1 && hT) ? hT + sn : nullptr;
+    }
+  }
+  const int64_t tend = max(tstart, (int64_t)__ldg(plan.cu + n + 1));
+
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_addr(sm);
@@ -718,7 +780,6 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kC_bars + 192);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kC_bars + 200);
   const int t = threadIdx.x, warp = t >> 5;
-  const int n = blockIdx.x, h = blockIdx.y;
 
   if (t == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -741,11 +802,6 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int c0 = __ldg(plan.chunk_off + n), c1 = __ldg(plan.chunk_off + n + 1);
-  const int nch = c1 - c0;
-  const int64_t tstart = __ldg(plan.cu + n);
-  const int64_t tend = max(tstart, (int64_t)__ldg(plan.cu + n + 1));
-  const int64_t state = ((int64_t)n * H + h) * D * D;
 
   if (warp == kCopyWarp) {
     // ------------------------------------------------------ tile copies (one thread)
@@ -784,15 +840,15 @@ __global__ void __launch_bounds__(kChainThreads, 1)
 #pragma unroll
       for (int qq = 0; qq < 2; ++qq) {
         const int col = 64 * ch + 32 * qq;
-        if (h0) {
+        if (init) {
 #pragma unroll
           for (int i = 0; i < 32; i += 4) {
-            const float4 x = *reinterpret_cast<const float4*>(h0 + state + (int64_t)lane * D + col + i);
+            const float4 x = *reinterpret_cast<const float4*>(init + (int64_t)lane * D + col + i);
             sv[i] = x.x; sv[i + 1] = x.y; sv[i + 2] = x.z; sv[i + 3] = x.w;
           }
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) sv[i] = 0.f;
+          for (int i = 0; i < 32; ++i) sv[i] = (ident && lane == col + i) ? 1.f : 0.f;
         }
         tmem_st32(lrow + col, sv);
       }
@@ -881,7 +937,8 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         uint32_t pk[16];  // bf16 pairs of this thread's 32 tokens of Vt^T
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const uint4 uu = *reinterpret_cast<const uint4*>(st + kUT + sw128_chunk(128, lane, 4 * ch + e));
+          const uint4 uu = use_u ? *reinterpret_cast<const uint4*>(st + kUT + sw128_chunk(128, lane, 4 * ch + e))
+                                 : make_uint4(0, 0, 0, 0);
           const uint32_t uw[4] = {uu.x, uu.y, uu.z, uu.w};
 #pragma unroll
           for (int p = 0; p < 4; ++p)
@@ -919,7 +976,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     }
     if (alive && nch > 0 && wait_or_abort(bar_m2, (nch - 1) & 1, err, abort_flag))
       tc_fence_after();
-    if (hT && !*abort_flag) {
+    if (fin && !*abort_flag) {
       tc_fence_after();
 #pragma unroll
       for (int qq = 0; qq < 2; ++qq) {
@@ -929,7 +986,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 32; i += 4)
-          *reinterpret_cast<float4*>(hT + state + (int64_t)lane * D + col + i) =
+          *reinterpret_cast<float4*>(fin + (int64_t)lane * D + col + i) =
               make_float4(sv[i], sv[i + 1], sv[i + 2], sv[i + 3]);
       }
     }
@@ -955,7 +1012,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       __nv_bfloat16* orow = o + (tc * H + h) * D + dv;
 #pragma unroll
       for (int r = 0; r < C; ++r)
-        if (tc + r < tend) orow[(int64_t)r * H * D] = __float2bfloat16_rn(ov[r >> 5][r & 31]);
+        if (write_o && tc + r < tend) orow[(int64_t)r * H * D] = __float2bfloat16_rn(ov[r >> 5][r & 31]);
     }
   }
   tc_fence_before();
@@ -963,6 +1020,122 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
+  }
+}
+
+// One CTA: cuts every sequence into segments of at most L chunks, writes the
+// segment table (sequence, first chunk, chunks, k | P << 16) and marks entries
+// beyond the last segment unused.  An empty sequence is one segment of no chunks.
+__global__ void __launch_bounds__(1024) seg_plan_kernel(Plan plan, int L, int4* __restrict__ tab,
+                                                        int segs_ub) {
+  __shared__ int32_t warp_sums[32];
+  __shared__ int32_t carry;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  for (int base = 0; base < plan.n_seqs; base += blockDim.x) {
+    const int n = base + tid;
+    int c0 = 0, nch = 0, P = 0;
+    if (n < plan.n_seqs) {
+      c0 = plan.chunk_off[n];
+      nch = plan.chunk_off[n + 1] - c0;
+      P = nch > 0 ? (nch + L - 1) / L : 1;
+    }
+    int32_t v = P;  // block-wide inclusive scan of P
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
+    }
+    if (lane == 31) warp_sums[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+      int32_t w = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      warp_sums[lane] = w;
+    }
+    __syncthreads();
+    const int32_t first = carry + v - P + (warp > 0 ? warp_sums[warp - 1] : 0);
+    for (int k = 0; k < P && first + k < segs_ub; ++k)
+      tab[first + k] = make_int4(n, c0 + k * L, min(L, nch - k * L) > 0 ? min(L, nch - k * L) : 0,
+                                 k | (P << 16));
+    __syncthreads();
+    if (tid == blockDim.x - 1) carry = first + P;
+    __syncthreads();
+  }
+  for (int i = carry + tid; i < segs_ub; i += blockDim.x) tab[i] = make_int4(-1, 0, 0, 0);
+}
+
+// Incoming states of the segments of one (sequence, head), in order:
+//   S_in(1) = S_end(0),   S_in(k+1)^T = S~(k)^T + S_in(k)^T M(k)^T,
+// in fp32 on the CUDA cores; each thread forms an 8 x 8 block of the 128 x 128 product.
+constexpr int kScanLd = 129;  // padded rows of the running state in shared memory
+constexpr uint32_t kScanSmem = (128 * kScanLd + 128 * 128) * 4;
+
+__global__ void __launch_bounds__(256, 1)
+    seg_scan_kernel(const int4* __restrict__ tab, int segs_ub, int H,
+                    const float* __restrict__ s_end, const float* __restrict__ m_t,
+                    float* __restrict__ s_in) {
+  extern __shared__ __align__(16) float scan_sm[];
+  float* X = scan_sm;                 // [128][kScanLd]
+  float* Mt = scan_sm + 128 * kScanLd;  // [128][128]
+  const int h = blockIdx.y, tid = threadIdx.x;
+  // the first segment of sequence blockIdx.x (the table is in sequence order)
+  const int n = blockIdx.x;
+  int first = -1;
+  for (int i = 0; i < segs_ub; ++i) {
+    const int4 e = tab[i];
+    if (e.x == n) { first = i; break; }
+    if (e.x < 0 || e.x > n) break;
+  }
+  if (first < 0) return;
+  const int P = tab[first].w >> 16;
+  if (P <= 1) return;
+  const auto head = [&](int seg) { return ((int64_t)seg * H + h) * D * D; };
+  // S_in(1) = S_end(0)
+  for (int i = tid; i < D * D; i += 256) {
+    const float x = s_end[head(first) + i];
+    X[(i >> 7) * kScanLd + (i & 127)] = x;
+    s_in[head(first + 1) + i] = x;
+  }
+  const int v0 = (tid >> 4) * 8, d0 = (tid & 15) * 8;
+  for (int k = 1; k + 1 < P; ++k) {
+    for (int i = tid; i < D * D / 4; i += 256)
+      reinterpret_cast<float4*>(Mt)[i] = reinterpret_cast<const float4*>(m_t + head(first + k))[i];
+    __syncthreads();
+    float acc[8][8];
+#pragma unroll
+    for (int a = 0; a < 8; ++a)
+#pragma unroll
+      for (int b = 0; b < 8; ++b) acc[a][b] = 0.f;
+    for (int e = 0; e < D; ++e) {
+      const float4 m0 = *reinterpret_cast<const float4*>(Mt + e * D + d0);
+      const float4 m1 = *reinterpret_cast<const float4*>(Mt + e * D + d0 + 4);
+      const float mv[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+#pragma unroll
+      for (int a = 0; a < 8; ++a) {
+        const float xv = X[(v0 + a) * kScanLd + e];
+#pragma unroll
+        for (int b = 0; b < 8; ++b) acc[a][b] = fmaf(xv, mv[b], acc[a][b]);
+      }
+    }
+    __syncthreads();  // every read of X done
+    const float* se = s_end + head(first + k);
+    float* out = s_in + head(first + k + 1);
+#pragma unroll
+    for (int a = 0; a < 8; ++a)
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        const int idx = (v0 + a) * D + d0 + b;
+        const float y = se[idx] + acc[a][b];
+        X[(v0 + a) * kScanLd + d0 + b] = y;
+        out[idx] = y;
+      }
+    __syncthreads();
   }
 }
 
@@ -1010,21 +1183,74 @@ int sm_count() {
 
 }  // namespace
 
-size_t tc_workspace_bytes(int64_t n_tokens, int n_seqs, int H) {
-  const size_t units = (size_t)chunks_upper_bound(n_tokens, n_seqs) * H;
-  return units * (kUnitBytes + kGamBytes) + 1024;
+namespace {
+
+// The tensor-core workspace after the plan: tiles, gamma_C, and with segments
+// the segment table and the three state arrays.
+struct TcLayout {
+  uint8_t* tiles;
+  float* gam;
+  int4* segtab;
+  float *s_end, *m_t, *s_in;
+  int segs_ub;
+  size_t bytes;  // from the start of the workspace
+};
+
+TcLayout tc_layout(void* ws, int64_t n_tokens, int n_seqs, int H, int seg_chunks) {
+  TcLayout l{};
+  const int64_t chunks = chunks_upper_bound(n_tokens, n_seqs);
+  const size_t units = (size_t)chunks * H;
+  size_t off = (plan_bytes(n_tokens, n_seqs) + 1023) & ~size_t(1023);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  l.tiles = base + off;
+  off += units * kUnitBytes;
+  l.gam = reinterpret_cast<float*>(base + off);
+  off += units * kGamBytes;
+  if (seg_chunks > 0) {
+    l.segs_ub = (int)(chunks / seg_chunks + n_seqs);
+    off = (off + 255) & ~size_t(255);
+    l.segtab = reinterpret_cast<int4*>(base + off);
+    off += (size_t)l.segs_ub * sizeof(int4);
+    off = (off + 255) & ~size_t(255);
+    const size_t st = (size_t)l.segs_ub * H * D * D * sizeof(float);
+    l.s_end = reinterpret_cast<float*>(base + off);
+    l.m_t = reinterpret_cast<float*>(base + off + st);
+    l.s_in = reinterpret_cast<float*>(base + off + 2 * st);
+    off += 3 * st;
+  }
+  l.bytes = off + 1024;  // slack for the 1024-byte alignment of an unaligned base
+  return l;
+}
+
+}  // namespace
+
+int chain_segment_chunks(int64_t n_tokens, int n_seqs, int H, int forced, bool sequential) {
+  if (sequential || n_seqs < 1 || H < 1) return 0;
+  if (forced > 0) return forced;
+  const int64_t sms = sm_count();
+  const int64_t chains = (int64_t)n_seqs * H;
+  if (2 * chains > sms) return 0;  // enough chains to fill the GPU
+  const int64_t per_seq = chunks_upper_bound(n_tokens, n_seqs) / n_seqs;
+  if (per_seq < 256) return 0;     // short chains: the serial chain is short
+  const int64_t parts = sms / chains >= 2 ? sms / chains : 2;
+  const int64_t L = (per_seq + parts - 1) / parts;
+  return (int)(L > 64 ? L : 64);
+}
+
+size_t tc_workspace_bytes(int64_t n_tokens, int n_seqs, int H, int seg_chunks) {
+  return tc_layout(nullptr, n_tokens, n_seqs, H, seg_chunks).bytes -
+         plan_bytes(n_tokens, n_seqs);
 }
 
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const float* g,
                             const void* z, const float* A, float g_min, const void* beta,
                             const float* h0, void* o, float* hT, int64_t n_tokens, int n_seqs,
-                            int H, void* ws, int* err, cudaStream_t s) {
+                            int H, int seg_chunks, void* ws, int* err, cudaStream_t s) {
   const Plan plan = plan_in(ws, n_tokens, n_seqs);
   const int64_t units = chunks_upper_bound(n_tokens, n_seqs) * H;
-  uintptr_t body = reinterpret_cast<uintptr_t>(ws) + plan_bytes(n_tokens, n_seqs);
-  body = (body + 1023) & ~uintptr_t(1023);
-  uint8_t* tiles = reinterpret_cast<uint8_t*>(body);
-  float* gam = reinterpret_cast<float*>(tiles + (size_t)units * kUnitBytes);
+  const TcLayout lay = tc_layout(ws, n_tokens, n_seqs, H, seg_chunks);
+  uint8_t* tiles = lay.tiles;
+  float* gam = lay.gam;
   cudaError_t e;
   using T = __nv_bfloat16;
   const bool fused = z != nullptr;
@@ -1051,10 +1277,43 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
   }
   e = cudaFuncSetAttribute(tc_chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kC_Smem);
   if (e != cudaSuccess) return e;
-  const dim3 cgrid((unsigned)n_seqs, (unsigned)H);
-  ProfScope prof_scope("kda_tc_chain", s);
-  tc_chain<<<cgrid, kChainThreads, kC_Smem, s>>>(tiles, gam, h0, plan, H, static_cast<T*>(o), hT,
-                                                  err);
+  if (seg_chunks <= 0) {
+    const dim3 cgrid((unsigned)n_seqs, (unsigned)H);
+    ProfScope prof_scope("kda_tc_chain", s);
+    tc_chain<<<cgrid, kChainThreads, kC_Smem, s>>>(tiles, gam, h0, plan, H, static_cast<T*>(o),
+                                                    hT, SegArgs{0, nullptr, nullptr, nullptr, nullptr},
+                                                    err);
+    return cudaGetLastError();
+  }
+  // sequence-segment parallel chain: segments, end states and transitions, scan, rerun
+  SegArgs sg{1, lay.segtab, lay.s_end, lay.m_t, lay.s_in};
+  {
+    ProfScope prof_scope("kda_seg_plan", s);
+    seg_plan_kernel<<<1, 1024, 0, s>>>(plan, seg_chunks, lay.segtab, lay.segs_ub);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  {
+    ProfScope prof_scope("kda_tc_chain_seg", s);
+    tc_chain<<<dim3((unsigned)lay.segs_ub, (unsigned)H, 2), kChainThreads, kC_Smem, s>>>(
+        tiles, gam, h0, plan, H, static_cast<T*>(o), hT, sg, err);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  e = cudaFuncSetAttribute(seg_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kScanSmem);
+  if (e != cudaSuccess) return e;
+  {
+    ProfScope prof_scope("kda_seg_scan", s);
+    seg_scan_kernel<<<dim3((unsigned)n_seqs, (unsigned)H), 256, kScanSmem, s>>>(
+        lay.segtab, lay.segs_ub, H, lay.s_end, lay.m_t, lay.s_in);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  sg.mode = 2;
+  ProfScope prof_scope("kda_tc_chain_seg", s);
+  tc_chain<<<dim3((unsigned)lay.segs_ub, (unsigned)H, 1), kChainThreads, kC_Smem, s>>>(
+      tiles, gam, h0, plan, H, static_cast<T*>(o), hT, sg, err);
   return cudaGetLastError();
 }
 

@@ -106,12 +106,15 @@ cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v, int b
                               cudaStream_t s);
 
 // bf16 tensor-core (tcgen05) chunk path.
-size_t tc_workspace_bytes(int64_t n_tokens, int n_seqs, int H);
+// Chunks per chain segment for the sequence-segment parallel chain (0: the chain of
+// each (sequence, head) runs in one CTA).  `forced` > 0 overrides the choice.
+int chain_segment_chunks(int64_t n_tokens, int n_seqs, int H, int forced, bool sequential);
+size_t tc_workspace_bytes(int64_t n_tokens, int n_seqs, int H, int seg_chunks);
 // With z non-null the gate is fused: g is formed from z (bf16), A and g_min and g
 // is ignored.
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const float* g,
                             const void* z, const float* A, float g_min, const void* beta,
                             const float* h0, void* o, float* hT, int64_t n_tokens, int n_seqs,
-                            int H, void* ws, int* err_flag, cudaStream_t s);
+                            int H, int seg_chunks, void* ws, int* err_flag, cudaStream_t s);
 
 }  // namespace kda

@@ -85,6 +85,9 @@ kda_status_t kda_gate(const void* z, int z_dtype, const float* A, float g_min, f
  * Returns 0 for invalid arguments.
  */
 size_t kda_chunk_fwd_workspace_size(int64_t n_tokens, int n_seqs, int H, int dtype);
+/* The same for kda_chunk_fwd_ex with `flags` (kda_chunk_fwd_workspace_size is flags = 0). */
+size_t kda_chunk_fwd_workspace_size_ex(int64_t n_tokens, int n_seqs, int H, int dtype,
+                                       unsigned flags);
 
 /*
  * kda_chunk_fwd -- prefill: the KDA forward over whole sequences, evaluated in
@@ -122,14 +125,33 @@ kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v, int dtyp
                            kda_stream_t stream);
 
 /* Flags of kda_chunk_fwd_ex. */
-enum { KDA_CHUNK_FP32_CORES = 1u /* evaluate on fp32 CUDA cores even for bf16 inputs */ };
+enum {
+  KDA_CHUNK_FP32_CORES = 1u, /* evaluate on fp32 CUDA cores even for bf16 inputs */
+  KDA_CHUNK_SEQUENTIAL = 2u  /* never split a sequence's chain into segments */
+};
+/* Split every sequence's chain into segments of n chunks (n in 1..65535). */
+#define KDA_CHUNK_SEGMENT_CHUNKS(n) (((unsigned)(n) & 0xffffu) << 16)
 
 /*
  * kda_chunk_fwd_ex -- kda_chunk_fwd with option flags (0 = kda_chunk_fwd).
  * KDA_CHUNK_FP32_CORES selects the fp32 CUDA-core evaluation of the same chunkwise
- * form for bf16 inputs (the path KDA_F32 inputs always take); its workspace
- * requirement is kda_chunk_fwd_workspace_size(NT, N, H, KDA_F32).  Unknown flag
- * bits return KDA_ERR_INVALID_ARG.
+ * form for bf16 inputs (the path KDA_F32 inputs always take).
+ *
+ * Sequence segments (bf16 tensor-core path): the state update of one (sequence,
+ * head) is serial over its chunks.  When there are too few (sequence, head)
+ * chains to occupy the GPU (2 N H <= number of SMs) and sequences average at
+ * least 256 chunks, the library cuts each sequence into segments that run in
+ * parallel and joins them with the context-parallel algebra of the K3 report
+ * ("Kimi K3 technical report review", section 8.1, Eq. 17): each segment's end
+ * state is S~ + M S_in with S~ its run from a zero state and M the product of its
+ * chunk transitions; the incoming states follow by an ordered scan and the
+ * segments are rerun from them.  The result equals the serial chain up to
+ * rounding.  KDA_CHUNK_SEQUENTIAL turns this off; KDA_CHUNK_SEGMENT_CHUNKS(n)
+ * forces segments of n chunks.
+ *
+ * The workspace requirement depends on the flags:
+ * kda_chunk_fwd_workspace_size_ex(NT, N, H, dtype, flags).  Unknown flag bits
+ * return KDA_ERR_INVALID_ARG.
  */
 kda_status_t kda_chunk_fwd_ex(const void* q, const void* k, const void* v, int dtype,
                               const float* g, const void* beta, const float* h0,

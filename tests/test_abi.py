@@ -71,7 +71,7 @@ def test_chunk_rejects_bad_arguments(L):
     assert _chunk(L, q=FAKE + 8) == 4
     assert _chunk(L, ws=FAKE + 16) == 4
     assert _chunk(L, ws_bytes=16) == 5
-    assert _chunk(L, flags=2) == 1
+    assert _chunk(L, flags=4) == 1
     assert _chunk(L, B=2, cu=FAKE, n_seqs=2) == 1  # B must be 1 with cu_seqlens
     assert _chunk(L, cu=FAKE, n_seqs=0) == 1
     assert _chunk(L, q=None) == 1
@@ -96,6 +96,14 @@ def test_chunk_gated_rejects_bad_arguments(L):
 
 
 def test_workspace_size(L):
+    L.kda_chunk_fwd_workspace_size_ex.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                                  ctypes.c_int, ctypes.c_uint]
+    L.kda_chunk_fwd_workspace_size_ex.restype = ctypes.c_size_t
+    # chain segments add state scratch; sequential and fp32-core evaluation do not
+    seg = L.kda_chunk_fwd_workspace_size_ex(16384, 1, 2, 1, 16 << 16)
+    seq = L.kda_chunk_fwd_workspace_size_ex(16384, 1, 2, 1, 2)
+    assert seg > seq > 0
+    assert L.kda_chunk_fwd_workspace_size_ex(8192, 1, 96, 1, 0) == L.kda_chunk_fwd_workspace_size(8192, 1, 96, 1)
     a = L.kda_chunk_fwd_workspace_size(8192, 1, 96, 1)
     b = L.kda_chunk_fwd_workspace_size(8192, 1, 96, 0)
     assert a > 0 and b > 0

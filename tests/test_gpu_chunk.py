@@ -237,3 +237,59 @@ def test_long_context_prefix(kda):
     o_full, _ = kda.chunk_fwd(dev["q"], dev["k"], dev["v"], g, dev["beta"], None,
                               dev["cu_seqlens"])
     assert torch.equal(o_full[:P], oP)
+
+
+# ---------------------------------------------------------------- chain segments
+@pytest.mark.parametrize("seg", [1, 3, 5])
+def test_segmented_chain_single_sequence(kda, seg):
+    """A 1489-token sequence (24 chunks, ragged tail) whose chain is cut into
+    segments of `seg` chunks, joined by the end-state scan, against the oracle."""
+    inp, g, dev = _inputs([64 * 23 + 17], H=2, dtype=torch.bfloat16, seed=300 + seg)
+    o, hT = _run(kda, dev, flags=kda.segment_chunks(seg))
+    o_ref, h_ref = oracle.recurrence(inp["q"], inp["k"], inp["v"], g, inp["beta"], inp["h0"],
+                                     inp["cu_seqlens"])
+    assert_close(o, o_ref, torch.bfloat16, f"o seg={seg}")
+    assert_close(hT, h_ref, torch.bfloat16, f"hT seg={seg}")
+
+
+def test_segmented_chain_varlen(kda):
+    """Segments of 3 chunks over packed sequences: empty, one chunk, ragged, long."""
+    lens = [300, 0, 1000, 64, 2000, 1]
+    inp, g, dev = _inputs(lens, H=3, dtype=torch.bfloat16, seed=41)
+    o, hT = _run(kda, dev, flags=kda.segment_chunks(3))
+    o_ref, h_ref = oracle.recurrence(inp["q"], inp["k"], inp["v"], g, inp["beta"], inp["h0"],
+                                     inp["cu_seqlens"])
+    assert_close(o, o_ref, torch.bfloat16, "o segmented varlen")
+    assert_close(hT, h_ref, torch.bfloat16, "hT segmented varlen")
+
+
+def test_segmented_chain_slow_decay(kda):
+    """Slow decays carry state across many segments: the scan's transitions matter."""
+    inp, g, dev = _inputs([64 * 40], H=2, dtype=torch.bfloat16, seed=43, g_lo=-0.02, g_hi=0.0)
+    o, hT = _run(kda, dev, flags=kda.segment_chunks(4))
+    o_ref, h_ref = oracle.recurrence(inp["q"], inp["k"], inp["v"], g, inp["beta"], inp["h0"],
+                                     inp["cu_seqlens"])
+    assert_close(o, o_ref, torch.bfloat16, "o segmented slow decay")
+    assert_close(hT, h_ref, torch.bfloat16, "hT segmented slow decay")
+
+
+def test_sequential_flag_and_auto_segments_agree_with_oracle(kda):
+    """B=1, T=32768, H=4 bf16: the automatic choice splits the chain (few chains,
+    long sequence); the sequential flag does not.  Both against the oracle on two
+    heads."""
+    w = workloads.custom([32768], H=4, dtype=torch.bfloat16, seed=51, h0_std=0.02)
+    dev = workloads.make_inputs(w, "cuda")
+    o_auto, h_auto = kda.chunk_fwd_gated(dev["q"], dev["k"], dev["v"], dev["z"], dev["A"],
+                                         dev["beta"], dev["h0"], dev["cu_seqlens"])
+    g = kda.gate(dev["z"], dev["A"])
+    o_seq, h_seq = kda.chunk_fwd(dev["q"], dev["k"], dev["v"], g, dev["beta"], dev["h0"],
+                                 dev["cu_seqlens"], flags=kda.SEQUENTIAL)
+    torch.cuda.synchronize()
+    for h in (0, 3):
+        sl = lambda t: t[:, h:h + 1]
+        g_ref = oracle.gate(sl(dev["z"]), dev["A"][h:h + 1])
+        o_ref, h_ref = oracle.recurrence(sl(dev["q"]), sl(dev["k"]), sl(dev["v"]), g_ref,
+                                         sl(dev["beta"]), dev["h0"][:, h:h + 1])
+        for name, o_, h_ in (("auto", o_auto, h_auto), ("sequential", o_seq, h_seq)):
+            assert_close(sl(o_), o_ref, torch.bfloat16, f"o {name} head {h}")
+            assert_close(h_[:, h:h + 1], h_ref, torch.bfloat16, f"hT {name} head {h}")
