@@ -80,19 +80,57 @@ def load_peaks():
 
 
 # ----------------------------------------------------------------------- clocks
+class _Nvml:
+    """Read-only NVML queries through ctypes (SM clock, its maximum, and the active
+    clock-event reasons): fast enough to sample short timed regions.  Nothing is
+    ever set."""
+
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+               0x4: "sw_power_cap"}
+
+    def __init__(self, index: int):
+        import ctypes
+        self.ok = False
+        try:
+            self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.lib.nvmlInit_v2() != 0:
+                return
+            self.handle = ctypes.c_void_p()
+            if self.lib.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(self.handle)) != 0:
+                return
+            self.ct = ctypes
+            self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(self.lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.ok = True
+        except (OSError, AttributeError):
+            pass
+
+    def sample(self):
+        ct = self.ct
+        sm, mx, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.handle, 1, ct.byref(sm)) != 0:  # NVML_CLOCK_SM
+            return None
+        self.lib.nvmlDeviceGetMaxClockInfo(self.handle, 1, ct.byref(mx))
+        self.reasons_fn(self.handle, ct.byref(rs))
+        return float(sm.value), float(mx.value), int(rs.value)
+
+
 class ClockSampler:
-    """Samples nvidia-smi SM clocks and throttle reasons every 200 ms."""
+    """Samples SM clocks and clock-event reasons while timed regions are open:
+    NVML every 5 ms when libnvidia-ml is loadable, else nvidia-smi every 200 ms."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, gpu_index: int = 0):
         self.gpu = gpu_index
-        self.samples = []
+        self.samples = []  # (time, sm MHz, max MHz, set of reasons)
         self._stop = threading.Event()
         self._thr = None
         self.marks = []
+        self.source = None
 
     def start(self):
         self._thr = threading.Thread(target=self._run, daemon=True)
@@ -102,13 +140,26 @@ class ClockSampler:
         self.marks.append((time.time(), on))
 
     def _run(self):
+        nv = _Nvml(self.gpu)
+        self.source = "nvml" if nv.ok else "nvidia-smi"
         while not self._stop.is_set():
             try:
+                if nv.ok:
+                    r = nv.sample()
+                    if r:
+                        reasons = {n for bit, n in _Nvml.REASONS.items() if r[2] & bit}
+                        self.samples.append((time.time(), r[0], r[1], reasons))
+                    self._stop.wait(0.005)
+                    continue
                 out = subprocess.run(["nvidia-smi", "-i", str(self.gpu),
                                       f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits"],
                                      capture_output=True, text=True, timeout=5).stdout.strip()
                 if out:
-                    self.samples.append((time.time(), [x.strip() for x in out.split(",")]))
+                    f = [x.strip() for x in out.split(",")]
+                    reasons = {n for i, n in enumerate(self.NAMES)
+                               if len(f) > 5 + i and f[5 + i].lower().startswith("active")}
+                    if _isnum(f[1]) and _isnum(f[2]):
+                        self.samples.append((time.time(), float(f[1]), float(f[2]), reasons))
             except Exception:
                 pass
             self._stop.wait(0.2)
@@ -120,7 +171,7 @@ class ClockSampler:
 
     def summary(self):
         if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clocks unavailable"]}
         # samples taken while a timed region was open
         spans, t_on = [], None
         for t, on in self.marks:
@@ -129,19 +180,12 @@ class ClockSampler:
             elif t_on is not None:
                 spans.append((t_on, t))
                 t_on = None
-        inside = [s for t, s in self.samples if any(a <= t <= b for a, b in spans)] or \
-            [s for _, s in self.samples]
-        sm = [float(s[1]) for s in inside if _isnum(s[1])]
-        mx = [float(s[2]) for s in inside if _isnum(s[2])]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = set()
-        for s in inside:
-            for i, n in enumerate(names):
-                if len(s) > 5 + i and s[5 + i].lower().startswith("active"):
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
-                "samples": len(inside)}
+        inside = [x for x in self.samples if any(a <= x[0] <= b for a, b in spans)]
+        use = inside or self.samples
+        reasons = set().union(*[x[3] for x in use])
+        return {"sm_mhz": statistics.median([x[1] for x in use]),
+                "sm_max_mhz": max(x[2] for x in use), "reasons": sorted(reasons),
+                "samples": len(inside), "source": self.source}
 
 
 def _isnum(x):
@@ -383,6 +427,34 @@ def run_gpu(args):
     dec_gbs = dec_bytes / (ms_dec * 1e-3) / 1e9
     del S
 
+    # the method's other prefill workloads: one timed fused prefill each, inputs in HBM
+    # (reported beside the headline, not part of it)
+    other = {}
+    if not args.skip_other_workloads:
+        for wl in (workloads.varlen(), workloads.long_context()):
+            inp2 = workloads.make_inputs(wl, dev)
+            N2 = wl.n_seqs
+            ws2 = torch.empty(kda.chunk_fwd_workspace_size(wl.n_tokens, N2, wl.H, torch.bfloat16),
+                              dtype=torch.uint8, device=dev)
+            o2 = torch.empty(wl.n_tokens, wl.H, D, dtype=torch.bfloat16, device=dev)
+            hT2 = torch.empty(N2, wl.H, D, D, dtype=torch.float32, device=dev)
+
+            def step2():
+                kda.chunk_fwd_gated(inp2["q"], inp2["k"], inp2["v"], inp2["z"], inp2["A"],
+                                    inp2["beta"], inp2["h0"], inp2["cu_seqlens"], workspace=ws2,
+                                    out=o2, final_state_out=hT2)
+
+            ms2 = timed(step2, 3, 3)
+            tok_heads2 = wl.n_tokens * wl.H
+            floor2 = (tok_heads2 * fused_prefill_bytes_per_token_head(2)
+                      + (2 if inp2["h0"] is not None else 1) * N2 * wl.H * state_bytes()) \
+                / (hbm_peak * 1e9) * 1e3
+            other[wl.name] = {"tokens": wl.n_tokens, "sequences": N2, "heads": wl.H,
+                              "ms_per_step": ms2, "tokens_per_s": wl.n_tokens * world / (ms2 * 1e-3),
+                              "step_floor_ms": floor2, "step_frac": floor2 / ms2}
+            del inp2, ws2, o2, hT2
+            torch.cuda.empty_cache()
+
     # end to end through the public API with host buffers
     pin = {k: v.cpu().pin_memory() for k, v in inp.items() if isinstance(v, torch.Tensor)
            and k in ("z", "q", "k", "v", "beta", "A", "h0", "cu_seqlens")}
@@ -392,9 +464,34 @@ def run_gpu(args):
     h2d = sum(v.numel() * v.element_size() for v in pin.values())
     d2h = o_host.numel() * 2 + hT_host.numel() * 4
 
+    # the large inputs are copied in slices on four copy streams (several copies in
+    # flight); a slice's copy waits until the previous step has consumed its buffer
+    copy_streams = [torch.cuda.Stream(dev) for _ in range(4)]
+    slices = []
+    for k_, v_ in pin.items():
+        n_sl = 4 if v_.numel() * v_.element_size() > (64 << 20) else 1
+        for part in torch.tensor_split(torch.arange(v_.shape[0]), n_sl):
+            if part.numel():
+                a, b = int(part[0]), int(part[-1]) + 1
+                slices.append((dbuf[k_][a:b], v_[a:b]))
+
     def e2e_step():
-        for k_, v_ in pin.items():
-            dbuf[k_].copy_(v_, non_blocking=True)
+        # the copies start after everything already on the timed stream: the timing
+        # start and the previous step, whose kernels read these buffers
+        step_begin = torch.cuda.Event()
+        step_begin.record(stream)
+        done = []
+        for i, (dst, src) in enumerate(slices):
+            cs = copy_streams[i % len(copy_streams)]
+            cs.wait_event(step_begin)
+            with torch.cuda.stream(cs):
+                dst.copy_(src, non_blocking=True)
+        for cs in copy_streams:
+            ev = torch.cuda.Event()
+            ev.record(cs)
+            done.append(ev)
+        for ev in done:
+            stream.wait_event(ev)
         if fused:
             kda.chunk_fwd_gated(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["z"], dbuf["A"],
                                 dbuf["beta"], dbuf["h0"], dbuf["cu_seqlens"], workspace=ws, out=o,
@@ -439,6 +536,7 @@ def run_gpu(args):
         "alt_step": {"step": "kda_gate + kda_chunk_fwd" if fused
                      else "kda_chunk_fwd_gated (gate fused)", "ms_per_step": ms_alt,
                      "value": NT * world / (ms_alt * 1e-3)},
+        "other_workloads": other,
         "decode": {"workload": dw.name, "ms_per_step": ms_dec, "achieved_gbs": dec_gbs,
                    "peak_gbs": hbm_peak, "frac": dec_gbs / hbm_peak,
                    "bytes_per_step": dec_bytes},
@@ -497,6 +595,8 @@ def main(argv=None):
     ap.add_argument("--path", choices=["fused", "separate"], default="fused",
                     help="prefill step: gate fused into the chunk kernels, or kda_gate then "
                          "kda_chunk_fwd (the other one is timed too, as alt_step)")
+    ap.add_argument("--skip-other-workloads", action="store_true",
+                    help="do not time the varlen and long-context prefills beside the headline")
     ap.add_argument("--profile-case", action="store_true",
                     help="run the small profiling case (for ncu captures) instead of the bench")
     ap.add_argument("--reps", type=int, default=2, help="prefill steps of --profile-case")
