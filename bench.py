@@ -425,6 +425,21 @@ def run_gpu(args):
     ms_dec = timed(dstep, max(args.steps, 20), args.warmup)
     dec_bytes = dw.N * dw.H * decode_bytes_per_head_step()
     dec_gbs = dec_bytes / (ms_dec * 1e-3) / 1e9
+
+    # four tokens per sequence in one pass over the state (speculative verify + commit)
+    TM = 4
+    mq = {k_: v_.unsqueeze(1).expand(dw.N, TM, *v_.shape[1:]).contiguous()
+          for k_, v_ in dinp.items() if k_ in ("q", "k", "v", "beta")}
+    mg = dg.unsqueeze(1).expand(dw.N, TM, *dg.shape[1:]).contiguous()
+    mo = torch.empty(dw.N, TM, dw.H, D, dtype=torch.bfloat16, device=dev)
+
+    def mstep():
+        kda.recurrent_multi_step(mq["q"], mq["k"], mq["v"], mg, mq["beta"], S, out=mo)
+
+    ms_multi = timed(mstep, max(args.steps, 20), args.warmup)
+    multi_bytes = dw.N * dw.H * (2 * state_bytes() + TM * (decode_bytes_per_head_step()
+                                                           - 2 * state_bytes()))
+    multi_gbs = multi_bytes / (ms_multi * 1e-3) / 1e9
     del S
 
     # the method's other prefill workloads: one timed fused prefill each, inputs in HBM
@@ -539,7 +554,10 @@ def run_gpu(args):
         "other_workloads": other,
         "decode": {"workload": dw.name, "ms_per_step": ms_dec, "achieved_gbs": dec_gbs,
                    "peak_gbs": hbm_peak, "frac": dec_gbs / hbm_peak,
-                   "bytes_per_step": dec_bytes},
+                   "bytes_per_step": dec_bytes,
+                   "multi_token": {"tokens_per_sequence": TM, "ms_per_step": ms_multi,
+                                   "achieved_gbs": multi_gbs, "frac": multi_gbs / hbm_peak,
+                                   "ms_per_token": ms_multi / TM}},
         "e2e": {"value": e2e_tps, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
         "gpu_launches": launches,

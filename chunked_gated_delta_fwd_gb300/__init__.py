@@ -27,7 +27,7 @@ from . import _build
 
 __all__ = ["KdaError", "gate", "chunk_fwd", "chunk_fwd_gated", "chunk_fwd_workspace_size", "recurrent_step",
            "library_path", "lib", "get_device_error", "profile_enable", "profile_collect", "G_MIN", "F32", "BF16", "FP32_CORES", "SEQUENTIAL",
-           "segment_chunks"]
+           "segment_chunks", "recurrent_multi_step"]
 
 G_MIN = -5.0
 F32, BF16 = 0, 1
@@ -70,6 +70,8 @@ def _load() -> ctypes.CDLL:
     L.kda_chunk_fwd_gated.argtypes = [vp, vp, vp, i32, vp, vp, f32, vp, vp, vp, i32, i32, i64,
                                       i32, i32, i32, vp, vp, vp, sz, vp]
     L.kda_recurrent_step.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, vp]
+    L.kda_recurrent_multi_step.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, i32, i32, i32,
+                                           i32, i32, vp]
     L.kda_last_error_string.restype = ctypes.c_char_p
     L.kda_get_device_error.argtypes = [vp]
     L.kda_version.restype = ctypes.c_char_p
@@ -77,7 +79,7 @@ def _load() -> ctypes.CDLL:
     L.kda_profile_get.argtypes = [i32, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(i32),
                                   ctypes.POINTER(ctypes.c_double)]
     for fn in (L.kda_gate, L.kda_chunk_fwd, L.kda_chunk_fwd_ex, L.kda_chunk_fwd_gated,
-               L.kda_recurrent_step, L.kda_get_device_error):
+               L.kda_recurrent_step, L.kda_recurrent_multi_step, L.kda_get_device_error):
         fn.restype = ctypes.c_int
     return L
 
@@ -247,6 +249,32 @@ def recurrent_step(q, k, v, g, beta, S, *, out=None):
     with torch.cuda.device(dev):
         _check(lib.kda_recurrent_step(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(g),
                                       _ptr(beta), _ptr(S), _ptr(o), N, H, dk, dv, _stream(dev)))
+    return o
+
+
+def recurrent_multi_step(q, k, v, g, beta, S, n_advance=None, *, out=None,
+                         return_outputs=True):
+    """T tokens per sequence: q, k, v [N, T, H, 128] (bf16/fp32), g [N, T, H, 128]
+    fp32, beta [N, T, H], S [N, H, 128, 128] fp32 advanced in place by n_advance[n]
+    tokens (int32 [N] on the device; None = all T).  Returns o [N, T, H, 128] (the
+    outputs of all T tokens), or None when return_outputs is False."""
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta)):
+        _need(t, name, q.dtype, dev)
+    _need(g, "g", torch.float32, dev)
+    _need(S, "S", torch.float32, dev)
+    if n_advance is not None:
+        _need(n_advance, "n_advance", torch.int32, dev)
+    N, T, H, dk = q.shape
+    dv = v.shape[-1]
+    o = None
+    if return_outputs:
+        o = out if out is not None else torch.empty(v.shape, dtype=v.dtype, device=dev)
+        _need(o, "out", v.dtype, dev)
+    with torch.cuda.device(dev):
+        _check(lib.kda_recurrent_multi_step(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(g),
+                                            _ptr(beta), _ptr(S), _ptr(o), _ptr(n_advance), N, T,
+                                            H, dk, dv, _stream(dev)))
     return o
 
 

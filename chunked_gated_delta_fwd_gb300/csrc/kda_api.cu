@@ -485,4 +485,32 @@ kda_status_t kda_recurrent_step(const void* q, const void* k, const void* v, int
   return KDA_OK;
 }
 
+kda_status_t kda_recurrent_multi_step(const void* q, const void* k, const void* v, int dtype,
+                                      const float* g, const void* beta, float* S, void* o,
+                                      const int32_t* n_advance, int N, int T, int H, int dk,
+                                      int dv, kda_stream_t stream) {
+  if (dtype != KDA_F32 && dtype != KDA_BF16)
+    return fail(KDA_ERR_UNSUPPORTED_DTYPE, "kda_recurrent_multi_step: dtype %d", dtype);
+  if (dk != kda::kD || dv != kda::kD)
+    return fail(KDA_ERR_UNSUPPORTED_SHAPE, "kda_recurrent_multi_step: dk=%d dv=%d (need 128)",
+                dk, dv);
+  if (H < 1 || N < 0 || T < 1 || T > KDA_MULTI_STEP_MAX_T)
+    return fail(KDA_ERR_UNSUPPORTED_SHAPE, "kda_recurrent_multi_step: N=%d T=%d H=%d", N, T, H);
+  if ((int64_t)N * H > INT32_MAX)
+    return fail(KDA_ERR_INVALID_ARG, "kda_recurrent_multi_step: N*H too large");
+  if (N == 0) return KDA_OK;
+  if (!q || !k || !v || !g || !beta || !S)
+    return fail(KDA_ERR_INVALID_ARG, "kda_recurrent_multi_step: null pointer");
+  const void* ptrs[] = {q, k, v, g, S, o};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p))
+      return fail(KDA_ERR_MISALIGNED, "kda_recurrent_multi_step: pointers must be 16-byte aligned");
+  kda_status_t st = check_device();
+  if (st != KDA_OK) return st;
+  cudaError_t e = kda::launch_decode_multi(q, k, v, dtype == KDA_BF16, g, beta, S, o, n_advance,
+                                           N, T, H, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kda_recurrent_multi_step launch");
+  return KDA_OK;
+}
+
 }  // extern "C"

@@ -89,7 +89,124 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(
   o[vec + row0 + lane] = from_f32<T>(o_mine);
 }
 
+// ---------------------------------------------------------------- several tokens
+// T tokens per (sequence, head) in one pass over the state: rows of S^T are
+// independent across tokens (row j only needs token t's k, q, alpha, beta and
+// v_j), so a warp keeps 8 rows in registers while it walks all T tokens, whose
+// vectors sit in shared memory.  The outputs of all T tokens are written; the
+// state written back is the state after the first n_adv tokens (n_adv = T when
+// no counts are given, 0 leaves the state as it was): a speculative-decode
+// verify pass (outputs for every draft token) and the commit of the accepted
+// prefix ("Kimi K3: architecture, training and inference systems", section
+// 13.2, speculative replay) in one kernel.
+constexpr int kMultiMaxT = 16;
+
+template <typename T>
+__global__ void __launch_bounds__(kDecodeThreads) decode_multi_kernel(
+    const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+    const float* __restrict__ g, const T* __restrict__ beta, float* __restrict__ S,
+    T* __restrict__ o, const int32_t* __restrict__ n_advance, int H, int Tn) {
+  // per token: q, k, alpha (4 x 128 floats with v), beta and q.k
+  __shared__ __align__(16) float tq[kMultiMaxT][kD], tk[kMultiMaxT][kD], ta[kMultiMaxT][kD],
+      tv[kMultiMaxT][kD];
+  __shared__ float tb[kMultiMaxT], tqk[kMultiMaxT];
+  const int unit = blockIdx.x;  // n * H + h
+  const int n = unit / H, h = unit - n * H;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
+  int adv = n_advance ? n_advance[n] : Tn;
+  adv = adv < 0 ? 0 : (adv > Tn ? Tn : adv);
+  for (int t = warp; t < Tn; t += kDecodeThreads / 32) {
+    const int64_t vec = (((int64_t)n * Tn + t) * H + h) * kD;
+    float qv[4], kv[4], vv[4];
+    load4(q + vec + 4 * lane, qv);
+    load4(k + vec + 4 * lane, kv);
+    load4(v + vec + 4 * lane, vv);
+    const float4 gg = *reinterpret_cast<const float4*>(g + vec + 4 * lane);
+    *reinterpret_cast<float4*>(&tq[t][4 * lane]) = make_float4(qv[0], qv[1], qv[2], qv[3]);
+    *reinterpret_cast<float4*>(&tk[t][4 * lane]) = make_float4(kv[0], kv[1], kv[2], kv[3]);
+    *reinterpret_cast<float4*>(&tv[t][4 * lane]) = make_float4(vv[0], vv[1], vv[2], vv[3]);
+    *reinterpret_cast<float4*>(&ta[t][4 * lane]) =
+        make_float4(expf(gg.x), expf(gg.y), expf(gg.z), expf(gg.w));
+    float qk = qv[0] * kv[0] + qv[1] * kv[1] + qv[2] * kv[2] + qv[3] * kv[3];
+#pragma unroll
+    for (int o_ = 16; o_ > 0; o_ >>= 1) qk += __shfl_xor_sync(0xffffffffu, qk, o_);
+    if (lane == 0) {
+      tqk[t] = qk;
+      tb[t] = to_f32(beta[((int64_t)n * Tn + t) * H + h]);
+    }
+  }
+  __syncthreads();
+  (void)tid;
+  const int row0 = warp * 32;
+  float4* Srow = reinterpret_cast<float4*>(S + (int64_t)unit * kD * kD) + row0 * (kD / 4) + lane;
+#pragma unroll 1
+  for (int r0 = 0; r0 < 32; r0 += kRowsPerIter) {
+    float4 s[kRowsPerIter];
+#pragma unroll
+    for (int i = 0; i < kRowsPerIter; ++i) s[i] = Srow[(r0 + i) * (kD / 4)];
+#pragma unroll 1
+    for (int t = 0; t < Tn; ++t) {
+      const float4 al = *reinterpret_cast<const float4*>(&ta[t][4 * lane]);
+      const float4 kk = *reinterpret_cast<const float4*>(&tk[t][4 * lane]);
+      const float4 qq = *reinterpret_cast<const float4*>(&tq[t][4 * lane]);
+      float p[kRowsPerIter], r[kRowsPerIter];
+#pragma unroll
+      for (int i = 0; i < kRowsPerIter; ++i) {
+        s[i].x *= al.x;
+        s[i].y *= al.y;
+        s[i].z *= al.z;
+        s[i].w *= al.w;
+        p[i] = kk.x * s[i].x + kk.y * s[i].y + kk.z * s[i].z + kk.w * s[i].w;
+        r[i] = qq.x * s[i].x + qq.y * s[i].y + qq.z * s[i].z + qq.w * s[i].w;
+      }
+#pragma unroll
+      for (int o_ = 16; o_ > 0; o_ >>= 1) {
+#pragma unroll
+        for (int i = 0; i < kRowsPerIter; ++i) {
+          p[i] += __shfl_xor_sync(0xffffffffu, p[i], o_);
+          r[i] += __shfl_xor_sync(0xffffffffu, r[i], o_);
+        }
+      }
+      const float b = tb[t], qk = tqk[t];
+      float o_val = 0.f;
+#pragma unroll
+      for (int i = 0; i < kRowsPerIter; ++i) {
+        const float u = b * (tv[t][row0 + r0 + i] - p[i]);
+        s[i].x = fmaf(u, kk.x, s[i].x);
+        s[i].y = fmaf(u, kk.y, s[i].y);
+        s[i].z = fmaf(u, kk.z, s[i].z);
+        s[i].w = fmaf(u, kk.w, s[i].w);
+        if (lane == i) o_val = fmaf(u, qk, r[i]);
+      }
+      if (o && lane < kRowsPerIter)
+        o[(((int64_t)n * Tn + t) * H + h) * kD + row0 + r0 + lane] = from_f32<T>(o_val);
+      if (t + 1 == adv) {
+#pragma unroll
+        for (int i = 0; i < kRowsPerIter; ++i) Srow[(r0 + i) * (kD / 4)] = s[i];
+      }
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_decode_multi(const void* q, const void* k, const void* v, int bf16,
+                                const float* g, const void* beta, float* S, void* o,
+                                const int32_t* n_advance, int N, int T, int H, cudaStream_t s) {
+  const unsigned grid = (unsigned)((int64_t)N * H);
+  ProfScope prof_scope("kda_decode_multi", s);
+  if (bf16) {
+    using E = __nv_bfloat16;
+    decode_multi_kernel<E><<<grid, kDecodeThreads, 0, s>>>(
+        static_cast<const E*>(q), static_cast<const E*>(k), static_cast<const E*>(v), g,
+        static_cast<const E*>(beta), S, static_cast<E*>(o), n_advance, H, T);
+  } else {
+    decode_multi_kernel<float><<<grid, kDecodeThreads, 0, s>>>(
+        static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v),
+        g, static_cast<const float*>(beta), S, static_cast<float*>(o), n_advance, H, T);
+  }
+  return cudaGetLastError();
+}
 
 cudaError_t launch_decode(const void* q, const void* k, const void* v, int bf16, const float* g,
                           const void* beta, float* S, void* o, int N, int H, cudaStream_t s) {

@@ -95,6 +95,11 @@ cudaError_t launch_gate(const void* z, int z_bf16, const float* A, float g_min, 
 cudaError_t launch_gate_cumsum(const void* z, int z_bf16, const float* A, float g_min, float* g,
                                float* gcum, int64_t n_tokens, int H, const int32_t* cu,
                                int n_seqs, cudaStream_t s);
+// T (<= 16) tokens per (sequence, head); the state is advanced by n_advance[n]
+// tokens (all T when n_advance is null); o may be null.
+cudaError_t launch_decode_multi(const void* q, const void* k, const void* v, int bf16,
+                                const float* g, const void* beta, float* S, void* o,
+                                const int32_t* n_advance, int N, int T, int H, cudaStream_t s);
 cudaError_t launch_decode(const void* q, const void* k, const void* v, int bf16, const float* g,
                           const void* beta, float* S, void* o, int N, int H, cudaStream_t s);
 

@@ -227,6 +227,29 @@ kda_status_t kda_recurrent_step(const void* q, const void* k, const void* v, int
                                 const float* g, const void* beta, float* S, void* o, int N, int H,
                                 int dk, int dv, kda_stream_t stream);
 
+/*
+ * kda_recurrent_multi_step -- T (1..KDA_MULTI_STEP_MAX_T) tokens per sequence in
+ * one pass over the states, for speculative decoding: the verify pass needs the
+ * outputs of every draft token, the commit advances the state over the accepted
+ * ones only ("Kimi K3: architecture, training and inference systems", section
+ * 13.2, speculative verify and replay).  Each token is the recurrence of
+ * kda_recurrent_step, applied to the T tokens in order.
+ *   q, k, v  [N][T][H][128] of `dtype` (token t of sequence n at row n*T + t)
+ *   g        [N][T][H][128] fp32 log-decays (any g <= 0);  beta [N][T][H], dtype
+ *   S        [N][H][dv][dk] fp32, in place: the state after the first
+ *            n_advance[n] tokens (n_advance: device int32 [N], values clamped to
+ *            [0, T]; NULL = all T tokens; 0 leaves the state unchanged)
+ *   o        [N][T][H][dv] of `dtype`: outputs of all T tokens computed with the
+ *            state evolving through them, whatever n_advance is; may be NULL
+ * Errors: as kda_recurrent_step; T outside 1..KDA_MULTI_STEP_MAX_T ->
+ * KDA_ERR_UNSUPPORTED_SHAPE (longer runs are prefills: kda_chunk_fwd).
+ */
+#define KDA_MULTI_STEP_MAX_T 16
+kda_status_t kda_recurrent_multi_step(const void* q, const void* k, const void* v, int dtype,
+                                      const float* g, const void* beta, float* S, void* o,
+                                      const int32_t* n_advance, int N, int T, int H, int dk,
+                                      int dv, kda_stream_t stream);
+
 /* Message for the last non-OK status returned on this thread (never NULL). */
 const char* kda_last_error_string(void);
 

@@ -124,6 +124,26 @@ def test_gate_rejects_bad_arguments(L):
     assert L.kda_gate(FAKE, 0, FAKE, -5.0, FAKE, 0, 2, 128, None, None, 1, None) == 0  # no-op
 
 
+def test_recurrent_multi_step_rejects_bad_arguments(L):
+    L.kda_recurrent_multi_step.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] + \
+        [ctypes.c_void_p] * 5 + [ctypes.c_int] * 5 + [ctypes.c_void_p]
+    args = [FAKE, FAKE, FAKE, 1, FAKE, FAKE, FAKE, FAKE, None, 4, 8, 2, 128, 128, None]
+    bad = list(args); bad[10] = 17           # T above the supported 16
+    assert L.kda_recurrent_multi_step(*bad) == 2
+    bad = list(args); bad[10] = 0
+    assert L.kda_recurrent_multi_step(*bad) == 2
+    bad = list(args); bad[12] = 64
+    assert L.kda_recurrent_multi_step(*bad) == 2
+    bad = list(args); bad[3] = 5
+    assert L.kda_recurrent_multi_step(*bad) == 3
+    bad = list(args); bad[6] = FAKE + 4
+    assert L.kda_recurrent_multi_step(*bad) == 4
+    bad = list(args); bad[0] = None
+    assert L.kda_recurrent_multi_step(*bad) == 1
+    bad = list(args); bad[9] = 0
+    assert L.kda_recurrent_multi_step(*bad) == 0   # N = 0 is a no-op
+
+
 def test_recurrent_step_rejects_bad_arguments(L):
     args = [FAKE, FAKE, FAKE, 1, FAKE, FAKE, FAKE, FAKE, 4, 2, 128, 128, None]
     bad = list(args); bad[10] = 64

@@ -91,3 +91,77 @@ def test_decode_zero_sequences_is_noop(kda):
     o = kda.recurrent_step(q, q, q, torch.zeros(0, 2, 128, device="cuda"),
                            torch.zeros(0, 2, device="cuda", dtype=torch.bfloat16), S)
     assert o.shape == (0, 2, 128)
+
+
+# ------------------------------------------------------ several tokens per step
+def _multi_inputs(N, T, H, dtype, seed):
+    w = workloads.custom([T] * N, H=H, dtype=dtype, seed=seed, h0_std=0.5)
+    inp = workloads.make_inputs(w, "cpu")
+    g = workloads.uniform_decay((N * T, H, 128), "cpu", seed=seed + 1, lo=-5.0, hi=0.0)
+    return inp, g
+
+
+def _multi_reference(inp, g, N, T, adv):
+    """Outputs of all tokens, and the state after the first adv[n] tokens, from the
+    oracle (the truncated sequences run as a packed batch)."""
+    o_ref, _ = oracle.recurrence(inp["q"], inp["k"], inp["v"], g, inp["beta"], inp["h0"],
+                                 inp["cu_seqlens"])
+    rows = torch.cat([torch.arange(n * T, n * T + a) for n, a in enumerate(adv)]).long()
+    cu = torch.tensor([0] + list(np.cumsum(adv)), dtype=torch.int32)
+    sel = lambda t: t[rows]
+    _, h_ref = oracle.recurrence(sel(inp["q"]), sel(inp["k"]), sel(inp["v"]), sel(g),
+                                 sel(inp["beta"]), inp["h0"], cu)
+    return o_ref, h_ref
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_multi_step_outputs_and_partial_commit(kda, dtype):
+    """N=5 sequences of T=6 draft tokens, H=3: outputs of all tokens, and each
+    state advanced by its own accepted count (0, 1, 3, 6, 6)."""
+    N, T, H = 5, 6, 3
+    inp, g = _multi_inputs(N, T, H, dtype, seed=61)
+    adv = [0, 1, 3, 6, 6]
+    S = inp["h0"].clone().cuda()
+    shp = lambda t: t.cuda().view(N, T, *t.shape[1:])
+    o = kda.recurrent_multi_step(shp(inp["q"]), shp(inp["k"]), shp(inp["v"]), shp(g),
+                                 shp(inp["beta"]), S,
+                                 torch.tensor(adv, dtype=torch.int32, device="cuda"))
+    o_ref, h_ref = _multi_reference(inp, g, N, T, adv)
+    assert_close(o.view(N * T, H, 128), o_ref, dtype, "o multi")
+    assert_close(S, h_ref, dtype, "S multi")
+
+
+def test_multi_step_full_advance_and_state_only(kda):
+    """n_advance omitted advances all T tokens; with outputs off only S changes."""
+    N, T, H = 4, 16, 2
+    inp, g = _multi_inputs(N, T, H, torch.bfloat16, seed=63)
+    shp = lambda t: t.cuda().view(N, T, *t.shape[1:])
+    S1 = inp["h0"].clone().cuda()
+    o = kda.recurrent_multi_step(shp(inp["q"]), shp(inp["k"]), shp(inp["v"]), shp(g),
+                                 shp(inp["beta"]), S1)
+    S2 = inp["h0"].clone().cuda()
+    none = kda.recurrent_multi_step(shp(inp["q"]), shp(inp["k"]), shp(inp["v"]), shp(g),
+                                    shp(inp["beta"]), S2, return_outputs=False)
+    assert none is None
+    o_ref, h_ref = _multi_reference(inp, g, N, T, [T] * N)
+    assert_close(o.view(N * T, H, 128), o_ref, torch.bfloat16, "o multi full")
+    assert_close(S1, h_ref, torch.bfloat16, "S multi full")
+    assert torch.equal(S1, S2)
+
+
+def test_multi_step_one_token_matches_recurrent_step(kda):
+    """T = 1 against the single-token decode step, both against the oracle."""
+    N, H = 7, 4
+    inp, g = _multi_inputs(N, 1, H, torch.bfloat16, seed=65)
+    S_multi = inp["h0"].clone().cuda()
+    S_one = inp["h0"].clone().cuda()
+    o_multi = kda.recurrent_multi_step(*(t.cuda().view(N, 1, *t.shape[1:]) for t in
+                                         (inp["q"], inp["k"], inp["v"], g, inp["beta"])),
+                                       S_multi)
+    o_one = kda.recurrent_step(inp["q"].cuda(), inp["k"].cuda(), inp["v"].cuda(), g.cuda(),
+                               inp["beta"].cuda(), S_one)
+    o_ref, h_ref = _multi_reference(inp, g, N, 1, [1] * N)
+    assert_close(o_multi.view(N, H, 128), o_ref, torch.bfloat16, "o multi T=1")
+    assert_close(o_one, o_ref, torch.bfloat16, "o step")
+    assert_close(S_multi, h_ref, torch.bfloat16, "S multi T=1")
+    assert_close(S_one, h_ref, torch.bfloat16, "S step")
