@@ -446,6 +446,28 @@ def run_gpu(args):
     # (reported beside the headline, not part of it)
     other = {}
     if not args.skip_other_workloads:
+        # the headline prefill (gate already applied) with and without the state
+        # written every 512 tokens (prefix-cache checkpoints)
+        kda.gate(inp["z"], inp["A"], out=g)
+        ck = torch.empty(NT // 512, H, D, D, dtype=torch.float32, device=dev)
+
+        def step_plain():
+            kda.chunk_fwd(inp["q"], inp["k"], inp["v"], g, inp["beta"], inp["h0"],
+                          inp["cu_seqlens"], workspace=ws, out=o, final_state_out=hT)
+
+        def step_ckpt():
+            kda.chunk_fwd_checkpointed(inp["q"], inp["k"], inp["v"], g, inp["beta"], inp["h0"],
+                                       inp["cu_seqlens"], ckpt_tokens=512,
+                                       ckpt_capacity=NT // 512, ckpt_out=ck, workspace=ws,
+                                       out=o, final_state_out=hT)
+
+        ms_plain = timed(step_plain, args.steps, args.warmup)
+        ms_ck = timed(step_ckpt, args.steps, args.warmup)
+        other["prefill_checkpoints_512"] = {
+            "checkpoints": NT // 512, "checkpoint_bytes": ck.numel() * 4,
+            "ms_per_step": ms_ck, "ms_per_step_without": ms_plain}
+        del ck
+
         for wl in (workloads.varlen(), workloads.long_context()):
             inp2 = workloads.make_inputs(wl, dev)
             N2 = wl.n_seqs

@@ -27,7 +27,7 @@ from . import _build
 
 __all__ = ["KdaError", "gate", "chunk_fwd", "chunk_fwd_gated", "chunk_fwd_workspace_size", "recurrent_step",
            "library_path", "lib", "get_device_error", "profile_enable", "profile_collect", "G_MIN", "F32", "BF16", "FP32_CORES", "SEQUENTIAL",
-           "segment_chunks", "recurrent_multi_step"]
+           "segment_chunks", "recurrent_multi_step", "chunk_fwd_checkpointed"]
 
 G_MIN = -5.0
 F32, BF16 = 0, 1
@@ -67,6 +67,8 @@ def _load() -> ctypes.CDLL:
     L.kda_chunk_fwd.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i64, i32, i32, i32, vp,
                                 vp, vp, sz, vp]
     L.kda_chunk_fwd_ex.argtypes = L.kda_chunk_fwd.argtypes + [u32]
+    L.kda_chunk_fwd_checkpointed.argtypes = (L.kda_chunk_fwd.argtypes[:16] + [vp, i32, i64]
+                                             + L.kda_chunk_fwd.argtypes[16:] + [u32])
     L.kda_chunk_fwd_gated.argtypes = [vp, vp, vp, i32, vp, vp, f32, vp, vp, vp, i32, i32, i64,
                                       i32, i32, i32, vp, vp, vp, sz, vp]
     L.kda_recurrent_step.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, vp]
@@ -176,6 +178,41 @@ def chunk_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, *, output_final_state=
                                     _ptr(c["ws"]), c["ws"].numel(), _stream(q.device),
                                     int(flags)))
     return c["o"], c["hT"]
+
+
+def chunk_fwd_checkpointed(q, k, v, g, beta, h0=None, cu_seqlens=None, *,
+                           ckpt_tokens: int = 512, ckpt_capacity=None, ckpt_out=None,
+                           output_final_state=True, workspace=None, flags: int = 0, out=None,
+                           final_state_out=None):
+    """``chunk_fwd`` that also returns the state after every ``ckpt_tokens`` tokens of
+    each sequence (bf16, tensor-core path).  Sequence n contributes
+    floor(len_n / ckpt_tokens) checkpoints, stacked in sequence order into
+    ``ckpt`` [n_ckpt, H, 128, 128] fp32 (layout of hT).  ``ckpt_capacity`` (slots to
+    allocate) defaults to the exact count, read from ``cu_seqlens`` on the host.
+    Returns ``(o, hT, ckpt)``."""
+    _need(g, "g", torch.float32, q.device)
+    c = _chunk_setup(q, k, v, beta, h0, cu_seqlens, output_final_state, workspace, flags, out,
+                     final_state_out)
+    if ckpt_capacity is None:
+        if ckpt_out is not None:
+            ckpt_capacity = ckpt_out.shape[0]
+        elif cu_seqlens is None:
+            ckpt_capacity = c["B"] * (c["T"] // int(ckpt_tokens))
+        else:
+            lens = torch.diff(cu_seqlens.to("cpu", torch.int64))
+            ckpt_capacity = int((lens.clamp(min=0) // int(ckpt_tokens)).sum())
+    ck = ckpt_out if ckpt_out is not None else torch.empty(
+        (int(ckpt_capacity), c["H"], c["dv"], c["dk"]), dtype=torch.float32, device=q.device)
+    _need(ck, "ckpt_out", torch.float32, q.device)
+    if ck.shape[0] < int(ckpt_capacity):
+        raise ValueError(f"ckpt_out holds {ck.shape[0]} < {ckpt_capacity} checkpoints")
+    with torch.cuda.device(q.device):
+        _check(lib.kda_chunk_fwd_checkpointed(
+            _ptr(q), _ptr(k), _ptr(v), c["dt"], _ptr(g), _ptr(beta), _ptr(h0),
+            _ptr(cu_seqlens), c["N"], c["B"], c["T"], c["H"], c["dk"], c["dv"], _ptr(c["o"]),
+            _ptr(c["hT"]), _ptr(ck) if int(ckpt_capacity) > 0 else None, int(ckpt_tokens),
+            int(ckpt_capacity), _ptr(c["ws"]), c["ws"].numel(), _stream(q.device), int(flags)))
+    return c["o"], c["hT"], ck
 
 
 def chunk_fwd_gated(q, k, v, z, A, beta, h0=None, cu_seqlens=None, *, g_min: float = -5.0,

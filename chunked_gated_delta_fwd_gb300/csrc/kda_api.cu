@@ -305,6 +305,9 @@ kda_status_t kda_get_device_error(kda_stream_t stream) {
   if (e != cudaSuccess) return cuda_fail(e, "clearing device error flag");
   if (host == kda::kDevErrTimeout)
     return fail(KDA_ERR_DEVICE_TIMEOUT, "a bounded device-side wait gave up");
+  if (host == kda::kDevErrCkptCapacity)
+    return fail(KDA_ERR_INVALID_ARG,
+                "more state checkpoints than ckpt_capacity (the excess was not written)");
   if (host == kda::kDevErrBadSeqlens)
     return fail(KDA_ERR_INVALID_ARG,
                 "cu_seqlens was not nondecreasing from 0 to n_tokens (clamped on the device)");
@@ -368,7 +371,8 @@ kda_status_t chunk_fwd_impl(const char* fn, const void* q, const void* k, const 
                             float g_min, const void* beta, const float* h0,
                             const int32_t* cu_seqlens, int n_seqs, int B, int64_t T, int H,
                             int dk, int dv, void* o, float* hT, void* workspace,
-                            size_t ws_bytes, kda_stream_t stream, unsigned flags) {
+                            size_t ws_bytes, kda_stream_t stream, unsigned flags,
+                            kda::CkptArgs ck = kda::CkptArgs{nullptr, 0, 0}) {
   if (dtype != KDA_F32 && dtype != KDA_BF16)
     return fail(KDA_ERR_UNSUPPORTED_DTYPE, "%s: dtype %d", fn, dtype);
   if (dk != kda::kD || dv != kda::kD)
@@ -413,7 +417,7 @@ kda_status_t chunk_fwd_impl(const char* fn, const void* q, const void* k, const 
     e = kda::launch_chunk_tc(q, k, v, g, z, A, g_min, beta, h0, o, hT, NT, N, H,
                              kda::chain_segment_chunks(NT, N, H, (int)(flags >> 16),
                                                        (flags & KDA_CHUNK_SEQUENTIAL) != 0),
-                             workspace, err, s);
+                             ck, workspace, err, s);
   else
     e = kda::launch_chunk_simt(q, k, v, dtype == KDA_BF16, g, beta, h0, o, hT, NT, N, H,
                                workspace, s);
@@ -449,6 +453,29 @@ kda_status_t kda_chunk_fwd_gated(const void* q, const void* k, const void* v, in
   return chunk_fwd_impl("kda_chunk_fwd_gated", q, k, v, dtype, nullptr, z, A, g_min, beta, h0,
                         cu_seqlens, n_seqs, B, T, H, dk, dv, o, hT, workspace, ws_bytes, stream,
                         0u);
+}
+
+kda_status_t kda_chunk_fwd_checkpointed(const void* q, const void* k, const void* v, int dtype,
+                                        const float* g, const void* beta, const float* h0,
+                                        const int32_t* cu_seqlens, int n_seqs, int B, int64_t T,
+                                        int H, int dk, int dv, void* o, float* hT, float* ckpt,
+                                        int ckpt_tokens, int64_t ckpt_capacity, void* workspace,
+                                        size_t ws_bytes, kda_stream_t stream, unsigned flags) {
+  const char* fn = "kda_chunk_fwd_checkpointed";
+  if (dtype != KDA_BF16 || (flags & KDA_CHUNK_FP32_CORES))
+    return fail(KDA_ERR_UNSUPPORTED_DTYPE, "%s: bf16 on the tensor-core path only", fn);
+  if (ckpt_tokens < kda::kChunk || ckpt_tokens % kda::kChunk != 0)
+    return fail(KDA_ERR_INVALID_ARG, "%s: ckpt_tokens=%d (a positive multiple of %d)", fn,
+                ckpt_tokens, kda::kChunk);
+  if (ckpt_capacity < 0 || (ckpt_capacity > 0 && !ckpt))
+    return fail(KDA_ERR_INVALID_ARG, "%s: ckpt_capacity=%lld with ckpt=%p", fn,
+                (long long)ckpt_capacity, (void*)ckpt);
+  if (ckpt && !aligned16(ckpt))
+    return fail(KDA_ERR_MISALIGNED, "%s: ckpt must be 16-byte aligned", fn);
+  return chunk_fwd_impl(fn, q, k, v, dtype, g, nullptr, nullptr, 0.f, beta, h0, cu_seqlens,
+                        n_seqs, B, T, H, dk, dv, o, hT, workspace, ws_bytes, stream, flags,
+                        kda::CkptArgs{ckpt_capacity > 0 ? ckpt : nullptr,
+                                      ckpt_tokens / kda::kChunk, ckpt_capacity});
 }
 
 kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v, int dtype,

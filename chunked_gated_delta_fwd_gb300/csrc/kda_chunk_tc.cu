@@ -721,7 +721,8 @@ struct SegArgs {
 __global__ void __launch_bounds__(kChainThreads, 1)
     tc_chain(const uint8_t* __restrict__ tiles, const float* __restrict__ gam,
              const float* __restrict__ h0, Plan plan, int H, __nv_bfloat16* __restrict__ o,
-             float* __restrict__ hT, SegArgs sg, int* err) {
+             float* __restrict__ hT, SegArgs sg, CkptArgs ck, const int* __restrict__ ck_off,
+             int* err) {
   // ---- this CTA's job: chunk range, initial and final state, outputs or not
   const int h = blockIdx.y;
   int n, c0, nch;
@@ -764,6 +765,18 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     }
   }
   const int64_t tend = max(tstart, (int64_t)__ldg(plan.cu + n + 1));
+  // state checkpoints of this job: the true state after every ck.every chunks of
+  // the sequence (chunk-local index jl counts from the sequence start)
+  const bool ckpt_on = ck.ckpt != nullptr && write_o;
+  const int jl0 = c0 - __ldg(plan.chunk_off + n);
+  const int64_t slen = (int64_t)__ldg(plan.cu + n + 1) - __ldg(plan.cu + n);
+  auto ckpt_row = [&](int jl_end) -> float* {  // the state after local chunk jl_end - 1
+    if (!ckpt_on || jl_end <= 0 || jl_end % ck.every != 0 || (int64_t)jl_end * C > slen)
+      return nullptr;
+    const int64_t idx = (int64_t)__ldg(ck_off + n) + jl_end / ck.every - 1;
+    if (idx >= __ldg(ck_off + n + 1) || idx >= ck.cap) return nullptr;
+    return ck.ckpt + (idx * H + h) * D * D;
+  };
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -880,6 +893,14 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       tmem_ld32(lrow + 64 * ch, sv[0]);
       tmem_ld32(lrow + 64 * ch + 32, sv[1]);
       tmem_wait_ld();
+      if (float* cp = j > 0 ? ckpt_row(jl0 + j) : nullptr) {
+#pragma unroll
+        for (int qq = 0; qq < 2; ++qq)
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(cp + (int64_t)lane * D + 64 * ch + 32 * qq + i) =
+                make_float4(sv[qq][i], sv[qq][i + 1], sv[qq][i + 2], sv[qq][i + 3]);
+      }
       {
         uint32_t pk[32];  // bf16 pairs of this thread's 64 columns of S^T
 #pragma unroll
@@ -976,7 +997,8 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     }
     if (alive && nch > 0 && wait_or_abort(bar_m2, (nch - 1) & 1, err, abort_flag))
       tc_fence_after();
-    if (fin && !*abort_flag) {
+    float* cp_end = (alive && nch > 0) ? ckpt_row(jl0 + nch) : nullptr;
+    if ((fin || cp_end) && !*abort_flag) {
       tc_fence_after();
 #pragma unroll
       for (int qq = 0; qq < 2; ++qq) {
@@ -986,8 +1008,11 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 32; i += 4)
-          *reinterpret_cast<float4*>(fin + (int64_t)lane * D + col + i) =
-              make_float4(sv[i], sv[i + 1], sv[i + 2], sv[i + 3]);
+        {
+          const float4 x = make_float4(sv[i], sv[i + 1], sv[i + 2], sv[i + 3]);
+          if (fin) *reinterpret_cast<float4*>(fin + (int64_t)lane * D + col + i) = x;
+          if (cp_end) *reinterpret_cast<float4*>(cp_end + (int64_t)lane * D + col + i) = x;
+        }
       }
     }
   } else {
@@ -1068,6 +1093,52 @@ __global__ void __launch_bounds__(1024) seg_plan_kernel(Plan plan, int L, int4* 
     __syncthreads();
   }
   for (int i = carry + tid; i < segs_ub; i += blockDim.x) tab[i] = make_int4(-1, 0, 0, 0);
+}
+
+// Checkpoint offsets: off[n] = number of state checkpoints of the sequences before n,
+// where sequence n has floor(len_n / (every * C)) of them (one per `every` whole
+// chunks, counted from its first token).  A total above `cap` flags
+// kDevErrCkptCapacity; the chain then writes only the checkpoints with index < cap.
+__global__ void __launch_bounds__(1024) ckpt_plan_kernel(Plan plan, int every, int64_t cap,
+                                                         int* __restrict__ off, int* err) {
+  __shared__ int64_t warp_sums[32];
+  __shared__ int64_t carry;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  const int64_t span = (int64_t)every * C;
+  for (int base = 0; base < plan.n_seqs; base += blockDim.x) {
+    const int n = base + tid;
+    int64_t cnt = 0;
+    if (n < plan.n_seqs) cnt = max((int64_t)0, (int64_t)(plan.cu[n + 1] - plan.cu[n])) / span;
+    int64_t v = cnt;  // block-wide inclusive scan of the counts
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
+    }
+    if (lane == 31) warp_sums[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+      int64_t w = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      warp_sums[lane] = w;
+    }
+    __syncthreads();
+    const int64_t first = carry + v - cnt + (warp > 0 ? warp_sums[warp - 1] : 0);
+    if (n < plan.n_seqs) off[n] = (int)min(first, (int64_t)INT32_MAX);
+    __syncthreads();
+    if (tid == blockDim.x - 1) carry = first + cnt;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    off[plan.n_seqs] = (int)min(carry, (int64_t)INT32_MAX);
+    if (carry > cap && err) atomicExch(err, kDevErrCkptCapacity);
+  }
 }
 
 // Incoming states of the segments of one (sequence, head), in order:
@@ -1191,6 +1262,7 @@ struct TcLayout {
   uint8_t* tiles;
   float* gam;
   int4* segtab;
+  int* ck_off;  // [n_seqs + 1] checkpoint offsets
   float *s_end, *m_t, *s_in;
   int segs_ub;
   size_t bytes;  // from the start of the workspace
@@ -1206,6 +1278,9 @@ TcLayout tc_layout(void* ws, int64_t n_tokens, int n_seqs, int H, int seg_chunks
   off += units * kUnitBytes;
   l.gam = reinterpret_cast<float*>(base + off);
   off += units * kGamBytes;
+  off = (off + 255) & ~size_t(255);
+  l.ck_off = reinterpret_cast<int*>(base + off);
+  off += ((size_t)n_seqs + 1) * sizeof(int);
   if (seg_chunks > 0) {
     l.segs_ub = (int)(chunks / seg_chunks + n_seqs);
     off = (off + 255) & ~size_t(255);
@@ -1245,7 +1320,8 @@ size_t tc_workspace_bytes(int64_t n_tokens, int n_seqs, int H, int seg_chunks) {
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const float* g,
                             const void* z, const float* A, float g_min, const void* beta,
                             const float* h0, void* o, float* hT, int64_t n_tokens, int n_seqs,
-                            int H, int seg_chunks, void* ws, int* err, cudaStream_t s) {
+                            int H, int seg_chunks, CkptArgs ck, void* ws, int* err,
+                            cudaStream_t s) {
   const Plan plan = plan_in(ws, n_tokens, n_seqs);
   const int64_t units = chunks_upper_bound(n_tokens, n_seqs) * H;
   const TcLayout lay = tc_layout(ws, n_tokens, n_seqs, H, seg_chunks);
@@ -1275,6 +1351,12 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
+  if (ck.every > 0) {  // checkpoints requested (a null ck.ckpt only checks the count)
+    ProfScope prof_scope("kda_ckpt_plan", s);
+    ckpt_plan_kernel<<<1, 1024, 0, s>>>(plan, ck.every, ck.cap, lay.ck_off, err);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   e = cudaFuncSetAttribute(tc_chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kC_Smem);
   if (e != cudaSuccess) return e;
   if (seg_chunks <= 0) {
@@ -1282,7 +1364,7 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
     ProfScope prof_scope("kda_tc_chain", s);
     tc_chain<<<cgrid, kChainThreads, kC_Smem, s>>>(tiles, gam, h0, plan, H, static_cast<T*>(o),
                                                     hT, SegArgs{0, nullptr, nullptr, nullptr, nullptr},
-                                                    err);
+                                                    ck, lay.ck_off, err);
     return cudaGetLastError();
   }
   // sequence-segment parallel chain: segments, end states and transitions, scan, rerun
@@ -1296,7 +1378,7 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
   {
     ProfScope prof_scope("kda_tc_chain_seg", s);
     tc_chain<<<dim3((unsigned)lay.segs_ub, (unsigned)H, 2), kChainThreads, kC_Smem, s>>>(
-        tiles, gam, h0, plan, H, static_cast<T*>(o), hT, sg, err);
+        tiles, gam, h0, plan, H, static_cast<T*>(o), hT, sg, ck, lay.ck_off, err);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -1313,7 +1395,7 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
   sg.mode = 2;
   ProfScope prof_scope("kda_tc_chain_seg", s);
   tc_chain<<<dim3((unsigned)lay.segs_ub, (unsigned)H, 1), kChainThreads, kC_Smem, s>>>(
-      tiles, gam, h0, plan, H, static_cast<T*>(o), hT, sg, err);
+      tiles, gam, h0, plan, H, static_cast<T*>(o), hT, sg, ck, lay.ck_off, err);
   return cudaGetLastError();
 }
 

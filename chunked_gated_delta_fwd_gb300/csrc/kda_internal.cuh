@@ -18,6 +18,7 @@ constexpr int kTile = 16;    // tokens per decay-reference tile inside a chunk
 constexpr int kDevErrNone = 0;
 constexpr int kDevErrTimeout = 7;
 constexpr int kDevErrBadSeqlens = 1;
+constexpr int kDevErrCkptCapacity = 2;
 
 // Address of this device's error flag (int on the device), or nullptr.
 int* device_error_flag();
@@ -117,9 +118,17 @@ int chain_segment_chunks(int64_t n_tokens, int n_seqs, int H, int forced, bool s
 size_t tc_workspace_bytes(int64_t n_tokens, int n_seqs, int H, int seg_chunks);
 // With z non-null the gate is fused: g is formed from z (bf16), A and g_min and g
 // is ignored.
+// State checkpoints: the state after every `every` chunks of each sequence (ckpt:
+// fp32 [cap][H][dv][dk], in sequence order); null ckpt writes none.
+struct CkptArgs {
+  float* ckpt;
+  int every;
+  int64_t cap;
+};
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const float* g,
                             const void* z, const float* A, float g_min, const void* beta,
                             const float* h0, void* o, float* hT, int64_t n_tokens, int n_seqs,
-                            int H, int seg_chunks, void* ws, int* err_flag, cudaStream_t s);
+                            int H, int seg_chunks, CkptArgs ck, void* ws, int* err_flag,
+                            cudaStream_t s);
 
 }  // namespace kda

@@ -160,6 +160,37 @@ kda_status_t kda_chunk_fwd_ex(const void* q, const void* k, const void* v, int d
                               size_t ws_bytes, kda_stream_t stream, unsigned flags);
 
 /*
+ * kda_chunk_fwd_checkpointed -- kda_chunk_fwd_ex that also writes the state at
+ * fixed token boundaries of every sequence, the KDA state checkpoints a prefix
+ * cache keeps at hash endpoints (e.g. every 512 tokens; "Kimi K3: architecture,
+ * training and inference systems", section 12.2).
+ *   ckpt         fp32 [ckpt_capacity][H][dv][dk], device, 16-byte aligned,
+ *                caller-owned; may be null only when ckpt_capacity is 0.
+ *   ckpt_tokens  checkpoint interval in tokens, a positive multiple of 64.
+ *   ckpt_capacity number of checkpoint slots in ckpt.
+ * Sequence n (of length len_n, in the order of cu_seqlens or of the batch) has
+ * c_n = floor(len_n / ckpt_tokens) checkpoints; its i-th (i = 1..c_n) is the state
+ * S^T after its first i * ckpt_tokens tokens, in the layout of hT, and is stored
+ * at index c_0 + ... + c_{n-1} + i - 1.  A checkpoint at the sequence end equals
+ * that sequence's hT.  Every other argument, the workspace size
+ * (kda_chunk_fwd_workspace_size_ex with the same flags) and the results are those
+ * of kda_chunk_fwd_ex.  The count is formed on the device from cu_seqlens: when
+ * it exceeds ckpt_capacity only the first ckpt_capacity checkpoints are written
+ * and kda_get_device_error reports KDA_ERR_INVALID_ARG.
+ * Errors: dtype other than KDA_BF16 or KDA_CHUNK_FP32_CORES set ->
+ * KDA_ERR_UNSUPPORTED_DTYPE (checkpoints are written by the tensor-core chain
+ * only); ckpt_tokens not a positive multiple of 64, negative capacity or null
+ * ckpt with a positive capacity -> KDA_ERR_INVALID_ARG; misaligned ckpt ->
+ * KDA_ERR_MISALIGNED; otherwise as kda_chunk_fwd_ex.
+ */
+kda_status_t kda_chunk_fwd_checkpointed(const void* q, const void* k, const void* v, int dtype,
+                                        const float* g, const void* beta, const float* h0,
+                                        const int32_t* cu_seqlens, int n_seqs, int B, int64_t T,
+                                        int H, int dk, int dv, void* o, float* hT, float* ckpt,
+                                        int ckpt_tokens, int64_t ckpt_capacity, void* workspace,
+                                        size_t ws_bytes, kda_stream_t stream, unsigned flags);
+
+/*
  * kda_chunk_fwd_gated -- kda_chunk_fwd with the bounded gate evaluated inside the
  * chunk kernels instead of read as g.  The gate is that of kda_gate ("Kimi K3
  * technical report review", section 3.2: g = g_min * Sigmoid(exp(A_h) z)); it is

@@ -95,6 +95,28 @@ def test_chunk_gated_rejects_bad_arguments(L):
     assert b"kda_chunk_fwd_gated" in L.kda_last_error_string()
 
 
+def _ckpt(L, dtype=1, ckpt=FAKE, every=512, cap=4, flags=0):
+    vp, i32, i64, sz, u32 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t,
+                             ctypes.c_uint)
+    L.kda_chunk_fwd_checkpointed.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i64, i32,
+                                             i32, i32, vp, vp, vp, i32, i64, vp, sz, vp, u32]
+    return L.kda_chunk_fwd_checkpointed(FAKE, FAKE, FAKE, dtype, FAKE, FAKE, None, None, 0, 1, 64,
+                                        2, 128, 128, FAKE, FAKE, ckpt, every, cap, FAKE, 1 << 40,
+                                        None, flags)
+
+
+def test_chunk_checkpointed_rejects_bad_arguments(L):
+    assert _ckpt(L, dtype=0) == 3        # checkpoints come from the tensor-core chain only
+    assert _ckpt(L, flags=1) == 3        # fp32-core evaluation requested
+    assert _ckpt(L, every=100) == 1      # not a multiple of the 64-token chunk
+    assert _ckpt(L, every=0) == 1
+    assert _ckpt(L, cap=-1) == 1
+    assert _ckpt(L, ckpt=None) == 1      # no buffer for a positive capacity
+    assert _ckpt(L, ckpt=FAKE + 4) == 4
+    assert _ckpt(L, flags=8) == 1        # unknown flag bit
+    assert b"kda_chunk_fwd_checkpointed" in L.kda_last_error_string()
+
+
 def test_workspace_size(L):
     L.kda_chunk_fwd_workspace_size_ex.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                                   ctypes.c_int, ctypes.c_uint]

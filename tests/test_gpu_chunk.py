@@ -293,3 +293,88 @@ def test_sequential_flag_and_auto_segments_agree_with_oracle(kda):
         for name, o_, h_ in (("auto", o_auto, h_auto), ("sequential", o_seq, h_seq)):
             assert_close(sl(o_), o_ref, torch.bfloat16, f"o {name} head {h}")
             assert_close(h_[:, h:h + 1], h_ref, torch.bfloat16, f"hT {name} head {h}")
+
+
+# ---------------------------------------------------------------- state checkpoints
+def _oracle_checkpoints(inp, g, lens, every):
+    """The oracle state after every `every` tokens of each sequence: the recurrence
+    run block by block, each block starting from the oracle's state at the end of
+    the previous one (the state is all the recurrence carries between tokens)."""
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    out = []
+    for n, L in enumerate(lens):
+        S = to64(inp["h0"][n:n + 1]) if inp["h0"] is not None else None
+        for i in range(L // every):
+            a, b = cu[n] + i * every, cu[n] + (i + 1) * every
+            sl = lambda t: t[a:b]
+            _, S = oracle.recurrence(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(g),
+                                     sl(inp["beta"]), S)
+            out.append(S[0])
+    H = inp["q"].shape[1]
+    return np.stack(out) if out else np.zeros((0, H, 128, 128))
+
+
+@pytest.mark.parametrize("every", [512, 128, 64])
+@pytest.mark.parametrize("flags", [0, 3 << 16], ids=["serial", "seg3"])
+def test_checkpoints_varlen(kda, every, flags):
+    """Packed sequences (empty, shorter than one interval, exact multiples, ragged)
+    with checkpoints every 512, 128 and 64 tokens, on the serial chain and on
+    segments of 3 chunks (checkpoints at segment ends and inside segments)."""
+    lens = [1024, 700, 512, 0, 1500, 64, 33]
+    inp, g, dev = _inputs(lens, H=2, dtype=torch.bfloat16, seed=61 + every)
+    o, hT, ck = kda.chunk_fwd_checkpointed(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"],
+                                           dev["h0"], dev["cu_seqlens"], ckpt_tokens=every,
+                                           flags=flags)
+    kda.get_device_error()
+    assert ck.shape[0] == sum(L // every for L in lens)
+    o_ref, h_ref = oracle.recurrence(inp["q"], inp["k"], inp["v"], g, inp["beta"], inp["h0"],
+                                     inp["cu_seqlens"])
+    assert_close(o, o_ref, torch.bfloat16, "o with checkpoints")
+    assert_close(hT, h_ref, torch.bfloat16, "hT with checkpoints")
+    ck_ref = _oracle_checkpoints(inp, g, lens, every)
+    for i in range(ck.shape[0]):
+        assert_close(ck[i], ck_ref[i], torch.bfloat16, f"checkpoint {i} every={every}")
+
+
+def test_checkpoint_at_sequence_end_equals_final_state(kda):
+    """A sequence that ends on a checkpoint boundary: its last checkpoint is hT, bit
+    for bit (both are written from the same accumulator)."""
+    lens = [256, 640]
+    inp, g, dev = _inputs(lens, H=3, dtype=torch.bfloat16, seed=71)
+    _, hT, ck = kda.chunk_fwd_checkpointed(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"],
+                                           dev["h0"], dev["cu_seqlens"], ckpt_tokens=128)
+    assert ck.shape[0] == 2 + 5
+    assert torch.equal(ck[1], hT[0]) and torch.equal(ck[6], hT[1])
+
+
+def test_checkpoints_batched_and_slow_decay_segments(kda):
+    """B=2 batched sequences of 3000 tokens with slow decays, segments of 4 chunks,
+    checkpoints every 512 tokens (5 per sequence)."""
+    B, T, H = 2, 3000, 2
+    inp, g, dev = _inputs([T] * B, H=H, dtype=torch.bfloat16, seed=73, g_lo=-0.05, g_hi=0.0)
+    shp = lambda t: t.view(B, T, *t.shape[1:])
+    o, hT, ck = kda.chunk_fwd_checkpointed(shp(dev["q"]), shp(dev["k"]), shp(dev["v"]),
+                                           shp(dev["g"]), shp(dev["beta"]), dev["h0"], None,
+                                           ckpt_tokens=512, flags=kda.segment_chunks(4))
+    assert ck.shape[0] == 10
+    ck_ref = _oracle_checkpoints(inp, g, [T] * B, 512)
+    for i in range(10):
+        assert_close(ck[i], ck_ref[i], torch.bfloat16, f"checkpoint {i}")
+
+
+def test_checkpoint_capacity_overflow_is_reported(kda):
+    """Fewer slots than checkpoints: the first `capacity` are written, nothing past
+    them, and the device error reads back as an invalid argument."""
+    lens = [700, 1100]
+    inp, g, dev = _inputs(lens, H=2, dtype=torch.bfloat16, seed=75)
+    buf = torch.full((6, 2, 128, 128), 7.0, device="cuda")
+    _, _, ck = kda.chunk_fwd_checkpointed(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"],
+                                          dev["h0"], dev["cu_seqlens"], ckpt_tokens=256,
+                                          ckpt_capacity=3, ckpt_out=buf)
+    with pytest.raises(kda.KdaError):
+        kda.get_device_error()
+    kda.get_device_error()  # the flag was cleared by the read
+    ck_ref = _oracle_checkpoints(inp, g, lens, 256)  # 2 + 4 checkpoints
+    for i in range(3):
+        assert_close(buf[i], ck_ref[i], torch.bfloat16, f"checkpoint {i}")
+    assert bool((buf[3:] == 7.0).all())
