@@ -470,8 +470,8 @@ kda_status_t kda_chunk_fwd_checkpointed(const void* q, const void* k, const void
   if (ckpt_capacity < 0 || (ckpt_capacity > 0 && !ckpt))
     return fail(KDA_ERR_INVALID_ARG, "%s: ckpt_capacity=%lld with ckpt=%p", fn,
                 (long long)ckpt_capacity, (void*)ckpt);
-  if (ckpt && !aligned16(ckpt))
-    return fail(KDA_ERR_MISALIGNED, "%s: ckpt must be 16-byte aligned", fn);
+  if (ckpt && (reinterpret_cast<uintptr_t>(ckpt) & 31u) != 0)
+    return fail(KDA_ERR_MISALIGNED, "%s: ckpt must be 32-byte aligned", fn);
   return chunk_fwd_impl(fn, q, k, v, dtype, g, nullptr, nullptr, 0.f, beta, h0, cu_seqlens,
                         n_seqs, B, T, H, dk, dv, o, hT, workspace, ws_bytes, stream, flags,
                         kda::CkptArgs{ckpt_capacity > 0 ? ckpt : nullptr,

@@ -897,9 +897,8 @@ __global__ void __launch_bounds__(kChainThreads, 1)
 #pragma unroll
         for (int qq = 0; qq < 2; ++qq)
 #pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4*>(cp + (int64_t)lane * D + 64 * ch + 32 * qq + i) =
-                make_float4(sv[qq][i], sv[qq][i + 1], sv[qq][i + 2], sv[qq][i + 3]);
+          for (int i = 0; i < 32; i += 8)
+            st_global_v8(cp + (int64_t)lane * D + 64 * ch + 32 * qq + i, &sv[qq][i]);
       }
       {
         uint32_t pk[32];  // bf16 pairs of this thread's 64 columns of S^T
@@ -1008,10 +1007,12 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 32; i += 4)
-        {
-          const float4 x = make_float4(sv[i], sv[i + 1], sv[i + 2], sv[i + 3]);
-          if (fin) *reinterpret_cast<float4*>(fin + (int64_t)lane * D + col + i) = x;
-          if (cp_end) *reinterpret_cast<float4*>(cp_end + (int64_t)lane * D + col + i) = x;
+          if (fin)
+            *reinterpret_cast<float4*>(fin + (int64_t)lane * D + col + i) =
+                make_float4(sv[i], sv[i + 1], sv[i + 2], sv[i + 3]);
+        if (cp_end) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) st_global_v8(cp_end + (int64_t)lane * D + col + i, &sv[i]);
         }
       }
     }

@@ -164,7 +164,7 @@ kda_status_t kda_chunk_fwd_ex(const void* q, const void* k, const void* v, int d
  * fixed token boundaries of every sequence, the KDA state checkpoints a prefix
  * cache keeps at hash endpoints (e.g. every 512 tokens; "Kimi K3: architecture,
  * training and inference systems", section 12.2).
- *   ckpt         fp32 [ckpt_capacity][H][dv][dk], device, 16-byte aligned,
+ *   ckpt         fp32 [ckpt_capacity][H][dv][dk], device, 32-byte aligned,
  *                caller-owned; may be null only when ckpt_capacity is 0.
  *   ckpt_tokens  checkpoint interval in tokens, a positive multiple of 64.
  *   ckpt_capacity number of checkpoint slots in ckpt.

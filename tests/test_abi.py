@@ -112,7 +112,7 @@ def test_chunk_checkpointed_rejects_bad_arguments(L):
     assert _ckpt(L, every=0) == 1
     assert _ckpt(L, cap=-1) == 1
     assert _ckpt(L, ckpt=None) == 1      # no buffer for a positive capacity
-    assert _ckpt(L, ckpt=FAKE + 4) == 4
+    assert _ckpt(L, ckpt=FAKE + 16) == 4  # 32-byte stores
     assert _ckpt(L, flags=8) == 1        # unknown flag bit
     assert b"kda_chunk_fwd_checkpointed" in L.kda_last_error_string()
 
