@@ -87,7 +87,7 @@ static_assert(kScratchBytes <= 49152, "the inverse scratch lives in the KC opera
 constexpr uint32_t kP_BKg = 163840;        // K-major (beta Gamma K)^T 128 x 64
 constexpr uint32_t kP_BV = 180224;         // K-major (beta V)^T 128 x 64
 constexpr uint32_t kP_beta = 196608;       // 64 fp32
-constexpr uint32_t kP_Tot = kP_beta + 256; // per-half-tile sums of g, [8][128] fp32
+constexpr uint32_t kP_Tot = kP_beta + 256; // per-tile sums of g, [4][128] fp32
 constexpr uint32_t kP_bars = kP_Tot + 4096;  // in_full, (unused), p, w + TMEM base
 // With the gate fused (z staged in bf16) the upper half of the g staging space and
 // one more 16 KB block hold the unit's Gamma*Q and Kt^T tiles on their way out.
@@ -95,6 +95,17 @@ constexpr uint32_t kP_Qs = kI_G + 16384;
 constexpr uint32_t kP_KTs = (kP_bars + 128 + 1023) & ~1023u;
 constexpr uint32_t kP_Smem = kP_KTs + 16384 + 1024;
 static_assert(kP_Smem <= 232448, "prep shared memory");
+// Running log-decays of the next unit, fp32 [64][128], tile-relative (G_r - R_a),
+// written during this unit's inverse: rows 0..31 and 32..63 in two 16 KB blocks.
+// Gated: the Gamma*Q staging block (its copy out has been read) and the upper half
+// of the product operand (dead once the products are done); otherwise in place
+// of the staged g.  Pass 2 reads them before it rewrites either block.
+template <bool kZ>
+__host__ __device__ constexpr uint32_t gs_block(int half) {
+  return kZ ? (half ? kP_Bop + 16384 : kP_Qs) : (half ? kI_G + 16384 : kI_G);
+}
+// warps 0-7 run the inverse on barrier 2 while warps 8-15 run the next unit's pass 1
+constexpr int kInvThreads = 256;
 constexpr int kLdL = 65, kLdT = 68;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -249,6 +260,39 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       tma_prefetch_l2_3d(&tm_g, 0, pend_h, pend_e.x);
     }
   };
+  // Pass 1 of unit `un` (warps 8-15, once its rows have landed): the gate (kZ) and
+  // the running log-decay over each 16-token tile, in base-2 units (G log2 e) so
+  // that every decay below is one ex2.  Thread -> channel pair (cp, cp + 1) of
+  // tile ta; it writes G_r - R_a for its 16 rows and the tile total.
+  auto pass1 = [&](const UnitInfo& un, uint32_t parity) -> bool {
+    if (un.chunk >= total) return true;
+    if (!mbar_wait(bar_full, parity, err)) return false;
+    const int t8 = t - kInvThreads, cp = 2 * (t8 & 63), ta = t8 >> 6;
+    const uint8_t* zg = sm + kI_G;
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll 4
+    for (int e = 0; e < 16; ++e) {
+      const int r = 16 * ta + e;
+      float2 gg = make_float2(0.f, 0.f);
+      if (r < un.len) {
+        if constexpr (kZ) {  // g = g_min / (1 + exp(-exp(A_h) z))
+          const uint32_t zw = *reinterpret_cast<const uint32_t*>(zg + (r * D + cp) * 2);
+          gg.x = __fdividef(gmin2, 1.f + exp2_approx(-un.ea * bf16_lo(zw)));
+          gg.y = __fdividef(gmin2, 1.f + exp2_approx(-un.ea * bf16_hi(zw)));
+        } else {
+          gg = *reinterpret_cast<const float2*>(zg + (r * D + cp) * 4);
+          gg.x *= kLog2e;
+          gg.y *= kLog2e;
+        }
+      }
+      s0 += gg.x;
+      s1 += gg.y;
+      *reinterpret_cast<float2*>(sm + gs_block<kZ>(r >> 5) + (r & 31) * 512 + cp * 4) =
+          make_float2(s0, s1);
+    }
+    *reinterpret_cast<float2*>(Tot + ta * D + cp) = make_float2(s0, s1);
+    return true;
+  };
   if (t == kLocator) {
     slots[0] = locate(blockIdx.x);
     slots[1] = locate(blockIdx.x + gridDim.x);
@@ -265,6 +309,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     tma_prefetch_l2_3d(&tm_g, 0, slots[1].h, (int)slots[1].t0);
   }
   named_sync(1, kPrepCompute);
+  const bool pre_ok = t < kInvThreads || pass1(slots[0], 0);
   uint32_t it = 0;
   {
     // --------------------------------------------------------- compute warps
@@ -279,51 +324,21 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     const __nv_bfloat16* sK = reinterpret_cast<const __nv_bfloat16*>(sm + kI_K);
     const __nv_bfloat16* sQ = reinterpret_cast<const __nv_bfloat16*>(sm + kI_Q);
     const __nv_bfloat16* sV = reinterpret_cast<const __nv_bfloat16*>(sm + kI_V);
-    const float* sG = reinterpret_cast<const float*>(sm + kI_G);
     for (int64_t u = blockIdx.x; u < units_ub; u += gridDim.x, ++it) {
       const UnitInfo ui = slots[it & 1];
       if (ui.chunk >= total) break;
       const int len = ui.len;
       uint8_t* unit = tiles + (size_t)u * kUnitBytes;
       if (t >= 64 && t < 128) beta_s[t - 64] = beta_nx;
-      bool ok = mbar_wait(bar_full, it & 1, err);
+      // the rows were waited for by pass 1 (warps 8-15); this wait returns at once
+      bool ok = (it > 0 || pre_ok) && mbar_wait(bar_full, it & 1, err);
       if (!named_sync_and(1, kPrepCompute, ok)) break;
 
-      // ---- pass 1: running log-decay over this thread's 8 rows, both channels, in
-      //      base-2 units (G log2 e) so that every decay below is one ex2
+      // ---- pass 2: operands of this thread's 8 rows, one channel at a time, from
+      //      the tile-relative log-decays G_r - R_a that pass 1 left in shared memory
       const int r0 = 16 * ta + 8 * hq;
-      float Gl[2][8];
-      {
-        float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int r = r0 + e;
-          float2 gg = make_float2(0.f, 0.f);
-          if (r < len) {
-            if constexpr (kZ) {  // g = g_min / (1 + exp(-exp(A_h) z))
-              const uint32_t zw = *reinterpret_cast<const uint32_t*>(
-                  reinterpret_cast<const __nv_bfloat16*>(sG) + r * D + cp);
-              gg.x = __fdividef(gmin2, 1.f + exp2_approx(-ui.ea * bf16_lo(zw)));
-              gg.y = __fdividef(gmin2, 1.f + exp2_approx(-ui.ea * bf16_hi(zw)));
-            } else {
-              gg = *reinterpret_cast<const float2*>(sG + r * D + cp);
-              gg.x *= kLog2e;
-              gg.y *= kLog2e;
-            }
-          }
-          s0 += gg.x;
-          s1 += gg.y;
-          Gl[0][e] = s0;
-          Gl[1][e] = s1;
-        }
-        *reinterpret_cast<float2*>(Tot + rg * D + cp) = make_float2(s0, s1);
-      }
-      if (t == kStorer) bulk_wait_read_all();  // pass 2 rewrites the staging space
-      named_sync(1, kPrepCompute);
-
-      // ---- pass 2: operands of this thread's 8 rows, one channel at a time
       uint32_t kw[8], qw[8], vw[8];
-      float bt[8];
+      float bt[8], Gl[2][8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const int r = r0 + e;
@@ -332,7 +347,12 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         qw[e] = in ? *reinterpret_cast<const uint32_t*>(sQ + r * D + cp) : 0u;
         vw[e] = in ? *reinterpret_cast<const uint32_t*>(sV + r * D + cp) : 0u;
         bt[e] = beta_s[r];
+        const float2 gv =
+            *reinterpret_cast<const float2*>(sm + gs_block<kZ>(r >> 5) + (r & 31) * 512 + cp * 4);
+        Gl[0][e] = gv.x;
+        Gl[1][e] = gv.y;
       }
+      if (t == kStorer) bulk_wait_read_all();  // pass 2 rewrites the staging space
       named_sync(1, kPrepCompute);  // the staged rows are all read: refill them
       if (t == kIssuer) issue_copies(slots[(it + 1) & 1]);
       if (sw) {  // visit channel cp + 1 first: swap the pair so o2 picks the half
@@ -350,14 +370,12 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
 #pragma unroll
       for (int o2 = 0; o2 < 2; ++o2) {
         const int s2 = o2 ^ sw, c = cp + s2;
-        // R_b = sum of the half-tile sums before tile b; G_C = all of them
-        float R[4], GC = 0.f, inner = 0.f;
+        // R_b = sum of the tile sums before tile b; G_C = all of them
+        float R[4], GC = 0.f;
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
           R[b] = GC;
-          const float h0s = Tot[(2 * b) * D + c], h1s = Tot[(2 * b + 1) * D + c];
-          if (b == ta && hq == 1) inner = h0s;  // the first half of this thread's tile
-          GC += h0s + h1s;
+          GC += Tot[b * D + c];
         }
         const float Ra = ta == 0 ? R[0] : (ta == 1 ? R[1] : (ta == 2 ? R[2] : R[3]));
         const float eRa = exp2_approx(Ra);       // exp(R_a) <= 1
@@ -365,7 +383,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         float f[8], fi[8], kv[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float dd = Gl[o2][e] + inner;  // G_r - R_a, in (-80, 0]
+          const float dd = Gl[o2][e];  // G_r - R_a, in (-80, 0]
           f[e] = exp2_approx(dd);
           fi[e] = exp2_approx(-dd);
           kv[e] = o2 ? bf16_hi(kw[e]) : bf16_lo(kw[e]);
@@ -463,143 +481,149 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
           *reinterpret_cast<uint4*>(sm + kP_AQs + sw128_chunk(64, r, 2 * pc + 1)) = pack8(pv + 8);
         }
       }
+      if (kZ && t == kStorer) bulk_wait_read_all();  // the next pass 1 rewrites the Q staging
       named_sync(1, kPrepCompute);
+      // Warps 8-15: pass 1 of the next unit while warps 0-7 form this unit's inverse.
+      bool ok1 = true;
+      if (t >= kInvThreads) ok1 = pass1(slots[(it + 1) & 1], (it + 1) & 1);
+      if (t < kInvThreads) {
 
-      // ---- T = (I + L)^{-1} in fp32.  Each diagonal 16x16 block from its 8x8 halves,
-      //      [A 0; C B]^{-1} = [A^{-1} 0; -B^{-1} C A^{-1}  B^{-1}], then the three
-      //      block-substitution stages for the blocks below the diagonal
-      if (t < C) {  // A^{-1}, B^{-1}: 8x8 forward substitution, one column per thread
-        const int ob = 8 * (t >> 3), cc = t & 7;
-        float x[8];
+        // ---- T = (I + L)^{-1} in fp32.  Each diagonal 16x16 block from its 8x8 halves,
+        //      [A 0; C B]^{-1} = [A^{-1} 0; -B^{-1} C A^{-1}  B^{-1}], then the three
+        //      block-substitution stages for the blocks below the diagonal
+        if (t < C) {  // A^{-1}, B^{-1}: 8x8 forward substitution, one column per thread
+          const int ob = 8 * (t >> 3), cc = t & 7;
+          float x[8];
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
+          for (int m = 0; m < 8; ++m) {
+            float acc = 0.f;
+#pragma unroll
+            for (int i2 = 0; i2 < m; ++i2) acc = fmaf(Lb[(ob + m) * kLdL + ob + i2], x[i2], acc);
+            x[m] = (m < cc) ? 0.f : (m == cc ? 1.f : -acc);
+          }
+#pragma unroll
+          for (int m = 0; m < 8; ++m) Tb[(ob + m) * kLdT + ob + cc] = x[m];
+          if (((t >> 3) & 1) == 0) {  // the zero upper-right 8x8 of the 16x16 block
+#pragma unroll
+            for (int m = 0; m < 8; ++m) Tb[(ob + m) * kLdT + ob + 8 + cc] = 0.f;
+          }
+        }
+        named_sync(2, kInvThreads);
+        {  // P = C A^{-1} per block
+          const int ba = t >> 6, i = (t >> 3) & 7, j = t & 7, o = 16 * ba;
           float acc = 0.f;
 #pragma unroll
-          for (int i2 = 0; i2 < m; ++i2) acc = fmaf(Lb[(ob + m) * kLdL + ob + i2], x[i2], acc);
-          x[m] = (m < cc) ? 0.f : (m == cc ? 1.f : -acc);
+          for (int k = 0; k < 8; ++k)  // A^{-1} has stored zeros above the diagonal
+            acc = fmaf(Lb[(o + 8 + i) * kLdL + o + k], Tb[(o + k) * kLdT + o + j], acc);
+          Ps[ba * 64 + i * 8 + j] = acc;
         }
+        named_sync(2, kInvThreads);
+        {  // lower-left 8x8 = -B^{-1} P
+          const int ba = t >> 6, i = (t >> 3) & 7, j = t & 7, o = 16 * ba;
+          float acc = 0.f;
 #pragma unroll
-        for (int m = 0; m < 8; ++m) Tb[(ob + m) * kLdT + ob + cc] = x[m];
-        if (((t >> 3) & 1) == 0) {  // the zero upper-right 8x8 of the 16x16 block
-#pragma unroll
-          for (int m = 0; m < 8; ++m) Tb[(ob + m) * kLdT + ob + 8 + cc] = 0.f;
+          for (int k = 0; k < 8; ++k)  // B^{-1} has stored zeros above the diagonal
+            acc = fmaf(Tb[(o + 8 + i) * kLdT + o + 8 + k], Ps[ba * 64 + k * 8 + j], acc);
+          Tb[(o + 8 + i) * kLdT + o + j] = -acc;
         }
-      }
-      named_sync(1, kPrepCompute);
-      if (t < 256) {  // P = C A^{-1} per block
-        const int ba = t >> 6, i = (t >> 3) & 7, j = t & 7, o = 16 * ba;
-        float acc = 0.f;
+        named_sync(2, kInvThreads);
+        // Blocks below the diagonal by doubling: first the 16x16 blocks (1,0), (3,2)
+        // of the two 32x32 diagonal blocks, then their 32x32 lower-left block,
+        //   [A 0; C B]^{-1} lower-left = -B^{-1} (C A^{-1})   (at both levels).
+        // Register-blocked: a thread computes 2 rows x 4 columns, so each shared-memory
+        // load feeds four (L) or two (T) FMAs.
+        if (t < 64) {  // level 1: P = L_{a+1,a} D_a (a = 0, 2)
+          const int blk = t >> 5, a = 2 * blk, R = a + 1, rp = (t >> 2) & 7, cq = t & 3;
+          float acc[2][4] = {};
 #pragma unroll
-        for (int k = 0; k < 8; ++k)  // A^{-1} has stored zeros above the diagonal
-          acc = fmaf(Lb[(o + 8 + i) * kLdL + o + k], Tb[(o + k) * kLdT + o + j], acc);
-        Ps[ba * 64 + i * 8 + j] = acc;
-      }
-      named_sync(1, kPrepCompute);
-      if (t < 256) {  // lower-left 8x8 = -B^{-1} P
-        const int ba = t >> 6, i = (t >> 3) & 7, j = t & 7, o = 16 * ba;
-        float acc = 0.f;
-#pragma unroll
-        for (int k = 0; k < 8; ++k)  // B^{-1} has stored zeros above the diagonal
-          acc = fmaf(Tb[(o + 8 + i) * kLdT + o + 8 + k], Ps[ba * 64 + k * 8 + j], acc);
-        Tb[(o + 8 + i) * kLdT + o + j] = -acc;
-      }
-      named_sync(1, kPrepCompute);
-      // Blocks below the diagonal by doubling: first the 16x16 blocks (1,0), (3,2)
-      // of the two 32x32 diagonal blocks, then their 32x32 lower-left block,
-      //   [A 0; C B]^{-1} lower-left = -B^{-1} (C A^{-1})   (at both levels).
-      // Register-blocked: a thread computes 2 rows x 4 columns, so each shared-memory
-      // load feeds four (L) or two (T) FMAs.
-      if (t < 64) {  // level 1: P = L_{a+1,a} D_a (a = 0, 2)
-        const int blk = t >> 5, a = 2 * blk, R = a + 1, rp = (t >> 2) & 7, cq = t & 3;
-        float acc[2][4] = {};
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {  // D_a has stored zeros above its diagonal
-          const float4 tv = *reinterpret_cast<const float4*>(Tb + (16 * a + k) * kLdT + 16 * a + 4 * cq);
-#pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            const float l = Lb[(16 * R + 2 * rp + r) * kLdL + 16 * a + k];
-            acc[r][0] = fmaf(l, tv.x, acc[r][0]);
-            acc[r][1] = fmaf(l, tv.y, acc[r][1]);
-            acc[r][2] = fmaf(l, tv.z, acc[r][2]);
-            acc[r][3] = fmaf(l, tv.w, acc[r][3]);
-          }
-        }
-#pragma unroll
-        for (int r = 0; r < 2; ++r)
-          *reinterpret_cast<float4*>(Ps + blk * 256 + (2 * rp + r) * 16 + 4 * cq) =
-              make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
-      }
-      named_sync(1, kPrepCompute);
-      if (t < 64) {  // level 1: T_{a+1,a} = -D_{a+1} P
-        const int blk = t >> 5, a = 2 * blk, R = a + 1, rp = (t >> 2) & 7, cq = t & 3;
-        float acc[2][4] = {};
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {  // D_{a+1} has stored zeros above its diagonal
-          const float4 pv = *reinterpret_cast<const float4*>(Ps + blk * 256 + k * 16 + 4 * cq);
-#pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            const float w = Tb[(16 * R + 2 * rp + r) * kLdT + 16 * R + k];
-            acc[r][0] = fmaf(w, pv.x, acc[r][0]);
-            acc[r][1] = fmaf(w, pv.y, acc[r][1]);
-            acc[r][2] = fmaf(w, pv.z, acc[r][2]);
-            acc[r][3] = fmaf(w, pv.w, acc[r][3]);
-          }
-        }
-#pragma unroll
-        for (int r = 0; r < 2; ++r)
-          *reinterpret_cast<float4*>(Tb + (16 * R + 2 * rp + r) * kLdT + 16 * a + 4 * cq) =
-              make_float4(-acc[r][0], -acc[r][1], -acc[r][2], -acc[r][3]);
-      }
-      named_sync(1, kPrepCompute);
-      // level 2: M = L[32:64, 0:32] T[0:32, 0:32] into the unused upper-right block of Tb
-      // (rows 0..31, columns 32..63); T[0:16, 16:32] is not stored (zero).
-      float* Mb = Tb + 32;
-      if (t < 128) {
-        const int rp = t >> 3, cq = t & 7, k0 = cq >= 4 ? 16 : 0;
-        float acc[2][4] = {};
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          if (k >= k0) {
-            const float4 tv = *reinterpret_cast<const float4*>(Tb + k * kLdT + 4 * cq);
+          for (int k = 0; k < 16; ++k) {  // D_a has stored zeros above its diagonal
+            const float4 tv = *reinterpret_cast<const float4*>(Tb + (16 * a + k) * kLdT + 16 * a + 4 * cq);
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
-              const float l = Lb[(32 + 2 * rp + r) * kLdL + k];
+              const float l = Lb[(16 * R + 2 * rp + r) * kLdL + 16 * a + k];
               acc[r][0] = fmaf(l, tv.x, acc[r][0]);
               acc[r][1] = fmaf(l, tv.y, acc[r][1]);
               acc[r][2] = fmaf(l, tv.z, acc[r][2]);
               acc[r][3] = fmaf(l, tv.w, acc[r][3]);
             }
           }
+#pragma unroll
+          for (int r = 0; r < 2; ++r)
+            *reinterpret_cast<float4*>(Ps + blk * 256 + (2 * rp + r) * 16 + 4 * cq) =
+                make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
         }
+        named_sync(2, kInvThreads);
+        if (t < 64) {  // level 1: T_{a+1,a} = -D_{a+1} P
+          const int blk = t >> 5, a = 2 * blk, R = a + 1, rp = (t >> 2) & 7, cq = t & 3;
+          float acc[2][4] = {};
 #pragma unroll
-        for (int r = 0; r < 2; ++r)
-          *reinterpret_cast<float4*>(Mb + (2 * rp + r) * kLdT + 4 * cq) =
-              make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
-      }
-      named_sync(1, kPrepCompute);
-      if (t < 128) {  // level 2: T[32:64, 0:32] = -T[32:64, 32:64] M; T[32:48, 48:64] is zero
-        const int rp = t >> 3, cq = t & 7, kn = rp < 8 ? 16 : 32;
-        float acc[2][4] = {};
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          if (k < kn) {
-            const float4 mv = *reinterpret_cast<const float4*>(Mb + k * kLdT + 4 * cq);
+          for (int k = 0; k < 16; ++k) {  // D_{a+1} has stored zeros above its diagonal
+            const float4 pv = *reinterpret_cast<const float4*>(Ps + blk * 256 + k * 16 + 4 * cq);
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
-              const float w = Tb[(32 + 2 * rp + r) * kLdT + 32 + k];
-              acc[r][0] = fmaf(w, mv.x, acc[r][0]);
-              acc[r][1] = fmaf(w, mv.y, acc[r][1]);
-              acc[r][2] = fmaf(w, mv.z, acc[r][2]);
-              acc[r][3] = fmaf(w, mv.w, acc[r][3]);
+              const float w = Tb[(16 * R + 2 * rp + r) * kLdT + 16 * R + k];
+              acc[r][0] = fmaf(w, pv.x, acc[r][0]);
+              acc[r][1] = fmaf(w, pv.y, acc[r][1]);
+              acc[r][2] = fmaf(w, pv.z, acc[r][2]);
+              acc[r][3] = fmaf(w, pv.w, acc[r][3]);
             }
           }
-        }
 #pragma unroll
-        for (int r = 0; r < 2; ++r)
-          *reinterpret_cast<float4*>(Tb + (32 + 2 * rp + r) * kLdT + 4 * cq) =
-              make_float4(-acc[r][0], -acc[r][1], -acc[r][2], -acc[r][3]);
+          for (int r = 0; r < 2; ++r)
+            *reinterpret_cast<float4*>(Tb + (16 * R + 2 * rp + r) * kLdT + 16 * a + 4 * cq) =
+                make_float4(-acc[r][0], -acc[r][1], -acc[r][2], -acc[r][3]);
+        }
+        named_sync(2, kInvThreads);
+        // level 2: M = L[32:64, 0:32] T[0:32, 0:32] into the unused upper-right block of Tb
+        // (rows 0..31, columns 32..63); T[0:16, 16:32] is not stored (zero).
+        float* Mb = Tb + 32;
+        if (t < 128) {
+          const int rp = t >> 3, cq = t & 7, k0 = cq >= 4 ? 16 : 0;
+          float acc[2][4] = {};
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            if (k >= k0) {
+              const float4 tv = *reinterpret_cast<const float4*>(Tb + k * kLdT + 4 * cq);
+#pragma unroll
+              for (int r = 0; r < 2; ++r) {
+                const float l = Lb[(32 + 2 * rp + r) * kLdL + k];
+                acc[r][0] = fmaf(l, tv.x, acc[r][0]);
+                acc[r][1] = fmaf(l, tv.y, acc[r][1]);
+                acc[r][2] = fmaf(l, tv.z, acc[r][2]);
+                acc[r][3] = fmaf(l, tv.w, acc[r][3]);
+              }
+            }
+          }
+#pragma unroll
+          for (int r = 0; r < 2; ++r)
+            *reinterpret_cast<float4*>(Mb + (2 * rp + r) * kLdT + 4 * cq) =
+                make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+        }
+        named_sync(2, kInvThreads);
+        if (t < 128) {  // level 2: T[32:64, 0:32] = -T[32:64, 32:64] M; T[32:48, 48:64] is zero
+          const int rp = t >> 3, cq = t & 7, kn = rp < 8 ? 16 : 32;
+          float acc[2][4] = {};
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            if (k < kn) {
+              const float4 mv = *reinterpret_cast<const float4*>(Mb + k * kLdT + 4 * cq);
+#pragma unroll
+              for (int r = 0; r < 2; ++r) {
+                const float w = Tb[(32 + 2 * rp + r) * kLdT + 32 + k];
+                acc[r][0] = fmaf(w, mv.x, acc[r][0]);
+                acc[r][1] = fmaf(w, mv.y, acc[r][1]);
+                acc[r][2] = fmaf(w, mv.z, acc[r][2]);
+                acc[r][3] = fmaf(w, mv.w, acc[r][3]);
+              }
+            }
+          }
+#pragma unroll
+          for (int r = 0; r < 2; ++r)
+            *reinterpret_cast<float4*>(Tb + (32 + 2 * rp + r) * kLdT + 4 * cq) =
+                make_float4(-acc[r][0], -acc[r][1], -acc[r][2], -acc[r][3]);
+        }
       }
-      named_sync(1, kPrepCompute);
+      if (!named_sync_and(1, kPrepCompute, ok1)) break;
       {  // T -> bf16 B operand (MN-major, X = row r, K = column j); zero above the diagonal
         const int j = t >> 3, o8 = t & 7;
         float x[8];
