@@ -20,11 +20,13 @@
 // the channels is sum_c k_rc k_ic exp(G_rc - G_ic).
 //
 // Kernel 1, tc_prep: one persistent 512-thread CTA per SM walks (chunk, head)
-// units.  A unit's k, q, v and g (or z, with the gate formed in-kernel) arrive
-// through 3-D tensor TMA copies issued as soon as the previous unit's rows are in
-// registers; every thread builds the operands of 8 tokens x 2 channels, one
-// thread issues the MMAs (the four tile products in one N=192 chain, then W^T and
-// U^T), the (I + A_kk)^{-1} inverse runs in fp32 on the CUDA cores, and the unit
+// units.  A unit's k, q, v arrive through 3-D tensor TMA copies issued as soon as
+// the previous unit's rows are in registers, its g (or z, with the gate formed
+// in-kernel) a unit earlier still: warps 8-15 form the gate and the running
+// log-decays of the next unit while warps 0-7 run this unit's (I + A_kk)^{-1}
+// inverse in fp32 on the CUDA cores.  Every thread builds the operands of 8
+// tokens x 2 channels and one thread issues the MMAs (the four tile products in
+// one N=192 chain, then W^T and U^T); the unit
 // leaves as MMA-ready bf16 tiles written with whole-tile bulk copies:
 //   W, Gamma*Q: MN-major, 64 token columns x 128 channels each (one operand with
 //               a 16 KB atom stride)
@@ -66,9 +68,10 @@ constexpr uint32_t kGamBytes = D * 4;
 // ============================================================== prep kernel
 constexpr int kPrepCompute = 512;                // 16 warps; thread 0 also issues the copies
 constexpr int kPrepThreads = kPrepCompute;
-// staged boxes per unit: k, q, v (bf16) and g (fp32), or z (bf16) when the gate is fused
+// staged boxes per unit: k, q, v (bf16), and g (fp32) or z (bf16) when the gate is fused
+constexpr uint32_t kKqvBytes = C * 3 * 256;
 template <bool kZ>
-__host__ __device__ constexpr uint32_t in_unit_bytes() { return C * (3 * 256 + (kZ ? 256 : 512)); }
+__host__ __device__ constexpr uint32_t g_unit_bytes() { return C * (kZ ? 256 : 512); }
 // shared memory (offsets from a 1024-aligned base)
 constexpr uint32_t kI_K = 0, kI_Q = 16384, kI_V = 32768, kI_G = 49152;  // staged rows
 constexpr uint32_t kP_Bop = 81920;         // MN-major X=128 (Kb/Qb rows), K=128
@@ -88,7 +91,7 @@ constexpr uint32_t kP_BKg = 163840;        // K-major (beta Gamma K)^T 128 x 64
 constexpr uint32_t kP_BV = 180224;         // K-major (beta V)^T 128 x 64
 constexpr uint32_t kP_beta = 196608;       // 64 fp32
 constexpr uint32_t kP_Tot = kP_beta + 256; // per-tile sums of g, [4][128] fp32
-constexpr uint32_t kP_bars = kP_Tot + 4096;  // in_full, (unused), p, w + TMEM base
+constexpr uint32_t kP_bars = kP_Tot + 4096;  // k/q/v full, g full, p, w + TMEM base
 // With the gate fused (z staged in bf16) the upper half of the g staging space and
 // one more 16 KB block hold the unit's Gamma*Q and Kt^T tiles on their way out.
 constexpr uint32_t kP_Qs = kI_G + 16384;
@@ -96,13 +99,15 @@ constexpr uint32_t kP_KTs = (kP_bars + 128 + 1023) & ~1023u;
 constexpr uint32_t kP_Smem = kP_KTs + 16384 + 1024;
 static_assert(kP_Smem <= 232448, "prep shared memory");
 // Running log-decays of the next unit, fp32 [64][128], tile-relative (G_r - R_a),
-// written during this unit's inverse: rows 0..31 and 32..63 in two 16 KB blocks.
-// Gated: the Gamma*Q staging block (its copy out has been read) and the upper half
-// of the product operand (dead once the products are done); otherwise in place
-// of the staged g.  Pass 2 reads them before it rewrites either block.
+// written during this unit's inverse: rows 0..31 and 32..63 in two 16 KB blocks,
+// the upper half of the product operand (dead once the products are done) and a
+// staging block that is idle then (gated: the Gamma*Q block, whose copy out has
+// been read; otherwise the Kt block, unused without the fused gate).  Pass 2
+// reads them before it rewrites either block.  The staged g / z stays free for
+// the copy of the unit after next.
 template <bool kZ>
 __host__ __device__ constexpr uint32_t gs_block(int half) {
-  return kZ ? (half ? kP_Bop + 16384 : kP_Qs) : (half ? kI_G + 16384 : kI_G);
+  return half ? kP_Bop + 16384 : (kZ ? kP_Qs : kP_KTs);
 }
 // warps 0-7 run the inverse on barrier 2 while warps 8-15 run the next unit's pass 1
 constexpr int kInvThreads = 256;
@@ -153,7 +158,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
   float* Ps = reinterpret_cast<float*>(sm + kP_Ps);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kP_bars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kP_bars + 32);
-  const uint32_t bar_full = smem_addr(&bars[0]);
+  const uint32_t bar_kqv = smem_addr(&bars[0]), bar_g = smem_addr(&bars[1]);
   const uint32_t bar_p = smem_addr(&bars[2]), bar_w = smem_addr(&bars[3]);
   const int t = threadIdx.x, warp = t >> 5;
 
@@ -161,7 +166,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
   for (uint32_t o = t * 16; o < 49152; o += kPrepThreads * 16)
     *reinterpret_cast<uint4*>(sm + kP_KC + o) = make_uint4(0, 0, 0, 0);
   if (t == 0) {
-    mbar_init(bar_full, 1);
+    mbar_init(bar_kqv, 1);
+    mbar_init(bar_g, 1);
     mbar_init(bar_p, 1);
     mbar_init(bar_w, 1);
     mbar_fence_init();
@@ -187,7 +193,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
   // masked below.
   constexpr int kIssuer = 64, kLocator = 96, kPrefetcher = 128, kStorer = 192;
   UnitInfo* slots = reinterpret_cast<UnitInfo*>(sm + kP_bars + 64);
-  uint32_t issued = 0;  // copies issued (thread kIssuer)
+  uint32_t issued_kqv = 0, issued_g = 0;  // copies issued (thread kIssuer)
   float beta_nx = 0.f;  // beta of token t - 64 of the next unit (threads 64..127)
   auto locate = [&](int64_t u) {
     UnitInfo ui;
@@ -195,15 +201,20 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     ui.ea = (kZ && ui.chunk < total) ? expf(__ldg(A + ui.h)) * kLog2e : 0.f;
     return ui;
   };
-  auto issue_copies = [&](const UnitInfo& ui) {
+  auto issue_kqv = [&](const UnitInfo& ui) {
     if (ui.chunk >= total) return;
-    mbar_arrive_expect_tx(bar_full, in_unit_bytes<kZ>());
+    mbar_arrive_expect_tx(bar_kqv, kKqvBytes);
     const int t0 = (int)ui.t0;
-    tma_load_3d(sbase + kI_K, &tm_k, 0, ui.h, t0, bar_full);
-    tma_load_3d(sbase + kI_Q, &tm_q, 0, ui.h, t0, bar_full);
-    tma_load_3d(sbase + kI_V, &tm_v, 0, ui.h, t0, bar_full);
-    tma_load_3d(sbase + kI_G, &tm_g, 0, ui.h, t0, bar_full);
-    ++issued;
+    tma_load_3d(sbase + kI_K, &tm_k, 0, ui.h, t0, bar_kqv);
+    tma_load_3d(sbase + kI_Q, &tm_q, 0, ui.h, t0, bar_kqv);
+    tma_load_3d(sbase + kI_V, &tm_v, 0, ui.h, t0, bar_kqv);
+    ++issued_kqv;
+  };
+  auto issue_g = [&](const UnitInfo& ui) {
+    if (ui.chunk >= total) return;
+    mbar_arrive_expect_tx(bar_g, g_unit_bytes<kZ>());
+    tma_load_3d(sbase + kI_G, &tm_g, 0, ui.h, (int)ui.t0, bar_g);
+    ++issued_g;
   };
   // pending table entry of the unit two ahead (threads kLocator and kPrefetcher)
   bool pend_ok = false;
@@ -266,28 +277,49 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
   // tile ta; it writes G_r - R_a for its 16 rows and the tile total.
   auto pass1 = [&](const UnitInfo& un, uint32_t parity) -> bool {
     if (un.chunk >= total) return true;
-    if (!mbar_wait(bar_full, parity, err)) return false;
+    if (!mbar_wait(bar_g, parity, err)) return false;
     const int t8 = t - kInvThreads, cp = 2 * (t8 & 63), ta = t8 >> 6;
     const uint8_t* zg = sm + kI_G;
     float s0 = 0.f, s1 = 0.f;
-#pragma unroll 4
-    for (int e = 0; e < 16; ++e) {
+#pragma unroll 2
+    for (int e = 0; e < 16; e += 2) {
       const int r = 16 * ta + e;
-      float2 gg = make_float2(0.f, 0.f);
-      if (r < un.len) {
-        if constexpr (kZ) {  // g = g_min / (1 + exp(-exp(A_h) z))
-          const uint32_t zw = *reinterpret_cast<const uint32_t*>(zg + (r * D + cp) * 2);
-          gg.x = __fdividef(gmin2, 1.f + exp2_approx(-un.ea * bf16_lo(zw)));
-          gg.y = __fdividef(gmin2, 1.f + exp2_approx(-un.ea * bf16_hi(zw)));
-        } else {
-          gg = *reinterpret_cast<const float2*>(zg + (r * D + cp) * 4);
-          gg.x *= kLog2e;
-          gg.y *= kLog2e;
-        }
+      float gv[4];  // rows r, r + 1 x channels cp, cp + 1
+      if constexpr (kZ) {
+        // g = g_min / d with d = 1 + exp(-exp(A_h) z).  The four quotients share one
+        // reciprocal: 1/d0 = d1 (d2 d3) / (d0 d1 d2 d3), and so on.  The exponent is
+        // clamped at 30 so that the product stays finite; that moves a sigmoid below
+        // 2^-30 by less than 2^-30.
+        const uint32_t z0 = *reinterpret_cast<const uint32_t*>(zg + (r * D + cp) * 2);
+        const uint32_t z1 = *reinterpret_cast<const uint32_t*>(zg + ((r + 1) * D + cp) * 2);
+        const float d0 = 1.f + exp2_approx(fminf(-un.ea * bf16_lo(z0), 30.f));
+        const float d1 = 1.f + exp2_approx(fminf(-un.ea * bf16_hi(z0), 30.f));
+        const float d2 = 1.f + exp2_approx(fminf(-un.ea * bf16_lo(z1), 30.f));
+        const float d3 = 1.f + exp2_approx(fminf(-un.ea * bf16_hi(z1), 30.f));
+        const float d01 = d0 * d1, d23 = d2 * d3;
+        const float rall = rcp_approx(d01 * d23);
+        const float q01 = gmin2 * d23 * rall, q23 = gmin2 * d01 * rall;  // g_min / (d0 d1), ...
+        gv[0] = d1 * q01;
+        gv[1] = d0 * q01;
+        gv[2] = d3 * q23;
+        gv[3] = d2 * q23;
+      } else {
+        const float2 a = *reinterpret_cast<const float2*>(zg + (r * D + cp) * 4);
+        const float2 b = *reinterpret_cast<const float2*>(zg + ((r + 1) * D + cp) * 4);
+        gv[0] = a.x * kLog2e;
+        gv[1] = a.y * kLog2e;
+        gv[2] = b.x * kLog2e;
+        gv[3] = b.y * kLog2e;
       }
-      s0 += gg.x;
-      s1 += gg.y;
+      if (r >= un.len) gv[0] = gv[1] = 0.f;  // rows past the sequence end
+      if (r + 1 >= un.len) gv[2] = gv[3] = 0.f;
+      s0 += gv[0];
+      s1 += gv[1];
       *reinterpret_cast<float2*>(sm + gs_block<kZ>(r >> 5) + (r & 31) * 512 + cp * 4) =
+          make_float2(s0, s1);
+      s0 += gv[2];
+      s1 += gv[3];
+      *reinterpret_cast<float2*>(sm + gs_block<kZ>(r >> 5) + ((r + 1) & 31) * 512 + cp * 4) =
           make_float2(s0, s1);
     }
     *reinterpret_cast<float2*>(Tot + ta * D + cp) = make_float2(s0, s1);
@@ -298,7 +330,10 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     slots[1] = locate(blockIdx.x + gridDim.x);
   }
   named_sync(1, kPrepCompute);
-  if (t == kIssuer) issue_copies(slots[0]);
+  if (t == kIssuer) {
+    issue_kqv(slots[0]);
+    issue_g(slots[0]);
+  }
   if (t >= 64 && t < 128)  // beta of unit 0
     beta_nx = (slots[0].chunk < total && t - 64 < slots[0].len)
                   ? __bfloat162float(beta[(slots[0].t0 + t - 64) * H + slots[0].h]) : 0.f;
@@ -330,9 +365,9 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       const int len = ui.len;
       uint8_t* unit = tiles + (size_t)u * kUnitBytes;
       if (t >= 64 && t < 128) beta_s[t - 64] = beta_nx;
-      // the rows were waited for by pass 1 (warps 8-15); this wait returns at once
-      bool ok = (it > 0 || pre_ok) && mbar_wait(bar_full, it & 1, err);
+      bool ok = (it > 0 || pre_ok) && mbar_wait(bar_kqv, it & 1, err);
       if (!named_sync_and(1, kPrepCompute, ok)) break;
+      if (it == 0 && t == kIssuer) issue_g(slots[1]);  // unit 0's g / z has been read
 
       // ---- pass 2: operands of this thread's 8 rows, one channel at a time, from
       //      the tile-relative log-decays G_r - R_a that pass 1 left in shared memory
@@ -354,7 +389,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       }
       if (t == kStorer) bulk_wait_read_all();  // pass 2 rewrites the staging space
       named_sync(1, kPrepCompute);  // the staged rows are all read: refill them
-      if (t == kIssuer) issue_copies(slots[(it + 1) & 1]);
+      if (t == kIssuer) issue_kqv(slots[(it + 1) & 1]);
       if (sw) {  // visit channel cp + 1 first: swap the pair so o2 picks the half
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -638,6 +673,9 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       named_sync(1, kPrepCompute);
+      // the next unit's g / z has been read by pass 1: fetch the one after it
+      // (its slot was just filled by fetch_finish)
+      if (t == kIssuer) issue_g(slots[it & 1]);
       if (t == 0) {
         tc_fence_after();
         const uint32_t id = idesc_bf16_mn(128, 64, 0, 1);
@@ -684,7 +722,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
   }
   if (t == kStorer) bulk_wait_all();
   // a copy still in flight (after an abort) must land before the CTA may exit
-  if (t == kIssuer && issued > it) mbar_wait(bar_full, (issued - 1) & 1, nullptr);
+  if (t == kIssuer && issued_kqv > 0) mbar_wait(bar_kqv, (issued_kqv - 1) & 1, nullptr);
+  if (t == kIssuer && issued_g > 0) mbar_wait(bar_g, (issued_g - 1) & 1, nullptr);
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();

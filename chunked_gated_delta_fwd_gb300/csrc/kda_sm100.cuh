@@ -384,6 +384,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_mn(int M, int N, int a_mn, int
 }
 
 // 2^x with the hardware's approximate base-2 exponential (ex2.approx).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ float exp2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
