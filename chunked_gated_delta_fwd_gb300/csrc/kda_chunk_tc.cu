@@ -82,10 +82,10 @@ constexpr uint32_t kP_AQs = kP_Bop + 8192;  //   and the A_qk tile on its way ou
 constexpr uint32_t kP_KC = 114688;
 constexpr int kKCX = 192;
 // reused after the products (the next unit rewrites every KC row it reads):
-constexpr uint32_t kP_Lb = kP_KC;            // L, fp32 [64][65] (lower blocks)
-constexpr uint32_t kP_Tb = kP_Lb + 16640;    // T, fp32 [64][68] row-major
+constexpr uint32_t kP_Lb = kP_KC;            // L, fp32 [64][68] (lower blocks)
+constexpr uint32_t kP_Tb = kP_Lb + 17408;    // T, fp32 [64][68] row-major
 constexpr uint32_t kP_Ps = kP_Tb + 17408;    // block-product scratch, fp32 [3][16][16]
-constexpr uint32_t kScratchBytes = 16640 + 17408 + 3072;
+constexpr uint32_t kScratchBytes = 17408 + 17408 + 3072;
 static_assert(kScratchBytes <= 49152, "the inverse scratch lives in the KC operand space");
 constexpr uint32_t kP_BKg = 163840;        // K-major (beta Gamma K)^T 128 x 64
 constexpr uint32_t kP_BV = 180224;         // K-major (beta V)^T 128 x 64
@@ -111,7 +111,7 @@ __host__ __device__ constexpr uint32_t gs_block(int half) {
 }
 // warps 0-7 run the inverse on barrier 2 while warps 8-15 run the next unit's pass 1
 constexpr int kInvThreads = 256;
-constexpr int kLdL = 65, kLdT = 68;
+constexpr int kLdL = 68, kLdT = 68;  // 16-byte rows: float4 loads along k
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ uint4 pack8(const float* x) {
@@ -506,8 +506,11 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
           if (pc <= tw) {
             const float br = beta_s[r];
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj)
-              Lb[r * kLdL + 16 * pc + jj] = (16 * pc + jj < r) ? br * pv[jj] : 0.f;
+            for (int jj = 0; jj < 16; ++jj) pv[jj] = (16 * pc + jj < r) ? br * pv[jj] : 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              *reinterpret_cast<float4*>(Lb + r * kLdL + 16 * pc + 4 * q) =
+                  make_float4(pv[4 * q], pv[4 * q + 1], pv[4 * q + 2], pv[4 * q + 3]);
           }
         } else {
 #pragma unroll
@@ -531,9 +534,14 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
           float x[8];
 #pragma unroll
           for (int m = 0; m < 8; ++m) {
+            float lr[8];  // row m of the 8x8 block, two 16-byte loads
+            *reinterpret_cast<float4*>(lr) =
+                *reinterpret_cast<const float4*>(Lb + (ob + m) * kLdL + ob);
+            *reinterpret_cast<float4*>(lr + 4) =
+                *reinterpret_cast<const float4*>(Lb + (ob + m) * kLdL + ob + 4);
             float acc = 0.f;
 #pragma unroll
-            for (int i2 = 0; i2 < m; ++i2) acc = fmaf(Lb[(ob + m) * kLdL + ob + i2], x[i2], acc);
+            for (int i2 = 0; i2 < m; ++i2) acc = fmaf(lr[i2], x[i2], acc);
             x[m] = (m < cc) ? 0.f : (m == cc ? 1.f : -acc);
           }
 #pragma unroll
@@ -546,19 +554,28 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         named_sync(2, kInvThreads);
         {  // P = C A^{-1} per block
           const int ba = t >> 6, i = (t >> 3) & 7, j = t & 7, o = 16 * ba;
+          float lr[8];
+          *reinterpret_cast<float4*>(lr) = *reinterpret_cast<const float4*>(Lb + (o + 8 + i) * kLdL + o);
+          *reinterpret_cast<float4*>(lr + 4) =
+              *reinterpret_cast<const float4*>(Lb + (o + 8 + i) * kLdL + o + 4);
           float acc = 0.f;
 #pragma unroll
           for (int k = 0; k < 8; ++k)  // A^{-1} has stored zeros above the diagonal
-            acc = fmaf(Lb[(o + 8 + i) * kLdL + o + k], Tb[(o + k) * kLdT + o + j], acc);
+            acc = fmaf(lr[k], Tb[(o + k) * kLdT + o + j], acc);
           Ps[ba * 64 + i * 8 + j] = acc;
         }
         named_sync(2, kInvThreads);
         {  // lower-left 8x8 = -B^{-1} P
           const int ba = t >> 6, i = (t >> 3) & 7, j = t & 7, o = 16 * ba;
+          float wr[8];
+          *reinterpret_cast<float4*>(wr) =
+              *reinterpret_cast<const float4*>(Tb + (o + 8 + i) * kLdT + o + 8);
+          *reinterpret_cast<float4*>(wr + 4) =
+              *reinterpret_cast<const float4*>(Tb + (o + 8 + i) * kLdT + o + 12);
           float acc = 0.f;
 #pragma unroll
           for (int k = 0; k < 8; ++k)  // B^{-1} has stored zeros above the diagonal
-            acc = fmaf(Tb[(o + 8 + i) * kLdT + o + 8 + k], Ps[ba * 64 + k * 8 + j], acc);
+            acc = fmaf(wr[k], Ps[ba * 64 + k * 8 + j], acc);
           Tb[(o + 8 + i) * kLdT + o + j] = -acc;
         }
         named_sync(2, kInvThreads);
@@ -571,15 +588,24 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
           const int blk = t >> 5, a = 2 * blk, R = a + 1, rp = (t >> 2) & 7, cq = t & 3;
           float acc[2][4] = {};
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {  // D_a has stored zeros above its diagonal
-            const float4 tv = *reinterpret_cast<const float4*>(Tb + (16 * a + k) * kLdT + 16 * a + 4 * cq);
+          for (int k4 = 0; k4 < 16; k4 += 4) {  // D_a has stored zeros above its diagonal
+            float lv[2][4];
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-              const float l = Lb[(16 * R + 2 * rp + r) * kLdL + 16 * a + k];
-              acc[r][0] = fmaf(l, tv.x, acc[r][0]);
-              acc[r][1] = fmaf(l, tv.y, acc[r][1]);
-              acc[r][2] = fmaf(l, tv.z, acc[r][2]);
-              acc[r][3] = fmaf(l, tv.w, acc[r][3]);
+            for (int r = 0; r < 2; ++r)
+              *reinterpret_cast<float4*>(lv[r]) =
+                  *reinterpret_cast<const float4*>(Lb + (16 * R + 2 * rp + r) * kLdL + 16 * a + k4);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const float4 tv =
+                  *reinterpret_cast<const float4*>(Tb + (16 * a + k4 + kk) * kLdT + 16 * a + 4 * cq);
+#pragma unroll
+              for (int r = 0; r < 2; ++r) {
+                const float l = lv[r][kk];
+                acc[r][0] = fmaf(l, tv.x, acc[r][0]);
+                acc[r][1] = fmaf(l, tv.y, acc[r][1]);
+                acc[r][2] = fmaf(l, tv.z, acc[r][2]);
+                acc[r][3] = fmaf(l, tv.w, acc[r][3]);
+              }
             }
           }
 #pragma unroll
@@ -592,15 +618,24 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
           const int blk = t >> 5, a = 2 * blk, R = a + 1, rp = (t >> 2) & 7, cq = t & 3;
           float acc[2][4] = {};
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {  // D_{a+1} has stored zeros above its diagonal
-            const float4 pv = *reinterpret_cast<const float4*>(Ps + blk * 256 + k * 16 + 4 * cq);
+          for (int k4 = 0; k4 < 16; k4 += 4) {  // D_{a+1} has stored zeros above its diagonal
+            float wv[2][4];
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-              const float w = Tb[(16 * R + 2 * rp + r) * kLdT + 16 * R + k];
-              acc[r][0] = fmaf(w, pv.x, acc[r][0]);
-              acc[r][1] = fmaf(w, pv.y, acc[r][1]);
-              acc[r][2] = fmaf(w, pv.z, acc[r][2]);
-              acc[r][3] = fmaf(w, pv.w, acc[r][3]);
+            for (int r = 0; r < 2; ++r)
+              *reinterpret_cast<float4*>(wv[r]) =
+                  *reinterpret_cast<const float4*>(Tb + (16 * R + 2 * rp + r) * kLdT + 16 * R + k4);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const float4 pv =
+                  *reinterpret_cast<const float4*>(Ps + blk * 256 + (k4 + kk) * 16 + 4 * cq);
+#pragma unroll
+              for (int r = 0; r < 2; ++r) {
+                const float w = wv[r][kk];
+                acc[r][0] = fmaf(w, pv.x, acc[r][0]);
+                acc[r][1] = fmaf(w, pv.y, acc[r][1]);
+                acc[r][2] = fmaf(w, pv.z, acc[r][2]);
+                acc[r][3] = fmaf(w, pv.w, acc[r][3]);
+              }
             }
           }
 #pragma unroll
@@ -616,16 +651,24 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
           const int rp = t >> 3, cq = t & 7, k0 = cq >= 4 ? 16 : 0;
           float acc[2][4] = {};
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            if (k >= k0) {
-              const float4 tv = *reinterpret_cast<const float4*>(Tb + k * kLdT + 4 * cq);
+          for (int k4 = 0; k4 < 32; k4 += 4) {
+            if (k4 >= k0) {
+              float lv[2][4];
 #pragma unroll
-              for (int r = 0; r < 2; ++r) {
-                const float l = Lb[(32 + 2 * rp + r) * kLdL + k];
-                acc[r][0] = fmaf(l, tv.x, acc[r][0]);
-                acc[r][1] = fmaf(l, tv.y, acc[r][1]);
-                acc[r][2] = fmaf(l, tv.z, acc[r][2]);
-                acc[r][3] = fmaf(l, tv.w, acc[r][3]);
+              for (int r = 0; r < 2; ++r)
+                *reinterpret_cast<float4*>(lv[r]) =
+                    *reinterpret_cast<const float4*>(Lb + (32 + 2 * rp + r) * kLdL + k4);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const float4 tv = *reinterpret_cast<const float4*>(Tb + (k4 + kk) * kLdT + 4 * cq);
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                  const float l = lv[r][kk];
+                  acc[r][0] = fmaf(l, tv.x, acc[r][0]);
+                  acc[r][1] = fmaf(l, tv.y, acc[r][1]);
+                  acc[r][2] = fmaf(l, tv.z, acc[r][2]);
+                  acc[r][3] = fmaf(l, tv.w, acc[r][3]);
+                }
               }
             }
           }
@@ -639,16 +682,24 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
           const int rp = t >> 3, cq = t & 7, kn = rp < 8 ? 16 : 32;
           float acc[2][4] = {};
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            if (k < kn) {
-              const float4 mv = *reinterpret_cast<const float4*>(Mb + k * kLdT + 4 * cq);
+          for (int k4 = 0; k4 < 32; k4 += 4) {
+            if (k4 < kn) {
+              float wv[2][4];
 #pragma unroll
-              for (int r = 0; r < 2; ++r) {
-                const float w = Tb[(32 + 2 * rp + r) * kLdT + 32 + k];
-                acc[r][0] = fmaf(w, mv.x, acc[r][0]);
-                acc[r][1] = fmaf(w, mv.y, acc[r][1]);
-                acc[r][2] = fmaf(w, mv.z, acc[r][2]);
-                acc[r][3] = fmaf(w, mv.w, acc[r][3]);
+              for (int r = 0; r < 2; ++r)
+                *reinterpret_cast<float4*>(wv[r]) =
+                    *reinterpret_cast<const float4*>(Tb + (32 + 2 * rp + r) * kLdT + 32 + k4);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const float4 mv = *reinterpret_cast<const float4*>(Mb + (k4 + kk) * kLdT + 4 * cq);
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                  const float w = wv[r][kk];
+                  acc[r][0] = fmaf(w, mv.x, acc[r][0]);
+                  acc[r][1] = fmaf(w, mv.y, acc[r][1]);
+                  acc[r][2] = fmaf(w, mv.z, acc[r][2]);
+                  acc[r][3] = fmaf(w, mv.w, acc[r][3]);
+                }
               }
             }
           }
