@@ -593,7 +593,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
 #pragma unroll
             for (int r = 0; r < 2; ++r)
               *reinterpret_cast<float4*>(lv[r]) =
-                  *reinterpret_cast<const float4*>(Lb + (16 * R + 2 * rp + r) * kLdL + 16 * a + k4);
+                  *reinterpret_cast<const float4*>(Lb + (16 * R + rp + 8 * r) * kLdL + 16 * a + k4);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               const float4 tv =
@@ -610,7 +610,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
           }
 #pragma unroll
           for (int r = 0; r < 2; ++r)
-            *reinterpret_cast<float4*>(Ps + blk * 256 + (2 * rp + r) * 16 + 4 * cq) =
+            *reinterpret_cast<float4*>(Ps + blk * 256 + (rp + 8 * r) * 16 + 4 * cq) =
                 make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
         }
         named_sync(2, kInvThreads);
@@ -623,7 +623,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
 #pragma unroll
             for (int r = 0; r < 2; ++r)
               *reinterpret_cast<float4*>(wv[r]) =
-                  *reinterpret_cast<const float4*>(Tb + (16 * R + 2 * rp + r) * kLdT + 16 * R + k4);
+                  *reinterpret_cast<const float4*>(Tb + (16 * R + rp + 8 * r) * kLdT + 16 * R + k4);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               const float4 pv =
@@ -640,7 +640,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
           }
 #pragma unroll
           for (int r = 0; r < 2; ++r)
-            *reinterpret_cast<float4*>(Tb + (16 * R + 2 * rp + r) * kLdT + 16 * a + 4 * cq) =
+            *reinterpret_cast<float4*>(Tb + (16 * R + rp + 8 * r) * kLdT + 16 * a + 4 * cq) =
                 make_float4(-acc[r][0], -acc[r][1], -acc[r][2], -acc[r][3]);
         }
         named_sync(2, kInvThreads);
@@ -710,8 +710,9 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         }
       }
       if (!named_sync_and(1, kPrepCompute, ok1)) break;
-      {  // T -> bf16 B operand (MN-major, X = row r, K = column j); zero above the diagonal
-        const int j = t >> 3, o8 = t & 7;
+      {  // T -> bf16 B operand (MN-major, X = row r, K = column j); zero above the diagonal.
+         // A warp reads 32 consecutive columns of one row: no bank conflicts.
+        const int j = t & 63, o8 = t >> 6;
         float x[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
