@@ -467,6 +467,24 @@ def run_gpu(args):
             "checkpoints": NT // 512, "checkpoint_bytes": ck.numel() * 4,
             "ms_per_step": ms_ck, "ms_per_step_without": ms_plain}
         del ck
+        # the same prefill with q, k normalised in the kernel and the output
+        # RMSNorm x Sigmoid gate applied before the store (gate logits read in bf16)
+        gz = torch.randn(NT, H, D, device=dev).to(torch.bfloat16)
+        nw = torch.ones(D, device=dev)
+
+        def step_all_fused():
+            kda.chunk_fwd_fused(inp["q"], inp["k"], inp["v"], inp["beta"], inp["h0"],
+                                inp["cu_seqlens"], z=inp["z"], A=inp["A"], qk_l2_eps=1e-6,
+                                out_gate=gz, out_norm_weight=nw, out_norm_eps=1e-6,
+                                workspace=ws, out=o, final_state_out=hT)
+
+        ms_fz = timed(step_all_fused, args.steps, args.warmup)
+        other["prefill_qk_norm_output_gate"] = {
+            "ms_per_step": ms_fz, "ms_per_step_gated_only": ms_step if fused else ms_alt,
+            "extra_bytes_per_token_head": D * 2,
+            "step_floor_ms": (NT * H * (fused_prefill_bytes_per_token_head(2) + D * 2)
+                              + 2 * H * state_bytes()) / (hbm_peak * 1e9) * 1e3}
+        del gz
 
         for wl in (workloads.varlen(), workloads.long_context()):
             inp2 = workloads.make_inputs(wl, dev)

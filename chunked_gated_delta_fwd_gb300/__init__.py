@@ -27,7 +27,8 @@ from . import _build
 
 __all__ = ["KdaError", "gate", "chunk_fwd", "chunk_fwd_gated", "chunk_fwd_workspace_size", "recurrent_step",
            "library_path", "lib", "get_device_error", "profile_enable", "profile_collect", "G_MIN", "F32", "BF16", "FP32_CORES", "SEQUENTIAL",
-           "segment_chunks", "recurrent_multi_step", "chunk_fwd_checkpointed"]
+           "segment_chunks", "recurrent_multi_step", "chunk_fwd_checkpointed",
+           "chunk_fwd_fused"]
 
 G_MIN = -5.0
 F32, BF16 = 0, 1
@@ -69,6 +70,8 @@ def _load() -> ctypes.CDLL:
     L.kda_chunk_fwd_ex.argtypes = L.kda_chunk_fwd.argtypes + [u32]
     L.kda_chunk_fwd_checkpointed.argtypes = (L.kda_chunk_fwd.argtypes[:16] + [vp, i32, i64]
                                              + L.kda_chunk_fwd.argtypes[16:] + [u32])
+    L.kda_chunk_fwd_fused.argtypes = [vp, vp, vp, i32, vp, vp, vp, f32, vp, vp, vp, i32, i32, i64,
+                                      i32, i32, i32, f32, vp, vp, f32, vp, vp, vp, sz, vp, u32]
     L.kda_chunk_fwd_gated.argtypes = [vp, vp, vp, i32, vp, vp, f32, vp, vp, vp, i32, i32, i64,
                                       i32, i32, i32, vp, vp, vp, sz, vp]
     L.kda_recurrent_step.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, vp]
@@ -213,6 +216,40 @@ def chunk_fwd_checkpointed(q, k, v, g, beta, h0=None, cu_seqlens=None, *,
             _ptr(c["hT"]), _ptr(ck) if int(ckpt_capacity) > 0 else None, int(ckpt_tokens),
             int(ckpt_capacity), _ptr(c["ws"]), c["ws"].numel(), _stream(q.device), int(flags)))
     return c["o"], c["hT"], ck
+
+
+def chunk_fwd_fused(q, k, v, beta, h0=None, cu_seqlens=None, *, g=None, z=None, A=None,
+                    g_min: float = -5.0, qk_l2_eps=None, out_gate=None, out_norm_weight=None,
+                    out_norm_eps: float = 1e-6, output_final_state=True, workspace=None,
+                    flags: int = 0, out=None, final_state_out=None):
+    """bf16 prefill with the prologue and epilogue fused: exactly one of ``g`` (fp32
+    log-decays) and ``z`` + ``A`` (gate computed in-kernel); ``qk_l2_eps`` (None: q, k
+    used as given) L2-normalises q and k per token and head; ``out_gate`` [..., H,
+    128] (dtype of q) applies o <- Sigmoid(out_gate) * w * o / rms(o) per head, with
+    ``out_norm_weight`` fp32 [128] (None: ones).  Returns ``(o, hT)``."""
+    if (g is None) == (z is None):
+        raise ValueError("give exactly one of g and z")
+    if g is not None:
+        _need(g, "g", torch.float32, q.device)
+    else:
+        _need(z, "z", q.dtype, q.device)
+        _need(A, "A", torch.float32, q.device)
+    if out_gate is not None:
+        _need(out_gate, "out_gate", q.dtype, q.device)
+        if tuple(out_gate.shape) != tuple(v.shape):
+            raise ValueError(f"out_gate must have the shape of v {tuple(v.shape)}")
+    if out_norm_weight is not None:
+        _need(out_norm_weight, "out_norm_weight", torch.float32, q.device)
+    c = _chunk_setup(q, k, v, beta, h0, cu_seqlens, output_final_state, workspace, flags, out,
+                     final_state_out)
+    with torch.cuda.device(q.device):
+        _check(lib.kda_chunk_fwd_fused(
+            _ptr(q), _ptr(k), _ptr(v), c["dt"], _ptr(g), _ptr(z), _ptr(A), float(g_min),
+            _ptr(beta), _ptr(h0), _ptr(cu_seqlens), c["N"], c["B"], c["T"], c["H"], c["dk"],
+            c["dv"], -1.0 if qk_l2_eps is None else float(qk_l2_eps), _ptr(out_gate),
+            _ptr(out_norm_weight), float(out_norm_eps), _ptr(c["o"]), _ptr(c["hT"]),
+            _ptr(c["ws"]), c["ws"].numel(), _stream(q.device), int(flags)))
+    return c["o"], c["hT"]
 
 
 def chunk_fwd_gated(q, k, v, z, A, beta, h0=None, cu_seqlens=None, *, g_min: float = -5.0,

@@ -4,6 +4,7 @@
 // All checks happen on the host before anything is enqueued, so a call that
 // returns an error has launched nothing.  Nothing here synchronizes except
 // kda_get_device_error().
+#include <cmath>
 #include <cuda_runtime.h>
 #include <stdarg.h>
 #include <stdint.h>
@@ -372,7 +373,8 @@ kda_status_t chunk_fwd_impl(const char* fn, const void* q, const void* k, const 
                             const int32_t* cu_seqlens, int n_seqs, int B, int64_t T, int H,
                             int dk, int dv, void* o, float* hT, void* workspace,
                             size_t ws_bytes, kda_stream_t stream, unsigned flags,
-                            kda::CkptArgs ck = kda::CkptArgs{nullptr, 0, 0}) {
+                            kda::CkptArgs ck = kda::CkptArgs{nullptr, 0, 0},
+                            kda::FuseArgs fz = kda::FuseArgs{-1.f, nullptr, nullptr, 0.f}) {
   if (dtype != KDA_F32 && dtype != KDA_BF16)
     return fail(KDA_ERR_UNSUPPORTED_DTYPE, "%s: dtype %d", fn, dtype);
   if (dk != kda::kD || dv != kda::kD)
@@ -417,7 +419,7 @@ kda_status_t chunk_fwd_impl(const char* fn, const void* q, const void* k, const 
     e = kda::launch_chunk_tc(q, k, v, g, z, A, g_min, beta, h0, o, hT, NT, N, H,
                              kda::chain_segment_chunks(NT, N, H, (int)(flags >> 16),
                                                        (flags & KDA_CHUNK_SEQUENTIAL) != 0),
-                             ck, workspace, err, s);
+                             ck, fz, workspace, err, s);
   else
     e = kda::launch_chunk_simt(q, k, v, dtype == KDA_BF16, g, beta, h0, o, hT, NT, N, H,
                                workspace, s);
@@ -476,6 +478,37 @@ kda_status_t kda_chunk_fwd_checkpointed(const void* q, const void* k, const void
                         n_seqs, B, T, H, dk, dv, o, hT, workspace, ws_bytes, stream, flags,
                         kda::CkptArgs{ckpt_capacity > 0 ? ckpt : nullptr,
                                       ckpt_tokens / kda::kChunk, ckpt_capacity});
+}
+
+kda_status_t kda_chunk_fwd_fused(const void* q, const void* k, const void* v, int dtype,
+                                 const float* g, const void* z, const float* A, float g_min,
+                                 const void* beta, const float* h0, const int32_t* cu_seqlens,
+                                 int n_seqs, int B, int64_t T, int H, int dk, int dv,
+                                 float qk_l2_eps, const void* out_gate,
+                                 const float* out_norm_weight, float out_norm_eps, void* o,
+                                 float* hT, void* workspace, size_t ws_bytes, kda_stream_t stream,
+                                 unsigned flags) {
+  const char* fn = "kda_chunk_fwd_fused";
+  if (dtype != KDA_BF16 || (flags & KDA_CHUNK_FP32_CORES))
+    return fail(KDA_ERR_UNSUPPORTED_DTYPE, "%s: bf16 on the tensor-core path only", fn);
+  if ((g != nullptr) == (z != nullptr))
+    return fail(KDA_ERR_INVALID_ARG, "%s: give exactly one of g and z", fn);
+  if (z && !(g_min >= -5.f && g_min < 0.f))
+    return fail(KDA_ERR_INVALID_ARG, "%s: g_min=%g outside [-5, 0)", fn, (double)g_min);
+  if (!(qk_l2_eps < 0.f || std::isfinite(qk_l2_eps)))
+    return fail(KDA_ERR_INVALID_ARG, "%s: qk_l2_eps is not finite", fn);
+  if (out_gate && !(out_norm_eps >= 0.f && std::isfinite(out_norm_eps)))
+    return fail(KDA_ERR_INVALID_ARG, "%s: out_norm_eps=%g (need finite, >= 0)", fn,
+                (double)out_norm_eps);
+  if ((out_gate && !aligned16(out_gate)) || (out_norm_weight && !aligned16(out_norm_weight)))
+    return fail(KDA_ERR_MISALIGNED, "%s: out_gate, out_norm_weight must be 16-byte aligned", fn);
+  if (out_norm_weight && !out_gate)
+    return fail(KDA_ERR_INVALID_ARG, "%s: out_norm_weight without out_gate", fn);
+  return chunk_fwd_impl(fn, q, k, v, dtype, g, z, A, g_min, beta, h0, cu_seqlens, n_seqs, B, T, H,
+                        dk, dv, o, hT, workspace, ws_bytes, stream, flags,
+                        kda::CkptArgs{nullptr, 0, 0},
+                        kda::FuseArgs{qk_l2_eps < 0.f ? -1.f : qk_l2_eps, out_gate,
+                                      out_norm_weight, out_norm_eps});
 }
 
 kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v, int dtype,

@@ -91,6 +91,8 @@ constexpr uint32_t kP_BKg = 163840;        // K-major (beta Gamma K)^T 128 x 64
 constexpr uint32_t kP_BV = 180224;         // K-major (beta V)^T 128 x 64
 constexpr uint32_t kP_beta = 196608;       // 64 fp32
 constexpr uint32_t kP_Tot = kP_beta + 256; // per-tile sums of g, [4][128] fp32
+constexpr uint32_t kP_Rq = kP_Tot + 2048;  // 1 / |q_r|, 1 / |k_r| (fp32 [64] each) when
+constexpr uint32_t kP_Rk = kP_Rq + 256;    //   q and k are normalised in the kernel
 constexpr uint32_t kP_bars = kP_Tot + 4096;  // k/q/v full, g full, p, w + TMEM base
 // With the gate fused (z staged in bf16) the upper half of the g staging space and
 // one more 16 KB block hold the unit's Gamma*Q and Kt^T tiles on their way out.
@@ -147,7 +149,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
             const __nv_bfloat16* __restrict__ beta, const float* __restrict__ A, float g_min,
             Plan plan, int H, int64_t units_ub, uint8_t* __restrict__ tiles,
-            float* __restrict__ gam_out, int* err) {
+            float* __restrict__ gam_out, float qk_eps, int* err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_addr(sm);
@@ -275,8 +277,33 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
   // the running log-decay over each 16-token tile, in base-2 units (G log2 e) so
   // that every decay below is one ex2.  Thread -> channel pair (cp, cp + 1) of
   // tile ta; it writes G_r - R_a for its 16 rows and the tile total.
+  const bool qk_norm = qk_eps >= 0.f;  // q, k L2-normalised per token and head here
   auto pass1 = [&](const UnitInfo& un, uint32_t parity) -> bool {
     if (un.chunk >= total) return true;
+    if (qk_norm) {
+      // 1 / sqrt(|x_r|^2 + eps) of q and k rows: four threads per row (q, k halves);
+      // each reads 64 channels as 16-byte pieces in a row-rotated order (no bank
+      // conflicts) and the halves meet by one shuffle, which every lane reaches
+      // (an expired wait is acted on after it).
+      const bool okq = mbar_wait(bar_kqv, parity, err);
+      const int t8 = t - kInvThreads, row = t8 >> 2, part = t8 & 3;
+      const uint8_t* base = sm + (part < 2 ? kI_Q : kI_K) + row * 256 + (part & 1) * 128;
+      float ss = 0.f;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 w4 = *reinterpret_cast<const uint4*>(base + ((c + row) & 7) * 16);
+        const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float lo = bf16_lo(ww[i]), hi = bf16_hi(ww[i]);
+          ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+        }
+      }
+      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+      if (!okq) return false;
+      if ((part & 1) == 0)
+        reinterpret_cast<float*>(sm + (part < 2 ? kP_Rq : kP_Rk))[row] = rsqrtf(ss + qk_eps);
+    }
     if (!mbar_wait(bar_g, parity, err)) return false;
     const int t8 = t - kInvThreads, cp = 2 * (t8 & 63), ta = t8 >> 6;
     const uint8_t* zg = sm + kI_G;
@@ -381,6 +408,12 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         kw[e] = in ? *reinterpret_cast<const uint32_t*>(sK + r * D + cp) : 0u;
         qw[e] = in ? *reinterpret_cast<const uint32_t*>(sQ + r * D + cp) : 0u;
         vw[e] = in ? *reinterpret_cast<const uint32_t*>(sV + r * D + cp) : 0u;
+        if (qk_norm) {  // normalised rows, rounded to bf16 like normalised inputs
+          const float rk = reinterpret_cast<const float*>(sm + kP_Rk)[r];
+          const float rq = reinterpret_cast<const float*>(sm + kP_Rq)[r];
+          kw[e] = pack_bf16(bf16_lo(kw[e]) * rk, bf16_hi(kw[e]) * rk);
+          qw[e] = pack_bf16(bf16_lo(qw[e]) * rq, bf16_hi(qw[e]) * rq);
+        }
         bt[e] = beta_s[r];
         const float2 gv =
             *reinterpret_cast<const float2*>(sm + gs_block<kZ>(r >> 5) + (r & 31) * 512 + cp * 4);
@@ -791,7 +824,9 @@ constexpr uint32_t kC_bars = kStages * kStageBytes;
 // operands of MMA1 (S^T, packed pairs, [384,448)) and MMA2 (Vt^T, two buffers of 32
 // columns at [448,512)).
 constexpr uint32_t kT_SB = 384, kT_VT = 448;
-constexpr uint32_t kC_Smem = kC_bars + 256 + 1024;
+// output gate scratch: per-warp partial sums of o^2 (fp32 [4][64]) and 1/rms ([64])
+constexpr uint32_t kC_red = kC_bars + 256, kC_rs = kC_red + 1024;
+constexpr uint32_t kC_Smem = kC_rs + 256 + 1024;
 constexpr int kEpi = 256;    // epilogue warps 0-7: (TMEM lane, column half)
 constexpr int kStore = 128;  // store warps 8-11: TMEM lane = value row, all 64 tokens
 constexpr int kCopyWarp = (kEpi + kStore) / 32;  // warp 12: tile copies
@@ -825,6 +860,13 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int
 //   scan:  S_in(1) = S_end(0), S_in(k+1) = S~(k) + M(k) S_in(k)  (seg_scan_kernel);
 //   mode 2: segments k >= 1 run from S_in(k) with outputs; the last writes hT.
 // mode 0 is the plain chain, one CTA per (sequence, head).  States are S^T.
+// Output gate of the chunk outputs (gz null: plain o).
+struct OutGate {
+  const __nv_bfloat16* gz;  // gate logits [NT][H][dv]
+  const float* w;           // RMSNorm weight [dv] (null: ones)
+  float eps;
+};
+
 struct SegArgs {
   int mode;
   const int4* tab;  // per segment: (sequence, first chunk, chunks, k | P << 16); x < 0: unused
@@ -837,7 +879,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     tc_chain(const uint8_t* __restrict__ tiles, const float* __restrict__ gam,
              const float* __restrict__ h0, Plan plan, int H, __nv_bfloat16* __restrict__ o,
              float* __restrict__ hT, SegArgs sg, CkptArgs ck, const int* __restrict__ ck_off,
-             int* err) {
+             OutGate og, int* err) {
   // ---- this CTA's job: chunk range, initial and final state, outputs or not
   const int h = blockIdx.y;
   int n, c0, nch;
@@ -1136,11 +1178,15 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     // Thread = value row dv; it reads the 64 outputs of its row from the chunk's D1
     // buffer and writes them (2-byte stores, 64 contiguous bytes per warp), then
     // frees the buffer for MMA1 two chunks later.
+    // With the output gate the store warps meet at barrier 2 every chunk; an
+    // expired wait then stops all of them at the same point (bar.red.and).
     const int dv = t - kEpi;
     const uint32_t lrow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    const bool gate_on = og.gz != nullptr && write_o;
     for (int j = 0; j < nch; ++j) {
       const int b = j & 1;
-      if (!wait_or_abort(bar_o0 + 8 * b, (j >> 1) & 1, err, abort_flag)) break;
+      const bool okw = wait_or_abort(bar_o0 + 8 * b, (j >> 1) & 1, err, abort_flag);
+      if (gate_on ? !named_sync_and(2, kStore, okw) : !okw) break;
       tc_fence_after();
       float ov[2][32];
       const uint32_t d1 = lrow + 128 + 128 * b + 64;
@@ -1151,9 +1197,63 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       mbar_arrive(bar_f0 + 8 * b);
       const int64_t tc = tstart + (int64_t)j * C;
       __nv_bfloat16* orow = o + (tc * H + h) * D + dv;
+      if (gate_on) {
+        // Output gate: y = Sigmoid(gz) * w * o / sqrt(mean_dv(o^2) + eps) per token.
+        // Sums of o^2 over this warp's 32 rows by a halving reduce-scatter: after
+        // the exchanges over lane bits 4..0 lane l holds tokens 2l and 2l + 1.
+        float a[32];
+        {
+          const bool up = (dv & 16) != 0;
 #pragma unroll
-      for (int r = 0; r < C; ++r)
-        if (write_o && tc + r < tend) orow[(int64_t)r * H * D] = __float2bfloat16_rn(ov[r >> 5][r & 31]);
+          for (int i = 0; i < 32; ++i) {
+            const float lo = ov[0][i] * ov[0][i], hi = ov[1][i] * ov[1][i];
+            a[i] = (up ? hi : lo) + __shfl_xor_sync(0xffffffffu, up ? lo : hi, 16);
+          }
+        }
+#pragma unroll
+        for (int m = 8, n = 16; m >= 1; m >>= 1, n >>= 1) {
+          const bool up = (dv & m) != 0;
+#pragma unroll
+          for (int i = 0; i < n; ++i)
+            a[i] = (up ? a[n + i] : a[i]) + __shfl_xor_sync(0xffffffffu, up ? a[i] : a[n + i], m);
+        }
+        float* red = reinterpret_cast<float*>(sm + kC_red);
+        float* rs = reinterpret_cast<float*>(sm + kC_rs);
+        *reinterpret_cast<float2*>(red + (warp & 3) * 64 + 2 * (dv & 31)) = make_float2(a[0], a[1]);
+        named_sync(2, kStore);
+        if (dv < C)
+          rs[dv] = rsqrtf((red[dv] + red[64 + dv] + red[128 + dv] + red[192 + dv]) * (1.f / D) +
+                          og.eps);
+        named_sync(2, kStore);
+        const float wv = og.w ? __ldg(og.w + dv) : 1.f;
+        const __nv_bfloat16* grow = og.gz + (tc * H + h) * D + dv;
+#pragma unroll
+        for (int r0 = 0; r0 < C; r0 += 4) {
+          // Sigmoid(x) = 1 / (1 + 2^(-x log2 e)); four quotients share one reciprocal
+          // (exponent clamped at 30: a gate below 2^-30 moves by less than 2^-30)
+          float d[4], y[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float x = tc + r0 + i < tend ? __bfloat162float(grow[(int64_t)(r0 + i) * H * D]) : 0.f;
+            d[i] = 1.f + exp2_approx(fminf(-x * kLog2e, 30.f));
+          }
+          const float d01 = d[0] * d[1], d23 = d[2] * d[3];
+          const float rall = rcp_approx(d01 * d23);
+          const float q01 = d23 * rall, q23 = d01 * rall;
+          const float sg[4] = {d[1] * q01, d[0] * q01, d[3] * q23, d[2] * q23};
+          const float4 r4 = *reinterpret_cast<const float4*>(rs + r0);
+          const float rv[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) y[i] = ov[(r0 + i) >> 5][(r0 + i) & 31] * rv[i] * wv * sg[i];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (tc + r0 + i < tend) orow[(int64_t)(r0 + i) * H * D] = __float2bfloat16_rn(y[i]);
+        }
+      } else {
+#pragma unroll
+        for (int r = 0; r < C; ++r)
+          if (write_o && tc + r < tend) orow[(int64_t)r * H * D] = __float2bfloat16_rn(ov[r >> 5][r & 31]);
+      }
     }
   }
   tc_fence_before();
@@ -1436,8 +1536,9 @@ size_t tc_workspace_bytes(int64_t n_tokens, int n_seqs, int H, int seg_chunks) {
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const float* g,
                             const void* z, const float* A, float g_min, const void* beta,
                             const float* h0, void* o, float* hT, int64_t n_tokens, int n_seqs,
-                            int H, int seg_chunks, CkptArgs ck, void* ws, int* err,
-                            cudaStream_t s) {
+                            int H, int seg_chunks, CkptArgs ck, FuseArgs fz, void* ws,
+                            int* err, cudaStream_t s) {
+  const OutGate og{static_cast<const __nv_bfloat16*>(fz.gz), fz.w, fz.eps};
   const Plan plan = plan_in(ws, n_tokens, n_seqs);
   const int64_t units = chunks_upper_bound(n_tokens, n_seqs) * H;
   const TcLayout lay = tc_layout(ws, n_tokens, n_seqs, H, seg_chunks);
@@ -1463,7 +1564,7 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
     ProfScope prof_scope(fused ? "kda_tc_prep_gated" : "kda_tc_prep", s);
     kern<<<grid, kPrepThreads, kP_Smem, s>>>(tm[0], tm[1], tm[2], tm[3],
                                              static_cast<const T*>(beta), A, g_min, plan, H,
-                                             units, tiles, gam, err);
+                                             units, tiles, gam, fz.qk_eps, err);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -1480,7 +1581,7 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
     ProfScope prof_scope("kda_tc_chain", s);
     tc_chain<<<cgrid, kChainThreads, kC_Smem, s>>>(tiles, gam, h0, plan, H, static_cast<T*>(o),
                                                     hT, SegArgs{0, nullptr, nullptr, nullptr, nullptr},
-                                                    ck, lay.ck_off, err);
+                                                    ck, lay.ck_off, og, err);
     return cudaGetLastError();
   }
   // sequence-segment parallel chain: segments, end states and transitions, scan, rerun
@@ -1494,7 +1595,7 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
   {
     ProfScope prof_scope("kda_tc_chain_seg", s);
     tc_chain<<<dim3((unsigned)lay.segs_ub, (unsigned)H, 2), kChainThreads, kC_Smem, s>>>(
-        tiles, gam, h0, plan, H, static_cast<T*>(o), hT, sg, ck, lay.ck_off, err);
+        tiles, gam, h0, plan, H, static_cast<T*>(o), hT, sg, ck, lay.ck_off, og, err);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -1511,7 +1612,7 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
   sg.mode = 2;
   ProfScope prof_scope("kda_tc_chain_seg", s);
   tc_chain<<<dim3((unsigned)lay.segs_ub, (unsigned)H, 1), kChainThreads, kC_Smem, s>>>(
-      tiles, gam, h0, plan, H, static_cast<T*>(o), hT, sg, ck, lay.ck_off, err);
+      tiles, gam, h0, plan, H, static_cast<T*>(o), hT, sg, ck, lay.ck_off, og, err);
   return cudaGetLastError();
 }
 

@@ -125,10 +125,19 @@ struct CkptArgs {
   int every;
   int64_t cap;
 };
+// Fused prologue / epilogue of the tensor-core chunk path: q, k L2-normalised in the
+// prepare kernel (qk_eps < 0: off) and the output RMSNorm x Sigmoid gate in the chain
+// (gz null: off; w null: unit weight).
+struct FuseArgs {
+  float qk_eps;
+  const void* gz;
+  const float* w;
+  float eps;
+};
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const float* g,
                             const void* z, const float* A, float g_min, const void* beta,
                             const float* h0, void* o, float* hT, int64_t n_tokens, int n_seqs,
-                            int H, int seg_chunks, CkptArgs ck, void* ws, int* err_flag,
-                            cudaStream_t s);
+                            int H, int seg_chunks, CkptArgs ck, FuseArgs fz, void* ws,
+                            int* err_flag, cudaStream_t s);
 
 }  // namespace kda

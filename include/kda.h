@@ -160,6 +160,45 @@ kda_status_t kda_chunk_fwd_ex(const void* q, const void* k, const void* v, int d
                               size_t ws_bytes, kda_stream_t stream, unsigned flags);
 
 /*
+ * kda_chunk_fwd_fused -- the bf16 tensor-core prefill with its prologue and
+ * epilogue fused: the gate from z (as kda_chunk_fwd_gated), q and k
+ * L2-normalised per token and head inside the prepare kernel (the FlashKDA
+ * prepare kernel normalises before the gate prefix sums: "Kimi K3 notes",
+ * section "FlashKDA", kernel K1), and the head-wise RMSNorm x Sigmoid output gate
+ * ("Kimi K3 technical report review", section 3.3, Eq. 6; "Kimi K3:
+ * architecture, training and inference systems", section 3.3) applied to the
+ * fp32 outputs before they are rounded and stored.
+ *   g or z, A, g_min  exactly one of g (as kda_chunk_fwd) and z (as
+ *              kda_chunk_fwd_gated; A and g_min then as there).
+ *   qk_l2_eps  >= 0: q_t <- q_t / sqrt(|q_t|^2 + qk_l2_eps), the same for k, per
+ *              token and head, before anything else uses them (the normalised
+ *              rows are rounded to bf16, as normalised inputs would be);
+ *              < 0: q and k are used as given (expected normalised).
+ *   out_gate   optional [NT][H][dv] of `dtype`, 16-byte aligned: gate logits x.
+ *              When given, o_t = Sigmoid(x_t) * w * o~_t / sqrt(mean(o~_t^2) +
+ *              out_norm_eps) with the mean over the dv channels of one head and
+ *              o~ the KDA output; NULL: o = o~.
+ *   out_norm_weight  optional fp32 [dv] RMSNorm weight w shared by the heads
+ *              (NULL: ones); only with out_gate.
+ *   out_norm_eps  finite, >= 0 (used only with out_gate).
+ * flags: KDA_CHUNK_SEQUENTIAL and KDA_CHUNK_SEGMENT_CHUNKS(n) as for
+ * kda_chunk_fwd_ex; the workspace is kda_chunk_fwd_workspace_size_ex(NT, N, H,
+ * KDA_BF16, flags).  Every other argument and result as kda_chunk_fwd.
+ * Errors: dtype other than KDA_BF16 or KDA_CHUNK_FP32_CORES ->
+ * KDA_ERR_UNSUPPORTED_DTYPE; both or neither of g and z, g_min outside [-5, 0),
+ * a non-finite epsilon or out_norm_weight without out_gate -> KDA_ERR_INVALID_ARG;
+ * otherwise as kda_chunk_fwd_ex.
+ */
+kda_status_t kda_chunk_fwd_fused(const void* q, const void* k, const void* v, int dtype,
+                                 const float* g, const void* z, const float* A, float g_min,
+                                 const void* beta, const float* h0, const int32_t* cu_seqlens,
+                                 int n_seqs, int B, int64_t T, int H, int dk, int dv,
+                                 float qk_l2_eps, const void* out_gate,
+                                 const float* out_norm_weight, float out_norm_eps, void* o,
+                                 float* hT, void* workspace, size_t ws_bytes, kda_stream_t stream,
+                                 unsigned flags);
+
+/*
  * kda_chunk_fwd_checkpointed -- kda_chunk_fwd_ex that also writes the state at
  * fixed token boundaries of every sequence, the KDA state checkpoints a prefix
  * cache keeps at hash endpoints (e.g. every 512 tokens; "Kimi K3: architecture,

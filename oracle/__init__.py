@@ -22,6 +22,13 @@ Functions and the passages they follow:
   cumulative decays in fp64 and a library linear solve; tiny sizes only.
 * :func:`decode_step` -- one token of the recurrence for many independent
   (sequence, head) states, the decode form.
+* :func:`l2_normalize` -- ``x / sqrt(|x|^2 + eps)`` per token and head, the
+  L2Norm applied to q and k before the recurrence ("Kimi K3: architecture,
+  training and inference systems", section 3.2, the q / k branches; done inside
+  the FlashKDA prepare kernel, "Kimi K3 notes", section "FlashKDA", K1).
+* :func:`output_gate` -- the head-wise RMSNorm of the KDA output times the
+  full-rank Sigmoid gate ("Kimi K3 technical report review", section 3.3, Eq. 6;
+  the same systems page, section 3.3), without the W_o / W_g projections.
 
 Pins: ``tests/test_oracle.py`` checks these against closed forms, special
 cases and invariants the pages fix (see that file's docstring).
@@ -237,3 +244,23 @@ def chunk_cumsum(g, cu_seqlens=None, C: int = 64) -> np.ndarray:
             e = min(s + C, cu[n + 1])
             out[s:e] = np.cumsum(g[s:e], axis=0)
     return out
+
+
+def l2_normalize(x, eps: float) -> np.ndarray:
+    """``x / sqrt(sum_c x_c^2 + eps)`` over the last axis (one head's channels) in
+    fp64.  The pages name the L2Norm without an epsilon; ``eps`` is the caller's."""
+    x = _f64(x)
+    return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps)
+
+
+def output_gate(o, x, w=None, eps: float = 1e-6) -> np.ndarray:
+    """``Sigmoid(x) * w * o / sqrt(mean_c(o_c^2) + eps)`` over the last axis (the dv
+    channels of one head) in fp64: the head-wise RMSNorm of the recurrent output
+    and the input-dependent full-rank gate, ``x`` being the gate logits W_g x_t.
+    ``w`` is the RMSNorm weight over the channels (None: ones)."""
+    o, x = _f64(o), _f64(x)
+    rms = np.sqrt(np.mean(o * o, axis=-1, keepdims=True) + eps)
+    y = o / rms / (1.0 + np.exp(-x))
+    if w is not None:
+        y = y * _f64(w)
+    return y

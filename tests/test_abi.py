@@ -117,6 +117,32 @@ def test_chunk_checkpointed_rejects_bad_arguments(L):
     assert b"kda_chunk_fwd_checkpointed" in L.kda_last_error_string()
 
 
+def _fused(L, dtype=1, g=None, z=0x10000, g_min=-5.0, qk=-1.0, gate=None, w=None, eps=1e-6,
+           flags=0):
+    vp, i32, i64, f32, sz, u32 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                                  ctypes.c_size_t, ctypes.c_uint)
+    L.kda_chunk_fwd_fused.argtypes = [vp, vp, vp, i32, vp, vp, vp, f32, vp, vp, vp, i32, i32, i64,
+                                      i32, i32, i32, f32, vp, vp, f32, vp, vp, vp, sz, vp, u32]
+    return L.kda_chunk_fwd_fused(FAKE, FAKE, FAKE, dtype, g, z, FAKE, g_min, FAKE, None, None, 0,
+                                 1, 64, 2, 128, 128, qk, gate, w, eps, FAKE, FAKE, FAKE, 1 << 40,
+                                 None, flags)
+
+
+def test_chunk_fused_rejects_bad_arguments(L):
+    assert _fused(L, dtype=0) == 3                 # tensor-core (bf16) path only
+    assert _fused(L, flags=1) == 3
+    assert _fused(L, g=FAKE) == 1                  # both g and z
+    assert _fused(L, z=None) == 1                  # neither
+    assert _fused(L, g_min=-6.0) == 1
+    assert _fused(L, qk=float("inf")) == 1
+    assert _fused(L, gate=FAKE, eps=-1.0) == 1
+    assert _fused(L, gate=FAKE, eps=float("nan")) == 1
+    assert _fused(L, w=FAKE) == 1                  # a weight without the gate
+    assert _fused(L, gate=FAKE + 8) == 4
+    assert _fused(L, flags=8) == 1
+    assert b"kda_chunk_fwd_fused" in L.kda_last_error_string()
+
+
 def test_workspace_size(L):
     L.kda_chunk_fwd_workspace_size_ex.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                                   ctypes.c_int, ctypes.c_uint]
