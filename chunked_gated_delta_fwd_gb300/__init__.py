@@ -28,12 +28,14 @@ from . import _build
 __all__ = ["KdaError", "gate", "chunk_fwd", "chunk_fwd_gated", "chunk_fwd_workspace_size", "recurrent_step",
            "library_path", "lib", "get_device_error", "profile_enable", "profile_collect", "G_MIN", "F32", "BF16", "FP32_CORES", "SEQUENTIAL",
            "segment_chunks", "recurrent_multi_step", "chunk_fwd_checkpointed",
-           "chunk_fwd_fused"]
+           "chunk_fwd_fused", "gate_softplus", "UNBOUNDED_GATE",
+           "output_gate"]
 
 G_MIN = -5.0
 F32, BF16 = 0, 1
 FP32_CORES = 1  # flag of chunk_fwd: evaluate bf16 inputs on fp32 CUDA cores
 SEQUENTIAL = 2  # flag of chunk_fwd: never split a sequence's chain into segments
+UNBOUNDED_GATE = 4  # flag of chunk_fwd: any g <= 0 (range-robust fp32-core evaluation)
 
 _STATUS = {
     0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED_SHAPE",
@@ -61,6 +63,8 @@ def _load() -> ctypes.CDLL:
     vp, i32, i64, f32, sz, u32 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
                                   ctypes.c_size_t, ctypes.c_uint)
     L.kda_gate.argtypes = [vp, i32, vp, f32, vp, i64, i32, i32, vp, vp, i32, vp]
+    L.kda_gate_softplus.argtypes = [vp, i32, vp, vp, i64, i32, i32, vp]
+    L.kda_output_gate.argtypes = [vp, i32, vp, vp, f32, vp, i64, i32, i32, vp]
     L.kda_chunk_fwd_workspace_size.argtypes = [i64, i32, i32, i32]
     L.kda_chunk_fwd_workspace_size.restype = sz
     L.kda_chunk_fwd_workspace_size_ex.argtypes = [i64, i32, i32, i32, u32]
@@ -147,6 +151,42 @@ def gate(z: torch.Tensor, A: torch.Tensor, g_min: float = G_MIN, *, out=None,
         _check(lib.kda_gate(_ptr(z), _dtype_code(z), _ptr(A), float(g_min), _ptr(g), NT, H, dk,
                             _ptr(gcum), _ptr(cu_seqlens), n_seqs, _stream(z.device)))
     return (g, gcum) if with_cumsum else g
+
+
+def output_gate(o: torch.Tensor, gate: torch.Tensor, weight=None, eps: float = 1e-6, *,
+                out=None):
+    """y = Sigmoid(gate) * weight * o / sqrt(mean(o^2) + eps) over the 128 channels of
+    each (token, head); o, gate [..., H, 128] (bf16/fp32, same dtype), weight fp32
+    [128] or None.  ``out=o`` works in place."""
+    _need(o, "o")
+    _need(gate, "gate", o.dtype, o.device)
+    if tuple(gate.shape) != tuple(o.shape):
+        raise ValueError("gate must have the shape of o")
+    if weight is not None:
+        _need(weight, "weight", torch.float32, o.device)
+    H, dv = o.shape[-2], o.shape[-1]
+    NT = o.numel() // (H * dv) if o.numel() else 0
+    y = out if out is not None else torch.empty_like(o)
+    _need(y, "out", o.dtype, o.device)
+    with torch.cuda.device(o.device):
+        _check(lib.kda_output_gate(_ptr(o), _dtype_code(o), _ptr(gate), _ptr(weight), float(eps),
+                                   _ptr(y), NT, H, dv, _stream(o.device)))
+    return y
+
+
+def gate_softplus(z: torch.Tensor, A: torch.Tensor, *, out=None):
+    """The unbounded gate g = -exp(A[h]) * Softplus(z), z [..., H, 128] (bf16/fp32);
+    a prefill on it needs the ``UNBOUNDED_GATE`` flag.  Returns g (fp32)."""
+    _need(z, "z")
+    _need(A, "A", torch.float32, z.device)
+    H, dk = z.shape[-2], z.shape[-1]
+    NT = z.numel() // (H * dk) if z.numel() else 0
+    g = out if out is not None else torch.empty(z.shape, dtype=torch.float32, device=z.device)
+    _need(g, "out", torch.float32, z.device)
+    with torch.cuda.device(z.device):
+        _check(lib.kda_gate_softplus(_ptr(z), _dtype_code(z), _ptr(A), _ptr(g), NT, H, dk,
+                                     _stream(z.device)))
+    return g
 
 
 def chunk_fwd_workspace_size(n_tokens: int, n_seqs: int, H: int, dtype=torch.bfloat16,

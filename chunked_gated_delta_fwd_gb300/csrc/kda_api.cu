@@ -344,10 +344,54 @@ kda_status_t kda_gate(const void* z, int z_dtype, const float* A, float g_min, f
   return KDA_OK;
 }
 
+kda_status_t kda_gate_softplus(const void* z, int z_dtype, const float* A, float* g,
+                               int64_t n_tokens, int H, int dk, kda_stream_t stream) {
+  if (z_dtype != KDA_F32 && z_dtype != KDA_BF16)
+    return fail(KDA_ERR_UNSUPPORTED_DTYPE, "kda_gate_softplus: z_dtype %d", z_dtype);
+  if (dk != kda::kD) return fail(KDA_ERR_UNSUPPORTED_SHAPE, "kda_gate_softplus: dk=%d", dk);
+  if (H < 1) return fail(KDA_ERR_UNSUPPORTED_SHAPE, "kda_gate_softplus: H=%d", H);
+  if (n_tokens < 0 || n_tokens > INT32_MAX)
+    return fail(KDA_ERR_INVALID_ARG, "kda_gate_softplus: n_tokens=%lld", (long long)n_tokens);
+  if (n_tokens == 0) return KDA_OK;
+  if (!z || !A || !g) return fail(KDA_ERR_INVALID_ARG, "kda_gate_softplus: null z, A or g");
+  if (!aligned16(z) || !aligned16(g))
+    return fail(KDA_ERR_MISALIGNED, "kda_gate_softplus: z, g must be 16-byte aligned");
+  kda_status_t st = check_device();
+  if (st != KDA_OK) return st;
+  cudaError_t e = kda::launch_gate_softplus(z, z_dtype == KDA_BF16, A, g, n_tokens, H,
+                                            reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kda_gate_softplus launch");
+  return KDA_OK;
+}
+
+kda_status_t kda_output_gate(const void* o, int dtype, const void* gate, const float* weight,
+                             float eps, void* y, int64_t n_tokens, int H, int dv,
+                             kda_stream_t stream) {
+  const char* fn = "kda_output_gate";
+  if (dtype != KDA_F32 && dtype != KDA_BF16)
+    return fail(KDA_ERR_UNSUPPORTED_DTYPE, "%s: dtype %d", fn, dtype);
+  if (dv != kda::kD) return fail(KDA_ERR_UNSUPPORTED_SHAPE, "%s: dv=%d (need 128)", fn, dv);
+  if (H < 1) return fail(KDA_ERR_UNSUPPORTED_SHAPE, "%s: H=%d", fn, H);
+  if (n_tokens < 0 || n_tokens > INT32_MAX)
+    return fail(KDA_ERR_INVALID_ARG, "%s: n_tokens=%lld", fn, (long long)n_tokens);
+  if (!(eps >= 0.f && std::isfinite(eps)))
+    return fail(KDA_ERR_INVALID_ARG, "%s: eps=%g (need finite, >= 0)", fn, (double)eps);
+  if (n_tokens == 0) return KDA_OK;
+  if (!o || !gate || !y) return fail(KDA_ERR_INVALID_ARG, "%s: null o, gate or y", fn);
+  if (!aligned16(o) || !aligned16(gate) || !aligned16(y) || (weight && !aligned16(weight)))
+    return fail(KDA_ERR_MISALIGNED, "%s: pointers must be 16-byte aligned", fn);
+  kda_status_t st = check_device();
+  if (st != KDA_OK) return st;
+  cudaError_t e = kda::launch_output_gate(o, dtype == KDA_BF16, gate, weight, eps, y, n_tokens,
+                                          H, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kda_output_gate launch");
+  return KDA_OK;
+}
+
 size_t kda_chunk_fwd_workspace_size_ex(int64_t n_tokens, int n_seqs, int H, int dtype,
                                        unsigned flags) {
   if (n_tokens < 0 || n_seqs < 1 || H < 1) return 0;
-  if (dtype == KDA_BF16 && !(flags & KDA_CHUNK_FP32_CORES)) {
+  if (dtype == KDA_BF16 && !(flags & (KDA_CHUNK_FP32_CORES | KDA_CHUNK_UNBOUNDED_GATE))) {
     const int segc = kda::chain_segment_chunks(n_tokens, n_seqs, H, (int)(flags >> 16),
                                                (flags & KDA_CHUNK_SEQUENTIAL) != 0);
     return kda::plan_bytes(n_tokens, n_seqs) + kda::tc_workspace_bytes(n_tokens, n_seqs, H, segc);
@@ -407,22 +451,28 @@ kda_status_t chunk_fwd_impl(const char* fn, const void* q, const void* k, const 
   if (ws_bytes < need)
     return fail(KDA_ERR_WORKSPACE_TOO_SMALL, "%s: workspace %zu < %zu bytes", fn,
                 ws_bytes, need);
-  if (flags & ~(unsigned)(KDA_CHUNK_FP32_CORES | KDA_CHUNK_SEQUENTIAL | 0xffff0000u))
+  if (flags & ~(unsigned)(KDA_CHUNK_FP32_CORES | KDA_CHUNK_SEQUENTIAL |
+                          KDA_CHUNK_UNBOUNDED_GATE | 0xffff0000u))
     return fail(KDA_ERR_INVALID_ARG, "%s: unknown flags 0x%x", fn, flags);
+  if ((flags & KDA_CHUNK_UNBOUNDED_GATE) && z)
+    return fail(KDA_ERR_INVALID_ARG, "%s: the unbounded-gate mode takes g, not z", fn);
   kda_status_t st = check_device();
   if (st != KDA_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int* err = kda::device_error_flag();
   cudaError_t e = kda::launch_plan(cu_seqlens, N, T_per_seq, NT, workspace, err, s);
   if (e != cudaSuccess) return cuda_fail(e, "chunk plan launch");
-  if (dtype == KDA_BF16 && !(flags & KDA_CHUNK_FP32_CORES))
+  if (dtype == KDA_BF16 && !(flags & (KDA_CHUNK_FP32_CORES | KDA_CHUNK_UNBOUNDED_GATE))) {
     e = kda::launch_chunk_tc(q, k, v, g, z, A, g_min, beta, h0, o, hT, NT, N, H,
                              kda::chain_segment_chunks(NT, N, H, (int)(flags >> 16),
                                                        (flags & KDA_CHUNK_SEQUENTIAL) != 0),
                              ck, fz, workspace, err, s);
-  else
+    if (e == cudaSuccess && fz.gz && NT > 0)  // the output gate, on o in place
+      e = kda::launch_output_gate(o, 1, fz.gz, fz.w, fz.eps, o, NT, H, s);
+  } else {
     e = kda::launch_chunk_simt(q, k, v, dtype == KDA_BF16, g, beta, h0, o, hT, NT, N, H,
-                               workspace, s);
+                               workspace, s, (flags & KDA_CHUNK_UNBOUNDED_GATE) ? 1 : 0);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "chunk launch");
   return KDA_OK;
 }
@@ -464,7 +514,7 @@ kda_status_t kda_chunk_fwd_checkpointed(const void* q, const void* k, const void
                                         int ckpt_tokens, int64_t ckpt_capacity, void* workspace,
                                         size_t ws_bytes, kda_stream_t stream, unsigned flags) {
   const char* fn = "kda_chunk_fwd_checkpointed";
-  if (dtype != KDA_BF16 || (flags & KDA_CHUNK_FP32_CORES))
+  if (dtype != KDA_BF16 || (flags & (KDA_CHUNK_FP32_CORES | KDA_CHUNK_UNBOUNDED_GATE)))
     return fail(KDA_ERR_UNSUPPORTED_DTYPE, "%s: bf16 on the tensor-core path only", fn);
   if (ckpt_tokens < kda::kChunk || ckpt_tokens % kda::kChunk != 0)
     return fail(KDA_ERR_INVALID_ARG, "%s: ckpt_tokens=%d (a positive multiple of %d)", fn,
@@ -489,7 +539,7 @@ kda_status_t kda_chunk_fwd_fused(const void* q, const void* k, const void* v, in
                                  float* hT, void* workspace, size_t ws_bytes, kda_stream_t stream,
                                  unsigned flags) {
   const char* fn = "kda_chunk_fwd_fused";
-  if (dtype != KDA_BF16 || (flags & KDA_CHUNK_FP32_CORES))
+  if (dtype != KDA_BF16 || (flags & (KDA_CHUNK_FP32_CORES | KDA_CHUNK_UNBOUNDED_GATE)))
     return fail(KDA_ERR_UNSUPPORTED_DTYPE, "%s: bf16 on the tensor-core path only", fn);
   if ((g != nullptr) == (z != nullptr))
     return fail(KDA_ERR_INVALID_ARG, "%s: give exactly one of g and z", fn);

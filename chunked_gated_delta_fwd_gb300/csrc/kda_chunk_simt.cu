@@ -21,6 +21,17 @@
 // where the first two factors are <= 1 and the last is < e^80 (16 tokens with
 // g >= -5).
 //
+// Range-robust mode (any g <= 0, e.g. the unbounded softplus gate of Kimi Linear,
+// "Kimi K3 technical report review", section 3.2): tiles below the diagonal take
+// the reference at the END of the key tile,
+//   exp(G_r - G_i) = exp(L_r) * exp(sum of the tile totals between) * exp(M_i),
+// with L_r the sum of g over tile a up to r and M_i the sum over tile b after i:
+// every factor <= 1.  The diagonal tiles are formed pair by pair,
+// sum_c k_rc k_ic exp(g_{i+1,c} + ... + g_{r,c}) -- the position-pair path the
+// bound removes.  Every exponent is a sum of non-positive terms, never the
+// difference of two running sums, so decays stay exact to fp32 rounding even
+// where a single g is -10^4.
+//
 // Two kernels: `simt_prep` (one CTA per (chunk, head), fully parallel) writes
 // W, U, Gamma*Q, (gamma_C/Gamma)*K, the masked 64x64 A_qk and gamma_C to the
 // workspace; `simt_chain` (one CTA per (sequence, head, 32-column slice of S))
@@ -60,6 +71,8 @@ struct PrepSmem {
   } u;
   float R[4][D];       // tile references R_0 = 0, R_a = G[16a - 1]
   float E[4][4][D];    // exp(R_a - R_b) for a > b
+  float X[C][LD];      // range-robust mode: the raw g
+  float Tt[4][D];      // range-robust mode: sum of g over tile a
   float GC[D];         // G at the chunk's last token
   float beta[C];
 };
@@ -78,7 +91,7 @@ template <typename T>
 __global__ void __launch_bounds__(kPrepThreads, 1) simt_prep(
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
     const float* __restrict__ g, const T* __restrict__ beta, Plan plan, int H,
-    float* __restrict__ out) {
+    float* __restrict__ out, int robust) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   PrepSmem& sm = *reinterpret_cast<PrepSmem*>(smem_raw);
   const int chunk = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
@@ -112,7 +125,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) simt_prep(
   __syncthreads();
 
   // ---- 2. running sum of g per channel, tile references
-  if (tid < D) {
+  if (tid < D && !robust) {
     const int c = tid;
     float acc = 0.f;
     sm.R[0][c] = 0.f;
@@ -122,22 +135,80 @@ __global__ void __launch_bounds__(kPrepThreads, 1) simt_prep(
       if ((r & (kTile - 1)) == kTile - 1 && r + 1 < C) sm.R[(r + 1) / kTile][c] = acc;
     }
     sm.GC[c] = acc;
+  } else if (tid < D) {
+    // range-robust: raw g kept in X; G <- L (sum over the tile up to r), KN <- M (sum
+    // over the tile after r), tile totals, R_a = totals before tile a
+    const int c = tid;
+    float pre = 0.f;
+    for (int a = 0; a < 4; ++a) {
+      sm.R[a][c] = pre;
+      float l = 0.f;
+      for (int e = 0; e < kTile; ++e) {
+        const int r = a * kTile + e;
+        const float gv = sm.u.G[r][c];
+        sm.X[r][c] = gv;
+        l += gv;
+        sm.u.G[r][c] = l;
+      }
+      float m = 0.f;
+      for (int e = kTile - 1; e >= 0; --e) {
+        const int r = a * kTile + e;
+        sm.KN[r][c] = m;
+        m += sm.X[r][c];
+      }
+      sm.Tt[a][c] = l;
+      pre += l;
+    }
+    sm.GC[c] = pre;
   }
   __syncthreads();
+
+  // ---- 2b. range-robust mode: the diagonal tiles pair by pair from the raw rows
+  //          (thread -> row ri, key ii of every diagonal tile)
+  float dk_[4] = {0.f, 0.f, 0.f, 0.f}, dq_[4] = {0.f, 0.f, 0.f, 0.f};
+  if (robust) {
+    const int ri = tid / 16, ii = tid % 16;
+    if (ii <= ri) {
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        const int r = a * kTile + ri, i = a * kTile + ii;
+        float ak = 0.f, aq = 0.f;
+#pragma unroll 4
+        for (int c = 0; c < D; ++c) {
+          float sg = 0.f;  // g over tokens i+1 .. r of this channel
+          for (int jj = i + 1; jj <= r; ++jj) sg += sm.X[jj][c];
+          const float t = sm.Kb[i][c] * expf(sg);
+          ak = fmaf(sm.Kb[r][c], t, ak);
+          aq = fmaf(sm.Qb[r][c], t, aq);
+        }
+        dk_[a] = ak;
+        dq_[a] = aq;
+      }
+    }
+  }
+  if (robust) __syncthreads();  // the raw rows are read before step 3 rescales them
+  // sum of the tile totals over tiles lo..hi (range-robust mode)
+  auto tiles_sum = [&](int lo, int hi, int c) {
+    float s = 0.f;
+    for (int t2 = lo; t2 <= hi; ++t2) s += sm.Tt[t2][c];
+    return s;
+  };
 
   // ---- 3. tile-referenced factors
   for (int e = tid; e < C * D; e += kPrepThreads) {
     const int r = e / D, c = e % D, a = r / kTile;
-    const float d = sm.u.G[r][c] - sm.R[a][c];  // in (-80, 0]
+    // G_r - R_a: in (-80, 0] (bounded), L_r (robust)
+    const float d = robust ? sm.u.G[r][c] : sm.u.G[r][c] - sm.R[a][c];
     const float f = expf(d);
     const float kk = sm.Kb[r][c];
     sm.Kb[r][c] = kk * f;
     sm.Qb[r][c] *= f;
-    sm.KN[r][c] = kk * expf(-d);
+    sm.KN[r][c] = kk * expf(robust ? sm.KN[r][c] : -d);  // < e^80 (bounded), <= 1 (robust)
   }
   for (int e = tid; e < 16 * D; e += kPrepThreads) {
     const int ab = e / D, c = e % D, a = ab / 4, b = ab % 4;
-    sm.E[a][b][c] = a > b ? expf(sm.R[a][c] - sm.R[b][c]) : 1.f;
+    sm.E[a][b][c] = a <= b ? 1.f
+                           : expf(robust ? tiles_sum(b + 1, a - 1, c) : sm.R[a][c] - sm.R[b][c]);
   }
   __syncthreads();
 
@@ -148,7 +219,10 @@ __global__ void __launch_bounds__(kPrepThreads, 1) simt_prep(
       for (int b = 0; b < 4; ++b) {
         const int r = a * kTile + ri, i = b * kTile + ii;
         float ak = 0.f, aq = 0.f;
-        if (b <= a) {
+        if (robust && b == a) {
+          ak = dk_[a];
+          aq = dq_[a];
+        } else if (b <= a) {
 #pragma unroll 8
           for (int c = 0; c < D; ++c) {
             const float t = sm.E[a][b][c] * sm.KN[i][c];
@@ -182,7 +256,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1) simt_prep(
     for (int e = tid - C; e < C * D; e += kPrepThreads - C) {
       const int r = e / D, c = e % D, a = r / kTile;
       const float ea = expf(sm.R[a][c]);                     // exp(R_a), <= 1
-      const float ec = expf(sm.GC[c] - sm.R[a][c]);          // exp(G_C - R_a), <= 1
+      // exp(G_C - reference of the key tile), <= 1
+      const float ec = expf(robust ? tiles_sum(a + 1, 3, c) : sm.GC[c] - sm.R[a][c]);
       sm.Kb[r][c] *= ea * sm.beta[r];                        // beta * Gamma * K
       sm.Qb[r][c] *= ea;                                     // Gamma * Q
       sm.KN[r][c] *= ec;                                     // (gamma_C / Gamma) * K
@@ -307,7 +382,7 @@ size_t simt_workspace_bytes(int64_t n_tokens, int n_seqs, int H) {
 cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v, int bf16,
                               const float* g, const void* beta, const float* h0, void* o,
                               float* hT, int64_t n_tokens, int n_seqs, int H, void* ws,
-                              cudaStream_t s) {
+                              cudaStream_t s, int robust) {
   const Plan plan = plan_in(ws, n_tokens, n_seqs);
   float* body = reinterpret_cast<float*>(static_cast<char*>(ws) + plan_bytes(n_tokens, n_seqs));
   const int64_t chunks = chunks_upper_bound(n_tokens, n_seqs);
@@ -323,14 +398,15 @@ cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v, int b
       if (e != cudaSuccess) return e;
       simt_prep<T><<<grid, kPrepThreads, prep_smem, s>>>(
           static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), g,
-          static_cast<const T*>(beta), plan, H, body);
+          static_cast<const T*>(beta), plan, H, body, robust);
     } else {
       e = cudaFuncSetAttribute(simt_prep<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)prep_smem);
       if (e != cudaSuccess) return e;
       simt_prep<float><<<grid, kPrepThreads, prep_smem, s>>>(
           static_cast<const float*>(q), static_cast<const float*>(k),
-          static_cast<const float*>(v), g, static_cast<const float*>(beta), plan, H, body);
+          static_cast<const float*>(v), g, static_cast<const float*>(beta), plan, H, body,
+          robust);
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -824,9 +824,7 @@ constexpr uint32_t kC_bars = kStages * kStageBytes;
 // operands of MMA1 (S^T, packed pairs, [384,448)) and MMA2 (Vt^T, two buffers of 32
 // columns at [448,512)).
 constexpr uint32_t kT_SB = 384, kT_VT = 448;
-// output gate scratch: per-warp partial sums of o^2 (fp32 [4][64]) and 1/rms ([64])
-constexpr uint32_t kC_red = kC_bars + 256, kC_rs = kC_red + 1024;
-constexpr uint32_t kC_Smem = kC_rs + 256 + 1024;
+constexpr uint32_t kC_Smem = kC_bars + 256 + 1024;
 constexpr int kEpi = 256;    // epilogue warps 0-7: (TMEM lane, column half)
 constexpr int kStore = 128;  // store warps 8-11: TMEM lane = value row, all 64 tokens
 constexpr int kCopyWarp = (kEpi + kStore) / 32;  // warp 12: tile copies
@@ -860,13 +858,6 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int
 //   scan:  S_in(1) = S_end(0), S_in(k+1) = S~(k) + M(k) S_in(k)  (seg_scan_kernel);
 //   mode 2: segments k >= 1 run from S_in(k) with outputs; the last writes hT.
 // mode 0 is the plain chain, one CTA per (sequence, head).  States are S^T.
-// Output gate of the chunk outputs (gz null: plain o).
-struct OutGate {
-  const __nv_bfloat16* gz;  // gate logits [NT][H][dv]
-  const float* w;           // RMSNorm weight [dv] (null: ones)
-  float eps;
-};
-
 struct SegArgs {
   int mode;
   const int4* tab;  // per segment: (sequence, first chunk, chunks, k | P << 16); x < 0: unused
@@ -879,7 +870,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     tc_chain(const uint8_t* __restrict__ tiles, const float* __restrict__ gam,
              const float* __restrict__ h0, Plan plan, int H, __nv_bfloat16* __restrict__ o,
              float* __restrict__ hT, SegArgs sg, CkptArgs ck, const int* __restrict__ ck_off,
-             OutGate og, int* err) {
+             int* err) {
   // ---- this CTA's job: chunk range, initial and final state, outputs or not
   const int h = blockIdx.y;
   int n, c0, nch;
@@ -1178,15 +1169,11 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     // Thread = value row dv; it reads the 64 outputs of its row from the chunk's D1
     // buffer and writes them (2-byte stores, 64 contiguous bytes per warp), then
     // frees the buffer for MMA1 two chunks later.
-    // With the output gate the store warps meet at barrier 2 every chunk; an
-    // expired wait then stops all of them at the same point (bar.red.and).
     const int dv = t - kEpi;
     const uint32_t lrow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-    const bool gate_on = og.gz != nullptr && write_o;
     for (int j = 0; j < nch; ++j) {
       const int b = j & 1;
-      const bool okw = wait_or_abort(bar_o0 + 8 * b, (j >> 1) & 1, err, abort_flag);
-      if (gate_on ? !named_sync_and(2, kStore, okw) : !okw) break;
+      if (!wait_or_abort(bar_o0 + 8 * b, (j >> 1) & 1, err, abort_flag)) break;
       tc_fence_after();
       float ov[2][32];
       const uint32_t d1 = lrow + 128 + 128 * b + 64;
@@ -1197,63 +1184,9 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       mbar_arrive(bar_f0 + 8 * b);
       const int64_t tc = tstart + (int64_t)j * C;
       __nv_bfloat16* orow = o + (tc * H + h) * D + dv;
-      if (gate_on) {
-        // Output gate: y = Sigmoid(gz) * w * o / sqrt(mean_dv(o^2) + eps) per token.
-        // Sums of o^2 over this warp's 32 rows by a halving reduce-scatter: after
-        // the exchanges over lane bits 4..0 lane l holds tokens 2l and 2l + 1.
-        float a[32];
-        {
-          const bool up = (dv & 16) != 0;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float lo = ov[0][i] * ov[0][i], hi = ov[1][i] * ov[1][i];
-            a[i] = (up ? hi : lo) + __shfl_xor_sync(0xffffffffu, up ? lo : hi, 16);
-          }
-        }
-#pragma unroll
-        for (int m = 8, n = 16; m >= 1; m >>= 1, n >>= 1) {
-          const bool up = (dv & m) != 0;
-#pragma unroll
-          for (int i = 0; i < n; ++i)
-            a[i] = (up ? a[n + i] : a[i]) + __shfl_xor_sync(0xffffffffu, up ? a[i] : a[n + i], m);
-        }
-        float* red = reinterpret_cast<float*>(sm + kC_red);
-        float* rs = reinterpret_cast<float*>(sm + kC_rs);
-        *reinterpret_cast<float2*>(red + (warp & 3) * 64 + 2 * (dv & 31)) = make_float2(a[0], a[1]);
-        named_sync(2, kStore);
-        if (dv < C)
-          rs[dv] = rsqrtf((red[dv] + red[64 + dv] + red[128 + dv] + red[192 + dv]) * (1.f / D) +
-                          og.eps);
-        named_sync(2, kStore);
-        const float wv = og.w ? __ldg(og.w + dv) : 1.f;
-        const __nv_bfloat16* grow = og.gz + (tc * H + h) * D + dv;
-#pragma unroll
-        for (int r0 = 0; r0 < C; r0 += 4) {
-          // Sigmoid(x) = 1 / (1 + 2^(-x log2 e)); four quotients share one reciprocal
-          // (exponent clamped at 30: a gate below 2^-30 moves by less than 2^-30)
-          float d[4], y[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float x = tc + r0 + i < tend ? __bfloat162float(grow[(int64_t)(r0 + i) * H * D]) : 0.f;
-            d[i] = 1.f + exp2_approx(fminf(-x * kLog2e, 30.f));
-          }
-          const float d01 = d[0] * d[1], d23 = d[2] * d[3];
-          const float rall = rcp_approx(d01 * d23);
-          const float q01 = d23 * rall, q23 = d01 * rall;
-          const float sg[4] = {d[1] * q01, d[0] * q01, d[3] * q23, d[2] * q23};
-          const float4 r4 = *reinterpret_cast<const float4*>(rs + r0);
-          const float rv[4] = {r4.x, r4.y, r4.z, r4.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) y[i] = ov[(r0 + i) >> 5][(r0 + i) & 31] * rv[i] * wv * sg[i];
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            if (tc + r0 + i < tend) orow[(int64_t)(r0 + i) * H * D] = __float2bfloat16_rn(y[i]);
-        }
-      } else {
-#pragma unroll
-        for (int r = 0; r < C; ++r)
-          if (write_o && tc + r < tend) orow[(int64_t)r * H * D] = __float2bfloat16_rn(ov[r >> 5][r & 31]);
-      }
+      for (int r = 0; r < C; ++r)
+        if (write_o && tc + r < tend) orow[(int64_t)r * H * D] = __float2bfloat16_rn(ov[r >> 5][r & 31]);
     }
   }
   tc_fence_before();
@@ -1538,7 +1471,6 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
                             const float* h0, void* o, float* hT, int64_t n_tokens, int n_seqs,
                             int H, int seg_chunks, CkptArgs ck, FuseArgs fz, void* ws,
                             int* err, cudaStream_t s) {
-  const OutGate og{static_cast<const __nv_bfloat16*>(fz.gz), fz.w, fz.eps};
   const Plan plan = plan_in(ws, n_tokens, n_seqs);
   const int64_t units = chunks_upper_bound(n_tokens, n_seqs) * H;
   const TcLayout lay = tc_layout(ws, n_tokens, n_seqs, H, seg_chunks);
@@ -1581,7 +1513,7 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
     ProfScope prof_scope("kda_tc_chain", s);
     tc_chain<<<cgrid, kChainThreads, kC_Smem, s>>>(tiles, gam, h0, plan, H, static_cast<T*>(o),
                                                     hT, SegArgs{0, nullptr, nullptr, nullptr, nullptr},
-                                                    ck, lay.ck_off, og, err);
+                                                    ck, lay.ck_off, err);
     return cudaGetLastError();
   }
   // sequence-segment parallel chain: segments, end states and transitions, scan, rerun
@@ -1595,7 +1527,7 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
   {
     ProfScope prof_scope("kda_tc_chain_seg", s);
     tc_chain<<<dim3((unsigned)lay.segs_ub, (unsigned)H, 2), kChainThreads, kC_Smem, s>>>(
-        tiles, gam, h0, plan, H, static_cast<T*>(o), hT, sg, ck, lay.ck_off, og, err);
+        tiles, gam, h0, plan, H, static_cast<T*>(o), hT, sg, ck, lay.ck_off, err);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -1612,7 +1544,7 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
   sg.mode = 2;
   ProfScope prof_scope("kda_tc_chain_seg", s);
   tc_chain<<<dim3((unsigned)lay.segs_ub, (unsigned)H, 1), kChainThreads, kC_Smem, s>>>(
-      tiles, gam, h0, plan, H, static_cast<T*>(o), hT, sg, ck, lay.ck_off, og, err);
+      tiles, gam, h0, plan, H, static_cast<T*>(o), hT, sg, ck, lay.ck_off, err);
   return cudaGetLastError();
 }
 

@@ -5,6 +5,9 @@
 // (the log of the in-chunk cumulative decay Gamma of the chunkwise form,
 // "Kimi K3 notes" (s1mplewind blog), section "Chunkwise form").
 //
+// The unbounded gate it replaces, g = -exp(A_h) * Softplus(z) (Kimi Linear, the same
+// review, section 3.2), is formed by the same kernel for the range-robust mode.
+//
 // Memory-bound elementwise work: 8 elements per thread per step with 16-byte
 // (bf16) or 32-byte (fp32) loads and 32-byte stores, grid-stride over a grid
 // sized to the SM count.
@@ -18,7 +21,12 @@ __device__ __forceinline__ float bounded_decay(float z, float scale, float g_min
   return g_min / (1.0f + expf(-scale * z));
 }
 
-template <typename Tz>
+// -scale * Softplus(z), Softplus(x) = log(1 + e^x) (= x to fp32 precision above 20)
+__device__ __forceinline__ float softplus_decay(float z, float scale) {
+  return -scale * (z > 20.f ? z : log1pf(expf(z)));
+}
+
+template <typename Tz, bool kSoftplus = false>
 __global__ void __launch_bounds__(256) gate_kernel(const Tz* __restrict__ z,
                                                    const float* __restrict__ A, float g_min,
                                                    float* __restrict__ g, int64_t n_groups,
@@ -30,15 +38,11 @@ __global__ void __launch_bounds__(256) gate_kernel(const Tz* __restrict__ z,
     const float scale = expf(__ldg(A + h));
     float x[8];
     load8(z + grp * 8, x);
-    float4 lo, hi;
-    lo.x = bounded_decay(x[0], scale, g_min);
-    lo.y = bounded_decay(x[1], scale, g_min);
-    lo.z = bounded_decay(x[2], scale, g_min);
-    lo.w = bounded_decay(x[3], scale, g_min);
-    hi.x = bounded_decay(x[4], scale, g_min);
-    hi.y = bounded_decay(x[5], scale, g_min);
-    hi.z = bounded_decay(x[6], scale, g_min);
-    hi.w = bounded_decay(x[7], scale, g_min);
+    float y[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      y[i] = kSoftplus ? softplus_decay(x[i], scale) : bounded_decay(x[i], scale, g_min);
+    const float4 lo = make_float4(y[0], y[1], y[2], y[3]), hi = make_float4(y[4], y[5], y[6], y[7]);
     float4* out = reinterpret_cast<float4*>(g + grp * 8);
     out[0] = lo;
     out[1] = hi;
@@ -117,6 +121,73 @@ cudaError_t launch_gate(const void* z, int z_bf16, const float* A, float g_min, 
     gate_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(z), A, g_min, g, n_groups, H);
   else
     gate_kernel<<<grid, 256, 0, s>>>(static_cast<const float*>(z), A, g_min, g, n_groups, H);
+  return cudaGetLastError();
+}
+
+namespace {
+
+// Output gate, one warp per (token, head): lane l holds channels 4l .. 4l + 3 of o
+// and of the gate logits; the sum of squares meets by a warp all-reduce.
+//   y = Sigmoid(x) * w * o / sqrt(mean(o^2) + eps)
+// ("Kimi K3 technical report review", section 3.3, Eq. 6, without W_o and W_g)
+template <typename T>
+__global__ void __launch_bounds__(256) out_gate_kernel(const T* __restrict__ o,
+                                                       const T* __restrict__ x,
+                                                       const float* __restrict__ w, float eps,
+                                                       T* y, int64_t n_rows) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  float wv[4] = {1.f, 1.f, 1.f, 1.f};
+  if (w) {
+    const float4 w4 = __ldg(reinterpret_cast<const float4*>(w) + lane);
+    wv[0] = w4.x; wv[1] = w4.y; wv[2] = w4.z; wv[3] = w4.w;
+  }
+  for (int64_t row = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5); row < n_rows;
+       row += nwarps) {
+    float ov[4], xv[4];
+    load4(o + row * kD + 4 * lane, ov);
+    load4(x + row * kD + 4 * lane, xv);
+    float ss = ov[0] * ov[0] + ov[1] * ov[1] + ov[2] * ov[2] + ov[3] * ov[3];
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+    const float r = rsqrtf(ss * (1.f / kD) + eps);
+    float yv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) yv[i] = ov[i] * r * wv[i] / (1.f + expf(-xv[i]));
+    store4(y + row * kD + 4 * lane, yv);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_output_gate(const void* o, int bf16, const void* x, const float* w, float eps,
+                               void* y, int64_t n_tokens, int H, cudaStream_t s) {
+  const int64_t rows = n_tokens * H;
+  if (rows == 0) return cudaSuccess;
+  const int grid = grid_for(rows * 32, 256);
+  ProfScope prof_scope("kda_output_gate", s);
+  if (bf16)
+    out_gate_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(o),
+                                         static_cast<const __nv_bfloat16*>(x), w, eps,
+                                         static_cast<__nv_bfloat16*>(y), rows);
+  else
+    out_gate_kernel<<<grid, 256, 0, s>>>(static_cast<const float*>(o),
+                                         static_cast<const float*>(x), w, eps,
+                                         static_cast<float*>(y), rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gate_softplus(const void* z, int z_bf16, const float* A, float* g,
+                                 int64_t n_tokens, int H, cudaStream_t s) {
+  const int64_t n_groups = n_tokens * H * (kD / 8);
+  const int grid = grid_for(n_groups, 256);
+  ProfScope prof_scope("kda_gate_softplus", s);
+  if (z_bf16)
+    gate_kernel<__nv_bfloat16, true><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(z), A,
+                                                          0.f, g, n_groups, H);
+  else
+    gate_kernel<float, true><<<grid, 256, 0, s>>>(static_cast<const float*>(z), A, 0.f, g,
+                                                  n_groups, H);
   return cudaGetLastError();
 }
 

@@ -69,6 +69,15 @@ __device__ __forceinline__ void load4(const __nv_bfloat16* p, float* out) {
   out[2] = __uint_as_float(u.y << 16);
   out[3] = __uint_as_float(u.y & 0xffff0000u);
 }
+// Stores 4 consecutive elements from fp32 (16-byte aligned for fp32, 8-byte for bf16).
+__device__ __forceinline__ void store4(float* p, const float* v) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+}
+__device__ __forceinline__ void store4(__nv_bfloat16* p, const float* v) {
+  const __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]), b = __floats2bfloat162_rn(v[2], v[3]);
+  *reinterpret_cast<uint2*>(p) =
+      make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+}
 
 // ---- chunk plan -------------------------------------------------------------
 // The workspace starts with the plan: cu[N+1] (int32 token offsets) followed by
@@ -93,6 +102,11 @@ inline int64_t chunks_upper_bound(int64_t n_tokens, int n_seqs) {
 // ---- kernels ----------------------------------------------------------------
 cudaError_t launch_gate(const void* z, int z_bf16, const float* A, float g_min, float* g,
                         int64_t n_tokens, int H, cudaStream_t s);
+cudaError_t launch_gate_softplus(const void* z, int z_bf16, const float* A, float* g,
+                                 int64_t n_tokens, int H, cudaStream_t s);
+// y = Sigmoid(x) * w * o / sqrt(mean(o^2) + eps) per (token, head); y may alias o.
+cudaError_t launch_output_gate(const void* o, int bf16, const void* x, const float* w, float eps,
+                               void* y, int64_t n_tokens, int H, cudaStream_t s);
 cudaError_t launch_gate_cumsum(const void* z, int z_bf16, const float* A, float g_min, float* g,
                                float* gcum, int64_t n_tokens, int H, const int32_t* cu,
                                int n_seqs, cudaStream_t s);
@@ -109,7 +123,7 @@ size_t simt_workspace_bytes(int64_t n_tokens, int n_seqs, int H);
 cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v, int bf16,
                               const float* g, const void* beta, const float* h0, void* o,
                               float* hT, int64_t n_tokens, int n_seqs, int H, void* ws,
-                              cudaStream_t s);
+                              cudaStream_t s, int robust = 0);
 
 // bf16 tensor-core (tcgen05) chunk path.
 // Chunks per chain segment for the sequence-segment parallel chain (0: the chain of
@@ -126,8 +140,8 @@ struct CkptArgs {
   int64_t cap;
 };
 // Fused prologue / epilogue of the tensor-core chunk path: q, k L2-normalised in the
-// prepare kernel (qk_eps < 0: off) and the output RMSNorm x Sigmoid gate in the chain
-// (gz null: off; w null: unit weight).
+// prepare kernel (qk_eps < 0: off) and the output RMSNorm x Sigmoid gate applied to
+// o right after the chain (gz null: off; w null: unit weight).
 struct FuseArgs {
   float qk_eps;
   const void* gz;

@@ -80,6 +80,16 @@ kda_status_t kda_gate(const void* z, int z_dtype, const float* A, float g_min, f
                       int n_seqs, kda_stream_t stream);
 
 /*
+ * kda_gate_softplus -- the unbounded log-decay that the bounded gate replaced
+ * (Kimi Linear; "Kimi K3 technical report review", section 3.2), elementwise:
+ *     g[t][h][c] = -exp(A[h]) * Softplus(z[t][h][c]),  Softplus(x) = log(1 + e^x)
+ * g lies in (-inf, 0); a prefill on it needs KDA_CHUNK_UNBOUNDED_GATE.  Arguments,
+ * layouts and errors as kda_gate (no g_min, no running sum).
+ */
+kda_status_t kda_gate_softplus(const void* z, int z_dtype, const float* A, float* g,
+                               int64_t n_tokens, int H, int dk, kda_stream_t stream);
+
+/*
  * kda_chunk_fwd_workspace_size -- bytes of device workspace kda_chunk_fwd needs
  * for n_tokens tokens in n_seqs sequences and H heads with inputs of `dtype`.
  * Returns 0 for invalid arguments.
@@ -126,8 +136,9 @@ kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v, int dtyp
 
 /* Flags of kda_chunk_fwd_ex. */
 enum {
-  KDA_CHUNK_FP32_CORES = 1u, /* evaluate on fp32 CUDA cores even for bf16 inputs */
-  KDA_CHUNK_SEQUENTIAL = 2u  /* never split a sequence's chain into segments */
+  KDA_CHUNK_FP32_CORES = 1u,     /* evaluate on fp32 CUDA cores even for bf16 inputs */
+  KDA_CHUNK_SEQUENTIAL = 2u,     /* never split a sequence's chain into segments */
+  KDA_CHUNK_UNBOUNDED_GATE = 4u  /* any g <= 0 (range-robust fp32-core evaluation) */
 };
 /* Split every sequence's chain into segments of n chunks (n in 1..65535). */
 #define KDA_CHUNK_SEGMENT_CHUNKS(n) (((unsigned)(n) & 0xffffu) << 16)
@@ -136,6 +147,14 @@ enum {
  * kda_chunk_fwd_ex -- kda_chunk_fwd with option flags (0 = kda_chunk_fwd).
  * KDA_CHUNK_FP32_CORES selects the fp32 CUDA-core evaluation of the same chunkwise
  * form for bf16 inputs (the path KDA_F32 inputs always take).
+ *
+ * KDA_CHUNK_UNBOUNDED_GATE lifts the g >= -5 precondition: any finite g <= 0 (the
+ * unbounded gate -exp(A) Softplus(z) of Kimi Linear, kda_gate_softplus).  The
+ * 16-token tile references are then taken so that every rescaling factor is <= 1
+ * and the diagonal 16x16 tiles are formed pair by pair, exp(G_r - G_i) per
+ * channel -- the position-pair path that the bound makes unnecessary ("Kimi K3
+ * technical report review", section 3.2).  It runs on the fp32 CUDA cores for
+ * either dtype (workspace as for KDA_CHUNK_FP32_CORES).
  *
  * Sequence segments (bf16 tensor-core path): the state update of one (sequence,
  * head) is serial over its chunks.  When there are too few (sequence, head)
@@ -166,8 +185,7 @@ kda_status_t kda_chunk_fwd_ex(const void* q, const void* k, const void* v, int d
  * prepare kernel normalises before the gate prefix sums: "Kimi K3 notes",
  * section "FlashKDA", kernel K1), and the head-wise RMSNorm x Sigmoid output gate
  * ("Kimi K3 technical report review", section 3.3, Eq. 6; "Kimi K3:
- * architecture, training and inference systems", section 3.3) applied to the
- * fp32 outputs before they are rounded and stored.
+ * architecture, training and inference systems", section 3.3) applied to o.
  *   g or z, A, g_min  exactly one of g (as kda_chunk_fwd) and z (as
  *              kda_chunk_fwd_gated; A and g_min then as there).
  *   qk_l2_eps  >= 0: q_t <- q_t / sqrt(|q_t|^2 + qk_l2_eps), the same for k, per
@@ -177,7 +195,8 @@ kda_status_t kda_chunk_fwd_ex(const void* q, const void* k, const void* v, int d
  *   out_gate   optional [NT][H][dv] of `dtype`, 16-byte aligned: gate logits x.
  *              When given, o_t = Sigmoid(x_t) * w * o~_t / sqrt(mean(o~_t^2) +
  *              out_norm_eps) with the mean over the dv channels of one head and
- *              o~ the KDA output; NULL: o = o~.
+ *              o~ the KDA output; NULL: o = o~.  It is applied by kda_output_gate
+ *              on o in place, enqueued right after the chunk kernels.
  *   out_norm_weight  optional fp32 [dv] RMSNorm weight w shared by the heads
  *              (NULL: ones); only with out_gate.
  *   out_norm_eps  finite, >= 0 (used only with out_gate).
@@ -197,6 +216,22 @@ kda_status_t kda_chunk_fwd_fused(const void* q, const void* k, const void* v, in
                                  const float* out_norm_weight, float out_norm_eps, void* o,
                                  float* hT, void* workspace, size_t ws_bytes, kda_stream_t stream,
                                  unsigned flags);
+
+/*
+ * kda_output_gate -- the head-wise RMSNorm x Sigmoid output gate on KDA outputs
+ * ("Kimi K3 technical report review", section 3.3, Eq. 6, without the W_o and W_g
+ * projections), per token t and head h over the dv channels c:
+ *     y[t][h][c] = Sigmoid(gate[t][h][c]) * weight[c] * o[t][h][c]
+ *                  / sqrt(mean_c(o[t][h][c]^2) + eps)
+ *   o, gate, y  [n_tokens][H][dv] of `dtype` (KDA_F32 or KDA_BF16), 16-byte aligned;
+ *               y may alias o (in place).
+ *   weight      optional fp32 [dv] (NULL: ones), shared by the heads.
+ *   eps         finite, >= 0.
+ * dv must be 128.  n_tokens == 0 is a no-op.  Errors as kda_gate.
+ */
+kda_status_t kda_output_gate(const void* o, int dtype, const void* gate, const float* weight,
+                             float eps, void* y, int64_t n_tokens, int H, int dv,
+                             kda_stream_t stream);
 
 /*
  * kda_chunk_fwd_checkpointed -- kda_chunk_fwd_ex that also writes the state at

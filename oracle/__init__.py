@@ -26,6 +26,8 @@ Functions and the passages they follow:
   L2Norm applied to q and k before the recurrence ("Kimi K3: architecture,
   training and inference systems", section 3.2, the q / k branches; done inside
   the FlashKDA prepare kernel, "Kimi K3 notes", section "FlashKDA", K1).
+* :func:`gate_softplus` -- the unbounded gate ``g = -exp(A_h) Softplus(z)`` that
+  the bounded one replaced ("Kimi K3 technical report review", section 3.2).
 * :func:`output_gate` -- the head-wise RMSNorm of the KDA output times the
   full-rank Sigmoid gate ("Kimi K3 technical report review", section 3.3, Eq. 6;
   the same systems page, section 3.3), without the W_o / W_g projections.
@@ -264,3 +266,10 @@ def output_gate(o, x, w=None, eps: float = 1e-6) -> np.ndarray:
     if w is not None:
         y = y * _f64(w)
     return y
+
+
+def gate_softplus(z, A) -> np.ndarray:
+    """``g[t, h, c] = -exp(A[h]) * log(1 + exp(z[t, h, c]))`` in fp64 (Softplus as
+    ``logaddexp(0, z)``, exact for large |z|)."""
+    z, A = _f64(z), _f64(A)
+    return -np.exp(A)[None, :, None] * np.logaddexp(0.0, z)

@@ -71,7 +71,7 @@ def test_chunk_rejects_bad_arguments(L):
     assert _chunk(L, q=FAKE + 8) == 4
     assert _chunk(L, ws=FAKE + 16) == 4
     assert _chunk(L, ws_bytes=16) == 5
-    assert _chunk(L, flags=4) == 1
+    assert _chunk(L, flags=8) == 1
     assert _chunk(L, B=2, cu=FAKE, n_seqs=2) == 1  # B must be 1 with cu_seqlens
     assert _chunk(L, cu=FAKE, n_seqs=0) == 1
     assert _chunk(L, q=None) == 1
@@ -139,8 +139,27 @@ def test_chunk_fused_rejects_bad_arguments(L):
     assert _fused(L, gate=FAKE, eps=float("nan")) == 1
     assert _fused(L, w=FAKE) == 1                  # a weight without the gate
     assert _fused(L, gate=FAKE + 8) == 4
+    assert _fused(L, flags=4) == 3                 # the unbounded-gate mode is not fused
     assert _fused(L, flags=8) == 1
     assert b"kda_chunk_fwd_fused" in L.kda_last_error_string()
+
+
+def test_output_gate_rejects_bad_arguments(L):
+    vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+    L.kda_output_gate.argtypes = [vp, i32, vp, vp, f32, vp, i64, i32, i32, vp]
+    og = lambda dtype=1, o=FAKE, x=FAKE, w=None, eps=1e-6, y=FAKE, n=10, H=2, dv=128: \
+        L.kda_output_gate(o, dtype, x, w, eps, y, n, H, dv, None)
+    assert og(dtype=5) == 3
+    assert og(dv=64) == 2
+    assert og(H=0) == 2
+    assert og(eps=-1.0) == 1
+    assert og(eps=float("inf")) == 1
+    assert og(n=-1) == 1
+    assert og(x=None) == 1
+    assert og(y=FAKE + 2) == 4
+    assert og(w=FAKE + 4) == 4
+    assert og(n=0) == 0                          # nothing to do, no device needed
+    assert b"kda_output_gate" in L.kda_last_error_string()
 
 
 def test_workspace_size(L):

@@ -378,3 +378,95 @@ def test_checkpoint_capacity_overflow_is_reported(kda):
     for i in range(3):
         assert_close(buf[i], ck_ref[i], torch.bfloat16, f"checkpoint {i}")
     assert bool((buf[3:] == 7.0).all())
+
+
+# ------------------------------------------------ unbounded gate (range-robust mode)
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_unbounded_softplus_gate(kda, dtype):
+    """g = -exp(A) Softplus(z) with A in [0, 2] and z ~ N(0, 4): per-token log-decays
+    down to about -50, 16-token sums far below the bounded path's -80.  The
+    range-robust mode against the oracle (fp32 or bf16 tolerance by input type)."""
+    lens = [5, 0, 70, 64, 129, 300]
+    w = workloads.custom(lens, H=3, dtype=dtype, seed=91, z_std=2.0, A_range=0.0, h0_std=0.5)
+    inp = workloads.make_inputs(w, "cpu")
+    A = torch.linspace(0.0, 2.0, 3)
+    g = torch.from_numpy(oracle.gate_softplus(inp["z"], A)).float()
+    assert float(g.min()) < -30.0
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    g_dev = kda.gate_softplus(dev["z"], A.cuda())
+    o, hT = kda.chunk_fwd(dev["q"], dev["k"], dev["v"], g_dev, dev["beta"], dev["h0"],
+                          dev["cu_seqlens"], flags=kda.UNBOUNDED_GATE)
+    o_ref, h_ref = oracle.recurrence(inp["q"], inp["k"], inp["v"], g, inp["beta"], inp["h0"],
+                                     inp["cu_seqlens"])
+    assert_close(o, o_ref, dtype, "o unbounded")
+    assert_close(hT, h_ref, dtype, "hT unbounded")
+
+
+def test_unbounded_mode_extremes(kda):
+    """fp32: g = -10^4 on some tokens (the state is wiped there), g = 0 on others, and
+    bounded g elsewhere, through the range-robust mode."""
+    lens = [200, 77]
+    inp, g, dev = _inputs(lens, H=2, dtype=torch.float32, seed=93)
+    gen = torch.Generator().manual_seed(94)
+    sel = torch.rand(sum(lens), 2, 1, generator=gen)
+    g = torch.where(sel < 0.1, torch.full_like(g, -1e4), torch.where(sel > 0.9, torch.zeros_like(g), g))
+    o, hT = kda.chunk_fwd(dev["q"], dev["k"], dev["v"], g.cuda(), dev["beta"], dev["h0"],
+                          dev["cu_seqlens"], flags=kda.UNBOUNDED_GATE)
+    o_ref, h_ref = oracle.recurrence(inp["q"], inp["k"], inp["v"], g, inp["beta"], inp["h0"],
+                                     inp["cu_seqlens"])
+    assert_close(o, o_ref, torch.float32, "o extremes")
+    assert_close(hT, h_ref, torch.float32, "hT extremes")
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_unbounded_mode_on_bounded_gate(kda, dtype):
+    """The range-robust mode on ordinary bounded decays gives the same answer."""
+    inp, g, dev = _inputs([5, 0, 70, 129, 300], H=2, dtype=dtype, seed=95)
+    o, hT = kda.chunk_fwd(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["h0"],
+                          dev["cu_seqlens"], flags=kda.UNBOUNDED_GATE)
+    o_ref, h_ref = oracle.recurrence(inp["q"], inp["k"], inp["v"], g, inp["beta"], inp["h0"],
+                                     inp["cu_seqlens"])
+    assert_close(o, o_ref, dtype, "o robust on bounded")
+    assert_close(hT, h_ref, dtype, "hT robust on bounded")
+
+
+def test_scalar_gate_gated_deltanet(kda):
+    """Gated DeltaNet (one decay per token and head, "Kimi K3 notes", section
+    "Kimi Delta Attention": alpha_t (I - b k k^T) S + b k v^T) is KDA with g constant
+    over the channels; bf16 tensor-core path against the oracle."""
+    lens = [300, 64, 5]
+    inp, g, dev = _inputs(lens, H=2, dtype=torch.bfloat16, seed=97)
+    gs = g[..., :1].expand_as(g).contiguous()
+    o, hT = kda.chunk_fwd(dev["q"], dev["k"], dev["v"], gs.cuda(), dev["beta"], dev["h0"],
+                          dev["cu_seqlens"])
+    o_ref, h_ref = oracle.recurrence(inp["q"], inp["k"], inp["v"], gs, inp["beta"], inp["h0"],
+                                     inp["cu_seqlens"])
+    assert_close(o, o_ref, torch.bfloat16, "o GDN")
+    assert_close(hT, h_ref, torch.bfloat16, "hT GDN")
+
+
+def test_each_path_launches_only_its_own_kernels(kda):
+    """The bf16 entry runs the plan and the tensor-core kernels only; the fp32-core
+    flag runs the CUDA-core kernels only (a second path on the same workspace would
+    write past it); the fused entry with an output gate adds exactly that kernel."""
+    inp, g, dev = _inputs([300, 77], H=2, dtype=torch.bfloat16, seed=99)
+    args = (dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["h0"], dev["cu_seqlens"])
+
+    def launched(fn):
+        torch.cuda.synchronize()
+        kda.profile_enable(True)
+        fn()
+        torch.cuda.synchronize()
+        names = set(kda.profile_collect())
+        kda.profile_enable(False)
+        return names
+
+    tc = launched(lambda: kda.chunk_fwd(*args, flags=kda.SEQUENTIAL))
+    assert tc == {"kda_plan", "kda_tc_prep", "kda_tc_chain"}, tc
+    simt = launched(lambda: kda.chunk_fwd(*args, flags=kda.FP32_CORES))
+    assert simt == {"kda_plan", "kda_simt_prep", "kda_simt_chain"}, simt
+    gz = torch.randn_like(dev["v"].float()).to(torch.bfloat16)
+    fused = launched(lambda: kda.chunk_fwd_fused(dev["q"], dev["k"], dev["v"], dev["beta"],
+                                                 dev["h0"], dev["cu_seqlens"], g=dev["g"],
+                                                 out_gate=gz, flags=kda.SEQUENTIAL))
+    assert fused == {"kda_plan", "kda_tc_prep", "kda_tc_chain", "kda_output_gate"}, fused

@@ -130,3 +130,26 @@ def test_fused_full_size_sampled(kda):
         y_ref = oracle.output_gate(o_ref, sl(gz), wt, 1e-6)
         assert_close_gated(sl(o), y_ref, o_ref, sl(gz), wt, 1e-6, f"y head {h}")
         assert_close(hT[:, h:h + 1], h_ref, torch.bfloat16, f"hT head {h}")
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_output_gate_kernel(kda, dtype):
+    """kda_output_gate on given outputs (row scales 1e-3 .. 10) against the oracle:
+    fp32 rel_L2 <= 1e-5; bf16 elementwise |y - y_ref| <= 2^-8 |y_ref| (one bf16
+    rounding of y after fp32 arithmetic on the given bf16 inputs); in place too."""
+    gen = torch.Generator().manual_seed(87)
+    NT, H = 300, 3
+    o = torch.randn(NT, H, 128, generator=gen) * torch.logspace(-3, 1, NT).view(NT, 1, 1)
+    x = 3.0 * torch.randn(NT, H, 128, generator=gen)
+    w = 0.5 + torch.rand(128, generator=gen)
+    o, x = o.to(dtype), x.to(dtype)
+    y = kda.output_gate(o.cuda(), x.cuda(), w.cuda(), 1e-6)
+    ref = oracle.output_gate(o, x, w, 1e-6)
+    if dtype == torch.float32:
+        assert_close(y, ref, torch.float32, "output gate f32")
+    else:
+        err = np.abs(y.cpu().double().numpy() - ref)
+        assert np.all(err <= 2.0 ** -8 * np.abs(ref) + 1e-30), float(np.max(err / np.abs(ref)))
+    oc = o.cuda()
+    kda.output_gate(oc, x.cuda(), w.cuda(), 1e-6, out=oc)
+    assert torch.equal(oc, y)

@@ -30,6 +30,19 @@ def test_gate_matches_oracle(kda, dtype):
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_gate_softplus_matches_oracle(kda, dtype):
+    """The unbounded gate, z ~ N(0, 9) and A in [-1, 1]: relative error <= 1e-6
+    elementwise (fp32 arithmetic), g far below -5 where z is large."""
+    w = workloads.custom([300], H=3, dtype=dtype, z_std=3.0, A_range=1.0, seed=43)
+    inp = workloads.make_inputs(w, "cpu")
+    g = kda.gate_softplus(inp["z"].cuda(), inp["A"].cuda())
+    ref = oracle.gate_softplus(inp["z"], inp["A"])
+    rel = np.max(np.abs(to64(g) - ref) / np.abs(ref))
+    assert rel <= 1e-6, rel
+    assert float(g.max()) < 0.0 and float(g.min()) < -5.0
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_gate_chunk_cumsum_matches_oracle(kda, dtype):
     lens = [100, 0, 200, 1, 64, 65]
     w = workloads.custom(lens, H=2, dtype=dtype, seed=42)

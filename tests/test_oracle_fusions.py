@@ -1,10 +1,13 @@
-"""Pins for the oracle's fused prologue / epilogue pieces (CPU only).
+"""Pins for the oracle's fused prologue / epilogue pieces and the unbounded gate
+(CPU only).
 
 * ``oracle.l2_normalize`` -- the L2Norm on the q and k branches ("Kimi K3:
   architecture, training and inference systems", section 3.2), with the
   caller's epsilon inside the square root.
 * ``oracle.output_gate`` -- head-wise RMSNorm of the KDA output times the
   Sigmoid gate ("Kimi K3 technical report review", section 3.3, Eq. 6).
+* ``oracle.gate_softplus`` -- the unbounded gate -exp(A) Softplus(z) the bounded
+  one replaced (same review, section 3.2), and the recurrence under it.
 
 Every expected value below is worked out by hand from those definitions.  Each
 pin takes the implementation as an argument so that the planted mistakes at the
@@ -147,3 +150,65 @@ def test_output_gate_mutant_trips_a_pin(mutant):
         except AssertionError:
             tripped += 1
     assert tripped > 0
+
+
+# ------------------------------------------------------------ unbounded gate pins
+def sp_pin_zero(f):
+    """Softplus(0) = ln 2: g = -ln 2 for A = 0 and -2 ln 2 for A = ln 2."""
+    z = np.zeros((1, 2, 1))
+    np.testing.assert_allclose(f(z, np.array([0.0, math.log(2.0)])),
+                               [[[-math.log(2.0)], [-2 * math.log(2.0)]]], rtol=1e-14)
+
+
+def sp_pin_tails(f):
+    """Softplus(x) = x + log(1 + e^-x) -> x for large x (no overflow at 1000) and
+    log(1 + e^x) = e^x (1 - e^x / 2 + ...) for very negative x."""
+    z = np.array([[[1000.0, 30.0, -30.0]]])
+    want = [[[-1000.0, -(30.0 + math.log1p(math.exp(-30.0))), -math.log1p(math.exp(-30.0))]]]
+    np.testing.assert_allclose(f(z, np.array([0.0])), want, rtol=1e-14)
+
+
+def sp_pin_unbounded_monotone(f):
+    """g is below any bound for large z and decreasing in z."""
+    z = np.linspace(-5, 200, 50).reshape(50, 1, 1)
+    g = f(z, np.array([0.5]))[:, 0, 0]
+    assert g[-1] < -300 and np.all(np.diff(g) < 0)
+
+
+SP_PINS = [sp_pin_zero, sp_pin_tails, sp_pin_unbounded_monotone]
+
+
+@pytest.mark.parametrize("pin", SP_PINS, ids=lambda p: p.__name__)
+def test_gate_softplus_pin(pin):
+    pin(oracle.gate_softplus)
+
+
+@pytest.mark.parametrize("mutant", [
+    lambda z, A: -np.exp(A)[None, :, None] * np.log1p(np.maximum(z, -0.999)),  # log(1 + z)
+    lambda z, A: -A[None, :, None] * np.logaddexp(0.0, z),                   # A without exp
+    lambda z, A: -np.exp(A)[None, :, None] * np.logaddexp(0.0, -z),          # sign of z
+], ids=["log1p_of_z", "A_without_exp", "z_sign"])
+def test_gate_softplus_mutant_trips_a_pin(mutant):
+    tripped = 0
+    for pin in SP_PINS:
+        try:
+            pin(mutant)
+        except (AssertionError, FloatingPointError):
+            tripped += 1
+    assert tripped > 0
+
+
+def test_recurrence_full_forgetting_closed_form(oracle_lib):
+    """g = -10^4 (alpha = e^-10000 = 0 in fp64): the state carries nothing between
+    tokens, so S_t = b_t k_t v_t^T and o_t = b_t (q_t . k_t) v_t."""
+    rng = np.random.default_rng(5)
+    T, H, dk, dv = 7, 2, 8, 5
+    q, k = rng.standard_normal((T, H, dk)), rng.standard_normal((T, H, dk))
+    v, b = rng.standard_normal((T, H, dv)), rng.uniform(0, 1, (T, H))
+    g = np.full((T, H, dk), -1e4)
+    h0 = rng.standard_normal((1, H, dv, dk))
+    o, hT = oracle.recurrence(q, k, v, g, b, h0, lib=oracle_lib)
+    want = b[..., None] * np.sum(q * k, axis=-1)[..., None] * v
+    np.testing.assert_allclose(o, want, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(hT[0], b[-1][:, None, None] * v[-1][:, :, None] * k[-1][:, None, :],
+                               rtol=1e-12, atol=1e-14)
