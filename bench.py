@@ -1,8 +1,10 @@
 """Benchmark of the KDA forward on one GB300 (or N independent replicas).
 
 One step = one pass of the whole prefill hot path over the one-layer K3
-workload (B=1, T=8192, H=96, dk=dv=128, bf16 q/k/v/beta, fp32 state and h0):
-  kda_gate (z -> g)  then  kda_chunk_fwd (q, k, v, g, beta, h0 -> o, hT).
+workload (B=1, T=8192, H=96, dk=dv=128, bf16 q/k/v/z/beta, fp32 state and h0):
+  kda_chunk_fwd_gated (q, k, v, z, beta, h0 -> o, hT; the gate formed inside)
+or, with --path separate, kda_gate (z -> g) then kda_chunk_fwd; the other path is
+timed beside it.
 Inputs are resident in HBM when the timed region starts and are larger than
 L2 (z, q, k, v are 201 MB each), so no L2 flush is needed between steps.
 
@@ -14,7 +16,8 @@ The JSON line also carries
     achieved HBM GB/s against the same peak;
   * e2e -- the same prefill metric through the public API with host buffers
     (pinned host -> device copies of the step's inputs, device -> host copy of
-    o and hT inside the timed region);
+    o and hT inside the timed region; device buffers are double-buffered so that
+    one step's upload overlaps the previous step's compute and download);
   * cpu_baseline -- the fp64 oracle on the host cores over a bounded sample.
 
 ``--impl reference`` times the oracle alone (the reference arm of this build).
@@ -515,30 +518,46 @@ def run_gpu(args):
            and k in ("z", "q", "k", "v", "beta", "A", "h0", "cu_seqlens")}
     o_host = torch.empty(NT, H, D, dtype=torch.bfloat16).pin_memory()
     hT_host = torch.empty(1, H, D, D, dtype=torch.float32).pin_memory()
-    dbuf = {k: torch.empty_like(v, device=dev) for k, v in pin.items()}
+    # two sets of device inputs and outputs: step i uses set i % 2, so the upload of
+    # step i + 1 runs while step i computes and downloads (each step still copies
+    # its own inputs in and its own results out inside the timed region; the
+    # compute stream is idle when the region opens, so no copy precedes its start)
+    dsets = [{k: torch.empty_like(v, device=dev) for k, v in pin.items()} for _ in range(2)]
+    osets = [(torch.empty(NT, H, D, dtype=torch.bfloat16, device=dev),
+              torch.empty(1, H, D, D, dtype=torch.float32, device=dev)) for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in pin.values())
     d2h = o_host.numel() * 2 + hT_host.numel() * 4
 
     # the large inputs are copied in slices on four copy streams (several copies in
-    # flight); a slice's copy waits until the previous step has consumed its buffer
+    # flight); the results go back on their own stream
     copy_streams = [torch.cuda.Stream(dev) for _ in range(4)]
-    slices = []
-    for k_, v_ in pin.items():
-        n_sl = 4 if v_.numel() * v_.element_size() > (64 << 20) else 1
-        for part in torch.tensor_split(torch.arange(v_.shape[0]), n_sl):
-            if part.numel():
-                a, b = int(part[0]), int(part[-1]) + 1
-                slices.append((dbuf[k_][a:b], v_[a:b]))
+    d2h_stream = torch.cuda.Stream(dev)
+
+    def slices_of(dbuf):
+        out = []
+        for k_, v_ in pin.items():
+            n_sl = 4 if v_.numel() * v_.element_size() > (64 << 20) else 1
+            for part in torch.tensor_split(torch.arange(v_.shape[0]), n_sl):
+                if part.numel():
+                    a_, b_ = int(part[0]), int(part[-1]) + 1
+                    out.append((dbuf[k_][a_:b_], v_[a_:b_]))
+        return out
+
+    slice_sets = [slices_of(d_) for d_ in dsets]
+    freed = [None, None]  # per set: the compute that last read it
+    n_e2e = [0]
 
     def e2e_step():
-        # the copies start after everything already on the timed stream: the timing
-        # start and the previous step, whose kernels read these buffers
-        step_begin = torch.cuda.Event()
-        step_begin.record(stream)
+        i = n_e2e[0]
+        n_e2e[0] += 1
+        sid = i % 2
+        dbuf, (o_d, hT_d) = dsets[sid], osets[sid]
+        # upload: may start once the step that last used this set has computed
         done = []
-        for i, (dst, src) in enumerate(slices):
-            cs = copy_streams[i % len(copy_streams)]
-            cs.wait_event(step_begin)
+        for j, (dst, src) in enumerate(slice_sets[sid]):
+            cs = copy_streams[j % len(copy_streams)]
+            if freed[sid] is not None:
+                cs.wait_event(freed[sid])
             with torch.cuda.stream(cs):
                 dst.copy_(src, non_blocking=True)
         for cs in copy_streams:
@@ -549,14 +568,24 @@ def run_gpu(args):
             stream.wait_event(ev)
         if fused:
             kda.chunk_fwd_gated(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["z"], dbuf["A"],
-                                dbuf["beta"], dbuf["h0"], dbuf["cu_seqlens"], workspace=ws, out=o,
-                                final_state_out=hT)
+                                dbuf["beta"], dbuf["h0"], dbuf["cu_seqlens"], workspace=ws,
+                                out=o_d, final_state_out=hT_d)
         else:
             kda.gate(dbuf["z"], dbuf["A"], out=g)
             kda.chunk_fwd(dbuf["q"], dbuf["k"], dbuf["v"], g, dbuf["beta"], dbuf["h0"],
-                          dbuf["cu_seqlens"], workspace=ws, out=o, final_state_out=hT)
-        o_host.copy_(o, non_blocking=True)
-        hT_host.copy_(hT, non_blocking=True)
+                          dbuf["cu_seqlens"], workspace=ws, out=o_d, final_state_out=hT_d)
+        computed = torch.cuda.Event()
+        computed.record(stream)
+        freed[sid] = computed
+        # download this step's results; the next step's compute (and the end of the
+        # timed region) waits for it
+        d2h_stream.wait_event(computed)
+        with torch.cuda.stream(d2h_stream):
+            o_host.copy_(o_d, non_blocking=True)
+            hT_host.copy_(hT_d, non_blocking=True)
+        fetched = torch.cuda.Event()
+        fetched.record(d2h_stream)
+        stream.wait_event(fetched)
 
     ms_e2e = timed(e2e_step, max(3, args.steps // 4), max(3, args.warmup))
     clocks.stop()
