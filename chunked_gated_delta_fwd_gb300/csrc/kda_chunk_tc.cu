@@ -38,9 +38,11 @@
 // copy (the A operand of MMA1), two D1 buffers and two Vt^T buffers:
 //   MMA1: D1 = S^T [W; Gamma*Q]^T      -> (W S)^T | (Gamma*Q S)^T
 //   MMA2: S^T += Vt^T Kt (after S^T *= gamma_C);  D1[:, 64:] += Vt^T A_qk^T
-// where Vt^T = U^T - (W S)^T is formed by eight epilogue warps, three of whose
-// threads issue the MMAs after named barriers; four store warps write o, and a
-// copy warp streams the tiles through a three-stage ring of bulk copies.
+// where Vt^T = U^T - (W S)^T is formed by eight epilogue warps, two of whose
+// threads issue the serial MMAs ((W S)^T, the state update) after named barriers;
+// an output warp issues the (Gamma*Q S)^T half and the O product, four store warps
+// write o, and a copy warp streams the tiles through a three-stage ring of bulk
+// copies.
 #include "kda_internal.cuh"
 #include "kda_sm100.cuh"
 
@@ -828,7 +830,8 @@ constexpr uint32_t kC_Smem = kC_bars + 256 + 1024;
 constexpr int kEpi = 256;    // epilogue warps 0-7: (TMEM lane, column half)
 constexpr int kStore = 128;  // store warps 8-11: TMEM lane = value row, all 64 tokens
 constexpr int kCopyWarp = (kEpi + kStore) / 32;  // warp 12: tile copies
-constexpr int kChainThreads = kEpi + kStore + 32;
+constexpr int kOutWarp = kCopyWarp + 1;            // warp 13: the output MMAs
+constexpr int kChainThreads = kEpi + kStore + 64;
 
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int* err,
                                               volatile int* abort_flag) {
@@ -932,12 +935,14 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kC_bars);
   // bars: 0..2 = full[stage], 3..5 = empty[stage] (every MMA of its chunk done),
   //       6 = MMA1 done, 7 = S update done, 8,9 = O of D1 buffer b final,
-  //       10,11 = D1 buffer b read out, 12..14 = drain of MMA-issuing thread i (abort path),
-  //       15 = the (Gamma Q S)^T half of MMA1 done (it reads the bf16 S^T copy)
+  //       10,11 = D1 buffer b read out, 12..14 = drain of MMA-issuing thread 0, the
+  //       output warp, thread 64 (abort path), 15 = the (Gamma Q S)^T half of MMA1
+  //       done (it reads the bf16 S^T copy), 16 = (W S)^T issued, 17 = S update issued
   const uint32_t bar_full0 = smem_addr(&bars[0]), bar_empty0 = smem_addr(&bars[3]);
   const uint32_t bar_m1 = smem_addr(&bars[6]), bar_m2 = smem_addr(&bars[7]);
   const uint32_t bar_o0 = smem_addr(&bars[8]), bar_f0 = smem_addr(&bars[10]);
   const uint32_t bar_dr = smem_addr(&bars[12]), bar_q = smem_addr(&bars[15]);
+  const uint32_t bar_wi = smem_addr(&bars[16]), bar_2i = smem_addr(&bars[17]);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kC_bars + 192);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kC_bars + 200);
   const int t = threadIdx.x, warp = t >> 5;
@@ -955,6 +960,8 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     }
     for (int i = 0; i < 3; ++i) mbar_init(bar_dr + 8 * i, 1);
     mbar_init(bar_q, 1);
+    mbar_init(bar_wi, 1);
+    mbar_init(bar_2i, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -992,6 +999,44 @@ __global__ void __launch_bounds__(kChainThreads, 1)
           mbar_wait(bar_full0 + 8 * (jj % kStages), (jj / kStages) & 1, nullptr);
       }
     }
+  } else if (warp == kOutWarp) {
+    // ------------------------------------------- output MMAs (one thread, off the
+    // serial path): (Gamma Q S)^T once the (W S)^T half is in the tensor pipe and the
+    // D1 buffer's outputs have been read (chunk j - 2); O^T += Vt^T A_qk^T once the
+    // state update is in the pipe.  No epilogue warp stalls on these issues.
+    if ((t & 31) == 0) {
+      const uint32_t id1 = idesc_bf16_mn(128, 64, 0, 1);
+      const uint32_t id2a = idesc_bf16_mn(128, 64, 0, 0);
+      bool any_mma = false;
+      for (int j = 0; j < nch; ++j) {
+        const int s = j % kStages;
+        const uint32_t sts = sbase + s * kStageBytes;
+        const uint32_t d1 = tmem + 128 + 128 * (j & 1);
+        if (!wait_or_abort(bar_wi, j & 1, err, abort_flag)) break;
+        if (j >= 2 && !wait_or_abort(bar_f0 + 8 * (j & 1), ((j - 2) >> 1) & 1, err, abort_flag))
+          break;
+        tc_fence_after();
+        const uint64_t bq = mnmajor_desc(sts + kQ, 1024, 0);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_bf16_ta(d1 + 64, tmem + kT_SB + 8 * ks, desc_advance(bq, ks * 2048), id1, ks > 0);
+        mma_commit(bar_q);
+        any_mma = true;
+        if (!wait_or_abort(bar_2i, j & 1, err, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t vt = tmem + kT_VT + 32 * (j & 1);
+        const uint64_t ba = kmajor_desc(sts + kAQ, 64, 0);
+#pragma unroll
+        for (int ks = 0; ks < C / 16; ++ks)
+          mma_bf16_ta(d1 + 64, vt + 8 * ks, desc_advance(ba, ks * 32), id2a, 1u);
+        mma_commit(bar_o0 + 8 * (j & 1));  // o of chunk j final
+        mma_commit(bar_empty0 + 8 * s);
+      }
+      if (*abort_flag && any_mma) {  // drain MMAs in flight
+        mma_commit(bar_dr + 8);
+        mbar_wait(bar_dr + 8, 0, nullptr);
+      }
+    }
   } else if (warp < kEpi / 32) {
     // ------------------------- epilogue warps: TMEM lane = dv, ch = column half
     const int lane = t & 127, ch = t >> 7;
@@ -1015,13 +1060,13 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       }
       tmem_wait_st();
     }
-    // Thread 0 issues the MMAs as soon as the epilogue warps meet at a named
-    // barrier (measured faster than handing off to a separate MMA warp, through
-    // an mbarrier or a named barrier).  Barriers that end a wait reduce the
-    // threads' results with bar.red.and, so an expired wait stops every epilogue
-    // thread at the same point.
-    const uint32_t id1 = idesc_bf16_mn(128, 64, 0, 1);    // S^T x W^T or S^T x (Gamma Q)^T
-    const uint32_t id2a = idesc_bf16_mn(128, 64, 0, 0);   // Vt^T x A_qk^T (K-major B)
+    // Threads 0 and 64 issue the serial MMAs as soon as the epilogue warps meet at
+    // a named barrier (measured faster than handing them to a separate MMA warp);
+    // the output MMAs, which only o needs, go to the output warp, so that no
+    // epilogue warp stalls on them (an issuing thread stalls while the tensor pipe
+    // drains).  Barriers that end a wait reduce the threads' results with
+    // bar.red.and, so an expired wait stops every epilogue thread at the same point.
+    const uint32_t id1 = idesc_bf16_mn(128, 64, 0, 1);    // S^T x W^T
     const uint32_t id2b = idesc_bf16_mn(128, 128, 0, 0);  // Vt^T x Kt^T (K-major B)
     bool any_mma = false;
     bool alive = true;
@@ -1057,11 +1102,10 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       named_sync(1, kEpi);
-      // MMA1 in two N = 64 halves issued by two threads (an issuing thread stalls
-      // while the tensor pipe drains, so no single warp carries all of it): thread 0
-      // the (W S)^T half that the Vt pass waits for, thread 32 the (Gamma Q S)^T
-      // half, which only the output needs.  A = bf16 S^T from TMEM; the descriptor
-      // of K step ks is the step-0 descriptor with its start advanced.
+      // MMA1 in two N = 64 halves: thread 0 the (W S)^T half that the Vt pass waits
+      // for, the output warp the (Gamma Q S)^T half, which only the output needs.
+      // A = bf16 S^T from TMEM; the descriptor of K step ks is the step-0
+      // descriptor with its start advanced.
       const uint32_t d1 = tmem + 128 + 128 * (j & 1);
       if (t == 0) {
         tc_fence_after();
@@ -1071,18 +1115,9 @@ __global__ void __launch_bounds__(kChainThreads, 1)
           mma_bf16_ta(d1, tmem + kT_SB + 8 * ks, desc_advance(bw, ks * 2048), id1, ks > 0);
         mma_commit(bar_m1);
         mma_commit(bar_empty0 + 8 * s);
+        tc_fence_before();
+        mbar_arrive(bar_wi);  // the output warp may issue the (Gamma Q S)^T half
         any_mma = true;
-      } else if (t == 32) {
-        tc_fence_after();
-        // the output half of D1 buffer j&1 must have been read out (chunk j-2)
-        if (j < 2 || wait_or_abort(bar_f0 + 8 * (j & 1), ((j - 2) >> 1) & 1, err, abort_flag)) {
-          const uint64_t bq = mnmajor_desc(sts + kQ, 1024, 0);
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks)
-            mma_bf16_ta(d1 + 64, tmem + kT_SB + 8 * ks, desc_advance(bq, ks * 2048), id1, ks > 0);
-          mma_commit(bar_q);
-          any_mma = true;
-        }
       }
       // the scaled state is ordered before MMA2 by the barrier after E1
 #pragma unroll
@@ -1127,18 +1162,12 @@ __global__ void __launch_bounds__(kChainThreads, 1)
           mma_bf16_ta(tmem + 0, vt + 8 * ks, desc_advance(bk, ks * 32), id2b, 1u);
         mma_commit(bar_m2);
         mma_commit(bar_empty0 + 8 * s);
+        tc_fence_before();
+        mbar_arrive(bar_2i);  // the output warp may issue O
         any_mma = true;
-      } else if (t == 32) {  // O^T += Vt^T A_qk^T onto (Gamma Q S)^T, after this thread's half
-        tc_fence_after();
-        const uint64_t ba = kmajor_desc(sts + kAQ, 64, 0);
-#pragma unroll
-        for (int ks = 0; ks < C / 16; ++ks)
-          mma_bf16_ta(d1 + 64, vt + 8 * ks, desc_advance(ba, ks * 32), id2a, 1u);
-        mma_commit(bar_o0 + 8 * (j & 1));  // o of chunk j final
-        mma_commit(bar_empty0 + 8 * s);
       }
     }
-    if ((t == 0 || t == 32 || t == 64) && *abort_flag && any_mma) {  // drain MMAs in flight
+    if ((t == 0 || t == 64) && *abort_flag && any_mma) {  // drain MMAs in flight
       mma_commit(bar_dr + 8 * (t >> 5));
       mbar_wait(bar_dr + 8 * (t >> 5), 0, nullptr);
     }
