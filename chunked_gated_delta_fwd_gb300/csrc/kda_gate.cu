@@ -126,8 +126,10 @@ cudaError_t launch_gate(const void* z, int z_bf16, const float* A, float g_min, 
 
 namespace {
 
-// Output gate, one warp per (token, head): lane l holds channels 4l .. 4l + 3 of o
-// and of the gate logits; the sum of squares meets by a warp all-reduce.
+// Output gate, a half warp per (token, head): lane l of the half holds channels
+// 8l .. 8l + 7 of o and of the gate logits (16-byte accesses for bf16); the sum of
+// squares meets by a half-warp all-reduce, and each warp keeps four token-heads
+// in flight.
 //   y = Sigmoid(x) * w * o / sqrt(mean(o^2) + eps)
 // ("Kimi K3 technical report review", section 3.3, Eq. 6, without W_o and W_g)
 template <typename T>
@@ -135,26 +137,43 @@ __global__ void __launch_bounds__(256) out_gate_kernel(const T* __restrict__ o,
                                                        const T* __restrict__ x,
                                                        const float* __restrict__ w, float eps,
                                                        T* y, int64_t n_rows) {
-  const int lane = threadIdx.x & 31;
+  const int hl = threadIdx.x & 15, half = (threadIdx.x >> 4) & 1;
+  const int64_t warp_g = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5);
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  float wv[4] = {1.f, 1.f, 1.f, 1.f};
-  if (w) {
-    const float4 w4 = __ldg(reinterpret_cast<const float4*>(w) + lane);
-    wv[0] = w4.x; wv[1] = w4.y; wv[2] = w4.z; wv[3] = w4.w;
-  }
-  for (int64_t row = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5); row < n_rows;
-       row += nwarps) {
-    float ov[4], xv[4];
-    load4(o + row * kD + 4 * lane, ov);
-    load4(x + row * kD + 4 * lane, xv);
-    float ss = ov[0] * ov[0] + ov[1] * ov[1] + ov[2] * ov[2] + ov[3] * ov[3];
+  float wv[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
+  if (w) load8(w + 8 * hl, wv);
+  // warp g takes rows 2g + half + 2 nwarps (2i + k): every row once; the loop and
+  // the shuffles are uniform over the warp, validity only gates loads and stores
+  for (int64_t base = 2 * warp_g; base < n_rows; base += 4 * nwarps) {
+    float ov[2][8], xv[2][8];
 #pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
-    const float r = rsqrtf(ss * (1.f / kD) + eps);
-    float yv[4];
+    for (int k = 0; k < 2; ++k) {
+      const int64_t row = base + k * 2 * nwarps + half;
+      if (row < n_rows) {
+        load8(o + row * kD + 8 * hl, ov[k]);
+        load8(x + row * kD + 8 * hl, xv[k]);
+      } else {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) yv[i] = ov[i] * r * wv[i] / (1.f + expf(-xv[i]));
-    store4(y + row * kD + 4 * lane, yv);
+        for (int i = 0; i < 8; ++i) ov[k][i] = xv[k][i] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      float ss = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss = fmaf(ov[k][i], ov[k][i], ss);
+#pragma unroll
+      for (int m = 8; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+      const float r = rsqrtf(ss * (1.f / kD) + eps);
+      const int64_t row = base + k * 2 * nwarps + half;
+      if (row < n_rows) {
+        float yv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          yv[i] = __fdividef(ov[k][i] * r * wv[i], 1.f + __expf(-xv[k][i]));
+        store8(y + row * kD + 8 * hl, yv);
+      }
+    }
   }
 }
 
@@ -164,7 +183,7 @@ cudaError_t launch_output_gate(const void* o, int bf16, const void* x, const flo
                                void* y, int64_t n_tokens, int H, cudaStream_t s) {
   const int64_t rows = n_tokens * H;
   if (rows == 0) return cudaSuccess;
-  const int grid = grid_for(rows * 32, 256);
+  const int grid = grid_for(rows * 8, 256);
   ProfScope prof_scope("kda_output_gate", s);
   if (bf16)
     out_gate_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(o),

@@ -69,6 +69,20 @@ __device__ __forceinline__ void load4(const __nv_bfloat16* p, float* out) {
   out[2] = __uint_as_float(u.y << 16);
   out[3] = __uint_as_float(u.y & 0xffff0000u);
 }
+// Stores 8 consecutive elements from fp32 (32-byte aligned for fp32, 16-byte for bf16).
+__device__ __forceinline__ void store8(float* p, const float* v) {
+  reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+  reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+__device__ __forceinline__ void store8(__nv_bfloat16* p, const float* v) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    w[i] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+  *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+}
 // Stores 4 consecutive elements from fp32 (16-byte aligned for fp32, 8-byte for bf16).
 __device__ __forceinline__ void store4(float* p, const float* v) {
   *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
