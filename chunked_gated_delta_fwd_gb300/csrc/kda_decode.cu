@@ -159,27 +159,50 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_multi_kernel(
         p[i] = kk.x * s[i].x + kk.y * s[i].y + kk.z * s[i].z + kk.w * s[i].w;
         r[i] = qq.x * s[i].x + qq.y * s[i].y + qq.z * s[i].z + qq.w * s[i].w;
       }
+      // Halving reduce-scatter of the 8 rows' partial sums over the warp (9 shuffles
+      // each instead of 40): lane l ends with the full k.s and q.s of row
+      // R(l) = 4 b4 + 2 b3 + b2 (b = bits of l).  Every lane then gathers all 8 k.s
+      // (the erase needs them); q.s stays with the lanes that store o.
+      {
+        const bool u4 = (lane & 16) != 0;
 #pragma unroll
-      for (int o_ = 16; o_ > 0; o_ >>= 1) {
-#pragma unroll
-        for (int i = 0; i < kRowsPerIter; ++i) {
-          p[i] += __shfl_xor_sync(0xffffffffu, p[i], o_);
-          r[i] += __shfl_xor_sync(0xffffffffu, r[i], o_);
+        for (int i = 0; i < 4; ++i) {
+          p[i] = (u4 ? p[4 + i] : p[i]) + __shfl_xor_sync(0xffffffffu, u4 ? p[i] : p[4 + i], 16);
+          r[i] = (u4 ? r[4 + i] : r[i]) + __shfl_xor_sync(0xffffffffu, u4 ? r[i] : r[4 + i], 16);
         }
+        const bool u3 = (lane & 8) != 0;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          p[i] = (u3 ? p[2 + i] : p[i]) + __shfl_xor_sync(0xffffffffu, u3 ? p[i] : p[2 + i], 8);
+          r[i] = (u3 ? r[2 + i] : r[i]) + __shfl_xor_sync(0xffffffffu, u3 ? r[i] : r[2 + i], 8);
+        }
+        const bool u2 = (lane & 4) != 0;
+        p[0] = (u2 ? p[1] : p[0]) + __shfl_xor_sync(0xffffffffu, u2 ? p[0] : p[1], 4);
+        r[0] = (u2 ? r[1] : r[0]) + __shfl_xor_sync(0xffffffffu, u2 ? r[0] : r[1], 4);
+        p[0] += __shfl_xor_sync(0xffffffffu, p[0], 2);
+        r[0] += __shfl_xor_sync(0xffffffffu, r[0], 2);
+        p[0] += __shfl_xor_sync(0xffffffffu, p[0], 1);
+        r[0] += __shfl_xor_sync(0xffffffffu, r[0], 1);
       }
+      const int Rl = 4 * ((lane >> 4) & 1) + 2 * ((lane >> 3) & 1) + ((lane >> 2) & 1);
+      const float pR = p[0], rR = r[0];  // row Rl of this block
+      float pa[kRowsPerIter];
+#pragma unroll
+      for (int i = 0; i < kRowsPerIter; ++i)  // row i sits on lane 16 (i>>2) + 8 ((i>>1)&1) + 4 (i&1)
+        pa[i] = __shfl_sync(0xffffffffu, pR, 16 * (i >> 2) + 8 * ((i >> 1) & 1) + 4 * (i & 1));
       const float b = tb[t], qk = tqk[t];
-      float o_val = 0.f;
 #pragma unroll
       for (int i = 0; i < kRowsPerIter; ++i) {
-        const float u = b * (tv[t][row0 + r0 + i] - p[i]);
+        const float u = b * (tv[t][row0 + r0 + i] - pa[i]);
         s[i].x = fmaf(u, kk.x, s[i].x);
         s[i].y = fmaf(u, kk.y, s[i].y);
         s[i].z = fmaf(u, kk.z, s[i].z);
         s[i].w = fmaf(u, kk.w, s[i].w);
-        if (lane == i) o_val = fmaf(u, qk, r[i]);
       }
-      if (o && lane < kRowsPerIter)
-        o[(((int64_t)n * Tn + t) * H + h) * kD + row0 + r0 + lane] = from_f32<T>(o_val);
+      if (o && (lane & 3) == 0) {
+        const float uR = b * (tv[t][row0 + r0 + Rl] - pR);
+        o[(((int64_t)n * Tn + t) * H + h) * kD + row0 + r0 + Rl] = from_f32<T>(fmaf(uR, qk, rR));
+      }
       if (t + 1 == adv) {
 #pragma unroll
         for (int i = 0; i < kRowsPerIter; ++i) Srow[(r0 + i) * (kD / 4)] = s[i];
