@@ -66,25 +66,49 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(
       p[i] = kv[0] * s[i].x + kv[1] * s[i].y + kv[2] * s[i].z + kv[3] * s[i].w;
       r[i] = qv[0] * s[i].x + qv[1] * s[i].y + qv[2] * s[i].z + qv[3] * s[i].w;
     }
+    // reduce-scatter of the 8 rows' k.s and q.s (see decode_multi_kernel): lane l
+    // ends with row R(l) = 4 b4 + 2 b3 + b2; k.s is gathered back to every lane
+    {
+      const bool u4 = (lane & 16) != 0;
 #pragma unroll
-    for (int o_ = 16; o_ > 0; o_ >>= 1) {
-#pragma unroll
-      for (int i = 0; i < kRowsPerIter; ++i) {
-        p[i] += __shfl_xor_sync(0xffffffffu, p[i], o_);
-        r[i] += __shfl_xor_sync(0xffffffffu, r[i], o_);
+      for (int i = 0; i < 4; ++i) {
+        p[i] = (u4 ? p[4 + i] : p[i]) + __shfl_xor_sync(0xffffffffu, u4 ? p[i] : p[4 + i], 16);
+        r[i] = (u4 ? r[4 + i] : r[i]) + __shfl_xor_sync(0xffffffffu, u4 ? r[i] : r[4 + i], 16);
       }
+      const bool u3 = (lane & 8) != 0;
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        p[i] = (u3 ? p[2 + i] : p[i]) + __shfl_xor_sync(0xffffffffu, u3 ? p[i] : p[2 + i], 8);
+        r[i] = (u3 ? r[2 + i] : r[i]) + __shfl_xor_sync(0xffffffffu, u3 ? r[i] : r[2 + i], 8);
+      }
+      const bool u2 = (lane & 4) != 0;
+      p[0] = (u2 ? p[1] : p[0]) + __shfl_xor_sync(0xffffffffu, u2 ? p[0] : p[1], 4);
+      r[0] = (u2 ? r[1] : r[0]) + __shfl_xor_sync(0xffffffffu, u2 ? r[0] : r[1], 4);
+      p[0] += __shfl_xor_sync(0xffffffffu, p[0], 2);
+      r[0] += __shfl_xor_sync(0xffffffffu, r[0], 2);
+      p[0] += __shfl_xor_sync(0xffffffffu, p[0], 1);
+      r[0] += __shfl_xor_sync(0xffffffffu, r[0], 1);
     }
+    const int Rl = 4 * ((lane >> 4) & 1) + 2 * ((lane >> 3) & 1) + ((lane >> 2) & 1);
+    const float pR = p[0], rR = r[0];
 #pragma unroll
     for (int i = 0; i < kRowsPerIter; ++i) {
+      const float pi = __shfl_sync(0xffffffffu, pR, 16 * (i >> 2) + 8 * ((i >> 1) & 1) + 4 * (i & 1));
       const float vj = __shfl_sync(0xffffffffu, v_mine, r0 + i);
-      const float u = b * (vj - p[i]);
+      const float u = b * (vj - pi);
       s[i].x = fmaf(u, kv[0], s[i].x);
       s[i].y = fmaf(u, kv[1], s[i].y);
       s[i].z = fmaf(u, kv[2], s[i].z);
       s[i].w = fmaf(u, kv[3], s[i].w);
       __stcs(Srow + (r0 + i) * (kD / 4), s[i]);
-      if (lane == r0 + i) o_mine = fmaf(u, qk, r[i]);
     }
+    // o of row r0 + R(l) = (u q.k + q.s) on the lanes that hold it
+    const float vR = __shfl_sync(0xffffffffu, v_mine, r0 + Rl);
+    const float oR = fmaf(b * (vR - pR), qk, rR);
+    const float oj = __shfl_sync(0xffffffffu, oR,
+                                 16 * (((lane - r0) & 7) >> 2) + 8 * ((((lane - r0) & 7) >> 1) & 1) +
+                                     4 * ((lane - r0) & 1));
+    if (lane >= r0 && lane < r0 + kRowsPerIter) o_mine = oj;
   }
   o[vec + row0 + lane] = from_f32<T>(o_mine);
 }
