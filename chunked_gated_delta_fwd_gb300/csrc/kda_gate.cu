@@ -17,8 +17,9 @@ namespace kda {
 namespace {
 
 __device__ __forceinline__ float bounded_decay(float z, float scale, float g_min) {
-  // g_min * Sigmoid(x) = g_min / (1 + exp(-x)); exp(-x) -> inf gives 0, -> 0 gives g_min.
-  return g_min / (1.0f + expf(-scale * z));
+  // g_min * Sigmoid(x) = g_min / (1 + exp(-x)); exp(-x) -> inf gives 0 (the fast
+  // quotient multiplies by the reciprocal, which is 0), -> 0 gives g_min.
+  return __fdividef(g_min, 1.0f + __expf(-scale * z));
 }
 
 // -scale * Softplus(z), Softplus(x) = log(1 + e^x) (= x to fp32 precision above 20)
