@@ -470,3 +470,24 @@ def test_each_path_launches_only_its_own_kernels(kda):
                                                  dev["h0"], dev["cu_seqlens"], g=dev["g"],
                                                  out_gate=gz, flags=kda.SEQUENTIAL))
     assert fused == {"kda_plan", "kda_tc_prep", "kda_tc_chain", "kda_output_gate"}, fused
+
+
+def test_checkpoints_full_size_sampled(kda):
+    """B=1, T=8192, H=96, bf16, a checkpoint every 512 tokens (16), as the bench runs
+    it: all 16 checkpoints of 2 sampled heads against the oracle run block by block."""
+    w = workloads.prefill()
+    dev = workloads.make_inputs(w, "cuda")
+    g = kda.gate(dev["z"], dev["A"])
+    _, hT, ck = kda.chunk_fwd_checkpointed(dev["q"], dev["k"], dev["v"], g, dev["beta"],
+                                           dev["h0"], dev["cu_seqlens"], ckpt_tokens=512)
+    torch.cuda.synchronize()
+    assert ck.shape[0] == 16
+    for h in (3, 90):
+        sl = lambda t: t[:, h:h + 1]
+        inp = dict(q=sl(dev["q"]), k=sl(dev["k"]), v=sl(dev["v"]), beta=sl(dev["beta"]),
+                   h0=dev["h0"][:, h:h + 1])
+        g_ref = oracle.gate(sl(dev["z"]), dev["A"][h:h + 1])
+        ck_ref = _oracle_checkpoints(inp, g_ref, [w.n_tokens], 512)
+        for i in range(16):
+            assert_close(ck[i, h:h + 1], ck_ref[i], torch.bfloat16, f"checkpoint {i} head {h}")
+        assert torch.equal(ck[15], hT[0])

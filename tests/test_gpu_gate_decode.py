@@ -178,3 +178,37 @@ def test_multi_step_one_token_matches_recurrent_step(kda):
     assert_close(o_one, o_ref, torch.bfloat16, "o step")
     assert_close(S_multi, h_ref, torch.bfloat16, "S multi T=1")
     assert_close(S_one, h_ref, torch.bfloat16, "S step")
+
+
+def test_multi_step_full_size_sampled(kda):
+    """512 sequences x 96 heads, fp32 state (3.2 GB), 4 tokens per sequence with a
+    partial commit (accepted prefix 0..4 tokens), as the bench runs it; 24 sampled
+    (sequence, head) pairs against the oracle (outputs of all 4 tokens, the state
+    after the accepted prefix)."""
+    dw = workloads.decode()
+    N, H, T = dw.N, dw.H, 4
+    S = workloads.make_decode_state(dw, "cuda")
+    steps = [workloads.make_decode_step(dw, i, "cuda") for i in range(T)]
+    stack = lambda key: torch.stack([st[key] for st in steps], dim=1).contiguous()  # [N, T, ...]
+    q, k, v, beta, z = stack("q"), stack("k"), stack("v"), stack("beta"), stack("z")
+    A = steps[0]["A"]
+    g = kda.gate(z, A)  # the GPU run's gate; the oracle forms its own from z
+    adv = (torch.arange(N, dtype=torch.int32) % (T + 1)).cuda()
+    r = np.random.default_rng(7)
+    pairs = sorted({(int(r.integers(N)), int(r.integers(H))) for _ in range(24)})
+    S0 = {p: S[p[0], p[1]].cpu().clone() for p in pairs}
+    o = kda.recurrent_multi_step(q, k, v, g, beta, S, adv)
+    torch.cuda.synchronize()
+    for n, h in pairs:
+        a = int(adv[n])
+        seq = lambda t: t[n, :, h:h + 1]  # [T, 1, ...]
+        g_ref = oracle.gate(seq(z), A[h:h + 1])
+        o_ref, _ = oracle.recurrence(seq(q), seq(k), seq(v), g_ref, seq(beta),
+                                     S0[(n, h)].view(1, 1, 128, 128))
+        assert_close(o[n, :, h:h + 1], o_ref, torch.bfloat16, f"o seq {n} head {h}")
+        if a > 0:
+            _, s_ref = oracle.recurrence(seq(q)[:a], seq(k)[:a], seq(v)[:a], g_ref[:a],
+                                         seq(beta)[:a], S0[(n, h)].view(1, 1, 128, 128))
+        else:
+            s_ref = S0[(n, h)].view(1, 1, 128, 128)
+        assert_close(S[n, h:h + 1].unsqueeze(0), s_ref, torch.bfloat16, f"state seq {n} head {h}")
