@@ -1485,9 +1485,22 @@ int chain_segment_chunks(int64_t n_tokens, int n_seqs, int H, int forced, bool s
   if (2 * chains > sms) return 0;  // enough chains to fill the GPU
   const int64_t per_seq = chunks_upper_bound(n_tokens, n_seqs) / n_seqs;
   if (per_seq < 256) return 0;     // short chains: the serial chain is short
-  const int64_t parts = sms / chains >= 2 ? sms / chains : 2;
-  const int64_t L = (per_seq + parts - 1) / parts;
-  return (int)(L > 64 ? L : 64);
+  // P segments of L chunks: the first launch runs chains x (2P - 2) CTAs (the runs
+  // from zero and the transition products), the rerun chains x (P - 1); each CTA
+  // walks L chunks.  Pick the P with the fewest waves x L.
+  auto waves = [&](int64_t ctas) { return (ctas + sms - 1) / sms; };
+  int64_t best_p = 1, best_cost = per_seq;
+  for (int64_t P = 2; P <= 64; ++P) {
+    const int64_t L = (per_seq + P - 1) / P;
+    if (L < 64) break;
+    const int64_t cost = (waves(chains * (2 * P - 2)) + waves(chains * (P - 1))) * L;
+    if (cost < best_cost) {
+      best_cost = cost;
+      best_p = P;
+    }
+  }
+  if (best_p == 1) return 0;
+  return (int)((per_seq + best_p - 1) / best_p);
 }
 
 size_t tc_workspace_bytes(int64_t n_tokens, int n_seqs, int H, int seg_chunks) {
