@@ -182,6 +182,22 @@ def test_workspace_size(L):
     assert L.kda_chunk_fwd_workspace_size(8192, 1, 97, 1) > a
 
 
+def test_segment_choice_for_long_sequences(L):
+    """The automatic chain segmentation of one 2^20-token sequence with 16 heads uses
+    10 segments of 1,639 chunks (the wave cost model: 16 x 18 CTAs, then 16 x 9, on
+    148-152 SMs), visible through the workspace the choice needs."""
+    L.kda_chunk_fwd_workspace_size_ex.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                                  ctypes.c_int, ctypes.c_uint]
+    L.kda_chunk_fwd_workspace_size_ex.restype = ctypes.c_size_t
+    f = L.kda_chunk_fwd_workspace_size_ex
+    auto = f(1 << 20, 1, 16, 1, 0)
+    assert auto == f(1 << 20, 1, 16, 1, 1639 << 16)
+    assert auto != f(1 << 20, 1, 16, 1, 1821 << 16)       # the former 9-segment choice
+    assert f(1 << 20, 1, 16, 1, 2) < auto                  # sequential: no segment state
+    # enough chains to fill the GPU: no segments
+    assert f(8192, 1, 96, 1, 0) == f(8192, 1, 96, 1, 2)
+
+
 def test_gate_rejects_bad_arguments(L):
     assert L.kda_gate(FAKE, 0, FAKE, -5.0, FAKE, 10, 2, 64, None, None, 1, None) == 2
     assert L.kda_gate(FAKE, 3, FAKE, -5.0, FAKE, 10, 2, 128, None, None, 1, None) == 3
