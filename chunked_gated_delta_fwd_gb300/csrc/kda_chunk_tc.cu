@@ -113,7 +113,8 @@ template <bool kZ>
 __host__ __device__ constexpr uint32_t gs_block(int half) {
   return half ? kP_Bop + 16384 : (kZ ? kP_Qs : kP_KTs);
 }
-// warps 0-7 run the inverse on barrier 2 while warps 8-15 run the next unit's pass 1
+// warps 0-3 run the inverse (barriers 2-4) while warps 8-15 run the next unit's pass 1
+// (threads from kInvThreads on); warps 4-7 wait at the join
 constexpr int kInvThreads = 256;
 constexpr int kLdL = 68, kLdT = 68;  // 16-byte rows: float4 loads along k
 constexpr float kLog2e = 1.4426950408889634f;
@@ -556,22 +557,25 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       }
       if (kZ && t == kStorer) bulk_wait_read_all();  // the next pass 1 rewrites the Q staging
       named_sync(1, kPrepCompute);
-      // Warps 8-15: pass 1 of the next unit while warps 0-7 form this unit's inverse.
+      // Warps 8-15: pass 1 of the next unit while warps 0-3 form this unit's inverse.
       bool ok1 = true;
       if (t >= kInvThreads) ok1 = pass1(slots[(it + 1) & 1], (it + 1) & 1);
-      if (t < kInvThreads) {
-
-        // ---- T = (I + L)^{-1} in fp32.  Each diagonal 16x16 block from its 8x8 halves,
-        //      [A 0; C B]^{-1} = [A^{-1} 0; -B^{-1} C A^{-1}  B^{-1}], then the three
-        //      block-substitution stages for the blocks below the diagonal
-        if (t < C) {  // A^{-1}, B^{-1}: 8x8 forward substitution, one column per thread
-          const int ob = 8 * (t >> 3), cc = t & 7;
+      if (t < 128) {
+        // ---- T = (I + L)^{-1} in fp32.  Warp wq owns diagonal 16x16 block wq: its 8x8
+        //      halves by forward substitution, then [A 0; C B]^{-1} lower-left
+        //      = -B^{-1} C A^{-1}, warp-synchronous.  Level 1: warp 2b forms
+        //      P = L_{2b+1,2b} D_{2b} from its own block and hands it to warp 2b+1
+        //      (named barrier 3 + b), which forms T_{2b+1,2b} = -D_{2b+1} P.  Level 2 on
+        //      warps 0-3 (barrier 2, 128 threads).  Stored blocks carry zeros above their
+        //      diagonals; blocks above the diagonal are never stored nor read.
+        const int wq = warp, o = 16 * wq, wl = t & 31;  // warp, its block, lane in warp
+        if (wl < 16) {  // A^{-1} (lanes 0-7), B^{-1} (lanes 8-15): one column per lane
+          const int ob = o + 8 * (wl >> 3), cc = wl & 7;
           float x[8];
 #pragma unroll
           for (int m = 0; m < 8; ++m) {
-            float lr[8];  // row m of the 8x8 block, two 16-byte loads
-            *reinterpret_cast<float4*>(lr) =
-                *reinterpret_cast<const float4*>(Lb + (ob + m) * kLdL + ob);
+            float lr[8];
+            *reinterpret_cast<float4*>(lr) = *reinterpret_cast<const float4*>(Lb + (ob + m) * kLdL + ob);
             *reinterpret_cast<float4*>(lr + 4) =
                 *reinterpret_cast<const float4*>(Lb + (ob + m) * kLdL + ob + 4);
             float acc = 0.f;
@@ -581,49 +585,50 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
           }
 #pragma unroll
           for (int m = 0; m < 8; ++m) Tb[(ob + m) * kLdT + ob + cc] = x[m];
-          if (((t >> 3) & 1) == 0) {  // the zero upper-right 8x8 of the 16x16 block
+          if (wl < 8) {  // the zero upper-right 8x8 of the 16x16 block
 #pragma unroll
             for (int m = 0; m < 8; ++m) Tb[(ob + m) * kLdT + ob + 8 + cc] = 0.f;
           }
         }
-        named_sync(2, kInvThreads);
-        {  // P = C A^{-1} per block
-          const int ba = t >> 6, i = (t >> 3) & 7, j = t & 7, o = 16 * ba;
+        __syncwarp();
+        const int di = wl >> 2, dj = 2 * (wl & 3);  // 8x8: row di, columns dj, dj + 1
+        {  // P = C A^{-1}
           float lr[8];
-          *reinterpret_cast<float4*>(lr) = *reinterpret_cast<const float4*>(Lb + (o + 8 + i) * kLdL + o);
+          *reinterpret_cast<float4*>(lr) = *reinterpret_cast<const float4*>(Lb + (o + 8 + di) * kLdL + o);
           *reinterpret_cast<float4*>(lr + 4) =
-              *reinterpret_cast<const float4*>(Lb + (o + 8 + i) * kLdL + o + 4);
-          float acc = 0.f;
+              *reinterpret_cast<const float4*>(Lb + (o + 8 + di) * kLdL + o + 4);
+          float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-          for (int k = 0; k < 8; ++k)  // A^{-1} has stored zeros above the diagonal
-            acc = fmaf(lr[k], Tb[(o + k) * kLdT + o + j], acc);
-          Ps[ba * 64 + i * 8 + j] = acc;
+          for (int k = 0; k < 8; ++k) {  // A^{-1} has stored zeros above the diagonal
+            a0 = fmaf(lr[k], Tb[(o + k) * kLdT + o + dj], a0);
+            a1 = fmaf(lr[k], Tb[(o + k) * kLdT + o + dj + 1], a1);
+          }
+          Ps[wq * 64 + di * 8 + dj] = a0;
+          Ps[wq * 64 + di * 8 + dj + 1] = a1;
         }
-        named_sync(2, kInvThreads);
+        __syncwarp();
         {  // lower-left 8x8 = -B^{-1} P
-          const int ba = t >> 6, i = (t >> 3) & 7, j = t & 7, o = 16 * ba;
           float wr[8];
-          *reinterpret_cast<float4*>(wr) =
-              *reinterpret_cast<const float4*>(Tb + (o + 8 + i) * kLdT + o + 8);
+          *reinterpret_cast<float4*>(wr) = *reinterpret_cast<const float4*>(Tb + (o + 8 + di) * kLdT + o + 8);
           *reinterpret_cast<float4*>(wr + 4) =
-              *reinterpret_cast<const float4*>(Tb + (o + 8 + i) * kLdT + o + 12);
-          float acc = 0.f;
+              *reinterpret_cast<const float4*>(Tb + (o + 8 + di) * kLdT + o + 12);
+          float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-          for (int k = 0; k < 8; ++k)  // B^{-1} has stored zeros above the diagonal
-            acc = fmaf(wr[k], Ps[ba * 64 + k * 8 + j], acc);
-          Tb[(o + 8 + i) * kLdT + o + j] = -acc;
+          for (int k = 0; k < 8; ++k) {  // B^{-1} has stored zeros above the diagonal
+            a0 = fmaf(wr[k], Ps[wq * 64 + k * 8 + dj], a0);
+            a1 = fmaf(wr[k], Ps[wq * 64 + k * 8 + dj + 1], a1);
+          }
+          Tb[(o + 8 + di) * kLdT + o + dj] = -a0;
+          Tb[(o + 8 + di) * kLdT + o + dj + 1] = -a1;
         }
-        named_sync(2, kInvThreads);
-        // Blocks below the diagonal by doubling: first the 16x16 blocks (1,0), (3,2)
-        // of the two 32x32 diagonal blocks, then their 32x32 lower-left block,
-        //   [A 0; C B]^{-1} lower-left = -B^{-1} (C A^{-1})   (at both levels).
-        // Register-blocked: a thread computes 2 rows x 4 columns, so each shared-memory
-        // load feeds four (L) or two (T) FMAs.
-        if (t < 64) {  // level 1: P = L_{a+1,a} D_a (a = 0, 2)
-          const int blk = t >> 5, a = 2 * blk, R = a + 1, rp = (t >> 2) & 7, cq = t & 3;
+        __syncwarp();
+        // level 1 (2 rows x 4 columns per wl: rows rp and rp + 8)
+        const int blk = wq >> 1, a = 2 * blk, R = a + 1, rp = (wl >> 2) & 7, cq = wl & 3;
+        float* P1 = Ps + 256 + blk * 256;
+        if ((wq & 1) == 0) {  // P = L_{a+1,a} D_a
           float acc[2][4] = {};
 #pragma unroll
-          for (int k4 = 0; k4 < 16; k4 += 4) {  // D_a has stored zeros above its diagonal
+          for (int k4 = 0; k4 < 16; k4 += 4) {
             float lv[2][4];
 #pragma unroll
             for (int r = 0; r < 2; ++r)
@@ -645,15 +650,14 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
           }
 #pragma unroll
           for (int r = 0; r < 2; ++r)
-            *reinterpret_cast<float4*>(Ps + blk * 256 + (rp + 8 * r) * 16 + 4 * cq) =
+            *reinterpret_cast<float4*>(P1 + (rp + 8 * r) * 16 + 4 * cq) =
                 make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
-        }
-        named_sync(2, kInvThreads);
-        if (t < 64) {  // level 1: T_{a+1,a} = -D_{a+1} P
-          const int blk = t >> 5, a = 2 * blk, R = a + 1, rp = (t >> 2) & 7, cq = t & 3;
+          named_arrive(3 + blk, 64);
+        } else {  // T_{a+1,a} = -D_{a+1} P
+          named_sync(3 + blk, 64);
           float acc[2][4] = {};
 #pragma unroll
-          for (int k4 = 0; k4 < 16; k4 += 4) {  // D_{a+1} has stored zeros above its diagonal
+          for (int k4 = 0; k4 < 16; k4 += 4) {
             float wv[2][4];
 #pragma unroll
             for (int r = 0; r < 2; ++r)
@@ -661,8 +665,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                   *reinterpret_cast<const float4*>(Tb + (16 * R + rp + 8 * r) * kLdT + 16 * R + k4);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              const float4 pv =
-                  *reinterpret_cast<const float4*>(Ps + blk * 256 + (k4 + kk) * 16 + 4 * cq);
+              const float4 pv = *reinterpret_cast<const float4*>(P1 + (k4 + kk) * 16 + 4 * cq);
 #pragma unroll
               for (int r = 0; r < 2; ++r) {
                 const float w = wv[r][kk];
@@ -678,11 +681,11 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             *reinterpret_cast<float4*>(Tb + (16 * R + rp + 8 * r) * kLdT + 16 * a + 4 * cq) =
                 make_float4(-acc[r][0], -acc[r][1], -acc[r][2], -acc[r][3]);
         }
-        named_sync(2, kInvThreads);
+        named_sync(2, 128);
         // level 2: M = L[32:64, 0:32] T[0:32, 0:32] into the unused upper-right block of Tb
         // (rows 0..31, columns 32..63); T[0:16, 16:32] is not stored (zero).
         float* Mb = Tb + 32;
-        if (t < 128) {
+        {
           const int rp = t >> 3, cq = t & 7, k0 = cq >= 4 ? 16 : 0;
           float acc[2][4] = {};
 #pragma unroll
@@ -712,8 +715,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             *reinterpret_cast<float4*>(Mb + (2 * rp + r) * kLdT + 4 * cq) =
                 make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
         }
-        named_sync(2, kInvThreads);
-        if (t < 128) {  // level 2: T[32:64, 0:32] = -T[32:64, 32:64] M; T[32:48, 48:64] is zero
+        named_sync(2, 128);
+        {  // level 2: T[32:64, 0:32] = -T[32:64, 32:64] M; T[32:48, 48:64] is zero
           const int rp = t >> 3, cq = t & 7, kn = rp < 8 ? 16 : 32;
           float acc[2][4] = {};
 #pragma unroll
