@@ -26,7 +26,7 @@
 // log-decays of the next unit while warps 0-7 run this unit's (I + A_kk)^{-1}
 // inverse in fp32 on the CUDA cores.  Every thread builds the operands of 8
 // tokens x 2 channels and one thread issues the MMAs (the four tile products in
-// one N=192 chain, then W^T and U^T); the unit
+// one N=160 chain, then W^T and U^T); the unit
 // leaves as MMA-ready bf16 tiles written with whole-tile bulk copies:
 //   W, Gamma*Q: MN-major, 64 token columns x 128 channels each (one operand with
 //               a 16 KB atom stride)
@@ -494,7 +494,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         gam_c[o2] = exp2_approx(GC);
       }
 
-      // ---- block products in one N=192 MMA chain: D[m][n] = Bop row m . KC row n
+      // ---- block products in one N=160 MMA chain: D[m][n] = Bop row m . KC row n
       //      over the channels; lane m = 32 ta + 16 part + j is K row (part 0) or
       //      Q row (part 1) j of tile ta, and KC(ta) sits at columns 8 ta (ta + 1)
       fence_proxy_async_smem();
@@ -502,7 +502,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       named_sync(1, kPrepCompute);
       if (t == 0) {
         tc_fence_after();
-        const uint32_t id = idesc_bf16_mn(128, kKCX, 1, 1);
+        const uint32_t id = idesc_bf16_mn(128, 160, 1, 1);  // KC columns 160..191 unused
         const uint64_t da = mnmajor_desc(sbase + kP_Bop, 2048, 0);
         const uint64_t db = mnmajor_desc(sbase + kP_KC, mn_sbo(kKCX), 0);
 #pragma unroll
