@@ -113,8 +113,9 @@ template <bool kZ>
 __host__ __device__ constexpr uint32_t gs_block(int half) {
   return half ? kP_Bop + 16384 : (kZ ? kP_Qs : kP_KTs);
 }
-// warps 0-3 run the inverse (barriers 2-4) while warps 8-15 run the next unit's pass 1
-// (threads from kInvThreads on); warps 4-7 wait at the join
+// warps 0-3 run the inverse (barriers 2-4); warps 4-7 start its last level once the
+// first two diagonal blocks are stored (barrier 5) and finish it with warps 0-3;
+// meanwhile warps 8-15 run the next unit's pass 1 (threads from kInvThreads on)
 constexpr int kInvThreads = 256;
 constexpr int kLdL = 68, kLdT = 68;  // 16-byte rows: float4 loads along k
 constexpr float kLog2e = 1.4426950408889634f;
@@ -565,9 +566,10 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         //      halves by forward substitution, then [A 0; C B]^{-1} lower-left
         //      = -B^{-1} C A^{-1}, warp-synchronous.  Level 1: warp 2b forms
         //      P = L_{2b+1,2b} D_{2b} from its own block and hands it to warp 2b+1
-        //      (named barrier 3 + b), which forms T_{2b+1,2b} = -D_{2b+1} P.  Level 2 on
-        //      warps 0-3 (barrier 2, 128 threads).  Stored blocks carry zeros above their
-        //      diagonals; blocks above the diagonal are never stored nor read.
+        //      (named barrier 3 + b), which forms T_{2b+1,2b} = -D_{2b+1} P.  Level 2 below,
+        //      on warps 4-7 from the end of level 0 and on warps 0-7 after level 1.
+        //      Stored blocks carry zeros above their diagonals; blocks above the
+        //      diagonal are never stored nor read.
         const int wq = warp, o = 16 * wq, wl = t & 31;  // warp, its block, lane in warp
         if (wl < 16) {  // A^{-1} (lanes 0-7), B^{-1} (lanes 8-15): one column per lane
           const int ob = o + 8 * (wl >> 3), cc = wl & 7;
@@ -622,6 +624,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
           Tb[(o + 8 + di) * kLdT + o + dj + 1] = -a1;
         }
         __syncwarp();
+        if (wq < 2) named_arrive(5, 192);  // D_0, D_1 are stored: warps 4-7 may read them
         // level 1 (2 rows x 4 columns per wl: rows rp and rp + 8)
         const int blk = wq >> 1, a = 2 * blk, R = a + 1, rp = (wl >> 2) & 7, cq = wl & 3;
         float* P1 = Ps + 256 + blk * 256;
@@ -681,44 +684,68 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             *reinterpret_cast<float4*>(Tb + (16 * R + rp + 8 * r) * kLdT + 16 * a + 4 * cq) =
                 make_float4(-acc[r][0], -acc[r][1], -acc[r][2], -acc[r][3]);
         }
-        named_sync(2, 128);
-        // level 2: M = L[32:64, 0:32] T[0:32, 0:32] into the unused upper-right block of Tb
-        // (rows 0..31, columns 32..63); T[0:16, 16:32] is not stored (zero).
-        float* Mb = Tb + 32;
-        {
-          const int rp = t >> 3, cq = t & 7, k0 = cq >= 4 ? 16 : 0;
-          float acc[2][4] = {};
+      } else if (t < kInvThreads) {
+        // Warps 4-7, while warps 0-3 run level 1: the terms of level 2's
+        // M = L[32:64, 0:32] T[0:32, 0:32] that need only D_0 and D_1, i.e.
+        // M[:, 0:16] = L[32:64, 0:16] D_0 and M[:, 16:32] = L[32:64, 16:32] D_1
+        // (T[0:16, 16:32] is zero), into the unused upper-right block of Tb (rows
+        // 0..31, columns 32..63).  2 rows x 4 columns per thread.
+        named_sync(5, 192);
+        const int tt = t - 128, rp = tt >> 3, cq = tt & 7, kb = cq >= 4 ? 16 : 0;
+        float acc[2][4] = {};
 #pragma unroll
-          for (int k4 = 0; k4 < 32; k4 += 4) {
-            if (k4 >= k0) {
-              float lv[2][4];
-#pragma unroll
-              for (int r = 0; r < 2; ++r)
-                *reinterpret_cast<float4*>(lv[r]) =
-                    *reinterpret_cast<const float4*>(Lb + (32 + 2 * rp + r) * kLdL + k4);
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const float4 tv = *reinterpret_cast<const float4*>(Tb + (k4 + kk) * kLdT + 4 * cq);
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                  const float l = lv[r][kk];
-                  acc[r][0] = fmaf(l, tv.x, acc[r][0]);
-                  acc[r][1] = fmaf(l, tv.y, acc[r][1]);
-                  acc[r][2] = fmaf(l, tv.z, acc[r][2]);
-                  acc[r][3] = fmaf(l, tv.w, acc[r][3]);
-                }
-              }
-            }
-          }
+        for (int k4 = 0; k4 < 16; k4 += 4) {
+          float lv[2][4];
 #pragma unroll
           for (int r = 0; r < 2; ++r)
-            *reinterpret_cast<float4*>(Mb + (2 * rp + r) * kLdT + 4 * cq) =
-                make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+            *reinterpret_cast<float4*>(lv[r]) =
+                *reinterpret_cast<const float4*>(Lb + (32 + 2 * rp + r) * kLdL + kb + k4);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const float4 tv = *reinterpret_cast<const float4*>(Tb + (kb + k4 + kk) * kLdT + 4 * cq);
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const float l = lv[r][kk];
+              acc[r][0] = fmaf(l, tv.x, acc[r][0]);
+              acc[r][1] = fmaf(l, tv.y, acc[r][1]);
+              acc[r][2] = fmaf(l, tv.z, acc[r][2]);
+              acc[r][3] = fmaf(l, tv.w, acc[r][3]);
+            }
+          }
         }
-        named_sync(2, 128);
-        {  // level 2: T[32:64, 0:32] = -T[32:64, 32:64] M; T[32:48, 48:64] is zero
-          const int rp = t >> 3, cq = t & 7, kn = rp < 8 ? 16 : 32;
-          float acc[2][4] = {};
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+          *reinterpret_cast<float4*>(Tb + 32 + (2 * rp + r) * kLdT + 4 * cq) =
+              make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+      }
+      if (t < kInvThreads) {
+        // level 2 on warps 0-7 (barrier 2, 256 threads): M[:, 0:16] += L[32:64, 16:32]
+        // T_{1,0} (one row x 2 columns per thread), then T[32:64, 0:32] = -T22 M.
+        named_sync(2, kInvThreads);
+        float* Mb = Tb + 32;
+        {
+          const int r = t >> 3, cp = t & 7;
+          float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+          for (int k4 = 16; k4 < 32; k4 += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(Lb + (32 + r) * kLdL + k4);
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const float2 tv = *reinterpret_cast<const float2*>(Tb + (k4 + kk) * kLdT + 2 * cp);
+              a0 = fmaf(lv[kk], tv.x, a0);
+              a1 = fmaf(lv[kk], tv.y, a1);
+            }
+          }
+          float2* mp = reinterpret_cast<float2*>(Mb + r * kLdT + 2 * cp);
+          const float2 m0 = *mp;
+          *mp = make_float2(m0.x + a0, m0.y + a1);
+        }
+        const int rp = t >> 4, cq = t & 15;
+        named_sync(2, kInvThreads);
+        {  // T[32:64, 0:32] = -T[32:64, 32:64] M; T[32:48, 48:64] is zero
+          const int kn = rp < 8 ? 16 : 32;  // warp-uniform: warps 0-3 hold rows 32..47
+          float acc[2][2] = {};
 #pragma unroll
           for (int k4 = 0; k4 < 32; k4 += 4) {
             if (k4 < kn) {
@@ -729,22 +756,19 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                     *reinterpret_cast<const float4*>(Tb + (32 + 2 * rp + r) * kLdT + 32 + k4);
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
-                const float4 mv = *reinterpret_cast<const float4*>(Mb + (k4 + kk) * kLdT + 4 * cq);
+                const float2 mv = *reinterpret_cast<const float2*>(Mb + (k4 + kk) * kLdT + 2 * cq);
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                  const float w = wv[r][kk];
-                  acc[r][0] = fmaf(w, mv.x, acc[r][0]);
-                  acc[r][1] = fmaf(w, mv.y, acc[r][1]);
-                  acc[r][2] = fmaf(w, mv.z, acc[r][2]);
-                  acc[r][3] = fmaf(w, mv.w, acc[r][3]);
+                  acc[r][0] = fmaf(wv[r][kk], mv.x, acc[r][0]);
+                  acc[r][1] = fmaf(wv[r][kk], mv.y, acc[r][1]);
                 }
               }
             }
           }
 #pragma unroll
           for (int r = 0; r < 2; ++r)
-            *reinterpret_cast<float4*>(Tb + (32 + 2 * rp + r) * kLdT + 4 * cq) =
-                make_float4(-acc[r][0], -acc[r][1], -acc[r][2], -acc[r][3]);
+            *reinterpret_cast<float2*>(Tb + (32 + 2 * rp + r) * kLdT + 2 * cq) =
+                make_float2(-acc[r][0], -acc[r][1]);
         }
       }
       if (!named_sync_and(1, kPrepCompute, ok1)) break;
