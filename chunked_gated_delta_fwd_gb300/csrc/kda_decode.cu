@@ -163,11 +163,17 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_multi_kernel(
   (void)tid;
   const int row0 = warp * 32;
   float4* Srow = reinterpret_cast<float4*>(S + (int64_t)unit * kD * kD) + row0 * (kD / 4) + lane;
+  // The next block of rows is loaded while the T tokens walk the current one, so
+  // that the state stream stays in flight during the token loop.
+  float4 s[kRowsPerIter], sn[kRowsPerIter];
+#pragma unroll
+  for (int i = 0; i < kRowsPerIter; ++i) s[i] = __ldcs(Srow + i * (kD / 4));
 #pragma unroll 1
   for (int r0 = 0; r0 < 32; r0 += kRowsPerIter) {
-    float4 s[kRowsPerIter];
+    if (r0 + kRowsPerIter < 32) {
 #pragma unroll
-    for (int i = 0; i < kRowsPerIter; ++i) s[i] = Srow[(r0 + i) * (kD / 4)];
+      for (int i = 0; i < kRowsPerIter; ++i) sn[i] = __ldcs(Srow + (r0 + kRowsPerIter + i) * (kD / 4));
+    }
 #pragma unroll 1
     for (int t = 0; t < Tn; ++t) {
       const float4 al = *reinterpret_cast<const float4*>(&ta[t][4 * lane]);
@@ -229,9 +235,11 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_multi_kernel(
       }
       if (t + 1 == adv) {
 #pragma unroll
-        for (int i = 0; i < kRowsPerIter; ++i) Srow[(r0 + i) * (kD / 4)] = s[i];
+        for (int i = 0; i < kRowsPerIter; ++i) __stcs(Srow + (r0 + i) * (kD / 4), s[i]);
       }
     }
+#pragma unroll
+    for (int i = 0; i < kRowsPerIter; ++i) s[i] = sn[i];
   }
 }
 
