@@ -8,8 +8,8 @@
 // The unbounded gate it replaces, g = -exp(A_h) * Softplus(z) (Kimi Linear, the same
 // review, section 3.2), is formed by the same kernel for the range-robust mode.
 //
-// Memory-bound elementwise work: 8 elements per thread per step with 16-byte
-// (bf16) or 32-byte (fp32) loads and 32-byte stores, grid-stride over a grid
+// Memory-bound elementwise work: 8-element groups, four per thread in flight
+// (16-byte bf16 or 32-byte fp32 loads, 32-byte stores), grid-stride over a grid
 // sized to the SM count.
 #include "kda_internal.cuh"
 
@@ -32,21 +32,38 @@ __global__ void __launch_bounds__(256) gate_kernel(const Tz* __restrict__ z,
                                                    const float* __restrict__ A, float g_min,
                                                    float* __restrict__ g, int64_t n_groups,
                                                    int H) {
-  // group = 8 consecutive channels of one (token, head); kD / 8 = 16 groups per (t, h)
-  for (int64_t grp = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; grp < n_groups;
-       grp += (int64_t)gridDim.x * blockDim.x) {
-    const int h = (int)((grp / (kD / 8)) % H);
-    const float scale = expf(__ldg(A + h));
-    float x[8];
-    load8(z + grp * 8, x);
-    float y[8];
+  // group = 8 consecutive channels of one (token, head), kD / 8 = 16 groups per
+  // (t, h).  Each thread takes four groups one grid stride apart (every access of a
+  // warp is one contiguous span) and issues their loads before any store.  The grid
+  // stride is a whole number of (token, head) rows, so the head index of the next
+  // group steps by a constant: one division per thread.
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t g0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (g0 >= n_groups) return;
+  int h = (int)((g0 >> 4) % H);
+  const int hstep = (int)((stride >> 4) % H);
+  for (int64_t grp = g0; grp < n_groups; grp += 4 * stride) {
+    float x[4][8];
+    int hj[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      y[i] = kSoftplus ? softplus_decay(x[i], scale) : bounded_decay(x[i], scale, g_min);
-    const float4 lo = make_float4(y[0], y[1], y[2], y[3]), hi = make_float4(y[4], y[5], y[6], y[7]);
-    float4* out = reinterpret_cast<float4*>(g + grp * 8);
-    out[0] = lo;
-    out[1] = hi;
+    for (int j = 0; j < 4; ++j) {
+      hj[j] = h;
+      h += hstep;
+      if (h >= H) h -= H;
+      if (grp + j * stride < n_groups) load8(z + (grp + j * stride) * 8, x[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (grp + j * stride >= n_groups) break;
+      const float scale = expf(__ldg(A + hj[j]));
+      float y[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        y[i] = kSoftplus ? softplus_decay(x[j][i], scale) : bounded_decay(x[j][i], scale, g_min);
+      float4* out = reinterpret_cast<float4*>(g + (grp + j * stride) * 8);
+      out[0] = make_float4(y[0], y[1], y[2], y[3]);
+      out[1] = make_float4(y[4], y[5], y[6], y[7]);
+    }
   }
 }
 
