@@ -36,6 +36,7 @@ F32, BF16 = 0, 1
 FP32_CORES = 1  # flag of chunk_fwd: evaluate bf16 inputs on fp32 CUDA cores
 SEQUENTIAL = 2  # flag of chunk_fwd: never split a sequence's chain into segments
 UNBOUNDED_GATE = 4  # flag of chunk_fwd: any g <= 0 (range-robust fp32-core evaluation)
+SCALAR_GATE = 8  # flag of chunk_fwd: g is [..., H], one log-decay per token and head
 
 _STATUS = {
     0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED_SHAPE",
@@ -206,7 +207,8 @@ def chunk_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, *, output_final_state=
     """KDA prefill over whole sequences.
 
     q, k: [B, T, H, 128] or packed [T, H, 128] (with ``cu_seqlens``), bf16 or fp32;
-    v like q; g: same shape, fp32 log-decays in [-5, 0]; beta: [..., H] (dtype of q);
+    v like q; g: same shape, fp32 log-decays in [-5, 0] (with ``flags`` holding
+    ``SCALAR_GATE``: [..., H], one per token and head); beta: [..., H] (dtype of q);
     h0: [N, H, 128, 128] fp32 (the state stored transposed, [dv][dk]) or None;
     cu_seqlens: int32 [N+1] on the device, or None for B sequences of length T.
     Returns ``(o, hT)`` with o like v and hT [N, H, 128, 128] fp32 (None if not asked).

@@ -218,6 +218,13 @@ kda_status_t cuda_fail(cudaError_t e, const char* what) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Byte offset, in the workspace of the fp32-core path, of the scalar gates spread
+// over the channels (after the plan and that path's own scratch, 256-aligned).
+size_t simt_scalar_gate_offset(int64_t n_tokens, int n_seqs, int H) {
+  const size_t b = kda::plan_bytes(n_tokens, n_seqs) + kda::simt_workspace_bytes(n_tokens, n_seqs, H);
+  return (b + 255) & ~(size_t)255;
+}
+
 kda_status_t check_device() {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -396,8 +403,12 @@ size_t kda_chunk_fwd_workspace_size_ex(int64_t n_tokens, int n_seqs, int H, int 
                                                (flags & KDA_CHUNK_SEQUENTIAL) != 0);
     return kda::plan_bytes(n_tokens, n_seqs) + kda::tc_workspace_bytes(n_tokens, n_seqs, H, segc);
   }
-  if (dtype == KDA_F32 || dtype == KDA_BF16)
-    return kda::plan_bytes(n_tokens, n_seqs) + kda::simt_workspace_bytes(n_tokens, n_seqs, H);
+  if (dtype == KDA_F32 || dtype == KDA_BF16) {
+    if (!(flags & KDA_CHUNK_SCALAR_GATE))
+      return kda::plan_bytes(n_tokens, n_seqs) + kda::simt_workspace_bytes(n_tokens, n_seqs, H);
+    return simt_scalar_gate_offset(n_tokens, n_seqs, H) +
+           (size_t)n_tokens * H * kda::kD * sizeof(float);  // the spread gates
+  }
   return 0;
 }
 
@@ -452,10 +463,13 @@ kda_status_t chunk_fwd_impl(const char* fn, const void* q, const void* k, const 
     return fail(KDA_ERR_WORKSPACE_TOO_SMALL, "%s: workspace %zu < %zu bytes", fn,
                 ws_bytes, need);
   if (flags & ~(unsigned)(KDA_CHUNK_FP32_CORES | KDA_CHUNK_SEQUENTIAL |
-                          KDA_CHUNK_UNBOUNDED_GATE | 0xffff0000u))
+                          KDA_CHUNK_UNBOUNDED_GATE | KDA_CHUNK_SCALAR_GATE | 0xffff0000u))
     return fail(KDA_ERR_INVALID_ARG, "%s: unknown flags 0x%x", fn, flags);
   if ((flags & KDA_CHUNK_UNBOUNDED_GATE) && z)
     return fail(KDA_ERR_INVALID_ARG, "%s: the unbounded-gate mode takes g, not z", fn);
+  if ((flags & KDA_CHUNK_SCALAR_GATE) && z)
+    return fail(KDA_ERR_INVALID_ARG, "%s: the scalar-gate mode takes g, not z", fn);
+  const bool scalar_g = (flags & KDA_CHUNK_SCALAR_GATE) != 0;
   kda_status_t st = check_device();
   if (st != KDA_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -466,11 +480,19 @@ kda_status_t chunk_fwd_impl(const char* fn, const void* q, const void* k, const 
     e = kda::launch_chunk_tc(q, k, v, g, z, A, g_min, beta, h0, o, hT, NT, N, H,
                              kda::chain_segment_chunks(NT, N, H, (int)(flags >> 16),
                                                        (flags & KDA_CHUNK_SEQUENTIAL) != 0),
-                             ck, fz, workspace, err, s);
+                             ck, fz, scalar_g, workspace, err, s);
     if (e == cudaSuccess && fz.gz && NT > 0)  // the output gate, on o in place
       e = kda::launch_output_gate(o, 1, fz.gz, fz.w, fz.eps, o, NT, H, s);
   } else {
-    e = kda::launch_chunk_simt(q, k, v, dtype == KDA_BF16, g, beta, h0, o, hT, NT, N, H,
+    const float* gf = g;
+    if (scalar_g) {  // this path reads per-channel decays: spread the scalar ones first
+      float* gx = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                           simt_scalar_gate_offset(NT, N, H));
+      e = kda::launch_expand_scalar_gate(g, gx, NT, H, s);
+      if (e != cudaSuccess) return cuda_fail(e, "scalar gate launch");
+      gf = gx;
+    }
+    e = kda::launch_chunk_simt(q, k, v, dtype == KDA_BF16, gf, beta, h0, o, hT, NT, N, H,
                                workspace, s, (flags & KDA_CHUNK_UNBOUNDED_GATE) ? 1 : 0);
   }
   if (e != cudaSuccess) return cuda_fail(e, "chunk launch");

@@ -95,7 +95,9 @@ constexpr uint32_t kP_beta = 196608;       // 64 fp32
 constexpr uint32_t kP_Tot = kP_beta + 256; // per-tile sums of g, [4][128] fp32
 constexpr uint32_t kP_Rq = kP_Tot + 2048;  // 1 / |q_r|, 1 / |k_r| (fp32 [64] each) when
 constexpr uint32_t kP_Rk = kP_Rq + 256;    //   q and k are normalised in the kernel
+constexpr uint32_t kP_Gsc = kP_Rk + 256;   // scalar gates of the next unit, fp32 [64]
 constexpr uint32_t kP_bars = kP_Tot + 4096;  // k/q/v full, g full, p, w + TMEM base
+static_assert(kP_Gsc + 256 <= kP_bars, "the scalar gates fit below the barriers");
 // With the gate fused (z staged in bf16) the upper half of the g staging space and
 // one more 16 KB block hold the unit's Gamma*Q and Kt^T tiles on their way out.
 constexpr uint32_t kP_Qs = kI_G + 16384;
@@ -153,11 +155,13 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
             const __nv_bfloat16* __restrict__ beta, const float* __restrict__ A, float g_min,
             Plan plan, int H, int64_t units_ub, uint8_t* __restrict__ tiles,
-            float* __restrict__ gam_out, float qk_eps, int* err) {
+            float* __restrict__ gam_out, float qk_eps, const float* __restrict__ g_sc,
+            int* err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_addr(sm);
   float* beta_s = reinterpret_cast<float*>(sm + kP_beta);
+  float* gsc_s = reinterpret_cast<float*>(sm + kP_Gsc);
   float* Tot = reinterpret_cast<float*>(sm + kP_Tot);
   float* Lb = reinterpret_cast<float*>(sm + kP_Lb);
   float* Tb = reinterpret_cast<float*>(sm + kP_Tb);
@@ -201,6 +205,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
   UnitInfo* slots = reinterpret_cast<UnitInfo*>(sm + kP_bars + 64);
   uint32_t issued_kqv = 0, issued_g = 0;  // copies issued (thread kIssuer)
   float beta_nx = 0.f;  // beta of token t - 64 of the next unit (threads 64..127)
+  float gsc_nx = 0.f;   // its scalar gate, when g is one decay per token and head
   auto locate = [&](int64_t u) {
     UnitInfo ui;
     if (u < units_ub) ui = unit_info(plan, H, u); else ui.chunk = total;
@@ -217,7 +222,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     ++issued_kqv;
   };
   auto issue_g = [&](const UnitInfo& ui) {
-    if (ui.chunk >= total) return;
+    if (ui.chunk >= total || g_sc) return;  // scalar gates are read by warps 2-3
     mbar_arrive_expect_tx(bar_g, g_unit_bytes<kZ>());
     tma_load_3d(sbase + kI_G, &tm_g, 0, ui.h, (int)ui.t0, bar_g);
     ++issued_g;
@@ -240,9 +245,11 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
   // loads only: beta of unit `un`, the table entry (and A_h) of the unit two ahead;
   // then steps that unit by the grid
   auto fetch_start = [&](const UnitInfo& un) {
-    if (t >= 64 && t < 128)
-      beta_nx = (un.chunk < total && t - 64 < un.len)
-                    ? __bfloat162float(beta[(un.t0 + t - 64) * H + un.h]) : 0.f;
+    if (t >= 64 && t < 128) {
+      const bool in = un.chunk < total && t - 64 < un.len;
+      beta_nx = in ? __bfloat162float(beta[(un.t0 + t - 64) * H + un.h]) : 0.f;
+      if (g_sc) gsc_nx = in ? __ldg(g_sc + (un.t0 + t - 64) * H + un.h) : 0.f;
+    }
     if (t == kLocator || t == kPrefetcher) {
       pend_ok = uf_chunk < chunks_ub;
       if (pend_ok) {
@@ -308,7 +315,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       if ((part & 1) == 0)
         reinterpret_cast<float*>(sm + (part < 2 ? kP_Rq : kP_Rk))[row] = rsqrtf(ss + qk_eps);
     }
-    if (!mbar_wait(bar_g, parity, err)) return false;
+    if (!g_sc && !mbar_wait(bar_g, parity, err)) return false;
     const int t8 = t - kInvThreads, cp = 2 * (t8 & 63), ta = t8 >> 6;
     const uint8_t* zg = sm + kI_G;
     float s0 = 0.f, s1 = 0.f;
@@ -334,6 +341,9 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         gv[1] = d0 * q01;
         gv[2] = d3 * q23;
         gv[3] = d2 * q23;
+      } else if (g_sc) {  // one decay per token and head, the same on every channel
+        gv[0] = gv[1] = gsc_s[r] * kLog2e;
+        gv[2] = gv[3] = gsc_s[r + 1] * kLog2e;
       } else {
         const float2 a = *reinterpret_cast<const float2*>(zg + (r * D + cp) * 4);
         const float2 b = *reinterpret_cast<const float2*>(zg + ((r + 1) * D + cp) * 4);
@@ -365,9 +375,11 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     issue_kqv(slots[0]);
     issue_g(slots[0]);
   }
-  if (t >= 64 && t < 128)  // beta of unit 0
-    beta_nx = (slots[0].chunk < total && t - 64 < slots[0].len)
-                  ? __bfloat162float(beta[(slots[0].t0 + t - 64) * H + slots[0].h]) : 0.f;
+  if (t >= 64 && t < 128) {  // beta (and scalar gates) of unit 0
+    const bool in = slots[0].chunk < total && t - 64 < slots[0].len;
+    beta_nx = in ? __bfloat162float(beta[(slots[0].t0 + t - 64) * H + slots[0].h]) : 0.f;
+    if (g_sc) gsc_s[t - 64] = in ? __ldg(g_sc + (slots[0].t0 + t - 64) * H + slots[0].h) : 0.f;
+  }
   if (t == kPrefetcher && slots[1].chunk < total) {  // unit 1's rows into L2
     tma_prefetch_l2_3d(&tm_k, 0, slots[1].h, (int)slots[1].t0);
     tma_prefetch_l2_3d(&tm_q, 0, slots[1].h, (int)slots[1].t0);
@@ -557,6 +569,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         }
       }
       if (kZ && t == kStorer) bulk_wait_read_all();  // the next pass 1 rewrites the Q staging
+      if (g_sc && t >= 64 && t < 128) gsc_s[t - 64] = gsc_nx;  // for the next pass 1
       named_sync(1, kPrepCompute);
       // Warps 8-15: pass 1 of the next unit while warps 0-3 form this unit's inverse.
       bool ok1 = true;
@@ -1538,8 +1551,8 @@ size_t tc_workspace_bytes(int64_t n_tokens, int n_seqs, int H, int seg_chunks) {
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const float* g,
                             const void* z, const float* A, float g_min, const void* beta,
                             const float* h0, void* o, float* hT, int64_t n_tokens, int n_seqs,
-                            int H, int seg_chunks, CkptArgs ck, FuseArgs fz, void* ws,
-                            int* err, cudaStream_t s) {
+                            int H, int seg_chunks, CkptArgs ck, FuseArgs fz, bool scalar_g,
+                            void* ws, int* err, cudaStream_t s) {
   const Plan plan = plan_in(ws, n_tokens, n_seqs);
   const int64_t units = chunks_upper_bound(n_tokens, n_seqs) * H;
   const TcLayout lay = tc_layout(ws, n_tokens, n_seqs, H, seg_chunks);
@@ -1558,14 +1571,20 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
     e = encode_rows(&tm[0], k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n_tokens);
     if (e == cudaSuccess) e = encode_rows(&tm[1], q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n_tokens);
     if (e == cudaSuccess) e = encode_rows(&tm[2], v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n_tokens);
-    if (e == cudaSuccess)
-      e = fused ? encode_rows(&tm[3], z, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n_tokens)
-                : encode_rows(&tm[3], g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, n_tokens);
+    if (e == cudaSuccess) {
+      if (fused)
+        e = encode_rows(&tm[3], z, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n_tokens);
+      else if (scalar_g)
+        tm[3] = tm[0];  // not used: scalar gates are plain loads
+      else
+        e = encode_rows(&tm[3], g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, n_tokens);
+    }
     if (e != cudaSuccess) return e;
     ProfScope prof_scope(fused ? "kda_tc_prep_gated" : "kda_tc_prep", s);
     kern<<<grid, kPrepThreads, kP_Smem, s>>>(tm[0], tm[1], tm[2], tm[3],
                                              static_cast<const T*>(beta), A, g_min, plan, H,
-                                             units, tiles, gam, fz.qk_eps, err);
+                                             units, tiles, gam, fz.qk_eps,
+                                             (scalar_g && !fused) ? g : nullptr, err);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

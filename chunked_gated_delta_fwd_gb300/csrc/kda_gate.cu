@@ -197,6 +197,32 @@ __global__ void __launch_bounds__(256) out_gate_kernel(const T* __restrict__ o,
 
 }  // namespace
 
+namespace {
+
+// Scalar gate (one log-decay per token and head, as Gated DeltaNet's gate) spread
+// over the kD channels for the fp32 chunk path: thread = 4 channels of one
+// (token, head), 16-byte stores.
+__global__ void __launch_bounds__(256) expand_scalar_gate_kernel(const float* __restrict__ gs,
+                                                                 float* __restrict__ g,
+                                                                 int64_t n_quads) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_quads;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const float x = __ldg(gs + i / (kD / 4));  // kD / 4 quads per (token, head)
+    reinterpret_cast<float4*>(g)[i] = make_float4(x, x, x, x);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_expand_scalar_gate(const float* gs, float* g, int64_t n_tokens, int H,
+                                      cudaStream_t s) {
+  const int64_t n_quads = n_tokens * H * (kD / 4);
+  if (n_quads == 0) return cudaSuccess;
+  ProfScope prof_scope("kda_expand_scalar_gate", s);
+  expand_scalar_gate_kernel<<<grid_for(n_quads, 256), 256, 0, s>>>(gs, g, n_quads);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_output_gate(const void* o, int bf16, const void* x, const float* w, float eps,
                                void* y, int64_t n_tokens, int H, cudaStream_t s) {
   const int64_t rows = n_tokens * H;

@@ -145,7 +145,7 @@ cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v, int b
 int chain_segment_chunks(int64_t n_tokens, int n_seqs, int H, int forced, bool sequential);
 size_t tc_workspace_bytes(int64_t n_tokens, int n_seqs, int H, int seg_chunks);
 // With z non-null the gate is fused: g is formed from z (bf16), A and g_min and g
-// is ignored.
+// is ignored.  With scalar_g, g is [n_tokens][H]: one log-decay per token and head.
 // State checkpoints: the state after every `every` chunks of each sequence (ckpt:
 // fp32 [cap][H][dv][dk], in sequence order); null ckpt writes none.
 struct CkptArgs {
@@ -165,7 +165,10 @@ struct FuseArgs {
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const float* g,
                             const void* z, const float* A, float g_min, const void* beta,
                             const float* h0, void* o, float* hT, int64_t n_tokens, int n_seqs,
-                            int H, int seg_chunks, CkptArgs ck, FuseArgs fz, void* ws,
-                            int* err_flag, cudaStream_t s);
+                            int H, int seg_chunks, CkptArgs ck, FuseArgs fz, bool scalar_g,
+                            void* ws, int* err_flag, cudaStream_t s);
+// g[t][h][c] = gs[t][h] for every channel c: scalar gates spread for the fp32 path.
+cudaError_t launch_expand_scalar_gate(const float* gs, float* g, int64_t n_tokens, int H,
+                                      cudaStream_t s);
 
 }  // namespace kda

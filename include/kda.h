@@ -138,7 +138,8 @@ kda_status_t kda_chunk_fwd(const void* q, const void* k, const void* v, int dtyp
 enum {
   KDA_CHUNK_FP32_CORES = 1u,     /* evaluate on fp32 CUDA cores even for bf16 inputs */
   KDA_CHUNK_SEQUENTIAL = 2u,     /* never split a sequence's chain into segments */
-  KDA_CHUNK_UNBOUNDED_GATE = 4u  /* any g <= 0 (range-robust fp32-core evaluation) */
+  KDA_CHUNK_UNBOUNDED_GATE = 4u, /* any g <= 0 (range-robust fp32-core evaluation) */
+  KDA_CHUNK_SCALAR_GATE = 8u     /* g is [NT][H]: one log-decay per token and head */
 };
 /* Split every sequence's chain into segments of n chunks (n in 1..65535). */
 #define KDA_CHUNK_SEGMENT_CHUNKS(n) (((unsigned)(n) & 0xffffu) << 16)
@@ -167,6 +168,15 @@ enum {
  * segments are rerun from them.  The result equals the serial chain up to
  * rounding.  KDA_CHUNK_SEQUENTIAL turns this off; KDA_CHUNK_SEGMENT_CHUNKS(n)
  * forces segments of n chunks.
+ *
+ * KDA_CHUNK_SCALAR_GATE: g is [NT][H] fp32, one log-decay per token and head
+ * applied to every key channel -- the scalar gate of Gated DeltaNet, which KDA
+ * refines to one decay per channel ("Kimi K3 notes", section "Kimi Delta
+ * Attention", its comparison with Gated DeltaNet).  The same precondition (-5 <= g <= 0 unless
+ * KDA_CHUNK_UNBOUNDED_GATE) holds.  The tensor-core path reads the scalars
+ * directly (4 bytes per token and head instead of 512); the fp32-core path
+ * first spreads them over the channels in the workspace.  Not combinable with a
+ * gate formed from z.
  *
  * The workspace requirement depends on the flags:
  * kda_chunk_fwd_workspace_size_ex(NT, N, H, dtype, flags).  Unknown flag bits

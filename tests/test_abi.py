@@ -71,7 +71,7 @@ def test_chunk_rejects_bad_arguments(L):
     assert _chunk(L, q=FAKE + 8) == 4
     assert _chunk(L, ws=FAKE + 16) == 4
     assert _chunk(L, ws_bytes=16) == 5
-    assert _chunk(L, flags=8) == 1
+    assert _chunk(L, flags=16) == 1  # an unknown flag bit
     assert _chunk(L, B=2, cu=FAKE, n_seqs=2) == 1  # B must be 1 with cu_seqlens
     assert _chunk(L, cu=FAKE, n_seqs=0) == 1
     assert _chunk(L, q=None) == 1
@@ -113,7 +113,7 @@ def test_chunk_checkpointed_rejects_bad_arguments(L):
     assert _ckpt(L, cap=-1) == 1
     assert _ckpt(L, ckpt=None) == 1      # no buffer for a positive capacity
     assert _ckpt(L, ckpt=FAKE + 16) == 4  # 32-byte stores
-    assert _ckpt(L, flags=8) == 1        # unknown flag bit
+    assert _ckpt(L, flags=16) == 1       # unknown flag bit
     assert b"kda_chunk_fwd_checkpointed" in L.kda_last_error_string()
 
 
@@ -140,7 +140,8 @@ def test_chunk_fused_rejects_bad_arguments(L):
     assert _fused(L, w=FAKE) == 1                  # a weight without the gate
     assert _fused(L, gate=FAKE + 8) == 4
     assert _fused(L, flags=4) == 3                 # the unbounded-gate mode is not fused
-    assert _fused(L, flags=8) == 1
+    assert _fused(L, flags=8) == 1                 # scalar gates with z
+    assert _fused(L, flags=16) == 1                # an unknown flag bit
     assert b"kda_chunk_fwd_fused" in L.kda_last_error_string()
 
 
@@ -177,6 +178,13 @@ def test_workspace_size(L):
     assert L.kda_chunk_fwd_workspace_size(-1, 1, 96, 1) == 0
     assert L.kda_chunk_fwd_workspace_size(10, 0, 96, 1) == 0
     assert L.kda_chunk_fwd_workspace_size(10, 1, 96, 5) == 0
+    # scalar gates: read as they are on the tensor-core path, spread over the
+    # channels in the workspace on the fp32-core paths
+    assert L.kda_chunk_fwd_workspace_size_ex(8192, 1, 96, 1, 8) == a
+    spread = 8192 * 96 * 128 * 4
+    assert L.kda_chunk_fwd_workspace_size_ex(8192, 1, 96, 0, 8) >= b + spread
+    assert L.kda_chunk_fwd_workspace_size_ex(8192, 1, 96, 1, 9) >= \
+        L.kda_chunk_fwd_workspace_size_ex(8192, 1, 96, 1, 1) + spread
     # grows with tokens and heads
     assert L.kda_chunk_fwd_workspace_size(16384, 1, 96, 1) > a
     assert L.kda_chunk_fwd_workspace_size(8192, 1, 97, 1) > a

@@ -475,6 +475,49 @@ def test_scalar_gate_gated_deltanet(kda):
     assert_close(hT, h_ref, torch.bfloat16, "hT GDN")
 
 
+@pytest.mark.parametrize("dtype,flags", PATHS, ids=PATH_IDS)
+def test_scalar_gate_layout(kda, dtype, flags):
+    """SCALAR_GATE: g given as [NT, H] (one log-decay per token and head, 4 bytes
+    instead of 512 per token-head) on every path, against the oracle run with that
+    decay on every channel; on the tensor-core path the result equals the run with
+    the broadcast [NT, H, 128] g bit for bit."""
+    lens = [300, 0, 64, 5, 129]
+    inp, g, dev = _inputs(lens, H=3, dtype=dtype, seed=98)
+    g1 = g[..., 0].contiguous()                       # [NT, H]
+    gb = g1[..., None].expand_as(g).contiguous()      # the same decay on every channel
+    o, hT = kda.chunk_fwd(dev["q"], dev["k"], dev["v"], g1.cuda(), dev["beta"], dev["h0"],
+                          dev["cu_seqlens"], flags=flags | kda.SCALAR_GATE)
+    o_ref, h_ref = oracle.recurrence(inp["q"], inp["k"], inp["v"], gb, inp["beta"], inp["h0"],
+                                     inp["cu_seqlens"])
+    assert_close(o, o_ref, dtype, "o scalar gate")
+    assert_close(hT, h_ref, dtype, "hT scalar gate")
+    ob, hb = kda.chunk_fwd(dev["q"], dev["k"], dev["v"], gb.cuda(), dev["beta"], dev["h0"],
+                           dev["cu_seqlens"], flags=flags)
+    assert torch.equal(o, ob) and torch.equal(hT, hb)
+
+
+def test_scalar_gate_unbounded_and_checkpoints(kda):
+    """Scalar gates with the unbounded mode (decays down to -40 per token) and with
+    state checkpoints on the tensor-core path."""
+    inp, g, dev = _inputs([256, 70], H=2, dtype=torch.bfloat16, seed=99, g_lo=-40.0)
+    g1 = g[..., 0].contiguous()
+    gb = g1[..., None].expand_as(g).contiguous()
+    o, hT = kda.chunk_fwd(dev["q"], dev["k"], dev["v"], g1.cuda(), dev["beta"], dev["h0"],
+                          dev["cu_seqlens"], flags=kda.SCALAR_GATE | kda.UNBOUNDED_GATE)
+    o_ref, h_ref = oracle.recurrence(inp["q"], inp["k"], inp["v"], gb, inp["beta"], inp["h0"],
+                                     inp["cu_seqlens"])
+    assert_close(o, o_ref, torch.bfloat16, "o scalar unbounded")
+    assert_close(hT, h_ref, torch.bfloat16, "hT scalar unbounded")
+    gc = (g1 / 8).cuda()  # inside [-5, 0] for the tensor-core path
+    o1, h1, c1 = kda.chunk_fwd_checkpointed(dev["q"], dev["k"], dev["v"], gc, dev["beta"],
+                                            dev["h0"], dev["cu_seqlens"], ckpt_tokens=128,
+                                            flags=kda.SCALAR_GATE)
+    gcb = gc[..., None].expand(-1, -1, 128).contiguous()
+    o2, h2, c2 = kda.chunk_fwd_checkpointed(dev["q"], dev["k"], dev["v"], gcb, dev["beta"],
+                                            dev["h0"], dev["cu_seqlens"], ckpt_tokens=128)
+    assert torch.equal(o1, o2) and torch.equal(h1, h2) and torch.equal(c1, c2)
+
+
 def test_each_path_launches_only_its_own_kernels(kda):
     """The bf16 entry runs the plan and the tensor-core kernels only; the fp32-core
     flag runs the CUDA-core kernels only (a second path on the same workspace would
