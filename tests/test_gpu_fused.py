@@ -95,6 +95,30 @@ def test_fused_with_g_and_segments(kda):
            "fused segmented")
 
 
+def test_fused_scalar_gate_equals_broadcast(kda):
+    """Scalar gates ([NT, H], SCALAR_GATE) with q/k normalisation and the output
+    gate give the same bits as the broadcast [NT, H, 128] gate; with q/k
+    normalisation alone they agree with the oracle.  (One decay for all channels
+    forgets the state in every channel at once, so a few rows of o come out ~100x
+    below the median; the output RMSNorm scales each row to unit size and would
+    weigh those rows' rounding 100x, which says nothing about the kernels.)"""
+    lens = [300, 0, 77]
+    inp, dev = _case(lens, H=2, seed=86)
+    g1 = workloads.uniform_decay((sum(lens), 2), "cpu", seed=87)
+    gb = g1[..., None].expand(-1, -1, 128).contiguous()
+    kw = dict(qk_l2_eps=1e-6, out_gate=dev["gz"], out_norm_weight=dev["w"], out_norm_eps=1e-6)
+    o1, h1 = kda.chunk_fwd_fused(dev["q"], dev["k"], dev["v"], dev["beta"], dev["h0"],
+                                 dev["cu_seqlens"], g=g1.cuda(), flags=kda.SCALAR_GATE, **kw)
+    o2, h2 = kda.chunk_fwd_fused(dev["q"], dev["k"], dev["v"], dev["beta"], dev["h0"],
+                                 dev["cu_seqlens"], g=gb.cuda(), **kw)
+    assert torch.equal(o1, o2) and torch.equal(h1, h2)
+    o3, h3 = kda.chunk_fwd_fused(dev["q"], dev["k"], dev["v"], dev["beta"], dev["h0"],
+                                 dev["cu_seqlens"], g=g1.cuda(), flags=kda.SCALAR_GATE,
+                                 qk_l2_eps=1e-6)
+    _check(o3, h3, inp, _reference(inp, 1e-6, False, False, 1e-6, g=gb), False, False, 1e-6,
+           "fused scalar gate")
+
+
 def test_fused_without_options_equals_gated(kda):
     """No normalisation and no output gate: the same kernels as kda_chunk_fwd_gated,
     bit for bit."""
