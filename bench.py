@@ -18,7 +18,8 @@ The JSON line also carries
     (pinned host -> device copies of the step's inputs, device -> host copy of
     o and hT inside the timed region; device buffers are double-buffered so that
     one step's upload overlaps the previous step's compute and download);
-  * cpu_baseline -- the fp64 oracle on the host cores over a bounded sample.
+  * cpu_baseline -- the fp64 oracle on the host cores over a bounded sample, and
+    (one_thread) on a single thread over two heads.
 
 ``--impl reference`` times the oracle alone (the reference arm of this build).
 """
@@ -312,10 +313,17 @@ def cpu_baseline(heads=96, T=8192, seed=1002):
     g = oracle.gate(z, A)
     oracle.recurrence(q, k, v, g, beta, None, n_threads=cores)
     dt = time.perf_counter() - t0
+    # the same oracle on one thread, over the first two heads
+    t1 = time.perf_counter()
+    oracle.recurrence(q[:, :2], k[:, :2], v[:, :2], g[:, :2], beta[:, :2], None, n_threads=1)
+    dt1 = time.perf_counter() - t1
     return {"value": T * heads / dt / 96, "unit": "tokens/s", "cores": min(cores, heads),
             "kind": "oracle",
             "sample": f"gate + fp64 recurrence, {heads} heads x {T} tokens "
-                      f"({dt:.1f} s), scaled to H=96"}
+                      f"({dt:.1f} s), scaled to H=96",
+            "one_thread": {"value": T * 2 / dt1 / 96, "unit": "tokens/s",
+                           "sample": f"fp64 recurrence, 2 heads x {T} tokens ({dt1:.2f} s), "
+                                     f"scaled to H=96"}}
 
 
 def run_gpu(args):
