@@ -69,8 +69,9 @@ def state_bytes(dk: int = D, dv: int = D) -> int:
 
 
 def decode_bytes_per_head_step(dk: int = D, dv: int = D) -> int:
-    """Decode: fp32 state read + written, q, k, v, o (bf16), g (fp32), beta (bf16)."""
-    return 2 * state_bytes(dk, dv) + dk * 2 * 3 + dk * 4 + 2
+    """Decode: fp32 state read + written, q, k (bf16, dk each), v and o (bf16, dv
+    each), g (fp32, dk), beta (bf16)."""
+    return 2 * state_bytes(dk, dv) + 2 * dk * 2 + 2 * dv * 2 + dk * 4 + 2
 
 
 def load_peaks():
@@ -280,7 +281,11 @@ def run_reference(args):
     line = {
         "impl": "reference", "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": per_step * 1e3 * w.H / heads, "higher_is_better": True,
+        # measured: one step is the sample below (heads of the 96), median over steps
+        "ms_per_step": per_step * 1e3,
+        # the same time scaled to all 96 heads (the time a whole step would take)
+        "ms_per_step_scaled_to_all_heads": per_step * 1e3 * w.H / heads,
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "sample": f"{heads} of {w.H} heads x {T} tokens",
                    "global_batch": 1, "seq_len": T, "parallelism": "none (host cores)"},
@@ -402,26 +407,30 @@ def run_gpu(args):
     dom_avg_ms = dom_ms / dom_n
     tok_heads = NT * H
     units = (NT // 64) * H  # (chunk, head) units of this single-sequence workload
-    kernel_bytes = {
-        "kda_gate": tok_heads * gate_bytes_per_token_head(2),
-        # inputs q, k, v, g, beta in; MMA-ready tiles (72 KiB) + gamma (512 B) out per unit
-        "kda_tc_prep": tok_heads * (prefill_bytes_per_token_head(2) - D * 2)
-        + units * (TC_UNIT_BYTES + D * 4),
-        # inputs q, k, v, z, beta in; the same tiles out
-        "kda_tc_prep_gated": tok_heads * (fused_prefill_bytes_per_token_head(2) - D * 2)
-        + units * (TC_UNIT_BYTES + D * 4),
-        # tiles + gamma in, o out, h0 in and hT out per (sequence, head)
-        "kda_tc_chain": units * (TC_UNIT_BYTES + D * 4) + tok_heads * D * 2
-        + 2 * H * state_bytes(),
-    }
-    alg_bytes = kernel_bytes.get(dom_name)
-    achieved = alg_bytes / (dom_avg_ms * 1e-3) / 1e9 if alg_bytes else None
+    # The method's algorithmic bytes for one step (the inputs read once, o and hT
+    # written once, h0 read once; no workspace intermediates): 1,282 B per
+    # token-head with the gate fused (z in bf16), 1,538 B with g read in fp32 (plus
+    # the gate kernel's own z read and g write on the separate path).
     if fused:
         step_bytes = tok_heads * fused_prefill_bytes_per_token_head(2) + 2 * H * state_bytes()
     else:
         step_bytes = tok_heads * (prefill_bytes_per_token_head(2)
                                   + gate_bytes_per_token_head(2)) + 2 * H * state_bytes()
     step_floor_ms = step_bytes / (hbm_peak * 1e9) * 1e3
+    # Each kernel's own input/output bytes, workspace tiles included (what a
+    # kernel on its own would have to move; context for the measured traffic).
+    tile_bytes = units * (TC_UNIT_BYTES + D * 4)
+    kernel_io_bytes = {
+        "kda_gate": tok_heads * gate_bytes_per_token_head(2),
+        "kda_tc_prep": tok_heads * (prefill_bytes_per_token_head(2) - D * 2) + tile_bytes,
+        "kda_tc_prep_gated": tok_heads * (fused_prefill_bytes_per_token_head(2) - D * 2)
+        + tile_bytes,
+        "kda_tc_chain": tile_bytes + tok_heads * D * 2 + 2 * H * state_bytes(),
+    }
+    # The roofline line follows the method's byte count: the step's algorithmic
+    # bytes over the dominant kernel's mean launch time (one launch per step).
+    alg_bytes = step_bytes
+    achieved = alg_bytes / (dom_avg_ms * 1e-3) / 1e9
 
     # decode step (512 x 96, fp32 state, in place)
     dw = workloads.decode()
@@ -626,6 +635,14 @@ def run_gpu(args):
     cpu = None
     if not args.no_cpu_baseline:
         cpu = cpu_baseline()
+    traffic = kernel_traffic(dom_name)
+    # measured DRAM bytes of one step: the captured kernels (the plan kernel moves a
+    # few KB and is not captured), per launch x launches per step
+    step_traffic = None
+    big = [k_ for k_ in per_kernel if k_ != "kda_plan"]
+    parts = [kernel_traffic(k_) for k_ in big]
+    if parts and all(p_ is not None for p_ in parts):
+        step_traffic = sum(p_ * per_kernel[k_][0] / args.steps for p_, k_ in zip(parts, big))
     line = {
         "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -638,12 +655,20 @@ def run_gpu(args):
                    "l2": "inputs larger than L2 (201 MB per q/k/v/z tensor), no flush",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": achieved,
-                     "peak": hbm_peak, "unit": "GB/s",
-                     "frac": (achieved / hbm_peak) if achieved else None,
-                     "traffic": kernel_traffic(dom_name),
-                     "alg_bytes_per_launch": alg_bytes, "mean_launch_ms": dom_avg_ms,
-                     "peak_source": f"{peak_src} hbm_gbs",
-                     "step_floor_ms": step_floor_ms, "step_frac": step_floor_ms / ms_step},
+                     "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                     "traffic": traffic,
+                     "traffic_over_alg": (traffic / alg_bytes) if traffic else None,
+                     "alg_bytes_per_launch": alg_bytes,
+                     "alg_bytes_rule": ("step bytes of the method per launch: "
+                                        + ("1282" if fused else "1538 + 768 (gate)")
+                                        + " B per token-head x token-heads + h0 and hT"),
+                     "kernel_io_bytes": kernel_io_bytes.get(dom_name),
+                     "mean_launch_ms": dom_avg_ms,
+                     "peak_source": f"{peak_src} hbm_gbs (copy, burst)",
+                     "step_floor_ms": step_floor_ms, "step_frac": step_floor_ms / ms_step,
+                     "step_traffic": step_traffic,
+                     "step_traffic_over_alg": (step_traffic / step_bytes) if step_traffic
+                     else None},
         "kernels": {k: {"launches": n, "mean_ms": t / n} for k, (n, t) in per_kernel.items()},
         "alt_step": {"step": "kda_gate + kda_chunk_fwd" if fused
                      else "kda_chunk_fwd_gated (gate fused)", "ms_per_step": ms_alt,

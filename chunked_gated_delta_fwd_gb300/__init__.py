@@ -29,7 +29,7 @@ __all__ = ["KdaError", "gate", "chunk_fwd", "chunk_fwd_gated", "chunk_fwd_worksp
            "library_path", "lib", "get_device_error", "profile_enable", "profile_collect", "G_MIN", "F32", "BF16", "FP32_CORES", "SEQUENTIAL",
            "segment_chunks", "recurrent_multi_step", "chunk_fwd_checkpointed",
            "chunk_fwd_fused", "gate_softplus", "UNBOUNDED_GATE",
-           "output_gate"]
+           "output_gate", "SCALAR_GATE", "CHECK_INPUTS", "selftest_wait_timeout"]
 
 G_MIN = -5.0
 F32, BF16 = 0, 1
@@ -37,6 +37,7 @@ FP32_CORES = 1  # flag of chunk_fwd: evaluate bf16 inputs on fp32 CUDA cores
 SEQUENTIAL = 2  # flag of chunk_fwd: never split a sequence's chain into segments
 UNBOUNDED_GATE = 4  # flag of chunk_fwd: any g <= 0 (range-robust fp32-core evaluation)
 SCALAR_GATE = 8  # flag of chunk_fwd: g is [..., H], one log-decay per token and head
+CHECK_INPUTS = 16  # flag of chunk_fwd: check g and beta against their ranges on the device
 
 _STATUS = {
     0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED_SHAPE",
@@ -82,6 +83,8 @@ def _load() -> ctypes.CDLL:
     L.kda_recurrent_step.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, vp]
     L.kda_recurrent_multi_step.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, i32, i32, i32,
                                            i32, i32, vp]
+    L.kda_selftest_wait_timeout.argtypes = [u32, ctypes.POINTER(i32), vp]
+    L.kda_selftest_wait_timeout.restype = ctypes.c_int
     L.kda_last_error_string.restype = ctypes.c_char_p
     L.kda_get_device_error.argtypes = [vp]
     L.kda_version.restype = ctypes.c_char_p
@@ -412,6 +415,18 @@ def profile_collect() -> dict:
         lib.kda_profile_get(i, ctypes.byref(name), ctypes.byref(launches), ctypes.byref(total))
         out[name.value.decode()] = (launches.value, total.value)
     return out
+
+
+def selftest_wait_timeout(timeout_us: int = 1000, device=None) -> int:
+    """Runs the library's bounded-wait self-test (a kernel whose waits nothing
+    signals gives up after ``timeout_us``); synchronizes and returns how many of
+    its four waiting warps saw the wait end unsatisfied.  The device error flag is
+    left set to KDA_ERR_DEVICE_TIMEOUT for :func:`get_device_error`."""
+    device = device or torch.device("cuda", torch.cuda.current_device())
+    n = ctypes.c_int(-1)
+    with torch.cuda.device(device):
+        _check(lib.kda_selftest_wait_timeout(int(timeout_us), ctypes.byref(n), _stream(device)))
+    return n.value
 
 
 def get_device_error(device=None):

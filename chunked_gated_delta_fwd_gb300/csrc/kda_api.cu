@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cuda_runtime.h>
 #include <stdarg.h>
+#include <stdlib.h>
 #include <stdint.h>
 #include <stdio.h>
 #include <string.h>
@@ -218,6 +219,16 @@ kda_status_t cuda_fail(cudaError_t e, const char* what) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// KDA_CHECKS=1 (any value but "0" or empty) in the environment turns the input
+// precondition pass on for every chunk call; read once per process.
+bool checks_from_env() {
+  static const bool on = [] {
+    const char* v = getenv("KDA_CHECKS");
+    return v && v[0] && strcmp(v, "0") != 0;
+  }();
+  return on;
+}
+
 // Byte offset, in the workspace of the fp32-core path, of the scalar gates spread
 // over the channels (after the plan and that path's own scratch, 256-aligned).
 size_t simt_scalar_gate_offset(int64_t n_tokens, int n_seqs, int H) {
@@ -319,7 +330,28 @@ kda_status_t kda_get_device_error(kda_stream_t stream) {
   if (host == kda::kDevErrBadSeqlens)
     return fail(KDA_ERR_INVALID_ARG,
                 "cu_seqlens was not nondecreasing from 0 to n_tokens (clamped on the device)");
+  if (host == kda::kDevErrPrecondition)
+    return fail(KDA_ERR_INVALID_ARG,
+                "input check: a log-decay g outside [-5, 0] (outside (-inf, 0] with "
+                "KDA_CHUNK_UNBOUNDED_GATE) or a beta outside [0, 1], or a NaN");
   return fail(KDA_ERR_CUDA, "device error code %d", host);
+}
+
+kda_status_t kda_selftest_wait_timeout(uint32_t timeout_us, int* warps_gave_up,
+                                       kda_stream_t stream) {
+  if (timeout_us < 1 || timeout_us > 1000000u)
+    return fail(KDA_ERR_INVALID_ARG, "kda_selftest_wait_timeout: timeout_us=%u (1..1000000)",
+                timeout_us);
+  if (!warps_gave_up) return fail(KDA_ERR_INVALID_ARG, "kda_selftest_wait_timeout: null output");
+  kda_status_t st = check_device();
+  if (st != KDA_OK) return st;
+  int* flag = kda::device_error_flag();
+  if (!flag) return fail(KDA_ERR_CUDA, "device error flag unavailable");
+  const cudaError_t e = kda::launch_wait_selftest((uint64_t)timeout_us * 1000u, flag,
+                                                  warps_gave_up,
+                                                  reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kda_selftest_wait_timeout");
+  return KDA_OK;
 }
 
 kda_status_t kda_gate(const void* z, int z_dtype, const float* A, float g_min, float* g,
@@ -463,7 +495,8 @@ kda_status_t chunk_fwd_impl(const char* fn, const void* q, const void* k, const 
     return fail(KDA_ERR_WORKSPACE_TOO_SMALL, "%s: workspace %zu < %zu bytes", fn,
                 ws_bytes, need);
   if (flags & ~(unsigned)(KDA_CHUNK_FP32_CORES | KDA_CHUNK_SEQUENTIAL |
-                          KDA_CHUNK_UNBOUNDED_GATE | KDA_CHUNK_SCALAR_GATE | 0xffff0000u))
+                          KDA_CHUNK_UNBOUNDED_GATE | KDA_CHUNK_SCALAR_GATE |
+                          KDA_CHUNK_CHECK_INPUTS | 0xffff0000u))
     return fail(KDA_ERR_INVALID_ARG, "%s: unknown flags 0x%x", fn, flags);
   if ((flags & KDA_CHUNK_UNBOUNDED_GATE) && z)
     return fail(KDA_ERR_INVALID_ARG, "%s: the unbounded-gate mode takes g, not z", fn);
@@ -474,7 +507,16 @@ kda_status_t chunk_fwd_impl(const char* fn, const void* q, const void* k, const 
   if (st != KDA_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int* err = kda::device_error_flag();
-  cudaError_t e = kda::launch_plan(cu_seqlens, N, T_per_seq, NT, workspace, err, s);
+  cudaError_t e;
+  if (((flags & KDA_CHUNK_CHECK_INPUTS) || checks_from_env()) && NT > 0) {
+    // the precondition pass: g in [-5, 0] (any finite g <= 0 in the unbounded mode)
+    // and beta in [0, 1]; a gate formed from z is in range by construction
+    const float g_lo = (flags & KDA_CHUNK_UNBOUNDED_GATE) ? -3.402823466e38f : -5.f;
+    const int64_t n_g = g ? NT * H * (scalar_g ? 1 : kda::kD) : 0;
+    e = kda::launch_check_inputs(g, n_g, g_lo, beta, dtype == KDA_BF16, NT * H, err, s);
+    if (e != cudaSuccess) return cuda_fail(e, "input check launch");
+  }
+  e = kda::launch_plan(cu_seqlens, N, T_per_seq, NT, workspace, err, s);
   if (e != cudaSuccess) return cuda_fail(e, "chunk plan launch");
   if (dtype == KDA_BF16 && !(flags & (KDA_CHUNK_FP32_CORES | KDA_CHUNK_UNBOUNDED_GATE))) {
     e = kda::launch_chunk_tc(q, k, v, g, z, A, g_min, beta, h0, o, hT, NT, N, H,

@@ -849,8 +849,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
   }
   if (t == kStorer) bulk_wait_all();
   // a copy still in flight (after an abort) must land before the CTA may exit
-  if (t == kIssuer && issued_kqv > 0) mbar_wait(bar_kqv, (issued_kqv - 1) & 1, nullptr);
-  if (t == kIssuer && issued_g > 0) mbar_wait(bar_g, (issued_g - 1) & 1, nullptr);
+  if (t == kIssuer && issued_kqv > 0) mbar_wait(bar_kqv, (issued_kqv - 1) & 1, err);
+  if (t == kIssuer && issued_g > 0) mbar_wait(bar_g, (issued_g - 1) & 1, err);
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
@@ -872,23 +872,6 @@ constexpr int kStore = 128;  // store warps 8-11: TMEM lane = value row, all 64 
 constexpr int kCopyWarp = (kEpi + kStore) / 32;  // warp 12: tile copies
 constexpr int kOutWarp = kCopyWarp + 1;            // warp 13: the output MMAs
 constexpr int kChainThreads = kEpi + kStore + 64;
-
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int* err,
-                                              volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0) {
-      if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitTimeoutNs) {
-        if (err) atomicExch(err, kDevErrTimeout);
-        *abort_flag = 1;
-        return false;
-      }
-    }
-  }
-}
 
 // Sequence-segment parallel chain (the KCP algebra applied inside one GPU: "Kimi
 // K3 technical report review", section 8.1 Eq. 17).  A long sequence is cut into P
@@ -1036,7 +1019,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       if (*abort_flag) {
         // copies already issued must land before the CTA exits
         for (int jj = max(0, issued - kStages); jj < issued; ++jj)
-          mbar_wait(bar_full0 + 8 * (jj % kStages), (jj / kStages) & 1, nullptr);
+          mbar_wait(bar_full0 + 8 * (jj % kStages), (jj / kStages) & 1, err);
       }
     }
   } else if (warp == kOutWarp) {
@@ -1074,7 +1057,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       }
       if (*abort_flag && any_mma) {  // drain MMAs in flight
         mma_commit(bar_dr + 8);
-        mbar_wait(bar_dr + 8, 0, nullptr);
+        mbar_wait(bar_dr + 8, 0, err);
       }
     }
   } else if (warp < kEpi / 32) {
@@ -1209,7 +1192,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     }
     if ((t == 0 || t == 64) && *abort_flag && any_mma) {  // drain MMAs in flight
       mma_commit(bar_dr + 8 * (t >> 5));
-      mbar_wait(bar_dr + 8 * (t >> 5), 0, nullptr);
+      mbar_wait(bar_dr + 8 * (t >> 5), 0, err);
     }
     if (alive && nch > 0 && wait_or_abort(bar_m2, (nch - 1) & 1, err, abort_flag))
       tc_fence_after();

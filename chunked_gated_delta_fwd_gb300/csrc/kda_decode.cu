@@ -11,8 +11,11 @@
 //     o_j   = q . s_j = r + beta (v_j - p) (q . k)
 // One CTA per (sequence, head), four warps, each warp streams 32 rows; lane l
 // holds channels 4l..4l+3, so a row is one coalesced 128-bit load and one
-// 128-bit store per lane.  p and r are reduced together with butterfly
-// shuffles.  The kernel is HBM-bound: 2 x 64 KiB of state per head and step.
+// 128-bit store per lane.  The per-row dot products p and r of a warp's 8 rows
+// in flight are reduce-scattered across the lanes (each halving step swaps half
+// of the partial sums with a partner lane, 9 shuffles for 8 rows); p is then
+// gathered back to every lane, r stays with the lane that writes o_j.  The
+// kernel is HBM-bound: 2 x 64 KiB of state per head and step.
 #include "kda_internal.cuh"
 
 namespace kda {

@@ -19,6 +19,7 @@ constexpr int kDevErrNone = 0;
 constexpr int kDevErrTimeout = 7;
 constexpr int kDevErrBadSeqlens = 1;
 constexpr int kDevErrCkptCapacity = 2;
+constexpr int kDevErrPrecondition = 3;  // an input outside its stated range (checks pass)
 
 // Address of this device's error flag (int on the device), or nullptr.
 int* device_error_flag();
@@ -167,6 +168,16 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
                             const float* h0, void* o, float* hT, int64_t n_tokens, int n_seqs,
                             int H, int seg_chunks, CkptArgs ck, FuseArgs fz, bool scalar_g,
                             void* ws, int* err_flag, cudaStream_t s);
+// Input-precondition pass: raises kDevErrPrecondition in *err if any of the n_g
+// log-decays g is outside [g_lo, 0] or any of the n_beta write strengths outside
+// [0, 1] (NaN counts as outside).  g or beta may be null (nothing to check).
+cudaError_t launch_check_inputs(const float* g, int64_t n_g, float g_lo, const void* beta,
+                                int beta_bf16, int64_t n_beta, int* err, cudaStream_t s);
+// Bounded-wait self-test: a kernel whose waits nothing signals gives up after
+// timeout_ns (recording kDevErrTimeout in *err); synchronizes s and returns in
+// *warps_gave_up how many of its four waiting warps saw their wait end unsatisfied.
+cudaError_t launch_wait_selftest(uint64_t timeout_ns, int* err, int* warps_gave_up,
+                                 cudaStream_t s);
 // g[t][h][c] = gs[t][h] for every channel c: scalar gates spread for the fp32 path.
 cudaError_t launch_expand_scalar_gate(const float* gs, float* g, int64_t n_tokens, int H,
                                       cudaStream_t s);

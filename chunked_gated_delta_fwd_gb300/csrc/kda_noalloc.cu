@@ -65,24 +65,23 @@ kda_status_t kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v, 
                                    const int32_t* cu_seqlens, int n_seqs, int B, int64_t T,
                                    int H, int dk, int dv, void* o, float* hT,
                                    kda_stream_t stream) {
-  const int N = cu_seqlens ? n_seqs : B;
-  const int64_t NT = cu_seqlens ? T : (int64_t)B * T;
-  const size_t need = kda_chunk_fwd_workspace_size(NT, N, H, dtype);
-  if (need > kScratchBytes) {
-    kda::set_error_message(
-        "kda_chunk_fwd_noalloc: this problem needs more scratch than the library's fixed "
-        "device array holds (KDA_NOALLOC_SCRATCH_BYTES); use kda_chunk_fwd with a workspace");
-    return KDA_ERR_WORKSPACE_TOO_SMALL;
-  }
   cudaError_t e = cudaSuccess;
   void* ws = scratch_address(&e);
   if (!ws) {
     kda::set_error_message("kda_chunk_fwd_noalloc: cannot resolve the scratch array's address");
     return KDA_ERR_CUDA;
   }
-  // Argument checks, the workspace-size check and the launches are kda_chunk_fwd's own.
-  return kda_chunk_fwd(q, k, v, dtype, g, beta, h0, cu_seqlens, n_seqs, B, T, H, dk, dv, o, hT,
-                       ws, kScratchBytes, stream);
+  // kda_chunk_fwd checks every argument first (shapes, dtypes, pointers, alignment)
+  // and only then compares its workspace need with the array's capacity, so a
+  // malformed call gets its own error and a well-formed one that is too large
+  // gets KDA_ERR_WORKSPACE_TOO_SMALL; either way nothing has been enqueued.
+  const kda_status_t st = kda_chunk_fwd(q, k, v, dtype, g, beta, h0, cu_seqlens, n_seqs, B, T,
+                                        H, dk, dv, o, hT, ws, kScratchBytes, stream);
+  if (st == KDA_ERR_WORKSPACE_TOO_SMALL)
+    kda::set_error_message(
+        "kda_chunk_fwd_noalloc: this problem needs more scratch than the library's fixed "
+        "device array holds (KDA_NOALLOC_SCRATCH_BYTES); use kda_chunk_fwd with a workspace");
+  return st;
 }
 
 }  // extern "C"

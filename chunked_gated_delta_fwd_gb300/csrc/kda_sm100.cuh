@@ -61,15 +61,38 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 // Waits for the phase with the given parity to complete.  Returns false (and
-// records kDevErrTimeout in *err) if it has not after kWaitTimeoutNs.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err) {
+// records kDevErrTimeout in *err) if it has not after `timeout_ns`.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err,
+                                          uint64_t timeout_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0 && global_timer_ns() - t0 > kWaitTimeoutNs) {
+    if ((it & 255u) == 0 && global_timer_ns() - t0 > timeout_ns) {
       if (err) atomicExch(err, kDevErrTimeout);
       return false;
+    }
+  }
+}
+
+// mbar_wait for a CTA whose threads wait on different barriers: a wait also ends
+// (returning false) as soon as another thread of the CTA has raised *abort_flag,
+// and a wait that runs out raises it, so that every waiting thread of the CTA
+// stops within a few polls of the first one that gives up.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int* err,
+                                              volatile int* abort_flag,
+                                              uint64_t timeout_ns = kWaitTimeoutNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > timeout_ns) {
+        if (err) atomicExch(err, kDevErrTimeout);
+        *abort_flag = 1;
+        return false;
+      }
     }
   }
 }

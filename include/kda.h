@@ -112,7 +112,9 @@ size_t kda_chunk_fwd_workspace_size_ex(int64_t n_tokens, int n_seqs, int H, int 
  *   g        [NT][H][dk] fp32 log-decays.  PRECONDITION: g_min_bound <= g <= 0 with
  *            g_min_bound = -5 (the output range of kda_gate with g_min = -5); the
  *            16-token tile range argument of the K3 report relies on it.  Values
- *            outside are not checked and give unspecified (possibly non-finite) output.
+ *            outside give unspecified (possibly non-finite) output; they are
+ *            detected only by the optional input check (KDA_CHUNK_CHECK_INPUTS of
+ *            kda_chunk_fwd_ex, or KDA_CHECKS=1 in the environment).
  *   beta     [NT][H], dtype, write strengths (expected in [0, 1])
  *   h0       optional [N][H][dv][dk] fp32 initial states (NULL = zero state)
  *   cu_seqlens optional device int32 [N+1], nondecreasing, cu[0] = 0, cu[N] = NT;
@@ -139,7 +141,8 @@ enum {
   KDA_CHUNK_FP32_CORES = 1u,     /* evaluate on fp32 CUDA cores even for bf16 inputs */
   KDA_CHUNK_SEQUENTIAL = 2u,     /* never split a sequence's chain into segments */
   KDA_CHUNK_UNBOUNDED_GATE = 4u, /* any g <= 0 (range-robust fp32-core evaluation) */
-  KDA_CHUNK_SCALAR_GATE = 8u     /* g is [NT][H]: one log-decay per token and head */
+  KDA_CHUNK_SCALAR_GATE = 8u,    /* g is [NT][H]: one log-decay per token and head */
+  KDA_CHUNK_CHECK_INPUTS = 16u   /* check the g and beta preconditions on the device */
 };
 /* Split every sequence's chain into segments of n chunks (n in 1..65535). */
 #define KDA_CHUNK_SEGMENT_CHUNKS(n) (((unsigned)(n) & 0xffffu) << 16)
@@ -177,6 +180,17 @@ enum {
  * directly (4 bytes per token and head instead of 512); the fp32-core path
  * first spreads them over the channels in the workspace.  Not combinable with a
  * gate formed from z.
+ *
+ * KDA_CHUNK_CHECK_INPUTS (also turned on for every chunk call by the environment
+ * variable KDA_CHECKS=1, read once per process): before the prefill, one pass
+ * over g and beta checks the preconditions the method relies on -- every
+ * log-decay in [-5, 0] (the bounded gate, "Kimi K3 technical report review",
+ * section 3.2; in the unbounded mode only g <= 0 and finite) and every beta in
+ * [0, 1] (a sigmoid output) -- and raises the device error flag if one fails or
+ * is NaN; kda_get_device_error then returns KDA_ERR_INVALID_ARG.  The prefill
+ * still runs (its output is then unspecified).  With a gate formed from z only
+ * beta is checked.  The pass reads g and beta once (about 60 us for the
+ * B=1, T=8192, H=96 workload) and is off by default.
  *
  * The workspace requirement depends on the flags:
  * kda_chunk_fwd_workspace_size_ex(NT, N, H, dtype, flags).  Unknown flag bits
@@ -368,9 +382,28 @@ kda_status_t kda_recurrent_multi_step(const void* q, const void* k, const void* 
 /* Message for the last non-OK status returned on this thread (never NULL). */
 const char* kda_last_error_string(void);
 
-/* Reads and clears the device error flag set by bounded waits in the kernels.
- * Synchronizes `stream`.  Returns KDA_OK or KDA_ERR_DEVICE_TIMEOUT. */
+/* Reads and clears the device error flag set by the kernels.  Synchronizes
+ * `stream`.  Returns KDA_OK; KDA_ERR_DEVICE_TIMEOUT when a bounded device-side
+ * wait gave up; KDA_ERR_INVALID_ARG when cu_seqlens was malformed (clamped on
+ * the device), more checkpoints than slots were asked for, or the input check
+ * (KDA_CHUNK_CHECK_INPUTS) found an out-of-range g or beta. */
 kda_status_t kda_get_device_error(kda_stream_t stream);
+
+/*
+ * kda_selftest_wait_timeout -- exercises the bounded-wait path that every
+ * tensor-core kernel uses (no counterpart on the KDA pages: it is the library's
+ * failure-detection self-test).  One CTA of four warps waits, through the same
+ * wait routine as the prefill kernels, on a barrier that nothing signals, with
+ * a limit of timeout_us microseconds (1 .. 1,000,000), while a real bulk copy is
+ * in flight.  The first wait to run out records KDA_ERR_DEVICE_TIMEOUT in the
+ * device error flag and raises the CTA's abort word, the other warps stop, the
+ * copy is drained, and the kernel returns: nothing is left waiting and the
+ * context stays usable.  Synchronizes `stream`; *warps_gave_up (host int) is
+ * the number of warps (4 expected) whose wait ended unsatisfied.  The flag is
+ * left set for kda_get_device_error to read.
+ */
+kda_status_t kda_selftest_wait_timeout(uint32_t timeout_us, int* warps_gave_up,
+                                       kda_stream_t stream);
 
 /*
  * Per-kernel timing with CUDA events (a tracing aid; off by default).

@@ -249,24 +249,47 @@ def test_gated_rejects_fp32(kda):
                             dev["cu_seqlens"])
 
 
-def test_long_context_prefix(kda):
-    """T=1,048,576, H=16 workload: the 4096-token prefix against the oracle, and the
-    first 4096 outputs of a 16384-token run equal the prefix run (causality)."""
-    w = workloads.long_context(T=16384)
+def test_long_context_full_instance(kda):
+    """The long-context workload itself (B=1, T=1,048,576, H=16, z ~ N(0, 2)) run as
+    the benchmark runs it -- kda_chunk_fwd_gated, the chain cut into automatic
+    segments joined by the end-state scan ("Kimi K3 technical report review",
+    section 8.1, Eq. 17):
+      * its first 4096 outputs equal a run on the 4096-token prefix (causality),
+        and that prefix run matches the oracle on every head;
+      * one head's o over all 1,048,576 tokens and its final state match the oracle
+        (token-by-token fp64 recurrence, about half a minute on one host thread);
+      * every head's final state matches the serial chain (KDA_CHUNK_SEQUENTIAL)."""
+    w = workloads.long_context()
     dev = workloads.make_inputs(w, "cuda")
-    g = kda.gate(dev["z"], dev["A"])
     P = 4096
-    cuP = torch.tensor([0, P], dtype=torch.int32, device="cuda")
-    oP, hP = kda.chunk_fwd(dev["q"][:P], dev["k"][:P], dev["v"][:P], g[:P], dev["beta"][:P], None,
-                           cuP)
-    g_ref = oracle.gate(dev["z"][:P], dev["A"])
-    o_ref, h_ref = oracle.recurrence(dev["q"][:P], dev["k"][:P], dev["v"][:P], g_ref,
-                                     dev["beta"][:P], None)
+    o_full, h_full = kda.chunk_fwd_gated(dev["q"], dev["k"], dev["v"], dev["z"], dev["A"],
+                                         dev["beta"], None, dev["cu_seqlens"])
+    pre = workloads.make_inputs(w, "cuda", tokens=P)  # the same values, drawn on their own
+    for key in ("q", "k", "v", "z", "beta"):
+        assert torch.equal(pre[key], dev[key][:P]), key
+    oP, hP = kda.chunk_fwd_gated(pre["q"], pre["k"], pre["v"], pre["z"], pre["A"], pre["beta"],
+                                 None, pre["cu_seqlens"])
+    torch.cuda.synchronize()
+    assert torch.equal(o_full[:P], oP)
+    g_ref = oracle.gate(pre["z"], pre["A"])
+    o_ref, h_ref = oracle.recurrence(pre["q"], pre["k"], pre["v"], g_ref, pre["beta"], None)
     assert_close(oP, o_ref, torch.bfloat16, "o prefix")
     assert_close(hP, h_ref, torch.bfloat16, "hT prefix")
-    o_full, _ = kda.chunk_fwd(dev["q"], dev["k"], dev["v"], g, dev["beta"], None,
-                              dev["cu_seqlens"])
-    assert torch.equal(o_full[:P], oP)
+    del pre, oP, hP, o_ref, h_ref, g_ref
+    # the serial chain on the same instance: hT of every head
+    _, h_seq = kda.chunk_fwd_fused(dev["q"], dev["k"], dev["v"], dev["beta"], None,
+                                   dev["cu_seqlens"], z=dev["z"], A=dev["A"],
+                                   flags=kda.SEQUENTIAL)
+    torch.cuda.synchronize()
+    assert_close(h_full, h_seq.double(), torch.bfloat16, "hT segmented vs serial")
+    # one head over the whole sequence against the oracle
+    h = 11
+    sl = lambda t: t[:, h:h + 1]
+    g_ref = oracle.gate(sl(dev["z"]), dev["A"][h:h + 1])
+    o_ref, h_ref = oracle.recurrence(sl(dev["q"]), sl(dev["k"]), sl(dev["v"]), g_ref,
+                                     sl(dev["beta"]), None, n_threads=1)
+    assert_close(sl(o_full), o_ref, torch.bfloat16, f"o head {h}, all tokens")
+    assert_close(h_full[:, h:h + 1], h_ref, torch.bfloat16, f"hT head {h}")
 
 
 # ---------------------------------------------------------------- chain segments

@@ -113,21 +113,57 @@ def _unit_rows(x: torch.Tensor) -> torch.Tensor:
     return x / x.norm(dim=-1, keepdim=True).clamp_min(1e-12)
 
 
-def make_inputs(w: Workload, device="cpu") -> dict:
-    """Draw every input of ``w`` from a generator seeded with ``w.seed``.
+BLOCK_TOKENS = 4096  # per-token draws are made block by block (see make_inputs)
 
-    Generation happens in fp32 on ``device``; q/k/v/beta are then cast to
-    ``w.dtype``.  The returned dict also carries ``cu_seqlens`` (int32).
+
+def _block_seed(seed: int, tensor: int, block: int) -> int:
+    """Seed of one token block of one tensor: a fixed mix of (workload seed,
+    tensor index, block index), so a block's values depend on nothing else."""
+    x = (seed * 0x9E3779B1 + tensor * 0x85EBCA77 + block * 0xC2B2AE3D) & ((1 << 62) - 1)
+    return x ^ (x >> 29)
+
+
+def _per_token(gen_dev, seed, tensor, NT, shape, draw):
+    """Concatenates ``draw(generator, n, shape)`` over token blocks of BLOCK_TOKENS,
+    each block from its own seeded generator."""
+    parts = []
+    for b, a in enumerate(range(0, NT, BLOCK_TOKENS)):
+        n = min(BLOCK_TOKENS, NT - a)
+        parts.append(draw(_gen(gen_dev, _block_seed(seed, tensor, b)), n, shape))
+    if not parts:
+        return draw(_gen(gen_dev, _block_seed(seed, tensor, 0)), 0, shape)
+    return torch.cat(parts) if len(parts) > 1 else parts[0]
+
+
+def make_inputs(w: Workload, device="cpu", tokens: Optional[int] = None) -> dict:
+    """Draw every input of ``w`` from generators seeded with ``w.seed``.
+
+    Per-token tensors (q, k, v, z, beta) are drawn in blocks of BLOCK_TOKENS tokens,
+    each block from its own generator seeded by (``w.seed``, tensor, block index):
+    the first n tokens of a workload are the same whatever its length, so
+    ``tokens=n`` (single-sequence workloads only) generates exactly the first n
+    tokens of the full instance.  A and h0 come from a generator seeded with
+    ``w.seed``.  Generation happens in fp32 on ``device``; q/k/v/beta are then cast
+    to ``w.dtype``.  The returned dict also carries ``cu_seqlens`` (int32).
     """
     dev = torch.device(device)
-    gen = _gen(dev, w.seed)
     NT, H, dk, dv = w.n_tokens, w.H, w.dk, w.dv
+    seq_lens = w.seq_lens
+    if tokens is not None:
+        if w.n_seqs != 1 or not 0 <= tokens <= NT:
+            raise ValueError("a prefix is defined for one-sequence workloads, 0 <= tokens <= T")
+        NT, seq_lens = int(tokens), (int(tokens),)
     f32 = torch.float32
-    q = _unit_rows(torch.randn(NT, H, dk, generator=gen, device=dev, dtype=f32))
-    k = _unit_rows(torch.randn(NT, H, dk, generator=gen, device=dev, dtype=f32))
-    v = torch.randn(NT, H, dv, generator=gen, device=dev, dtype=f32)
-    z = torch.randn(NT, H, dk, generator=gen, device=dev, dtype=f32) * w.z_std
-    beta = torch.sigmoid(torch.randn(NT, H, generator=gen, device=dev, dtype=f32))
+
+    def normal(g, n, shp):
+        return torch.randn(n, *shp, generator=g, device=dev, dtype=f32)
+
+    q = _unit_rows(_per_token(dev, w.seed, 0, NT, (H, dk), normal))
+    k = _unit_rows(_per_token(dev, w.seed, 1, NT, (H, dk), normal))
+    v = _per_token(dev, w.seed, 2, NT, (H, dv), normal)
+    z = _per_token(dev, w.seed, 3, NT, (H, dk), normal) * w.z_std
+    beta = torch.sigmoid(_per_token(dev, w.seed, 4, NT, (H,), normal))
+    gen = _gen(dev, w.seed)
     if w.A_range > 0:
         A = (torch.rand(H, generator=gen, device=dev, dtype=f32) * 2 - 1) * w.A_range
     else:
@@ -136,8 +172,8 @@ def make_inputs(w: Workload, device="cpu") -> dict:
         h0 = torch.randn(w.n_seqs, H, dv, dk, generator=gen, device=dev, dtype=f32) * w.h0_std
     else:
         h0 = None
-    cu = torch.zeros(w.n_seqs + 1, dtype=torch.int64)
-    cu[1:] = torch.cumsum(torch.tensor(w.seq_lens, dtype=torch.int64), 0)
+    cu = torch.zeros(len(seq_lens) + 1, dtype=torch.int64)
+    cu[1:] = torch.cumsum(torch.tensor(seq_lens, dtype=torch.int64), 0)
     dt = w.dtype
     return dict(q=q.to(dt), k=k.to(dt), v=v.to(dt), z=z.to(dt), beta=beta.to(dt), A=A,
                 h0=h0, cu_seqlens=cu.to(torch.int32).to(dev))
