@@ -519,6 +519,22 @@ def run_gpu(args):
                                 workspace=ws, out=o, final_state_out=hT)
 
         ms_fz = timed(step_all_fused, args.steps, args.warmup)
+
+        # the headline step with the precise state update (KDA_CHUNK_PRECISE: Kt in
+        # fp32, tf32 state-update MMAs); its own, larger workspace
+        ws_p = torch.empty(kda.chunk_fwd_workspace_size(NT, 1, H, torch.bfloat16, kda.PRECISE),
+                           dtype=torch.uint8, device=dev)
+
+        def step_precise():
+            kda.chunk_fwd_fused(inp["q"], inp["k"], inp["v"], inp["beta"], inp["h0"],
+                                inp["cu_seqlens"], z=inp["z"], A=inp["A"], workspace=ws_p,
+                                out=o, final_state_out=hT, flags=kda.PRECISE)
+
+        ms_pr = timed(step_precise, args.steps, args.warmup)
+        other["prefill_precise_state"] = {
+            "ms_per_step": ms_pr, "ms_per_step_default": ms_step if fused else ms_alt,
+            "workspace_bytes": ws_p.numel(), "workspace_bytes_default": ws.numel()}
+        del ws_p
         other["prefill_qk_norm_output_gate"] = {
             "ms_per_step": ms_fz, "ms_per_step_gated_only": ms_step if fused else ms_alt,
             "extra_bytes_per_token_head": D * 2,

@@ -29,7 +29,7 @@ __all__ = ["KdaError", "gate", "chunk_fwd", "chunk_fwd_gated", "chunk_fwd_worksp
            "library_path", "lib", "get_device_error", "profile_enable", "profile_collect", "G_MIN", "F32", "BF16", "FP32_CORES", "SEQUENTIAL",
            "segment_chunks", "recurrent_multi_step", "chunk_fwd_checkpointed",
            "chunk_fwd_fused", "gate_softplus", "UNBOUNDED_GATE",
-           "output_gate", "SCALAR_GATE", "CHECK_INPUTS", "selftest_wait_timeout"]
+           "output_gate", "SCALAR_GATE", "CHECK_INPUTS", "PRECISE", "selftest_wait_timeout"]
 
 G_MIN = -5.0
 F32, BF16 = 0, 1
@@ -38,6 +38,7 @@ SEQUENTIAL = 2  # flag of chunk_fwd: never split a sequence's chain into segment
 UNBOUNDED_GATE = 4  # flag of chunk_fwd: any g <= 0 (range-robust fp32-core evaluation)
 SCALAR_GATE = 8  # flag of chunk_fwd: g is [..., H], one log-decay per token and head
 CHECK_INPUTS = 16  # flag of chunk_fwd: check g and beta against their ranges on the device
+PRECISE = 32  # flag of chunk_fwd (bf16 tensor cores): the state update at tf32 precision
 
 _STATUS = {
     0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED_SHAPE",

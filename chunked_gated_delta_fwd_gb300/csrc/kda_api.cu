@@ -433,7 +433,8 @@ size_t kda_chunk_fwd_workspace_size_ex(int64_t n_tokens, int n_seqs, int H, int 
   if (dtype == KDA_BF16 && !(flags & (KDA_CHUNK_FP32_CORES | KDA_CHUNK_UNBOUNDED_GATE))) {
     const int segc = kda::chain_segment_chunks(n_tokens, n_seqs, H, (int)(flags >> 16),
                                                (flags & KDA_CHUNK_SEQUENTIAL) != 0);
-    return kda::plan_bytes(n_tokens, n_seqs) + kda::tc_workspace_bytes(n_tokens, n_seqs, H, segc);
+    return kda::plan_bytes(n_tokens, n_seqs) +
+           kda::tc_workspace_bytes(n_tokens, n_seqs, H, segc, (flags & KDA_CHUNK_PRECISE) != 0);
   }
   if (dtype == KDA_F32 || dtype == KDA_BF16) {
     if (!(flags & KDA_CHUNK_SCALAR_GATE))
@@ -496,7 +497,7 @@ kda_status_t chunk_fwd_impl(const char* fn, const void* q, const void* k, const 
                 ws_bytes, need);
   if (flags & ~(unsigned)(KDA_CHUNK_FP32_CORES | KDA_CHUNK_SEQUENTIAL |
                           KDA_CHUNK_UNBOUNDED_GATE | KDA_CHUNK_SCALAR_GATE |
-                          KDA_CHUNK_CHECK_INPUTS | 0xffff0000u))
+                          KDA_CHUNK_CHECK_INPUTS | KDA_CHUNK_PRECISE | 0xffff0000u))
     return fail(KDA_ERR_INVALID_ARG, "%s: unknown flags 0x%x", fn, flags);
   if ((flags & KDA_CHUNK_UNBOUNDED_GATE) && z)
     return fail(KDA_ERR_INVALID_ARG, "%s: the unbounded-gate mode takes g, not z", fn);
@@ -522,7 +523,8 @@ kda_status_t chunk_fwd_impl(const char* fn, const void* q, const void* k, const 
     e = kda::launch_chunk_tc(q, k, v, g, z, A, g_min, beta, h0, o, hT, NT, N, H,
                              kda::chain_segment_chunks(NT, N, H, (int)(flags >> 16),
                                                        (flags & KDA_CHUNK_SEQUENTIAL) != 0),
-                             ck, fz, scalar_g, workspace, err, s);
+                             ck, fz, scalar_g, (flags & KDA_CHUNK_PRECISE) != 0, workspace,
+                             err, s);
     if (e == cudaSuccess && fz.gz && NT > 0)  // the output gate, on o in place
       e = kda::launch_output_gate(o, 1, fz.gz, fz.w, fz.eps, o, NT, H, s);
   } else {

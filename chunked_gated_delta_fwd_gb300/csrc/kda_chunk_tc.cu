@@ -66,6 +66,14 @@ constexpr uint32_t kAQ = 49152;    // K-major A_qk, 64 rows r x 64 columns i: 8 
 constexpr uint32_t kKT = 57344;    // K-major 128 rows x 64: 16 KB
 constexpr uint32_t kUnitBytes = 73728;
 constexpr uint32_t kGamBytes = D * 4;
+// The precise-state mode keeps Kt^T in fp32 (K-major SW128 with 32 fp32 per
+// 128-byte row: two column blocks of 128 rows x 32 tokens), 16 KB more per unit.
+template <bool kP>
+__host__ __device__ constexpr uint32_t unit_bytes() { return kP ? kUnitBytes + 16384 : kUnitBytes; }
+// Byte offset of tokens 4 xc .. 4 xc + 3 of row (channel) c in the fp32 Kt^T tile.
+__host__ __device__ __forceinline__ uint32_t kt32_chunk(int c, int xc) {
+  return (uint32_t)((xc >> 3) * 16384 + c * 128 + (((xc & 7) ^ (c & 7)) << 4));
+}
 
 // ============================================================== prep kernel
 constexpr int kPrepCompute = 512;                // 16 warps; thread 0 also issues the copies
@@ -149,7 +157,8 @@ __device__ __forceinline__ UnitInfo unit_info(const Plan& plan, int H, int64_t u
 
 // kZ: tm_g maps z (bf16) instead of g, and g = g_min * Sigmoid(exp(A_h) z) is formed
 // while the decays are summed ("Kimi K3 technical report review", section 3.2).
-template <bool kZ>
+// kP: the precise-state mode, Kt^T written in fp32 (straight to the workspace).
+template <bool kZ, bool kP>
 __global__ void __launch_bounds__(kPrepThreads, 1)
     tc_prep(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
@@ -406,7 +415,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       const UnitInfo ui = slots[it & 1];
       if (ui.chunk >= total) break;
       const int len = ui.len;
-      uint8_t* unit = tiles + (size_t)u * kUnitBytes;
+      uint8_t* unit = tiles + (size_t)u * unit_bytes<kP>();
       if (t >= 64 && t < 128) beta_s[t - 64] = beta_nx;
       bool ok = (it > 0 || pre_ok) && mbar_wait(bar_kqv, it & 1, err);
       if (!named_sync_and(1, kPrepCompute, ok)) break;
@@ -493,8 +502,15 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         for (int e = 0; e < 8; ++e) kv[e] *= fi[e];  // k exp(R_a - G_r)
 #pragma unroll
         for (int e = 0; e < 8; ++e) x[e] = kv[e] * eCa;  // (gamma_C / Gamma) k
-        *reinterpret_cast<uint4*>((kZ ? sm + kP_KTs : unit + kKT) +
-                                  sw128_chunk(128, c, 2 * ta + hq)) = pack8(x);
+        if (kP) {  // fp32, tokens r0 .. r0 + 3 and r0 + 4 .. r0 + 7 of row c
+          *reinterpret_cast<float4*>(unit + kKT + kt32_chunk(c, 4 * ta + 2 * hq)) =
+              make_float4(x[0], x[1], x[2], x[3]);
+          *reinterpret_cast<float4*>(unit + kKT + kt32_chunk(c, 4 * ta + 2 * hq + 1)) =
+              make_float4(x[4], x[5], x[6], x[7]);
+        } else {
+          *reinterpret_cast<uint4*>((kZ ? sm + kP_KTs : unit + kKT) +
+                                    sw128_chunk(128, c, 2 * ta + hq)) = pack8(x);
+        }
 #pragma unroll
         for (int ap = 0; ap < 4; ++ap) {
           if (ap < ta) continue;
@@ -532,7 +548,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       }
       if (kZ && t == kStorer) {
         bulk_s2g(unit + kQ, sbase + kP_Qs, 16384);
-        bulk_s2g(unit + kKT, sbase + kP_KTs, 16384);
+        if (!kP) bulk_s2g(unit + kKT, sbase + kP_KTs, 16384);
         bulk_commit();
       }
       ok = mbar_wait(bar_p, it & 1, err);
@@ -859,14 +875,34 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
 }
 
 // ============================================================= chain kernel
-constexpr int kStages = 3;
-constexpr uint32_t kStageBytes = 75776;             // unit (72 KB) + gamma (512 B), 1024-aligned
-constexpr uint32_t kC_bars = kStages * kStageBytes;
-// TMEM columns: S^T fp32 [0,128); two D1 buffers [128,256), [256,384); the bf16 A
-// operands of MMA1 (S^T, packed pairs, [384,448)) and MMA2 (Vt^T, two buffers of 32
-// columns at [448,512)).
-constexpr uint32_t kT_SB = 384, kT_VT = 448;
-constexpr uint32_t kC_Smem = kC_bars + 256 + 1024;
+// Stages of the tile ring: a unit (72 KB; 88 KB with fp32 Kt^T) + gamma (512 B),
+// 1024-aligned; three of them, two in the precise-state mode.
+template <bool kP> __host__ __device__ constexpr int stages() { return kP ? 2 : 3; }
+template <bool kP> __host__ __device__ constexpr uint32_t stage_bytes() {
+  return (unit_bytes<kP>() + kGamBytes + 1023) & ~1023u;
+}
+template <bool kP> __host__ __device__ constexpr uint32_t chain_bars() {
+  return stages<kP>() * stage_bytes<kP>();
+}
+template <bool kP> __host__ __device__ constexpr uint32_t chain_smem() {
+  return chain_bars<kP>() + 256 + 1024;
+}
+static_assert(chain_smem<false>() <= 232448 && chain_smem<true>() <= 232448, "chain smem");
+// TMEM columns.  Default: S^T fp32 [0,128); two D1 buffers [128,256), [256,384)
+// (each (W S)^T | (Gamma Q S)^T then O); the bf16 A operands of MMA1 (S^T, packed
+// pairs, [384,448)) and MMA2 (Vt^T, two buffers of 32 columns at [448,512)).
+// Precise-state mode: S^T [0,128); (W S)^T [128,192) (read by the epilogue before
+// the next MMA1 is issued, so one buffer); two O buffers [192,256), [256,320); the
+// bf16 S^T copy [320,384); Vt^T in fp32, the tf32 A operand of MMA2, [384,448);
+// the bf16 Vt^T buffers of the O product [448,512).
+template <bool kP> __device__ __forceinline__ uint32_t t_ws(int j) {
+  return kP ? 128u : 128u + 128u * (uint32_t)(j & 1);
+}
+template <bool kP> __device__ __forceinline__ uint32_t t_o(int j) {
+  return kP ? 192u + 64u * (uint32_t)(j & 1) : 192u + 128u * (uint32_t)(j & 1);
+}
+template <bool kP> __host__ __device__ constexpr uint32_t t_sb() { return kP ? 320u : 384u; }
+constexpr uint32_t kT_VF = 384, kT_VT = 448;
 constexpr int kEpi = 256;    // epilogue warps 0-7: (TMEM lane, column half)
 constexpr int kStore = 128;  // store warps 8-11: TMEM lane = value row, all 64 tokens
 constexpr int kCopyWarp = (kEpi + kStore) / 32;  // warp 12: tile copies
@@ -892,6 +928,9 @@ struct SegArgs {
   float* s_in;
 };
 
+// kP: the precise-state mode (Kt^T fp32 in the tiles, Vt^T fp32 in TMEM, the state
+// update as kind::tf32 MMAs).
+template <bool kP>
 __global__ void __launch_bounds__(kChainThreads, 1)
     tc_chain(const uint8_t* __restrict__ tiles, const float* __restrict__ gam,
              const float* __restrict__ h0, Plan plan, int H, __nv_bfloat16* __restrict__ o,
@@ -955,6 +994,9 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_addr(sm);
+  constexpr int kStages = stages<kP>();
+  constexpr uint32_t kStageBytes = stage_bytes<kP>(), kC_bars = chain_bars<kP>();
+  constexpr uint32_t kUnitB = unit_bytes<kP>(), kT_SB = t_sb<kP>();
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kC_bars);
   // bars: 0..2 = full[stage], 3..5 = empty[stage] (every MMA of its chunk done),
   //       6 = MMA1 done, 7 = S update done, 8,9 = O of D1 buffer b final,
@@ -1005,9 +1047,9 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         const int s = jj % kStages;
         const int64_t u = (int64_t)(c0 + jj) * H + h;
         const uint32_t bar = bar_full0 + 8 * s;
-        mbar_arrive_expect_tx(bar, kUnitBytes + kGamBytes);
-        bulk_g2s(sbase + s * kStageBytes, tiles + (size_t)u * kUnitBytes, kUnitBytes, bar);
-        bulk_g2s(sbase + s * kStageBytes + kUnitBytes, gam + (size_t)u * D, kGamBytes, bar);
+        mbar_arrive_expect_tx(bar, kUnitB + kGamBytes);
+        bulk_g2s(sbase + s * kStageBytes, tiles + (size_t)u * kUnitB, kUnitB, bar);
+        bulk_g2s(sbase + s * kStageBytes + kUnitB, gam + (size_t)u * D, kGamBytes, bar);
       };
       int issued = 0;
       for (; issued < min(kStages, nch); ++issued) issue(issued);
@@ -1034,7 +1076,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       for (int j = 0; j < nch; ++j) {
         const int s = j % kStages;
         const uint32_t sts = sbase + s * kStageBytes;
-        const uint32_t d1 = tmem + 128 + 128 * (j & 1);
+        const uint32_t dq = tmem + t_o<kP>(j);  // (Gamma Q S)^T, then O of chunk j
         if (!wait_or_abort(bar_wi, j & 1, err, abort_flag)) break;
         if (j >= 2 && !wait_or_abort(bar_f0 + 8 * (j & 1), ((j - 2) >> 1) & 1, err, abort_flag))
           break;
@@ -1042,7 +1084,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         const uint64_t bq = mnmajor_desc(sts + kQ, 1024, 0);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
-          mma_bf16_ta(d1 + 64, tmem + kT_SB + 8 * ks, desc_advance(bq, ks * 2048), id1, ks > 0);
+          mma_bf16_ta(dq, tmem + kT_SB + 8 * ks, desc_advance(bq, ks * 2048), id1, ks > 0);
         mma_commit(bar_q);
         any_mma = true;
         if (!wait_or_abort(bar_2i, j & 1, err, abort_flag)) break;
@@ -1051,7 +1093,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         const uint64_t ba = kmajor_desc(sts + kAQ, 64, 0);
 #pragma unroll
         for (int ks = 0; ks < C / 16; ++ks)
-          mma_bf16_ta(d1 + 64, vt + 8 * ks, desc_advance(ba, ks * 32), id2a, 1u);
+          mma_bf16_ta(dq, vt + 8 * ks, desc_advance(ba, ks * 32), id2a, 1u);
         mma_commit(bar_o0 + 8 * (j & 1));  // o of chunk j final
         mma_commit(bar_empty0 + 8 * s);
       }
@@ -1097,7 +1139,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       const int s = j % kStages;
       uint8_t* st = sm + s * kStageBytes;
       const uint32_t sts = sbase + s * kStageBytes;
-      const float* gam_s = reinterpret_cast<const float*>(st + kUnitBytes);
+      const float* gam_s = reinterpret_cast<const float*>(st + kUnitB);
       // E0: S^T row -> bf16 operand copy (MMA1 may start), then S^T *= gamma_C
       // S^T updated, and the bf16 copy of the previous chunk read by both MMA1 halves
       bool ok = j == 0 || (wait_or_abort(bar_m2, (j - 1) & 1, err, abort_flag) &&
@@ -1129,7 +1171,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       // for, the output warp the (Gamma Q S)^T half, which only the output needs.
       // A = bf16 S^T from TMEM; the descriptor of K step ks is the step-0
       // descriptor with its start advanced.
-      const uint32_t d1 = tmem + 128 + 128 * (j & 1);
+      const uint32_t d1 = tmem + t_ws<kP>(j);
       if (t == 0) {
         tc_fence_after();
         const uint64_t bw = mnmajor_desc(sts + kW, 1024, 0);
@@ -1158,7 +1200,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       if (ok) {
         tc_fence_after();
         float wsv[32];
-        tmem_ld32(lrow + 128 + 128 * (j & 1) + 32 * ch, wsv);
+        tmem_ld32(lrow + t_ws<kP>(j) + 32 * ch, wsv);
         tmem_wait_ld();
         uint32_t pk[16];  // bf16 pairs of this thread's 32 tokens of Vt^T
 #pragma unroll
@@ -1167,11 +1209,14 @@ __global__ void __launch_bounds__(kChainThreads, 1)
                                  : make_uint4(0, 0, 0, 0);
           const uint32_t uw[4] = {uu.x, uu.y, uu.z, uu.w};
 #pragma unroll
-          for (int p = 0; p < 4; ++p)
-            pk[4 * e + p] = pack_bf16(bf16_lo(uw[p]) - wsv[8 * e + 2 * p],
-                                      bf16_hi(uw[p]) - wsv[8 * e + 2 * p + 1]);
+          for (int p = 0; p < 4; ++p) {
+            wsv[8 * e + 2 * p] = bf16_lo(uw[p]) - wsv[8 * e + 2 * p];
+            wsv[8 * e + 2 * p + 1] = bf16_hi(uw[p]) - wsv[8 * e + 2 * p + 1];
+            pk[4 * e + p] = pack_bf16(wsv[8 * e + 2 * p], wsv[8 * e + 2 * p + 1]);
+          }
         }
         tmem_st16(lrow + kT_VT + 32 * (j & 1) + 16 * ch, pk);
+        if (kP) tmem_st32(lrow + kT_VF + 32 * ch, wsv);  // Vt^T in fp32 for the tf32 update
         tmem_wait_st();
       }
       tc_fence_before();
@@ -1179,10 +1224,17 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       const uint32_t vt = tmem + kT_VT + 32 * (j & 1);
       if (t == 64) {  // S^T += Vt^T Kt
         tc_fence_after();
-        const uint64_t bk = kmajor_desc(sts + kKT, 128, 0);
+        if (kP) {  // kind::tf32, fp32 Vt^T from TMEM, fp32 Kt^T (two 32-token blocks)
+          constexpr uint32_t id2t = idesc_tf32_mn(128, 128, 0, 0);
 #pragma unroll
-        for (int ks = 0; ks < C / 16; ++ks)
-          mma_bf16_ta(tmem + 0, vt + 8 * ks, desc_advance(bk, ks * 32), id2b, 1u);
+          for (int ks = 0; ks < C / 8; ++ks)
+            mma_tf32_ta(tmem + 0, tmem + kT_VF + 8 * ks, kmajor_desc(sts + kKT, 128, ks), id2t, 1u);
+        } else {
+          const uint64_t bk = kmajor_desc(sts + kKT, 128, 0);
+#pragma unroll
+          for (int ks = 0; ks < C / 16; ++ks)
+            mma_bf16_ta(tmem + 0, vt + 8 * ks, desc_advance(bk, ks * 32), id2b, 1u);
+        }
         mma_commit(bar_m2);
         mma_commit(bar_empty0 + 8 * s);
         tc_fence_before();
@@ -1228,7 +1280,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       if (!wait_or_abort(bar_o0 + 8 * b, (j >> 1) & 1, err, abort_flag)) break;
       tc_fence_after();
       float ov[2][32];
-      const uint32_t d1 = lrow + 128 + 128 * b + 64;
+      const uint32_t d1 = lrow + t_o<kP>(j);
       tmem_ld32(d1, ov[0]);
       tmem_ld32(d1 + 32, ov[1]);
       tmem_wait_ld();
@@ -1469,14 +1521,15 @@ struct TcLayout {
   size_t bytes;  // from the start of the workspace
 };
 
-TcLayout tc_layout(void* ws, int64_t n_tokens, int n_seqs, int H, int seg_chunks) {
+TcLayout tc_layout(void* ws, int64_t n_tokens, int n_seqs, int H, int seg_chunks,
+                   bool precise) {
   TcLayout l{};
   const int64_t chunks = chunks_upper_bound(n_tokens, n_seqs);
   const size_t units = (size_t)chunks * H;
   size_t off = (plan_bytes(n_tokens, n_seqs) + 1023) & ~size_t(1023);
   uint8_t* base = static_cast<uint8_t*>(ws);
   l.tiles = base + off;
-  off += units * kUnitBytes;
+  off += units * (precise ? unit_bytes<true>() : unit_bytes<false>());
   l.gam = reinterpret_cast<float*>(base + off);
   off += units * kGamBytes;
   off = (off + 255) & ~size_t(255);
@@ -1526,8 +1579,8 @@ int chain_segment_chunks(int64_t n_tokens, int n_seqs, int H, int forced, bool s
   return (int)((per_seq + best_p - 1) / best_p);
 }
 
-size_t tc_workspace_bytes(int64_t n_tokens, int n_seqs, int H, int seg_chunks) {
-  return tc_layout(nullptr, n_tokens, n_seqs, H, seg_chunks).bytes -
+size_t tc_workspace_bytes(int64_t n_tokens, int n_seqs, int H, int seg_chunks, bool precise) {
+  return tc_layout(nullptr, n_tokens, n_seqs, H, seg_chunks, precise).bytes -
          plan_bytes(n_tokens, n_seqs);
 }
 
@@ -1535,17 +1588,18 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
                             const void* z, const float* A, float g_min, const void* beta,
                             const float* h0, void* o, float* hT, int64_t n_tokens, int n_seqs,
                             int H, int seg_chunks, CkptArgs ck, FuseArgs fz, bool scalar_g,
-                            void* ws, int* err, cudaStream_t s) {
+                            bool precise, void* ws, int* err, cudaStream_t s) {
   const Plan plan = plan_in(ws, n_tokens, n_seqs);
   const int64_t units = chunks_upper_bound(n_tokens, n_seqs) * H;
-  const TcLayout lay = tc_layout(ws, n_tokens, n_seqs, H, seg_chunks);
+  const TcLayout lay = tc_layout(ws, n_tokens, n_seqs, H, seg_chunks, precise);
   uint8_t* tiles = lay.tiles;
   float* gam = lay.gam;
   cudaError_t e;
   using T = __nv_bfloat16;
   const bool fused = z != nullptr;
   if (units > 0 && n_tokens > 0) {  // with no tokens there are no chunks to prepare
-    auto kern = fused ? tc_prep<true> : tc_prep<false>;
+    auto kern = precise ? (fused ? tc_prep<true, true> : tc_prep<false, true>)
+                        : (fused ? tc_prep<true, false> : tc_prep<false, false>);
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kP_Smem);
     if (e != cudaSuccess) return e;
     const int sms = sm_count();
@@ -1577,12 +1631,14 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  e = cudaFuncSetAttribute(tc_chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kC_Smem);
+  auto chain = precise ? tc_chain<true> : tc_chain<false>;
+  const uint32_t chain_sm = precise ? chain_smem<true>() : chain_smem<false>();
+  e = cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)chain_sm);
   if (e != cudaSuccess) return e;
   if (seg_chunks <= 0) {
     const dim3 cgrid((unsigned)n_seqs, (unsigned)H);
     ProfScope prof_scope("kda_tc_chain", s);
-    tc_chain<<<cgrid, kChainThreads, kC_Smem, s>>>(tiles, gam, h0, plan, H, static_cast<T*>(o),
+    chain<<<cgrid, kChainThreads, chain_sm, s>>>(tiles, gam, h0, plan, H, static_cast<T*>(o),
                                                     hT, SegArgs{0, nullptr, nullptr, nullptr, nullptr},
                                                     ck, lay.ck_off, err);
     return cudaGetLastError();
@@ -1597,7 +1653,7 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
   }
   {
     ProfScope prof_scope("kda_tc_chain_seg", s);
-    tc_chain<<<dim3((unsigned)lay.segs_ub, (unsigned)H, 2), kChainThreads, kC_Smem, s>>>(
+    chain<<<dim3((unsigned)lay.segs_ub, (unsigned)H, 2), kChainThreads, chain_sm, s>>>(
         tiles, gam, h0, plan, H, static_cast<T*>(o), hT, sg, ck, lay.ck_off, err);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -1614,7 +1670,7 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
   }
   sg.mode = 2;
   ProfScope prof_scope("kda_tc_chain_seg", s);
-  tc_chain<<<dim3((unsigned)lay.segs_ub, (unsigned)H, 1), kChainThreads, kC_Smem, s>>>(
+  chain<<<dim3((unsigned)lay.segs_ub, (unsigned)H, 1), kChainThreads, chain_sm, s>>>(
       tiles, gam, h0, plan, H, static_cast<T*>(o), hT, sg, ck, lay.ck_off, err);
   return cudaGetLastError();
 }

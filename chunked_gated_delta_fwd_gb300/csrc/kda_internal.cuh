@@ -144,7 +144,8 @@ cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v, int b
 // Chunks per chain segment for the sequence-segment parallel chain (0: the chain of
 // each (sequence, head) runs in one CTA).  `forced` > 0 overrides the choice.
 int chain_segment_chunks(int64_t n_tokens, int n_seqs, int H, int forced, bool sequential);
-size_t tc_workspace_bytes(int64_t n_tokens, int n_seqs, int H, int seg_chunks);
+// precise: the precise-state mode (Kt fp32 in the workspace, tf32 state update).
+size_t tc_workspace_bytes(int64_t n_tokens, int n_seqs, int H, int seg_chunks, bool precise);
 // With z non-null the gate is fused: g is formed from z (bf16), A and g_min and g
 // is ignored.  With scalar_g, g is [n_tokens][H]: one log-decay per token and head.
 // State checkpoints: the state after every `every` chunks of each sequence (ckpt:
@@ -167,7 +168,7 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
                             const void* z, const float* A, float g_min, const void* beta,
                             const float* h0, void* o, float* hT, int64_t n_tokens, int n_seqs,
                             int H, int seg_chunks, CkptArgs ck, FuseArgs fz, bool scalar_g,
-                            void* ws, int* err_flag, cudaStream_t s);
+                            bool precise, void* ws, int* err_flag, cudaStream_t s);
 // Input-precondition pass: raises kDevErrPrecondition in *err if any of the n_g
 // log-decays g is outside [g_lo, 0] or any of the n_beta write strengths outside
 // [0, 1] (NaN counts as outside).  g or beta may be null (nothing to check).

@@ -298,6 +298,27 @@ __device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// Instruction descriptor: kind::tf32 (fp32 operands used at tf32 precision, fp32 D),
+// operand majorness as idesc_bf16_mn.
+__host__ __device__ constexpr uint32_t idesc_tf32_mn(int M, int N, int a_mn, int b_mn) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T for one K=8 step of kind::tf32.  A (M=128 rows =
+// lanes) holds one fp32 element per 32-bit column: 8 columns per K step.  B is a
+// K-major SW128 tile of fp32 (32 elements per 128-byte row), so a K step is 32 bytes
+// as for bf16.
+__device__ __forceinline__ void mma_tf32_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // 32 lanes x 16 columns store (16 registers per thread).
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
   asm volatile(

@@ -142,7 +142,8 @@ enum {
   KDA_CHUNK_SEQUENTIAL = 2u,     /* never split a sequence's chain into segments */
   KDA_CHUNK_UNBOUNDED_GATE = 4u, /* any g <= 0 (range-robust fp32-core evaluation) */
   KDA_CHUNK_SCALAR_GATE = 8u,    /* g is [NT][H]: one log-decay per token and head */
-  KDA_CHUNK_CHECK_INPUTS = 16u   /* check the g and beta preconditions on the device */
+  KDA_CHUNK_CHECK_INPUTS = 16u,  /* check the g and beta preconditions on the device */
+  KDA_CHUNK_PRECISE = 32u        /* tensor-core path: the state update at tf32 precision */
 };
 /* Split every sequence's chain into segments of n chunks (n in 1..65535). */
 #define KDA_CHUNK_SEGMENT_CHUNKS(n) (((unsigned)(n) & 0xffffu) << 16)
@@ -180,6 +181,17 @@ enum {
  * directly (4 bytes per token and head instead of 512); the fp32-core path
  * first spreads them over the channels in the workspace.  Not combinable with a
  * gate formed from z.
+ *
+ * KDA_CHUNK_PRECISE (bf16 tensor-core path): the chunk's state update
+ * S <- Diag(gamma_C) S + Kt^T Vt takes Kt = (gamma_C / Gamma) K and the pseudo-values
+ * Vt = U - W S at tf32 precision (kind::tf32 MMAs, Kt kept in fp32 in the
+ * workspace) instead of bf16.  With nearly parallel keys and beta near 1 the
+ * update cancels large terms, and the bf16 rounding of Kt and Vt is what moves the
+ * final state most: on keys with k_i . k_j ~ 0.99, beta = 1 and slow decay the
+ * final state is at relative L2 ~1.2e-2 by default and ~6e-3 with this flag.  It
+ * costs 16 KB more workspace per (chunk, head), a two-stage tile ring in the chain
+ * and twice the tensor-pipe time of the update.  Workspace:
+ * kda_chunk_fwd_workspace_size_ex with the flag.
  *
  * KDA_CHUNK_CHECK_INPUTS (also turned on for every chunk call by the environment
  * variable KDA_CHECKS=1, read once per process): before the prefill, one pass

@@ -40,8 +40,9 @@ def _run(kda, dev, flags=0, varlen=True):
                          dev["cu_seqlens"] if varlen else None, flags=flags)
 
 
-PATHS = [(torch.float32, 0), (torch.bfloat16, 0), (torch.bfloat16, 1)]
-PATH_IDS = ["f32", "bf16-tc", "bf16-f32cores"]
+PRECISE = 32  # KDA_CHUNK_PRECISE: the tensor-core path with the state update at tf32
+PATHS = [(torch.float32, 0), (torch.bfloat16, 0), (torch.bfloat16, 1), (torch.bfloat16, PRECISE)]
+PATH_IDS = ["f32", "bf16-tc", "bf16-f32cores", "bf16-tc-precise"]
 
 
 @pytest.mark.parametrize("T", [1, 15, 16, 17, 63, 64, 65, 127, 200])
@@ -102,14 +103,17 @@ def test_no_decay_slow_forgetting(kda, dtype, flags):
 
 
 # (dtype, flags, key noise): keys = normalise(base + noise * N(0, 1)) per head, so
-# k_i . k_j is about 0.99 at noise 0.1 and 0.92 at 0.3.  The fp32 paths are held to
-# the bound at 0.1; the tensor-core path, whose tiles and state copy are bf16, is a
+# k_i . k_j is about 0.99 at noise 0.1 and 0.92 at 0.3.  The fp32 paths and the
+# tensor-core path with the precise state update are held to the bound at 0.1; the
+# default tensor-core path, whose Kt and Vt enter the state update in bf16, is a
 # little over it there (final state rel-L2 1.2e-2 at 0.1, 1.0e-2 at 0.15, measured)
 # and is held to it at 0.3 (7.8e-3).
-CORRELATED = [(torch.float32, 0, 0.1), (torch.bfloat16, 1, 0.1), (torch.bfloat16, 0, 0.3)]
+CORRELATED = [(torch.float32, 0, 0.1), (torch.bfloat16, 1, 0.1), (torch.bfloat16, PRECISE, 0.1),
+              (torch.bfloat16, 0, 0.3)]
 
 
-@pytest.mark.parametrize("dtype,flags,noise", CORRELATED, ids=["f32", "bf16-f32cores", "bf16-tc"])
+@pytest.mark.parametrize("dtype,flags,noise", CORRELATED,
+                         ids=["f32", "bf16-f32cores", "bf16-tc-precise", "bf16-tc"])
 def test_correlated_keys_full_erase(kda, dtype, flags, noise):
     """beta = 1 and the keys of each head nearly parallel under slow decay: the
     strictly lower A_kk has entries near 1 in every block, so the fp32 inverse and
@@ -241,6 +245,32 @@ def test_gated_ragged_varlen(kda, z_scale, A_val):
     assert_close(hT, h_ref, torch.bfloat16, "hT gated")
 
 
+def test_precise_mode_with_fused_gate_and_checkpoints(kda):
+    """The precise state update behind the fused gate (z read by the prepare kernel,
+    Kt written in fp32 straight to the workspace) and with state checkpoints."""
+    lens = [5, 0, 70, 64, 129, 300, 17]
+    w = workloads.custom(lens, H=3, dtype=torch.bfloat16, seed=23, h0_std=0.5)
+    inp = workloads.make_inputs(w, "cpu")
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    o, hT = kda.chunk_fwd_fused(dev["q"], dev["k"], dev["v"], dev["beta"], dev["h0"],
+                                dev["cu_seqlens"], z=dev["z"], A=dev["A"], flags=PRECISE)
+    g_ref = oracle.gate(inp["z"], inp["A"])
+    o_ref, h_ref = oracle.recurrence(inp["q"], inp["k"], inp["v"], g_ref, inp["beta"], inp["h0"],
+                                     inp["cu_seqlens"])
+    assert_close(o, o_ref, torch.bfloat16, "o precise gated")
+    assert_close(hT, h_ref, torch.bfloat16, "hT precise gated")
+    g = kda.gate(dev["z"], dev["A"])
+    o2, h2, ck = kda.chunk_fwd_checkpointed(dev["q"], dev["k"], dev["v"], g, dev["beta"],
+                                            dev["h0"], dev["cu_seqlens"], ckpt_tokens=64,
+                                            flags=PRECISE)
+    assert_close(o2, o_ref, torch.bfloat16, "o precise checkpointed")
+    assert_close(h2, h_ref, torch.bfloat16, "hT precise checkpointed")
+    ck_ref = _oracle_checkpoints(dict(inp), g_ref, lens, 64)
+    assert ck.shape[0] == ck_ref.shape[0]
+    for i in range(ck.shape[0]):
+        assert_close(ck[i], ck_ref[i], torch.bfloat16, f"checkpoint {i}")
+
+
 def test_gated_rejects_fp32(kda):
     w = workloads.custom([64], H=2, dtype=torch.float32, seed=1)
     dev = workloads.make_inputs(w, "cuda")
@@ -294,11 +324,12 @@ def test_long_context_full_instance(kda):
 
 # ---------------------------------------------------------------- chain segments
 @pytest.mark.parametrize("seg", [1, 3, 5])
-def test_segmented_chain_single_sequence(kda, seg):
+@pytest.mark.parametrize("precise", [0, PRECISE], ids=["default", "precise"])
+def test_segmented_chain_single_sequence(kda, seg, precise):
     """A 1489-token sequence (24 chunks, ragged tail) whose chain is cut into
     segments of `seg` chunks, joined by the end-state scan, against the oracle."""
     inp, g, dev = _inputs([64 * 23 + 17], H=2, dtype=torch.bfloat16, seed=300 + seg)
-    o, hT = _run(kda, dev, flags=kda.segment_chunks(seg))
+    o, hT = _run(kda, dev, flags=kda.segment_chunks(seg) | precise)
     o_ref, h_ref = oracle.recurrence(inp["q"], inp["k"], inp["v"], g, inp["beta"], inp["h0"],
                                      inp["cu_seqlens"])
     assert_close(o, o_ref, torch.bfloat16, f"o seg={seg}")
