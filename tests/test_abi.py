@@ -71,7 +71,7 @@ def test_chunk_rejects_bad_arguments(L):
     assert _chunk(L, q=FAKE + 8) == 4
     assert _chunk(L, ws=FAKE + 16) == 4
     assert _chunk(L, ws_bytes=16) == 5
-    assert _chunk(L, flags=32) == 1  # an unknown flag bit
+    assert _chunk(L, flags=64) == 1  # an unknown flag bit
     assert _chunk(L, B=2, cu=FAKE, n_seqs=2) == 1  # B must be 1 with cu_seqlens
     assert _chunk(L, cu=FAKE, n_seqs=0) == 1
     assert _chunk(L, q=None) == 1
@@ -113,7 +113,7 @@ def test_chunk_checkpointed_rejects_bad_arguments(L):
     assert _ckpt(L, cap=-1) == 1
     assert _ckpt(L, ckpt=None) == 1      # no buffer for a positive capacity
     assert _ckpt(L, ckpt=FAKE + 16) == 4  # 32-byte stores
-    assert _ckpt(L, flags=32) == 1       # unknown flag bit
+    assert _ckpt(L, flags=64) == 1       # unknown flag bit
     assert b"kda_chunk_fwd_checkpointed" in L.kda_last_error_string()
 
 
@@ -141,7 +141,7 @@ def test_chunk_fused_rejects_bad_arguments(L):
     assert _fused(L, gate=FAKE + 8) == 4
     assert _fused(L, flags=4) == 3                 # the unbounded-gate mode is not fused
     assert _fused(L, flags=8) == 1                 # scalar gates with z
-    assert _fused(L, flags=32) == 1                # an unknown flag bit
+    assert _fused(L, flags=64) == 1                # an unknown flag bit
     assert b"kda_chunk_fwd_fused" in L.kda_last_error_string()
 
 
