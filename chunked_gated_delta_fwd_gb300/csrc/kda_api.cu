@@ -525,8 +525,7 @@ kda_status_t chunk_fwd_impl(const char* fn, const void* q, const void* k, const 
                                                        (flags & KDA_CHUNK_SEQUENTIAL) != 0),
                              ck, fz, scalar_g, (flags & KDA_CHUNK_PRECISE) != 0, workspace,
                              err, s);
-    if (e == cudaSuccess && fz.gz && NT > 0)  // the output gate, on o in place
-      e = kda::launch_output_gate(o, 1, fz.gz, fz.w, fz.eps, o, NT, H, s);
+
   } else {
     const float* gf = g;
     if (scalar_g) {  // this path reads per-channel decays: spread the scalar ones first

@@ -48,6 +48,8 @@
 
 #include <cuda.h>
 
+#include <string.h>
+
 #include <mutex>
 
 namespace kda {
@@ -884,8 +886,11 @@ template <bool kP> __host__ __device__ constexpr uint32_t stage_bytes() {
 template <bool kP> __host__ __device__ constexpr uint32_t chain_bars() {
   return stages<kP>() * stage_bytes<kP>();
 }
+// After the stages: 256 bytes of barriers and flags, then the output gate's
+// per-token partial sums (fp32 [4 store warps][64]) and 1/rms (fp32 [64]).
+constexpr uint32_t kC_GateScratch = 4 * 64 * 4 + 64 * 4;
 template <bool kP> __host__ __device__ constexpr uint32_t chain_smem() {
-  return chain_bars<kP>() + 256 + 1024;
+  return chain_bars<kP>() + 256 + kC_GateScratch + 1024;
 }
 static_assert(chain_smem<false>() <= 232448 && chain_smem<true>() <= 232448, "chain smem");
 // TMEM columns.  Default: S^T fp32 [0,128); two D1 buffers [128,256), [256,384)
@@ -904,10 +909,17 @@ template <bool kP> __device__ __forceinline__ uint32_t t_o(int j) {
 template <bool kP> __host__ __device__ constexpr uint32_t t_sb() { return kP ? 320u : 384u; }
 constexpr uint32_t kT_VF = 384, kT_VT = 448;
 constexpr int kEpi = 256;    // epilogue warps 0-7: (TMEM lane, column half)
-constexpr int kStore = 128;  // store warps 8-11: TMEM lane = value row, all 64 tokens
-constexpr int kCopyWarp = (kEpi + kStore) / 32;  // warp 12: tile copies
-constexpr int kOutWarp = kCopyWarp + 1;            // warp 13: the output MMAs
-constexpr int kChainThreads = kEpi + kStore + 64;
+// Store warps from warp 8 on, TMEM lane = value row: four warps over all 64 tokens
+// of a chunk; with the output gate (kG) eight, warps 8-11 on tokens 0-31 and 12-15
+// on tokens 32-63 (two on each SM sub-partition, for the gate's extra work).  Then
+// the copy warp and the output-MMA warp.
+template <bool kG> __host__ __device__ constexpr int store_threads() { return kG ? 256 : 128; }
+template <bool kG> __host__ __device__ constexpr int copy_warp() {
+  return (kEpi + store_threads<kG>()) / 32;
+}
+template <bool kG> __host__ __device__ constexpr int chain_threads() {
+  return kEpi + store_threads<kG>() + 64;
+}
 
 // Sequence-segment parallel chain (the KCP algebra applied inside one GPU: "Kimi
 // K3 technical report review", section 8.1 Eq. 17).  A long sequence is cut into P
@@ -920,6 +932,16 @@ constexpr int kChainThreads = kEpi + kStore + 64;
 //   scan:  S_in(1) = S_end(0), S_in(k+1) = S~(k) + M(k) S_in(k)  (seg_scan_kernel);
 //   mode 2: segments k >= 1 run from S_in(k) with outputs; the last writes hT.
 // mode 0 is the plain chain, one CTA per (sequence, head).  States are S^T.
+// The head-wise RMSNorm x Sigmoid output gate applied by the store warps before o
+// is written ("Kimi K3 technical report review", section 3.3, Eq. 6):
+//   y = Sigmoid(x) * w * o / sqrt(mean over the dv channels of o^2 + eps),
+// x the gate logits [NT][H][128] bf16 (read one 64-token tile per chunk by a tensor
+// copy, tm_x), w fp32 [128] (null: ones).  Used by the kG instances of tc_chain.
+struct GateArgs {
+  const float* w;
+  float eps;
+};
+
 struct SegArgs {
   int mode;
   const int4* tab;  // per segment: (sequence, first chunk, chunks, k | P << 16); x < 0: unused
@@ -929,13 +951,13 @@ struct SegArgs {
 };
 
 // kP: the precise-state mode (Kt^T fp32 in the tiles, Vt^T fp32 in TMEM, the state
-// update as kind::tf32 MMAs).
-template <bool kP>
-__global__ void __launch_bounds__(kChainThreads, 1)
+// update as kind::tf32 MMAs).  kG: the output gate is applied before o is written.
+template <bool kP, bool kG>
+__global__ void __launch_bounds__(chain_threads<kG>(), 1)
     tc_chain(const uint8_t* __restrict__ tiles, const float* __restrict__ gam,
              const float* __restrict__ h0, Plan plan, int H, __nv_bfloat16* __restrict__ o,
              float* __restrict__ hT, SegArgs sg, CkptArgs ck, const int* __restrict__ ck_off,
-             int* err) {
+             int* err, const __grid_constant__ CUtensorMap tm_x, GateArgs ga) {
   // ---- this CTA's job: chunk range, initial and final state, outputs or not
   const int h = blockIdx.y;
   int n, c0, nch;
@@ -978,6 +1000,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     }
   }
   const int64_t tend = max(tstart, (int64_t)__ldg(plan.cu + n + 1));
+  const bool gate_on = kG && write_o;  // uniform over the CTA
   // state checkpoints of this job: the true state after every ck.every chunks of
   // the sequence (chunk-local index jl counts from the sequence start)
   const bool ckpt_on = ck.ckpt != nullptr && write_o;
@@ -995,6 +1018,8 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_addr(sm);
   constexpr int kStages = stages<kP>();
+  constexpr int kStore = store_threads<kG>(), kCopyWarp = copy_warp<kG>();
+  constexpr int kOutWarp = kCopyWarp + 1;
   constexpr uint32_t kStageBytes = stage_bytes<kP>(), kC_bars = chain_bars<kP>();
   constexpr uint32_t kUnitB = unit_bytes<kP>(), kT_SB = t_sb<kP>();
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kC_bars);
@@ -1002,8 +1027,10 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   //       6 = MMA1 done, 7 = S update done, 8,9 = O of D1 buffer b final,
   //       10,11 = D1 buffer b read out, 12..14 = drain of MMA-issuing thread 0, the
   //       output warp, thread 64 (abort path), 15 = the (Gamma Q S)^T half of MMA1
-  //       done (it reads the bf16 S^T copy), 16 = (W S)^T issued, 17 = S update issued
+  //       done (it reads the bf16 S^T copy), 16 = (W S)^T issued, 17 = S update issued,
+  //       18..20 = gate-logit tile of stage s landed (output gate only)
   const uint32_t bar_full0 = smem_addr(&bars[0]), bar_empty0 = smem_addr(&bars[3]);
+  const uint32_t bar_x0 = smem_addr(&bars[18]);
   const uint32_t bar_m1 = smem_addr(&bars[6]), bar_m2 = smem_addr(&bars[7]);
   const uint32_t bar_o0 = smem_addr(&bars[8]), bar_f0 = smem_addr(&bars[10]);
   const uint32_t bar_dr = smem_addr(&bars[12]), bar_q = smem_addr(&bars[15]);
@@ -1015,7 +1042,10 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   if (t == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar_full0 + 8 * s, 1);
-      mbar_init(bar_empty0 + 8 * s, 3);  // one commit from each MMA-issuing thread
+      // one commit from each MMA-issuing thread, and with the output gate one arrival
+      // from the store warps once they have read the gate logits kept in the stage
+      mbar_init(bar_empty0 + 8 * s, gate_on ? 4 : 3);
+      mbar_init(bar_x0 + 8 * s, 1);
     }
     mbar_init(bar_m1, 1);
     mbar_init(bar_m2, 1);
@@ -1050,6 +1080,8 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         mbar_arrive_expect_tx(bar, kUnitB + kGamBytes);
         bulk_g2s(sbase + s * kStageBytes, tiles + (size_t)u * kUnitB, kUnitB, bar);
         bulk_g2s(sbase + s * kStageBytes + kUnitB, gam + (size_t)u * D, kGamBytes, bar);
+        // the chunk's gate logits into L2, for the copy the output warp makes later
+        if (gate_on) tma_prefetch_l2_3d(&tm_x, 0, h, (int)(tstart + (int64_t)jj * C));
       };
       int issued = 0;
       for (; issued < min(kStages, nch); ++issued) issue(issued);
@@ -1073,6 +1105,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       const uint32_t id1 = idesc_bf16_mn(128, 64, 0, 1);
       const uint32_t id2a = idesc_bf16_mn(128, 64, 0, 0);
       bool any_mma = false;
+      int x_issued = 0;  // gate-logit tile copies issued
       for (int j = 0; j < nch; ++j) {
         const int s = j % kStages;
         const uint32_t sts = sbase + s * kStageBytes;
@@ -1096,10 +1129,22 @@ __global__ void __launch_bounds__(kChainThreads, 1)
           mma_bf16_ta(dq, vt + 8 * ks, desc_advance(ba, ks * 32), id2a, 1u);
         mma_commit(bar_o0 + 8 * (j & 1));  // o of chunk j final
         mma_commit(bar_empty0 + 8 * s);
+        if (gate_on) {
+          // W is dead once the (W S)^T half of MMA1 has read it, which the epilogue
+          // waited for before the state update was issued: the chunk's gate logits
+          // (64 tokens x 128 bf16, 16 KB) take its place in the stage
+          mbar_arrive_expect_tx(bar_x0 + 8 * s, 16384);
+          tma_load_3d(sts + kW, &tm_x, 0, h, (int)(tstart + (int64_t)j * C), bar_x0 + 8 * s);
+          ++x_issued;
+        }
       }
       if (*abort_flag && any_mma) {  // drain MMAs in flight
         mma_commit(bar_dr + 8);
         mbar_wait(bar_dr + 8, 0, err);
+      }
+      if (*abort_flag) {  // gate-logit copies in flight must land before the CTA exits
+        for (int jx = max(0, x_issued - kStages); jx < x_issued; ++jx)
+          mbar_wait(bar_x0 + 8 * (jx % kStages), (jx / kStages) & 1, err);
       }
     }
   } else if (warp < kEpi / 32) {
@@ -1147,22 +1192,27 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       ok = ok && wait_or_abort(bar_full0 + 8 * s, (j / kStages) & 1, err, abort_flag);
       if (!named_sync_and(1, kEpi, ok)) { alive = false; break; }
       tc_fence_after();
-      float sv[2][32];
-      tmem_ld32(lrow + 64 * ch, sv[0]);
-      tmem_ld32(lrow + 64 * ch + 32, sv[1]);
-      tmem_wait_ld();
-      if (float* cp = j > 0 ? ckpt_row(jl0 + j) : nullptr) {
-#pragma unroll
-        for (int qq = 0; qq < 2; ++qq)
-#pragma unroll
-          for (int i = 0; i < 32; i += 8)
-            st_global_v8(cp + (int64_t)lane * D + 64 * ch + 32 * qq + i, &sv[qq][i]);
-      }
+      // With the gate, the kernel runs more threads and fewer registers each, so the
+      // state is handled 32 columns at a time and read again for the scaling below;
+      // without it the thread keeps its 64 columns in registers.
+      float sv[kG ? 1 : 2][32];
       {
-        uint32_t pk[32];  // bf16 pairs of this thread's 64 columns of S^T
+        float* cp = j > 0 ? ckpt_row(jl0 + j) : nullptr;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(sv[e >> 4][2 * (e & 15)], sv[e >> 4][2 * (e & 15) + 1]);
-        tmem_st32u(lrow + kT_SB + 32 * ch, pk);
+        for (int qq = 0; qq < 2; ++qq) {  // this thread's 64 columns of S^T, 32 at a time
+          float* v = sv[kG ? 0 : qq];
+          tmem_ld32(lrow + 64 * ch + 32 * qq, *reinterpret_cast<float(*)[32]>(v));
+          tmem_wait_ld();
+          if (cp) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 8)
+              st_global_v8(cp + (int64_t)lane * D + 64 * ch + 32 * qq + i, &v[i]);
+          }
+          uint32_t pk[16];  // bf16 pairs
+#pragma unroll
+          for (int e = 0; e < 16; ++e) pk[e] = pack_bf16(v[2 * e], v[2 * e + 1]);
+          tmem_st16(lrow + kT_SB + 32 * ch + 16 * qq, pk);
+        }
       }
       tmem_wait_st();
       tc_fence_before();
@@ -1184,15 +1234,22 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         mbar_arrive(bar_wi);  // the output warp may issue the (Gamma Q S)^T half
         any_mma = true;
       }
-      // the scaled state is ordered before MMA2 by the barrier after E1
+      // S^T *= gamma_C (with the gate read again from TMEM while MMA1 runs: MMA1
+      // reads the bf16 copy); the scaled state is ordered before MMA2 by the barrier
+      // after E1
 #pragma unroll
       for (int qq = 0; qq < 2; ++qq) {
+        float* v = sv[kG ? 0 : qq];
+        if (kG) {
+          tmem_ld32(lrow + 64 * ch + 32 * qq, *reinterpret_cast<float(*)[32]>(v));
+          tmem_wait_ld();
+        }
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
           const float4 gm = *reinterpret_cast<const float4*>(gam_s + 64 * ch + 32 * qq + i);
-          sv[qq][i] *= gm.x; sv[qq][i + 1] *= gm.y; sv[qq][i + 2] *= gm.z; sv[qq][i + 3] *= gm.w;
+          v[i] *= gm.x; v[i + 1] *= gm.y; v[i + 2] *= gm.z; v[i + 3] *= gm.w;
         }
-        tmem_st32(lrow + 64 * ch + 32 * qq, sv[qq]);
+        tmem_st32(lrow + 64 * ch + 32 * qq, *reinterpret_cast<float(*)[32]>(v));
       }
       tmem_wait_st();
       // E1: Vt^T = U^T - (W S)^T on this thread's 32 tokens
@@ -1270,27 +1327,111 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     }
   } else {
     // ------------------------- store warps: o rows of each chunk, off the serial path
-    // Thread = value row dv; it reads the 64 outputs of its row from the chunk's D1
-    // buffer and writes them (2-byte stores, 64 contiguous bytes per warp), then
-    // frees the buffer for MMA1 two chunks later.
-    const int dv = t - kEpi;
+    // Without the gate: thread = value row dv; it reads the 64 outputs of its row
+    // from the chunk's D1 buffer and writes them (2-byte stores, 64 contiguous bytes
+    // per warp), then frees the buffer for MMA1 two chunks later.
+    if constexpr (!kG) {
+      const int dv = t - kEpi;
+      const uint32_t lrow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+      for (int j = 0; j < nch; ++j) {
+        const int b = j & 1;
+        // warp-uniform outcome: the TMEM loads below are whole-warp instructions
+        if (!__all_sync(0xffffffffu, wait_or_abort(bar_o0 + 8 * b, (j >> 1) & 1, err, abort_flag)))
+          break;
+        tc_fence_after();
+        float ov[2][32];
+        const uint32_t d1 = lrow + t_o<kP>(j);
+        tmem_ld32(d1, ov[0]);
+        tmem_ld32(d1 + 32, ov[1]);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar_f0 + 8 * b);
+        const int64_t tc = tstart + (int64_t)j * C;
+        __nv_bfloat16* orow = o + (tc * H + h) * D + dv;
+#pragma unroll
+        for (int r = 0; r < C; ++r)
+          if (write_o && tc + r < tend) orow[(int64_t)r * H * D] = __float2bfloat16_rn(ov[r >> 5][r & 31]);
+      }
+    } else {
+    // With the gate: eight warps, thread = value row and one 32-token half of the
+    // chunk.  A thread reads its 32 outputs and frees the D1 buffer at once; the
+    // warps form each token's sum of o^2 over the 128 value rows (a halving
+    // reduce-scatter inside the warp leaves lane l the warp's sum for token l of its
+    // half; the four warps of a half meet in shared memory); each thread takes its
+    // column of the gate logits that the output warp copied into the stage into
+    // registers and the stage goes back to the copy warp; the outputs are scaled by
+    // Sigmoid(x) w / rms and stored.  Segment runs without outputs (gate_on false)
+    // only read the buffers out and free them.
+    const int st = t - kEpi, sw = (st >> 5) & 3, th = st >> 7, sl = st & 31;
+    const int dv = 32 * sw + sl, t0h = 32 * th;  // value row, first token of the half
     const uint32_t lrow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    float* gpart = reinterpret_cast<float*>(sm + kC_bars + 256);  // [4 row quarters][64 tokens]
+    float* grr = gpart + 4 * 64;                                    // [64]: 1 / rms
+    const float gw = (gate_on && ga.w) ? __ldg(ga.w + dv) : 1.f;
     for (int j = 0; j < nch; ++j) {
-      const int b = j & 1;
-      if (!wait_or_abort(bar_o0 + 8 * b, (j >> 1) & 1, err, abort_flag)) break;
-      tc_fence_after();
-      float ov[2][32];
-      const uint32_t d1 = lrow + t_o<kP>(j);
-      tmem_ld32(d1, ov[0]);
-      tmem_ld32(d1 + 32, ov[1]);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(bar_f0 + 8 * b);
-      const int64_t tc = tstart + (int64_t)j * C;
+      const int b = j & 1, s = j % kStages;
+      // warp-uniform outcome: the TMEM load below is a whole-warp instruction
+      const bool ok_o = __all_sync(0xffffffffu, wait_or_abort(bar_o0 + 8 * b, (j >> 1) & 1, err,
+                                                              abort_flag));
+      float ov[32];
+      if (ok_o) {
+        tc_fence_after();
+        tmem_ld32(lrow + t_o<kP>(j) + t0h, ov);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar_f0 + 8 * b);  // D1 buffer b read out
+      }
+      if (!gate_on) {
+        if (!ok_o) break;
+        continue;
+      }
+      if (ok_o) {
+        float a[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) a[i] = ov[i] * ov[i];
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) {  // 32 sums over the lanes -> one per lane
+          const bool up = (sl & m) != 0;
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (i < m) a[i] = (up ? a[i + m] : a[i]) + __shfl_xor_sync(0xffffffffu, up ? a[i] : a[i + m], m);
+        }
+        gpart[sw * 64 + t0h + sl] = a[0];  // token t0h + sl
+      }
+      const bool ok_x = ok_o && wait_or_abort(bar_x0 + 8 * s, (j / kStages) & 1, err, abort_flag);
+      if (!named_sync_and(2, kStore, ok_x)) break;
+      uint32_t xp[16];  // this thread's column of its 32 logits, bf16 pairs (tokens 2i, 2i+1)
+      {
+        const uint8_t* xs = sm + s * kStageBytes + kW + t0h * 256 + dv * 2;  // [64][128] bf16
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          xp[i] = (uint32_t)*reinterpret_cast<const uint16_t*>(xs + (2 * i) * 256) |
+                  ((uint32_t)*reinterpret_cast<const uint16_t*>(xs + (2 * i + 1) * 256) << 16);
+      }
+      if (st < C)
+        grr[st] = rsqrtf((gpart[st] + gpart[64 + st] + gpart[128 + st] + gpart[192 + st]) *
+                             (1.f / D) + ga.eps);
+      named_sync(2, kStore);  // logits read, 1 / rms formed
+      if (st == 0) mbar_arrive(bar_empty0 + 8 * s);  // the stage may be refilled
+      const int64_t tc = tstart + (int64_t)j * C + t0h;
       __nv_bfloat16* orow = o + (tc * H + h) * D + dv;
 #pragma unroll
-      for (int r = 0; r < C; ++r)
-        if (write_o && tc + r < tend) orow[(int64_t)r * H * D] = __float2bfloat16_rn(ov[r >> 5][r & 31]);
+      for (int g8 = 0; g8 < 32; g8 += 8) {
+        float rg[8];
+        *reinterpret_cast<float4*>(rg) = *reinterpret_cast<const float4*>(grr + t0h + g8);
+        *reinterpret_cast<float4*>(rg + 4) = *reinterpret_cast<const float4*>(grr + t0h + g8 + 4);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = g8 + i;
+          const float x = (r & 1) ? bf16_hi(xp[r >> 1]) : bf16_lo(xp[r >> 1]);
+          const float sig = fmaf(0.5f, tanh_approx(0.5f * x), 0.5f);  // Sigmoid(x)
+          const float y = ov[r] * (rg[i] * gw) * sig;
+          if (tc + r < tend) orow[(int64_t)r * H * D] = __float2bfloat16_rn(y);
+        }
+      }
+      // (grr and gpart are rewritten only after the next chunk's first barrier,
+      // which every thread reaches after its last read of them here)
+    }
     }
   }
   tc_fence_before();
@@ -1631,16 +1772,26 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  auto chain = precise ? tc_chain<true> : tc_chain<false>;
+  // the output gate, applied by the chain's store warps (a tensor map over the logits)
+  CUtensorMap tm_x;
+  memset(&tm_x, 0, sizeof(tm_x));
+  const GateArgs ga{fz.w, fz.eps};
+  if (fz.gz) {
+    e = encode_rows(&tm_x, fz.gz, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n_tokens);
+    if (e != cudaSuccess) return e;
+  }
+  auto chain = precise ? (fz.gz ? tc_chain<true, true> : tc_chain<true, false>)
+                       : (fz.gz ? tc_chain<false, true> : tc_chain<false, false>);
+  const int chain_thr = fz.gz ? chain_threads<true>() : chain_threads<false>();
   const uint32_t chain_sm = precise ? chain_smem<true>() : chain_smem<false>();
   e = cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)chain_sm);
   if (e != cudaSuccess) return e;
   if (seg_chunks <= 0) {
     const dim3 cgrid((unsigned)n_seqs, (unsigned)H);
     ProfScope prof_scope("kda_tc_chain", s);
-    chain<<<cgrid, kChainThreads, chain_sm, s>>>(tiles, gam, h0, plan, H, static_cast<T*>(o),
+    chain<<<cgrid, chain_thr, chain_sm, s>>>(tiles, gam, h0, plan, H, static_cast<T*>(o),
                                                     hT, SegArgs{0, nullptr, nullptr, nullptr, nullptr},
-                                                    ck, lay.ck_off, err);
+                                                    ck, lay.ck_off, err, tm_x, ga);
     return cudaGetLastError();
   }
   // sequence-segment parallel chain: segments, end states and transitions, scan, rerun
@@ -1653,8 +1804,8 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
   }
   {
     ProfScope prof_scope("kda_tc_chain_seg", s);
-    chain<<<dim3((unsigned)lay.segs_ub, (unsigned)H, 2), kChainThreads, chain_sm, s>>>(
-        tiles, gam, h0, plan, H, static_cast<T*>(o), hT, sg, ck, lay.ck_off, err);
+    chain<<<dim3((unsigned)lay.segs_ub, (unsigned)H, 2), chain_thr, chain_sm, s>>>(
+        tiles, gam, h0, plan, H, static_cast<T*>(o), hT, sg, ck, lay.ck_off, err, tm_x, ga);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -1670,8 +1821,8 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
   }
   sg.mode = 2;
   ProfScope prof_scope("kda_tc_chain_seg", s);
-  chain<<<dim3((unsigned)lay.segs_ub, (unsigned)H, 1), kChainThreads, chain_sm, s>>>(
-      tiles, gam, h0, plan, H, static_cast<T*>(o), hT, sg, ck, lay.ck_off, err);
+  chain<<<dim3((unsigned)lay.segs_ub, (unsigned)H, 1), chain_thr, chain_sm, s>>>(
+      tiles, gam, h0, plan, H, static_cast<T*>(o), hT, sg, ck, lay.ck_off, err, tm_x, ga);
   return cudaGetLastError();
 }
 

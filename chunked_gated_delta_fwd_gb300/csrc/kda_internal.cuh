@@ -156,8 +156,9 @@ struct CkptArgs {
   int64_t cap;
 };
 // Fused prologue / epilogue of the tensor-core chunk path: q, k L2-normalised in the
-// prepare kernel (qk_eps < 0: off) and the output RMSNorm x Sigmoid gate applied to
-// o right after the chain (gz null: off; w null: unit weight).
+// prepare kernel (qk_eps < 0: off) and the output RMSNorm x Sigmoid gate applied by
+// the chain's store warps before o is written (gz: bf16 logits [NT][H][128], null:
+// off; w null: unit weight).
 struct FuseArgs {
   float qk_eps;
   const void* gz;

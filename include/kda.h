@@ -231,8 +231,10 @@ kda_status_t kda_chunk_fwd_ex(const void* q, const void* k, const void* v, int d
  *   out_gate   optional [NT][H][dv] of `dtype`, 16-byte aligned: gate logits x.
  *              When given, o_t = Sigmoid(x_t) * w * o~_t / sqrt(mean(o~_t^2) +
  *              out_norm_eps) with the mean over the dv channels of one head and
- *              o~ the KDA output; NULL: o = o~.  It is applied by kda_output_gate
- *              on o in place, enqueued right after the chunk kernels.
+ *              o~ the KDA output; NULL: o = o~.  The chain kernel applies it before
+ *              it writes o: each 64-token tile of logits is copied into the chain's
+ *              tile ring, the per-token RMS is reduced across the warps that hold
+ *              o~ in fp32, and y is written once (o~ never goes to memory).
  *   out_norm_weight  optional fp32 [dv] RMSNorm weight w shared by the heads
  *              (NULL: ones); only with out_gate.
  *   out_norm_eps  finite, >= 0 (used only with out_gate).

@@ -64,17 +64,19 @@ def _check(o, hT, inp, ref, use_gate, use_w, eps, what):
     assert_close(hT, h_ref, torch.bfloat16, f"hT {what}")
 
 
-@pytest.mark.parametrize("qk,gate,wt", [(True, True, True), (True, False, False),
-                                        (False, True, False), (False, True, True)],
-                         ids=["all", "qk-only", "gate-only", "gate+w"])
-def test_fused_varlen(kda, qk, gate, wt):
+@pytest.mark.parametrize("qk,gate,wt,flags", [(True, True, True, 0), (True, False, False, 0),
+                                              (False, True, False, 0), (False, True, True, 0),
+                                              (True, True, True, 32)],
+                         ids=["all", "qk-only", "gate-only", "gate+w", "all-precise"])
+def test_fused_varlen(kda, qk, gate, wt, flags):
     lens = [5, 0, 70, 64, 129, 1, 300]
     inp, dev = _case(lens, H=3, seed=81, scale_qk=qk)  # without the norm: unit rows
     qk_eps = 1e-6 if qk else None
     o, hT = kda.chunk_fwd_fused(dev["q"], dev["k"], dev["v"], dev["beta"], dev["h0"], dev["cu_seqlens"],
                                 z=dev["z"], A=dev["A"], qk_l2_eps=qk_eps,
                                 out_gate=dev["gz"] if gate else None,
-                                out_norm_weight=dev["w"] if wt else None, out_norm_eps=1e-5)
+                                out_norm_weight=dev["w"] if wt else None, out_norm_eps=1e-5,
+                                flags=flags)
     kda.get_device_error()
     _check(o, hT, inp, _reference(inp, qk_eps, gate, wt, 1e-5), gate, wt, 1e-5, "fused")
 
@@ -93,6 +95,25 @@ def test_fused_with_g_and_segments(kda):
     kda.get_device_error()
     _check(o, hT, inp, _reference(inp, 1e-6, True, True, 1e-6, g=g), True, True, 1e-6,
            "fused segmented")
+
+
+def test_gate_in_the_chain_agrees_with_the_standalone_kernel(kda):
+    """The output gate applied by the chain's store warps (from o in fp32) against
+    kda_output_gate on the ungated bf16 o of the same prefill: the two differ only
+    by where o is rounded to bf16 and by the approximate sigmoid, so every element
+    agrees within a few bf16 roundings of |y|, plus a 1e-6 floor near zero."""
+    lens = [5, 0, 70, 64, 129, 1, 300]
+    inp, dev = _case(lens, H=3, seed=88)
+    kw = dict(z=dev["z"], A=dev["A"], qk_l2_eps=1e-6)
+    y, _ = kda.chunk_fwd_fused(dev["q"], dev["k"], dev["v"], dev["beta"], dev["h0"],
+                               dev["cu_seqlens"], out_gate=dev["gz"], out_norm_weight=dev["w"],
+                               out_norm_eps=1e-6, **kw)
+    o, _ = kda.chunk_fwd_fused(dev["q"], dev["k"], dev["v"], dev["beta"], dev["h0"],
+                               dev["cu_seqlens"], **kw)
+    y2 = kda.output_gate(o, dev["gz"], dev["w"], 1e-6)
+    a, b = y.double(), y2.double()
+    assert bool((a - b).abs().le(4 * 2.0 ** -8 * b.abs() + 1e-6).all()), \
+        float(((a - b).abs() / (b.abs() + 1e-6)).max())
 
 
 def test_fused_scalar_gate_equals_broadcast(kda):
