@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
   // masked below.
   constexpr int kIssuer = 64, kLocator = 96, kPrefetcher = 128, kStorer = 192;
   UnitInfo* slots = reinterpret_cast<UnitInfo*>(sm + kP_bars + 64);
-  uint32_t issued_kqv = 0, issued_g = 0;  // copies issued (thread kIssuer)
+  uint32_t issued_kqv = 0, issued_g = 0;  // copies issued (threads kStorer, kIssuer)
   float beta_nx = 0.f;  // beta of token t - 64 of the next unit (threads 64..127)
   float gsc_nx = 0.f;   // its scalar gate, when g is one decay per token and head
   auto locate = [&](int64_t u) {
@@ -382,8 +382,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     slots[1] = locate(blockIdx.x + gridDim.x);
   }
   named_sync(1, kPrepCompute);
+  if (t == kStorer) issue_kqv(slots[0]);
   if (t == kIssuer) {
-    issue_kqv(slots[0]);
     issue_g(slots[0]);
   }
   if (t >= 64 && t < 128) {  // beta (and scalar gates) of unit 0
@@ -413,6 +413,36 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     const __nv_bfloat16* sK = reinterpret_cast<const __nv_bfloat16*>(sm + kI_K);
     const __nv_bfloat16* sQ = reinterpret_cast<const __nv_bfloat16*>(sm + kI_Q);
     const __nv_bfloat16* sV = reinterpret_cast<const __nv_bfloat16*>(sm + kI_V);
+    // W^T and U^T of a unit (TMEM columns 256..383, its W/U products complete) ->
+    // bf16 tiles staged in the k and q staging space -> whole-tile bulk stores by
+    // thread kStorer.  Runs for unit n - 1 while unit n's block products are on the
+    // tensor cores (and once more after the loop for the last unit).
+    auto write_wu = [&](uint8_t* dunit) {
+      tc_fence_after();
+      float w[32];
+      tmem_ld32(lane_addr + 256 + 32 * q4, w);
+      tmem_wait_ld();
+      if (q4 < 2) {  // W tokens 32*q4 .. +31 of K-row dk = lane (MN-major X = 64)
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch)
+          *reinterpret_cast<uint4*>(sm + kI_K + mn_chunk(64, 4 * q4 + ch, lane)) =
+              pack8(&w[8 * ch]);
+      } else {  // U^T row dv = lane, tokens 32*(q4-2) .. +31 (K-major)
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch)
+          *reinterpret_cast<uint4*>(sm + kI_Q + sw128_chunk(128, lane, 4 * (q4 - 2) + ch)) =
+              pack8(&w[8 * ch]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_sync(1, kPrepCompute);
+      if (t == kStorer) {
+        bulk_s2g(dunit + kW, sbase + kI_K, 16384);
+        bulk_s2g(dunit + kUT, sbase + kI_Q, 16384);
+        bulk_commit();
+      }
+    };
+    bool aborted = false;
     for (int64_t u = blockIdx.x; u < units_ub; u += gridDim.x, ++it) {
       const UnitInfo ui = slots[it & 1];
       if (ui.chunk >= total) break;
@@ -420,7 +450,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       uint8_t* unit = tiles + (size_t)u * unit_bytes<kP>();
       if (t >= 64 && t < 128) beta_s[t - 64] = beta_nx;
       bool ok = (it > 0 || pre_ok) && mbar_wait(bar_kqv, it & 1, err);
-      if (!named_sync_and(1, kPrepCompute, ok)) break;
+      if (!named_sync_and(1, kPrepCompute, ok)) { aborted = true; break; }
       if (it == 0 && t == kIssuer) issue_g(slots[1]);  // unit 0's g / z has been read
 
       // ---- pass 2: operands of this thread's 8 rows, one channel at a time, from
@@ -448,8 +478,11 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         Gl[1][e] = gv.y;
       }
       if (t == kStorer) bulk_wait_read_all();  // pass 2 rewrites the staging space
-      named_sync(1, kPrepCompute);  // the staged rows are all read: refill them
-      if (t == kIssuer) issue_kqv(slots[(it + 1) & 1]);
+      // and the operands of the previous unit's W/U products (still running while
+      // this unit's rows were loaded): their completion frees (beta Gamma K)^T,
+      // (beta V)^T and T for this pass, and W^T, U^T for write_wu below
+      ok = it == 0 || mbar_wait(bar_w, (it - 1) & 1, err);
+      if (!named_sync_and(1, kPrepCompute, ok)) { aborted = true; break; }
       if (sw) {  // visit channel cp + 1 first: swap the pair so o2 picks the half
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -553,8 +586,10 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         if (!kP) bulk_s2g(unit + kKT, sbase + kP_KTs, 16384);
         bulk_commit();
       }
+      // the previous unit's W and U^T leave while the products run
+      if (it > 0) write_wu(tiles + (size_t)(u - gridDim.x) * unit_bytes<kP>());
       ok = mbar_wait(bar_p, it & 1, err);
-      if (!named_sync_and(1, kPrepCompute, ok)) break;
+      if (!named_sync_and(1, kPrepCompute, ok)) { aborted = true; break; }
       tc_fence_after();
       {
         // warp -> tile tw = warp & 3 (its TMEM lane quarter) and key piece pc = warp >> 2
@@ -588,7 +623,18 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       }
       if (kZ && t == kStorer) bulk_wait_read_all();  // the next pass 1 rewrites the Q staging
       if (g_sc && t >= 64 && t < 128) gsc_s[t - 64] = gsc_nx;  // for the next pass 1
+      fence_proxy_async_smem();  // the A_qk tile leaves by a bulk copy
       named_sync(1, kPrepCompute);
+      if (t == kStorer) {
+        // W^T, U^T of the previous unit (and the Gamma*Q, Kt^T tiles) have left the
+        // k, q staging by now: fetch the next unit's rows into it -- before the next
+        // unit's pass 1, which reads them when q and k are normalised here -- then
+        // send A_qk
+        bulk_wait_read_all();
+        issue_kqv(slots[(it + 1) & 1]);
+        bulk_s2g(unit + kAQ, sbase + kP_AQs, 8192);
+        bulk_commit();
+      }
       // Warps 8-15: pass 1 of the next unit while warps 0-3 form this unit's inverse.
       bool ok1 = true;
       if (t >= kInvThreads) ok1 = pass1(slots[(it + 1) & 1], (it + 1) & 1);
@@ -802,7 +848,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                 make_float2(-acc[r][0], -acc[r][1]);
         }
       }
-      if (!named_sync_and(1, kPrepCompute, ok1)) break;
+      if (!named_sync_and(1, kPrepCompute, ok1)) { aborted = true; break; }
       {  // T -> bf16 B operand (MN-major, X = row r, K = column j); zero above the diagonal.
          // A warp reads 32 consecutive columns of one row: no bank conflicts.
         const int j = t & 63, o8 = t >> 6;
@@ -833,41 +879,19 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
 #pragma unroll
         for (int s = 0; s < C / 16; ++s)  // U^T = (beta V)^T T^T
           mma_bf16(tmem + 320, desc_advance(dv, s * 32), desc_advance(dt, s * 2048), id, s > 0);
-        mma_commit(bar_w);
+        mma_commit(bar_w);  // waited for by the next unit (or after the loop)
       }
-      ok = mbar_wait(bar_w, it & 1, err);
-      if (!named_sync_and(1, kPrepCompute, ok)) break;
-      tc_fence_after();
-      {
-        float w[32];
-        tmem_ld32(lane_addr + 256 + 32 * q4, w);
-        tmem_wait_ld();
-        if (q4 < 2) {  // W tokens 32*q4 .. +31 of K-row dk = lane, staged in the BKg space
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch)
-            *reinterpret_cast<uint4*>(sm + kP_BKg + mn_chunk(64, 4 * q4 + ch, lane)) =
-                pack8(&w[8 * ch]);
-        } else {  // U^T row dv = lane, tokens 32*(q4-2) .. +31, staged in the BV space
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch)
-            *reinterpret_cast<uint4*>(sm + kP_BV + sw128_chunk(128, lane, 4 * (q4 - 2) + ch)) =
-                pack8(&w[8 * ch]);
-        }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      named_sync(1, kPrepCompute);
-      if (t == kStorer) {  // staged tiles leave as whole-tile bulk copies
-        bulk_s2g(unit + kAQ, sbase + kP_AQs, 8192);
-        bulk_s2g(unit + kW, sbase + kP_BKg, 16384);
-        bulk_s2g(unit + kUT, sbase + kP_BV, 16384);
-        bulk_commit();
-      }
+    }
+    // the last unit's W and U^T
+    if (!aborted && it > 0) {
+      const bool okw = mbar_wait(bar_w, (it - 1) & 1, err);
+      if (named_sync_and(1, kPrepCompute, okw))
+        write_wu(tiles + (size_t)(blockIdx.x + (int64_t)(it - 1) * gridDim.x) * unit_bytes<kP>());
     }
   }
   if (t == kStorer) bulk_wait_all();
   // a copy still in flight (after an abort) must land before the CTA may exit
-  if (t == kIssuer && issued_kqv > 0) mbar_wait(bar_kqv, (issued_kqv - 1) & 1, err);
+  if (t == kStorer && issued_kqv > 0) mbar_wait(bar_kqv, (issued_kqv - 1) & 1, err);
   if (t == kIssuer && issued_g > 0) mbar_wait(bar_g, (issued_g - 1) & 1, err);
   __syncthreads();
   if (warp == 0) {
