@@ -100,7 +100,11 @@ constexpr uint32_t kP_Ps = kP_Tb + 17408;    // block-product scratch, fp32 [3][
 constexpr uint32_t kScratchBytes = 17408 + 17408 + 3072;
 static_assert(kScratchBytes <= 49152, "the inverse scratch lives in the KC operand space");
 constexpr uint32_t kP_BKg = 163840;        // K-major (beta Gamma K)^T 128 x 64
-constexpr uint32_t kP_BV = 180224;         // K-major (beta V)^T 128 x 64
+// The v rows arrive by tensor copies (two 64-channel boxes, 128-byte swizzle) directly
+// in the MN-major layout the U^T product reads (A = V^T, M = dv), alternately here and
+// in the staging slot kI_V: unit n's v sits in slot n & 1 until its W/U products are
+// done, while unit n + 1's is already being copied into the other slot.
+constexpr uint32_t kP_V2 = 180224;
 constexpr uint32_t kP_beta = 196608;       // 64 fp32
 constexpr uint32_t kP_Tot = kP_beta + 256; // per-tile sums of g, [4][128] fp32
 constexpr uint32_t kP_Rq = kP_Tot + 2048;  // 1 / |q_r|, 1 / |k_r| (fp32 [64] each) when
@@ -229,7 +233,9 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     const int t0 = (int)ui.t0;
     tma_load_3d(sbase + kI_K, &tm_k, 0, ui.h, t0, bar_kqv);
     tma_load_3d(sbase + kI_Q, &tm_q, 0, ui.h, t0, bar_kqv);
-    tma_load_3d(sbase + kI_V, &tm_v, 0, ui.h, t0, bar_kqv);
+    const uint32_t vs = sbase + ((issued_kqv & 1) ? kP_V2 : kI_V);
+    tma_load_3d(vs, &tm_v, 0, ui.h, t0, bar_kqv);
+    tma_load_3d(vs + 8192, &tm_v, 64, ui.h, t0, bar_kqv);
     ++issued_kqv;
   };
   auto issue_g = [&](const UnitInfo& ui) {
@@ -292,6 +298,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       tma_prefetch_l2_3d(&tm_k, 0, pend_h, pend_e.x);
       tma_prefetch_l2_3d(&tm_q, 0, pend_h, pend_e.x);
       tma_prefetch_l2_3d(&tm_v, 0, pend_h, pend_e.x);
+      tma_prefetch_l2_3d(&tm_v, 64, pend_h, pend_e.x);
       tma_prefetch_l2_3d(&tm_g, 0, pend_h, pend_e.x);
     }
   };
@@ -395,6 +402,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     tma_prefetch_l2_3d(&tm_k, 0, slots[1].h, (int)slots[1].t0);
     tma_prefetch_l2_3d(&tm_q, 0, slots[1].h, (int)slots[1].t0);
     tma_prefetch_l2_3d(&tm_v, 0, slots[1].h, (int)slots[1].t0);
+    tma_prefetch_l2_3d(&tm_v, 64, slots[1].h, (int)slots[1].t0);
     tma_prefetch_l2_3d(&tm_g, 0, slots[1].h, (int)slots[1].t0);
   }
   named_sync(1, kPrepCompute);
@@ -412,7 +420,6 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     const __nv_bfloat16* sK = reinterpret_cast<const __nv_bfloat16*>(sm + kI_K);
     const __nv_bfloat16* sQ = reinterpret_cast<const __nv_bfloat16*>(sm + kI_Q);
-    const __nv_bfloat16* sV = reinterpret_cast<const __nv_bfloat16*>(sm + kI_V);
     // W^T and U^T of a unit (TMEM columns 256..383, its W/U products complete) ->
     // bf16 tiles staged in the k and q staging space -> whole-tile bulk stores by
     // thread kStorer.  Runs for unit n - 1 while unit n's block products are on the
@@ -456,22 +463,20 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       // ---- pass 2: operands of this thread's 8 rows, one channel at a time, from
       //      the tile-relative log-decays G_r - R_a that pass 1 left in shared memory
       const int r0 = 16 * ta + 8 * hq;
-      uint32_t kw[8], qw[8], vw[8];
-      float bt[8], Gl[2][8];
+      uint32_t kw[8], qw[8];
+      float Gl[2][8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const int r = r0 + e;
         const bool in = r < len;
         kw[e] = in ? *reinterpret_cast<const uint32_t*>(sK + r * D + cp) : 0u;
         qw[e] = in ? *reinterpret_cast<const uint32_t*>(sQ + r * D + cp) : 0u;
-        vw[e] = in ? *reinterpret_cast<const uint32_t*>(sV + r * D + cp) : 0u;
         if (qk_norm) {  // normalised rows, rounded to bf16 like normalised inputs
           const float rk = reinterpret_cast<const float*>(sm + kP_Rk)[r];
           const float rq = reinterpret_cast<const float*>(sm + kP_Rq)[r];
           kw[e] = pack_bf16(bf16_lo(kw[e]) * rk, bf16_hi(kw[e]) * rk);
           qw[e] = pack_bf16(bf16_lo(qw[e]) * rq, bf16_hi(qw[e]) * rq);
         }
-        bt[e] = beta_s[r];
         const float2 gv =
             *reinterpret_cast<const float2*>(sm + gs_block<kZ>(r >> 5) + (r & 31) * 512 + cp * 4);
         Gl[0][e] = gv.x;
@@ -479,8 +484,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       }
       if (t == kStorer) bulk_wait_read_all();  // pass 2 rewrites the staging space
       // and the operands of the previous unit's W/U products (still running while
-      // this unit's rows were loaded): their completion frees (beta Gamma K)^T,
-      // (beta V)^T and T for this pass, and W^T, U^T for write_wu below
+      // this unit's rows were loaded): their completion frees (Gamma K)^T and T for
+      // this pass, its v slot for the next copy, and W^T, U^T for write_wu below
       ok = it == 0 || mbar_wait(bar_w, (it - 1) & 1, err);
       if (!named_sync_and(1, kPrepCompute, ok)) { aborted = true; break; }
       if (sw) {  // visit channel cp + 1 first: swap the pair so o2 picks the half
@@ -488,7 +493,6 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         for (int e = 0; e < 8; ++e) {
           kw[e] = __byte_perm(kw[e], 0u, 0x1032);
           qw[e] = __byte_perm(qw[e], 0u, 0x1032);
-          vw[e] = __byte_perm(vw[e], 0u, 0x1032);
           const float tmp = Gl[0][e];
           Gl[0][e] = Gl[1][e];
           Gl[1][e] = tmp;
@@ -521,7 +525,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         for (int e = 0; e < 8; ++e) x[e] = kv[e] * f[e];  // k exp(G_r - R_a)
         *reinterpret_cast<uint4*>(sm + kP_Bop + mn_chunk(128, 4 * ta + hq, c)) = pack8(x);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] *= eRa * bt[e];  // beta Gamma k
+        for (int e = 0; e < 8; ++e) x[e] *= eRa;  // Gamma k (beta is folded into T)
         *reinterpret_cast<uint4*>(sm + kP_BKg + sw128_chunk(128, c, 2 * ta + hq)) = pack8(x);
 #pragma unroll
         for (int e = 0; e < 8; ++e) x[e] = (o2 ? bf16_hi(qw[e]) : bf16_lo(qw[e])) * f[e];
@@ -530,9 +534,6 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         for (int e = 0; e < 8; ++e) x[e] *= eRa;  // Gamma q
         *reinterpret_cast<uint4*>((kZ ? sm + kP_Qs : unit + kQ) + mn_chunk(64, 2 * ta + hq, c)) =
             pack8(x);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = (o2 ? bf16_hi(vw[e]) : bf16_lo(vw[e])) * bt[e];
-        *reinterpret_cast<uint4*>(sm + kP_BV + sw128_chunk(128, c, 2 * ta + hq)) = pack8(x);
 #pragma unroll
         for (int e = 0; e < 8; ++e) kv[e] *= fi[e];  // k exp(R_a - G_r)
 #pragma unroll
@@ -849,14 +850,17 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         }
       }
       if (!named_sync_and(1, kPrepCompute, ok1)) { aborted = true; break; }
-      {  // T -> bf16 B operand (MN-major, X = row r, K = column j); zero above the diagonal.
-         // A warp reads 32 consecutive columns of one row: no bank conflicts.
+      {  // M = T Diag(beta) -> bf16 B operand (MN-major, X = row r, K = column j); zero
+         // above the diagonal.  A warp reads 32 consecutive columns of one row: no bank
+         // conflicts.  With beta in M, W = M (Gamma K) and U = M V take Gamma K and V
+         // as they are (beta is zero on the rows past a sequence's end).
         const int j = t & 63, o8 = t >> 6;
+        const float bj = beta_s[j];
         float x[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int r = 8 * o8 + e;
-          x[e] = (r >= j) ? Tb[r * kLdT + j] : 0.f;
+          x[e] = (r >= j) ? Tb[r * kLdT + j] * bj : 0.f;
         }
         *reinterpret_cast<uint4*>(sm + kP_T + mn_chunk(64, o8, j)) = pack8(x);
       }
@@ -870,15 +874,17 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       if (t == 0) {
         tc_fence_after();
         const uint32_t id = idesc_bf16_mn(128, 64, 0, 1);
+        const uint32_t idv = idesc_bf16_mn(128, 64, 1, 1);  // A = V^T read MN-major
         const uint64_t dk = kmajor_desc(sbase + kP_BKg, 128, 0);
-        const uint64_t dv = kmajor_desc(sbase + kP_BV, 128, 0);
+        // V in slot it & 1: two 64-channel atoms 8 KB apart, 8-token groups 1 KB apart
+        const uint64_t dv = mnmajor_desc_lbo(sbase + ((it & 1) ? kP_V2 : kI_V), 8192, 1024, 0);
         const uint64_t dt = mnmajor_desc(sbase + kP_T, 1024, 0);
 #pragma unroll
-        for (int s = 0; s < C / 16; ++s)  // W^T = (beta Gamma K)^T T^T
+        for (int s = 0; s < C / 16; ++s)  // W^T = (Gamma K)^T M^T
           mma_bf16(tmem + 256, desc_advance(dk, s * 32), desc_advance(dt, s * 2048), id, s > 0);
 #pragma unroll
-        for (int s = 0; s < C / 16; ++s)  // U^T = (beta V)^T T^T
-          mma_bf16(tmem + 320, desc_advance(dv, s * 32), desc_advance(dt, s * 2048), id, s > 0);
+        for (int s = 0; s < C / 16; ++s)  // U^T = V^T M^T
+          mma_bf16(tmem + 320, desc_advance(dv, s * 2048), desc_advance(dt, s * 2048), idv, s > 0);
         mma_commit(bar_w);  // waited for by the next unit (or after the loop)
       }
     }
@@ -1648,17 +1654,19 @@ EncodeTiledFn encode_tiled_fn() {
   return fn;
 }
 
-// Tensor map over a token-major [NT][H][128] tensor: boxes of 64 tokens of one head.
+// Tensor map over a token-major [NT][H][128] tensor: boxes of 64 tokens of one head,
+// `box_c` channels wide, with the given shared-memory swizzle.
 cudaError_t encode_rows(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int esz,
-                        int H, int64_t n_tokens) {
+                        int H, int64_t n_tokens, int box_c = D,
+                        CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE) {
   EncodeTiledFn fn = encode_tiled_fn();
   if (!fn) return cudaErrorNotSupported;
   const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)n_tokens};
   const cuuint64_t strides[2] = {(cuuint64_t)D * esz, (cuuint64_t)H * D * esz};
-  const cuuint32_t box[3] = {(cuuint32_t)D, 1u, (cuuint32_t)C};
+  const cuuint32_t box[3] = {(cuuint32_t)box_c, 1u, (cuuint32_t)C};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
   const CUresult r = fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -1772,7 +1780,9 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
     CUtensorMap tm[4];
     e = encode_rows(&tm[0], k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n_tokens);
     if (e == cudaSuccess) e = encode_rows(&tm[1], q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n_tokens);
-    if (e == cudaSuccess) e = encode_rows(&tm[2], v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n_tokens);
+    if (e == cudaSuccess)
+      e = encode_rows(&tm[2], v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n_tokens, 64,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
     if (e == cudaSuccess) {
       if (fused)
         e = encode_rows(&tm[3], z, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n_tokens);
