@@ -728,14 +728,22 @@ def run_profile_case(args):
     del S
     w = workloads.custom([8192], H=32, dtype=torch.bfloat16, seed=3, h0_std=0.02)
     inp = workloads.make_inputs(w, dev)
+    gz = torch.randn(w.n_tokens, w.H, D, device=dev).to(torch.bfloat16)
     for _ in range(args.reps):
         o, hT = kda.chunk_fwd_gated(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"],
                                     inp["beta"], inp["h0"], inp["cu_seqlens"])
         g = kda.gate(inp["z"], inp["A"])
         o2, _ = kda.chunk_fwd(inp["q"], inp["k"], inp["v"], g, inp["beta"], inp["h0"],
                               inp["cu_seqlens"])
+        # the output gate applied by the chain, and the precise state update
+        kda.chunk_fwd_fused(inp["q"], inp["k"], inp["v"], inp["beta"], inp["h0"],
+                            inp["cu_seqlens"], z=inp["z"], A=inp["A"], out_gate=gz)
+        kda.chunk_fwd_fused(inp["q"], inp["k"], inp["v"], inp["beta"], inp["h0"],
+                            inp["cu_seqlens"], z=inp["z"], A=inp["A"], flags=kda.PRECISE)
     torch.cuda.synchronize(dev)
-    print(json.dumps({"profile_case": "decode N=128 H=96; prefill B=1 T=8192 H=32",
+    kda.get_device_error()
+    print(json.dumps({"profile_case": "decode N=128 H=96; prefill B=1 T=8192 H=32 "
+                      "(gate fused; gate + chunk; output gate in the chain; precise)",
                       "reps": args.reps, "o_mean_abs": float(o.float().abs().mean()),
                       "paths_max_diff": float((o.float() - o2.float()).abs().max())}))
     return 0
