@@ -19,15 +19,14 @@
 // is k_r * exp(G_r - R_a) <= 1 (resp. q_r * exp(G_r - R_a)); their product over
 // the channels is sum_c k_rc k_ic exp(G_rc - G_ic).
 //
-// Kernel 1, tc_prep: one persistent 512-thread CTA per SM walks (chunk, head)
-// units.  A unit's k, q, v arrive through 3-D tensor TMA copies issued as soon as
-// the previous unit's rows are in registers, its g (or z, with the gate formed
-// in-kernel) a unit earlier still: warps 8-15 form the gate and the running
-// log-decays of the next unit while warps 0-7 run this unit's (I + A_kk)^{-1}
-// inverse in fp32 on the CUDA cores.  Every thread builds the operands of 8
-// tokens x 2 channels and one thread issues the MMAs (the four tile products in
-// one N=160 chain, then W^T and U^T); the unit
-// leaves as MMA-ready bf16 tiles written with whole-tile bulk copies:
+// Kernel 1, tc_prep: persistent 256-thread CTAs, two per SM, walk (chunk, head)
+// units, each CTA one unit at a time; the SM's two CTAs overlap each other's
+// phases.  A unit's k, q and z (or g) arrive by 3-D tensor copies issued during the
+// previous unit; each thread sums the decays of 16 tokens x 2 channels in
+// registers and builds their operands; one thread issues the MMAs (the four tile
+// products in one N=160 chain, then W^T and U^T); the (I + A_kk)^{-1} inverse runs
+// in fp32 on the CUDA cores.  The unit leaves as MMA-ready bf16 tiles written with
+// bulk copies from shared memory:
 //   W, Gamma*Q: MN-major, 64 token columns x 128 channels each (one operand with
 //               a 16 KB atom stride)
 //   UT: K-major, U^T (128 value rows x 64 tokens)
@@ -78,62 +77,14 @@ __host__ __device__ __forceinline__ uint32_t kt32_chunk(int c, int xc) {
 }
 
 // ============================================================== prep kernel
-constexpr int kPrepCompute = 512;                // 16 warps; thread 0 also issues the copies
-constexpr int kPrepThreads = kPrepCompute;
-// staged boxes per unit: k, q, v (bf16), and g (fp32) or z (bf16) when the gate is fused
-constexpr uint32_t kKqvBytes = C * 3 * 256;
-template <bool kZ>
-__host__ __device__ constexpr uint32_t g_unit_bytes() { return C * (kZ ? 256 : 512); }
-// shared memory (offsets from a 1024-aligned base)
-constexpr uint32_t kI_K = 0, kI_Q = 16384, kI_V = 32768, kI_G = 49152;  // staged rows
-constexpr uint32_t kP_Bop = 81920;         // MN-major X=128 (Kb/Qb rows), K=128
-constexpr uint32_t kP_T = kP_Bop;          //   reused after the products: bf16 T, MN-major 64x64
-constexpr uint32_t kP_AQs = kP_Bop + 8192;  //   and the A_qk tile on its way out
-// MN-major X=192, K=128: [KC(0) | KC(1) | KC(2) | KC(3)] at X = 0, 16, 48, 96
-// (16, 32, 48, 64 rows), X = 160..191 unused
-constexpr uint32_t kP_KC = 114688;
+// The key operand, MN-major X=192 (tokens), K=128: [KC(0) | KC(1) | KC(2) | KC(3)] at
+// X = 0, 16, 48, 96 (16, 32, 48, 64 rows), X = 160..191 unused.
 constexpr int kKCX = 192;
-// reused after the products (the next unit rewrites every KC row it reads):
-constexpr uint32_t kP_Lb = kP_KC;            // L, fp32 [64][68] (lower blocks)
-constexpr uint32_t kP_Tb = kP_Lb + 17408;    // T, fp32 [64][68] row-major
-constexpr uint32_t kP_Ps = kP_Tb + 17408;    // block-product scratch, fp32 [3][16][16]
+// The inverse's scratch: L, T fp32 [64][68] (16-byte rows: float4 loads along k) and
+// the block products, fp32 [3][16][16].
+constexpr int kLdL = 68, kLdT = 68;
 constexpr uint32_t kScratchBytes = 17408 + 17408 + 3072;
-static_assert(kScratchBytes <= 49152, "the inverse scratch lives in the KC operand space");
-constexpr uint32_t kP_BKg = 163840;        // K-major (beta Gamma K)^T 128 x 64
-// The v rows arrive by tensor copies (two 64-channel boxes, 128-byte swizzle) directly
-// in the MN-major layout the U^T product reads (A = V^T, M = dv), alternately here and
-// in the staging slot kI_V: unit n's v sits in slot n & 1 until its W/U products are
-// done, while unit n + 1's is already being copied into the other slot.
-constexpr uint32_t kP_V2 = 180224;
-constexpr uint32_t kP_beta = 196608;       // 64 fp32
-constexpr uint32_t kP_Tot = kP_beta + 256; // per-tile sums of g, [4][128] fp32
-constexpr uint32_t kP_Rq = kP_Tot + 2048;  // 1 / |q_r|, 1 / |k_r| (fp32 [64] each) when
-constexpr uint32_t kP_Rk = kP_Rq + 256;    //   q and k are normalised in the kernel
-constexpr uint32_t kP_Gsc = kP_Rk + 256;   // scalar gates of the next unit, fp32 [64]
-constexpr uint32_t kP_bars = kP_Tot + 4096;  // k/q/v full, g full, p, w + TMEM base
-static_assert(kP_Gsc + 256 <= kP_bars, "the scalar gates fit below the barriers");
-// With the gate fused (z staged in bf16) the upper half of the g staging space and
-// one more 16 KB block hold the unit's Gamma*Q and Kt^T tiles on their way out.
-constexpr uint32_t kP_Qs = kI_G + 16384;
-constexpr uint32_t kP_KTs = (kP_bars + 128 + 1023) & ~1023u;
-constexpr uint32_t kP_Smem = kP_KTs + 16384 + 1024;
-static_assert(kP_Smem <= 232448, "prep shared memory");
-// Running log-decays of the next unit, fp32 [64][128], tile-relative (G_r - R_a),
-// written during this unit's inverse: rows 0..31 and 32..63 in two 16 KB blocks,
-// the upper half of the product operand (dead once the products are done) and a
-// staging block that is idle then (gated: the Gamma*Q block, whose copy out has
-// been read; otherwise the Kt block, unused without the fused gate).  Pass 2
-// reads them before it rewrites either block.  The staged g / z stays free for
-// the copy of the unit after next.
-template <bool kZ>
-__host__ __device__ constexpr uint32_t gs_block(int half) {
-  return half ? kP_Bop + 16384 : (kZ ? kP_Qs : kP_KTs);
-}
-// warps 0-3 run the inverse (barriers 2-4); warps 4-7 start its last level once the
-// first two diagonal blocks are stored (barrier 5) and finish it with warps 0-3;
-// meanwhile warps 8-15 run the next unit's pass 1 (threads from kInvThreads on)
-constexpr int kInvThreads = 256;
-constexpr int kLdL = 68, kLdT = 68;  // 16-byte rows: float4 loads along k
+constexpr int kInvThreads = 256;  // the inverse runs on warps 0-7
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ uint4 pack8(const float* x) {
@@ -141,411 +92,556 @@ __device__ __forceinline__ uint4 pack8(const float* x) {
                     pack_bf16(x[6], x[7]));
 }
 
-struct UnitInfo {
-  int chunk, h;
-  int64_t t0;
-  int len;
-  float ea;  // exp(A_h) log2(e), when the gate is fused
-};
-
-// Position of unit u = (chunk, head) from the plan's chunk table.  Chunks at or
-// beyond the plan's total read unused table entries and are never processed.
-__device__ __forceinline__ UnitInfo unit_info(const Plan& plan, int H, int64_t u) {
-  UnitInfo ui;
-  ui.chunk = (int)(u / H);
-  ui.h = (int)(u % H);
-  const int2 e = __ldg(plan.tab + ui.chunk);
-  ui.t0 = e.x;
-  ui.len = e.y;
-  ui.ea = 0.f;
-  return ui;
+// T = (I + L)^{-1} of a unit's strictly lower, beta-scaled L (fp32 [64][kLdL] in Lb)
+// into Tb (fp32 [64][kLdT], zeros above the diagonal of each stored block), with
+// block products in Ps.  Called by threads 0..255 (warps 0-7) together; uses named
+// barriers 2-5.
+__device__ __forceinline__ void invert_unit_lower(const float* __restrict__ Lb,
+                                                  float* __restrict__ Tb,
+                                                  float* __restrict__ Ps, int t) {
+  const int warp = t >> 5;
+  if (t < 128) {
+    // ---- T = (I + L)^{-1} in fp32.  Warp wq owns diagonal 16x16 block wq: its 8x8
+    //      halves by forward substitution, then [A 0; C B]^{-1} lower-left
+    //      = -B^{-1} C A^{-1}, warp-synchronous.  Level 1: warp 2b forms
+    //      P = L_{2b+1,2b} D_{2b} from its own block and hands it to warp 2b+1
+    //      (named barrier 3 + b), which forms T_{2b+1,2b} = -D_{2b+1} P.  Level 2 below,
+    //      on warps 4-7 from the end of level 0 and on warps 0-7 after level 1.
+    //      Stored blocks carry zeros above their diagonals; blocks above the
+    //      diagonal are never stored nor read.
+    const int wq = warp, o = 16 * wq, wl = t & 31;  // warp, its block, lane in warp
+    if (wl < 16) {  // A^{-1} (lanes 0-7), B^{-1} (lanes 8-15): one column per lane
+      const int ob = o + 8 * (wl >> 3), cc = wl & 7;
+      float x[8];
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        float lr[8];
+        *reinterpret_cast<float4*>(lr) = *reinterpret_cast<const float4*>(Lb + (ob + m) * kLdL + ob);
+        *reinterpret_cast<float4*>(lr + 4) =
+            *reinterpret_cast<const float4*>(Lb + (ob + m) * kLdL + ob + 4);
+        float acc = 0.f;
+#pragma unroll
+        for (int i2 = 0; i2 < m; ++i2) acc = fmaf(lr[i2], x[i2], acc);
+        x[m] = (m < cc) ? 0.f : (m == cc ? 1.f : -acc);
+      }
+#pragma unroll
+      for (int m = 0; m < 8; ++m) Tb[(ob + m) * kLdT + ob + cc] = x[m];
+      if (wl < 8) {  // the zero upper-right 8x8 of the 16x16 block
+#pragma unroll
+        for (int m = 0; m < 8; ++m) Tb[(ob + m) * kLdT + ob + 8 + cc] = 0.f;
+      }
+    }
+    __syncwarp();
+    const int di = wl >> 2, dj = 2 * (wl & 3);  // 8x8: row di, columns dj, dj + 1
+    {  // P = C A^{-1}
+      float lr[8];
+      *reinterpret_cast<float4*>(lr) = *reinterpret_cast<const float4*>(Lb + (o + 8 + di) * kLdL + o);
+      *reinterpret_cast<float4*>(lr + 4) =
+          *reinterpret_cast<const float4*>(Lb + (o + 8 + di) * kLdL + o + 4);
+      float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {  // A^{-1} has stored zeros above the diagonal
+        a0 = fmaf(lr[k], Tb[(o + k) * kLdT + o + dj], a0);
+        a1 = fmaf(lr[k], Tb[(o + k) * kLdT + o + dj + 1], a1);
+      }
+      Ps[wq * 64 + di * 8 + dj] = a0;
+      Ps[wq * 64 + di * 8 + dj + 1] = a1;
+    }
+    __syncwarp();
+    {  // lower-left 8x8 = -B^{-1} P
+      float wr[8];
+      *reinterpret_cast<float4*>(wr) = *reinterpret_cast<const float4*>(Tb + (o + 8 + di) * kLdT + o + 8);
+      *reinterpret_cast<float4*>(wr + 4) =
+          *reinterpret_cast<const float4*>(Tb + (o + 8 + di) * kLdT + o + 12);
+      float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {  // B^{-1} has stored zeros above the diagonal
+        a0 = fmaf(wr[k], Ps[wq * 64 + k * 8 + dj], a0);
+        a1 = fmaf(wr[k], Ps[wq * 64 + k * 8 + dj + 1], a1);
+      }
+      Tb[(o + 8 + di) * kLdT + o + dj] = -a0;
+      Tb[(o + 8 + di) * kLdT + o + dj + 1] = -a1;
+    }
+    __syncwarp();
+    if (wq < 2) named_arrive(5, 192);  // D_0, D_1 are stored: warps 4-7 may read them
+    // level 1 (2 rows x 4 columns per wl: rows rp and rp + 8)
+    const int blk = wq >> 1, a = 2 * blk, R = a + 1, rp = (wl >> 2) & 7, cq = wl & 3;
+    float* P1 = Ps + 256 + blk * 256;
+    if ((wq & 1) == 0) {  // P = L_{a+1,a} D_a
+      float acc[2][4] = {};
+#pragma unroll
+      for (int k4 = 0; k4 < 16; k4 += 4) {
+        float lv[2][4];
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+          *reinterpret_cast<float4*>(lv[r]) =
+              *reinterpret_cast<const float4*>(Lb + (16 * R + rp + 8 * r) * kLdL + 16 * a + k4);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const float4 tv =
+              *reinterpret_cast<const float4*>(Tb + (16 * a + k4 + kk) * kLdT + 16 * a + 4 * cq);
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const float l = lv[r][kk];
+            acc[r][0] = fmaf(l, tv.x, acc[r][0]);
+            acc[r][1] = fmaf(l, tv.y, acc[r][1]);
+            acc[r][2] = fmaf(l, tv.z, acc[r][2]);
+            acc[r][3] = fmaf(l, tv.w, acc[r][3]);
+          }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+        *reinterpret_cast<float4*>(P1 + (rp + 8 * r) * 16 + 4 * cq) =
+            make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+      named_arrive(3 + blk, 64);
+    } else {  // T_{a+1,a} = -D_{a+1} P
+      named_sync(3 + blk, 64);
+      float acc[2][4] = {};
+#pragma unroll
+      for (int k4 = 0; k4 < 16; k4 += 4) {
+        float wv[2][4];
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+          *reinterpret_cast<float4*>(wv[r]) =
+              *reinterpret_cast<const float4*>(Tb + (16 * R + rp + 8 * r) * kLdT + 16 * R + k4);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const float4 pv = *reinterpret_cast<const float4*>(P1 + (k4 + kk) * 16 + 4 * cq);
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const float w = wv[r][kk];
+            acc[r][0] = fmaf(w, pv.x, acc[r][0]);
+            acc[r][1] = fmaf(w, pv.y, acc[r][1]);
+            acc[r][2] = fmaf(w, pv.z, acc[r][2]);
+            acc[r][3] = fmaf(w, pv.w, acc[r][3]);
+          }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+        *reinterpret_cast<float4*>(Tb + (16 * R + rp + 8 * r) * kLdT + 16 * a + 4 * cq) =
+            make_float4(-acc[r][0], -acc[r][1], -acc[r][2], -acc[r][3]);
+    }
+  } else if (t < kInvThreads) {
+    // Warps 4-7, while warps 0-3 run level 1: the terms of level 2's
+    // M = L[32:64, 0:32] T[0:32, 0:32] that need only D_0 and D_1, i.e.
+    // M[:, 0:16] = L[32:64, 0:16] D_0 and M[:, 16:32] = L[32:64, 16:32] D_1
+    // (T[0:16, 16:32] is zero), into the unused upper-right block of Tb (rows
+    // 0..31, columns 32..63).  2 rows x 4 columns per thread.
+    named_sync(5, 192);
+    const int tt = t - 128, rp = tt >> 3, cq = tt & 7, kb = cq >= 4 ? 16 : 0;
+    float acc[2][4] = {};
+#pragma unroll
+    for (int k4 = 0; k4 < 16; k4 += 4) {
+      float lv[2][4];
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+        *reinterpret_cast<float4*>(lv[r]) =
+            *reinterpret_cast<const float4*>(Lb + (32 + 2 * rp + r) * kLdL + kb + k4);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const float4 tv = *reinterpret_cast<const float4*>(Tb + (kb + k4 + kk) * kLdT + 4 * cq);
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const float l = lv[r][kk];
+          acc[r][0] = fmaf(l, tv.x, acc[r][0]);
+          acc[r][1] = fmaf(l, tv.y, acc[r][1]);
+          acc[r][2] = fmaf(l, tv.z, acc[r][2]);
+          acc[r][3] = fmaf(l, tv.w, acc[r][3]);
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+      *reinterpret_cast<float4*>(Tb + 32 + (2 * rp + r) * kLdT + 4 * cq) =
+          make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+  }
+  if (t < kInvThreads) {
+    // level 2 on warps 0-7 (barrier 2, 256 threads): M[:, 0:16] += L[32:64, 16:32]
+    // T_{1,0} (one row x 2 columns per thread), then T[32:64, 0:32] = -T22 M.
+    named_sync(2, kInvThreads);
+    float* Mb = Tb + 32;
+    {
+      const int r = t >> 3, cp = t & 7;
+      float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+      for (int k4 = 16; k4 < 32; k4 += 4) {
+        const float4 l4 = *reinterpret_cast<const float4*>(Lb + (32 + r) * kLdL + k4);
+        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const float2 tv = *reinterpret_cast<const float2*>(Tb + (k4 + kk) * kLdT + 2 * cp);
+          a0 = fmaf(lv[kk], tv.x, a0);
+          a1 = fmaf(lv[kk], tv.y, a1);
+        }
+      }
+      float2* mp = reinterpret_cast<float2*>(Mb + r * kLdT + 2 * cp);
+      const float2 m0 = *mp;
+      *mp = make_float2(m0.x + a0, m0.y + a1);
+    }
+    const int rp = t >> 4, cq = t & 15;
+    named_sync(2, kInvThreads);
+    {  // T[32:64, 0:32] = -T[32:64, 32:64] M; T[32:48, 48:64] is zero
+      const int kn = rp < 8 ? 16 : 32;  // warp-uniform: warps 0-3 hold rows 32..47
+      float acc[2][2] = {};
+#pragma unroll
+      for (int k4 = 0; k4 < 32; k4 += 4) {
+        if (k4 < kn) {
+          float wv[2][4];
+#pragma unroll
+          for (int r = 0; r < 2; ++r)
+            *reinterpret_cast<float4*>(wv[r]) =
+                *reinterpret_cast<const float4*>(Tb + (32 + 2 * rp + r) * kLdT + 32 + k4);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const float2 mv = *reinterpret_cast<const float2*>(Mb + (k4 + kk) * kLdT + 2 * cq);
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              acc[r][0] = fmaf(wv[r][kk], mv.x, acc[r][0]);
+              acc[r][1] = fmaf(wv[r][kk], mv.y, acc[r][1]);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+        *reinterpret_cast<float2*>(Tb + (32 + 2 * rp + r) * kLdT + 2 * cq) =
+            make_float2(-acc[r][0], -acc[r][1]);
+    }
+  }
 }
+
+// tc_prep: two 256-thread CTAs share an
+// SM (109 KB of shared memory, 256 TMEM columns and at most 128 registers a thread
+// each).  A CTA takes its units one after the other; the two CTAs of an SM overlap
+// each other's phases (one's latency-bound inverse under the other's issue-bound
+// operand pass, its products under the other's copies).
+//
+// Thread t -> channel pair (cp, cp + 1), cp = 2 (t & 63), and 16-token tile
+// ta = t >> 6, for the whole operand side: the thread reads its 16 rows of k, q
+// and g (or z) from the staged copy into registers, sums the decays in registers
+// and builds the operands of its 16 rows x 2 channels.  Only the per-tile totals of
+// g cross threads.  Every shared-memory block serves several phases of a unit:
+//   row operand (32 KB): K/Q rows for the products; then Gamma*Q and Kt^T on
+//     their way out (parked in TMEM meanwhile); then V (tensor copy) and
+//     T Diag(beta) for the W/U products; then the next unit's g (fp32), or U^T on
+//     its way out (gate fused)
+//   key operand (48 KB): KC for the products; then the inverse's scratch; then the
+//     next unit's k, q and z (copied in while this unit's W/U products run), or U^T
+//     on its way out (g read)
+//   (Gamma K)^T (16 KB): the W product's A operand; then W on its way out
+//   A_qk (8 KB) on its way out
+constexpr int kP2Threads = 256;
+constexpr uint32_t kQ_Bop = 0;              // MN-major X=128 (K/Q rows), K=128
+constexpr uint32_t kQ_V = kQ_Bop;           //   V: two 64-channel SW128 boxes
+constexpr uint32_t kQ_T = kQ_Bop + 16384;   //   bf16 T Diag(beta), MN-major 64x64
+constexpr uint32_t kQ_Gin = kQ_Bop;         //   the next unit's g, fp32 [64][128]
+constexpr uint32_t kQ_KC = 32768;           // MN-major X=192, K=128
+constexpr uint32_t kQ_Lb = kQ_KC;           //   the inverse's scratch
+constexpr uint32_t kQ_Tb = kQ_Lb + 17408;
+constexpr uint32_t kQ_Ps = kQ_Tb + 17408;
+constexpr uint32_t kQ_Kin = kQ_KC;          //   the next unit's k, q, z (bf16 [64][128])
+constexpr uint32_t kQ_Qin = kQ_KC + 16384;
+constexpr uint32_t kQ_Zin = kQ_KC + 32768;
+constexpr uint32_t kQ_BKg = 81920;          // K-major (Gamma K)^T 128 x 64
+constexpr uint32_t kQ_AQ = 98304;           // K-major A_qk 64 x 64
+constexpr uint32_t kQ_Tot = kQ_AQ + 8192;   // per-tile sums of g, fp32 [4][128]
+constexpr uint32_t kQ_beta = kQ_Tot + 2048;  // fp32 [64]
+constexpr uint32_t kQ_Gsc = kQ_beta + 256;   // scalar gates, fp32 [64]
+constexpr uint32_t kQ_Red = kQ_Gsc + 256;    // row sums of squares, fp32 [8 warps][32]
+constexpr uint32_t kQ_bars = kQ_Red + 1024;  // five mbarriers + the TMEM base
+constexpr uint32_t kQ_Smem = kQ_bars + 64 + 1024;  // + slack for the 1024-byte alignment
+static_assert(kScratchBytes <= kQ_BKg - kQ_KC, "the inverse scratch fits the KC space");
+static_assert(2 * (kQ_Smem + 1024) <= 233472, "two CTAs per SM");
+template <bool kZ>
+__host__ __device__ constexpr uint32_t q_ustage() { return kZ ? kQ_Bop : kQ_Zin; }
 
 // kZ: tm_g maps z (bf16) instead of g, and g = g_min * Sigmoid(exp(A_h) z) is formed
 // while the decays are summed ("Kimi K3 technical report review", section 3.2).
 // kP: the precise-state mode, Kt^T written in fp32 (straight to the workspace).
+// tm_g maps g (fp32) otherwise; g_sc: one gate per token and head (fp32 [NT][H])
+// instead, or null.  qk_eps >= 0: q and k are L2-normalised per token and head here.
 template <bool kZ, bool kP>
-__global__ void __launch_bounds__(kPrepThreads, 1)
+__global__ void __launch_bounds__(kP2Threads, 2)
     tc_prep(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
-            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
-            const __nv_bfloat16* __restrict__ beta, const float* __restrict__ A, float g_min,
-            Plan plan, int H, int64_t units_ub, uint8_t* __restrict__ tiles,
-            float* __restrict__ gam_out, float qk_eps, const float* __restrict__ g_sc,
-            int* err) {
+             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+             const __nv_bfloat16* __restrict__ beta, const float* __restrict__ A, float g_min,
+             Plan plan, int H, int64_t units_ub, uint8_t* __restrict__ tiles,
+             float* __restrict__ gam_out, float qk_eps, const float* __restrict__ g_sc,
+             int* err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_addr(sm);
-  float* beta_s = reinterpret_cast<float*>(sm + kP_beta);
-  float* gsc_s = reinterpret_cast<float*>(sm + kP_Gsc);
-  float* Tot = reinterpret_cast<float*>(sm + kP_Tot);
-  float* Lb = reinterpret_cast<float*>(sm + kP_Lb);
-  float* Tb = reinterpret_cast<float*>(sm + kP_Tb);
-  float* Ps = reinterpret_cast<float*>(sm + kP_Ps);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kP_bars);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kP_bars + 32);
-  const uint32_t bar_kqv = smem_addr(&bars[0]), bar_g = smem_addr(&bars[1]);
-  const uint32_t bar_p = smem_addr(&bars[2]), bar_w = smem_addr(&bars[3]);
-  const int t = threadIdx.x, warp = t >> 5;
+  float* Tot = reinterpret_cast<float*>(sm + kQ_Tot);
+  float* beta_s = reinterpret_cast<float*>(sm + kQ_beta);
+  float* gsc_s = reinterpret_cast<float*>(sm + kQ_Gsc);
+  float* red = reinterpret_cast<float*>(sm + kQ_Red);
+  float* Lb = reinterpret_cast<float*>(sm + kQ_Lb);
+  float* Tb = reinterpret_cast<float*>(sm + kQ_Tb);
+  float* Ps = reinterpret_cast<float*>(sm + kQ_Ps);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kQ_bars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kQ_bars + 48);
+  const uint32_t bar_p = smem_addr(&bars[0]), bar_v = smem_addr(&bars[1]);
+  const uint32_t bar_w = smem_addr(&bars[2]), bar_in = smem_addr(&bars[3]);
+  const uint32_t bar_g = smem_addr(&bars[4]);
+  const int t = threadIdx.x, warp = t >> 5, lane32 = t & 31;
+  const bool g_fp32 = !kZ && g_sc == nullptr;  // g arrives by its own copy
 
-  // the unused X = 160..191 part of the KC operand starts out as zeros
-  for (uint32_t o = t * 16; o < 49152; o += kPrepThreads * 16)
-    *reinterpret_cast<uint4*>(sm + kP_KC + o) = make_uint4(0, 0, 0, 0);
   if (t == 0) {
-    mbar_init(bar_kqv, 1);
-    mbar_init(bar_g, 1);
     mbar_init(bar_p, 1);
+    mbar_init(bar_v, 1);
     mbar_init(bar_w, 1);
+    mbar_init(bar_in, 1);
+    mbar_init(bar_g, 1);
     mbar_fence_init();
   }
-  if (warp == 0) tmem_alloc(smem_addr(tmem_slot), 512);
+  if (warp == 0) tmem_alloc(smem_addr(tmem_slot), 256);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int total = __ldg(plan.chunk_off + plan.n_seqs);
-  const float gmin2 = g_min * kLog2e;  // the fused gate's bound in base-2 units
+  const float gmin2 = g_min * kLog2e;
+  const bool qk_norm = qk_eps >= 0.f;
 
-  // Inputs: one tensor copy per input per unit (64 tokens x 1 head x 128
-  // channels) into the single staging buffer. Thread kIssuer issues unit n+1's
-  // copies as soon as every thread has read unit n's rows into registers.
-  // Unit positions run two units ahead in a two-slot ring (slot n & 1), read from
-  // the plan's chunk table: while unit n's products run on the tensor cores,
-  // warps 2-3 load beta of unit n+1 and threads kLocator / kPrefetcher load the
-  // table entry of unit n+2; the entry is written to its slot, and unit n+2's
-  // rows are prefetched into L2, only after the inverse, once the loads have
-  // long arrived.  No global-load latency sits on the critical path.  Tokens past
-  // the end of the packed batch arrive as zeros; tokens of the next sequence are
-  // masked below.
-  constexpr int kIssuer = 64, kLocator = 96, kPrefetcher = 128, kStorer = 192;
-  UnitInfo* slots = reinterpret_cast<UnitInfo*>(sm + kP_bars + 64);
-  uint32_t issued_kqv = 0, issued_g = 0;  // copies issued (threads kStorer, kIssuer)
-  float beta_nx = 0.f;  // beta of token t - 64 of the next unit (threads 64..127)
-  float gsc_nx = 0.f;   // its scalar gate, when g is one decay per token and head
-  auto locate = [&](int64_t u) {
-    UnitInfo ui;
-    if (u < units_ub) ui = unit_info(plan, H, u); else ui.chunk = total;
-    ui.ea = (kZ && ui.chunk < total) ? expf(__ldg(A + ui.h)) * kLog2e : 0.f;
-    return ui;
-  };
-  auto issue_kqv = [&](const UnitInfo& ui) {
-    if (ui.chunk >= total) return;
-    mbar_arrive_expect_tx(bar_kqv, kKqvBytes);
-    const int t0 = (int)ui.t0;
-    tma_load_3d(sbase + kI_K, &tm_k, 0, ui.h, t0, bar_kqv);
-    tma_load_3d(sbase + kI_Q, &tm_q, 0, ui.h, t0, bar_kqv);
-    const uint32_t vs = sbase + ((issued_kqv & 1) ? kP_V2 : kI_V);
-    tma_load_3d(vs, &tm_v, 0, ui.h, t0, bar_kqv);
-    tma_load_3d(vs + 8192, &tm_v, 64, ui.h, t0, bar_kqv);
-    ++issued_kqv;
-  };
-  auto issue_g = [&](const UnitInfo& ui) {
-    if (ui.chunk >= total || g_sc) return;  // scalar gates are read by warps 2-3
-    mbar_arrive_expect_tx(bar_g, g_unit_bytes<kZ>());
-    tma_load_3d(sbase + kI_G, &tm_g, 0, ui.h, (int)ui.t0, bar_g);
-    ++issued_g;
-  };
-  // pending table entry of the unit two ahead (threads kLocator and kPrefetcher)
-  bool pend_ok = false;
-  int pend_chunk = 0, pend_h = 0;
-  int2 pend_e = make_int2(0, 0);
-  float pend_a = 0.f;
-  // (chunk, head) of the unit two ahead, stepped by the grid size without dividing
-  const int64_t chunks_ub = units_ub / H;
+  const int pr = t & 63, ta = t >> 6, cp = 2 * pr, sw = (pr >> 2) & 1;
+  const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+  // Gamma*Q and Kt^T of the thread's 16 rows x 2 channels wait in TMEM columns
+  // 160..223 (idle during the products) until the products have freed the row
+  // operand, which then stages them for one bulk copy: TMEM lane 64 (ta & 1) + pr
+  // (the thread's own warp's lane quarter), 32 columns per pair of tiles,
+  // Gamma*Q in the first 16 and Kt^T in the next 16, 4 per (channel visit, half)
+  const uint32_t t_park = lane_addr + 160u + 32u * (uint32_t)(ta >> 1);
+  constexpr int kCopier = 224;  // warp 7 lane 0: copies out Gamma*Q, Kt^T and A_qk, then V in
+
+  // (chunk, head) of the current and the next unit, stepped by the grid without
+  // dividing; the next unit's table entry (and beta, scalar gates) a unit ahead
   const int grid_q = (int)(gridDim.x / H), grid_r = (int)(gridDim.x % H);
-  int64_t uf_chunk;
-  int uf_h;
+  const int64_t chunks_ub = units_ub / H;
+  int64_t cur_chunk = blockIdx.x / H;
+  int cur_h = (int)(blockIdx.x % H);
+  int2 cur_e = cur_chunk < chunks_ub ? __ldg(plan.tab + cur_chunk) : make_int2(0, 0);
+  float cur_a = (kZ && cur_chunk < chunks_ub) ? __ldg(A + cur_h) : 0.f;
+  // outstanding asynchronous work of the issuing thread (thread 0; kCopier for V):
+  // the phase it completes, or -1; drained before the CTA exits
+  int pend_p = -1, pend_v = -1, pend_w = -1, pend_in = -1, pend_g = -1;
+  auto issue_in = [&](int hh, int tt0, int ph) {  // k, q (and z) into the key-operand space
+    mbar_arrive_expect_tx(bar_in, kZ ? 49152u : 32768u);
+    tma_load_3d(sbase + kQ_Kin, &tm_k, 0, hh, tt0, bar_in);
+    tma_load_3d(sbase + kQ_Qin, &tm_q, 0, hh, tt0, bar_in);
+    if (kZ) tma_load_3d(sbase + kQ_Zin, &tm_g, 0, hh, tt0, bar_in);
+    pend_in = ph;
+  };
+  auto issue_g = [&](int hh, int tt0, int ph) {  // g (fp32) into the row-operand space
+    mbar_arrive_expect_tx(bar_g, 32768u);
+    tma_load_3d(sbase + kQ_Gin, &tm_g, 0, hh, tt0, bar_g);
+    pend_g = ph;
+  };
+  float b_cur = 0.f, b_nx = 0.f, gs_nx = 0.f;  // threads 0..63: beta, scalar gate of token t
   {
-    const int64_t u2 = blockIdx.x + 2 * (int64_t)gridDim.x;
-    uf_chunk = u2 / H;
-    uf_h = (int)(u2 % H);
-  }
-  // loads only: beta of unit `un`, the table entry (and A_h) of the unit two ahead;
-  // then steps that unit by the grid
-  auto fetch_start = [&](const UnitInfo& un) {
-    if (t >= 64 && t < 128) {
-      const bool in = un.chunk < total && t - 64 < un.len;
-      beta_nx = in ? __bfloat162float(beta[(un.t0 + t - 64) * H + un.h]) : 0.f;
-      if (g_sc) gsc_nx = in ? __ldg(g_sc + (un.t0 + t - 64) * H + un.h) : 0.f;
+    const bool valid = cur_chunk < chunks_ub && cur_chunk < total;
+    if (t == 0 && valid) {
+      issue_in(cur_h, cur_e.x, 0);
+      if (g_fp32) issue_g(cur_h, cur_e.x, 0);
     }
-    if (t == kLocator || t == kPrefetcher) {
-      pend_ok = uf_chunk < chunks_ub;
-      if (pend_ok) {
-        pend_chunk = (int)uf_chunk;
-        pend_h = uf_h;
-        pend_e = __ldg(plan.tab + pend_chunk);
-        if (kZ) pend_a = __ldg(A + pend_h);
-      }
-      uf_chunk += grid_q;
-      uf_h += grid_r;
-      if (uf_h >= H) {
-        uf_h -= H;
-        ++uf_chunk;
-      }
+    if (t < 64) {
+      const bool in = valid && t < cur_e.y;
+      b_cur = in ? __bfloat162float(beta[((size_t)cur_e.x + t) * H + cur_h]) : 0.f;
+      if (g_sc) gsc_s[t] = in ? __ldg(g_sc + ((size_t)cur_e.x + t) * H + cur_h) : 0.f;
     }
-  };
-  // uses of the loads: slot sf <- unit `uf`, its rows into L2
-  auto fetch_finish = [&](int sf) {
-    const bool live = pend_ok && pend_chunk < total;
-    if (t == kLocator) {
-      UnitInfo ui;
-      ui.chunk = live ? pend_chunk : total;
-      ui.h = pend_h;
-      ui.t0 = pend_e.x;
-      ui.len = pend_e.y;
-      ui.ea = (kZ && live) ? expf(pend_a) * kLog2e : 0.f;
-      slots[sf] = ui;
-    } else if (t == kPrefetcher && live) {
-      tma_prefetch_l2_3d(&tm_k, 0, pend_h, pend_e.x);
-      tma_prefetch_l2_3d(&tm_q, 0, pend_h, pend_e.x);
-      tma_prefetch_l2_3d(&tm_v, 0, pend_h, pend_e.x);
-      tma_prefetch_l2_3d(&tm_v, 64, pend_h, pend_e.x);
-      tma_prefetch_l2_3d(&tm_g, 0, pend_h, pend_e.x);
-    }
-  };
-  // Pass 1 of unit `un` (warps 8-15, once its rows have landed): the gate (kZ) and
-  // the running log-decay over each 16-token tile, in base-2 units (G log2 e) so
-  // that every decay below is one ex2.  Thread -> channel pair (cp, cp + 1) of
-  // tile ta; it writes G_r - R_a for its 16 rows and the tile total.
-  const bool qk_norm = qk_eps >= 0.f;  // q, k L2-normalised per token and head here
-  auto pass1 = [&](const UnitInfo& un, uint32_t parity) -> bool {
-    if (un.chunk >= total) return true;
-    if (qk_norm) {
-      // 1 / sqrt(|x_r|^2 + eps) of q and k rows: four threads per row (q, k halves);
-      // each reads 64 channels as 16-byte pieces in a row-rotated order (no bank
-      // conflicts) and the halves meet by one shuffle, which every lane reaches
-      // (an expired wait is acted on after it).
-      const bool okq = mbar_wait(bar_kqv, parity, err);
-      const int t8 = t - kInvThreads, row = t8 >> 2, part = t8 & 3;
-      const uint8_t* base = sm + (part < 2 ? kI_Q : kI_K) + row * 256 + (part & 1) * 128;
-      float ss = 0.f;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 w4 = *reinterpret_cast<const uint4*>(base + ((c + row) & 7) * 16);
-        const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float lo = bf16_lo(ww[i]), hi = bf16_hi(ww[i]);
-          ss = fmaf(lo, lo, fmaf(hi, hi, ss));
-        }
-      }
-      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-      if (!okq) return false;
-      if ((part & 1) == 0)
-        reinterpret_cast<float*>(sm + (part < 2 ? kP_Rq : kP_Rk))[row] = rsqrtf(ss + qk_eps);
-    }
-    if (!g_sc && !mbar_wait(bar_g, parity, err)) return false;
-    const int t8 = t - kInvThreads, cp = 2 * (t8 & 63), ta = t8 >> 6;
-    const uint8_t* zg = sm + kI_G;
-    float s0 = 0.f, s1 = 0.f;
-#pragma unroll 2
-    for (int e = 0; e < 16; e += 2) {
-      const int r = 16 * ta + e;
-      float gv[4];  // rows r, r + 1 x channels cp, cp + 1
-      if constexpr (kZ) {
-        // g = g_min / d with d = 1 + exp(-exp(A_h) z).  The four quotients share one
-        // reciprocal: 1/d0 = d1 (d2 d3) / (d0 d1 d2 d3), and so on.  The exponent is
-        // clamped at 30 so that the product stays finite; that moves a sigmoid below
-        // 2^-30 by less than 2^-30.
-        const uint32_t z0 = *reinterpret_cast<const uint32_t*>(zg + (r * D + cp) * 2);
-        const uint32_t z1 = *reinterpret_cast<const uint32_t*>(zg + ((r + 1) * D + cp) * 2);
-        const float d0 = 1.f + exp2_approx(fminf(-un.ea * bf16_lo(z0), 30.f));
-        const float d1 = 1.f + exp2_approx(fminf(-un.ea * bf16_hi(z0), 30.f));
-        const float d2 = 1.f + exp2_approx(fminf(-un.ea * bf16_lo(z1), 30.f));
-        const float d3 = 1.f + exp2_approx(fminf(-un.ea * bf16_hi(z1), 30.f));
-        const float d01 = d0 * d1, d23 = d2 * d3;
-        const float rall = rcp_approx(d01 * d23);
-        const float q01 = gmin2 * d23 * rall, q23 = gmin2 * d01 * rall;  // g_min / (d0 d1), ...
-        gv[0] = d1 * q01;
-        gv[1] = d0 * q01;
-        gv[2] = d3 * q23;
-        gv[3] = d2 * q23;
-      } else if (g_sc) {  // one decay per token and head, the same on every channel
-        gv[0] = gv[1] = gsc_s[r] * kLog2e;
-        gv[2] = gv[3] = gsc_s[r + 1] * kLog2e;
-      } else {
-        const float2 a = *reinterpret_cast<const float2*>(zg + (r * D + cp) * 4);
-        const float2 b = *reinterpret_cast<const float2*>(zg + ((r + 1) * D + cp) * 4);
-        gv[0] = a.x * kLog2e;
-        gv[1] = a.y * kLog2e;
-        gv[2] = b.x * kLog2e;
-        gv[3] = b.y * kLog2e;
-      }
-      if (r >= un.len) gv[0] = gv[1] = 0.f;  // rows past the sequence end
-      if (r + 1 >= un.len) gv[2] = gv[3] = 0.f;
-      s0 += gv[0];
-      s1 += gv[1];
-      *reinterpret_cast<float2*>(sm + gs_block<kZ>(r >> 5) + (r & 31) * 512 + cp * 4) =
-          make_float2(s0, s1);
-      s0 += gv[2];
-      s1 += gv[3];
-      *reinterpret_cast<float2*>(sm + gs_block<kZ>(r >> 5) + ((r + 1) & 31) * 512 + cp * 4) =
-          make_float2(s0, s1);
-    }
-    *reinterpret_cast<float2*>(Tot + ta * D + cp) = make_float2(s0, s1);
-    return true;
-  };
-  if (t == kLocator) {
-    slots[0] = locate(blockIdx.x);
-    slots[1] = locate(blockIdx.x + gridDim.x);
+    __syncthreads();
   }
-  named_sync(1, kPrepCompute);
-  if (t == kStorer) issue_kqv(slots[0]);
-  if (t == kIssuer) {
-    issue_g(slots[0]);
-  }
-  if (t >= 64 && t < 128) {  // beta (and scalar gates) of unit 0
-    const bool in = slots[0].chunk < total && t - 64 < slots[0].len;
-    beta_nx = in ? __bfloat162float(beta[(slots[0].t0 + t - 64) * H + slots[0].h]) : 0.f;
-    if (g_sc) gsc_s[t - 64] = in ? __ldg(g_sc + (slots[0].t0 + t - 64) * H + slots[0].h) : 0.f;
-  }
-  if (t == kPrefetcher && slots[1].chunk < total) {  // unit 1's rows into L2
-    tma_prefetch_l2_3d(&tm_k, 0, slots[1].h, (int)slots[1].t0);
-    tma_prefetch_l2_3d(&tm_q, 0, slots[1].h, (int)slots[1].t0);
-    tma_prefetch_l2_3d(&tm_v, 0, slots[1].h, (int)slots[1].t0);
-    tma_prefetch_l2_3d(&tm_v, 64, slots[1].h, (int)slots[1].t0);
-    tma_prefetch_l2_3d(&tm_g, 0, slots[1].h, (int)slots[1].t0);
-  }
-  named_sync(1, kPrepCompute);
-  const bool pre_ok = t < kInvThreads || pass1(slots[0], 0);
+  bool ok = true;
   uint32_t it = 0;
-  {
-    // --------------------------------------------------------- compute warps
-    // operand passes: thread -> channel pair (cp, cp+1), 8-token half hq of tile ta.
-    // The two channels are visited in a per-thread order (sw) so that each warp's
-    // 16-byte stores cover all eight 16-byte positions of the swizzle pattern.
-    const int pr = t & 63, rg = t >> 6, ta = rg >> 1, hq = rg & 1;
-    const int cp = 2 * pr, sw = (pr >> 2) & 1;
-    // read-outs: thread -> TMEM lane (t & 127), column quarter q4
-    const int lane = t & 127, q4 = t >> 7;
-    const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-    const __nv_bfloat16* sK = reinterpret_cast<const __nv_bfloat16*>(sm + kI_K);
-    const __nv_bfloat16* sQ = reinterpret_cast<const __nv_bfloat16*>(sm + kI_Q);
-    // W^T and U^T of a unit (TMEM columns 256..383, its W/U products complete) ->
-    // bf16 tiles staged in the k and q staging space -> whole-tile bulk stores by
-    // thread kStorer.  Runs for unit n - 1 while unit n's block products are on the
-    // tensor cores (and once more after the loop for the last unit).
-    auto write_wu = [&](uint8_t* dunit) {
-      tc_fence_after();
-      float w[32];
-      tmem_ld32(lane_addr + 256 + 32 * q4, w);
-      tmem_wait_ld();
-      if (q4 < 2) {  // W tokens 32*q4 .. +31 of K-row dk = lane (MN-major X = 64)
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch)
-          *reinterpret_cast<uint4*>(sm + kI_K + mn_chunk(64, 4 * q4 + ch, lane)) =
-              pack8(&w[8 * ch]);
-      } else {  // U^T row dv = lane, tokens 32*(q4-2) .. +31 (K-major)
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch)
-          *reinterpret_cast<uint4*>(sm + kI_Q + sw128_chunk(128, lane, 4 * (q4 - 2) + ch)) =
-              pack8(&w[8 * ch]);
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      named_sync(1, kPrepCompute);
-      if (t == kStorer) {
-        bulk_s2g(dunit + kW, sbase + kI_K, 16384);
-        bulk_s2g(dunit + kUT, sbase + kI_Q, 16384);
-        bulk_commit();
-      }
-    };
-    bool aborted = false;
-    for (int64_t u = blockIdx.x; u < units_ub; u += gridDim.x, ++it) {
-      const UnitInfo ui = slots[it & 1];
-      if (ui.chunk >= total) break;
-      const int len = ui.len;
-      uint8_t* unit = tiles + (size_t)u * unit_bytes<kP>();
-      if (t >= 64 && t < 128) beta_s[t - 64] = beta_nx;
-      bool ok = (it > 0 || pre_ok) && mbar_wait(bar_kqv, it & 1, err);
-      if (!named_sync_and(1, kPrepCompute, ok)) { aborted = true; break; }
-      if (it == 0 && t == kIssuer) issue_g(slots[1]);  // unit 0's g / z has been read
+  for (int64_t u = blockIdx.x; u < units_ub; u += gridDim.x, ++it) {
+    const int h = cur_h;
+    if (cur_chunk >= total) break;
+    const int64_t t0 = cur_e.x;
+    const int len = cur_e.y;
+    const float ea = kZ ? expf(cur_a) * kLog2e : 0.f;
+    uint8_t* unit = tiles + (size_t)u * unit_bytes<kP>();
+    int64_t nx_chunk = cur_chunk + grid_q;
+    int nx_h = cur_h + grid_r;
+    if (nx_h >= H) {
+      nx_h -= H;
+      ++nx_chunk;
+    }
+    const bool nx_in = nx_chunk < chunks_ub;
+    const int2 nx_e = nx_in ? __ldg(plan.tab + nx_chunk) : make_int2(0, 0);
+    const float nx_a = (kZ && nx_in) ? __ldg(A + nx_h) : 0.f;
+    const bool nx_valid = nx_in && nx_chunk < total;
+    if (t < 64) {
+      beta_s[t] = b_cur;
+      const bool in = nx_valid && t < nx_e.y;
+      b_nx = in ? __bfloat162float(beta[((size_t)nx_e.x + t) * H + nx_h]) : 0.f;
+      if (g_sc) gs_nx = in ? __ldg(g_sc + ((size_t)nx_e.x + t) * H + nx_h) : 0.f;
+    }
 
-      // ---- pass 2: operands of this thread's 8 rows, one channel at a time, from
-      //      the tile-relative log-decays G_r - R_a that pass 1 left in shared memory
-      const int r0 = 16 * ta + 8 * hq;
-      uint32_t kw[8], qw[8];
-      float Gl[2][8];
+    // ---- this unit's rows, copied in during the previous unit: 16 rows x 2 channels
+    bool okin = mbar_wait(bar_in, it & 1, err);
+    if (g_fp32) okin = mbar_wait(bar_g, it & 1, err) && okin;
+    if (t == 0 && okin) pend_in = pend_g = -1;
+    uint32_t kw[16], qw[16];
+    float Gl[2][16];
+    {
+      float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int r = r0 + e;
+      for (int e = 0; e < 16; ++e) {
+        const int r = 16 * ta + e;
         const bool in = r < len;
-        kw[e] = in ? *reinterpret_cast<const uint32_t*>(sK + r * D + cp) : 0u;
-        qw[e] = in ? *reinterpret_cast<const uint32_t*>(sQ + r * D + cp) : 0u;
-        if (qk_norm) {  // normalised rows, rounded to bf16 like normalised inputs
-          const float rk = reinterpret_cast<const float*>(sm + kP_Rk)[r];
-          const float rq = reinterpret_cast<const float*>(sm + kP_Rq)[r];
-          kw[e] = pack_bf16(bf16_lo(kw[e]) * rk, bf16_hi(kw[e]) * rk);
-          qw[e] = pack_bf16(bf16_lo(qw[e]) * rq, bf16_hi(qw[e]) * rq);
-        }
-        const float2 gv =
-            *reinterpret_cast<const float2*>(sm + gs_block<kZ>(r >> 5) + (r & 31) * 512 + cp * 4);
-        Gl[0][e] = gv.x;
-        Gl[1][e] = gv.y;
+        kw[e] = in ? *reinterpret_cast<const uint32_t*>(sm + kQ_Kin + r * 256 + cp * 2) : 0u;
+        qw[e] = in ? *reinterpret_cast<const uint32_t*>(sm + kQ_Qin + r * 256 + cp * 2) : 0u;
       }
-      if (t == kStorer) bulk_wait_read_all();  // pass 2 rewrites the staging space
-      // and the operands of the previous unit's W/U products (still running while
-      // this unit's rows were loaded): their completion frees (Gamma K)^T and T for
-      // this pass, its v slot for the next copy, and W^T, U^T for write_wu below
-      ok = it == 0 || mbar_wait(bar_w, (it - 1) & 1, err);
-      if (!named_sync_and(1, kPrepCompute, ok)) { aborted = true; break; }
-      if (sw) {  // visit channel cp + 1 first: swap the pair so o2 picks the half
+      // ---- pass 1: the gate (kZ) and the running log-decay over the thread's tile,
+      //      base 2, tile-relative: Gl[c][e] = G_r - R_a for row r = 16 ta + e
+#pragma unroll
+      for (int e = 0; e < 16; e += 2) {
+        const int r = 16 * ta + e;
+        float gv[4];  // rows r, r + 1 x channels cp, cp + 1
+        if constexpr (kZ) {
+          // g = g_min / d with d = 1 + exp(-exp(A_h) z); the four quotients share one
+          // reciprocal, the exponent clamped at 30 (see the key-operand layout above)
+          const uint32_t z0 = *reinterpret_cast<const uint32_t*>(sm + kQ_Zin + r * 256 + cp * 2);
+          const uint32_t z1 =
+              *reinterpret_cast<const uint32_t*>(sm + kQ_Zin + (r + 1) * 256 + cp * 2);
+          const float d0 = 1.f + exp2_approx(fminf(-ea * bf16_lo(z0), 30.f));
+          const float d1 = 1.f + exp2_approx(fminf(-ea * bf16_hi(z0), 30.f));
+          const float d2 = 1.f + exp2_approx(fminf(-ea * bf16_lo(z1), 30.f));
+          const float d3 = 1.f + exp2_approx(fminf(-ea * bf16_hi(z1), 30.f));
+          const float d01 = d0 * d1, d23 = d2 * d3;
+          const float rall = rcp_approx(d01 * d23);
+          const float q01 = gmin2 * d23 * rall, q23 = gmin2 * d01 * rall;
+          gv[0] = d1 * q01;
+          gv[1] = d0 * q01;
+          gv[2] = d3 * q23;
+          gv[3] = d2 * q23;
+        } else if (g_sc) {
+          gv[0] = gv[1] = gsc_s[r] * kLog2e;
+          gv[2] = gv[3] = gsc_s[r + 1] * kLog2e;
+        } else {
+          const float2 a = *reinterpret_cast<const float2*>(sm + kQ_Gin + r * 512 + cp * 4);
+          const float2 b = *reinterpret_cast<const float2*>(sm + kQ_Gin + (r + 1) * 512 + cp * 4);
+          gv[0] = a.x * kLog2e;
+          gv[1] = a.y * kLog2e;
+          gv[2] = b.x * kLog2e;
+          gv[3] = b.y * kLog2e;
+        }
+        if (r >= len) gv[0] = gv[1] = 0.f;  // rows past the sequence end
+        if (r + 1 >= len) gv[2] = gv[3] = 0.f;
+        s0 += gv[0];
+        s1 += gv[1];
+        Gl[0][e] = s0;
+        Gl[1][e] = s1;
+        s0 += gv[2];
+        s1 += gv[3];
+        Gl[0][e + 1] = s0;
+        Gl[1][e + 1] = s1;
+      }
+      *reinterpret_cast<float2*>(Tot + ta * D + cp) = make_float2(s0, s1);
+    }
+    if (qk_norm) {
+      // |k_r|^2 and |q_r|^2 over this warp's 64 channels, each by a reduce-scatter
+      // over 16 lanes and one exchange: lane i ends with row i & 15 summed over the
+      // warp (k for lanes 0-15, q for lanes 16-31)
+      float sk = 0.f, sq = 0.f;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        float v[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const uint32_t x = which ? qw[e] : kw[e];
+          v[e] = fmaf(bf16_lo(x), bf16_lo(x), bf16_hi(x) * bf16_hi(x));
+        }
+#pragma unroll
+        for (int w = 8; w >= 1; w >>= 1) {
+          const bool up = (lane32 & w) != 0;
+#pragma unroll
+          for (int i = 0; i < w; ++i) {
+            const float send = up ? v[i] : v[i + w];
+            const float keep = up ? v[i + w] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+          }
+        }
+        v[0] += __shfl_xor_sync(0xffffffffu, v[0], 16);
+        if (which) sq = v[0]; else sk = v[0];
+      }
+      red[warp * 32 + lane32] = lane32 < 16 ? sk : sq;
+    }
+    // the previous unit's outgoing copies have read their staging space (the blocks
+    // the operand pass below rewrites)
+    if (lane32 == 0) bulk_wait_read_all();
+    // the previous unit's W/U wait, this unit's copies, every thread's tile totals
+    if (!__syncthreads_and(ok && okin)) break;
+    if (qk_norm) {  // normalised rows, rounded to bf16 like normalised inputs
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const float rk = rsqrtf(red[64 * ta + e] + red[64 * ta + 32 + e] + qk_eps);
+        const float rq = rsqrtf(red[64 * ta + 16 + e] + red[64 * ta + 48 + e] + qk_eps);
+        const bool in = 16 * ta + e < len;
+        kw[e] = in ? pack_bf16(bf16_lo(kw[e]) * rk, bf16_hi(kw[e]) * rk) : 0u;
+        qw[e] = in ? pack_bf16(bf16_lo(qw[e]) * rq, bf16_hi(qw[e]) * rq) : 0u;
+      }
+    }
+
+    // ---- operands of the thread's 16 rows, one channel at a time (the order sw
+    //      makes each warp's 16-byte stores cover all eight swizzle positions)
+    if (sw) {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        kw[e] = __byte_perm(kw[e], 0u, 0x1032);
+        qw[e] = __byte_perm(qw[e], 0u, 0x1032);
+        const float tmp = Gl[0][e];
+        Gl[0][e] = Gl[1][e];
+        Gl[1][e] = tmp;
+      }
+    }
+#pragma unroll
+    for (int o2 = 0; o2 < 2; ++o2) {
+      const int c = cp + (o2 ^ sw);
+      float R[4], GC = 0.f;  // R_b = sum of the tile sums before tile b; G_C = all
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        R[b] = GC;
+        GC += Tot[b * D + c];
+      }
+      const float Ra = ta == 0 ? R[0] : (ta == 1 ? R[1] : (ta == 2 ? R[2] : R[3]));
+      const float eRa = exp2_approx(Ra);       // exp(R_a) <= 1
+      const float eCa = exp2_approx(GC - Ra);  // exp(G_C - R_a) <= 1
+#pragma unroll
+      for (int hq = 0; hq < 2; ++hq) {
+        float f[8], fi[8], kv[8], x[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          kw[e] = __byte_perm(kw[e], 0u, 0x1032);
-          qw[e] = __byte_perm(qw[e], 0u, 0x1032);
-          const float tmp = Gl[0][e];
-          Gl[0][e] = Gl[1][e];
-          Gl[1][e] = tmp;
-        }
-      }
-      float gam_c[2];  // gamma_C of this thread's two channels
-#pragma unroll
-      for (int o2 = 0; o2 < 2; ++o2) {
-        const int s2 = o2 ^ sw, c = cp + s2;
-        // R_b = sum of the tile sums before tile b; G_C = all of them
-        float R[4], GC = 0.f;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          R[b] = GC;
-          GC += Tot[b * D + c];
-        }
-        const float Ra = ta == 0 ? R[0] : (ta == 1 ? R[1] : (ta == 2 ? R[2] : R[3]));
-        const float eRa = exp2_approx(Ra);       // exp(R_a) <= 1
-        const float eCa = exp2_approx(GC - Ra);  // exp(G_C - R_a) <= 1
-        float f[8], fi[8], kv[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float dd = Gl[o2][e];  // G_r - R_a, in (-80, 0]
+          const float dd = Gl[o2][8 * hq + e];  // G_r - R_a, in (-80, 0]
           f[e] = exp2_approx(dd);
           fi[e] = exp2_approx(-dd);
-          kv[e] = o2 ? bf16_hi(kw[e]) : bf16_lo(kw[e]);
+          kv[e] = o2 ? bf16_hi(kw[8 * hq + e]) : bf16_lo(kw[8 * hq + e]);
         }
-        float x[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) x[e] = kv[e] * f[e];  // k exp(G_r - R_a)
-        *reinterpret_cast<uint4*>(sm + kP_Bop + mn_chunk(128, 4 * ta + hq, c)) = pack8(x);
+        *reinterpret_cast<uint4*>(sm + kQ_Bop + mn_chunk(128, 4 * ta + hq, c)) = pack8(x);
 #pragma unroll
         for (int e = 0; e < 8; ++e) x[e] *= eRa;  // Gamma k (beta is folded into T)
-        *reinterpret_cast<uint4*>(sm + kP_BKg + sw128_chunk(128, c, 2 * ta + hq)) = pack8(x);
+        *reinterpret_cast<uint4*>(sm + kQ_BKg + sw128_chunk(128, c, 2 * ta + hq)) = pack8(x);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = (o2 ? bf16_hi(qw[e]) : bf16_lo(qw[e])) * f[e];
-        *reinterpret_cast<uint4*>(sm + kP_Bop + mn_chunk(128, 4 * ta + 2 + hq, c)) = pack8(x);
+        for (int e = 0; e < 8; ++e)
+          x[e] = (o2 ? bf16_hi(qw[8 * hq + e]) : bf16_lo(qw[8 * hq + e])) * f[e];
+        *reinterpret_cast<uint4*>(sm + kQ_Bop + mn_chunk(128, 4 * ta + 2 + hq, c)) = pack8(x);
 #pragma unroll
         for (int e = 0; e < 8; ++e) x[e] *= eRa;  // Gamma q
-        *reinterpret_cast<uint4*>((kZ ? sm + kP_Qs : unit + kQ) + mn_chunk(64, 2 * ta + hq, c)) =
-            pack8(x);
+        tmem_st4(t_park + 4 * (2 * o2 + hq), pack8(x));
 #pragma unroll
         for (int e = 0; e < 8; ++e) kv[e] *= fi[e];  // k exp(R_a - G_r)
 #pragma unroll
         for (int e = 0; e < 8; ++e) x[e] = kv[e] * eCa;  // (gamma_C / Gamma) k
-        if (kP) {  // fp32, tokens r0 .. r0 + 3 and r0 + 4 .. r0 + 7 of row c
+        if (kP) {  // fp32, tokens 8 hq .. +3 and +4 .. +7 of the tile
           *reinterpret_cast<float4*>(unit + kKT + kt32_chunk(c, 4 * ta + 2 * hq)) =
               make_float4(x[0], x[1], x[2], x[3]);
           *reinterpret_cast<float4*>(unit + kKT + kt32_chunk(c, 4 * ta + 2 * hq + 1)) =
               make_float4(x[4], x[5], x[6], x[7]);
         } else {
-          *reinterpret_cast<uint4*>((kZ ? sm + kP_KTs : unit + kKT) +
-                                    sw128_chunk(128, c, 2 * ta + hq)) = pack8(x);
+          tmem_st4(t_park + 16 + 4 * (2 * o2 + hq), pack8(x));
         }
 #pragma unroll
         for (int ap = 0; ap < 4; ++ap) {
@@ -553,52 +649,70 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
           const float E = (ap > ta) ? exp2_approx(R[ap] - Ra) : 1.f;  // exp(R_ap - R_a) <= 1
 #pragma unroll
           for (int e = 0; e < 8; ++e) x[e] = kv[e] * E;
-          *reinterpret_cast<uint4*>(sm + kP_KC + mn_chunk(kKCX, ap * (ap + 1) + 2 * ta + hq, c)) =
+          *reinterpret_cast<uint4*>(sm + kQ_KC + mn_chunk(kKCX, ap * (ap + 1) + 2 * ta + hq, c)) =
               pack8(x);
         }
-        gam_c[o2] = exp2_approx(GC);
       }
+      if (ta == 0) gam_out[(size_t)u * D + c] = exp2_approx(GC);
+    }
+    tmem_wait_st();
 
-      // ---- block products in one N=160 MMA chain: D[m][n] = Bop row m . KC row n
-      //      over the channels; lane m = 32 ta + 16 part + j is K row (part 0) or
-      //      Q row (part 1) j of tile ta, and KC(ta) sits at columns 8 ta (ta + 1)
-      fence_proxy_async_smem();
-      tc_fence_before();
-      named_sync(1, kPrepCompute);
-      if (t == 0) {
-        tc_fence_after();
-        const uint32_t id = idesc_bf16_mn(128, 160, 1, 1);  // KC columns 160..191 unused
-        const uint64_t da = mnmajor_desc(sbase + kP_Bop, 2048, 0);
-        const uint64_t db = mnmajor_desc(sbase + kP_KC, mn_sbo(kKCX), 0);
-#pragma unroll
-        for (int s = 0; s < D / 16; ++s)
-          mma_bf16(tmem + 0, desc_advance(da, s * 2 * 2048), desc_advance(db, s * 2 * mn_sbo(kKCX)),
-                   id, s > 0);
-        mma_commit(bar_p);
-      }
-      // loads for the units ahead while the products run
-      fetch_start(slots[(it + 1) & 1]);
-      if (rg == 0) {  // global stores only after the proxy fence above (it waits for them)
-        gam_out[(size_t)u * D + cp + sw] = gam_c[0];
-        gam_out[(size_t)u * D + cp + (sw ^ 1)] = gam_c[1];
-      }
-      if (kZ && t == kStorer) {
-        bulk_s2g(unit + kQ, sbase + kP_Qs, 16384);
-        if (!kP) bulk_s2g(unit + kKT, sbase + kP_KTs, 16384);
-        bulk_commit();
-      }
-      // the previous unit's W and U^T leave while the products run
-      if (it > 0) write_wu(tiles + (size_t)(u - gridDim.x) * unit_bytes<kP>());
-      ok = mbar_wait(bar_p, it & 1, err);
-      if (!named_sync_and(1, kPrepCompute, ok)) { aborted = true; break; }
+    // ---- block products in one N=160 MMA chain (see the key-operand layout above)
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (t == 0) {
       tc_fence_after();
-      {
-        // warp -> tile tw = warp & 3 (its TMEM lane quarter) and key piece pc = warp >> 2
-        // (keys i = 16 pc .. +15); lane -> row r = 16 tw + (lane & 15), K or Q row
-        const int tw = warp & 3, pc = warp >> 2, r = 16 * tw + (t & 15);
-        const bool qrow = (t & 16) != 0;
+      const uint32_t id = idesc_bf16_mn(128, 160, 1, 1);
+      const uint64_t da = mnmajor_desc(sbase + kQ_Bop, 2048, 0);
+      const uint64_t db = mnmajor_desc(sbase + kQ_KC, mn_sbo(kKCX), 0);
+#pragma unroll
+      for (int s = 0; s < D / 16; ++s)
+        mma_bf16(tmem + 0, desc_advance(da, s * 2 * 2048), desc_advance(db, s * 2 * mn_sbo(kKCX)),
+                 id, s > 0);
+      mma_commit(bar_p);
+      pend_p = (int)(it & 1);
+    }
+    if (t == 32 && nx_valid) {  // the next unit's rows into L2
+      tma_prefetch_l2_3d(&tm_k, 0, nx_h, nx_e.x);
+      tma_prefetch_l2_3d(&tm_q, 0, nx_h, nx_e.x);
+      tma_prefetch_l2_3d(&tm_v, 0, nx_h, nx_e.x);
+      tma_prefetch_l2_3d(&tm_v, 64, nx_h, nx_e.x);
+      if (!g_sc) tma_prefetch_l2_3d(&tm_g, 0, nx_h, nx_e.x);
+    }
+    const bool okp = mbar_wait(bar_p, it & 1, err);
+    if (t == 0 && okp) pend_p = -1;
+    tc_fence_after();
+    {  // the parked Gamma*Q and Kt^T -> the row operand's space (dead now), MMA-ready
+      float pk[32];
+      tmem_ld32(t_park, pk);
+      tmem_wait_ld();
+#pragma unroll
+      for (int o2 = 0; o2 < 2; ++o2) {
+        const int c = cp + (o2 ^ sw);
+#pragma unroll
+        for (int hq = 0; hq < 2; ++hq) {
+          const int j = 4 * (2 * o2 + hq);
+          *reinterpret_cast<uint4*>(sm + kQ_Bop + mn_chunk(64, 2 * ta + hq, c)) =
+              make_uint4(__float_as_uint(pk[j]), __float_as_uint(pk[j + 1]),
+                         __float_as_uint(pk[j + 2]), __float_as_uint(pk[j + 3]));
+          if (!kP)
+            *reinterpret_cast<uint4*>(sm + kQ_Bop + 16384 + sw128_chunk(128, c, 2 * ta + hq)) =
+                make_uint4(__float_as_uint(pk[16 + j]), __float_as_uint(pk[17 + j]),
+                           __float_as_uint(pk[18 + j]), __float_as_uint(pk[19 + j]));
+        }
+      }
+    }
+    {
+      // read-out: warp -> tile tw (its TMEM lane quarter) and key pieces pc of 16
+      // keys; lane -> row r = 16 tw + (lane & 15), a K row or (lane & 16) a Q row
+      const int tw = warp & 3, r = 16 * tw + (t & 15);
+      const bool qrow = (t & 16) != 0;
+#pragma unroll
+      for (int pp = 0; pp < 2; ++pp) {
+        const int pc = 2 * (warp >> 2) + pp;
         float pv[16];
-        if (pc <= tw) {  // keys of tiles up to tw only (warp-uniform)
+        if (pc <= tw) {
           tmem_ld16(lane_addr + 8 * tw * (tw + 1) + 16 * pc, pv);
           tmem_wait_ld();
         } else {
@@ -618,291 +732,129 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         } else {
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) pv[jj] = (16 * pc + jj <= r) ? pv[jj] : 0.f;
-          *reinterpret_cast<uint4*>(sm + kP_AQs + sw128_chunk(64, r, 2 * pc)) = pack8(pv);
-          *reinterpret_cast<uint4*>(sm + kP_AQs + sw128_chunk(64, r, 2 * pc + 1)) = pack8(pv + 8);
+          *reinterpret_cast<uint4*>(sm + kQ_AQ + sw128_chunk(64, r, 2 * pc)) = pack8(pv);
+          *reinterpret_cast<uint4*>(sm + kQ_AQ + sw128_chunk(64, r, 2 * pc + 1)) = pack8(pv + 8);
         }
       }
-      if (kZ && t == kStorer) bulk_wait_read_all();  // the next pass 1 rewrites the Q staging
-      if (g_sc && t >= 64 && t < 128) gsc_s[t - 64] = gsc_nx;  // for the next pass 1
-      fence_proxy_async_smem();  // the A_qk tile leaves by a bulk copy
-      named_sync(1, kPrepCompute);
-      if (t == kStorer) {
-        // W^T, U^T of the previous unit (and the Gamma*Q, Kt^T tiles) have left the
-        // k, q staging by now: fetch the next unit's rows into it -- before the next
-        // unit's pass 1, which reads them when q and k are normalised here -- then
-        // send A_qk
-        bulk_wait_read_all();
-        issue_kqv(slots[(it + 1) & 1]);
-        bulk_s2g(unit + kAQ, sbase + kP_AQs, 8192);
-        bulk_commit();
-      }
-      // Warps 8-15: pass 1 of the next unit while warps 0-3 form this unit's inverse.
-      bool ok1 = true;
-      if (t >= kInvThreads) ok1 = pass1(slots[(it + 1) & 1], (it + 1) & 1);
-      if (t < 128) {
-        // ---- T = (I + L)^{-1} in fp32.  Warp wq owns diagonal 16x16 block wq: its 8x8
-        //      halves by forward substitution, then [A 0; C B]^{-1} lower-left
-        //      = -B^{-1} C A^{-1}, warp-synchronous.  Level 1: warp 2b forms
-        //      P = L_{2b+1,2b} D_{2b} from its own block and hands it to warp 2b+1
-        //      (named barrier 3 + b), which forms T_{2b+1,2b} = -D_{2b+1} P.  Level 2 below,
-        //      on warps 4-7 from the end of level 0 and on warps 0-7 after level 1.
-        //      Stored blocks carry zeros above their diagonals; blocks above the
-        //      diagonal are never stored nor read.
-        const int wq = warp, o = 16 * wq, wl = t & 31;  // warp, its block, lane in warp
-        if (wl < 16) {  // A^{-1} (lanes 0-7), B^{-1} (lanes 8-15): one column per lane
-          const int ob = o + 8 * (wl >> 3), cc = wl & 7;
-          float x[8];
+    }
+    fence_proxy_async_smem();  // Gamma*Q, Kt^T and A_qk leave by bulk copies
+    tc_fence_before();
+    if (!__syncthreads_and(okp)) {
+      ok = false;
+      break;
+    }
+    if (t == kCopier) {
+      bulk_s2g(unit + kQ, sbase + kQ_Bop, 16384);
+      if (!kP) bulk_s2g(unit + kKT, sbase + kQ_Bop + 16384, 16384);
+      bulk_s2g(unit + kAQ, sbase + kQ_AQ, 8192);
+      bulk_commit();
+      // V lands in the row operand's space once the copies have read it (while
+      // warps 0-3 run the first level of the inverse)
+      bulk_wait_read_all();
+      mbar_arrive_expect_tx(bar_v, 16384);
+      tma_load_3d(sbase + kQ_V, &tm_v, 0, h, (int)t0, bar_v);
+      tma_load_3d(sbase + kQ_V + 8192, &tm_v, 64, h, (int)t0, bar_v);
+      pend_v = (int)(it & 1);
+    }
+    invert_unit_lower(Lb, Tb, Ps, t);
+    __syncthreads();
+    {  // M = T Diag(beta) -> bf16 B operand (MN-major, X = row r, K = column j)
+      const int j = t & 63;
+      const float bj = beta_s[j];
 #pragma unroll
-          for (int m = 0; m < 8; ++m) {
-            float lr[8];
-            *reinterpret_cast<float4*>(lr) = *reinterpret_cast<const float4*>(Lb + (ob + m) * kLdL + ob);
-            *reinterpret_cast<float4*>(lr + 4) =
-                *reinterpret_cast<const float4*>(Lb + (ob + m) * kLdL + ob + 4);
-            float acc = 0.f;
-#pragma unroll
-            for (int i2 = 0; i2 < m; ++i2) acc = fmaf(lr[i2], x[i2], acc);
-            x[m] = (m < cc) ? 0.f : (m == cc ? 1.f : -acc);
-          }
-#pragma unroll
-          for (int m = 0; m < 8; ++m) Tb[(ob + m) * kLdT + ob + cc] = x[m];
-          if (wl < 8) {  // the zero upper-right 8x8 of the 16x16 block
-#pragma unroll
-            for (int m = 0; m < 8; ++m) Tb[(ob + m) * kLdT + ob + 8 + cc] = 0.f;
-          }
-        }
-        __syncwarp();
-        const int di = wl >> 2, dj = 2 * (wl & 3);  // 8x8: row di, columns dj, dj + 1
-        {  // P = C A^{-1}
-          float lr[8];
-          *reinterpret_cast<float4*>(lr) = *reinterpret_cast<const float4*>(Lb + (o + 8 + di) * kLdL + o);
-          *reinterpret_cast<float4*>(lr + 4) =
-              *reinterpret_cast<const float4*>(Lb + (o + 8 + di) * kLdL + o + 4);
-          float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {  // A^{-1} has stored zeros above the diagonal
-            a0 = fmaf(lr[k], Tb[(o + k) * kLdT + o + dj], a0);
-            a1 = fmaf(lr[k], Tb[(o + k) * kLdT + o + dj + 1], a1);
-          }
-          Ps[wq * 64 + di * 8 + dj] = a0;
-          Ps[wq * 64 + di * 8 + dj + 1] = a1;
-        }
-        __syncwarp();
-        {  // lower-left 8x8 = -B^{-1} P
-          float wr[8];
-          *reinterpret_cast<float4*>(wr) = *reinterpret_cast<const float4*>(Tb + (o + 8 + di) * kLdT + o + 8);
-          *reinterpret_cast<float4*>(wr + 4) =
-              *reinterpret_cast<const float4*>(Tb + (o + 8 + di) * kLdT + o + 12);
-          float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {  // B^{-1} has stored zeros above the diagonal
-            a0 = fmaf(wr[k], Ps[wq * 64 + k * 8 + dj], a0);
-            a1 = fmaf(wr[k], Ps[wq * 64 + k * 8 + dj + 1], a1);
-          }
-          Tb[(o + 8 + di) * kLdT + o + dj] = -a0;
-          Tb[(o + 8 + di) * kLdT + o + dj + 1] = -a1;
-        }
-        __syncwarp();
-        if (wq < 2) named_arrive(5, 192);  // D_0, D_1 are stored: warps 4-7 may read them
-        // level 1 (2 rows x 4 columns per wl: rows rp and rp + 8)
-        const int blk = wq >> 1, a = 2 * blk, R = a + 1, rp = (wl >> 2) & 7, cq = wl & 3;
-        float* P1 = Ps + 256 + blk * 256;
-        if ((wq & 1) == 0) {  // P = L_{a+1,a} D_a
-          float acc[2][4] = {};
-#pragma unroll
-          for (int k4 = 0; k4 < 16; k4 += 4) {
-            float lv[2][4];
-#pragma unroll
-            for (int r = 0; r < 2; ++r)
-              *reinterpret_cast<float4*>(lv[r]) =
-                  *reinterpret_cast<const float4*>(Lb + (16 * R + rp + 8 * r) * kLdL + 16 * a + k4);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const float4 tv =
-                  *reinterpret_cast<const float4*>(Tb + (16 * a + k4 + kk) * kLdT + 16 * a + 4 * cq);
-#pragma unroll
-              for (int r = 0; r < 2; ++r) {
-                const float l = lv[r][kk];
-                acc[r][0] = fmaf(l, tv.x, acc[r][0]);
-                acc[r][1] = fmaf(l, tv.y, acc[r][1]);
-                acc[r][2] = fmaf(l, tv.z, acc[r][2]);
-                acc[r][3] = fmaf(l, tv.w, acc[r][3]);
-              }
-            }
-          }
-#pragma unroll
-          for (int r = 0; r < 2; ++r)
-            *reinterpret_cast<float4*>(P1 + (rp + 8 * r) * 16 + 4 * cq) =
-                make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
-          named_arrive(3 + blk, 64);
-        } else {  // T_{a+1,a} = -D_{a+1} P
-          named_sync(3 + blk, 64);
-          float acc[2][4] = {};
-#pragma unroll
-          for (int k4 = 0; k4 < 16; k4 += 4) {
-            float wv[2][4];
-#pragma unroll
-            for (int r = 0; r < 2; ++r)
-              *reinterpret_cast<float4*>(wv[r]) =
-                  *reinterpret_cast<const float4*>(Tb + (16 * R + rp + 8 * r) * kLdT + 16 * R + k4);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const float4 pv = *reinterpret_cast<const float4*>(P1 + (k4 + kk) * 16 + 4 * cq);
-#pragma unroll
-              for (int r = 0; r < 2; ++r) {
-                const float w = wv[r][kk];
-                acc[r][0] = fmaf(w, pv.x, acc[r][0]);
-                acc[r][1] = fmaf(w, pv.y, acc[r][1]);
-                acc[r][2] = fmaf(w, pv.z, acc[r][2]);
-                acc[r][3] = fmaf(w, pv.w, acc[r][3]);
-              }
-            }
-          }
-#pragma unroll
-          for (int r = 0; r < 2; ++r)
-            *reinterpret_cast<float4*>(Tb + (16 * R + rp + 8 * r) * kLdT + 16 * a + 4 * cq) =
-                make_float4(-acc[r][0], -acc[r][1], -acc[r][2], -acc[r][3]);
-        }
-      } else if (t < kInvThreads) {
-        // Warps 4-7, while warps 0-3 run level 1: the terms of level 2's
-        // M = L[32:64, 0:32] T[0:32, 0:32] that need only D_0 and D_1, i.e.
-        // M[:, 0:16] = L[32:64, 0:16] D_0 and M[:, 16:32] = L[32:64, 16:32] D_1
-        // (T[0:16, 16:32] is zero), into the unused upper-right block of Tb (rows
-        // 0..31, columns 32..63).  2 rows x 4 columns per thread.
-        named_sync(5, 192);
-        const int tt = t - 128, rp = tt >> 3, cq = tt & 7, kb = cq >= 4 ? 16 : 0;
-        float acc[2][4] = {};
-#pragma unroll
-        for (int k4 = 0; k4 < 16; k4 += 4) {
-          float lv[2][4];
-#pragma unroll
-          for (int r = 0; r < 2; ++r)
-            *reinterpret_cast<float4*>(lv[r]) =
-                *reinterpret_cast<const float4*>(Lb + (32 + 2 * rp + r) * kLdL + kb + k4);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const float4 tv = *reinterpret_cast<const float4*>(Tb + (kb + k4 + kk) * kLdT + 4 * cq);
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-              const float l = lv[r][kk];
-              acc[r][0] = fmaf(l, tv.x, acc[r][0]);
-              acc[r][1] = fmaf(l, tv.y, acc[r][1]);
-              acc[r][2] = fmaf(l, tv.z, acc[r][2]);
-              acc[r][3] = fmaf(l, tv.w, acc[r][3]);
-            }
-          }
-        }
-#pragma unroll
-        for (int r = 0; r < 2; ++r)
-          *reinterpret_cast<float4*>(Tb + 32 + (2 * rp + r) * kLdT + 4 * cq) =
-              make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
-      }
-      if (t < kInvThreads) {
-        // level 2 on warps 0-7 (barrier 2, 256 threads): M[:, 0:16] += L[32:64, 16:32]
-        // T_{1,0} (one row x 2 columns per thread), then T[32:64, 0:32] = -T22 M.
-        named_sync(2, kInvThreads);
-        float* Mb = Tb + 32;
-        {
-          const int r = t >> 3, cp = t & 7;
-          float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-          for (int k4 = 16; k4 < 32; k4 += 4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(Lb + (32 + r) * kLdL + k4);
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const float2 tv = *reinterpret_cast<const float2*>(Tb + (k4 + kk) * kLdT + 2 * cp);
-              a0 = fmaf(lv[kk], tv.x, a0);
-              a1 = fmaf(lv[kk], tv.y, a1);
-            }
-          }
-          float2* mp = reinterpret_cast<float2*>(Mb + r * kLdT + 2 * cp);
-          const float2 m0 = *mp;
-          *mp = make_float2(m0.x + a0, m0.y + a1);
-        }
-        const int rp = t >> 4, cq = t & 15;
-        named_sync(2, kInvThreads);
-        {  // T[32:64, 0:32] = -T[32:64, 32:64] M; T[32:48, 48:64] is zero
-          const int kn = rp < 8 ? 16 : 32;  // warp-uniform: warps 0-3 hold rows 32..47
-          float acc[2][2] = {};
-#pragma unroll
-          for (int k4 = 0; k4 < 32; k4 += 4) {
-            if (k4 < kn) {
-              float wv[2][4];
-#pragma unroll
-              for (int r = 0; r < 2; ++r)
-                *reinterpret_cast<float4*>(wv[r]) =
-                    *reinterpret_cast<const float4*>(Tb + (32 + 2 * rp + r) * kLdT + 32 + k4);
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const float2 mv = *reinterpret_cast<const float2*>(Mb + (k4 + kk) * kLdT + 2 * cq);
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                  acc[r][0] = fmaf(wv[r][kk], mv.x, acc[r][0]);
-                  acc[r][1] = fmaf(wv[r][kk], mv.y, acc[r][1]);
-                }
-              }
-            }
-          }
-#pragma unroll
-          for (int r = 0; r < 2; ++r)
-            *reinterpret_cast<float2*>(Tb + (32 + 2 * rp + r) * kLdT + 2 * cq) =
-                make_float2(-acc[r][0], -acc[r][1]);
-        }
-      }
-      if (!named_sync_and(1, kPrepCompute, ok1)) { aborted = true; break; }
-      {  // M = T Diag(beta) -> bf16 B operand (MN-major, X = row r, K = column j); zero
-         // above the diagonal.  A warp reads 32 consecutive columns of one row: no bank
-         // conflicts.  With beta in M, W = M (Gamma K) and U = M V take Gamma K and V
-         // as they are (beta is zero on the rows past a sequence's end).
-        const int j = t & 63, o8 = t >> 6;
-        const float bj = beta_s[j];
+      for (int oo = 0; oo < 2; ++oo) {
+        const int o8 = (t >> 6) + 4 * oo;
         float x[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int r = 8 * o8 + e;
           x[e] = (r >= j) ? Tb[r * kLdT + j] * bj : 0.f;
         }
-        *reinterpret_cast<uint4*>(sm + kP_T + mn_chunk(64, o8, j)) = pack8(x);
+        *reinterpret_cast<uint4*>(sm + kQ_T + mn_chunk(64, o8, j)) = pack8(x);
       }
-      fetch_finish(it & 1);
+    }
+    if (g_sc && t < 64) gsc_s[t] = gs_nx;  // the next unit's pass 1 reads them
+    fence_proxy_async_smem();
+    tc_fence_before();
+    bool okv = true;
+    if (t == kCopier) {
+      okv = mbar_wait(bar_v, it & 1, err);
+      if (okv) pend_v = -1;
+    }
+    if (!__syncthreads_and(okv)) {
+      ok = false;
+      break;
+    }
+    if (t == 0) {
+      tc_fence_after();
+      const uint32_t id = idesc_bf16_mn(128, 64, 0, 1);
+      const uint32_t idv = idesc_bf16_mn(128, 64, 1, 1);  // A = V^T read MN-major
+      const uint64_t dk = kmajor_desc(sbase + kQ_BKg, 128, 0);
+      const uint64_t dv = mnmajor_desc_lbo(sbase + kQ_V, 8192, 1024, 0);
+      const uint64_t dt = mnmajor_desc(sbase + kQ_T, 1024, 0);
+#pragma unroll
+      for (int s = 0; s < C / 16; ++s)  // W^T = (Gamma K)^T M^T
+        mma_bf16(tmem + 0, desc_advance(dk, s * 32), desc_advance(dt, s * 2048), id, s > 0);
+#pragma unroll
+      for (int s = 0; s < C / 16; ++s)  // U^T = V^T M^T
+        mma_bf16(tmem + 64, desc_advance(dv, s * 2048), desc_advance(dt, s * 2048), idv, s > 0);
+      mma_commit(bar_w);
+      pend_w = (int)(it & 1);
+      // the inverse's scratch is read: the next unit's k, q, z land in its space
+      if (nx_valid) issue_in(nx_h, nx_e.x, (int)((it + 1) & 1));
+    }
+    ok = mbar_wait(bar_w, it & 1, err);
+    if (t == 0 && ok) {
+      pend_w = -1;
+      // the W/U products have read V and T: the next unit's g lands in their space
+      if (g_fp32 && nx_valid) issue_g(nx_h, nx_e.x, (int)((it + 1) & 1));
+    }
+    tc_fence_after();
+    {  // W (MN-major, warps 0-3) and U^T (K-major, warps 4-7), row = TMEM lane: each
+       // warp's 32 rows are 4 KB of the tile, staged and sent by one bulk copy
+      const int row = 32 * (warp & 3) + lane32;
+      const uint32_t stage = warp < 4 ? kQ_BKg : q_ustage<kZ>();
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        float w[32];
+        tmem_ld32(lane_addr + 64 * (warp >> 2) + 32 * part, w);
+        tmem_wait_ld();
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          const int xc = 4 * part + ch;
+          const uint32_t off = warp < 4 ? mn_chunk(64, xc, row) : sw128_chunk(128, row, xc);
+          *reinterpret_cast<uint4*>(sm + stage + off) = pack8(&w[8 * ch]);
+        }
+      }
       fence_proxy_async_smem();
-      tc_fence_before();
-      named_sync(1, kPrepCompute);
-      // the next unit's g / z has been read by pass 1: fetch the one after it
-      // (its slot was just filled by fetch_finish)
-      if (t == kIssuer) issue_g(slots[it & 1]);
-      if (t == 0) {
-        tc_fence_after();
-        const uint32_t id = idesc_bf16_mn(128, 64, 0, 1);
-        const uint32_t idv = idesc_bf16_mn(128, 64, 1, 1);  // A = V^T read MN-major
-        const uint64_t dk = kmajor_desc(sbase + kP_BKg, 128, 0);
-        // V in slot it & 1: two 64-channel atoms 8 KB apart, 8-token groups 1 KB apart
-        const uint64_t dv = mnmajor_desc_lbo(sbase + ((it & 1) ? kP_V2 : kI_V), 8192, 1024, 0);
-        const uint64_t dt = mnmajor_desc(sbase + kP_T, 1024, 0);
-#pragma unroll
-        for (int s = 0; s < C / 16; ++s)  // W^T = (Gamma K)^T M^T
-          mma_bf16(tmem + 256, desc_advance(dk, s * 32), desc_advance(dt, s * 2048), id, s > 0);
-#pragma unroll
-        for (int s = 0; s < C / 16; ++s)  // U^T = V^T M^T
-          mma_bf16(tmem + 320, desc_advance(dv, s * 2048), desc_advance(dt, s * 2048), idv, s > 0);
-        mma_commit(bar_w);  // waited for by the next unit (or after the loop)
+      __syncwarp();
+      if (lane32 == 0) {
+        const uint32_t piece = 4096u * (uint32_t)(warp & 3);
+        bulk_s2g(unit + (warp < 4 ? kW : kUT) + piece, sbase + stage + piece, 4096);
+        bulk_commit();
       }
     }
-    // the last unit's W and U^T
-    if (!aborted && it > 0) {
-      const bool okw = mbar_wait(bar_w, (it - 1) & 1, err);
-      if (named_sync_and(1, kPrepCompute, okw))
-        write_wu(tiles + (size_t)(blockIdx.x + (int64_t)(it - 1) * gridDim.x) * unit_bytes<kP>());
-    }
+    tc_fence_before();
+    cur_chunk = nx_chunk;
+    cur_h = nx_h;
+    cur_e = nx_e;
+    cur_a = nx_a;
+    b_cur = b_nx;
   }
-  if (t == kStorer) bulk_wait_all();
-  // a copy still in flight (after an abort) must land before the CTA may exit
-  if (t == kStorer && issued_kqv > 0) mbar_wait(bar_kqv, (issued_kqv - 1) & 1, err);
-  if (t == kIssuer && issued_g > 0) mbar_wait(bar_g, (issued_g - 1) & 1, err);
+  // after an abort: let the copies and products in flight finish before the TMEM
+  // and the shared memory go away
+  if (t == kCopier && pend_v >= 0) mbar_wait(bar_v, (uint32_t)pend_v, err);
+  if (t == 0) {
+    if (pend_p >= 0) mbar_wait(bar_p, (uint32_t)pend_p, err);
+    if (pend_w >= 0) mbar_wait(bar_w, (uint32_t)pend_w, err);
+    if (pend_in >= 0) mbar_wait(bar_in, (uint32_t)pend_in, err);
+    if (pend_g >= 0) mbar_wait(bar_g, (uint32_t)pend_g, err);
+  }
+  if (lane32 == 0) bulk_wait_all();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, 256);
   }
 }
 
@@ -1773,10 +1725,13 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
   if (units > 0 && n_tokens > 0) {  // with no tokens there are no chunks to prepare
     auto kern = precise ? (fused ? tc_prep<true, true> : tc_prep<false, true>)
                         : (fused ? tc_prep<true, false> : tc_prep<false, false>);
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kP_Smem);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kQ_Smem);
+    if (e == cudaSuccess)  // room for two CTAs per SM
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    const int sms = sm_count();
-    const int grid = (int)(units < sms ? units : sms);
+    const int ctas = 2 * sm_count();
+    const int grid = (int)(units < ctas ? units : ctas);
     CUtensorMap tm[4];
     e = encode_rows(&tm[0], k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n_tokens);
     if (e == cudaSuccess) e = encode_rows(&tm[1], q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n_tokens);
@@ -1787,16 +1742,16 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
       if (fused)
         e = encode_rows(&tm[3], z, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n_tokens);
       else if (scalar_g)
-        tm[3] = tm[0];  // not used: scalar gates are plain loads
+        tm[3] = tm[0];  // not used: scalar gates are plain loads, not prefetched
       else
         e = encode_rows(&tm[3], g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, n_tokens);
     }
     if (e != cudaSuccess) return e;
     ProfScope prof_scope(fused ? "kda_tc_prep_gated" : "kda_tc_prep", s);
-    kern<<<grid, kPrepThreads, kP_Smem, s>>>(tm[0], tm[1], tm[2], tm[3],
-                                             static_cast<const T*>(beta), A, g_min, plan, H,
-                                             units, tiles, gam, fz.qk_eps,
-                                             (scalar_g && !fused) ? g : nullptr, err);
+    kern<<<grid, kP2Threads, kQ_Smem, s>>>(tm[0], tm[1], tm[2], tm[3],
+                                           static_cast<const T*>(beta), A, g_min, plan, H,
+                                           units, tiles, gam, fz.qk_eps,
+                                           (scalar_g && !fused) ? g : nullptr, err);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
