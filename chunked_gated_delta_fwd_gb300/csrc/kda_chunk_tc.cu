@@ -83,7 +83,6 @@ constexpr int kKCX = 192;
 // The inverse's scratch: L, T fp32 [64][68] (16-byte rows: float4 loads along k) and
 // the block products, fp32 [3][16][16].
 constexpr int kLdL = 68, kLdT = 68;
-constexpr uint32_t kScratchBytes = 17408 + 17408 + 3072;
 constexpr int kInvThreads = 256;  // the inverse runs on warps 0-7
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -169,7 +168,7 @@ __device__ __forceinline__ void invert_unit_lower(const float* __restrict__ Lb,
     float* P1 = Ps + 256 + blk * 256;
     if ((wq & 1) == 0) {  // P = L_{a+1,a} D_a
       float acc[2][4] = {};
-#pragma unroll
+#pragma unroll 1  // kept rolled: less code for the instruction cache
       for (int k4 = 0; k4 < 16; k4 += 4) {
         float lv[2][4];
 #pragma unroll
@@ -198,7 +197,7 @@ __device__ __forceinline__ void invert_unit_lower(const float* __restrict__ Lb,
     } else {  // T_{a+1,a} = -D_{a+1} P
       named_sync(3 + blk, 64);
       float acc[2][4] = {};
-#pragma unroll
+#pragma unroll 1  // kept rolled: less code for the instruction cache
       for (int k4 = 0; k4 < 16; k4 += 4) {
         float wv[2][4];
 #pragma unroll
@@ -232,7 +231,7 @@ __device__ __forceinline__ void invert_unit_lower(const float* __restrict__ Lb,
     named_sync(5, 192);
     const int tt = t - 128, rp = tt >> 3, cq = tt & 7, kb = cq >= 4 ? 16 : 0;
     float acc[2][4] = {};
-#pragma unroll
+#pragma unroll 1  // kept rolled: less code for the instruction cache
     for (int k4 = 0; k4 < 16; k4 += 4) {
       float lv[2][4];
 #pragma unroll
@@ -285,7 +284,7 @@ __device__ __forceinline__ void invert_unit_lower(const float* __restrict__ Lb,
     {  // T[32:64, 0:32] = -T[32:64, 32:64] M; T[32:48, 48:64] is zero
       const int kn = rp < 8 ? 16 : 32;  // warp-uniform: warps 0-3 hold rows 32..47
       float acc[2][2] = {};
-#pragma unroll
+#pragma unroll 1  // kept rolled: less code for the instruction cache
       for (int k4 = 0; k4 < 32; k4 += 4) {
         if (k4 < kn) {
           float wv[2][4];
@@ -324,38 +323,41 @@ __device__ __forceinline__ void invert_unit_lower(const float* __restrict__ Lb,
 // and builds the operands of its 16 rows x 2 channels.  Only the per-tile totals of
 // g cross threads.  Every shared-memory block serves several phases of a unit:
 //   row operand (32 KB): K/Q rows for the products; then Gamma*Q and Kt^T on
-//     their way out (parked in TMEM meanwhile); then V (tensor copy) and
-//     T Diag(beta) for the W/U products; then the next unit's g (fp32), or U^T on
-//     its way out (gate fused)
+//     their way out (parked in TMEM meanwhile); then V (tensor copy), T Diag(beta)
+//     and the next unit's z rows 0-31 (copied in as soon as the outgoing copies
+//     have read the space); then the next unit's g (fp32), or U^T on its way out
+//     (gate fused)
 //   key operand (48 KB): KC for the products; then the inverse's scratch; then the
-//     next unit's k, q and z (copied in while this unit's W/U products run), or U^T
-//     on its way out (g read)
+//     next unit's k and q (copied in once T is read), or U^T on its way out (g read)
 //   (Gamma K)^T (16 KB): the W product's A operand; then W on its way out
-//   A_qk (8 KB) on its way out
+//   A_qk (8 KB) on its way out; then the next unit's z rows 32-63
 constexpr int kP2Threads = 256;
 constexpr uint32_t kQ_Bop = 0;              // MN-major X=128 (K/Q rows), K=128
 constexpr uint32_t kQ_V = kQ_Bop;           //   V: two 64-channel SW128 boxes
 constexpr uint32_t kQ_T = kQ_Bop + 16384;   //   bf16 T Diag(beta), MN-major 64x64
+constexpr uint32_t kQ_Zlo = kQ_Bop + 24576;  //   the next unit's z rows 0-31 (bf16)
 constexpr uint32_t kQ_Gin = kQ_Bop;         //   the next unit's g, fp32 [64][128]
 constexpr uint32_t kQ_KC = 32768;           // MN-major X=192, K=128
-constexpr uint32_t kQ_Lb = kQ_KC;           //   the inverse's scratch
-constexpr uint32_t kQ_Tb = kQ_Lb + 17408;
-constexpr uint32_t kQ_Ps = kQ_Tb + 17408;
-constexpr uint32_t kQ_Kin = kQ_KC;          //   the next unit's k, q, z (bf16 [64][128])
+constexpr uint32_t kQ_Tb = kQ_KC;           //   the inverse's scratch: T, the block
+constexpr uint32_t kQ_Ps = kQ_Tb + 17408;   //   products, and L at the end (dead one
+constexpr uint32_t kQ_Lb = kQ_KC + 49152 - 17408;  //   phase before T)
+constexpr uint32_t kQ_Kin = kQ_KC;          //   the next unit's k, q (bf16 [64][128])
 constexpr uint32_t kQ_Qin = kQ_KC + 16384;
-constexpr uint32_t kQ_Zin = kQ_KC + 32768;
+constexpr uint32_t kQ_Ug = kQ_KC + 32768;   //   U^T on its way out (g read)
 constexpr uint32_t kQ_BKg = 81920;          // K-major (Gamma K)^T 128 x 64
 constexpr uint32_t kQ_AQ = 98304;           // K-major A_qk 64 x 64
+constexpr uint32_t kQ_Zhi = kQ_AQ;          //   the next unit's z rows 32-63 (bf16)
 constexpr uint32_t kQ_Tot = kQ_AQ + 8192;   // per-tile sums of g, fp32 [4][128]
 constexpr uint32_t kQ_beta = kQ_Tot + 2048;  // fp32 [64]
 constexpr uint32_t kQ_Gsc = kQ_beta + 256;   // scalar gates, fp32 [64]
 constexpr uint32_t kQ_Red = kQ_Gsc + 256;    // row sums of squares, fp32 [8 warps][32]
 constexpr uint32_t kQ_bars = kQ_Red + 1024;  // five mbarriers + the TMEM base
 constexpr uint32_t kQ_Smem = kQ_bars + 64 + 1024;  // + slack for the 1024-byte alignment
-static_assert(kScratchBytes <= kQ_BKg - kQ_KC, "the inverse scratch fits the KC space");
+static_assert(kQ_Ps + 3072 <= kQ_Lb && kQ_Lb + 17408 == kQ_BKg, "the inverse scratch fits the KC space");
+static_assert(kQ_Qin + 16384 <= kQ_Lb + 1024 && kQ_T + 8192 <= kQ_Zlo, "k, q land in T's space, z past T");
 static_assert(2 * (kQ_Smem + 1024) <= 233472, "two CTAs per SM");
 template <bool kZ>
-__host__ __device__ constexpr uint32_t q_ustage() { return kZ ? kQ_Bop : kQ_Zin; }
+__host__ __device__ constexpr uint32_t q_ustage() { return kZ ? kQ_Bop : kQ_Ug; }
 
 // kZ: tm_g maps z (bf16) instead of g, and g = g_min * Sigmoid(exp(A_h) z) is formed
 // while the decays are summed ("Kimi K3 technical report review", section 3.2).
@@ -383,8 +385,8 @@ __global__ void __launch_bounds__(kP2Threads, 2)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kQ_bars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kQ_bars + 48);
   const uint32_t bar_p = smem_addr(&bars[0]), bar_v = smem_addr(&bars[1]);
-  const uint32_t bar_w = smem_addr(&bars[2]), bar_in = smem_addr(&bars[3]);
-  const uint32_t bar_g = smem_addr(&bars[4]);
+  const uint32_t bar_w = smem_addr(&bars[2]), bar_kq = smem_addr(&bars[3]);
+  const uint32_t bar_g = smem_addr(&bars[4]);  // the next unit's z or g
   const int t = threadIdx.x, warp = t >> 5, lane32 = t & 31;
   const bool g_fp32 = !kZ && g_sc == nullptr;  // g arrives by its own copy
 
@@ -392,7 +394,7 @@ __global__ void __launch_bounds__(kP2Threads, 2)
     mbar_init(bar_p, 1);
     mbar_init(bar_v, 1);
     mbar_init(bar_w, 1);
-    mbar_init(bar_in, 1);
+    mbar_init(bar_kq, 1);
     mbar_init(bar_g, 1);
     mbar_fence_init();
   }
@@ -415,39 +417,59 @@ __global__ void __launch_bounds__(kP2Threads, 2)
   const uint32_t t_park = lane_addr + 160u + 32u * (uint32_t)(ta >> 1);
   constexpr int kCopier = 224;  // warp 7 lane 0: copies out Gamma*Q, Kt^T and A_qk, then V in
 
-  // (chunk, head) of the current and the next unit, stepped by the grid without
-  // dividing; the next unit's table entry (and beta, scalar gates) a unit ahead
+  // (chunk, head) of the current and the next two units, stepped by the grid
+  // without dividing; table entries are loaded two units ahead, beta and the
+  // scalar gates one unit ahead
   const int grid_q = (int)(gridDim.x / H), grid_r = (int)(gridDim.x % H);
   const int64_t chunks_ub = units_ub / H;
-  int64_t cur_chunk = blockIdx.x / H;
-  int cur_h = (int)(blockIdx.x % H);
+  auto step = [&](int64_t& ch, int& hh) {
+    ch += grid_q;
+    hh += grid_r;
+    if (hh >= H) {
+      hh -= H;
+      ++ch;
+    }
+  };
+  int64_t cur_chunk = blockIdx.x / H, nx_chunk = cur_chunk;
+  int cur_h = (int)(blockIdx.x % H), nx_h = cur_h;
+  step(nx_chunk, nx_h);
   int2 cur_e = cur_chunk < chunks_ub ? __ldg(plan.tab + cur_chunk) : make_int2(0, 0);
   float cur_a = (kZ && cur_chunk < chunks_ub) ? __ldg(A + cur_h) : 0.f;
-  // outstanding asynchronous work of the issuing thread (thread 0; kCopier for V):
-  // the phase it completes, or -1; drained before the CTA exits
-  int pend_p = -1, pend_v = -1, pend_w = -1, pend_in = -1, pend_g = -1;
-  auto issue_in = [&](int hh, int tt0, int ph) {  // k, q (and z) into the key-operand space
-    mbar_arrive_expect_tx(bar_in, kZ ? 49152u : 32768u);
-    tma_load_3d(sbase + kQ_Kin, &tm_k, 0, hh, tt0, bar_in);
-    tma_load_3d(sbase + kQ_Qin, &tm_q, 0, hh, tt0, bar_in);
-    if (kZ) tma_load_3d(sbase + kQ_Zin, &tm_g, 0, hh, tt0, bar_in);
-    pend_in = ph;
+  int2 nx_e = nx_chunk < chunks_ub ? __ldg(plan.tab + nx_chunk) : make_int2(0, 0);
+  float nx_a = (kZ && nx_chunk < chunks_ub) ? __ldg(A + nx_h) : 0.f;
+  // outstanding asynchronous work of the issuing thread (thread 0; kCopier for V
+  // and z): the phase it completes, or -1; drained before the CTA exits
+  int pend_p = -1, pend_v = -1, pend_w = -1, pend_kq = -1, pend_g = -1;
+  auto issue_kq = [&](int hh, int tt0, int ph) {  // k, q into the key-operand space
+    mbar_arrive_expect_tx(bar_kq, 32768u);
+    tma_load_3d(sbase + kQ_Kin, &tm_k, 0, hh, tt0, bar_kq);
+    tma_load_3d(sbase + kQ_Qin, &tm_q, 0, hh, tt0, bar_kq);
+    pend_kq = ph;
   };
-  auto issue_g = [&](int hh, int tt0, int ph) {  // g (fp32) into the row-operand space
-    mbar_arrive_expect_tx(bar_g, 32768u);
-    tma_load_3d(sbase + kQ_Gin, &tm_g, 0, hh, tt0, bar_g);
+  // z (bf16, two 32-token boxes) or g (fp32) into the row-operand space
+  auto issue_g = [&](int hh, int tt0, int ph) {
+    mbar_arrive_expect_tx(bar_g, kZ ? 16384u : 32768u);
+    if (kZ) {
+      tma_load_3d(sbase + kQ_Zlo, &tm_g, 0, hh, tt0, bar_g);
+      tma_load_3d(sbase + kQ_Zhi, &tm_g, 0, hh, tt0 + 32, bar_g);
+    } else {
+      tma_load_3d(sbase + kQ_Gin, &tm_g, 0, hh, tt0, bar_g);
+    }
     pend_g = ph;
   };
-  float b_cur = 0.f, b_nx = 0.f, gs_nx = 0.f;  // threads 0..63: beta, scalar gate of token t
+  // threads 0..63: beta (bf16 bits) and the scalar gate of token t of this and the
+  // next unit
+  uint32_t b_cur = 0u, b_nx = 0u;
+  float gs_nx = 0.f;
   {
     const bool valid = cur_chunk < chunks_ub && cur_chunk < total;
     if (t == 0 && valid) {
-      issue_in(cur_h, cur_e.x, 0);
-      if (g_fp32) issue_g(cur_h, cur_e.x, 0);
+      issue_kq(cur_h, cur_e.x, 0);
+      if (kZ || g_fp32) issue_g(cur_h, cur_e.x, 0);
     }
     if (t < 64) {
       const bool in = valid && t < cur_e.y;
-      b_cur = in ? __bfloat162float(beta[((size_t)cur_e.x + t) * H + cur_h]) : 0.f;
+      if (in) b_cur = __ldg(reinterpret_cast<const unsigned short*>(beta) + ((size_t)cur_e.x + t) * H + cur_h);
       if (g_sc) gsc_s[t] = in ? __ldg(g_sc + ((size_t)cur_e.x + t) * H + cur_h) : 0.f;
     }
     __syncthreads();
@@ -461,38 +483,35 @@ __global__ void __launch_bounds__(kP2Threads, 2)
     const int len = cur_e.y;
     const float ea = kZ ? expf(cur_a) * kLog2e : 0.f;
     uint8_t* unit = tiles + (size_t)u * unit_bytes<kP>();
-    int64_t nx_chunk = cur_chunk + grid_q;
-    int nx_h = cur_h + grid_r;
-    if (nx_h >= H) {
-      nx_h -= H;
-      ++nx_chunk;
+    // the unit after next: its entry is loaded now and used a unit from now
+    int64_t n2_chunk = nx_chunk;
+    int n2_h = nx_h;
+    step(n2_chunk, n2_h);
+    // (predicated loads, no select on their results: nothing waits for them here)
+    int2 n2_e = make_int2(0, 0);
+    float n2_a = 0.f;
+    if (n2_chunk < chunks_ub) {
+      n2_e = __ldg(plan.tab + n2_chunk);
+      if (kZ) n2_a = __ldg(A + n2_h);
     }
-    const bool nx_in = nx_chunk < chunks_ub;
-    const int2 nx_e = nx_in ? __ldg(plan.tab + nx_chunk) : make_int2(0, 0);
-    const float nx_a = (kZ && nx_in) ? __ldg(A + nx_h) : 0.f;
-    const bool nx_valid = nx_in && nx_chunk < total;
+    const bool nx_valid = nx_chunk < chunks_ub && nx_chunk < total;
     if (t < 64) {
-      beta_s[t] = b_cur;
-      const bool in = nx_valid && t < nx_e.y;
-      b_nx = in ? __bfloat162float(beta[((size_t)nx_e.x + t) * H + nx_h]) : 0.f;
-      if (g_sc) gs_nx = in ? __ldg(g_sc + ((size_t)nx_e.x + t) * H + nx_h) : 0.f;
+      beta_s[t] = bf16_lo(b_cur);
+      b_nx = 0u;
+      gs_nx = 0.f;
+      if (nx_valid && t < nx_e.y) {
+        b_nx = __ldg(reinterpret_cast<const unsigned short*>(beta) + ((size_t)nx_e.x + t) * H + nx_h);
+        if (g_sc) gs_nx = __ldg(g_sc + ((size_t)nx_e.x + t) * H + nx_h);
+      }
     }
 
-    // ---- this unit's rows, copied in during the previous unit: 16 rows x 2 channels
-    bool okin = mbar_wait(bar_in, it & 1, err);
-    if (g_fp32) okin = mbar_wait(bar_g, it & 1, err) && okin;
-    if (t == 0 && okin) pend_in = pend_g = -1;
+    // ---- this unit's rows, copied in during the previous unit: 16 rows x 2 channels;
+    //      z / g first (pass 1 reads them), k and q meanwhile
+    bool okin = (!kZ && !g_fp32) || mbar_wait(bar_g, it & 1, err);
     uint32_t kw[16], qw[16];
     float Gl[2][16];
     {
       float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int r = 16 * ta + e;
-        const bool in = r < len;
-        kw[e] = in ? *reinterpret_cast<const uint32_t*>(sm + kQ_Kin + r * 256 + cp * 2) : 0u;
-        qw[e] = in ? *reinterpret_cast<const uint32_t*>(sm + kQ_Qin + r * 256 + cp * 2) : 0u;
-      }
       // ---- pass 1: the gate (kZ) and the running log-decay over the thread's tile,
       //      base 2, tile-relative: Gl[c][e] = G_r - R_a for row r = 16 ta + e
 #pragma unroll
@@ -502,9 +521,9 @@ __global__ void __launch_bounds__(kP2Threads, 2)
         if constexpr (kZ) {
           // g = g_min / d with d = 1 + exp(-exp(A_h) z); the four quotients share one
           // reciprocal, the exponent clamped at 30 (see the key-operand layout above)
-          const uint32_t z0 = *reinterpret_cast<const uint32_t*>(sm + kQ_Zin + r * 256 + cp * 2);
-          const uint32_t z1 =
-              *reinterpret_cast<const uint32_t*>(sm + kQ_Zin + (r + 1) * 256 + cp * 2);
+          const uint8_t* zrow = sm + (ta < 2 ? kQ_Zlo : kQ_Zhi) + (r & 31) * 256 + cp * 2;
+          const uint32_t z0 = *reinterpret_cast<const uint32_t*>(zrow);
+          const uint32_t z1 = *reinterpret_cast<const uint32_t*>(zrow + 256);
           const float d0 = 1.f + exp2_approx(fminf(-ea * bf16_lo(z0), 30.f));
           const float d1 = 1.f + exp2_approx(fminf(-ea * bf16_hi(z0), 30.f));
           const float d2 = 1.f + exp2_approx(fminf(-ea * bf16_lo(z1), 30.f));
@@ -539,6 +558,15 @@ __global__ void __launch_bounds__(kP2Threads, 2)
         Gl[1][e + 1] = s1;
       }
       *reinterpret_cast<float2*>(Tot + ta * D + cp) = make_float2(s0, s1);
+    }
+    okin = mbar_wait(bar_kq, it & 1, err) && okin;
+    if (okin) pend_kq = pend_g = -1;  // (the issuing threads' records)
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const int r = 16 * ta + e;
+      const bool in = r < len;
+      kw[e] = in ? *reinterpret_cast<const uint32_t*>(sm + kQ_Kin + r * 256 + cp * 2) : 0u;
+      qw[e] = in ? *reinterpret_cast<const uint32_t*>(sm + kQ_Qin + r * 256 + cp * 2) : 0u;
     }
     if (qk_norm) {
       // |k_r|^2 and |q_r|^2 over this warp's 64 channels, each by a reduce-scatter
@@ -679,6 +707,7 @@ __global__ void __launch_bounds__(kP2Threads, 2)
       tma_prefetch_l2_3d(&tm_v, 0, nx_h, nx_e.x);
       tma_prefetch_l2_3d(&tm_v, 64, nx_h, nx_e.x);
       if (!g_sc) tma_prefetch_l2_3d(&tm_g, 0, nx_h, nx_e.x);
+      if (kZ) tma_prefetch_l2_3d(&tm_g, 0, nx_h, nx_e.x + 32);
     }
     const bool okp = mbar_wait(bar_p, it & 1, err);
     if (t == 0 && okp) pend_p = -1;
@@ -755,6 +784,8 @@ __global__ void __launch_bounds__(kP2Threads, 2)
       tma_load_3d(sbase + kQ_V, &tm_v, 0, h, (int)t0, bar_v);
       tma_load_3d(sbase + kQ_V + 8192, &tm_v, 64, h, (int)t0, bar_v);
       pend_v = (int)(it & 1);
+      // and the next unit's z in the row operand's tail and the A_qk block
+      if (kZ && nx_valid) issue_g(nx_h, nx_e.x, (int)((it + 1) & 1));
     }
     invert_unit_lower(Lb, Tb, Ps, t);
     __syncthreads();
@@ -800,8 +831,8 @@ __global__ void __launch_bounds__(kP2Threads, 2)
         mma_bf16(tmem + 64, desc_advance(dv, s * 2048), desc_advance(dt, s * 2048), idv, s > 0);
       mma_commit(bar_w);
       pend_w = (int)(it & 1);
-      // the inverse's scratch is read: the next unit's k, q, z land in its space
-      if (nx_valid) issue_in(nx_h, nx_e.x, (int)((it + 1) & 1));
+      // T is read: the next unit's k and q land in its space
+      if (nx_valid) issue_kq(nx_h, nx_e.x, (int)((it + 1) & 1));
     }
     ok = mbar_wait(bar_w, it & 1, err);
     if (t == 0 && ok) {
@@ -839,17 +870,19 @@ __global__ void __launch_bounds__(kP2Threads, 2)
     cur_h = nx_h;
     cur_e = nx_e;
     cur_a = nx_a;
+    nx_chunk = n2_chunk;
+    nx_h = n2_h;
+    nx_e = n2_e;
+    nx_a = n2_a;
     b_cur = b_nx;
   }
   // after an abort: let the copies and products in flight finish before the TMEM
-  // and the shared memory go away
-  if (t == kCopier && pend_v >= 0) mbar_wait(bar_v, (uint32_t)pend_v, err);
-  if (t == 0) {
-    if (pend_p >= 0) mbar_wait(bar_p, (uint32_t)pend_p, err);
-    if (pend_w >= 0) mbar_wait(bar_w, (uint32_t)pend_w, err);
-    if (pend_in >= 0) mbar_wait(bar_in, (uint32_t)pend_in, err);
-    if (pend_g >= 0) mbar_wait(bar_g, (uint32_t)pend_g, err);
-  }
+  // and the shared memory go away (each issuing thread waits for its own)
+  if (pend_p >= 0) mbar_wait(bar_p, (uint32_t)pend_p, err);
+  if (pend_v >= 0) mbar_wait(bar_v, (uint32_t)pend_v, err);
+  if (pend_w >= 0) mbar_wait(bar_w, (uint32_t)pend_w, err);
+  if (pend_kq >= 0) mbar_wait(bar_kq, (uint32_t)pend_kq, err);
+  if (pend_g >= 0) mbar_wait(bar_g, (uint32_t)pend_g, err);
   if (lane32 == 0) bulk_wait_all();
   __syncthreads();
   if (warp == 0) {
@@ -1610,12 +1643,12 @@ EncodeTiledFn encode_tiled_fn() {
 // `box_c` channels wide, with the given shared-memory swizzle.
 cudaError_t encode_rows(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int esz,
                         int H, int64_t n_tokens, int box_c = D,
-                        CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE) {
+                        CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE, int box_t = C) {
   EncodeTiledFn fn = encode_tiled_fn();
   if (!fn) return cudaErrorNotSupported;
   const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)n_tokens};
   const cuuint64_t strides[2] = {(cuuint64_t)D * esz, (cuuint64_t)H * D * esz};
-  const cuuint32_t box[3] = {(cuuint32_t)box_c, 1u, (cuuint32_t)C};
+  const cuuint32_t box[3] = {(cuuint32_t)box_c, 1u, (cuuint32_t)box_t};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
   const CUresult r = fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
@@ -1739,8 +1772,9 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
       e = encode_rows(&tm[2], v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n_tokens, 64,
                       CU_TENSOR_MAP_SWIZZLE_128B);
     if (e == cudaSuccess) {
-      if (fused)
-        e = encode_rows(&tm[3], z, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n_tokens);
+      if (fused)  // z in two boxes of 32 tokens
+        e = encode_rows(&tm[3], z, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n_tokens, D,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, C / 2);
       else if (scalar_g)
         tm[3] = tm[0];  // not used: scalar gates are plain loads, not prefetched
       else
