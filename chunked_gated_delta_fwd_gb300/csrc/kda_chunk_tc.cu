@@ -601,11 +601,16 @@ __global__ void __launch_bounds__(kP2Threads, 2)
     if (lane32 == 0) bulk_wait_read_all();
     // the previous unit's W/U wait, this unit's copies, every thread's tile totals
     if (!__syncthreads_and(ok && okin)) break;
-    if (qk_norm) {  // normalised rows, rounded to bf16 like normalised inputs
+    if (qk_norm) {
+      // normalised rows, rounded to bf16 like normalised inputs.  Lane i forms
+      // 1 / sqrt(|x|^2 + eps) of row i & 15 of the tile (k rows for lanes 0-15, q
+      // rows for 16-31) from the two warps' halves of the channels; every thread
+      // takes its rows' factors from those lanes.
+      const float rn = rsqrtf(red[64 * ta + lane32] + red[64 * ta + 32 + lane32] + qk_eps);
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
-        const float rk = rsqrtf(red[64 * ta + e] + red[64 * ta + 32 + e] + qk_eps);
-        const float rq = rsqrtf(red[64 * ta + 16 + e] + red[64 * ta + 48 + e] + qk_eps);
+        const float rk = __shfl_sync(0xffffffffu, rn, e);
+        const float rq = __shfl_sync(0xffffffffu, rn, 16 + e);
         const bool in = 16 * ta + e < len;
         kw[e] = in ? pack_bf16(bf16_lo(kw[e]) * rk, bf16_hi(kw[e]) * rk) : 0u;
         qw[e] = in ? pack_bf16(bf16_lo(qw[e]) * rq, bf16_hi(qw[e]) * rq) : 0u;
