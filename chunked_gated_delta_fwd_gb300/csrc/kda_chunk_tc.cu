@@ -91,13 +91,34 @@ __device__ __forceinline__ uint4 pack8(const float* x) {
                     pack_bf16(x[6], x[7]));
 }
 
+// One 16-byte chunk of M = T Diag(beta) as the bf16 B operand of the W/U products
+// (MN-major, X = row r, K = column j): rows 8 o8 .. 8 o8 + 7 of column j, zero above
+// the diagonal.  A warp reads 32 consecutive columns of one row: no bank conflicts.
+// With beta in M, W = M (Gamma K) and U = M V take Gamma K and V as they are (beta
+// is zero on the rows past a sequence's end).
+__device__ __forceinline__ void store_m_chunk(const float* __restrict__ Tb,
+                                              const float* __restrict__ beta_s,
+                                              uint8_t* __restrict__ mt, int o8, int j) {
+  const float bj = beta_s[j];
+  float x[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const int r = 8 * o8 + e;
+    x[e] = (r >= j) ? Tb[r * kLdT + j] * bj : 0.f;
+  }
+  *reinterpret_cast<uint4*>(mt + mn_chunk(64, o8, j)) = pack8(x);
+}
+
 // T = (I + L)^{-1} of a unit's strictly lower, beta-scaled L (fp32 [64][kLdL] in Lb)
 // into Tb (fp32 [64][kLdT], zeros above the diagonal of each stored block), with
-// block products in Ps.  Called by threads 0..255 (warps 0-7) together; uses named
-// barriers 2-5.
+// block products in Ps, and M = T Diag(beta) into the bf16 tile mt: three quarters
+// of it once level 1 is done, the lower-left 32x32 block by the warp pair that forms
+// it.  Called by threads 0..255 (warps 0-7) together; uses named barriers 2-9.
 __device__ __forceinline__ void invert_unit_lower(const float* __restrict__ Lb,
                                                   float* __restrict__ Tb,
-                                                  float* __restrict__ Ps, int t) {
+                                                  float* __restrict__ Ps,
+                                                  const float* __restrict__ beta_s,
+                                                  uint8_t* __restrict__ mt, int t) {
   const int warp = t >> 5;
   if (t < 128) {
     // ---- T = (I + L)^{-1} in fp32.  Warp wq owns diagonal 16x16 block wq: its 8x8
@@ -260,6 +281,9 @@ __device__ __forceinline__ void invert_unit_lower(const float* __restrict__ Lb,
     // level 2 on warps 0-7 (barrier 2, 256 threads): M[:, 0:16] += L[32:64, 16:32]
     // T_{1,0} (one row x 2 columns per thread), then T[32:64, 0:32] = -T22 M.
     named_sync(2, kInvThreads);
+    // rows 0..31 and T[32:64, 32:64] are final: their chunks of M
+    store_m_chunk(Tb, beta_s, mt, t >> 6, t & 63);
+    if ((t & 63) >= 32) store_m_chunk(Tb, beta_s, mt, 4 + (t >> 6), t & 63);
     float* Mb = Tb + 32;
     {
       const int r = t >> 3, cp = t & 7;
@@ -308,11 +332,14 @@ __device__ __forceinline__ void invert_unit_lower(const float* __restrict__ Lb,
         *reinterpret_cast<float2*>(Tb + (32 + 2 * rp + r) * kLdT + 2 * cq) =
             make_float2(-acc[r][0], -acc[r][1]);
     }
+    // rows 32 + 8 o .. + 7 of T[32:64, 0:32] come from threads 64 o .. 64 o + 63
+    named_sync(6 + (t >> 6), 64);
+    if ((t & 63) < 32) store_m_chunk(Tb, beta_s, mt, 4 + (t >> 6), t & 31);
   }
 }
 
 // tc_prep: two 256-thread CTAs share an
-// SM (109 KB of shared memory, 256 TMEM columns and at most 128 registers a thread
+// SM (111 KB of shared memory, 256 TMEM columns and at most 128 registers a thread
 // each).  A CTA takes its units one after the other; the two CTAs of an SM overlap
 // each other's phases (one's latency-bound inverse under the other's issue-bound
 // operand pass, its products under the other's copies).
@@ -792,23 +819,7 @@ __global__ void __launch_bounds__(kP2Threads, 2)
       // and the next unit's z in the row operand's tail and the A_qk block
       if (kZ && nx_valid) issue_g(nx_h, nx_e.x, (int)((it + 1) & 1));
     }
-    invert_unit_lower(Lb, Tb, Ps, t);
-    __syncthreads();
-    {  // M = T Diag(beta) -> bf16 B operand (MN-major, X = row r, K = column j)
-      const int j = t & 63;
-      const float bj = beta_s[j];
-#pragma unroll
-      for (int oo = 0; oo < 2; ++oo) {
-        const int o8 = (t >> 6) + 4 * oo;
-        float x[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int r = 8 * o8 + e;
-          x[e] = (r >= j) ? Tb[r * kLdT + j] * bj : 0.f;
-        }
-        *reinterpret_cast<uint4*>(sm + kQ_T + mn_chunk(64, o8, j)) = pack8(x);
-      }
-    }
+    invert_unit_lower(Lb, Tb, Ps, beta_s, sm + kQ_T, t);
     if (g_sc && t < 64) gsc_s[t] = gs_nx;  // the next unit's pass 1 reads them
     fence_proxy_async_smem();
     tc_fence_before();
