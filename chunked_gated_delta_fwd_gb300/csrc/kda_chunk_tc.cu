@@ -114,11 +114,14 @@ __device__ __forceinline__ void store_m_chunk(const float* __restrict__ Tb,
 // block products in Ps, and M = T Diag(beta) into the bf16 tile mt: three quarters
 // of it once level 1 is done, the lower-left 32x32 block by the warp pair that forms
 // it.  Called by threads 0..255 (warps 0-7) together; uses named barriers 2-9.
+// before_level2() runs on every thread between level 1 and level 2.
+template <typename Hook>
 __device__ __forceinline__ void invert_unit_lower(const float* __restrict__ Lb,
                                                   float* __restrict__ Tb,
                                                   float* __restrict__ Ps,
                                                   const float* __restrict__ beta_s,
-                                                  uint8_t* __restrict__ mt, int t) {
+                                                  uint8_t* __restrict__ mt, int t,
+                                                  Hook&& before_level2) {
   const int warp = t >> 5;
   if (t < 128) {
     // ---- T = (I + L)^{-1} in fp32.  Warp wq owns diagonal 16x16 block wq: its 8x8
@@ -277,6 +280,7 @@ __device__ __forceinline__ void invert_unit_lower(const float* __restrict__ Lb,
       *reinterpret_cast<float4*>(Tb + 32 + (2 * rp + r) * kLdT + 4 * cq) =
           make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
   }
+  before_level2();
   if (t < kInvThreads) {
     // level 2 on warps 0-7 (barrier 2, 256 threads): M[:, 0:16] += L[32:64, 16:32]
     // T_{1,0} (one row x 2 columns per thread), then T[32:64, 0:32] = -T22 M.
@@ -806,20 +810,26 @@ __global__ void __launch_bounds__(kP2Threads, 2)
     }
     if (t == kCopier) {
       bulk_s2g(unit + kQ, sbase + kQ_Bop, 16384);
+      bulk_commit();  // Gamma*Q: its space is V's
       if (!kP) bulk_s2g(unit + kKT, sbase + kQ_Bop + 16384, 16384);
       bulk_s2g(unit + kAQ, sbase + kQ_AQ, 8192);
-      bulk_commit();
-      // V lands in the row operand's space once the copies have read it (while
+      bulk_commit();  // Kt^T and A_qk: their space is the next unit's z
+      // V lands in the row operand's space once the Gamma*Q copy has read it (while
       // warps 0-3 run the first level of the inverse)
-      bulk_wait_read_all();
+      bulk_wait_read_all_but_last();
       mbar_arrive_expect_tx(bar_v, 16384);
       tma_load_3d(sbase + kQ_V, &tm_v, 0, h, (int)t0, bar_v);
       tma_load_3d(sbase + kQ_V + 8192, &tm_v, 64, h, (int)t0, bar_v);
       pend_v = (int)(it & 1);
-      // and the next unit's z in the row operand's tail and the A_qk block
-      if (kZ && nx_valid) issue_g(nx_h, nx_e.x, (int)((it + 1) & 1));
     }
-    invert_unit_lower(Lb, Tb, Ps, beta_s, sm + kQ_T, t);
+    invert_unit_lower(Lb, Tb, Ps, beta_s, sm + kQ_T, t, [&] {
+      if (kZ && t == kCopier) {
+        // Kt^T and A_qk have left by now: the next unit's z lands in the row
+        // operand's tail and the A_qk block
+        bulk_wait_read_all();
+        if (nx_valid) issue_g(nx_h, nx_e.x, (int)((it + 1) & 1));
+      }
+    });
     if (g_sc && t < 64) gsc_s[t] = gs_nx;  // the next unit's pass 1 reads them
     fence_proxy_async_smem();
     tc_fence_before();
