@@ -737,11 +737,11 @@ __global__ void __launch_bounds__(kP2Threads, 2)
       mma_commit(bar_p);
       pend_p = (int)(it & 1);
     }
-    if (t == 32 && nx_valid) {  // the next unit's rows into L2
+    if (t == 32 && nx_valid) {
+      // the next unit's k, q and z / g into L2 (its v is copied in late enough in
+      // its unit not to need it: prefetching it as well measured slower)
       tma_prefetch_l2_3d(&tm_k, 0, nx_h, nx_e.x);
       tma_prefetch_l2_3d(&tm_q, 0, nx_h, nx_e.x);
-      tma_prefetch_l2_3d(&tm_v, 0, nx_h, nx_e.x);
-      tma_prefetch_l2_3d(&tm_v, 64, nx_h, nx_e.x);
       if (!g_sc) tma_prefetch_l2_3d(&tm_g, 0, nx_h, nx_e.x);
       if (kZ) tma_prefetch_l2_3d(&tm_g, 0, nx_h, nx_e.x + 32);
     }
