@@ -342,11 +342,11 @@ __device__ __forceinline__ void invert_unit_lower(const float* __restrict__ Lb,
   }
 }
 
-// tc_prep: two 256-thread CTAs share an
-// SM (111 KB of shared memory, 256 TMEM columns and at most 128 registers a thread
-// each).  A CTA takes its units one after the other; the two CTAs of an SM overlap
-// each other's phases (one's latency-bound inverse under the other's issue-bound
-// operand pass, its products under the other's copies).
+// tc_prep: two 256-thread CTAs share an SM (111 KB of shared memory, 256 TMEM
+// columns and at most 128 registers a thread each).  A CTA takes its units one
+// after the other; the two CTAs of an SM overlap each other's phases (one's
+// latency-bound inverse under the other's issue-bound operand pass, its products
+// under the other's copies).
 //
 // Thread t -> channel pair (cp, cp + 1), cp = 2 (t & 63), and 16-token tile
 // ta = t >> 6, for the whole operand side: the thread reads its 16 rows of k, q
@@ -354,10 +354,10 @@ __device__ __forceinline__ void invert_unit_lower(const float* __restrict__ Lb,
 // and builds the operands of its 16 rows x 2 channels.  Only the per-tile totals of
 // g cross threads.  Every shared-memory block serves several phases of a unit:
 //   row operand (32 KB): K/Q rows for the products; then Gamma*Q and Kt^T on
-//     their way out (parked in TMEM meanwhile); then V (tensor copy), T Diag(beta)
-//     and the next unit's z rows 0-31 (copied in as soon as the outgoing copies
-//     have read the space); then the next unit's g (fp32), or U^T on its way out
-//     (gate fused)
+//     their way out (parked in TMEM meanwhile); then V (tensor copy, once the
+//     Gamma*Q copy has read its space), T Diag(beta) and the next unit's z rows
+//     0-31 (copied in between the inverse's levels, once the Kt^T copy has read
+//     its space); then the next unit's g (fp32), or U^T on its way out (gate fused)
 //   key operand (48 KB): KC for the products; then the inverse's scratch; then the
 //     next unit's k and q (copied in once T is read), or U^T on its way out (g read)
 //   (Gamma K)^T (16 KB): the W product's A operand; then W on its way out
