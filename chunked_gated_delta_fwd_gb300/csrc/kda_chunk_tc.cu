@@ -394,8 +394,9 @@ __host__ __device__ constexpr uint32_t q_ustage() { return kZ ? kQ_Bop : kQ_Ug; 
 // while the decays are summed ("Kimi K3 technical report review", section 3.2).
 // kP: the precise-state mode, Kt^T written in fp32 (straight to the workspace).
 // tm_g maps g (fp32) otherwise; g_sc: one gate per token and head (fp32 [NT][H])
-// instead, or null.  qk_eps >= 0: q and k are L2-normalised per token and head here.
-template <bool kZ, bool kP>
+// instead, or null.  kN: q and k are L2-normalised per token and head here (with
+// qk_eps), a template argument so that the other instances carry none of its code.
+template <bool kZ, bool kP, bool kN>
 __global__ void __launch_bounds__(kP2Threads, 2)
     tc_prep(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
@@ -436,7 +437,7 @@ __global__ void __launch_bounds__(kP2Threads, 2)
   const uint32_t tmem = *tmem_slot;
   const int total = __ldg(plan.chunk_off + plan.n_seqs);
   const float gmin2 = g_min * kLog2e;
-  const bool qk_norm = qk_eps >= 0.f;
+  constexpr bool qk_norm = kN;
 
   const int pr = t & 63, ta = t >> 6, cp = 2 * pr, sw = (pr >> 2) & 1;
   const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
@@ -1782,8 +1783,14 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
   using T = __nv_bfloat16;
   const bool fused = z != nullptr;
   if (units > 0 && n_tokens > 0) {  // with no tokens there are no chunks to prepare
-    auto kern = precise ? (fused ? tc_prep<true, true> : tc_prep<false, true>)
-                        : (fused ? tc_prep<true, false> : tc_prep<false, false>);
+    // instances: <gate fused, precise, q/k normalised>
+    using PrepFn = decltype(&tc_prep<false, false, false>);
+    static const PrepFn kPrep[2][2][2] = {
+        {{tc_prep<false, false, false>, tc_prep<false, false, true>},
+         {tc_prep<false, true, false>, tc_prep<false, true, true>}},
+        {{tc_prep<true, false, false>, tc_prep<true, false, true>},
+         {tc_prep<true, true, false>, tc_prep<true, true, true>}}};
+    const PrepFn kern = kPrep[fused ? 1 : 0][precise ? 1 : 0][fz.qk_eps >= 0.f ? 1 : 0];
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kQ_Smem);
     if (e == cudaSuccess)  // room for two CTAs per SM
       e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
