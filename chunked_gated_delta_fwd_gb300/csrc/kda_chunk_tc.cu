@@ -402,8 +402,11 @@ __global__ void __launch_bounds__(kP2Threads, 2)
              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
              const __nv_bfloat16* __restrict__ beta, const float* __restrict__ A, float g_min,
              Plan plan, int H, int64_t units_ub, uint8_t* __restrict__ tiles,
-             float* __restrict__ gam_out, float qk_eps, const float* __restrict__ g_sc,
+             float* __restrict__ gam_out, float qk_eps, const float* __restrict__ g_sc_arg,
              int* err) {
+  // scalar gates exist only without the fused gate: a constant null otherwise, so
+  // that the gated instances carry none of their code
+  const float* __restrict__ const g_sc = kZ ? nullptr : g_sc_arg;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_addr(sm);
