@@ -997,7 +997,9 @@ struct SegArgs {
 
 // kP: the precise-state mode (Kt^T fp32 in the tiles, Vt^T fp32 in TMEM, the state
 // update as kind::tf32 MMAs).  kG: the output gate is applied before o is written.
-template <bool kP, bool kG>
+// kC: state checkpoints may be requested (ck.ckpt); a template argument so that the
+// other instances carry none of their code.
+template <bool kP, bool kG, bool kC>
 __global__ void __launch_bounds__(chain_threads<kG>(), 1)
     tc_chain(const uint8_t* __restrict__ tiles, const float* __restrict__ gam,
              const float* __restrict__ h0, Plan plan, int H, __nv_bfloat16* __restrict__ o,
@@ -1048,7 +1050,7 @@ __global__ void __launch_bounds__(chain_threads<kG>(), 1)
   const bool gate_on = kG && write_o;  // uniform over the CTA
   // state checkpoints of this job: the true state after every ck.every chunks of
   // the sequence (chunk-local index jl counts from the sequence start)
-  const bool ckpt_on = ck.ckpt != nullptr && write_o;
+  const bool ckpt_on = kC && ck.ckpt != nullptr && write_o;
   const int jl0 = c0 - __ldg(plan.chunk_off + n);
   const int64_t slen = (int64_t)__ldg(plan.cu + n + 1) - __ldg(plan.cu + n);
   auto ckpt_row = [&](int jl_end) -> float* {  // the state after local chunk jl_end - 1
@@ -1839,8 +1841,14 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
     e = encode_rows(&tm_x, fz.gz, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, n_tokens);
     if (e != cudaSuccess) return e;
   }
-  auto chain = precise ? (fz.gz ? tc_chain<true, true> : tc_chain<true, false>)
-                       : (fz.gz ? tc_chain<false, true> : tc_chain<false, false>);
+  // instances: <precise, output gate, checkpoints>
+  using ChainFn = decltype(&tc_chain<false, false, false>);
+  static const ChainFn kChain[2][2][2] = {
+      {{tc_chain<false, false, false>, tc_chain<false, false, true>},
+       {tc_chain<false, true, false>, tc_chain<false, true, true>}},
+      {{tc_chain<true, false, false>, tc_chain<true, false, true>},
+       {tc_chain<true, true, false>, tc_chain<true, true, true>}}};
+  const ChainFn chain = kChain[precise ? 1 : 0][fz.gz ? 1 : 0][ck.ckpt ? 1 : 0];
   const int chain_thr = fz.gz ? chain_threads<true>() : chain_threads<false>();
   const uint32_t chain_sm = precise ? chain_smem<true>() : chain_smem<false>();
   e = cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)chain_sm);
