@@ -90,6 +90,15 @@ __device__ __forceinline__ uint4 pack8(const float* x) {
   return make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
                     pack_bf16(x[6], x[7]));
 }
+__device__ __forceinline__ uint4 pack8(const float2* x) {
+  return make_uint4(pack_bf16(x[0].x, x[0].y), pack_bf16(x[1].x, x[1].y), pack_bf16(x[2].x, x[2].y),
+                    pack_bf16(x[3].x, x[3].y));
+}
+// Products and sums on two fp32 lanes at once (one packed f32x2 instruction, each
+// lane rounded like the scalar operation): s2 broadcasts a scalar into both lanes.
+__device__ __forceinline__ float2 s2(float a) { return make_float2(a, a); }
+__device__ __forceinline__ float2 lo2(float4 v) { return make_float2(v.x, v.y); }
+__device__ __forceinline__ float2 hi2(float4 v) { return make_float2(v.z, v.w); }
 
 // One 16-byte chunk of M = T Diag(beta) as the bf16 B operand of the W/U products
 // (MN-major, X = row r, K = column j): rows 8 o8 .. 8 o8 + 7 of column j, zero above
@@ -191,7 +200,7 @@ __device__ __forceinline__ void invert_unit_lower(const float* __restrict__ Lb,
     const int blk = wq >> 1, a = 2 * blk, R = a + 1, rp = (wl >> 2) & 7, cq = wl & 3;
     float* P1 = Ps + 256 + blk * 256;
     if ((wq & 1) == 0) {  // P = L_{a+1,a} D_a
-      float acc[2][4] = {};
+      float2 acc[2][2] = {};
 #pragma unroll 1  // kept rolled: less code for the instruction cache
       for (int k4 = 0; k4 < 16; k4 += 4) {
         float lv[2][4];
@@ -205,22 +214,19 @@ __device__ __forceinline__ void invert_unit_lower(const float* __restrict__ Lb,
               *reinterpret_cast<const float4*>(Tb + (16 * a + k4 + kk) * kLdT + 16 * a + 4 * cq);
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
-            const float l = lv[r][kk];
-            acc[r][0] = fmaf(l, tv.x, acc[r][0]);
-            acc[r][1] = fmaf(l, tv.y, acc[r][1]);
-            acc[r][2] = fmaf(l, tv.z, acc[r][2]);
-            acc[r][3] = fmaf(l, tv.w, acc[r][3]);
+            acc[r][0] = __ffma2_rn(s2(lv[r][kk]), lo2(tv), acc[r][0]);
+            acc[r][1] = __ffma2_rn(s2(lv[r][kk]), hi2(tv), acc[r][1]);
           }
         }
       }
 #pragma unroll
       for (int r = 0; r < 2; ++r)
         *reinterpret_cast<float4*>(P1 + (rp + 8 * r) * 16 + 4 * cq) =
-            make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+            make_float4(acc[r][0].x, acc[r][0].y, acc[r][1].x, acc[r][1].y);
       named_arrive(3 + blk, 64);
     } else {  // T_{a+1,a} = -D_{a+1} P
       named_sync(3 + blk, 64);
-      float acc[2][4] = {};
+      float2 acc[2][2] = {};
 #pragma unroll 1  // kept rolled: less code for the instruction cache
       for (int k4 = 0; k4 < 16; k4 += 4) {
         float wv[2][4];
@@ -233,18 +239,15 @@ __device__ __forceinline__ void invert_unit_lower(const float* __restrict__ Lb,
           const float4 pv = *reinterpret_cast<const float4*>(P1 + (k4 + kk) * 16 + 4 * cq);
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
-            const float w = wv[r][kk];
-            acc[r][0] = fmaf(w, pv.x, acc[r][0]);
-            acc[r][1] = fmaf(w, pv.y, acc[r][1]);
-            acc[r][2] = fmaf(w, pv.z, acc[r][2]);
-            acc[r][3] = fmaf(w, pv.w, acc[r][3]);
+            acc[r][0] = __ffma2_rn(s2(wv[r][kk]), lo2(pv), acc[r][0]);
+            acc[r][1] = __ffma2_rn(s2(wv[r][kk]), hi2(pv), acc[r][1]);
           }
         }
       }
 #pragma unroll
       for (int r = 0; r < 2; ++r)
         *reinterpret_cast<float4*>(Tb + (16 * R + rp + 8 * r) * kLdT + 16 * a + 4 * cq) =
-            make_float4(-acc[r][0], -acc[r][1], -acc[r][2], -acc[r][3]);
+            make_float4(-acc[r][0].x, -acc[r][0].y, -acc[r][1].x, -acc[r][1].y);
     }
   } else if (t < kInvThreads) {
     // Warps 4-7, while warps 0-3 run level 1: the terms of level 2's
@@ -254,7 +257,7 @@ __device__ __forceinline__ void invert_unit_lower(const float* __restrict__ Lb,
     // 0..31, columns 32..63).  2 rows x 4 columns per thread.
     named_sync(5, 192);
     const int tt = t - 128, rp = tt >> 3, cq = tt & 7, kb = cq >= 4 ? 16 : 0;
-    float acc[2][4] = {};
+    float2 acc[2][2] = {};
 #pragma unroll 1  // kept rolled: less code for the instruction cache
     for (int k4 = 0; k4 < 16; k4 += 4) {
       float lv[2][4];
@@ -267,18 +270,15 @@ __device__ __forceinline__ void invert_unit_lower(const float* __restrict__ Lb,
         const float4 tv = *reinterpret_cast<const float4*>(Tb + (kb + k4 + kk) * kLdT + 4 * cq);
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-          const float l = lv[r][kk];
-          acc[r][0] = fmaf(l, tv.x, acc[r][0]);
-          acc[r][1] = fmaf(l, tv.y, acc[r][1]);
-          acc[r][2] = fmaf(l, tv.z, acc[r][2]);
-          acc[r][3] = fmaf(l, tv.w, acc[r][3]);
+          acc[r][0] = __ffma2_rn(s2(lv[r][kk]), lo2(tv), acc[r][0]);
+          acc[r][1] = __ffma2_rn(s2(lv[r][kk]), hi2(tv), acc[r][1]);
         }
       }
     }
 #pragma unroll
     for (int r = 0; r < 2; ++r)
       *reinterpret_cast<float4*>(Tb + 32 + (2 * rp + r) * kLdT + 4 * cq) =
-          make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+          make_float4(acc[r][0].x, acc[r][0].y, acc[r][1].x, acc[r][1].y);
   }
   before_level2();
   if (t < kInvThreads) {
@@ -291,7 +291,7 @@ __device__ __forceinline__ void invert_unit_lower(const float* __restrict__ Lb,
     float* Mb = Tb + 32;
     {
       const int r = t >> 3, cp = t & 7;
-      float a0 = 0.f, a1 = 0.f;
+      float2 a01 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int k4 = 16; k4 < 32; k4 += 4) {
         const float4 l4 = *reinterpret_cast<const float4*>(Lb + (32 + r) * kLdL + k4);
@@ -299,19 +299,17 @@ __device__ __forceinline__ void invert_unit_lower(const float* __restrict__ Lb,
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const float2 tv = *reinterpret_cast<const float2*>(Tb + (k4 + kk) * kLdT + 2 * cp);
-          a0 = fmaf(lv[kk], tv.x, a0);
-          a1 = fmaf(lv[kk], tv.y, a1);
+          a01 = __ffma2_rn(s2(lv[kk]), tv, a01);
         }
       }
       float2* mp = reinterpret_cast<float2*>(Mb + r * kLdT + 2 * cp);
-      const float2 m0 = *mp;
-      *mp = make_float2(m0.x + a0, m0.y + a1);
+      *mp = __fadd2_rn(*mp, a01);
     }
     const int rp = t >> 4, cq = t & 15;
     named_sync(2, kInvThreads);
     {  // T[32:64, 0:32] = -T[32:64, 32:64] M; T[32:48, 48:64] is zero
       const int kn = rp < 8 ? 16 : 32;  // warp-uniform: warps 0-3 hold rows 32..47
-      float acc[2][2] = {};
+      float2 acc[2] = {};
 #pragma unroll 1  // kept rolled: less code for the instruction cache
       for (int k4 = 0; k4 < 32; k4 += 4) {
         if (k4 < kn) {
@@ -324,17 +322,14 @@ __device__ __forceinline__ void invert_unit_lower(const float* __restrict__ Lb,
           for (int kk = 0; kk < 4; ++kk) {
             const float2 mv = *reinterpret_cast<const float2*>(Mb + (k4 + kk) * kLdT + 2 * cq);
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-              acc[r][0] = fmaf(wv[r][kk], mv.x, acc[r][0]);
-              acc[r][1] = fmaf(wv[r][kk], mv.y, acc[r][1]);
-            }
+            for (int r = 0; r < 2; ++r) acc[r] = __ffma2_rn(s2(wv[r][kk]), mv, acc[r]);
           }
         }
       }
 #pragma unroll
       for (int r = 0; r < 2; ++r)
         *reinterpret_cast<float2*>(Tb + (32 + 2 * rp + r) * kLdT + 2 * cq) =
-            make_float2(-acc[r][0], -acc[r][1]);
+            make_float2(-acc[r].x, -acc[r].y);
     }
     // rows 32 + 8 o .. + 7 of T[32:64, 0:32] come from threads 64 o .. 64 o + 63
     named_sync(6 + (t >> 6), 64);
@@ -678,36 +673,41 @@ __global__ void __launch_bounds__(kP2Threads, 2)
       const float eCa = exp2_approx(GC - Ra);  // exp(G_C - R_a) <= 1
 #pragma unroll
       for (int hq = 0; hq < 2; ++hq) {
-        float f[8], fi[8], kv[8], x[8];
+        // rows 8 hq + 2 i, 8 hq + 2 i + 1 of the tile in lanes x, y
+        float2 f[4], fi[4], kv[4], x[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float dd = Gl[o2][8 * hq + e];  // G_r - R_a, in (-80, 0]
-          f[e] = exp2_approx(dd);
-          fi[e] = exp2_approx(-dd);
-          kv[e] = o2 ? bf16_hi(kw[8 * hq + e]) : bf16_lo(kw[8 * hq + e]);
+        for (int i = 0; i < 4; ++i) {
+          const float d0 = Gl[o2][8 * hq + 2 * i], d1 = Gl[o2][8 * hq + 2 * i + 1];  // G_r - R_a, in (-80, 0]
+          f[i] = make_float2(exp2_approx(d0), exp2_approx(d1));
+          fi[i] = make_float2(exp2_approx(-d0), exp2_approx(-d1));
+          const uint32_t k0 = kw[8 * hq + 2 * i], k1 = kw[8 * hq + 2 * i + 1];
+          kv[i] = o2 ? make_float2(bf16_hi(k0), bf16_hi(k1)) : make_float2(bf16_lo(k0), bf16_lo(k1));
         }
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = kv[e] * f[e];  // k exp(G_r - R_a)
+        for (int i = 0; i < 4; ++i) x[i] = __fmul2_rn(kv[i], f[i]);  // k exp(G_r - R_a)
         *reinterpret_cast<uint4*>(sm + kQ_Bop + mn_chunk(128, 4 * ta + hq, c)) = pack8(x);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] *= eRa;  // Gamma k (beta is folded into T)
+        for (int i = 0; i < 4; ++i) x[i] = __fmul2_rn(x[i], s2(eRa));  // Gamma k (beta is folded into T)
         *reinterpret_cast<uint4*>(sm + kQ_BKg + sw128_chunk(128, c, 2 * ta + hq)) = pack8(x);
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          x[e] = (o2 ? bf16_hi(qw[8 * hq + e]) : bf16_lo(qw[8 * hq + e])) * f[e];
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t q0 = qw[8 * hq + 2 * i], q1 = qw[8 * hq + 2 * i + 1];
+          x[i] = __fmul2_rn(o2 ? make_float2(bf16_hi(q0), bf16_hi(q1)) : make_float2(bf16_lo(q0), bf16_lo(q1)),
+                            f[i]);
+        }
         *reinterpret_cast<uint4*>(sm + kQ_Bop + mn_chunk(128, 4 * ta + 2 + hq, c)) = pack8(x);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] *= eRa;  // Gamma q
+        for (int i = 0; i < 4; ++i) x[i] = __fmul2_rn(x[i], s2(eRa));  // Gamma q
         tmem_st4(t_park + 4 * (2 * o2 + hq), pack8(x));
 #pragma unroll
-        for (int e = 0; e < 8; ++e) kv[e] *= fi[e];  // k exp(R_a - G_r)
+        for (int i = 0; i < 4; ++i) kv[i] = __fmul2_rn(kv[i], fi[i]);  // k exp(R_a - G_r)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = kv[e] * eCa;  // (gamma_C / Gamma) k
+        for (int i = 0; i < 4; ++i) x[i] = __fmul2_rn(kv[i], s2(eCa));  // (gamma_C / Gamma) k
         if (kP) {  // fp32, tokens 8 hq .. +3 and +4 .. +7 of the tile
           *reinterpret_cast<float4*>(unit + kKT + kt32_chunk(c, 4 * ta + 2 * hq)) =
-              make_float4(x[0], x[1], x[2], x[3]);
+              make_float4(x[0].x, x[0].y, x[1].x, x[1].y);
           *reinterpret_cast<float4*>(unit + kKT + kt32_chunk(c, 4 * ta + 2 * hq + 1)) =
-              make_float4(x[4], x[5], x[6], x[7]);
+              make_float4(x[2].x, x[2].y, x[3].x, x[3].y);
         } else {
           tmem_st4(t_park + 16 + 4 * (2 * o2 + hq), pack8(x));
         }
@@ -716,7 +716,7 @@ __global__ void __launch_bounds__(kP2Threads, 2)
           if (ap < ta) continue;
           const float E = (ap > ta) ? exp2_approx(R[ap] - Ra) : 1.f;  // exp(R_ap - R_a) <= 1
 #pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = kv[e] * E;
+          for (int i = 0; i < 4; ++i) x[i] = __fmul2_rn(kv[i], s2(E));
           *reinterpret_cast<uint4*>(sm + kQ_KC + mn_chunk(kKCX, ap * (ap + 1) + 2 * ta + hq, c)) =
               pack8(x);
         }
