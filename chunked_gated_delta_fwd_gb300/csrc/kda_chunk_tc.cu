@@ -1294,7 +1294,9 @@ __global__ void __launch_bounds__(chain_threads<kG>(), 1)
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
           const float4 gm = *reinterpret_cast<const float4*>(gam_s + 64 * ch + 32 * qq + i);
-          v[i] *= gm.x; v[i + 1] *= gm.y; v[i + 2] *= gm.z; v[i + 3] *= gm.w;
+          const float2 v01 = __fmul2_rn(make_float2(v[i], v[i + 1]), lo2(gm));
+          const float2 v23 = __fmul2_rn(make_float2(v[i + 2], v[i + 3]), hi2(gm));
+          v[i] = v01.x; v[i + 1] = v01.y; v[i + 2] = v23.x; v[i + 3] = v23.y;
         }
         tmem_st32(lrow + 64 * ch + 32 * qq, *reinterpret_cast<float(*)[32]>(v));
       }
@@ -1313,10 +1315,12 @@ __global__ void __launch_bounds__(chain_threads<kG>(), 1)
                                  : make_uint4(0, 0, 0, 0);
           const uint32_t uw[4] = {uu.x, uu.y, uu.z, uu.w};
 #pragma unroll
-          for (int p = 0; p < 4; ++p) {
-            wsv[8 * e + 2 * p] = bf16_lo(uw[p]) - wsv[8 * e + 2 * p];
-            wsv[8 * e + 2 * p + 1] = bf16_hi(uw[p]) - wsv[8 * e + 2 * p + 1];
-            pk[4 * e + p] = pack_bf16(wsv[8 * e + 2 * p], wsv[8 * e + 2 * p + 1]);
+          for (int p = 0; p < 4; ++p) {  // u - ws as one fused (-1) ws + u per pair
+            const float2 d = __ffma2_rn(make_float2(wsv[8 * e + 2 * p], wsv[8 * e + 2 * p + 1]), s2(-1.f),
+                                        make_float2(bf16_lo(uw[p]), bf16_hi(uw[p])));
+            wsv[8 * e + 2 * p] = d.x;
+            wsv[8 * e + 2 * p + 1] = d.y;
+            pk[4 * e + p] = pack_bf16(d.x, d.y);
           }
         }
         tmem_st16(lrow + kT_VT + 32 * (j & 1) + 16 * ch, pk);
