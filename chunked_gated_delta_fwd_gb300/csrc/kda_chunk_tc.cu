@@ -1245,11 +1245,18 @@ __global__ void __launch_bounds__(chain_threads<kG>(), 1)
       float sv[kG ? 1 : 2][32];
       {
         float* cp = j > 0 ? ckpt_row(jl0 + j) : nullptr;
+        if constexpr (!kG) {  // both halves in flight at once: one load round trip
+          tmem_ld32(lrow + 64 * ch, sv[0]);
+          tmem_ld32(lrow + 64 * ch + 32, sv[kG ? 0 : 1]);
+          tmem_wait_ld();
+        }
 #pragma unroll
         for (int qq = 0; qq < 2; ++qq) {  // this thread's 64 columns of S^T, 32 at a time
           float* v = sv[kG ? 0 : qq];
-          tmem_ld32(lrow + 64 * ch + 32 * qq, *reinterpret_cast<float(*)[32]>(v));
-          tmem_wait_ld();
+          if constexpr (kG) {
+            tmem_ld32(lrow + 64 * ch + 32 * qq, *reinterpret_cast<float(*)[32]>(v));
+            tmem_wait_ld();
+          }
           if (cp) {
 #pragma unroll
             for (int i = 0; i < 32; i += 8)
