@@ -99,7 +99,9 @@ def _l2_no_root(x, eps):
 
 
 def _l2_first_axis(x, eps):
-    return x / np.sqrt(np.sum(x * x, axis=0, keepdims=True) + eps)
+    # (an all-zero column over the wrong axis gives 0 / 0 here: expected of the mutant)
+    with np.errstate(invalid="ignore", divide="ignore"):
+        return x / np.sqrt(np.sum(x * x, axis=0, keepdims=True) + eps)
 
 
 def _og_sum_for_mean(o, x, w, eps):
